@@ -1,0 +1,118 @@
+"""Whole-layer pins of the oracle (CPU only).
+
+* a closed-form layer: permutation Q8_0 weights at position 0 with one visible key;
+* the verify block of L tokens equals L decode steps one after another;
+* a batch of sequences equals the sequences stepped one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from quantized_attention_layer_gb300 import workloads as wl
+
+
+def _perm_q8_0(perm, cols):
+    """Q8_0 bytes of the 0/1 matrix with W[r, perm[r]] = 1 (d = 1.0 = fp16 0x3C00)."""
+    rows = len(perm)
+    blk = np.zeros((rows, cols // 32, 34), dtype=np.uint8)
+    blk[:, :, 0] = 0x00
+    blk[:, :, 1] = 0x3C
+    for r, c in enumerate(perm):
+        blk[r, c // 32, 2 + c % 32] = 1
+    return blk.reshape(rows, -1)
+
+
+@pytest.mark.parametrize("v_unit_norm", [False, True])
+def test_closed_form_layer_with_permutation_weights(orc, v_unit_norm):
+    # H = nh * hd so that o_proj is square; GQA group 2.
+    w = wl.Workload(name="perm", hidden=64, num_heads=4, num_kv_heads=2, head_dim=16,
+                    layer_type=wl.FULL, window=0, kv_capacity=4, ring=False, batch=1,
+                    rope_theta=1e4, seed=9, seq_pos=0, v_unit_norm=v_unit_norm)
+    rng = np.random.default_rng(9)
+    pv = rng.permutation(64)[:32]
+    po = rng.permutation(64)
+    weights = wl.make_weights(w)
+    weights["wv"] = _perm_q8_0(pv, 64)
+    weights["wo"] = _perm_q8_0(po, 64)
+    x = wl.make_x(w)
+    kv = wl.make_kv_cache(w)
+    r = orc.decode_step(w, weights, x, [0], kv["k_cache"], kv["v_cache"])
+
+    xd = x.to(torch.float64).numpy()[0]
+    w_in = weights["w_in"].to(torch.float64).numpy()
+    n = xd * w_in / np.sqrt(np.mean(xd * xd) + w.eps)       # input RMSNorm
+    v = n[pv].reshape(2, 16)                                   # V projection
+    if v_unit_norm:
+        v = v / np.sqrt(np.mean(v * v, axis=1, keepdims=True) + w.eps)
+    v_b = np.array([[oracle.bf16_scalar_to_f64(oracle.f64_to_bf16(t)) for t in row] for row in v])
+    o = np.concatenate([v_b[0], v_b[0], v_b[1], v_b[1]])     # one key: o = V; head h -> h // 2
+    y = o[po]                                                  # O projection
+    assert np.max(np.abs(r["v"][0] - v)) <= 1e-14
+    assert np.array_equal(r["attn"][0].reshape(-1), o)
+    assert np.max(np.abs(r["out"][0] - (xd + y))) <= 1e-14
+    # the appended slot holds exactly the bf16 rounding of v; other slots are untouched
+    vc = r["v_cache"].reshape(2, 4, 16)
+    assert np.array_equal(oracle.bf16_to_f64(vc[:, 0, :]), v_b)
+    assert np.array_equal(vc[:, 1:, :], oracle.bf16_bits(kv["v_cache"]).reshape(2, 4, 16)[:, 1:, :])
+
+
+def test_verify_block_equals_sequential_decode_steps(orc):
+    w = wl.Workload(name="ver", hidden=96, num_heads=4, num_kv_heads=2, head_dim=16,
+                    layer_type=wl.FULL, window=0, kv_capacity=24, ring=False, batch=1,
+                    rope_theta=1e4, seed=21, base_pos=10, verify_len=5, softcap=30.0)
+    weights = wl.make_weights(w)
+    x = wl.make_x(w)
+    kv = wl.make_kv_cache(w)
+    ver = orc.verify_block(w, weights, x, 10, kv["k_cache"], kv["v_cache"])
+    kc, vc = kv["k_cache"], kv["v_cache"]
+    for i in range(5):
+        step = orc.decode_step(w, weights, x[i:i + 1], [10 + i], kc, vc)
+        kc = torch.from_numpy(step["k_cache"].view(np.int16)).view(torch.bfloat16)
+        vc = torch.from_numpy(step["v_cache"].view(np.int16)).view(torch.bfloat16)
+        for key in ("q", "k", "v", "attn", "out"):
+            assert np.max(np.abs(step[key][0] - ver[key][i])) <= 1e-13, (key, i)
+    assert np.array_equal(oracle.bf16_bits(kc), ver["k_cache"])
+    assert np.array_equal(oracle.bf16_bits(vc), ver["v_cache"])
+
+
+def test_sliding_verify_block_matches_decode_steps(orc):
+    w = wl.Workload(name="versl", hidden=64, num_heads=2, num_kv_heads=1, head_dim=32,
+                    layer_type=wl.SLIDING, window=6, kv_capacity=32, ring=False, batch=1,
+                    rope_theta=1e4, seed=22, base_pos=12, verify_len=4)
+    weights = wl.make_weights(w)
+    x = wl.make_x(w)
+    kv = wl.make_kv_cache(w)
+    ver = orc.verify_block(w, weights, x, 12, kv["k_cache"], kv["v_cache"])
+    kc, vc = kv["k_cache"], kv["v_cache"]
+    for i in range(4):
+        step = orc.decode_step(w, weights, x[i:i + 1], [12 + i], kc, vc)
+        kc = torch.from_numpy(step["k_cache"].view(np.int16)).view(torch.bfloat16)
+        vc = torch.from_numpy(step["v_cache"].view(np.int16)).view(torch.bfloat16)
+        assert np.max(np.abs(step["out"][0] - ver["out"][i])) <= 1e-13
+
+
+def test_batch_equals_independent_sequences(orc):
+    w = wl.Workload(name="batch", hidden=64, num_heads=4, num_kv_heads=2, head_dim=16,
+                    layer_type=wl.SLIDING, window=8, kv_capacity=8, ring=True, batch=3,
+                    rope_theta=1e4, seed=23, seq_pos_range=(8, 40))
+    weights = wl.make_weights(w)
+    x = wl.make_x(w)
+    kv = wl.make_kv_cache(w)
+    pos = wl.make_positions(w)
+    full = orc.decode_step(w, weights, x, pos, kv["k_cache"], kv["v_cache"])
+    one = w.replace(batch=1)
+    for b in range(3):
+        r = orc.decode_step(one, weights, x[b:b + 1], pos[b:b + 1], kv["k_cache"][b:b + 1],
+                            kv["v_cache"][b:b + 1])
+        for key in ("q", "attn", "out"):
+            assert np.array_equal(r[key][0], full[key][b])
+        assert np.array_equal(r["k_cache"][0], full["k_cache"][b])
+
+
+def test_decode_rejects_out_of_range_positions(orc):
+    w = wl.TINY_SLIDING
+    weights = wl.make_weights(w)
+    kv = wl.make_kv_cache(w)
+    with pytest.raises(ValueError):
+        orc.decode_step(w, weights, wl.make_x(w), [w.kv_capacity], kv["k_cache"], kv["v_cache"])
