@@ -1,0 +1,363 @@
+"""Benchmark of the single-token decode step of one attention layer on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload full_b1_32k] [--replicas R]
+
+One step = one pass of the whole decode path (input norm + QKV + norms + RoPE + KV append
+-> flash-decode -> o_proj + residual) over one batch of the workload.  Every timed step
+runs on a different layer replica (distinct weights and caches in HBM, R replicas of
+~179 MB for the 32K full-attention layer), so the inputs of a step are never L2-resident:
+together they are far larger than the 129 MB L2.
+
+Printed (one JSON line, rank 0): steps/s for the whole job, ms per step, the roofline of
+the dominant kernel (flash-decode: KV bytes / its CUDA-event duration against the
+measured HBM copy bandwidth), the end-to-end rate through the host-buffer entry point,
+the CPU oracle baseline, SM clocks sampled during the timed region, and the launch count.
+
+--impl reference times the CPU oracle (the plain fp64 implementation the tests check the
+library against) on the host cores, same workload, metric and unit.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "decode steps/sec per layer at 1 GB300; achieved HBM GB/s as % of peak"
+UNIT = "steps/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="full_b1_32k")
+    p.add_argument("--replicas", type=int, default=8)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def dist_setup(n):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def workload_bytes(w, pos):
+    """Algorithmic bytes of one step: Q8_0 weights at 34/32 B per weight, the visible
+    bf16 K and V rows, activations in and out, the appended K/V row."""
+    H, nh, nkv, hd = w.hidden, w.num_heads, w.num_kv_heads, w.head_dim
+    wbytes = (w.q_rows + 2 * w.kv_rows) * H * 34 // 32 + H * w.q_rows * 34 // 32
+    kv = 0
+    for P in pos:
+        if w.ring:
+            n = min(int(P) + 1, w.kv_capacity)
+        elif w.layer_type == 0:
+            n = int(P) - max(0, int(P) - w.window + 1) + 1
+        else:
+            n = int(P) + 1
+        kv += n * nkv * hd * 2 * 2
+    act = len(pos) * (H * 2 * 2 + nkv * hd * 2 * 2)
+    return wbytes, kv, act
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def ncu_traffic(kernel_file, summary_name):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source it was
+    taken on is the current one (its sha256 is recorded in the summary)."""
+    path = os.path.join(ROOT, "profiles", summary_name)
+    src = os.path.join(ROOT, "quantized_attention_layer_gb300", "csrc", kernel_file)
+    if not (os.path.exists(path) and os.path.exists(src)):
+        return None
+    text = open(path).read()
+    m_sha = re.search(r"source sha256:\s*([0-9a-f]{64})", text)
+    m_b = re.search(r"dram bytes per launch:\s*([0-9.eE+]+)", text)
+    if not (m_sha and m_b):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    return float(m_b.group(1)) if sha == m_sha.group(1) else None
+
+
+def cpu_baseline(w, weights, x, pos, kv, budget_s=15.0):
+    import oracle
+    oracle.build()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.decode_step(w, weights, x, pos, kv["k_cache"], kv["v_cache"])
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n} full oracle decode steps of {w.name} (batch {len(pos)}), fp64, "
+                      f"{dt:.1f} s on the host cores"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from quantized_attention_layer_gb300 import workloads as wl
+    import oracle
+    oracle.build()
+    w = wl.BY_NAME[args.workload]
+    weights = wl.make_weights(w)
+    x = wl.make_x(w)
+    pos = wl.make_positions(w)
+    kv = wl.make_kv_cache(w)
+    for _ in range(args.warmup):
+        oracle.decode_step(w, weights, x, pos, kv["k_cache"], kv["v_cache"])
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.decode_step(w, weights, x, pos, kv["k_cache"], kv["v_cache"])
+    dt = time.perf_counter() - t0
+    value = args.steps * len(pos) / dt / len(pos)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "hidden": w.hidden,
+                       "heads": f"{w.num_heads}/{w.num_kv_heads}", "head_dim": w.head_dim,
+                       "context": int(pos.max()) + 1, "weights": "q8_0"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                             "kind": "oracle",
+                             "sample": f"{args.steps} full oracle decode steps of {w.name}"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local):
+    from quantized_attention_layer_gb300 import build, hfa, workloads as wl
+    build.build()
+    assert torch.cuda.is_available(), "bench.py needs a CUDA device"
+    torch.cuda.set_device(local)
+    w = wl.BY_NAME[args.workload]
+    if w.verify_len:
+        raise SystemExit("the decode benchmark needs a decode workload")
+    weights = wl.make_weights(w)
+    x = wl.make_x(w)
+    pos = wl.make_positions(w)
+    kv = wl.make_kv_cache(w)
+    B = len(pos)
+    dev_w = hfa.weights_to_device(w, weights)
+    R = max(1, args.replicas)
+    stream = torch.cuda.Stream()
+    layers, caches = [], []
+    with torch.cuda.stream(stream):
+        for r in range(R):
+            layers.append(hfa.Layer(hfa.desc_for(w), dev_w, stream=stream))
+            caches.append((kv["k_cache"].cuda(), kv["v_cache"].cuda()))
+    del dev_w
+    xd = x.cuda()
+    posd = torch.from_numpy(pos).cuda()
+    out = torch.empty((B, w.hidden), dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
+
+    def step(i):
+        kc, vc = caches[i % R]
+        layers[i % R].hfa_decode_step(xd, posd, pos, kc, vc, out, stream=stream)
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    for L in layers:
+        L.hfa_check_device_status(stream=stream)
+
+    # ---------------------------------------------------------------- timed region
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    ms = ev0.elapsed_time(ev1)
+    ms = max_over_ranks(ms, world)
+    clocks = clk.summary()
+    ms_per_step = ms / args.steps
+    value = world * B * args.steps / (ms / 1e3) / B  # steps/s over the whole job
+    for L in layers:
+        L.hfa_check_device_status(stream=stream)
+
+    # ---------------------------------------------------------------- per-kernel events
+    for L in layers:
+        L.hfa_set_kernel_timing(True)
+        L.hfa_kernel_times()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        step(i)
+    torch.cuda.synchronize()
+    ktimes = {}
+    for L in layers:
+        for name, (kms, cnt) in L.hfa_kernel_times().items():
+            a = ktimes.setdefault(name, [0.0, 0])
+            a[0] += kms
+            a[1] += cnt
+        L.hfa_set_kernel_timing(False)
+    wbytes, kvbytes, actbytes = workload_bytes(w, pos)
+    peak, peak_src = measured_peaks()
+    attn_ms = ktimes.get("flash_decode", [float("nan"), 1])
+    attn_avg_ms = attn_ms[0] / max(attn_ms[1], 1)
+    attn_gbs = kvbytes / (attn_avg_ms * 1e-3) / 1e9
+    traffic = ncu_traffic("k_attn.cu", f"flash_decode_{w.name}.md")
+    roofline = {"bound": "hbm", "achieved": attn_gbs, "peak": peak, "unit": "GB/s",
+                "frac": attn_gbs / peak, "traffic": traffic, "kernel": "flash_decode",
+                "algorithmic_bytes_per_launch": kvbytes, "peak_source": peak_src}
+    step_bytes = wbytes + kvbytes + actbytes
+    kernels = {k: {"avg_us": v[0] / max(v[1], 1) * 1e3, "launches": v[1]} for k, v in ktimes.items()}
+
+    # ---------------------------------------------------------------- end to end
+    x_h = x.pin_memory()
+    out_h = torch.empty((B, w.hidden), dtype=torch.bfloat16).pin_memory()
+    for i in range(3):
+        kc, vc = caches[i % R]
+        layers[i % R].hfa_decode_step_host(x_h, pos, kc, vc, out_h, stream=stream)
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        kc, vc = caches[i % R]
+        layers[i % R].hfa_decode_step_host(x_h, pos, kc, vc, out_h, stream=stream)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    e2e = {"value": world * args.steps / e2e_s, "unit": UNIT,
+           "h2d_bytes_per_step": B * w.hidden * 2 + B * 4, "d2h_bytes_per_step": B * w.hidden * 2}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "batch": B, "hidden": w.hidden,
+                       "heads": f"{w.num_heads}/{w.num_kv_heads}", "head_dim": w.head_dim,
+                       "context": int(pos.max()) + 1, "weights": "q8_0",
+                       "kv": "bf16", "parallelism": f"replicas x{world}",
+                       "l2": f"inputs larger than L2: {R} layer replicas rotated, "
+                             f"{R * step_bytes / 1e9:.2f} GB"},
+            "step_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
+            "step_frac_of_peak": step_bytes / (ms_per_step * 1e-3) / 1e9 / peak,
+            "step_bytes": step_bytes,
+            "roofline": roofline, "kernels": kernels, "e2e": e2e, "clocks": clocks,
+            "gpu_launches": 3 * args.steps}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, weights, x, pos, kv)
+    for L in layers:
+        L.hfa_destroy()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

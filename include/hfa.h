@@ -1,0 +1,213 @@
+/*
+ * hfa.h -- C ABI of libhfa: the single-token decode step and the multi-token verify
+ * block of one Gemma-style attention layer on an NVIDIA GB300 (sm_103a).
+ *
+ * Sources of the operation (hf2q documentation pages):
+ *   "gemma4/gpu_full_attn.rs", encode_one_layer: the per-layer decode encoder --
+ *     pre-attention norm, the Q/K/V projections (dispatch_qmatmul), the fused per-head
+ *     norm + RoPE, the GPU V norm, the dense KV copy, dense flash_attn_vec (main +
+ *     reduce) and the O projection.  FlashAttnVecParams gives the attention
+ *     parameters: num_heads, num_kv_heads, head_dim, kv_seq_len, kv_capacity, scale,
+ *     mask_type, sliding_window, softcap.
+ *   "gemma4/model.rs": the Q8_0 block format (Q8_0 lm_head re-quantiser), the dense
+ *     KV buffer layout [n_kv_heads, capacity, head_dim] with sliding layers as rings
+ *     of capacity = sliding window, and the dense tree-verify entry point.
+ *   "spec_decode/dflash/forward.rs": per-head RMSNorm over rows = L * n_heads, NeoX
+ *     RoPE with a position offset, the logit softcap tanh(s / cap) * cap, the residual
+ *     add, and SDPA of an L-row block over the cache (all rows of the block appended).
+ *
+ * Conventions for every entry point:
+ *   - Pointers named *_dev are CUDA device pointers on the current device; pointers
+ *     named *_host are host pointers.  `stream` is a cudaStream_t (NULL = legacy
+ *     default stream).  Work is enqueued on `stream` and returns before it completes,
+ *     unless the entry point says otherwise.
+ *   - All argument checks run on the host before anything is launched; a rejected
+ *     call launches nothing and touches no device memory.  The reason is available
+ *     from hfa_last_error().
+ *   - No entry point allocates device memory except hfa_layer_create.
+ *   - bf16 = IEEE bfloat16 bit pattern (uint16), row-major, densely packed.
+ */
+#ifndef HFA_H
+#define HFA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct hfa_layer hfa_layer; /* opaque; owned by the library */
+
+typedef enum {
+  HFA_OK = 0,
+  HFA_EINVAL = -1,       /* bad argument: null pointer, shape, flag combination */
+  HFA_ERANGE = -2,       /* a position outside the cache or the layer's limits */
+  HFA_ENOMEM = -3,       /* device allocation failed (hfa_layer_create only) */
+  HFA_ECUDA = -4,        /* a CUDA call failed; hfa_last_error has the CUDA message */
+  HFA_EUNSUPPORTED = -5, /* valid request this build does not implement */
+  HFA_EDEVICE = -6,      /* no usable sm_103 device, or a device-side check failed */
+} hfa_status;
+
+typedef enum { HFA_SLIDING = 0, HFA_FULL = 1 } hfa_layer_type;
+
+/* flags */
+#define HFA_F_V_UNIT_NORM 0x1u  /* V gets a per-head RMSNorm with unit weight (GPU V norm) */
+#define HFA_F_WEIGHTS_BF16 0x2u /* Q/K/V/O are dense bf16 [out, in] instead of Q8_0 */
+#define HFA_F_RING 0x4u         /* sliding ring buffer: slot = pos % kv_capacity */
+#define HFA_F_DEBUG_TAPS 0x8u   /* keep fp32 copies of q, k, v, attention and output */
+
+typedef struct {
+  int hidden;       /* H, multiple of 64 */
+  int num_heads;    /* query heads nh */
+  int num_kv_heads; /* key/value heads nkv; nh % nkv == 0 and nh / nkv <= 8 */
+  int head_dim;     /* hd in {64, 128, 256} */
+  int layer_type;   /* hfa_layer_type */
+  int window;       /* sliding window W (keys with P-W < p <= P visible); SLIDING only */
+  float eps;        /* RMSNorm epsilon of the input norm and the per-head norms */
+  float rope_theta; /* RoPE base; NeoX pairing (i, i + hd/2), phi_i = P * theta^(-2i/hd) */
+  float attn_scale; /* logit scale; 1.0 on the Gemma decode path */
+  float softcap;    /* 0 = off; else logits s -> softcap * tanh(s / softcap) */
+  int kv_capacity;  /* C: slots per (sequence, kv head); a ring needs C == window */
+  int max_batch;    /* largest batch a decode step may pass (sizes the scratch) */
+  int max_verify_len; /* largest L of hfa_verify_block; 0 = verify not used */
+  unsigned flags;   /* HFA_F_* */
+} hfa_layer_desc;
+
+/*
+ * Create a layer.  Weights are read from device memory and copied (Q8_0: re-laid out
+ * for coalesced loads; the values are untouched) into library-owned memory, so the
+ * caller may free them when the call returns.  The call synchronises `stream`.
+ *
+ *   wq_dev [nh*hd, H], wk_dev [nkv*hd, H], wv_dev [nkv*hd, H], wo_dev [H, nh*hd]:
+ *     Q8_0: rows of H/32 (resp. nh*hd/32) blocks of 34 bytes -- fp16 scale d (little
+ *     endian) then 32 int8 q, value = d * q (Q8_0 lm_head re-quantiser, model.rs).
+ *     With HFA_F_WEIGHTS_BF16: dense bf16, row-major [out, in].
+ *   w_in_dev f32 [H], w_q_dev f32 [hd], w_k_dev f32 [hd]: RMSNorm weights, used as
+ *     y = x * w / sqrt(mean(x^2) + eps).
+ * Errors: HFA_EINVAL (shape, flags), HFA_EUNSUPPORTED (a shape this build does not
+ * cover), HFA_EDEVICE (no sm_103 device), HFA_ENOMEM, HFA_ECUDA.  *out is NULL on
+ * error.
+ */
+hfa_status hfa_layer_create(const hfa_layer_desc* desc, const void* wq_dev, const void* wk_dev,
+                            const void* wv_dev, const void* wo_dev, const float* w_in_dev,
+                            const float* w_q_dev, const float* w_k_dev, void* stream,
+                            hfa_layer** out);
+
+/*
+ * One decode step for `batch` independent sequences (encode_one_layer, attention half):
+ *   n = RMSNorm(x) ; [q;k;v] = W n ; q,k = per-head RMSNorm + RoPE at seq_pos ;
+ *   append bf16(k), bf16(v) at slot seq_pos (linear) or seq_pos % C (ring) ;
+ *   o = softmax(scale * q K^T [softcap] [window mask]) V over the visible keys ;
+ *   out = x + Wo o.
+ *
+ *   x_dev        bf16 [batch, H]
+ *   seq_pos_dev  int32 [batch], device copy read by the kernels
+ *   seq_pos_host int32 [batch], host copy of the same values, used for validation
+ *   k_cache_dev, v_cache_dev  bf16 [batch, nkv, C, hd]; one slot per sequence and
+ *                kv head is written in place, every other slot is only read
+ *   out_dev      bf16 [batch, H]
+ * Linear caches need 0 <= seq_pos < C (HFA_ERANGE otherwise).  Requires Q8_0 weights.
+ * The cache must hold the earlier positions of each sequence: positions
+ * max(0, P-W+1) .. P-1 (sliding) or 0 .. P-1 (full).
+ */
+hfa_status hfa_decode_step(hfa_layer* layer, void* stream, const void* x_dev,
+                           const int32_t* seq_pos_dev, const int32_t* seq_pos_host, int batch,
+                           void* k_cache_dev, void* v_cache_dev, void* out_dev);
+
+/*
+ * The same decode step taking its per-step input and output in host memory:
+ * copies x_host and seq_pos_host to library staging buffers on `stream`, runs the
+ * step, copies the result back to out_host and synchronises `stream` before
+ * returning.  x_host bf16 [batch, H], out_host bf16 [batch, H] (pinned memory gives
+ * asynchronous copies; pageable memory works but is slower).  The caches stay in
+ * device memory.
+ */
+hfa_status hfa_decode_step_host(hfa_layer* layer, void* stream, const void* x_host,
+                                const int32_t* seq_pos_host, int batch, void* k_cache_dev,
+                                void* v_cache_dev, void* out_host);
+
+/*
+ * Multi-token verify block, one sequence (the dense tree-verify entry of model.rs;
+ * the block form of forward.rs): L tokens at positions base_pos .. base_pos+L-1.
+ * All L K/V rows are appended; row i attends to cache positions <= base_pos + i
+ * (and within the window when sliding).  Accepting or rolling back the appended rows
+ * is the caller's business.
+ *   x_dev bf16 [L, H]; k_cache_dev, v_cache_dev bf16 [1, nkv, C, hd]; out_dev bf16 [L, H].
+ * Needs a linear cache with base_pos + L <= C and 1 <= L <= max_verify_len.
+ */
+hfa_status hfa_verify_block(hfa_layer* layer, void* stream, const void* x_dev, int L,
+                            int base_pos, void* k_cache_dev, void* v_cache_dev, void* out_dev);
+
+/*
+ * The attention step alone ("Dense flash_attn_vec" of encode_one_layer), for callers
+ * that compute q themselves: split-K GQA flash-decode of one query per head over the
+ * visible keys of a bf16 cache, optional softcap, log-sum-exp merge of the chunks.
+ *   q_dev        f32 [batch, nh, hd]: queries after norm and RoPE (scale not applied)
+ *   seq_pos_dev / seq_pos_host  int32 [batch]: the query positions (as in the decode step)
+ *   k_cache_dev, v_cache_dev    bf16 [batch, nkv, C, hd], read only
+ *   workspace_dev  device scratch of at least hfa_attention_workspace_bytes(desc, batch)
+ *                  bytes, 16-byte aligned, all zero before its first use; each call leaves
+ *                  it ready for the next (its counters return to zero).  Word 0 is a
+ *                  device status word: non-zero means a bounded wait gave up (bit 0) or a
+ *                  position was refused (bit 1).  Calls sharing a workspace must not
+ *                  overlap on the GPU.
+ *   o_dev        f32 [batch, nh, hd]
+ * Errors come back as for hfa_layer_create (message via hfa_last_error(NULL)).
+ */
+typedef struct {
+  int num_heads, num_kv_heads, head_dim; /* as in hfa_layer_desc */
+  int layer_type, window, kv_capacity;
+  float attn_scale, softcap;
+  unsigned flags; /* HFA_F_RING or 0 */
+} hfa_attn_desc;
+
+size_t hfa_attention_workspace_bytes(const hfa_attn_desc* desc, int batch);
+hfa_status hfa_attention_decode(const hfa_attn_desc* desc, void* stream, const float* q_dev,
+                                const int32_t* seq_pos_dev, const int32_t* seq_pos_host,
+                                int batch, const void* k_cache_dev, const void* v_cache_dev,
+                                void* workspace_dev, size_t workspace_bytes, float* o_dev);
+
+/* Release the layer and its device memory (synchronises the device first). */
+hfa_status hfa_destroy(hfa_layer* layer);
+
+/* Last error message of `layer`; with NULL, the last error of a create on this thread. */
+const char* hfa_last_error(const hfa_layer* layer);
+
+/*
+ * Copies of the fp32 intermediate values of the last step, for layers created with
+ * HFA_F_DEBUG_TAPS (HFA_EINVAL otherwise).  Device pointers, each nullable:
+ *   q [rows, nh, hd] after norm + RoPE;  k, v [rows, nkv, hd] before the bf16 rounding;
+ *   attn [rows, nh, hd];  out [rows, H] before the bf16 rounding;
+ * rows = the batch of the last decode step, or L of the last verify block.
+ * Enqueued on `stream`.
+ */
+hfa_status hfa_debug_taps(hfa_layer* layer, void* stream, float* q_dev, float* k_dev,
+                          float* v_dev, float* attn_dev, float* out_dev);
+
+/*
+ * Device-side status of earlier steps: bounded waits that gave up, or positions the
+ * kernels refused.  Synchronises `stream`; returns HFA_OK, or HFA_EDEVICE with the
+ * reason in hfa_last_error, and clears the record.
+ */
+hfa_status hfa_check_device_status(hfa_layer* layer, void* stream);
+
+/*
+ * Per-kernel timing: when enabled, the library records CUDA events around each of
+ * its kernels on the launching stream.  hfa_kernel_times synchronises and returns,
+ * for up to `n` kernel slots, the summed milliseconds and the launch count since the
+ * last call, and each slot's name (static strings).  Returns the number of slots.
+ */
+int hfa_set_kernel_timing(hfa_layer* layer, int enable);
+int hfa_kernel_times(hfa_layer* layer, int n, const char** names, float* total_ms,
+                     int* launches);
+
+/* Launch plan details (for logs and the benchmark): fills up to n ints:
+ * [0] attention splits per (sequence, kv head) of the last step, [1] keys per
+ * attention stage, [2] GEMV grid, [3] attention grid, [4] SM count. */
+int hfa_plan_info(const hfa_layer* layer, int n, int* values);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* HFA_H */

@@ -1,0 +1,41 @@
+// hfa_verify.h -- the multi-token verify block (host interface between hfa_api.cu and
+// the verify kernels).
+#pragma once
+#include <cuda_runtime.h>
+
+#include "hfa_internal.h"
+
+namespace hfa {
+
+struct VerifyState;
+
+struct VerifyCall {
+  const hfa_layer_desc* d;
+  cudaStream_t stream;
+  const __nv_bfloat16* x;  // [L, H]
+  int L;
+  int base_pos;
+  __nv_bfloat16* k_cache;  // [1, nkv, C, hd]
+  __nv_bfloat16* v_cache;
+  __nv_bfloat16* out;      // [L, H]
+  const __nv_bfloat16* wqkv;  // [(nh + 2 nkv) hd, H]
+  const __nv_bfloat16* wo;    // [H, nh hd]
+  const float* w_in;
+  const float* w_q;
+  const float* w_k;
+  const float2* rope_g;
+  float* q_f32;   // [L, nh, hd]
+  float* o_f32;   // [L, nh, hd]
+  float* k_tap;   // nullable [L, nkv, hd]
+  float* v_tap;
+  float* out_tap; // nullable [L, H]
+  unsigned* err;
+  int num_sms;
+};
+
+hfa_status verify_create(const hfa_layer_desc& d, int num_sms, VerifyState** out);
+void verify_free(VerifyState* v);
+const char* verify_error();
+hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int msg_len);
+
+}  // namespace hfa

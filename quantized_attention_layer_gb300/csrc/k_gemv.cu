@@ -1,0 +1,357 @@
+// k_gemv.cu -- dequantising Q8_0 GEMV for the decode step.
+//
+// Two modes share one kernel body:
+//  * kModeQKV  (pre-attention norm + QKV projection + per-head norm + RoPE + KV append):
+//    gemma4/gpu_full_attn.rs, encode_one_layer: "Pre-attention norm", "QKV projections",
+//    "Fused per-head RMS norm + RoPE on Q and K", "GPU V norm" and the dense KV copy.
+//  * kModeOProj (o_proj + residual): encode_one_layer "O-proj"; the residual
+//    connection of dflash/forward.rs (dispatch_dflash_residual_add, h = x + attn).
+//
+// Work split.  The weight matrix is a sequence of 16x32 tiles (row group r, k-block b)
+// ordered (k-split s, r, b).  Each CTA takes a contiguous range of that sequence and each
+// warp a contiguous sub-range, so every warp streams the same number of tiles (+-1).
+// One 16-byte load per lane brings a whole tile; two m16n8k16 fp16 MMAs per tile and
+// per batch tile multiply it with the activations.  Activations enter as fp16 hi + lo
+// pairs (columns 2j and 2j+1 of the MMA's N dimension), which keeps about 22 bits of the
+// fp32 value; int8 -> fp16 is exact, and the per-block fp16 scale multiplies the fp32
+// partial products of each block.
+//
+// Completion.  Partial sums go to an fp32 accumulator with red.add; each warp then adds
+// the number of tiles it finished to a per-head (QKV) or per-row-group (o_proj) ticket.
+// The warp whose tiles complete a head / row group reads the sums back, resets them to
+// zero and runs the epilogue for it.  No warp ever waits for another.
+#include "hfa_common.cuh"
+#include "hfa_internal.h"
+
+namespace hfa {
+
+constexpr int kUnroll = 8;  // tiles in flight per lane (16 B weights + 4 B scales each)
+
+// Cosine and sine of phi = P * theta^(-2i/hd) with phi reduced exactly enough in fp32:
+// u = P * g with g = theta^(-2i/hd) / (2 pi) held as an fp32 (hi, lo) pair; the product
+// P * hi is split into its rounded value and exact error (fma), the integer part is
+// dropped, and sincospi of twice the fractional turn gives the rotation.
+__device__ __forceinline__ void rope_cs(int P, float2 gpair, float& c, float& s) {
+  const float Pf = (float)P;
+  const float p1 = Pf * gpair.x;
+  const float e1 = fmaf(Pf, gpair.x, -p1);
+  const float k = rintf(p1);
+  const float r = (p1 - k) + (e1 + Pf * gpair.y);
+  sincospif(2.0f * r, &s, &c);
+}
+
+// Epilogue of one attention head (QKV mode): rows [hh*hd, hh*hd + hd) of the QKV output.
+template <int HD>
+__device__ void finish_head(const GemvArgs& a, int hh, int lane) {
+  constexpr int J = HD / 32;   // values per lane; pairs (j, j + J/2) are RoPE partners
+  const int R16 = a.R * 16;
+  const int kind = hh < a.nh ? 0 : (hh < a.nh + a.nkv ? 1 : 2);  // q, k, v
+  for (int b = 0; b < a.batch; ++b) {
+    float v[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      float* p = a.acc + (size_t)b * R16 + (size_t)hh * HD + lane + 32 * j;
+      v[j] = ld_cg_f32(p);
+      *p = 0.0f;
+    }
+    const int seq = a.rows_are_tokens ? 0 : b;
+    const int P = a.rows_are_tokens ? a.seq_pos[0] + b : a.seq_pos[b];
+    if (kind < 2 || a.v_unit_norm) {
+      float ss = 0.f;
+#pragma unroll
+      for (int j = 0; j < J; ++j) ss += v[j] * v[j];
+      ss = warp_sum(ss);
+      const float inv = rsqrtf(ss / HD + a.eps);
+      const float* w = kind == 0 ? a.w_q : (kind == 1 ? a.w_k : nullptr);
+#pragma unroll
+      for (int j = 0; j < J; ++j) v[j] *= inv * (w ? __ldg(w + lane + 32 * j) : 1.0f);
+    }
+    if (kind < 2) {
+#pragma unroll
+      for (int j = 0; j < J / 2; ++j) {
+        float c, s;
+        rope_cs(P, a.rope_g[lane + 32 * j], c, s);
+        const float x0 = v[j], x1 = v[j + J / 2];
+        v[j] = x0 * c - x1 * s;
+        v[j + J / 2] = x0 * s + x1 * c;
+      }
+    }
+    if (kind == 0) {
+      float* q = a.q_out + ((size_t)b * a.nh + hh) * HD;
+#pragma unroll
+      for (int j = 0; j < J; ++j) q[lane + 32 * j] = v[j];
+    } else {
+      const int kvh = kind == 1 ? hh - a.nh : hh - a.nh - a.nkv;
+      if (P < 0 || (!a.ring && P >= a.C)) {
+        if (lane == 0) atomicOr(a.err, kErrBadPosition);
+        continue;
+      }
+      const int slot = a.ring ? P % a.C : P;
+      __nv_bfloat16* cache = kind == 1 ? a.k_cache : a.v_cache;
+      __nv_bfloat16* dst = cache + (((size_t)seq * a.nkv + kvh) * a.C + slot) * HD;
+      float* tap = kind == 1 ? a.k_tap : a.v_tap;
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        dst[lane + 32 * j] = __float2bfloat16_rn(v[j]);
+        if (tap) tap[((size_t)b * a.nkv + kvh) * HD + lane + 32 * j] = v[j];
+      }
+    }
+  }
+}
+
+// Epilogue of one row group (o_proj mode): out = bf16(x + y).
+__device__ void finish_rowgroup(const GemvArgs& a, int r, int lane) {
+  const int R16 = a.R * 16;
+  for (int i = lane; i < 16 * a.batch; i += 32) {
+    const int b = i >> 4, row = r * 16 + (i & 15);
+    float* p = a.acc + (size_t)b * R16 + row;
+    const float y = ld_cg_f32(p);
+    *p = 0.0f;
+    const float o = __bfloat162float(a.x[(size_t)b * R16 + row]) + y;
+    a.out[(size_t)b * R16 + row] = __float2bfloat16_rn(o);
+    if (a.out_tap) a.out_tap[(size_t)b * R16 + row] = o;
+  }
+}
+
+template <int NT, int MODE>
+__device__ __forceinline__ void flush_item(const GemvArgs& a, float (&acc)[NT][4], int r,
+                                           int ntiles, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  const int R16 = a.R * 16;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int b = nt * 4 + t;
+    if (b < a.batch) {
+      red_add_f32(a.acc + (size_t)b * R16 + r * 16 + g, acc[nt][0] + acc[nt][1]);
+      red_add_f32(a.acc + (size_t)b * R16 + r * 16 + g + 8, acc[nt][2] + acc[nt][3]);
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+  }
+  __syncwarp();
+  int done = 0;
+  int key = MODE == kModeQKV ? (r * 16) / a.hd : r;
+  int need = MODE == kModeQKV ? (a.hd / 16) * a.nb : a.nb;
+  if (lane == 0) done = (atom_add_acq_rel(a.ticket + key, ntiles) + ntiles == need);
+  done = __shfl_sync(0xffffffffu, done, 0);
+  __syncwarp();
+  if (done) {
+    if (lane == 0) a.ticket[key] = 0;
+    if (MODE == kModeQKV) {
+      if (a.hd == 64) finish_head<64>(a, key, lane);
+      else if (a.hd == 128) finish_head<128>(a, key, lane);
+      else finish_head<256>(a, key, lane);
+    } else {
+      finish_rowgroup(a, key, lane);
+    }
+  }
+}
+
+template <int NT, int MODE>
+__global__ void __launch_bounds__(512) gemv_q8_kernel(const GemvArgs a) {
+  extern __shared__ __align__(16) uint4 xf[];  // [blocks of this CTA][NT][32 lanes]
+  __shared__ float s_inv[16];
+  const int nwarps = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2;
+  const long long per_split = (long long)a.R * a.nbs;
+  const long long cta_begin = a.tiles * blockIdx.x / gridDim.x;
+  const long long cta_end = a.tiles * (blockIdx.x + 1) / gridDim.x;
+  if (cta_begin >= cta_end) {
+    pdl_wait();
+    return;
+  }
+  const int s_first = (int)(cta_begin / per_split);
+  const int s_last = (int)((cta_end - 1) / per_split);
+  const int blk0 = s_first * a.nbs;
+  const int nblk = (s_last - s_first + 1) * a.nbs;
+
+  // The weights never depend on an earlier kernel: warm L2 with this CTA's first tiles
+  // while the previous kernel finishes, then wait for it.
+  {
+    const long long first = cta_begin + threadIdx.x;
+    if (first < cta_end && threadIdx.x < 64) {
+      const long long item = first / a.nbs;
+      const int j = (int)(first - item * a.nbs);
+      const int s = (int)(item / a.R), r = (int)(item - (long long)s * a.R);
+      prefetch_l2(a.wq + ((size_t)r * a.nb + s * a.nbs + j) * 512);
+    }
+  }
+  pdl_wait();
+
+  if (MODE == kModeQKV) {
+    // input RMSNorm statistics of every batch row (full rows, fp32)
+    for (int b = warp; b < a.batch; b += nwarps) {
+      float ss = 0.f;
+      const __nv_bfloat16* xr = a.x + (size_t)b * a.cols;
+      for (int k = lane * 8; k < a.cols; k += 256) {
+        uint4 raw = *reinterpret_cast<const uint4*>(xr + k);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float2 f = __bfloat1622float2(h[e]);
+          ss += f.x * f.x + f.y * f.y;
+        }
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) s_inv[b] = rsqrtf(ss / a.cols + a.eps);
+    }
+    __syncthreads();
+  }
+
+  // activation operand registers for the blocks this CTA touches: one thread turns 8
+  // consecutive activations of one batch row into the hi and lo words of 4 lanes
+  {
+    uint32_t* xw = reinterpret_cast<uint32_t*>(xf);
+    const int groups = nblk * 4;  // 8-column groups per batch row
+    for (int e = threadIdx.x; e < NT * 4 * groups; e += blockDim.x) {
+      const int b = e / groups, gi = e - b * groups;
+      const int jb = gi >> 2, c = gi & 3;         // block, 8-column group in the block
+      const int k = (blk0 + jb) * 32 + c * 8;
+      float v[8];
+      if (b < a.batch) {
+        if (MODE == kModeQKV) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(a.x + (size_t)b * a.cols + k);
+          const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.w_in + k));
+          const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.w_in + k + 4));
+          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+          const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+          const float inv = s_inv[b];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(h[i]);
+            v[2 * i] = f.x * inv * wv[2 * i];
+            v[2 * i + 1] = f.y * inv * wv[2 * i + 1];
+          }
+        } else {
+          const float4 f0 = *reinterpret_cast<const float4*>(a.xin + (size_t)b * a.cols + k);
+          const float4 f1 = *reinterpret_cast<const float4*>(a.xin + (size_t)b * a.cols + k + 4);
+          v[0] = f0.x; v[1] = f0.y; v[2] = f0.z; v[3] = f0.w;
+          v[4] = f1.x; v[5] = f1.y; v[6] = f1.z; v[7] = f1.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = 0.f;
+      }
+      // columns 8c .. 8c+7 of the block: k-step ks = c / 2, register half hf = c % 2;
+      // lane t holds the pair (2t, 2t+1); lanes g = 2(b%4) (hi) and 2(b%4)+1 (lo)
+      const int ks = c >> 1, hf = c & 1, nt = b >> 2, gh = 2 * (b & 3);
+      const int word = 2 * ks + hf;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        __half h0, l0, h1, l1;
+        split_f16(v[2 * t], h0, l0);
+        split_f16(v[2 * t + 1], h1, l1);
+        const int base = ((jb * NT + nt) * 32) * 4 + word;
+        xw[base + (gh * 4 + t) * 4] = pack_h2(h0, h1);
+        xw[base + ((gh + 1) * 4 + t) * 4] = pack_h2(l0, l1);
+      }
+    }
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+
+  const long long n = cta_end - cta_begin;
+  const long long w_begin = cta_begin + n * warp / nwarps;
+  const long long w_end = cta_begin + n * (warp + 1) / nwarps;
+  float acc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+
+  long long tt0 = w_begin;
+  while (tt0 < w_end) {
+    // one item = the tiles of (s, r) inside this warp's range
+    const long long item = tt0 / a.nbs;
+    const long long item_end = (item + 1) * a.nbs < w_end ? (item + 1) * a.nbs : w_end;
+    const int s = (int)(item / a.R), r = (int)(item - (long long)s * a.R);
+    const int j_first = (int)(tt0 - item * a.nbs);
+    const int nt_item = (int)(item_end - tt0);
+    const uint8_t* wbase = a.wq + ((size_t)r * a.nb + s * a.nbs) * 512 + lane * 16;
+    const __half2* dbase = a.wd + ((size_t)r * a.nb + s * a.nbs) * 8 + g;
+    for (int c = 0; c < nt_item; c += kUnroll) {
+      uint4 wv[kUnroll];
+      uint32_t dv[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        if (c + u < nt_item) {
+          const int j = j_first + c + u;
+          wv[u] = ldg_stream_v4(wbase + (size_t)j * 512);
+          dv[u] = ldg_stream_u32(dbase + (size_t)j * 8);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        if (c + u < nt_item) {
+          const int jb = s * a.nbs + j_first + c + u - blk0;
+          uint32_t A0[4], A1[4];
+          A0[0] = u8x2_to_h2(wv[u].x, kSelLo);
+          A0[1] = u8x2_to_h2(wv[u].y, kSelLo);
+          A0[2] = u8x2_to_h2(wv[u].x, kSelHi);
+          A0[3] = u8x2_to_h2(wv[u].y, kSelHi);
+          A1[0] = u8x2_to_h2(wv[u].z, kSelLo);
+          A1[1] = u8x2_to_h2(wv[u].w, kSelLo);
+          A1[2] = u8x2_to_h2(wv[u].z, kSelHi);
+          A1[3] = u8x2_to_h2(wv[u].w, kSelHi);
+          const __half2 d2 = *reinterpret_cast<const __half2*>(&dv[u]);
+          const float dg = __low2float(d2), dg8 = __high2float(d2);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const uint4 xb = xf[(jb * NT + nt) * 32 + lane];
+            float tmp[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_f16(tmp, A0, xb.x, xb.y);
+            mma_f16(tmp, A1, xb.z, xb.w);
+            acc[nt][0] = fmaf(tmp[0], dg, acc[nt][0]);
+            acc[nt][1] = fmaf(tmp[1], dg, acc[nt][1]);
+            acc[nt][2] = fmaf(tmp[2], dg8, acc[nt][2]);
+            acc[nt][3] = fmaf(tmp[3], dg8, acc[nt][3]);
+          }
+        }
+      }
+    }
+    flush_item<NT, MODE>(a, acc, r, nt_item, lane);
+    tt0 = item_end;
+  }
+}
+
+int gemv_ntiles(int batch) { return batch <= 4 ? 1 : (batch <= 8 ? 2 : 4); }
+
+size_t gemv_smem_bytes(int batch, int blocks_per_cta_max) {
+  return (size_t)blocks_per_cta_max * gemv_ntiles(batch) * 32 * sizeof(uint4);
+}
+
+template <int NT, int MODE>
+static cudaError_t launch_t(const GemvArgs& a, int grid, int threads, size_t smem, bool pdl,
+                            cudaStream_t s) {
+  auto kern = gemv_q8_kernel<NT, MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+cudaError_t launch_gemv(int mode, const GemvArgs& a, int grid, int threads, size_t smem,
+                        bool pdl, cudaStream_t s) {
+  const int nt = gemv_ntiles(a.batch);
+  if (mode == kModeQKV) {
+    if (nt == 1) return launch_t<1, kModeQKV>(a, grid, threads, smem, pdl, s);
+    if (nt == 2) return launch_t<2, kModeQKV>(a, grid, threads, smem, pdl, s);
+    return launch_t<4, kModeQKV>(a, grid, threads, smem, pdl, s);
+  }
+  if (nt == 1) return launch_t<1, kModeOProj>(a, grid, threads, smem, pdl, s);
+  if (nt == 2) return launch_t<2, kModeOProj>(a, grid, threads, smem, pdl, s);
+  return launch_t<4, kModeOProj>(a, grid, threads, smem, pdl, s);
+}
+
+}  // namespace hfa

@@ -1,0 +1,66 @@
+// k_repack.cu -- Q8_0 blocks -> MMA-ready tiles (run once at layer creation).
+//
+// Input: the Q8_0 layout of the Q8_0 lm_head re-quantiser (gemma4/model.rs): per row,
+// cols/32 blocks of 34 bytes = fp16 scale d (little endian) + 32 int8 q.  The 34-byte
+// stride is not 16-byte aligned, so the decode GEMV could not use 128-bit loads on it.
+// Output (values untouched, only moved):
+//   q tiles: tile (row group r, block b) = 512 bytes; lane l = 4g + t owns bytes
+//     [16l, 16l+16): word 0 = row g, word 1 = row g+8 for columns {2t, 2t+1, 2t+8, 2t+9}
+//     of the block's first 16 columns; words 2, 3 the same for columns 16 + {...}.
+//     Each byte stores q + 128 (so the GEMV converts it to fp16 without a sign step).
+//   d tiles: tile (r, b) = 8 half2, entry g = (d[row g], d[row g + 8]).
+#include "hfa_common.cuh"
+#include "hfa_internal.h"
+
+namespace hfa {
+
+__global__ void repack_q8_0_kernel(const uint8_t* __restrict__ src, int rows, int cols,
+                                   uint8_t* __restrict__ qdst, __half2* __restrict__ ddst,
+                                   int row0) {
+  const int nb = cols / 32;
+  const long long n = (long long)(rows / 16) * nb * 32;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int lane = (int)(idx & 31);
+    const long long tile = idx >> 5;
+    const int b = (int)(tile % nb);
+    const int r = (int)(tile / nb);
+    const int g = lane >> 2, t = lane & 3;
+    const uint8_t* row_g = src + (size_t)(16 * r + g) * nb * 34 + (size_t)b * 34;
+    const uint8_t* row_g8 = row_g + (size_t)8 * nb * 34;
+    uint32_t w[4];
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const uint8_t* rp = half ? row_g8 : row_g;
+        const int c0 = 16 * ks + 2 * t;
+        const int cs[4] = {c0, c0 + 1, c0 + 8, c0 + 9};
+        uint32_t v = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v |= (uint32_t)((uint8_t)(rp[2 + cs[e]] + 128u)) << (8 * e);
+        w[2 * ks + half] = v;
+      }
+    }
+    const long long out_tile = (long long)(row0 / 16 + r) * nb + b;
+    reinterpret_cast<uint4*>(qdst)[out_tile * 32 + lane] = make_uint4(w[0], w[1], w[2], w[3]);
+    if (t == 0) {
+      __half dg = __ushort_as_half((unsigned short)(row_g[0] | (row_g[1] << 8)));
+      __half dg8 = __ushort_as_half((unsigned short)(row_g8[0] | (row_g8[1] << 8)));
+      ddst[out_tile * 8 + g] = __halves2half2(dg, dg8);
+    }
+  }
+}
+
+cudaError_t launch_repack_q8_0(const uint8_t* src, int rows, int cols, Q8Tiles* dst,
+                               size_t row_offset_rows, cudaStream_t s) {
+  long long n = (long long)(rows / 16) * (cols / 32) * 32;
+  int threads = 256;
+  long long blocks = (n + threads - 1) / threads;
+  if (blocks > 65535) blocks = 65535;
+  repack_q8_0_kernel<<<(int)blocks, threads, 0, s>>>(src, rows, cols, dst->q, dst->d,
+                                                     (int)row_offset_rows);
+  return cudaGetLastError();
+}
+
+}  // namespace hfa

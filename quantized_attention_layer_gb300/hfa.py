@@ -1,0 +1,256 @@
+"""ctypes binding of libhfa (include/hfa.h): argument marshalling only.
+
+Every step of the decode path runs in the CUDA kernels of libhfa.so; this module
+converts torch tensors to raw pointers and checks return codes.  There is no CPU
+fallback: if the library is missing, :func:`lib` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Dict, List, Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import workloads as wl
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libhfa.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "hfa.h")
+
+HFA_OK, HFA_EINVAL, HFA_ERANGE, HFA_ENOMEM, HFA_ECUDA, HFA_EUNSUPPORTED, HFA_EDEVICE = \
+    0, -1, -2, -3, -4, -5, -6
+STATUS_NAMES = {0: "HFA_OK", -1: "HFA_EINVAL", -2: "HFA_ERANGE", -3: "HFA_ENOMEM",
+                -4: "HFA_ECUDA", -5: "HFA_EUNSUPPORTED", -6: "HFA_EDEVICE"}
+
+HFA_F_V_UNIT_NORM = 0x1
+HFA_F_WEIGHTS_BF16 = 0x2
+HFA_F_RING = 0x4
+HFA_F_DEBUG_TAPS = 0x8
+
+
+class HfaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class hfa_layer_desc(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int), ("num_heads", ctypes.c_int),
+                ("num_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
+                ("layer_type", ctypes.c_int), ("window", ctypes.c_int),
+                ("eps", ctypes.c_float), ("rope_theta", ctypes.c_float),
+                ("attn_scale", ctypes.c_float), ("softcap", ctypes.c_float),
+                ("kv_capacity", ctypes.c_int), ("max_batch", ctypes.c_int),
+                ("max_verify_len", ctypes.c_int), ("flags", ctypes.c_uint)]
+
+
+class hfa_attn_desc(ctypes.Structure):
+    _fields_ = [("num_heads", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("layer_type", ctypes.c_int),
+                ("window", ctypes.c_int), ("kv_capacity", ctypes.c_int),
+                ("attn_scale", ctypes.c_float), ("softcap", ctypes.c_float),
+                ("flags", ctypes.c_uint)]
+
+
+def attn_desc_for(w: wl.Workload) -> hfa_attn_desc:
+    return hfa_attn_desc(num_heads=w.num_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
+                         layer_type=w.layer_type, window=w.window, kv_capacity=w.kv_capacity,
+                         attn_scale=w.attn_scale, softcap=w.softcap,
+                         flags=HFA_F_RING if w.ring else 0)
+
+
+_lib = None
+
+
+def lib():
+    """Load libhfa.so (raises when it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: run quantized_attention_layer_gb300.build")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, C = ctypes.c_void_p, ctypes.c_int, ctypes.c_int
+        L.hfa_layer_create.restype = C
+        L.hfa_layer_create.argtypes = [ctypes.POINTER(hfa_layer_desc), P, P, P, P, P, P, P, P,
+                                       ctypes.POINTER(P)]
+        L.hfa_decode_step.restype = C
+        L.hfa_decode_step.argtypes = [P, P, P, P, P, I, P, P, P]
+        L.hfa_decode_step_host.restype = C
+        L.hfa_decode_step_host.argtypes = [P, P, P, P, I, P, P, P]
+        L.hfa_verify_block.restype = C
+        L.hfa_verify_block.argtypes = [P, P, P, I, I, P, P, P]
+        L.hfa_destroy.restype = C
+        L.hfa_destroy.argtypes = [P]
+        L.hfa_last_error.restype = ctypes.c_char_p
+        L.hfa_last_error.argtypes = [P]
+        L.hfa_debug_taps.restype = C
+        L.hfa_debug_taps.argtypes = [P, P, P, P, P, P, P]
+        L.hfa_check_device_status.restype = C
+        L.hfa_check_device_status.argtypes = [P, P]
+        L.hfa_set_kernel_timing.restype = C
+        L.hfa_set_kernel_timing.argtypes = [P, I]
+        L.hfa_kernel_times.restype = C
+        L.hfa_kernel_times.argtypes = [P, I, ctypes.POINTER(ctypes.c_char_p),
+                                       ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int)]
+        L.hfa_plan_info.restype = C
+        L.hfa_plan_info.argtypes = [P, I, ctypes.POINTER(ctypes.c_int)]
+        L.hfa_attention_workspace_bytes.restype = ctypes.c_size_t
+        L.hfa_attention_workspace_bytes.argtypes = [ctypes.POINTER(hfa_attn_desc), I]
+        L.hfa_attention_decode.restype = C
+        L.hfa_attention_decode.argtypes = [ctypes.POINTER(hfa_attn_desc), P, P, P, P, I, P, P, P,
+                                           ctypes.c_size_t, P]
+        _lib = L
+    return _lib
+
+
+def header_functions() -> List[str]:
+    """Names of the functions include/hfa.h declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(hfa_[a-z_0-9]+)\s*\(", text)))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def hfa_attention_workspace_bytes(desc: hfa_attn_desc, batch: int) -> int:
+    return int(lib().hfa_attention_workspace_bytes(ctypes.byref(desc), int(batch)))
+
+
+def hfa_attention_decode(desc: hfa_attn_desc, q: torch.Tensor, seq_pos_dev: torch.Tensor,
+                         seq_pos_host, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                         workspace: torch.Tensor, o: torch.Tensor, stream=None) -> torch.Tensor:
+    pos_h = np.ascontiguousarray(seq_pos_host, dtype=np.int32)
+    st = lib().hfa_attention_decode(ctypes.byref(desc), _stream_ptr(stream), _ptr(q),
+                                    _ptr(seq_pos_dev), ctypes.c_void_p(pos_h.ctypes.data),
+                                    int(pos_h.size), _ptr(k_cache), _ptr(v_cache), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _ptr(o))
+    if st != HFA_OK:
+        raise HfaError(st, lib().hfa_last_error(None).decode())
+    return o
+
+
+def desc_for(w: wl.Workload, max_batch: Optional[int] = None, max_verify_len: Optional[int] = None,
+             debug_taps: bool = False) -> hfa_layer_desc:
+    flags = w.flags | (HFA_F_DEBUG_TAPS if debug_taps else 0)
+    return hfa_layer_desc(
+        hidden=w.hidden, num_heads=w.num_heads, num_kv_heads=w.num_kv_heads,
+        head_dim=w.head_dim, layer_type=w.layer_type, window=w.window, eps=w.eps,
+        rope_theta=w.rope_theta, attn_scale=w.attn_scale, softcap=w.softcap,
+        kv_capacity=w.kv_capacity,
+        max_batch=max_batch if max_batch is not None else max(1, w.batch),
+        max_verify_len=max_verify_len if max_verify_len is not None else w.verify_len,
+        flags=flags)
+
+
+def weights_to_device(w: wl.Workload, weights: Dict, device="cuda") -> Dict[str, torch.Tensor]:
+    out = {}
+    for k, v in weights.items():
+        if isinstance(v, np.ndarray):
+            v = torch.from_numpy(np.ascontiguousarray(v))
+        out[k] = v.to(device).contiguous()
+    return out
+
+
+class Layer:
+    """One attention layer held by libhfa (hfa_layer_create ... hfa_destroy)."""
+
+    def __init__(self, desc: hfa_layer_desc, dev_weights: Dict[str, torch.Tensor], stream=None):
+        self.desc = desc
+        self._h = ctypes.c_void_p()
+        st = lib().hfa_layer_create(
+            ctypes.byref(desc), _ptr(dev_weights["wq"]), _ptr(dev_weights["wk"]),
+            _ptr(dev_weights["wv"]), _ptr(dev_weights["wo"]), _ptr(dev_weights["w_in"]),
+            _ptr(dev_weights["w_q"]), _ptr(dev_weights["w_k"]), _stream_ptr(stream),
+            ctypes.byref(self._h))
+        if st != HFA_OK:
+            raise HfaError(st, lib().hfa_last_error(None).decode())
+
+    @property
+    def handle(self) -> ctypes.c_void_p:
+        return self._h
+
+    def _check(self, st: int):
+        if st != HFA_OK:
+            raise HfaError(st, lib().hfa_last_error(self._h).decode())
+
+    def hfa_decode_step(self, x: torch.Tensor, seq_pos_dev: torch.Tensor, seq_pos_host: np.ndarray,
+                        k_cache: torch.Tensor, v_cache: torch.Tensor, out: torch.Tensor,
+                        stream=None) -> torch.Tensor:
+        pos_h = np.ascontiguousarray(seq_pos_host, dtype=np.int32)
+        self._check(lib().hfa_decode_step(self._h, _stream_ptr(stream), _ptr(x), _ptr(seq_pos_dev),
+                                          ctypes.c_void_p(pos_h.ctypes.data), int(pos_h.size),
+                                          _ptr(k_cache), _ptr(v_cache), _ptr(out)))
+        return out
+
+    def hfa_decode_step_host(self, x_host: torch.Tensor, seq_pos_host: np.ndarray,
+                             k_cache: torch.Tensor, v_cache: torch.Tensor, out_host: torch.Tensor,
+                             stream=None) -> torch.Tensor:
+        pos_h = np.ascontiguousarray(seq_pos_host, dtype=np.int32)
+        self._check(lib().hfa_decode_step_host(self._h, _stream_ptr(stream), _ptr(x_host),
+                                               ctypes.c_void_p(pos_h.ctypes.data), int(pos_h.size),
+                                               _ptr(k_cache), _ptr(v_cache), _ptr(out_host)))
+        return out_host
+
+    def hfa_verify_block(self, x: torch.Tensor, base_pos: int, k_cache: torch.Tensor,
+                         v_cache: torch.Tensor, out: torch.Tensor, stream=None) -> torch.Tensor:
+        self._check(lib().hfa_verify_block(self._h, _stream_ptr(stream), _ptr(x), int(x.shape[0]),
+                                           int(base_pos), _ptr(k_cache), _ptr(v_cache), _ptr(out)))
+        return out
+
+    def hfa_debug_taps(self, rows: int, stream=None) -> Dict[str, torch.Tensor]:
+        d = self.desc
+        dev = torch.device("cuda")
+        t = {"q": torch.empty((rows, d.num_heads, d.head_dim), device=dev),
+             "k": torch.empty((rows, d.num_kv_heads, d.head_dim), device=dev),
+             "v": torch.empty((rows, d.num_kv_heads, d.head_dim), device=dev),
+             "attn": torch.empty((rows, d.num_heads, d.head_dim), device=dev),
+             "out": torch.empty((rows, d.hidden), device=dev)}
+        self._check(lib().hfa_debug_taps(self._h, _stream_ptr(stream), _ptr(t["q"]), _ptr(t["k"]),
+                                          _ptr(t["v"]), _ptr(t["attn"]), _ptr(t["out"])))
+        return t
+
+    def hfa_check_device_status(self, stream=None) -> None:
+        self._check(lib().hfa_check_device_status(self._h, _stream_ptr(stream)))
+
+    def hfa_set_kernel_timing(self, enable: bool) -> None:
+        lib().hfa_set_kernel_timing(self._h, int(bool(enable)))
+
+    def hfa_kernel_times(self) -> Dict[str, tuple]:
+        n = 16
+        names = (ctypes.c_char_p * n)()
+        ms = (ctypes.c_float * n)()
+        cnt = (ctypes.c_int * n)()
+        k = lib().hfa_kernel_times(self._h, n, names, ms, cnt)
+        return {names[i].decode(): (float(ms[i]), int(cnt[i])) for i in range(max(k, 0))}
+
+    def hfa_plan_info(self) -> Dict[str, int]:
+        v = (ctypes.c_int * 5)()
+        lib().hfa_plan_info(self._h, 5, v)
+        return {"attn_splits": v[0], "keys_per_stage": v[1], "gemv_grid": v[2],
+                "attn_grid": v[3], "num_sms": v[4]}
+
+    def hfa_destroy(self) -> None:
+        if self._h:
+            lib().hfa_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    close = hfa_destroy
+
+    def __del__(self):
+        try:
+            self.hfa_destroy()
+        except Exception:
+            pass

@@ -1,0 +1,67 @@
+"""CPU checks of the C-ABI library: it builds, loads, and exports every declared symbol.
+
+No compute call is made here (there is no GPU); argument checks that run before any
+CUDA call are exercised where the call needs no device.
+"""
+import ctypes
+import os
+
+import pytest
+
+from quantized_attention_layer_gb300 import build, hfa
+
+
+@pytest.fixture(scope="module")
+def libhfa():
+    build.build()
+    return hfa.lib()
+
+
+def test_header_declares_the_boundary():
+    names = hfa.header_functions()
+    for required in ("hfa_layer_create", "hfa_decode_step", "hfa_verify_block", "hfa_destroy",
+                     "hfa_last_error", "hfa_debug_taps", "hfa_decode_step_host"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(libhfa):
+    for name in hfa.header_functions():
+        assert hasattr(libhfa, name), f"libhfa.so does not export {name}"
+
+
+def test_create_rejects_bad_descriptors_before_touching_a_device(libhfa):
+    from quantized_attention_layer_gb300 import workloads as wl
+    bad = [
+        dict(hidden=100),             # not a multiple of 64
+        dict(head_dim=96),            # unsupported head_dim
+        dict(num_kv_heads=3),         # nh % nkv != 0
+        dict(max_batch=17),
+        dict(kv_capacity=0),
+    ]
+    for kw in bad:
+        d = hfa.desc_for(wl.TINY_SLIDING)
+        for k, v in kw.items():
+            setattr(d, k, v)
+        h = ctypes.c_void_p()
+        dummy = ctypes.c_void_p(16)
+        st = libhfa.hfa_layer_create(ctypes.byref(d), dummy, dummy, dummy, dummy, dummy, dummy,
+                                     dummy, None, ctypes.byref(h))
+        assert st in (hfa.HFA_EINVAL, hfa.HFA_EUNSUPPORTED), (kw, st)
+        assert not h.value
+        assert libhfa.hfa_last_error(None)
+
+
+def test_ring_needs_capacity_equal_to_window(libhfa):
+    from quantized_attention_layer_gb300 import workloads as wl
+    d = hfa.desc_for(wl.SLIDING_B16)
+    d.kv_capacity = 2048
+    h = ctypes.c_void_p()
+    dummy = ctypes.c_void_p(16)
+    st = libhfa.hfa_layer_create(ctypes.byref(d), dummy, dummy, dummy, dummy, dummy, dummy, dummy,
+                                 None, ctypes.byref(h))
+    assert st == hfa.HFA_EINVAL
+
+
+def test_null_handle_is_rejected(libhfa):
+    assert libhfa.hfa_decode_step(None, None, None, None, None, 1, None, None, None) == hfa.HFA_EINVAL
+    assert libhfa.hfa_destroy(None) == hfa.HFA_EINVAL
