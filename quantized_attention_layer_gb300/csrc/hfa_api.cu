@@ -22,6 +22,8 @@ using namespace hfa;
 
 static thread_local char g_create_error[512];
 
+void hfa::set_thread_error(const char* msg) { snprintf(g_create_error, sizeof g_create_error, "%s", msg); }
+
 struct KernelTimer {
   const char* name;
   cudaEvent_t start, stop;
@@ -139,6 +141,19 @@ hfa_status hfa_encode_kv_map(CUtensorMap* map, void* base, int rows, int hd, int
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? HFA_OK : HFA_EINVAL;
+}
+
+bool hfa::encode_bf16_2d(CUtensorMap* map, void* base, int inner, int rows, int box_inner,
+                         int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // ------------------------------------------------------------------ timing
@@ -313,7 +328,8 @@ extern "C" hfa_status hfa_layer_create(const hfa_layer_desc* desc, const void* w
   LA(L->qkv_acc, (size_t)MR * L->rows_qkv);
   LA(L->head_ticket, nh + 2 * nkv);
   LA(L->q_f32, (size_t)MR * nh * hd);
-  LA(L->attn_part, (size_t)units * L->max_splits * 8 * (hd + 2));
+  // one (m, l, O) record per attention chunk: units * splits <= max(2 SMs, units)
+  LA(L->attn_part, (size_t)(units > L->max_splits ? units : L->max_splits) * 8 * (hd + 2));
   LA(L->attn_ticket, units);
   LA(L->o_f32, (size_t)MR * nh * hd);
   LA(L->y_acc, (size_t)MR * H);
@@ -605,10 +621,13 @@ static int current_sm_count() {
   return n;
 }
 
-// workspace: [status word + tickets, 256-byte aligned][partials]
+// workspace: [status word + tickets, 256-byte aligned][one (m, l, O) record per chunk].
+// The plan gives S = floor(slots / units) chunks per unit (at least 1), so units * S
+// never exceeds max(slots, units) with slots = 2 * SMs.
 static size_t attn_ws_head_bytes(int units) { return ((size_t)(units + 1) * 4 + 255) / 256 * 256; }
-static size_t attn_ws_bytes(int units, int max_splits, int hd) {
-  return attn_ws_head_bytes(units) + (size_t)units * max_splits * 8 * (hd + 2) * 4;
+static size_t attn_ws_bytes(int units, int slots, int hd) {
+  const size_t chunks = (size_t)(units > slots ? units : slots);
+  return attn_ws_head_bytes(units) + chunks * 8 * (hd + 2) * 4;
 }
 
 extern "C" size_t hfa_attention_workspace_bytes(const hfa_attn_desc* d, int batch) {

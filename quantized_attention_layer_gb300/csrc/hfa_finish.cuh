@@ -1,0 +1,98 @@
+// hfa_finish.cuh -- epilogues that run once a head (QKV) or a row group (o_proj) of a
+// projection is complete: per-head RMSNorm, NeoX RoPE and the bf16 KV append
+// (gemma4/gpu_full_attn.rs, encode_one_layer: fused per-head norm + RoPE, GPU V norm,
+// dense KV copy), and the residual add (dflash/forward.rs, dispatch_dflash_residual_add).
+// Shared by the decode GEMV and the verify-block GEMM.
+#pragma once
+#include "hfa_common.cuh"
+#include "hfa_internal.h"
+
+namespace hfa {
+
+// Cosine and sine of phi = P * theta^(-2i/hd) with phi reduced exactly enough in fp32:
+// u = P * g with g = theta^(-2i/hd) / (2 pi) held as an fp32 (hi, lo) pair; the product
+// P * hi is split into its rounded value and exact error (fma), the integer part is
+// dropped, and sincospi of twice the fractional turn gives the rotation.
+__device__ __forceinline__ void rope_cs(int P, float2 gpair, float& c, float& s) {
+  const float Pf = (float)P;
+  const float p1 = Pf * gpair.x;
+  const float e1 = fmaf(Pf, gpair.x, -p1);
+  const float k = rintf(p1);
+  const float r = (p1 - k) + (e1 + Pf * gpair.y);
+  sincospif(2.0f * r, &s, &c);
+}
+
+// Epilogue of one attention head (QKV mode): rows [hh*hd, hh*hd + hd) of the QKV output.
+template <int HD>
+static __device__ void finish_head(const GemvArgs& a, int hh, int lane) {
+  constexpr int J = HD / 32;   // values per lane; pairs (j, j + J/2) are RoPE partners
+  const int R16 = a.R * 16;
+  const int kind = hh < a.nh ? 0 : (hh < a.nh + a.nkv ? 1 : 2);  // q, k, v
+  for (int b = 0; b < a.batch; ++b) {
+    float v[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      float* p = a.acc + (size_t)b * R16 + (size_t)hh * HD + lane + 32 * j;
+      v[j] = ld_cg_f32(p);
+      *p = 0.0f;
+    }
+    const int seq = a.rows_are_tokens ? 0 : b;
+    const int P = a.rows_are_tokens ? a.base_pos + b : a.seq_pos[b];
+    if (kind < 2 || a.v_unit_norm) {
+      float ss = 0.f;
+#pragma unroll
+      for (int j = 0; j < J; ++j) ss += v[j] * v[j];
+      ss = warp_sum(ss);
+      const float inv = rsqrtf(ss / HD + a.eps);
+      const float* w = kind == 0 ? a.w_q : (kind == 1 ? a.w_k : nullptr);
+#pragma unroll
+      for (int j = 0; j < J; ++j) v[j] *= inv * (w ? __ldg(w + lane + 32 * j) : 1.0f);
+    }
+    if (kind < 2) {
+#pragma unroll
+      for (int j = 0; j < J / 2; ++j) {
+        float c, s;
+        rope_cs(P, a.rope_g[lane + 32 * j], c, s);
+        const float x0 = v[j], x1 = v[j + J / 2];
+        v[j] = x0 * c - x1 * s;
+        v[j + J / 2] = x0 * s + x1 * c;
+      }
+    }
+    if (kind == 0) {
+      float* q = a.q_out + ((size_t)b * a.nh + hh) * HD;
+#pragma unroll
+      for (int j = 0; j < J; ++j) q[lane + 32 * j] = v[j];
+    } else {
+      const int kvh = kind == 1 ? hh - a.nh : hh - a.nh - a.nkv;
+      if (P < 0 || (!a.ring && P >= a.C)) {
+        if (lane == 0) atomicOr(a.err, kErrBadPosition);
+        continue;
+      }
+      const int slot = a.ring ? P % a.C : P;
+      __nv_bfloat16* cache = kind == 1 ? a.k_cache : a.v_cache;
+      __nv_bfloat16* dst = cache + (((size_t)seq * a.nkv + kvh) * a.C + slot) * HD;
+      float* tap = kind == 1 ? a.k_tap : a.v_tap;
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        dst[lane + 32 * j] = __float2bfloat16_rn(v[j]);
+        if (tap) tap[((size_t)b * a.nkv + kvh) * HD + lane + 32 * j] = v[j];
+      }
+    }
+  }
+}
+
+// Epilogue of one row group (o_proj mode): out = bf16(x + y).
+static __device__ void finish_rowgroup(const GemvArgs& a, int r, int lane) {
+  const int R16 = a.R * 16;
+  for (int i = lane; i < 16 * a.batch; i += 32) {
+    const int b = i >> 4, row = r * 16 + (i & 15);
+    float* p = a.acc + (size_t)b * R16 + row;
+    const float y = ld_cg_f32(p);
+    *p = 0.0f;
+    const float o = __bfloat162float(a.x[(size_t)b * R16 + row]) + y;
+    a.out[(size_t)b * R16 + row] = __float2bfloat16_rn(o);
+    if (a.out_tap) a.out_tap[(size_t)b * R16 + row] = o;
+  }
+}
+
+}  // namespace hfa

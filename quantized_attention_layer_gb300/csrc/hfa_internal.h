@@ -51,8 +51,9 @@ struct GemvArgs {
   // OPROJ finisher
   __nv_bfloat16* out;      // bf16 [B, R*16]
   float* out_tap;          // nullable f32 [B, R*16]
-  // verify rows: row b of the GEMV uses position seq_pos[0] + b and sequence 0
+  // verify rows: row b of the GEMV is token b of sequence 0 at position base_pos + b
   int rows_are_tokens;
+  int base_pos;
 };
 
 struct AttnArgs {
@@ -71,6 +72,14 @@ struct AttnArgs {
 };
 
 enum GemvMode { kModeQKV = 0, kModeOProj = 1 };
+
+// message returned by hfa_last_error(NULL) on this thread
+void set_thread_error(const char* msg);
+
+// TMA descriptor of a row-major bf16 matrix [rows, inner] with boxes of
+// box_inner x box_rows and the 128-byte swizzle (box_inner * 2 must be 128)
+bool encode_bf16_2d(CUtensorMap* map, void* base, int inner, int rows, int box_inner,
+                    int box_rows);
 
 cudaError_t launch_repack_q8_0(const uint8_t* src, int rows, int cols, Q8Tiles* dst,
                                size_t row_offset_rows, cudaStream_t s);

@@ -1,23 +1,727 @@
-// k_verify.cu -- multi-token verify block (placeholder until the tensor-core path lands).
+// k_verify.cu -- the multi-token verify block of one layer (L <= 16 tokens, batch 1).
+//
+// gemma4/model.rs names the dense tree-verify entry of the full layer; the block form is
+// the one dflash/forward.rs builds for its drafter: input norm and projections of all L
+// rows, per-head norms, RoPE at positions base .. base+L-1, all L K/V rows appended to
+// the cache, attention of every row over the cache (causal inside the block), o_proj,
+// residual.  With bf16 weights the projections are dense contractions [L, H] x [H, N]:
+//
+//  * verify_gemm_kernel (tcgen05): swap-AB -- the weight rows are the MMA's M = 128, the
+//    activations its N = 32 (16 tokens x fp32 split into bf16 hi and lo, so the product
+//    keeps ~16 bits of the activation), K in 64-element stages.  A TMA producer thread
+//    streams 128x64 weight tiles (128-byte swizzle) into a 4-stage mbarrier ring; one
+//    thread issues tcgen05.mma into a 128x32 fp32 TMEM accumulator and releases stages
+//    with tcgen05.commit; the four warps read the accumulator back (tcgen05.ld) and add
+//    their partial sums (k-split) into an fp32 accumulator.  The CTA whose chunks
+//    complete a head / row tile runs the same epilogue as the decode GEMV.
+//  * attn_verify_kernel: one CTA per (KV head, key chunk); a TMA producer warp streams K
+//    and V tiles, each consumer warp owns 8 query rows (bf16 hi/lo in MMA rows g and
+//    g + 8) and sweeps every key of the stage with the causal mask of its rows.
 #include <stdio.h>
 
+#include "hfa_common.cuh"
+#include "hfa_finish.cuh"
+#include "hfa_internal.h"
 #include "hfa_verify.h"
+
+hfa_status hfa_encode_kv_map(CUtensorMap* map, void* base, int rows, int hd, int box_rows);
 
 namespace hfa {
 
-struct VerifyState {
-  int unused;
+// ------------------------------------------------------------------ GEMM (tcgen05)
+constexpr int kVM = 128;         // weight rows per CTA = MMA M
+constexpr int kVN = 32;          // MMA N: 16 tokens x (hi, lo)
+constexpr int kVK = 64;          // K elements per stage (one 128-byte swizzled row)
+constexpr int kVStages = 4;
+constexpr int kVMaxChunks = 24;  // K stages per CTA whose activation tile stays resident
+constexpr int kAStageBytes = kVM * kVK * 2;  // 16 KB
+constexpr int kBChunkBytes = kVN * kVK * 2;  // 4 KB
+constexpr size_t kVGemmSmem =
+    1024 + (size_t)kVStages * kAStageBytes + (size_t)kVMaxChunks * kBChunkBytes + 256;
+
+struct VGemmArgs {
+  GemvArgs g;        // epilogue arguments (accumulator, tickets, norms, caches, ...)
+  int rows;          // output features
+  int K;             // input features
+  int chunks;        // K / 64
+  int splits;        // k-splits per row tile
+  int need;          // chunk contributions that complete a head (QKV) / row tile (o_proj)
 };
 
-hfa_status verify_create(const hfa_layer_desc&, int, VerifyState** out) {
-  *out = new VerifyState();
+template <int MODE>
+__global__ void __launch_bounds__(128) verify_gemm_kernel(const __grid_constant__ CUtensorMap tw,
+                                                          const VGemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~(uintptr_t)1023);
+  uint8_t* sa = smem;                                   // A stages
+  uint8_t* sb = smem + kVStages * kAStageBytes;         // B chunks of this CTA
+  uint64_t* full = reinterpret_cast<uint64_t*>(sb + kVMaxChunks * kBChunkBytes);
+  uint64_t* empty = full + kVStages;
+  uint64_t* done = empty + kVStages;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(done + 1);
+  int* s_fin = reinterpret_cast<int*>(s_tmem + 1);      // [0..3] finished heads / tile flag
+  __shared__ float s_inv[16];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt = blockIdx.x / a.splits, sp = blockIdx.x - mt * a.splits;
+  const int c0 = a.chunks * sp / a.splits, c1 = a.chunks * (sp + 1) / a.splits;
+  const int nch = c1 - c0;
+  const int m0 = mt * kVM;
+  const int L = a.g.batch;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kVStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(done, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(s_tmem, kVN);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) prefetch_tmap(&tw);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  pdl_wait();
+
+  // ---- B operand: activations of chunks [c0, c1), rows 0..15 bf16 hi, 16..31 bf16 lo
+  if (MODE == kModeQKV) {
+    for (int t = warp; t < L; t += 4) {
+      float ss = 0.f;
+      const __nv_bfloat16* xr = a.g.x + (size_t)t * a.K;
+      for (int k = lane * 8; k < a.K; k += 256) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(xr + k);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(h[e]);
+          ss += f.x * f.x + f.y * f.y;
+        }
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) s_inv[t] = rsqrtf(ss / a.K + a.g.eps);
+    }
+    __syncthreads();
+  }
+  for (int e = threadIdx.x; e < nch * 16 * 8; e += blockDim.x) {
+    const int c = e >> 7, t = (e >> 3) & 15, c16 = e & 7;
+    const int k = (c0 + c) * kVK + c16 * 8;
+    float v[8];
+    if (t < L) {
+      if (MODE == kModeQKV) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(a.g.x + (size_t)t * a.K + k);
+        const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.g.w_in + k));
+        const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.g.w_in + k + 4));
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+        const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __bfloat1622float2(h[i]);
+          v[2 * i] = f.x * s_inv[t] * wv[2 * i];
+          v[2 * i + 1] = f.y * s_inv[t] * wv[2 * i + 1];
+        }
+      } else {
+        const float4 f0 = *reinterpret_cast<const float4*>(a.g.xin + (size_t)t * a.K + k);
+        const float4 f1 = *reinterpret_cast<const float4*>(a.g.xin + (size_t)t * a.K + k + 4);
+        v[0] = f0.x; v[1] = f0.y; v[2] = f0.z; v[3] = f0.w;
+        v[4] = f1.x; v[5] = f1.y; v[6] = f1.z; v[7] = f1.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = 0.f;
+    }
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat16 h0, l0, h1, l1;
+      split_bf16(v[2 * i], h0, l0);
+      split_bf16(v[2 * i + 1], h1, l1);
+      hw[i] = pack_bf2(h0, h1);
+      lw[i] = pack_bf2(l0, l1);
+    }
+    uint8_t* chunk = sb + c * kBChunkBytes;
+    const int rh = t, rl = 16 + t;
+    *reinterpret_cast<uint4*>(chunk + rh * 128 + ((c16 ^ (rh & 7)) << 4)) =
+        make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(chunk + rl * 128 + ((c16 ^ (rl & 7)) << 4)) =
+        make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  }
+  fence_proxy_async_smem();  // generic-proxy writes above are read by the tensor cores
+  __syncthreads();
+  pdl_launch_dependents();
+
+  if (warp == 0 && lane == 0) {
+    // ---- TMA producer
+    for (int i = 0; i < nch; ++i) {
+      const int st = i % kVStages;
+      if (i >= kVStages && !mbar_wait(&empty[st], ((i / kVStages) - 1) & 1, a.g.err)) break;
+      mbar_arrive_expect_tx(&full[st], kAStageBytes);
+      tma_load_2d(sa + st * kAStageBytes, &tw, &full[st], (c0 + i) * kVK, m0);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer
+    constexpr uint32_t idesc = idesc_bf16_f32(kVM, kVN);
+    for (int i = 0; i < nch; ++i) {
+      const int st = i % kVStages;
+      if (!mbar_wait(&full[st], (i / kVStages) & 1, a.g.err)) break;
+      tc_fence_after();
+      const uint32_t abase = smem_u32(sa + st * kAStageBytes);
+      const uint32_t bbase = smem_u32(sb + i * kBChunkBytes);
+#pragma unroll
+      for (int kk = 0; kk < kVK / 16; ++kk)
+        tc_mma_f16(tmem, smem_desc_sw128(abase + kk * 32), smem_desc_sw128(bbase + kk * 32),
+                   idesc, (i | kk) != 0);
+      tc_commit(&empty[st]);
+    }
+    tc_commit(done);
+  }
+  __syncwarp();
+  // ---- epilogue: accumulator rows 32w..32w+31, columns 0..15 hi, 16..31 lo
+  const bool ok = mbar_wait(done, 0, a.g.err);
+  tc_fence_after();
+  if (ok) {
+    float hi[16], lo[16];
+    const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16);
+    tmem_ld_32x32b_x16(taddr, hi);
+    tmem_ld_32x32b_x16(taddr + 16, lo);
+    const int row = m0 + 32 * warp + lane;
+    const int R16 = a.g.R * 16;
+#pragma unroll
+    for (int t = 0; t < 16; ++t)
+      if (t < L) red_add_f32(a.g.acc + (size_t)t * R16 + row, hi[t] + lo[t]);
+  }
+  tc_fence_before();
+  __threadfence();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, kVN);
+
+  // ---- completion tickets and epilogues
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 4; ++i) s_fin[i] = -1;
+    if (MODE == kModeQKV) {
+      const int h0 = m0 / a.g.hd, h1 = (m0 + kVM - 1) / a.g.hd;
+      for (int h = h0, j = 0; h <= h1 && j < 4; ++h, ++j)
+        if (atomicAdd(a.g.ticket + h, nch) + nch == a.need) s_fin[j] = h;
+    } else {
+      if (atomicAdd(a.g.ticket + mt, nch) + nch == a.need) s_fin[0] = mt;
+    }
+  }
+  __syncthreads();
+  __threadfence();
+  if (MODE == kModeQKV) {
+    if (s_fin[warp] >= 0) {
+      if (lane == 0) a.g.ticket[s_fin[warp]] = 0;
+      if (a.g.hd == 64) finish_head<64>(a.g, s_fin[warp], lane);
+      else if (a.g.hd == 128) finish_head<128>(a.g, s_fin[warp], lane);
+      else finish_head<256>(a.g, s_fin[warp], lane);
+    }
+  } else if (s_fin[0] >= 0) {
+    if (threadIdx.x == 0) a.g.ticket[mt] = 0;
+    for (int r = warp; r < kVM / 16; r += 4) finish_rowgroup(a.g, m0 / 16 + r, lane);
+  }
+}
+
+// ------------------------------------------------------------------ block attention
+constexpr int kVT = 64;  // keys per stage
+
+struct VAttnArgs {
+  const float* q;  // [L, nh, hd]
+  int L, nh, nkv, G, C, base, sliding, window;
+  float qscale, cap_log2;
+  int splits, chunk, klo, khi;  // keys [klo, khi] are read by some row
+  float* part;                  // [nkv][splits][64 rows][hd + 2]
+  int* ticket;                  // [nkv]
+  float* o;                     // [L, nh, hd]
+  unsigned* err;
+};
+
+template <int HD>
+struct VACfg {
+  static constexpr int NS = HD >= 256 ? 2 : 3;  // stages (shared memory budget)
+  static constexpr int TILE = kVT * HD * 2;
+  static constexpr int STAGE = 2 * TILE;
+  static constexpr int KS = HD / 16;
+  static constexpr int NTO = HD / 8;
+  static constexpr size_t SMEM = 1024 + (size_t)NS * STAGE + 8 * KS * 32 * 16 + 256;
+};
+
+template <int HD>
+__device__ __forceinline__ uint32_t vswz(int row, int chunk) {
+  const int box = chunk >> 3, c = chunk & 7;
+  return (uint32_t)(box * (kVT * 128) + row * 128 + ((c ^ (row & 7)) << 4));
+}
+
+template <int HD>
+__global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant__ CUtensorMap tmk,
+                                                          const __grid_constant__ CUtensorMap tmv,
+                                                          const VAttnArgs a) {
+  using Cfg = VACfg<HD>;
+  constexpr int NS = Cfg::NS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~(uintptr_t)1023);
+  uint8_t* stages = smem;
+  uint4* qf = reinterpret_cast<uint4*>(smem + NS * Cfg::STAGE);  // [warp][KS][32]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * Cfg::STAGE + 8 * Cfg::KS * 512);
+  uint64_t* empty = full + NS;
+  int* s_flags = reinterpret_cast<int*>(empty + NS);
+
+  const int nc = (blockDim.x >> 5) - 1;  // consumer warps, 8 query rows each
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int kvh = blockIdx.x / a.splits, split = blockIdx.x - kvh * a.splits;
+  const int NQ = a.L * a.G;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], nc);
+    }
+    s_flags[0] = 0;
+    s_flags[1] = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  pdl_wait();
+
+  const int k_begin = a.klo + split * a.chunk;
+  int k_end = k_begin + a.chunk;
+  if (k_end > a.khi + 1) k_end = a.khi + 1;
+  const int nkeys = k_end > k_begin ? k_end - k_begin : 0;
+  const int ntiles = (nkeys + kVT - 1) / kVT;
+  const int row0 = kvh * a.C + k_begin;
+  float* part = a.part + ((size_t)kvh * a.splits + split) * 64 * (HD + 2);
+
+  if (warp == nc) {
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < ntiles; ++i) {
+        const int st = i % NS;
+        if (i >= NS && !mbar_wait(&empty[st], ((i / NS) - 1) & 1, a.err, &s_flags[0])) {
+          atomicExch(&s_flags[0], 1);
+          break;
+        }
+        if (*(volatile int*)&s_flags[0]) break;
+        uint8_t* kt = stages + st * Cfg::STAGE;
+        mbar_arrive_expect_tx(&full[st], Cfg::STAGE);
+#pragma unroll
+        for (int j = 0; j < HD / 64; ++j) {
+          tma_load_2d(kt + j * kVT * 128, &tmk, &full[st], 64 * j, row0 + i * kVT);
+          tma_load_2d(kt + Cfg::TILE + j * kVT * 128, &tmv, &full[st], 64 * j, row0 + i * kVT);
+        }
+        issued = i + 1;
+      }
+      s_flags[1] = issued;
+    }
+  } else {
+    // query rows of this warp: q = 8 warp + g  ->  token q / G, head kvh G + q % G
+    const int qrow = 8 * warp + g;
+    const bool qvalid = qrow < NQ;
+    const int tok = qvalid ? qrow / a.G : 0;
+    const int limit = a.base + tok;  // last visible position of this row
+    uint4* myq = qf + warp * Cfg::KS * 32;
+    for (int ks = 0; ks < Cfg::KS; ++ks) {
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
+      if (qvalid) {
+        const float* q =
+            a.q + ((size_t)tok * a.nh + kvh * a.G + qrow % a.G) * HD + ks * 16 + 2 * t;
+        __nv_bfloat16 h[4], l[4];
+        split_bf16(q[0] * a.qscale, h[0], l[0]);
+        split_bf16(q[1] * a.qscale, h[1], l[1]);
+        split_bf16(q[8] * a.qscale, h[2], l[2]);
+        split_bf16(q[9] * a.qscale, h[3], l[3]);
+        w[0] = pack_bf2(h[0], h[1]);
+        w[1] = pack_bf2(l[0], l[1]);
+        w[2] = pack_bf2(h[2], h[3]);
+        w[3] = pack_bf2(l[2], l[3]);
+      }
+      myq[ks * 32 + lane] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __syncwarp();
+    float m = -INFINITY, l = 0.f;
+    float o[Cfg::NTO][4];
+#pragma unroll
+    for (int i = 0; i < Cfg::NTO; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    const uint32_t stage_base = smem_u32(stages);
+    for (int i = 0; i < ntiles; ++i) {
+      const int st = i % NS;
+      if (*(volatile int*)&s_flags[0]) break;
+      if (!mbar_wait(&full[st], (i / NS) & 1, a.err, &s_flags[0])) {
+        atomicExch(&s_flags[0], 1);
+        break;
+      }
+      const uint32_t kb = stage_base + st * Cfg::STAGE;
+      const uint32_t vb = kb + Cfg::TILE;
+      for (int kg = 0; kg < kVT / 16; ++kg) {
+        const int krow = kg * 16;
+        const int key0 = k_begin + i * kVT + krow;
+        if (key0 >= k_end) break;
+        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < Cfg::KS; ++ks) {
+          const uint4 qa = myq[ks * 32 + lane];
+          const uint32_t A[4] = {qa.x, qa.y, qa.z, qa.w};
+          const int mrow = krow + ((lane >> 4) << 3) + (lane & 7);
+          const int mchunk = ks * 2 + ((lane >> 3) & 1);
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4(kb + vswz<HD>(mrow, mchunk), b0, b1, b2, b3);
+          mma_bf16(s0, A, b0, b1);
+          mma_bf16(s1, A, b2, b3);
+        }
+        float sv[4] = {s0[0] + s0[2], s0[1] + s0[3], s1[0] + s1[2], s1[1] + s1[3]};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int key = key0 + 2 * t + (e & 1) + ((e >> 1) << 3);
+          float s = sv[e];
+          if (a.cap_log2 != 0.f) s = a.cap_log2 * tanhf(s);
+          const bool vis = key < k_end && key <= limit && (!a.sliding || key > limit - a.window);
+          sv[e] = vis ? s : -INFINITY;
+        }
+        float mloc = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
+        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
+        const float m_new = fmaxf(m, mloc);
+        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+        const float corr = exp2f(m - m_use);
+        float p[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) p[e] = exp2f(sv[e] - m_use);
+        l = l * corr + (p[0] + p[1]) + (p[2] + p[3]);
+        m = m_new;
+#pragma unroll
+        for (int nt = 0; nt < Cfg::NTO; ++nt) {
+          o[nt][0] *= corr;
+          o[nt][1] *= corr;
+          o[nt][2] *= corr;
+          o[nt][3] *= corr;
+        }
+        uint32_t PA[4];
+        {
+          __nv_bfloat16 h[4], lw[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) split_bf16(p[e], h[e], lw[e]);
+          PA[0] = pack_bf2(h[0], h[1]);
+          PA[1] = pack_bf2(lw[0], lw[1]);
+          PA[2] = pack_bf2(h[2], h[3]);
+          PA[3] = pack_bf2(lw[2], lw[3]);
+        }
+#pragma unroll
+        for (int np = 0; np < Cfg::NTO / 2; ++np) {
+          const int mrow = krow + (((lane >> 3) & 1) << 3) + (lane & 7);
+          const int mchunk = np * 2 + (lane >> 4);
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4_trans(vb + vswz<HD>(mrow, mchunk), b0, b1, b2, b3);
+          mma_bf16(o[2 * np], PA, b0, b1);
+          mma_bf16(o[2 * np + 1], PA, b2, b3);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+    }
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    if (qvalid) {
+      float* pr = part + (size_t)qrow * (HD + 2);
+      if (t == 0) {
+        pr[HD] = m;
+        pr[HD + 1] = l;
+      }
+#pragma unroll
+      for (int nt = 0; nt < Cfg::NTO; ++nt) {
+        pr[nt * 8 + 2 * t] = o[nt][0] + o[nt][2];
+        pr[nt * 8 + 2 * t + 1] = o[nt][1] + o[nt][3];
+      }
+    }
+  }
+
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int issued = s_flags[1];
+    for (int st = 0; st < NS && st < issued; ++st) {
+      const int last = st + ((issued - 1 - st) / NS) * NS;
+      mbar_wait(&full[st], (last / NS) & 1, a.err);
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_flags[2] = (atomicAdd(a.ticket + kvh, 1) == a.splits - 1);
+  __syncthreads();
+  if (!s_flags[2]) return;
+  __threadfence();
+  if (threadIdx.x == 0) a.ticket[kvh] = 0;
+  const float* up = a.part + (size_t)kvh * a.splits * 64 * (HD + 2);
+  float* wsm = reinterpret_cast<float*>(stages);  // [64 rows][splits]
+  const int nwarps = blockDim.x >> 5;
+  for (int r = warp; r < NQ; r += nwarps) {
+    float M = -INFINITY;
+    for (int sp = lane; sp < a.splits; sp += 32)
+      M = fmaxf(M, ld_cg_f32(up + ((size_t)sp * 64 + r) * (HD + 2) + HD));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float Mu = M == -INFINITY ? 0.f : M;
+    float den = 0.f;
+    for (int sp = lane; sp < a.splits; sp += 32) {
+      const float* ps = up + ((size_t)sp * 64 + r) * (HD + 2);
+      const float f = exp2f(ld_cg_f32(ps + HD) - Mu);
+      wsm[r * a.splits + sp] = f;
+      den += f * ld_cg_f32(ps + HD + 1);
+    }
+    den = warp_sum(den);
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    __syncwarp();
+    for (int sp = lane; sp < a.splits; sp += 32) wsm[r * a.splits + sp] *= inv;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < NQ * HD; e += blockDim.x) {
+    const int r = e / HD, d = e - r * HD;
+    float acc = 0.f;
+    for (int sp = 0; sp < a.splits; ++sp)
+      acc += wsm[r * a.splits + sp] * ld_cg_f32(up + ((size_t)sp * 64 + r) * (HD + 2) + d);
+    const int tok = r / a.G, h = kvh * a.G + r % a.G;
+    a.o[((size_t)tok * a.nh + h) * HD + d] = acc;
+  }
+}
+
+// ------------------------------------------------------------------ host side
+struct VerifyState {
+  CUtensorMap tm_wqkv, tm_wo;
+  const void* tm_wqkv_ptr = nullptr;
+  int* head_ticket = nullptr;   // [nh + 2 nkv]
+  int* tile_ticket = nullptr;   // [H / 128]
+  int* attn_ticket = nullptr;   // [nkv]
+  float* part = nullptr;        // [max(SMs, nkv)][64][hd + 2]
+  float* qkv_acc = nullptr;     // [16][rows_qkv]
+  float* y_acc = nullptr;       // [16][H]
+  size_t part_records = 0;
+};
+
+static char g_verify_error[256];
+const char* verify_error() { return g_verify_error; }
+
+hfa_status verify_create(const hfa_layer_desc& d, int num_sms, VerifyState** out) {
+  *out = nullptr;
+  if (!(d.flags & HFA_F_WEIGHTS_BF16)) {
+    *out = new VerifyState();  // a Q8_0 layer has no verify block: nothing to allocate
+    return HFA_OK;
+  }
+  const int rows_qkv = (d.num_heads + 2 * d.num_kv_heads) * d.head_dim;
+  if (rows_qkv % kVM || d.hidden % kVM || d.hidden % kVK || (d.num_heads * d.head_dim) % kVK) {
+    snprintf(g_verify_error, sizeof g_verify_error,
+             "verify GEMM needs projection sizes that are multiples of 128");
+    return HFA_EUNSUPPORTED;
+  }
+  VerifyState* v = new VerifyState();
+  const int nkv = d.num_kv_heads;
+  v->part_records = (size_t)(num_sms > nkv ? num_sms : nkv);
+  cudaError_t e = cudaMalloc(&v->head_ticket, (d.num_heads + 2 * nkv) * sizeof(int));
+  if (e == cudaSuccess) e = cudaMalloc(&v->tile_ticket, (d.hidden / kVM) * sizeof(int));
+  if (e == cudaSuccess) e = cudaMalloc(&v->attn_ticket, nkv * sizeof(int));
+  if (e == cudaSuccess)
+    e = cudaMalloc(&v->part, v->part_records * 64 * (d.head_dim + 2) * sizeof(float));
+  if (e == cudaSuccess) e = cudaMalloc(&v->qkv_acc, (size_t)16 * rows_qkv * sizeof(float));
+  if (e == cudaSuccess) e = cudaMalloc(&v->y_acc, (size_t)16 * d.hidden * sizeof(float));
+  if (e == cudaSuccess) e = cudaMemset(v->head_ticket, 0, (d.num_heads + 2 * nkv) * sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(v->tile_ticket, 0, (d.hidden / kVM) * sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(v->attn_ticket, 0, nkv * sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(v->qkv_acc, 0, (size_t)16 * rows_qkv * sizeof(float));
+  if (e == cudaSuccess) e = cudaMemset(v->y_acc, 0, (size_t)16 * d.hidden * sizeof(float));
+  if (e != cudaSuccess) {
+    snprintf(g_verify_error, sizeof g_verify_error, "%s", cudaGetErrorString(e));
+    verify_free(v);
+    return HFA_ENOMEM;
+  }
+  *out = v;
   return HFA_OK;
 }
-void verify_free(VerifyState* v) { delete v; }
-const char* verify_error() { return ""; }
-hfa_status verify_run(VerifyState*, const VerifyCall&, char* msg, int n) {
-  snprintf(msg, n, "verify block not built yet");
-  return HFA_EUNSUPPORTED;
+
+void verify_free(VerifyState* v) {
+  if (!v) return;
+  cudaFree(v->head_ticket);
+  cudaFree(v->tile_ticket);
+  cudaFree(v->attn_ticket);
+  cudaFree(v->part);
+  cudaFree(v->qkv_acc);
+  cudaFree(v->y_acc);
+  delete v;
+}
+
+template <typename Kern, typename... Args>
+static cudaError_t launch_ex(Kern kern, int grid, int threads, size_t smem, bool pdl,
+                             cudaStream_t s, Args... args) {
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+static int gemm_splits(int tiles, int chunks, int num_sms) {
+  int S = num_sms / tiles;
+  if (S < 1) S = 1;
+  const int min_s = (chunks + kVMaxChunks - 1) / kVMaxChunks;
+  if (S < min_s) S = min_s;
+  if (S > chunks) S = chunks;
+  return S;
+}
+
+hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
+  const hfa_layer_desc& d = *c.d;
+  const int H = d.hidden, nh = d.num_heads, nkv = d.num_kv_heads, hd = d.head_dim;
+  const int G = nh / nkv;
+  const int rows_qkv = (nh + 2 * nkv) * hd;
+  if (!(d.flags & HFA_F_WEIGHTS_BF16) || !v->part) {
+    snprintf(msg, n, "verify is built for bf16 weights");
+    return HFA_EUNSUPPORTED;
+  }
+  if (c.L * G > 64) {
+    snprintf(msg, n, "L * (num_heads / num_kv_heads) = %d > 64 query rows per KV head", c.L * G);
+    return HFA_EUNSUPPORTED;
+  }
+  if (v->tm_wqkv_ptr != c.wqkv) {
+    if (!encode_bf16_2d(&v->tm_wqkv, (void*)c.wqkv, H, rows_qkv, kVK, kVM) ||
+        !encode_bf16_2d(&v->tm_wo, (void*)c.wo, nh * hd, H, kVK, kVM)) {
+      snprintf(msg, n, "cannot describe the weights to the TMA unit");
+      return HFA_EINVAL;
+    }
+    v->tm_wqkv_ptr = c.wqkv;
+  }
+  CUtensorMap tk, tv;
+  if (hfa_encode_kv_map(&tk, c.k_cache, nkv * d.kv_capacity, hd, kVT) != HFA_OK ||
+      hfa_encode_kv_map(&tv, c.v_cache, nkv * d.kv_capacity, hd, kVT) != HFA_OK) {
+    snprintf(msg, n, "cannot describe the KV cache to the TMA unit");
+    return HFA_EINVAL;
+  }
+  cudaStream_t s = c.stream;
+  cudaError_t e;
+
+  // (1) input norm + QKV projection + per-head norms + RoPE + append of all L rows
+  VGemmArgs qa{};
+  qa.g.batch = c.L;
+  qa.g.x = c.x;
+  qa.g.w_in = c.w_in;
+  qa.g.eps = d.eps;
+  qa.g.R = rows_qkv / 16;
+  qa.g.acc = v->qkv_acc;
+  qa.g.ticket = v->head_ticket;
+  qa.g.err = c.err;
+  qa.g.nh = nh;
+  qa.g.nkv = nkv;
+  qa.g.hd = hd;
+  qa.g.C = d.kv_capacity;
+  qa.g.ring = 0;
+  qa.g.w_q = c.w_q;
+  qa.g.w_k = c.w_k;
+  qa.g.rope_g = c.rope_g;
+  qa.g.v_unit_norm = (d.flags & HFA_F_V_UNIT_NORM) ? 1 : 0;
+  qa.g.q_out = c.q_f32;
+  qa.g.k_cache = c.k_cache;
+  qa.g.v_cache = c.v_cache;
+  qa.g.k_tap = c.k_tap;
+  qa.g.v_tap = c.v_tap;
+  qa.g.rows_are_tokens = 1;
+  qa.g.base_pos = c.base_pos;
+  qa.rows = rows_qkv;
+  qa.K = H;
+  qa.chunks = H / kVK;
+  const int qtiles = rows_qkv / kVM;
+  qa.splits = gemm_splits(qtiles, qa.chunks, c.num_sms);
+  qa.need = qa.chunks * (hd > kVM ? hd / kVM : 1);
+  e = launch_ex(verify_gemm_kernel<kModeQKV>, qtiles * qa.splits, 128, kVGemmSmem, true, s,
+                v->tm_wqkv, qa);
+  if (e != cudaSuccess) {
+    snprintf(msg, n, "verify QKV launch: %s", cudaGetErrorString(e));
+    return HFA_ECUDA;
+  }
+
+  // (2) block attention
+  VAttnArgs aa{};
+  aa.q = c.q_f32;
+  aa.L = c.L;
+  aa.nh = nh;
+  aa.nkv = nkv;
+  aa.G = G;
+  aa.C = d.kv_capacity;
+  aa.base = c.base_pos;
+  aa.sliding = d.layer_type == HFA_SLIDING;
+  aa.window = d.window;
+  const float log2e = 1.4426950408889634f;
+  if (d.softcap > 0.f) {
+    aa.qscale = d.attn_scale / d.softcap;
+    aa.cap_log2 = d.softcap * log2e;
+  } else {
+    aa.qscale = d.attn_scale * log2e;
+    aa.cap_log2 = 0.f;
+  }
+  aa.klo = aa.sliding ? (c.base_pos - d.window + 1 > 0 ? c.base_pos - d.window + 1 : 0) : 0;
+  aa.khi = c.base_pos + c.L - 1;
+  const int nkeys = aa.khi - aa.klo + 1;
+  int S = c.num_sms / nkv;
+  const int max_tiles = (nkeys + kVT - 1) / kVT;
+  if (S > max_tiles) S = max_tiles;
+  if ((size_t)S * nkv > v->part_records) S = (int)(v->part_records / nkv);
+  if (S < 1) S = 1;
+  int chunk = (nkeys + S - 1) / S;
+  chunk = (chunk + kVT - 1) / kVT * kVT;
+  S = (nkeys + chunk - 1) / chunk;
+  aa.splits = S;
+  aa.chunk = chunk;
+  aa.part = v->part;
+  aa.ticket = v->attn_ticket;
+  aa.o = c.o_f32;
+  aa.err = c.err;
+  const int nq_warps = (c.L * G + 7) / 8;
+  const int athreads = (nq_warps + 1) * 32;
+  if (hd == 64)
+    e = launch_ex(attn_verify_kernel<64>, nkv * S, athreads, VACfg<64>::SMEM, true, s, tk, tv, aa);
+  else if (hd == 128)
+    e = launch_ex(attn_verify_kernel<128>, nkv * S, athreads, VACfg<128>::SMEM, true, s, tk, tv,
+                  aa);
+  else
+    e = launch_ex(attn_verify_kernel<256>, nkv * S, athreads, VACfg<256>::SMEM, true, s, tk, tv,
+                  aa);
+  if (e != cudaSuccess) {
+    snprintf(msg, n, "verify attention launch: %s", cudaGetErrorString(e));
+    return HFA_ECUDA;
+  }
+
+  // (3) o_proj + residual
+  VGemmArgs oa{};
+  oa.g.batch = c.L;
+  oa.g.x = c.x;
+  oa.g.xin = c.o_f32;
+  oa.g.R = H / 16;
+  oa.g.acc = v->y_acc;
+  oa.g.ticket = v->tile_ticket;
+  oa.g.err = c.err;
+  oa.g.out = c.out;
+  oa.g.out_tap = c.out_tap;
+  oa.rows = H;
+  oa.K = nh * hd;
+  oa.chunks = oa.K / kVK;
+  const int otiles = H / kVM;
+  oa.splits = gemm_splits(otiles, oa.chunks, c.num_sms);
+  oa.need = oa.chunks;
+  e = launch_ex(verify_gemm_kernel<kModeOProj>, otiles * oa.splits, 128, kVGemmSmem, true, s,
+                v->tm_wo, oa);
+  if (e != cudaSuccess) {
+    snprintf(msg, n, "verify o_proj launch: %s", cudaGetErrorString(e));
+    return HFA_ECUDA;
+  }
+  return HFA_OK;
 }
 
 }  // namespace hfa

@@ -107,3 +107,61 @@ def check_decode(w: wl.Workload, pos, gpu, ref, kv_before, tol=REL_L2):
         assert report[key] <= tol, f"{key}: rel L2 {report[key]:.3e} > {tol}"
     assert report["out_bf16_exact"], "bf16 out is not the RNE of the kernel's fp32 out"
     return report
+
+
+def run_gpu_verify(w: wl.Workload, weights, x, base, kv):
+    layer = hfa.Layer(hfa.desc_for(w, debug_taps=True), hfa.weights_to_device(w, weights))
+    kc, vc = kv["k_cache"].cuda(), kv["v_cache"].cuda()
+    L = x.shape[0]
+    out = torch.empty((L, w.hidden), dtype=torch.bfloat16, device="cuda")
+    layer.hfa_verify_block(x.cuda(), base, kc, vc, out)
+    layer.hfa_check_device_status()
+    res = {"out_bf16": out, "k_cache": kc, "v_cache": vc}
+    res.update(layer.hfa_debug_taps(L))
+    torch.cuda.synchronize()
+    res = {k: v.cpu() for k, v in res.items()}
+    layer.hfa_destroy()
+    return res
+
+
+def check_verify(w: wl.Workload, base, gpu, ref, kv_before, tol=REL_L2):
+    """Float taps per token within tol; appended rows as in check_append; the rest of
+    the cache unchanged."""
+    L = gpu["q"].shape[0]
+    report = {}
+    for key in ("q", "k", "v", "attn", "out"):
+        report[key] = max(rel_l2(gpu[key][i].numpy(), ref[key][i]) for i in range(L))
+    own = np.array([oracle.f64_to_bf16(float(v)) for v in gpu["out"].numpy().ravel()],
+                   dtype=np.uint16)
+    report["out_bf16_exact"] = bool(np.array_equal(bits_of(gpu["out_bf16"]).ravel(), own))
+    n_mid = 0
+    for key in ("k", "v"):
+        g = bits_of(gpu[key + "_cache"]).reshape(w.num_kv_heads, w.kv_capacity, w.head_dim)
+        r = ref[key + "_cache"].reshape(g.shape)
+        before = bits_of(kv_before[key + "_cache"]).reshape(g.shape)
+        tap = gpu[key].numpy()                       # [L, nkv, hd]
+        for i in range(L):
+            slot = base + i
+            got = g[:, slot, :]
+            own_b = np.array([[oracle.f64_to_bf16(float(v)) for v in row] for row in tap[i]],
+                             dtype=np.uint16)
+            assert np.array_equal(got, own_b), "appended bytes are not the RNE of the kernel's fp32"
+            diff = got != r[:, slot, :]
+            if diff.any():
+                mid = 0.5 * (oracle.bf16_to_f64(got[diff]) + oracle.bf16_to_f64(r[:, slot, :][diff]))
+                v = ref[key][i][diff]
+                t = tap[i][diff].astype(np.float64)
+                rms = np.broadcast_to(np.sqrt(np.mean(ref[key][i] ** 2, axis=-1, keepdims=True)),
+                                      ref[key][i].shape)[diff]
+                assert np.all((t - mid) * (v - mid) <= 0)
+                assert np.all(np.abs(t - v) <= MIDPOINT_WINDOW * rms)
+                n_mid += int(diff.sum())
+        mask = np.ones(w.kv_capacity, dtype=bool)
+        mask[base:base + L] = False
+        assert np.array_equal(g[:, mask, :], before[:, mask, :]), "an untouched slot changed"
+    report["midpoints"] = n_mid
+    print(w.name, report)
+    for key in ("q", "k", "v", "attn", "out"):
+        assert report[key] <= tol, f"{key}: rel L2 {report[key]:.3e} > {tol}"
+    assert report["out_bf16_exact"]
+    return report

@@ -1,0 +1,56 @@
+"""GPU parity of the multi-token verify block (tcgen05 projections) against the oracle."""
+import pytest
+import torch
+
+import oracle
+from quantized_attention_layer_gb300 import workloads as wl
+
+from parity import check_verify, run_gpu_verify
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from quantized_attention_layer_gb300 import build
+    build.build()
+    oracle.build()
+
+
+def _case(w, L, base):
+    weights = wl.make_weights(w)
+    x = wl.make_x(w, rows=L)
+    kv = wl.make_kv_cache(w)
+    gpu = run_gpu_verify(w, weights, x, base, kv)
+    ref = oracle.verify_block(w, weights, x, base, kv["k_cache"], kv["v_cache"])
+    return check_verify(w, base, gpu, ref, kv)
+
+
+def test_verify_block_full_size():
+    w = wl.VERIFY_L16
+    _case(w, w.verify_len, w.base_pos)
+
+
+@pytest.mark.parametrize("L", [1, 5, 16])
+def test_verify_block_small_lengths(L):
+    w = wl.Workload(name=f"ver{L}", hidden=1024, num_heads=8, num_kv_heads=2, head_dim=128,
+                    layer_type=wl.FULL, window=0, kv_capacity=700, ring=False, batch=1,
+                    rope_theta=1e6, seed=90 + L, weights_bf16=True, verify_len=16, base_pos=0)
+    _case(w, L, 300)
+
+
+def test_verify_block_sliding_window_softcap_hd64():
+    w = wl.Workload(name="ver_sl", hidden=512, num_heads=8, num_kv_heads=4, head_dim=64,
+                    layer_type=wl.SLIDING, window=100, kv_capacity=600, ring=False, batch=1,
+                    rope_theta=1e4, seed=95, weights_bf16=True, verify_len=16, base_pos=0,
+                    softcap=30.0)
+    _case(w, 12, 450)
+
+
+def test_verify_block_at_position_zero():
+    w = wl.Workload(name="ver0", hidden=512, num_heads=4, num_kv_heads=2, head_dim=128,
+                    layer_type=wl.FULL, window=0, kv_capacity=64, ring=False, batch=1,
+                    rope_theta=1e6, seed=96, weights_bf16=True, verify_len=16, base_pos=0)
+    _case(w, 16, 0)
