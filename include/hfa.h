@@ -168,6 +168,26 @@ hfa_status hfa_attention_decode(const hfa_attn_desc* desc, void* stream, const f
                                 int batch, const void* k_cache_dev, const void* v_cache_dev,
                                 void* workspace_dev, size_t workspace_bytes, float* o_dev);
 
+/*
+ * hfa_attention_decode without a workspace argument, for callers that cannot allocate
+ * device memory where they run attention (an engine that fixes all device memory at
+ * start-up, a plugin whose host owns the allocator, code that must not let
+ * cudaMalloc/cudaFree synchronise the device).  No counterpart on the documentation
+ * pages: an interface addition of this library.
+ * Its scratch is a file-scope device array of 4 MiB that every GPU loading the library
+ * holds until exit.  Arguments and results are those of hfa_attention_decode; a batch
+ * whose scratch (hfa_attention_workspace_bytes) exceeds 4 MiB is rejected with
+ * HFA_ERANGE.  The first call on each device looks up the array's address (make it
+ * before any stream capture).  Each call clears the array's counters on `stream`; all
+ * calls share the array, so calls that overlap on the GPU race and must not be issued.
+ * Device-side wait timeouts of this variant are not reported.  Allocates nothing.
+ */
+hfa_status hfa_attention_decode_noalloc(const hfa_attn_desc* desc, void* stream,
+                                        const float* q_dev, const int32_t* seq_pos_dev,
+                                        const int32_t* seq_pos_host, int batch,
+                                        const void* k_cache_dev, const void* v_cache_dev,
+                                        float* o_dev);
+
 /* Release the layer and its device memory (synchronises the device first). */
 hfa_status hfa_destroy(hfa_layer* layer);
 

@@ -102,6 +102,9 @@ def lib():
         L.hfa_attention_decode.restype = C
         L.hfa_attention_decode.argtypes = [ctypes.POINTER(hfa_attn_desc), P, P, P, P, I, P, P, P,
                                            ctypes.c_size_t, P]
+        L.hfa_attention_decode_noalloc.restype = C
+        L.hfa_attention_decode_noalloc.argtypes = [ctypes.POINTER(hfa_attn_desc), P, P, P, P, I,
+                                                   P, P, P]
         _lib = L
     return _lib
 
@@ -137,6 +140,19 @@ def hfa_attention_decode(desc: hfa_attn_desc, q: torch.Tensor, seq_pos_dev: torc
                                     _ptr(seq_pos_dev), ctypes.c_void_p(pos_h.ctypes.data),
                                     int(pos_h.size), _ptr(k_cache), _ptr(v_cache), _ptr(workspace),
                                     workspace.numel() * workspace.element_size(), _ptr(o))
+    if st != HFA_OK:
+        raise HfaError(st, lib().hfa_last_error(None).decode())
+    return o
+
+
+def hfa_attention_decode_noalloc(desc: hfa_attn_desc, q: torch.Tensor, seq_pos_dev: torch.Tensor,
+                                 seq_pos_host, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                 o: torch.Tensor, stream=None) -> torch.Tensor:
+    """hfa_attention_decode with the library's static scratch instead of a workspace."""
+    pos_h = np.ascontiguousarray(seq_pos_host, dtype=np.int32)
+    st = lib().hfa_attention_decode_noalloc(ctypes.byref(desc), _stream_ptr(stream), _ptr(q),
+                                            _ptr(seq_pos_dev), ctypes.c_void_p(pos_h.ctypes.data),
+                                            int(pos_h.size), _ptr(k_cache), _ptr(v_cache), _ptr(o))
     if st != HFA_OK:
         raise HfaError(st, lib().hfa_last_error(None).decode())
     return o
