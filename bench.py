@@ -234,7 +234,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(local)
     w = wl.BY_NAME[args.workload]
     if w.verify_len:
-        raise SystemExit("the decode benchmark needs a decode workload")
+        return run_verify(args, rank, world, w)
     weights = wl.make_weights(w)
     x = wl.make_x(w)
     pos = wl.make_positions(w)
@@ -343,6 +343,89 @@ def run_ours(args, rank, world, local):
         line["cpu_baseline"] = cpu_baseline(w, weights, x, pos, kv)
     for L in layers:
         L.hfa_destroy()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_verify(args, rank, world, w):
+    """The multi-token verify block (L tokens through one layer, bf16 weights): blocks/s,
+    and the roofline of its QKV projection (tcgen05 GEMM) against HBM and tensor peaks."""
+    from quantized_attention_layer_gb300 import hfa, workloads as wl
+    weights = wl.make_weights(w)
+    x = wl.make_x(w)
+    kv = wl.make_kv_cache(w)
+    L, base = w.verify_len, w.base_pos
+    dev_w = hfa.weights_to_device(w, weights)
+    R = max(1, args.replicas)
+    stream = torch.cuda.Stream()
+    layers, caches = [], []
+    with torch.cuda.stream(stream):
+        for _ in range(R):
+            layers.append(hfa.Layer(hfa.desc_for(w), dev_w, stream=stream))
+            caches.append((kv["k_cache"].cuda(), kv["v_cache"].cuda()))
+    del dev_w
+    xd = x.cuda()
+    out = torch.empty((L, w.hidden), dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
+
+    def step(i):
+        kc, vc = caches[i % R]
+        layers[i % R].hfa_verify_block(xd, base, kc, vc, out, stream=stream)
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+    for Lr in layers:
+        Lr.hfa_check_device_status(stream=stream)
+        Lr.hfa_set_kernel_timing(True)
+        Lr.hfa_kernel_times()
+    for i in range(args.steps):
+        step(i)
+    torch.cuda.synchronize()
+    kt = {}
+    for Lr in layers:
+        for name, (kms, cnt) in Lr.hfa_kernel_times().items():
+            a = kt.setdefault(name, [0.0, 0])
+            a[0] += kms
+            a[1] += cnt
+        Lr.hfa_set_kernel_timing(False)
+    H, qr, kr = w.hidden, w.q_rows, w.kv_rows
+    wqkv_bytes = (qr + 2 * kr) * H * 2
+    wo_bytes = H * qr * 2
+    kv_bytes = (base + L) * w.num_kv_heads * w.head_dim * 2 * 2
+    step_bytes = wqkv_bytes + wo_bytes + kv_bytes + 2 * L * H * 2
+    peak, src = measured_peaks()
+    g = kt.get("verify_qkv_gemm", [float("nan"), 1])
+    g_us = g[0] / max(g[1], 1) * 1e3
+    flops = 2.0 * L * (qr + 2 * kr) * H
+    line = {"metric": "verify blocks/sec per layer (L tokens, bf16 weights)", "value": world * args.steps / (ms / 1e3),
+            "unit": "blocks/s", "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup),
+            "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "tokens": L, "prior": base, "hidden": H,
+                       "heads": f"{w.num_heads}/{w.num_kv_heads}", "head_dim": w.head_dim,
+                       "weights": "bf16", "l2": f"{R} layer replicas rotated"},
+            "step_gbs": step_bytes / (ms / args.steps * 1e-3) / 1e9,
+            "step_bytes": step_bytes,
+            "roofline": {"bound": "hbm", "kernel": "verify_qkv_gemm", "achieved": wqkv_bytes / (g_us * 1e-6) / 1e9,
+                         "peak": peak, "unit": "GB/s", "frac": wqkv_bytes / (g_us * 1e-6) / 1e9 / peak,
+                         "traffic": None, "useful_tflops": flops / (g_us * 1e-6) / 1e12,
+                         "peak_source": src},
+            "kernels": {k: {"avg_us": v[0] / max(v[1], 1) * 1e3, "launches": v[1]} for k, v in kt.items()},
+            "clocks": clk.summary(), "gpu_launches": 3 * args.steps}
+    for Lr in layers:
+        Lr.hfa_destroy()
     if rank == 0:
         print(json.dumps(line), flush=True)
 

@@ -29,6 +29,18 @@ struct KernelTimer {
   cudaEvent_t start, stop;
 };
 
+struct hfa_layer;
+static void timer_begin(hfa_layer* L, cudaStream_t s, const char* name, KernelTimer* t);
+static void timer_end(hfa_layer* L, cudaStream_t s, KernelTimer* t);
+
+// adapter that lets the verify kernels record into the layer's timing slots
+struct LayerTimer : hfa::LaunchTimer {
+  hfa_layer* L = nullptr;
+  KernelTimer t{};
+  void begin(cudaStream_t s, const char* name) override { timer_begin(L, s, name, &t); }
+  void end(cudaStream_t s) override { timer_end(L, s, &t); }
+};
+
 struct hfa_layer {
   hfa_layer_desc d{};
   int device = 0;
@@ -329,7 +341,7 @@ extern "C" hfa_status hfa_layer_create(const hfa_layer_desc* desc, const void* w
   LA(L->head_ticket, nh + 2 * nkv);
   LA(L->q_f32, (size_t)MR * nh * hd);
   // one (m, l, O) record per attention chunk: units * splits <= max(2 SMs, units)
-  LA(L->attn_part, (size_t)(units > L->max_splits ? units : L->max_splits) * 8 * (hd + 2));
+  LA(L->attn_part, (size_t)(units > L->max_splits ? units : L->max_splits) * attn_record_floats(hd));
   LA(L->attn_ticket, units);
   LA(L->o_f32, (size_t)MR * nh * hd);
   LA(L->y_acc, (size_t)MR * H);
@@ -393,23 +405,25 @@ static void fill_gemv_common(hfa_layer* L, GemvArgs& a, const Q8Tiles& w, int ba
 
 // k-split and grid of one GEMV: every warp streams the same number of tiles; the
 // activation operand of the (at most two) k-splits a CTA touches must fit in shared memory.
+// Work items of the GEMV: (k-split, row group) pairs of nbs tiles, one warp each, CTAs
+// of gemv_items_per_cta() consecutive items.  nbs = 16 blocks (512 columns) where the row
+// allows it, doubled while that leaves more than three CTAs per SM.
 static void plan_gemv(hfa_layer* L, GemvArgs& a, int* grid, int* threads, size_t* smem) {
-  const int nt = gemv_ntiles(a.batch);
-  const size_t per_block = (size_t)nt * 32 * 16;
-  int S = 1;
-  if ((size_t)a.nb * per_block > 96 * 1024) {
-    S = 2;
-    while ((a.nb % S) || (size_t)2 * (a.nb / S) * per_block > 160 * 1024) ++S;
-  }
-  a.S = S;
-  a.nbs = a.nb / S;
-  a.tiles = (long long)S * a.R * a.nbs;
-  const int blocks_max = S == 1 ? a.nb : 2 * a.nbs;
+  const int ipc = gemv_items_per_cta();
+  int nbs = a.nb % 16 == 0 ? 16 : (a.nb % 8 == 0 ? 8 : a.nb);
+  const long long resident = (gemv_ntiles(a.batch) >= 4 ? 2LL : 3LL) * L->num_sms;  // CTAs
+  while (a.nb % (2 * nbs) == 0 && (long long)(a.nb / nbs) * a.R / ipc > resident) nbs *= 2;
+  a.S = a.nb / nbs;
+  a.nbs = nbs;
+  a.tiles = (long long)a.S * a.R * a.nbs;
+  const int items = a.S * a.R;
+  // k-splits one CTA's ipc consecutive items can span (one when R is a multiple of ipc)
+  int spans = a.R % ipc == 0 ? 1 : (ipc - 1) / a.R + 2;
+  if (spans > a.S) spans = a.S;
+  const int blocks_max = spans * nbs;
   *smem = gemv_smem_bytes(a.batch, blocks_max);
-  *threads = nt == 4 ? 512 : 256;
-  const int per_sm = (*smem <= 100 * 1024 && *threads == 256) ? 2 : 1;
-  *grid = L->num_sms * per_sm;
-  if (*grid > a.tiles) *grid = (int)a.tiles;
+  *threads = ipc * 32;
+  *grid = (items + ipc - 1) / ipc;
 }
 
 static hfa_status launch_qkv(hfa_layer* L, cudaStream_t s, const void* x, const int* pos_dev,
@@ -627,7 +641,7 @@ static int current_sm_count() {
 static size_t attn_ws_head_bytes(int units) { return ((size_t)(units + 1) * 4 + 255) / 256 * 256; }
 static size_t attn_ws_bytes(int units, int slots, int hd) {
   const size_t chunks = (size_t)(units > slots ? units : slots);
-  return attn_ws_head_bytes(units) + chunks * 8 * (hd + 2) * 4;
+  return attn_ws_head_bytes(units) + chunks * attn_record_floats(hd) * 4;
 }
 
 extern "C" size_t hfa_attention_workspace_bytes(const hfa_attn_desc* d, int batch) {
@@ -751,6 +765,9 @@ extern "C" hfa_status hfa_verify_block(hfa_layer* L, void* stream, const void* x
   c.out_tap = L->out_tap;
   c.err = L->err;
   c.num_sms = L->num_sms;
+  LayerTimer lt;
+  lt.L = L;
+  c.timer = L->timing ? &lt : nullptr;
   char msg[256] = {0};
   hfa_status st = hfa::verify_run(L->verify, c, msg, sizeof msg);
   if (st != HFA_OK) return fail(L, st, "%s", msg);

@@ -127,6 +127,10 @@ __device__ __forceinline__ void fence_acq_rel_gpu() {
 __device__ __forceinline__ void red_add_f32(float* p, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
+// bulk prefetch of [p, p + bytes) into L2 (p and bytes multiples of 16)
+__device__ __forceinline__ void prefetch_bulk_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2::evict_normal [%0];" ::"l"(p));
 }

@@ -25,7 +25,7 @@ struct GemvArgs {
   int R;             // row groups of 16
   int nb;            // 32-column blocks per row
   int S;             // k splits
-  int nbs;           // blocks per split (nb / S)
+  int nbs;           // blocks per split (nb / S): the tiles of one work item
   long long tiles;   // S * R * nbs
   int batch;
   int cols;
@@ -65,13 +65,21 @@ struct AttnArgs {
   float cap_log2;      // softcap*log2(e), 0 = no softcap
   int splits;          // S per (sequence, kv head)
   int chunk;           // keys per split
-  float* part;         // [B*nkv][S][G][hd + 2]
+  float* part;         // [B*nkv][S][8][hd + 4]: O[hd], m, l, pad
   int* ticket;         // [B*nkv]
   float* o;            // f32 [B, nh, hd]
   unsigned* err;
 };
 
 enum GemvMode { kModeQKV = 0, kModeOProj = 1 };
+
+// Optional per-launch event timing (the layer's hfa_set_kernel_timing); begin/end
+// bracket one kernel launch on `s`.
+struct LaunchTimer {
+  virtual void begin(cudaStream_t s, const char* name) = 0;
+  virtual void end(cudaStream_t s) = 0;
+  virtual ~LaunchTimer() {}
+};
 
 // message returned by hfa_last_error(NULL) on this thread
 void set_thread_error(const char* msg);
@@ -87,11 +95,13 @@ cudaError_t launch_gemv(int mode, const GemvArgs& a, int grid, int threads, size
                         bool pdl, cudaStream_t s);
 size_t gemv_smem_bytes(int batch, int blocks_per_cta_max);
 int gemv_ntiles(int batch);
+int gemv_items_per_cta();
 
 cudaError_t launch_attn(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                         int grid, bool pdl, cudaStream_t s);
 int attn_keys_per_stage(int hd);
 size_t attn_smem_bytes(int hd);
 int attn_threads(int hd);
+int attn_record_floats(int hd);  // floats of one chunk record (8 heads x (hd + 4))
 
 }  // namespace hfa

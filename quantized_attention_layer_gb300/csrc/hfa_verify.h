@@ -31,6 +31,7 @@ struct VerifyCall {
   float* out_tap; // nullable [L, H]
   unsigned* err;
   int num_sms;
+  LaunchTimer* timer;  // nullable; when set, launches are timed and not PDL-chained
 };
 
 hfa_status verify_create(const hfa_layer_desc& d, int num_sms, VerifyState** out);

@@ -21,21 +21,23 @@
 
 namespace hfa {
 
-constexpr int kNC = 4;         // consumer warps
 constexpr int kKeysPerWarp = 16;
 constexpr int kStages = 3;
 
+// One CTA per SM streams 3 stages of ~64 KB (K + V); consumer warps take 16 keys each.
 template <int HD>
 struct AttnCfg {
-  static constexpr int T = kNC * kKeysPerWarp;       // keys per stage
-  static constexpr int BOXES = HD / 64;              // 64-element (128 B) TMA boxes per row
-  static constexpr int TILE_BYTES = T * HD * 2;      // one of K or V
+  static constexpr int NC = HD >= 256 ? 4 : 8;       // consumer warps
+  static constexpr int T = NC * kKeysPerWarp;         // keys per stage
+  static constexpr int BOXES = HD / 64;               // 64-element (128 B) TMA boxes per row
+  static constexpr int TILE_BYTES = T * HD * 2;       // one of K or V
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-  static constexpr int KS = HD / 16;                 // k16 steps of S = Q K^T
-  static constexpr int NTO = HD / 8;                 // n8 tiles of O
+  static constexpr int KS = HD / 16;                  // k16 steps of S = Q K^T
+  static constexpr int NTO = HD / 8;                  // n8 tiles of O
   static constexpr int QF_BYTES = KS * 32 * 16;
+  static constexpr int RS = HD + 4;                   // record stride: O[HD], m, l, pad
   // the cross-warp merge reuses the stage buffers after the last stage
-  static constexpr int RED_BYTES = kNC * 8 * (HD + 2) * 4;
+  static constexpr int RED_BYTES = NC * 8 * RS * 4;
   static constexpr size_t SMEM = 1024 + (size_t)kStages * STAGE_BYTES + QF_BYTES + 256;
   static_assert(RED_BYTES <= kStages * STAGE_BYTES, "merge area must fit in the stages");
 };
@@ -50,11 +52,13 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 }
 
 template <int HD>
-__global__ void __launch_bounds__((kNC + 1) * 32)
+__global__ void __launch_bounds__(288)
     attn_decode_kernel(const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, const AttnArgs a) {
   using Cfg = AttnCfg<HD>;
   constexpr int T = Cfg::T;
+  constexpr int kNC = Cfg::NC;
+  constexpr int RS = Cfg::RS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
@@ -104,7 +108,7 @@ __global__ void __launch_bounds__((kNC + 1) * 32)
   const int ntiles = (nkeys + T - 1) / T;
   const int row0 = unit * a.C + k_begin;  // TMA row of the first key of this chunk
 
-  float* part = a.part + ((size_t)unit * a.splits + split) * 8 * (HD + 2);
+  float* part = a.part + ((size_t)unit * a.splits + split) * 8 * RS;
 
   if (warp == kNC) {
     // ------------------------------------------------------------- producer
@@ -240,17 +244,17 @@ __global__ void __launch_bounds__((kNC + 1) * 32)
     // ------------------------------------------------- merge the consumer warps
     // every stage has been consumed (or the CTA aborted): reuse the stage buffers
     asm volatile("bar.sync 1, %0;" ::"n"(kNC * 32));
-    float* red = reinterpret_cast<float*>(stages);  // [warp][8][HD + 2]
-    float* mine = red + warp * 8 * (HD + 2);
+    float* red = reinterpret_cast<float*>(stages);  // [warp][8][RS]
+    float* mine = red + warp * 8 * RS;
     if (g < G) {
       if (t == 0) {
-        mine[g * (HD + 2) + HD] = m;
-        mine[g * (HD + 2) + HD + 1] = l;
+        mine[g * RS + HD] = m;
+        mine[g * RS + HD + 1] = l;
       }
 #pragma unroll
       for (int nt = 0; nt < Cfg::NTO; ++nt) {
-        mine[g * (HD + 2) + nt * 8 + 2 * t] = o[nt][0] + o[nt][2];
-        mine[g * (HD + 2) + nt * 8 + 2 * t + 1] = o[nt][1] + o[nt][3];
+        mine[g * RS + nt * 8 + 2 * t] = o[nt][0] + o[nt][2];
+        mine[g * RS + nt * 8 + 2 * t + 1] = o[nt][1] + o[nt][3];
       }
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kNC * 32));
@@ -258,7 +262,7 @@ __global__ void __launch_bounds__((kNC + 1) * 32)
       const int h = e / (HD + 2), d = e - h * (HD + 2);
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kNC; ++w) M = fmaxf(M, red[(w * 8 + h) * (HD + 2) + HD]);
+      for (int w = 0; w < kNC; ++w) M = fmaxf(M, red[(w * 8 + h) * RS + HD]);
       const float Mu = M == -INFINITY ? 0.f : M;
       float acc = 0.f;
       if (d == HD) {
@@ -266,9 +270,9 @@ __global__ void __launch_bounds__((kNC + 1) * 32)
       } else {
 #pragma unroll
         for (int w = 0; w < kNC; ++w)
-          acc += exp2f(red[(w * 8 + h) * (HD + 2) + HD] - Mu) * red[(w * 8 + h) * (HD + 2) + d];
+          acc += exp2f(red[(w * 8 + h) * RS + HD] - Mu) * red[(w * 8 + h) * RS + d];
       }
-      part[h * (HD + 2) + d] = acc;
+      part[h * RS + d] = acc;
     }
   }
 
@@ -293,20 +297,20 @@ __global__ void __launch_bounds__((kNC + 1) * 32)
   if (!s_flags[2]) return;
   __threadfence();
   if (threadIdx.x == 0) a.ticket[unit] = 0;
-  const float* up = a.part + (size_t)unit * a.splits * 8 * (HD + 2);
+  const float* up = a.part + (size_t)unit * a.splits * 8 * RS;
   // weight of chunk s for head h: 2^(m_s - M) / sum_s' 2^(m_s' - M) l_s'
   float* wsm = reinterpret_cast<float*>(stages);  // [8][splits]
   const int nwarps = blockDim.x >> 5;
   for (int h = warp; h < G; h += nwarps) {
     float M = -INFINITY;
     for (int sp = lane; sp < a.splits; sp += 32)
-      M = fmaxf(M, ld_cg_f32(up + (sp * 8 + h) * (HD + 2) + HD));
+      M = fmaxf(M, ld_cg_f32(up + (sp * 8 + h) * RS + HD));
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     const float Mu = M == -INFINITY ? 0.f : M;
     float den = 0.f;
     for (int sp = lane; sp < a.splits; sp += 32) {
-      const float* ps = up + (sp * 8 + h) * (HD + 2);
+      const float* ps = up + (sp * 8 + h) * RS;
       const float f = exp2f(ld_cg_f32(ps + HD) - Mu);
       wsm[h * a.splits + sp] = f;
       den += f * ld_cg_f32(ps + HD + 1);
@@ -317,17 +321,55 @@ __global__ void __launch_bounds__((kNC + 1) * 32)
     for (int sp = lane; sp < a.splits; sp += 32) wsm[h * a.splits + sp] *= inv;
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < G * HD; e += blockDim.x) {
-    const int h = e / HD, d = e - h * HD;
-    float acc = 0.f;
-    for (int sp = 0; sp < a.splits; ++sp)
-      acc += wsm[h * a.splits + sp] * ld_cg_f32(up + (sp * 8 + h) * (HD + 2) + d);
-    a.o[((size_t)b * a.nh + kvh * G + h) * HD + d] = acc;
+  // o[h][d] = sum_s w[h][s] O_s[h][d]: warps stride over chunks, lanes over float4
+  // columns, every load of a warp independent; partial sums meet in shared memory
+  float* osum = wsm + 8 * a.splits;  // [nwarps][G * HD]
+  constexpr int Q4 = HD / 4;
+  const int ncol = G * Q4;
+  for (int c = lane; c < ncol; c += 32) {
+    const int h = c / Q4, d4 = c - h * Q4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int sp = warp;
+    for (; sp + nwarps < a.splits; sp += 2 * nwarps) {
+      const float4 v0 = __ldcg(reinterpret_cast<const float4*>(up + (sp * 8 + h) * RS) + d4);
+      const float4 v1 =
+          __ldcg(reinterpret_cast<const float4*>(up + ((sp + nwarps) * 8 + h) * RS) + d4);
+      const float w0 = wsm[h * a.splits + sp], w1 = wsm[h * a.splits + sp + nwarps];
+      acc.x += w0 * v0.x + w1 * v1.x;
+      acc.y += w0 * v0.y + w1 * v1.y;
+      acc.z += w0 * v0.z + w1 * v1.z;
+      acc.w += w0 * v0.w + w1 * v1.w;
+    }
+    if (sp < a.splits) {
+      const float4 v0 = __ldcg(reinterpret_cast<const float4*>(up + (sp * 8 + h) * RS) + d4);
+      const float w0 = wsm[h * a.splits + sp];
+      acc.x += w0 * v0.x;
+      acc.y += w0 * v0.y;
+      acc.z += w0 * v0.z;
+      acc.w += w0 * v0.w;
+    }
+    reinterpret_cast<float4*>(osum + warp * G * HD)[c] = acc;
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < ncol; c += blockDim.x) {
+    float4 acc = reinterpret_cast<const float4*>(osum)[c];
+    for (int w = 1; w < nwarps; ++w) {
+      const float4 v = reinterpret_cast<const float4*>(osum + w * G * HD)[c];
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    const int h = c / Q4, d4 = c - h * Q4;
+    reinterpret_cast<float4*>(a.o + ((size_t)b * a.nh + kvh * G + h) * HD)[d4] = acc;
   }
 }
 
-int attn_keys_per_stage(int) { return kNC * kKeysPerWarp; }
-int attn_threads(int) { return (kNC + 1) * 32; }
+int attn_keys_per_stage(int hd) {
+  return hd == 64 ? AttnCfg<64>::T : (hd == 128 ? AttnCfg<128>::T : AttnCfg<256>::T);
+}
+int attn_threads(int hd) { return (attn_keys_per_stage(hd) / kKeysPerWarp + 1) * 32; }
+int attn_record_floats(int hd) { return 8 * (hd + 4); }
 size_t attn_smem_bytes(int hd) {
   if (hd == 64) return AttnCfg<64>::SMEM;
   if (hd == 128) return AttnCfg<128>::SMEM;
@@ -344,7 +386,7 @@ static cudaError_t launch_hd(const AttnArgs& a, const CUtensorMap& tk, const CUt
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3((kNC + 1) * 32);
+  cfg.blockDim = dim3((AttnCfg<HD>::NC + 1) * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

@@ -26,7 +26,8 @@
 
 namespace hfa {
 
-constexpr int kUnroll = 8;  // tiles in flight per lane (16 B weights + 4 B scales each)
+constexpr int kChunk = 8;        // tiles in flight per lane (16 B weights + 4 B scales each)
+constexpr int kItemsPerCta = 8;  // warps per CTA, one work item each
 
 template <int NT, int MODE>
 __device__ __forceinline__ void flush_item(const GemvArgs& a, float (&acc)[NT][4], int r,
@@ -62,55 +63,113 @@ __device__ __forceinline__ void flush_item(const GemvArgs& a, float (&acc)[NT][4
   }
 }
 
+// One tile: convert the 16 biased bytes of this lane into the A registers of two k16
+// MMAs, multiply with every batch tile of the activation, scale by the block's d.
+template <int NT>
+__device__ __forceinline__ void tile_mma(float (&acc)[NT][4], const uint4 w, uint32_t dbits,
+                                         const uint4* xrow) {
+  uint32_t A0[4], A1[4];
+  A0[0] = u8x2_to_h2(w.x, kSelLo);
+  A0[1] = u8x2_to_h2(w.y, kSelLo);
+  A0[2] = u8x2_to_h2(w.x, kSelHi);
+  A0[3] = u8x2_to_h2(w.y, kSelHi);
+  A1[0] = u8x2_to_h2(w.z, kSelLo);
+  A1[1] = u8x2_to_h2(w.w, kSelLo);
+  A1[2] = u8x2_to_h2(w.z, kSelHi);
+  A1[3] = u8x2_to_h2(w.w, kSelHi);
+  const __half2 d2 = *reinterpret_cast<const __half2*>(&dbits);
+  const float dg = __low2float(d2), dg8 = __high2float(d2);
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const uint4 xb = xrow[nt * 32];
+    float tmp[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_f16(tmp, A0, xb.x, xb.y);
+    mma_f16(tmp, A1, xb.z, xb.w);
+    acc[nt][0] = fmaf(tmp[0], dg, acc[nt][0]);
+    acc[nt][1] = fmaf(tmp[1], dg, acc[nt][1]);
+    acc[nt][2] = fmaf(tmp[2], dg8, acc[nt][2]);
+    acc[nt][3] = fmaf(tmp[3], dg8, acc[nt][3]);
+  }
+}
+
+// Work item = (k-split s, row group r): the nbs consecutive tiles of 16 rows x (nbs x 32)
+// columns, one warp per item, CTAs of kItemsPerCta consecutive items (s-major).  The
+// first kChunk tiles are loaded before anything else; the kernel's prologue (input
+// norm statistics, activation operand of the CTA's k-range) hides their latency.
 template <int NT, int MODE>
-__global__ void __launch_bounds__(512) gemv_q8_kernel(const GemvArgs a) {
+__global__ void __launch_bounds__(kItemsPerCta * 32, NT >= 4 ? 2 : 3)
+    gemv_q8_kernel(const GemvArgs a) {
   extern __shared__ __align__(16) uint4 xf[];  // [blocks of this CTA][NT][32 lanes]
   __shared__ float s_inv[16];
-  const int nwarps = blockDim.x >> 5;
+  __shared__ float s_ss[16];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2;
-  const long long per_split = (long long)a.R * a.nbs;
-  const long long cta_begin = a.tiles * blockIdx.x / gridDim.x;
-  const long long cta_end = a.tiles * (blockIdx.x + 1) / gridDim.x;
-  if (cta_begin >= cta_end) {
-    pdl_wait();
-    return;
-  }
-  const int s_first = (int)(cta_begin / per_split);
-  const int s_last = (int)((cta_end - 1) / per_split);
+  const int items = a.S * a.R;
+  const int item0 = blockIdx.x * kItemsPerCta;
+  const int nitems = items - item0 < kItemsPerCta ? items - item0 : kItemsPerCta;
+  const int s_first = item0 / a.R, s_last = (item0 + nitems - 1) / a.R;
   const int blk0 = s_first * a.nbs;
   const int nblk = (s_last - s_first + 1) * a.nbs;
+  const bool active = warp < nitems;
+  const int item = active ? item0 + warp : item0;
+  const int s = item / a.R, r = item - s * a.R;
+  const uint8_t* wbase = a.wq + ((size_t)r * a.nb + (size_t)s * a.nbs) * 512 + lane * 16;
+  const __half2* dbase = a.wd + ((size_t)r * a.nb + (size_t)s * a.nbs) * 8 + g;
 
-  // The weights never depend on an earlier kernel: warm L2 with this CTA's first tiles
-  // while the previous kernel finishes, then wait for it.
-  {
-    const long long first = cta_begin + threadIdx.x;
-    if (first < cta_end && threadIdx.x < 64) {
-      const long long item = first / a.nbs;
-      const int j = (int)(first - item * a.nbs);
-      const int s = (int)(item / a.R), r = (int)(item - (long long)s * a.R);
-      prefetch_l2(a.wq + ((size_t)r * a.nb + s * a.nbs + j) * 512);
+  // weights never depend on an earlier kernel: start their first chunk now
+  uint4 wv[kChunk];
+  uint32_t dv[kChunk];
+  if (active) {
+#pragma unroll
+    for (int u = 0; u < kChunk; ++u)
+      if (u < a.nbs) {
+        wv[u] = ldg_stream_v4(wbase + (size_t)u * 512);
+        dv[u] = ldg_stream_u32(dbase + (size_t)u * 8);
+      }
+    if (lane == 0 && a.nbs > kChunk) {
+      prefetch_bulk_l2(wbase + (size_t)kChunk * 512, (uint32_t)(a.nbs - kChunk) * 512u);
     }
   }
   pdl_wait();
 
   if (MODE == kModeQKV) {
-    // input RMSNorm statistics of every batch row (full rows, fp32)
-    for (int b = warp; b < a.batch; b += nwarps) {
-      float ss = 0.f;
-      const __nv_bfloat16* xr = a.x + (size_t)b * a.cols;
-      for (int k = lane * 8; k < a.cols; k += 256) {
-        uint4 raw = *reinterpret_cast<const uint4*>(xr + k);
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+    // input RMSNorm statistics of every batch row (full rows, fp32): all threads share
+    // the 8-column groups of all rows, partial sums meet in shared memory
+    if (threadIdx.x < 16) s_ss[threadIdx.x] = 0.f;
+    __syncthreads();
+    const int gpr = a.cols / 8;  // groups per row
+    const int ngroups = a.batch * gpr;
+    for (int e0 = threadIdx.x; e0 < ngroups; e0 += 4 * blockDim.x) {
+      uint4 raw[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float2 f = __bfloat1622float2(h[e]);
-          ss += f.x * f.x + f.y * f.y;
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + u * blockDim.x;
+        if (e < ngroups)
+          raw[u] = *reinterpret_cast<const uint4*>(a.x + (size_t)(e / gpr) * a.cols + (e % gpr) * 8);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + u * blockDim.x;
+        if (e < ngroups) {
+          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[u]);
+          float ss = 0.f;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(h[i]);
+            ss += f.x * f.x + f.y * f.y;
+          }
+          if (gpr % 32 == 0) {
+            // a warp's 32 consecutive groups lie in one row: one shared atomic per warp
+            ss = warp_sum(ss);
+            if ((threadIdx.x & 31) == 0) atomicAdd(&s_ss[e / gpr], ss);
+          } else {
+            atomicAdd(&s_ss[e / gpr], ss);
+          }
         }
       }
-      ss = warp_sum(ss);
-      if (lane == 0) s_inv[b] = rsqrtf(ss / a.cols + a.eps);
     }
+    __syncthreads();
+    if (threadIdx.x < a.batch) s_inv[threadIdx.x] = rsqrtf(s_ss[threadIdx.x] / a.cols + a.eps);
     __syncthreads();
   }
 
@@ -130,13 +189,13 @@ __global__ void __launch_bounds__(512) gemv_q8_kernel(const GemvArgs a) {
           const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.w_in + k));
           const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.w_in + k + 4));
           const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
-          const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+          const float wv8[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
           const float inv = s_inv[b];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const float2 f = __bfloat1622float2(h[i]);
-            v[2 * i] = f.x * inv * wv[2 * i];
-            v[2 * i + 1] = f.y * inv * wv[2 * i + 1];
+            v[2 * i] = f.x * inv * wv8[2 * i];
+            v[2 * i + 1] = f.y * inv * wv8[2 * i + 1];
           }
         } else {
           const float4 f0 = *reinterpret_cast<const float4*>(a.xin + (size_t)b * a.cols + k);
@@ -165,72 +224,48 @@ __global__ void __launch_bounds__(512) gemv_q8_kernel(const GemvArgs a) {
   }
   __syncthreads();
   pdl_launch_dependents();
+  if (!active) return;
 
-  const long long n = cta_end - cta_begin;
-  const long long w_begin = cta_begin + n * warp / nwarps;
-  const long long w_end = cta_begin + n * (warp + 1) / nwarps;
   float acc[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+  const uint4* xrow = xf + (size_t)((s * a.nbs - blk0) * NT) * 32 + lane;
 
-  long long tt0 = w_begin;
-  while (tt0 < w_end) {
-    // one item = the tiles of (s, r) inside this warp's range
-    const long long item = tt0 / a.nbs;
-    const long long item_end = (item + 1) * a.nbs < w_end ? (item + 1) * a.nbs : w_end;
-    const int s = (int)(item / a.R), r = (int)(item - (long long)s * a.R);
-    const int j_first = (int)(tt0 - item * a.nbs);
-    const int nt_item = (int)(item_end - tt0);
-    const uint8_t* wbase = a.wq + ((size_t)r * a.nb + s * a.nbs) * 512 + lane * 16;
-    const __half2* dbase = a.wd + ((size_t)r * a.nb + s * a.nbs) * 8 + g;
-    for (int c = 0; c < nt_item; c += kUnroll) {
-      uint4 wv[kUnroll];
-      uint32_t dv[kUnroll];
+  if (a.nbs % kChunk == 0) {
+    for (int c = 0; c < a.nbs; c += kChunk) {
+      if (c > 0) {
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        if (c + u < nt_item) {
-          const int j = j_first + c + u;
-          wv[u] = ldg_stream_v4(wbase + (size_t)j * 512);
-          dv[u] = ldg_stream_u32(dbase + (size_t)j * 8);
+        for (int u = 0; u < kChunk; ++u) {
+          wv[u] = ldg_stream_v4(wbase + (size_t)(c + u) * 512);
+          dv[u] = ldg_stream_u32(dbase + (size_t)(c + u) * 8);
         }
       }
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        if (c + u < nt_item) {
-          const int jb = s * a.nbs + j_first + c + u - blk0;
-          uint32_t A0[4], A1[4];
-          A0[0] = u8x2_to_h2(wv[u].x, kSelLo);
-          A0[1] = u8x2_to_h2(wv[u].y, kSelLo);
-          A0[2] = u8x2_to_h2(wv[u].x, kSelHi);
-          A0[3] = u8x2_to_h2(wv[u].y, kSelHi);
-          A1[0] = u8x2_to_h2(wv[u].z, kSelLo);
-          A1[1] = u8x2_to_h2(wv[u].w, kSelLo);
-          A1[2] = u8x2_to_h2(wv[u].z, kSelHi);
-          A1[3] = u8x2_to_h2(wv[u].w, kSelHi);
-          const __half2 d2 = *reinterpret_cast<const __half2*>(&dv[u]);
-          const float dg = __low2float(d2), dg8 = __high2float(d2);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const uint4 xb = xf[(jb * NT + nt) * 32 + lane];
-            float tmp[4] = {0.f, 0.f, 0.f, 0.f};
-            mma_f16(tmp, A0, xb.x, xb.y);
-            mma_f16(tmp, A1, xb.z, xb.w);
-            acc[nt][0] = fmaf(tmp[0], dg, acc[nt][0]);
-            acc[nt][1] = fmaf(tmp[1], dg, acc[nt][1]);
-            acc[nt][2] = fmaf(tmp[2], dg8, acc[nt][2]);
-            acc[nt][3] = fmaf(tmp[3], dg8, acc[nt][3]);
-          }
-        }
-      }
+      for (int u = 0; u < kChunk; ++u) tile_mma<NT>(acc, wv[u], dv[u], xrow + (c + u) * NT * 32);
     }
-    flush_item<NT, MODE>(a, acc, r, nt_item, lane);
-    tt0 = item_end;
+  } else {
+    for (int c = 0; c < a.nbs; c += kChunk) {
+      if (c > 0) {
+#pragma unroll
+        for (int u = 0; u < kChunk; ++u)
+          if (c + u < a.nbs) {
+            wv[u] = ldg_stream_v4(wbase + (size_t)(c + u) * 512);
+            dv[u] = ldg_stream_u32(dbase + (size_t)(c + u) * 8);
+          }
+      }
+#pragma unroll
+      for (int u = 0; u < kChunk; ++u)
+        if (c + u < a.nbs) tile_mma<NT>(acc, wv[u], dv[u], xrow + (c + u) * NT * 32);
+    }
   }
+  flush_item<NT, MODE>(a, acc, r, a.nbs, lane);
 }
 
 int gemv_ntiles(int batch) { return batch <= 4 ? 1 : (batch <= 8 ? 2 : 4); }
+
+int gemv_items_per_cta() { return kItemsPerCta; }
 
 size_t gemv_smem_bytes(int batch, int blocks_per_cta_max) {
   return (size_t)blocks_per_cta_max * gemv_ntiles(batch) * 32 * sizeof(uint4);

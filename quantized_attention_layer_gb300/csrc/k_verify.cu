@@ -607,6 +607,9 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   }
   cudaStream_t s = c.stream;
   cudaError_t e;
+  const bool pdl = c.timer == nullptr;
+  auto tb = [&](const char* nm) { if (c.timer) c.timer->begin(s, nm); };
+  auto te = [&]() { if (c.timer) c.timer->end(s); };
 
   // (1) input norm + QKV projection + per-head norms + RoPE + append of all L rows
   VGemmArgs qa{};
@@ -640,8 +643,10 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   const int qtiles = rows_qkv / kVM;
   qa.splits = gemm_splits(qtiles, qa.chunks, c.num_sms);
   qa.need = qa.chunks * (hd > kVM ? hd / kVM : 1);
-  e = launch_ex(verify_gemm_kernel<kModeQKV>, qtiles * qa.splits, 128, kVGemmSmem, true, s,
+  tb("verify_qkv_gemm");
+  e = launch_ex(verify_gemm_kernel<kModeQKV>, qtiles * qa.splits, 128, kVGemmSmem, pdl, s,
                 v->tm_wqkv, qa);
+  te();
   if (e != cudaSuccess) {
     snprintf(msg, n, "verify QKV launch: %s", cudaGetErrorString(e));
     return HFA_ECUDA;
@@ -685,14 +690,16 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   aa.err = c.err;
   const int nq_warps = (c.L * G + 7) / 8;
   const int athreads = (nq_warps + 1) * 32;
+  tb("verify_attention");
   if (hd == 64)
-    e = launch_ex(attn_verify_kernel<64>, nkv * S, athreads, VACfg<64>::SMEM, true, s, tk, tv, aa);
+    e = launch_ex(attn_verify_kernel<64>, nkv * S, athreads, VACfg<64>::SMEM, pdl, s, tk, tv, aa);
   else if (hd == 128)
-    e = launch_ex(attn_verify_kernel<128>, nkv * S, athreads, VACfg<128>::SMEM, true, s, tk, tv,
+    e = launch_ex(attn_verify_kernel<128>, nkv * S, athreads, VACfg<128>::SMEM, pdl, s, tk, tv,
                   aa);
   else
-    e = launch_ex(attn_verify_kernel<256>, nkv * S, athreads, VACfg<256>::SMEM, true, s, tk, tv,
+    e = launch_ex(attn_verify_kernel<256>, nkv * S, athreads, VACfg<256>::SMEM, pdl, s, tk, tv,
                   aa);
+  te();
   if (e != cudaSuccess) {
     snprintf(msg, n, "verify attention launch: %s", cudaGetErrorString(e));
     return HFA_ECUDA;
@@ -715,8 +722,10 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   const int otiles = H / kVM;
   oa.splits = gemm_splits(otiles, oa.chunks, c.num_sms);
   oa.need = oa.chunks;
-  e = launch_ex(verify_gemm_kernel<kModeOProj>, otiles * oa.splits, 128, kVGemmSmem, true, s,
+  tb("verify_oproj_gemm");
+  e = launch_ex(verify_gemm_kernel<kModeOProj>, otiles * oa.splits, 128, kVGemmSmem, pdl, s,
                 v->tm_wo, oa);
+  te();
   if (e != cudaSuccess) {
     snprintf(msg, n, "verify o_proj launch: %s", cudaGetErrorString(e));
     return HFA_ECUDA;
