@@ -839,7 +839,7 @@ extern "C" int hfa_kernel_times(hfa_layer* L, int n, const char** names, float* 
   }
   L->pending.clear();
   static const char* kNames[] = {"qkv_norm_rope_append", "flash_decode", "oproj_residual",
-                                 "verify_qkv_gemm", "verify_norm_rope_append", "verify_attention",
+                                 "verify_prep", "verify_qkv_gemm", "verify_norm_rope_append", "verify_attention",
                                  "verify_oproj_gemm", "verify_residual"};
   int k = 0;
   for (size_t i = 0; i < L->slot_names.size() && k < n; ++i, ++k) {

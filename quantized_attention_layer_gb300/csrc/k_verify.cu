@@ -29,6 +29,26 @@ hfa_status hfa_encode_kv_map(CUtensorMap* map, void* base, int rows, int hd, int
 namespace hfa {
 
 // ------------------------------------------------------------------ GEMM (tcgen05)
+// Writes columns [8e, 8e + 8) of activation row t into the operand: bf16 hi in row t,
+// bf16 lo in row 16 + t of chunk e / 8, 16-byte group (e % 8) XOR (row % 8).
+__device__ __forceinline__ void store_bop_group(uint8_t* bops, int t, int e, const float (&v)[8]) {
+  uint32_t hw[4], lw[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat16 h0, l0, h1, l1;
+    split_bf16(v[2 * i], h0, l0);
+    split_bf16(v[2 * i + 1], h1, l1);
+    hw[i] = pack_bf2(h0, h1);
+    lw[i] = pack_bf2(l0, l1);
+  }
+  uint8_t* chunk = bops + (size_t)(e >> 3) * (32 * 128);
+  const int c16 = e & 7, rh = t, rl = 16 + t;
+  *reinterpret_cast<uint4*>(chunk + rh * 128 + ((c16 ^ (rh & 7)) << 4)) =
+      make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  *reinterpret_cast<uint4*>(chunk + rl * 128 + ((c16 ^ (rl & 7)) << 4)) =
+      make_uint4(lw[0], lw[1], lw[2], lw[3]);
+}
+
 constexpr int kVM = 128;         // weight rows per CTA = MMA M
 constexpr int kVN = 32;          // MMA N: 16 tokens x (hi, lo)
 constexpr int kVK = 64;          // K elements per stage (one 128-byte swizzled row)
@@ -41,12 +61,68 @@ constexpr size_t kVGemmSmem =
 
 struct VGemmArgs {
   GemvArgs g;        // epilogue arguments (accumulator, tickets, norms, caches, ...)
+  const uint8_t* bops;  // activation operand, [K / 64 chunks][32 rows][128 B], swizzled
   int rows;          // output features
   int K;             // input features
   int chunks;        // K / 64
   int splits;        // k-splits per row tile
   int need;          // chunk contributions that complete a head (QKV) / row tile (o_proj)
 };
+
+// Activation operand of the verify GEMMs, built once per call: row t of the block
+// (t < L; zero rows otherwise), normalised by its input RMSNorm (QKV mode), split into
+// bf16 hi (operand row t) and lo (row 16 + t), written chunk by chunk (64 columns,
+// 32 rows of 128 B) in the 128-byte swizzled order the tensor cores read.
+// One CTA per operand row pair t.
+__global__ void __launch_bounds__(256) verify_prep_kernel(const __nv_bfloat16* __restrict__ x,
+                                                         const float* __restrict__ w_in,
+                                                         float eps, int L, int K,
+                                                         uint8_t* __restrict__ bops) {
+  __shared__ float s_red[8];
+  const int t = blockIdx.x;
+  const int ngroups = K / 8;
+  pdl_wait();
+  float inv = 0.f;
+  if (t < L) {
+    float ss = 0.f;
+    for (int e = threadIdx.x; e < ngroups; e += blockDim.x) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(x + (size_t)t * K + e * 8);
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        ss += f.x * f.x + f.y * f.y;
+      }
+    }
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += s_red[w];
+    inv = rsqrtf(tot / K + eps);
+  }
+  for (int e = threadIdx.x; e < ngroups; e += blockDim.x) {
+    float v[8];
+    if (t < L) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(x + (size_t)t * K + e * 8);
+      const float4 w0 = __ldg(reinterpret_cast<const float4*>(w_in + e * 8));
+      const float4 w1 = __ldg(reinterpret_cast<const float4*>(w_in + e * 8 + 4));
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+      const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        v[2 * i] = f.x * inv * wv[2 * i];
+        v[2 * i + 1] = f.y * inv * wv[2 * i + 1];
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = 0.f;
+    }
+    store_bop_group(bops, t, e, v);
+  }
+  pdl_launch_dependents();
+}
 
 template <int MODE>
 __global__ void __launch_bounds__(128) verify_gemm_kernel(const __grid_constant__ CUtensorMap tw,
@@ -59,10 +135,9 @@ __global__ void __launch_bounds__(128) verify_gemm_kernel(const __grid_constant_
   uint64_t* full = reinterpret_cast<uint64_t*>(sb + kVMaxChunks * kBChunkBytes);
   uint64_t* empty = full + kVStages;
   uint64_t* done = empty + kVStages;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* bready = done + 1;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bready + 1);
   int* s_fin = reinterpret_cast<int*>(s_tmem + 1);      // [0..3] finished heads / tile flag
-  __shared__ float s_inv[16];
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = blockIdx.x / a.splits, sp = blockIdx.x - mt * a.splits;
   const int c0 = a.chunks * sp / a.splits, c1 = a.chunks * (sp + 1) / a.splits;
@@ -76,6 +151,7 @@ __global__ void __launch_bounds__(128) verify_gemm_kernel(const __grid_constant_
       mbar_init(&empty[i], 1);
     }
     mbar_init(done, 1);
+    mbar_init(bready, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -87,77 +163,27 @@ __global__ void __launch_bounds__(128) verify_gemm_kernel(const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
-  pdl_wait();
 
-  // ---- B operand: activations of chunks [c0, c1), rows 0..15 bf16 hi, 16..31 bf16 lo
-  if (MODE == kModeQKV) {
-    for (int t = warp; t < L; t += 4) {
-      float ss = 0.f;
-      const __nv_bfloat16* xr = a.g.x + (size_t)t * a.K;
-      for (int k = lane * 8; k < a.K; k += 256) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(xr + k);
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __bfloat1622float2(h[e]);
-          ss += f.x * f.x + f.y * f.y;
-        }
-      }
-      ss = warp_sum(ss);
-      if (lane == 0) s_inv[t] = rsqrtf(ss / a.K + a.g.eps);
+  // the weights never depend on an earlier kernel: fill the ring right away
+  const int npre = nch < kVStages ? nch : kVStages;
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < npre; ++i) {
+      mbar_arrive_expect_tx(&full[i], kAStageBytes);
+      tma_load_2d(sa + i * kAStageBytes, &tw, &full[i], (c0 + i) * kVK, m0);
     }
-    __syncthreads();
   }
-  for (int e = threadIdx.x; e < nch * 16 * 8; e += blockDim.x) {
-    const int c = e >> 7, t = (e >> 3) & 15, c16 = e & 7;
-    const int k = (c0 + c) * kVK + c16 * 8;
-    float v[8];
-    if (t < L) {
-      if (MODE == kModeQKV) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(a.g.x + (size_t)t * a.K + k);
-        const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.g.w_in + k));
-        const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.g.w_in + k + 4));
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
-        const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = __bfloat1622float2(h[i]);
-          v[2 * i] = f.x * s_inv[t] * wv[2 * i];
-          v[2 * i + 1] = f.y * s_inv[t] * wv[2 * i + 1];
-        }
-      } else {
-        const float4 f0 = *reinterpret_cast<const float4*>(a.g.xin + (size_t)t * a.K + k);
-        const float4 f1 = *reinterpret_cast<const float4*>(a.g.xin + (size_t)t * a.K + k + 4);
-        v[0] = f0.x; v[1] = f0.y; v[2] = f0.z; v[3] = f0.w;
-        v[4] = f1.x; v[5] = f1.y; v[6] = f1.z; v[7] = f1.w;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = 0.f;
-    }
-    uint32_t hw[4], lw[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      __nv_bfloat16 h0, l0, h1, l1;
-      split_bf16(v[2 * i], h0, l0);
-      split_bf16(v[2 * i + 1], h1, l1);
-      hw[i] = pack_bf2(h0, h1);
-      lw[i] = pack_bf2(l0, l1);
-    }
-    uint8_t* chunk = sb + c * kBChunkBytes;
-    const int rh = t, rl = 16 + t;
-    *reinterpret_cast<uint4*>(chunk + rh * 128 + ((c16 ^ (rh & 7)) << 4)) =
-        make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    *reinterpret_cast<uint4*>(chunk + rl * 128 + ((c16 ^ (rl & 7)) << 4)) =
-        make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  pdl_wait();
+  // B operand: the chunks [c0, c1) of the activation operand that verify_prep_kernel
+  // (or the block attention's merge) laid out in shared-memory order, one bulk copy
+  if (warp == 1 && lane == 0) {
+    mbar_arrive_expect_tx(bready, (uint32_t)nch * kBChunkBytes);
+    bulk_load(sb, a.bops + (size_t)c0 * kBChunkBytes, (uint32_t)nch * kBChunkBytes, bready);
   }
-  fence_proxy_async_smem();  // generic-proxy writes above are read by the tensor cores
-  __syncthreads();
   pdl_launch_dependents();
 
   if (warp == 0 && lane == 0) {
     // ---- TMA producer
-    for (int i = 0; i < nch; ++i) {
+    for (int i = npre; i < nch; ++i) {
       const int st = i % kVStages;
       if (i >= kVStages && !mbar_wait(&empty[st], ((i / kVStages) - 1) & 1, a.g.err)) break;
       mbar_arrive_expect_tx(&full[st], kAStageBytes);
@@ -166,7 +192,8 @@ __global__ void __launch_bounds__(128) verify_gemm_kernel(const __grid_constant_
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer
     constexpr uint32_t idesc = idesc_bf16_f32(kVM, kVN);
-    for (int i = 0; i < nch; ++i) {
+    const bool bok = mbar_wait(bready, 0, a.g.err);
+    for (int i = 0; bok && i < nch; ++i) {
       const int st = i % kVStages;
       if (!mbar_wait(&full[st], (i / kVStages) & 1, a.g.err)) break;
       tc_fence_after();
@@ -234,7 +261,8 @@ struct VAttnArgs {
   int L, nh, nkv, G, C, base, sliding, window;
   float qscale, cap_log2;
   int splits, chunk, klo, khi;  // keys [klo, khi] are read by some row
-  float* part;                  // [nkv][splits][64 rows][hd + 2]
+  float* part;                  // [nkv][splits][64 rows][hd + 4]: O[hd], m, l, pad
+  uint8_t* bops;                // o_proj activation operand (see store_bop_group)
   int* ticket;                  // [nkv]
   float* o;                     // [L, nh, hd]
   unsigned* err;
@@ -295,7 +323,8 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
   const int nkeys = k_end > k_begin ? k_end - k_begin : 0;
   const int ntiles = (nkeys + kVT - 1) / kVT;
   const int row0 = kvh * a.C + k_begin;
-  float* part = a.part + ((size_t)kvh * a.splits + split) * 64 * (HD + 2);
+  constexpr int RS = HD + 4;
+  float* part = a.part + ((size_t)kvh * a.splits + split) * 64 * RS;
 
   if (warp == nc) {
     if (lane == 0) {
@@ -426,7 +455,7 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
     l += __shfl_xor_sync(0xffffffffu, l, 1);
     l += __shfl_xor_sync(0xffffffffu, l, 2);
     if (qvalid) {
-      float* pr = part + (size_t)qrow * (HD + 2);
+      float* pr = part + (size_t)qrow * RS;
       if (t == 0) {
         pr[HD] = m;
         pr[HD + 1] = l;
@@ -454,19 +483,19 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
   if (!s_flags[2]) return;
   __threadfence();
   if (threadIdx.x == 0) a.ticket[kvh] = 0;
-  const float* up = a.part + (size_t)kvh * a.splits * 64 * (HD + 2);
+  const float* up = a.part + (size_t)kvh * a.splits * 64 * RS;
   float* wsm = reinterpret_cast<float*>(stages);  // [64 rows][splits]
   const int nwarps = blockDim.x >> 5;
   for (int r = warp; r < NQ; r += nwarps) {
     float M = -INFINITY;
     for (int sp = lane; sp < a.splits; sp += 32)
-      M = fmaxf(M, ld_cg_f32(up + ((size_t)sp * 64 + r) * (HD + 2) + HD));
+      M = fmaxf(M, ld_cg_f32(up + ((size_t)sp * 64 + r) * RS + HD));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     const float Mu = M == -INFINITY ? 0.f : M;
     float den = 0.f;
     for (int sp = lane; sp < a.splits; sp += 32) {
-      const float* ps = up + ((size_t)sp * 64 + r) * (HD + 2);
+      const float* ps = up + ((size_t)sp * 64 + r) * RS;
       const float f = exp2f(ld_cg_f32(ps + HD) - Mu);
       wsm[r * a.splits + sp] = f;
       den += f * ld_cg_f32(ps + HD + 1);
@@ -477,13 +506,44 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
     for (int sp = lane; sp < a.splits; sp += 32) wsm[r * a.splits + sp] *= inv;
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < NQ * HD; e += blockDim.x) {
-    const int r = e / HD, d = e - r * HD;
-    float acc = 0.f;
-    for (int sp = 0; sp < a.splits; ++sp)
-      acc += wsm[r * a.splits + sp] * ld_cg_f32(up + ((size_t)sp * 64 + r) * (HD + 2) + d);
+  // one item = 8 consecutive output columns of one query row; chunks summed with
+  // independent 16-byte loads, four chunks at a time
+  constexpr int G8 = HD / 8;
+  for (int it = threadIdx.x; it < NQ * G8; it += blockDim.x) {
+    const int r = it / G8, d8 = it - r * G8;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    int sp = 0;
+    for (; sp + 4 <= a.splits; sp += 4) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float4* src =
+            reinterpret_cast<const float4*>(up + ((size_t)(sp + u) * 64 + r) * RS) + 2 * d8;
+        v[2 * u] = __ldcg(src);
+        v[2 * u + 1] = __ldcg(src + 1);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float w = wsm[r * a.splits + sp + u];
+        acc[0] += w * v[2 * u].x; acc[1] += w * v[2 * u].y;
+        acc[2] += w * v[2 * u].z; acc[3] += w * v[2 * u].w;
+        acc[4] += w * v[2 * u + 1].x; acc[5] += w * v[2 * u + 1].y;
+        acc[6] += w * v[2 * u + 1].z; acc[7] += w * v[2 * u + 1].w;
+      }
+    }
+    for (; sp < a.splits; ++sp) {
+      const float4* src = reinterpret_cast<const float4*>(up + ((size_t)sp * 64 + r) * RS) + 2 * d8;
+      const float4 v0 = __ldcg(src), v1 = __ldcg(src + 1);
+      const float w = wsm[r * a.splits + sp];
+      acc[0] += w * v0.x; acc[1] += w * v0.y; acc[2] += w * v0.z; acc[3] += w * v0.w;
+      acc[4] += w * v1.x; acc[5] += w * v1.y; acc[6] += w * v1.z; acc[7] += w * v1.w;
+    }
     const int tok = r / a.G, h = kvh * a.G + r % a.G;
-    a.o[((size_t)tok * a.nh + h) * HD + d] = acc;
+    float4* dst = reinterpret_cast<float4*>(a.o + ((size_t)tok * a.nh + h) * HD) + 2 * d8;
+    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    // the same values as the o_proj GEMM's activation operand (column h * HD + 8 d8)
+    store_bop_group(a.bops, tok, (h * HD) / 8 + d8, acc);
   }
 }
 
@@ -497,6 +557,8 @@ struct VerifyState {
   float* part = nullptr;        // [max(SMs, nkv)][64][hd + 2]
   float* qkv_acc = nullptr;     // [16][rows_qkv]
   float* y_acc = nullptr;       // [16][H]
+  uint8_t* bq = nullptr;        // QKV activation operand [H / 64][32][128 B]
+  uint8_t* bo = nullptr;        // o_proj activation operand [nh hd / 64][32][128 B]
   size_t part_records = 0;
 };
 
@@ -522,7 +584,12 @@ hfa_status verify_create(const hfa_layer_desc& d, int num_sms, VerifyState** out
   if (e == cudaSuccess) e = cudaMalloc(&v->tile_ticket, (d.hidden / kVM) * sizeof(int));
   if (e == cudaSuccess) e = cudaMalloc(&v->attn_ticket, nkv * sizeof(int));
   if (e == cudaSuccess)
-    e = cudaMalloc(&v->part, v->part_records * 64 * (d.head_dim + 2) * sizeof(float));
+    e = cudaMalloc(&v->part, v->part_records * 64 * (d.head_dim + 4) * sizeof(float));
+  if (e == cudaSuccess) e = cudaMalloc(&v->bq, (size_t)(d.hidden / kVK) * kBChunkBytes);
+  if (e == cudaSuccess)
+    e = cudaMalloc(&v->bo, (size_t)(d.num_heads * d.head_dim / kVK) * kBChunkBytes);
+  if (e == cudaSuccess)
+    e = cudaMemset(v->bo, 0, (size_t)(d.num_heads * d.head_dim / kVK) * kBChunkBytes);
   if (e == cudaSuccess) e = cudaMalloc(&v->qkv_acc, (size_t)16 * rows_qkv * sizeof(float));
   if (e == cudaSuccess) e = cudaMalloc(&v->y_acc, (size_t)16 * d.hidden * sizeof(float));
   if (e == cudaSuccess) e = cudaMemset(v->head_ticket, 0, (d.num_heads + 2 * nkv) * sizeof(int));
@@ -547,6 +614,8 @@ void verify_free(VerifyState* v) {
   cudaFree(v->part);
   cudaFree(v->qkv_acc);
   cudaFree(v->y_acc);
+  cudaFree(v->bq);
+  cudaFree(v->bo);
   delete v;
 }
 
@@ -611,8 +680,18 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   auto tb = [&](const char* nm) { if (c.timer) c.timer->begin(s, nm); };
   auto te = [&]() { if (c.timer) c.timer->end(s); };
 
-  // (1) input norm + QKV projection + per-head norms + RoPE + append of all L rows
+  // (0) activation operand of the QKV projection: input RMSNorm, bf16 hi/lo split
+  tb("verify_prep");
+  e = launch_ex(verify_prep_kernel, 16, 256, 0, pdl, s, c.x, c.w_in, d.eps, c.L, H, v->bq);
+  te();
+  if (e != cudaSuccess) {
+    snprintf(msg, n, "verify prep launch: %s", cudaGetErrorString(e));
+    return HFA_ECUDA;
+  }
+
+  // (1) QKV projection + per-head norms + RoPE + append of all L rows
   VGemmArgs qa{};
+  qa.bops = v->bq;
   qa.g.batch = c.L;
   qa.g.x = c.x;
   qa.g.w_in = c.w_in;
@@ -685,6 +764,7 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   aa.splits = S;
   aa.chunk = chunk;
   aa.part = v->part;
+  aa.bops = v->bo;
   aa.ticket = v->attn_ticket;
   aa.o = c.o_f32;
   aa.err = c.err;
@@ -707,6 +787,7 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
 
   // (3) o_proj + residual
   VGemmArgs oa{};
+  oa.bops = v->bo;
   oa.g.batch = c.L;
   oa.g.x = c.x;
   oa.g.xin = c.o_f32;
