@@ -110,6 +110,9 @@ hfa_status hfa_layer_create(const hfa_layer_desc* desc, const void* wq_dev, cons
  * Linear caches need 0 <= seq_pos < C (HFA_ERANGE otherwise).  Requires Q8_0 weights.
  * The cache must hold the earlier positions of each sequence: positions
  * max(0, P-W+1) .. P-1 (sliding) or 0 .. P-1 (full).
+ * The step is one cooperative launch of one CTA per SM; it fails with HFA_ECUDA when the
+ * device cannot hold that grid at once (e.g. SMs taken by another context).  Steps on
+ * one layer handle must not overlap on the GPU (they share the layer's scratch).
  */
 hfa_status hfa_decode_step(hfa_layer* layer, void* stream, const void* x_dev,
                            const int32_t* seq_pos_dev, const int32_t* seq_pos_host, int batch,
@@ -208,7 +211,8 @@ hfa_status hfa_debug_taps(hfa_layer* layer, void* stream, float* q_dev, float* k
 /*
  * Device-side status of earlier steps: bounded waits that gave up, or positions the
  * kernels refused.  Synchronises `stream`; returns HFA_OK, or HFA_EDEVICE with the
- * reason in hfa_last_error, and clears the record.
+ * reason in hfa_last_error, and clears the record (and, after a give-up, resets the
+ * step kernel's grid barrier so that later steps start clean).
  */
 hfa_status hfa_check_device_status(hfa_layer* layer, void* stream);
 
@@ -223,8 +227,8 @@ int hfa_kernel_times(hfa_layer* layer, int n, const char** names, float* total_m
                      int* launches);
 
 /* Launch plan details (for logs and the benchmark): fills up to n ints:
- * [0] attention splits per (sequence, kv head) of the last step, [1] keys per
- * attention stage, [2] GEMV grid, [3] attention grid, [4] SM count. */
+ * [0] key tiles of the last step (all sequences and kv heads), [1] keys per tile,
+ * [2] step grid, [3] step grid, [4] SM count. */
 int hfa_plan_info(const hfa_layer* layer, int n, int* values);
 
 #ifdef __cplusplus

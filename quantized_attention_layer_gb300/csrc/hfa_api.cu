@@ -2,8 +2,9 @@
 //
 // Host side only: argument validation (before any launch), ownership of the repacked
 // weights and of the per-layer scratch, launch plans, and the kernel launches of one
-// decode step: (1) input RMSNorm + QKV GEMV + per-head norm + RoPE + KV append,
-// (2) split-K flash-decode with the chunk merge, (3) o_proj GEMV + residual.
+// decode step: one persistent kernel (k_step.cuh) that runs the QKV projection, the
+// per-head norms, RoPE and KV append, the split-K flash-decode and the o_proj GEMV with
+// the residual.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -48,8 +49,10 @@ struct hfa_layer {
   int G = 0;
   int rows_qkv = 0;
   int max_rows = 0;
-  // weights
-  Q8Tiles wqkv, wo;
+  // weights: Q8_0 tiles in the decode-step layout
+  uint8_t* wqkv_t = nullptr;
+  uint8_t* wo_t = nullptr;
+  StepGemv g_qkv{}, g_o{};
   __nv_bfloat16* wqkv_bf16 = nullptr;  // verify path: [(nh + 2 nkv) hd, H]
   __nv_bfloat16* wo_bf16 = nullptr;    // [H, nh hd]
   float* w_in = nullptr;
@@ -57,14 +60,16 @@ struct hfa_layer {
   float* w_k = nullptr;
   float2* rope_g = nullptr;
   // scratch
-  float* qkv_acc = nullptr;
-  int* head_ticket = nullptr;
+  float* qkv_part = nullptr;
+  float* ss_part = nullptr;
   float* q_f32 = nullptr;
-  float* attn_part = nullptr;
-  int* attn_ticket = nullptr;
+  float* attn_rec = nullptr;
+  unsigned long long* attn_gmax = nullptr;
   float* o_f32 = nullptr;
-  float* y_acc = nullptr;
+  float* y_part = nullptr;
   int* row_ticket = nullptr;
+  unsigned long long* gbar = nullptr;
+  unsigned long long steps_launched = 0;  // decode steps launched (grid barrier epoch)
   float* k_tap = nullptr;
   float* v_tap = nullptr;
   float* out_tap = nullptr;
@@ -72,7 +77,6 @@ struct hfa_layer {
   __nv_bfloat16* x_stage = nullptr;
   int* pos_stage = nullptr;
   __nv_bfloat16* out_stage = nullptr;
-  int max_splits = 0;
   hfa::VerifyState* verify = nullptr;
   // tensor maps of the caches of the last call
   const void* tm_k_ptr = nullptr;
@@ -80,7 +84,7 @@ struct hfa_layer {
   int tm_rows = 0;
   CUtensorMap tm_k{}, tm_v{};
   // plan of the last call
-  int last_splits = 0, last_gemv_grid = 0, last_attn_grid = 0;
+  int last_splits = 0, last_gemv_grid = 0, last_attn_grid = 0;  // tiles, grids
   int last_rows = 0;
   // timing
   bool timing = false;
@@ -224,6 +228,23 @@ static hfa_status validate_desc(const hfa_layer_desc* d) {
   return HFA_OK;
 }
 
+// Split-K shape of a decode-step GEMV: k-splits of nbs 32-column blocks, nbs the largest
+// divisor of the block count up to 16 (512 columns), and as many nbs-tile work items per
+// 64 KiB ring stage as fit.
+static void plan_step_gemv(StepGemv* g, int rows, int cols) {
+  g->R = rows / 16;
+  g->nb = cols / 32;
+  g->nbs = 1;
+  for (int d = 16; d >= 1; --d)
+    if (g->nb % d == 0) {
+      g->nbs = d;
+      break;
+    }
+  g->S = g->nb / g->nbs;
+  g->ips = (int)(step_stage_bytes() / ((size_t)g->nbs * kQ8TileBytes));
+  g->w = nullptr;
+}
+
 // ------------------------------------------------------------------ create / destroy
 static void free_layer(hfa_layer* L) {
   if (!L) return;
@@ -291,19 +312,30 @@ extern "C" hfa_status hfa_layer_create(const hfa_layer_desc* desc, const void* w
   } while (0)
 
   if (!bf16w) {
-    L->wqkv.rows = L->rows_qkv;
-    L->wqkv.cols = H;
-    LA(L->wqkv.q, (size_t)L->rows_qkv * H);
-    LA(L->wqkv.d, (size_t)L->rows_qkv / 16 * (H / 32) * 8);
-    L->wo.rows = H;
-    L->wo.cols = nh * hd;
-    LA(L->wo.q, (size_t)H * nh * hd);
-    LA(L->wo.d, (size_t)H / 16 * (nh * hd / 32) * 8);
-    LC(launch_repack_q8_0((const uint8_t*)wq, nh * hd, H, &L->wqkv, 0, s), "repack wq");
-    LC(launch_repack_q8_0((const uint8_t*)wk, nkv * hd, H, &L->wqkv, nh * hd, s), "repack wk");
-    LC(launch_repack_q8_0((const uint8_t*)wv, nkv * hd, H, &L->wqkv, (nh + nkv) * hd, s),
+    plan_step_gemv(&L->g_qkv, L->rows_qkv, H);
+    plan_step_gemv(&L->g_o, H, nh * hd);
+    if (L->g_qkv.S > L->num_sms || L->g_o.S > L->num_sms) {
+      snprintf(g_create_error, 512, "hidden=%d / nh*hd=%d need more k-splits than the %d SMs",
+               H, nh * hd, L->num_sms);
+      delete L;
+      return HFA_EUNSUPPORTED;
+    }
+    const int Rq = L->rows_qkv / 16;
+    LA(L->wqkv_t, (size_t)Rq * L->g_qkv.nb * kQ8TileBytes);
+    LA(L->wo_t, (size_t)(H / 16) * L->g_o.nb * kQ8TileBytes);
+    L->g_qkv.w = L->wqkv_t;
+    L->g_o.w = L->wo_t;
+    const int nbq = L->g_qkv.nbs, nbo = L->g_o.nbs;
+    LC(launch_repack_q8_0_split((const uint8_t*)wq, nh * hd, H, L->wqkv_t, 0, Rq, nbq, s),
+       "repack wq");
+    LC(launch_repack_q8_0_split((const uint8_t*)wk, nkv * hd, H, L->wqkv_t, nh * hd / 16, Rq, nbq,
+                                s),
+       "repack wk");
+    LC(launch_repack_q8_0_split((const uint8_t*)wv, nkv * hd, H, L->wqkv_t, (nh + nkv) * hd / 16,
+                                Rq, nbq, s),
        "repack wv");
-    LC(launch_repack_q8_0((const uint8_t*)wo, H, nh * hd, &L->wo, 0, s), "repack wo");
+    LC(launch_repack_q8_0_split((const uint8_t*)wo, H, nh * hd, L->wo_t, 0, H / 16, nbo, s),
+       "repack wo");
   } else {
     LA(L->wqkv_bf16, (size_t)L->rows_qkv * H);
     LA(L->wo_bf16, (size_t)H * nh * hd);
@@ -335,16 +367,18 @@ extern "C" hfa_status hfa_layer_create(const hfa_layer_desc* desc, const void* w
     LC(cudaStreamSynchronize(s), "create sync");
   }
   // scratch
-  L->max_splits = 2 * L->num_sms;
   const int units = d.max_batch * nkv;
-  LA(L->qkv_acc, (size_t)MR * L->rows_qkv);
-  LA(L->head_ticket, nh + 2 * nkv);
+  if (!bf16w) {
+    LA(L->qkv_part, (size_t)L->g_qkv.S * d.max_batch * L->rows_qkv);
+    LA(L->ss_part, (size_t)L->g_qkv.S * 16);
+    LA(L->y_part, (size_t)L->g_o.S * d.max_batch * H);
+  }
   LA(L->q_f32, (size_t)MR * nh * hd);
-  // one (m, l, O) record per attention chunk: units * splits <= max(2 SMs, units)
-  LA(L->attn_part, (size_t)(units > L->max_splits ? units : L->max_splits) * attn_record_floats(hd));
-  LA(L->attn_ticket, units);
+  // one (m, l, O) record per (CTA, unit) pair of the step kernel: ids c + u are unique
+  LA(L->attn_rec, (size_t)(L->num_sms + units) * attn_record_floats(hd));
+  LA(L->gbar, 1);
+  LA(L->attn_gmax, (size_t)d.max_batch * nh);
   LA(L->o_f32, (size_t)MR * nh * hd);
-  LA(L->y_acc, (size_t)MR * H);
   LA(L->row_ticket, H / 16);
   LA(L->err, 1);
   LA(L->x_stage, (size_t)d.max_batch * H);
@@ -358,10 +392,9 @@ extern "C" hfa_status hfa_layer_create(const hfa_layer_desc* desc, const void* w
   for (void* p : L->allocations) {
     (void)p;
   }
-  LC(cudaMemsetAsync(L->qkv_acc, 0, (size_t)MR * L->rows_qkv * 4, s), "memset");
-  LC(cudaMemsetAsync(L->head_ticket, 0, (nh + 2 * nkv) * 4, s), "memset");
-  LC(cudaMemsetAsync(L->attn_ticket, 0, units * 4, s), "memset");
-  LC(cudaMemsetAsync(L->y_acc, 0, (size_t)MR * H * 4, s), "memset");
+
+  LC(cudaMemsetAsync(L->gbar, 0, 8, s), "memset");
+  LC(cudaMemsetAsync(L->attn_gmax, 0, (size_t)d.max_batch * nh * 8, s), "memset");
   LC(cudaMemsetAsync(L->row_ticket, 0, H / 16 * 4, s), "memset");
   LC(cudaMemsetAsync(L->err, 0, 4, s), "memset");
   if (d.max_verify_len > 0) {
@@ -392,97 +425,6 @@ extern "C" const char* hfa_last_error(const hfa_layer* L) {
 
 // ------------------------------------------------------------------ decode step
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
-
-static void fill_gemv_common(hfa_layer* L, GemvArgs& a, const Q8Tiles& w, int batch) {
-  a.wq = w.q;
-  a.wd = w.d;
-  a.R = w.rows / 16;
-  a.nb = w.cols / 32;
-  a.batch = batch;
-  a.cols = w.cols;
-  a.err = L->err;
-}
-
-// k-split and grid of one GEMV: every warp streams the same number of tiles; the
-// activation operand of the (at most two) k-splits a CTA touches must fit in shared memory.
-// Work items of the GEMV: (k-split, row group) pairs of nbs tiles, one warp each, CTAs
-// of gemv_items_per_cta() consecutive items.  nbs = 16 blocks (512 columns) where the row
-// allows it, doubled while that leaves more than three CTAs per SM.
-static void plan_gemv(hfa_layer* L, GemvArgs& a, int* grid, int* threads, size_t* smem) {
-  const int ipc = gemv_items_per_cta();
-  int nbs = a.nb % 16 == 0 ? 16 : (a.nb % 8 == 0 ? 8 : a.nb);
-  const long long resident = (gemv_ntiles(a.batch) >= 4 ? 2LL : 3LL) * L->num_sms;  // CTAs
-  while (a.nb % (2 * nbs) == 0 && (long long)(a.nb / nbs) * a.R / ipc > resident) nbs *= 2;
-  a.S = a.nb / nbs;
-  a.nbs = nbs;
-  a.tiles = (long long)a.S * a.R * a.nbs;
-  const int items = a.S * a.R;
-  // k-splits one CTA's ipc consecutive items can span (one when R is a multiple of ipc)
-  int spans = a.R % ipc == 0 ? 1 : (ipc - 1) / a.R + 2;
-  if (spans > a.S) spans = a.S;
-  const int blocks_max = spans * nbs;
-  *smem = gemv_smem_bytes(a.batch, blocks_max);
-  *threads = ipc * 32;
-  *grid = (items + ipc - 1) / ipc;
-}
-
-static hfa_status launch_qkv(hfa_layer* L, cudaStream_t s, const void* x, const int* pos_dev,
-                             int rows, bool tokens, void* kc, void* vc) {
-  GemvArgs a{};
-  fill_gemv_common(L, a, L->wqkv, rows);
-  a.x = (const __nv_bfloat16*)x;
-  a.w_in = L->w_in;
-  a.eps = L->d.eps;
-  a.acc = L->qkv_acc;
-  a.ticket = L->head_ticket;
-  a.nh = L->d.num_heads;
-  a.nkv = L->d.num_kv_heads;
-  a.hd = L->d.head_dim;
-  a.C = L->d.kv_capacity;
-  a.ring = (L->d.flags & HFA_F_RING) ? 1 : 0;
-  a.w_q = L->w_q;
-  a.w_k = L->w_k;
-  a.rope_g = L->rope_g;
-  a.seq_pos = pos_dev;
-  a.v_unit_norm = (L->d.flags & HFA_F_V_UNIT_NORM) ? 1 : 0;
-  a.q_out = L->q_f32;
-  a.k_cache = (__nv_bfloat16*)kc;
-  a.v_cache = (__nv_bfloat16*)vc;
-  a.k_tap = L->k_tap;
-  a.v_tap = L->v_tap;
-  a.rows_are_tokens = tokens ? 1 : 0;
-  int grid, threads;
-  size_t smem;
-  plan_gemv(L, a, &grid, &threads, &smem);
-  L->last_gemv_grid = grid;
-  KernelTimer t;
-  timer_begin(L, s, "qkv_norm_rope_append", &t);
-  cudaError_t e = launch_gemv(kModeQKV, a, grid, threads, smem, !L->timing, s);
-  timer_end(L, s, &t);
-  if (e != cudaSuccess) return cuda_fail(L, e, "qkv kernel launch");
-  return HFA_OK;
-}
-
-static hfa_status launch_oproj(hfa_layer* L, cudaStream_t s, const void* x, int rows,
-                               void* out) {
-  GemvArgs a{};
-  fill_gemv_common(L, a, L->wo, rows);
-  a.x = (const __nv_bfloat16*)x;
-  a.xin = L->o_f32;
-  a.acc = L->y_acc;
-  a.ticket = L->row_ticket;
-  a.out = (__nv_bfloat16*)out;
-  a.out_tap = L->out_tap;
-  int grid, threads;
-  size_t smem;
-  plan_gemv(L, a, &grid, &threads, &smem);
-  KernelTimer t;
-  timer_begin(L, s, "oproj_residual", &t);
-  cudaError_t e = launch_gemv(kModeOProj, a, grid, threads, smem, !L->timing, s);
-  timer_end(L, s, &t);
-  if (e != cudaSuccess) return cuda_fail(L, e, "o_proj kernel launch");
-  return HFA_OK;
-}
 
 static hfa_status ensure_maps(hfa_layer* L, void* kc, void* vc, int rows) {
   if (L->tm_k_ptr == kc && L->tm_v_ptr == vc && L->tm_rows == rows) return HFA_OK;
@@ -567,39 +509,70 @@ extern "C" hfa_status hfa_decode_step(hfa_layer* L, void* stream, const void* x,
   cudaStream_t s = (cudaStream_t)stream;
   const int nkv = d.num_kv_heads, hd = d.head_dim;
   const long long rows = (long long)batch * nkv * d.kv_capacity;
-  if (rows >= (1ll << 31)) return fail(L, HFA_EUNSUPPORTED, "cache too large for 32-bit TMA rows");
+  if (rows + 256 >= (1ll << 31))
+    return fail(L, HFA_EUNSUPPORTED, "cache too large for 32-bit TMA rows");
   hfa_status st = ensure_maps(L, kc, vc, (int)rows);
   if (st != HFA_OK) return st;
 
-  // (1) input norm + QKV + per-head norm + RoPE + append
-  st = launch_qkv(L, s, x, pos_dev, batch, false, kc, vc);
-  if (st != HFA_OK) return st;
-
-  // (2) attention
-  AttnArgs aa{};
-  int S = 0;
-  fill_attn(aa, d.num_heads, nkv, hd, d.kv_capacity, d.layer_type, d.window, ring, d.attn_scale,
-            d.softcap, batch, max_keys, L->num_sms, L->max_splits, &S);
-  aa.q = L->q_f32;
-  aa.seq_pos = pos_dev;
-  aa.part = L->attn_part;
-  aa.ticket = L->attn_ticket;
-  aa.o = L->o_f32;
-  aa.err = L->err;
-  const int units = batch * nkv;
-  L->last_splits = S;
-  L->last_attn_grid = units * S;
-  {
-    KernelTimer t;
-    timer_begin(L, s, "flash_decode", &t);
-    cudaError_t e = launch_attn(aa, L->tm_k, L->tm_v, units * S, !L->timing, s);
-    timer_end(L, s, &t);
-    if (e != cudaSuccess) return cuda_fail(L, e, "attention kernel launch");
+  const bool taps = d.flags & HFA_F_DEBUG_TAPS;
+  StepArgs sa{};
+  sa.qkv = L->g_qkv;
+  sa.o = L->g_o;
+  sa.x = (const __nv_bfloat16*)x;
+  sa.w_in = L->w_in;
+  sa.w_q = L->w_q;
+  sa.w_k = L->w_k;
+  sa.rope_g = L->rope_g;
+  sa.seq_pos = pos_dev;
+  sa.k_cache = (__nv_bfloat16*)kc;
+  sa.v_cache = (__nv_bfloat16*)vc;
+  sa.qkv_part = L->qkv_part;
+  sa.ss_part = L->ss_part;
+  sa.rec = L->attn_rec;
+  sa.y_part = L->y_part;
+  sa.row_ticket = L->row_ticket;
+  sa.gbar = L->gbar;
+  sa.gbar_base = 2ull * (unsigned long long)L->num_sms * L->steps_launched;
+  sa.gmax = L->attn_gmax;
+  sa.step = (unsigned)(L->steps_launched + 1);
+  sa.err = L->err;
+  sa.q_tap = taps ? L->q_f32 : nullptr;
+  sa.k_tap = L->k_tap;
+  sa.v_tap = L->v_tap;
+  sa.o_tap = taps ? L->o_f32 : nullptr;
+  sa.out_tap = L->out_tap;
+  sa.out = (__nv_bfloat16*)out;
+  sa.B = batch;
+  sa.H = d.hidden;
+  sa.nh = d.num_heads;
+  sa.nkv = nkv;
+  sa.C = d.kv_capacity;
+  sa.cache_rows = rows;
+  sa.sliding = d.layer_type == HFA_SLIDING;
+  sa.window = d.window;
+  sa.ring = ring ? 1 : 0;
+  sa.v_unit_norm = (d.flags & HFA_F_V_UNIT_NORM) ? 1 : 0;
+  sa.eps = d.eps;
+  const float log2e = 1.4426950408889634f;
+  if (d.softcap > 0.f) {
+    sa.qscale = d.attn_scale / d.softcap;
+    sa.cap_log2 = d.softcap * log2e;
+  } else {
+    sa.qscale = d.attn_scale * log2e;
+    sa.cap_log2 = 0.f;
   }
-
-  // (3) o_proj + residual
-  st = launch_oproj(L, s, x, batch, out);
-  if (st != HFA_OK) return st;
+  const int T = attn_keys_per_stage(hd);
+  int tiles = 0;
+  for (int b = 0; b < batch; ++b) tiles += (visible_keys(d, pos_host[b]) + T - 1) / T * nkv;
+  L->last_splits = tiles;
+  L->last_gemv_grid = L->num_sms;
+  L->last_attn_grid = L->num_sms;
+  KernelTimer t;
+  timer_begin(L, s, "decode_step", &t);
+  cudaError_t e = launch_step(sa, L->tm_k, L->tm_v, hd, L->num_sms, s);
+  timer_end(L, s, &t);
+  if (e != cudaSuccess) return cuda_fail(L, e, "decode-step kernel launch");
+  ++L->steps_launched;
   L->last_rows = batch;
   return HFA_OK;
 }
@@ -684,7 +657,7 @@ extern "C" hfa_status hfa_attention_decode(const hfa_attn_desc* d, void* stream,
   if (ws_bytes < need)
     return fail(nullptr, HFA_EINVAL, "workspace of %zu bytes, %zu needed", ws_bytes, need);
   const long long rows = (long long)units * d->kv_capacity;
-  if (rows >= (1ll << 31)) return fail(nullptr, HFA_EUNSUPPORTED, "cache too large");
+  if (rows + 256 >= (1ll << 31)) return fail(nullptr, HFA_EUNSUPPORTED, "cache too large");
   CUtensorMap tk, tv;
   const int T = attn_keys_per_stage(d->head_dim);
   if (hfa_encode_kv_map(&tk, (void*)kc, (int)rows, d->head_dim, T) != HFA_OK ||
@@ -804,6 +777,13 @@ extern "C" hfa_status hfa_check_device_status(hfa_layer* L, void* stream) {
   CK(L, cudaStreamSynchronize(s), "sync");
   if (v == 0) return HFA_OK;
   CK(L, cudaMemsetAsync(L->err, 0, 4, s), "clear status");
+  // a step that gave up may have left the grid barrier mid-count
+  CK(L, cudaMemsetAsync(L->gbar, 0, 8, s), "reset grid barrier");
+  if (L->attn_gmax)
+    CK(L, cudaMemsetAsync(L->attn_gmax, 0, (size_t)L->d.max_batch * L->d.num_heads * 8, s),
+       "reset record maxima");
+  CK(L, cudaStreamSynchronize(s), "sync");
+  L->steps_launched = 0;
   CK(L, cudaStreamSynchronize(s), "sync");
   return fail(L, HFA_EDEVICE, "device status 0x%x:%s%s%s", v,
               (v & kErrWaitTimeout) ? " a bounded wait gave up;" : "",
@@ -838,7 +818,7 @@ extern "C" int hfa_kernel_times(hfa_layer* L, int n, const char** names, float* 
     L->event_pool.push_back(t.stop);
   }
   L->pending.clear();
-  static const char* kNames[] = {"qkv_norm_rope_append", "flash_decode", "oproj_residual",
+  static const char* kNames[] = {"decode_step", "flash_decode",
                                  "verify_prep", "verify_qkv_gemm", "verify_norm_rope_append", "verify_attention",
                                  "verify_oproj_gemm", "verify_residual"};
   int k = 0;

@@ -10,25 +10,11 @@
 
 namespace hfa {
 
-// Repacked Q8_0 matrix: 16-row x 32-column tiles of 512 bytes, laid out so that one
-// 16-byte load per lane gives that lane's operand registers of two m16n8k16 MMAs.
-struct Q8Tiles {
-  uint8_t* q = nullptr;  // [rows/16][cols/32][32 lanes][16 B], bytes hold q + 128
-  __half2* d = nullptr;  // [rows/16][cols/32][8]: (d[row g], d[row g + 8])
-  int rows = 0, cols = 0;
-};
-
-// Arguments of the dequantising GEMV kernels (both modes).
+// Epilogue arguments of the verify-block GEMMs (per-head norm + RoPE + KV append, and
+// the residual), shared with the finishers of hfa_finish.cuh.
 struct GemvArgs {
-  const uint8_t* wq;
-  const __half2* wd;
   int R;             // row groups of 16
-  int nb;            // 32-column blocks per row
-  int S;             // k splits
-  int nbs;           // blocks per split (nb / S): the tiles of one work item
-  long long tiles;   // S * R * nbs
   int batch;
-  int cols;
   const __nv_bfloat16* x;  // QKV: layer input bf16 [B, cols]; OPROJ: residual bf16 [B, R*16]
   const float* w_in;       // QKV: input RMSNorm weight [cols]
   const float* xin;        // OPROJ: attention output f32 [B, cols]
@@ -73,6 +59,54 @@ struct AttnArgs {
 
 enum GemvMode { kModeQKV = 0, kModeOProj = 1 };
 
+// One Q8_0 projection in the layout of the persistent decode-step kernel: 16 x 32 tiles
+// of 544 bytes (512 bytes of biased int8 in MMA operand order, then 8 half2 scales),
+// ordered (k-split s, row group r, block bb) so that the row groups one CTA owns in one
+// k-split are a single contiguous byte range.
+constexpr int kQ8TileBytes = 544;
+struct StepGemv {
+  const uint8_t* w;  // [S][R][nbs] tiles
+  int R;             // row groups of 16 rows
+  int nb;            // 32-column blocks per row
+  int nbs;           // blocks per k-split
+  int S;             // k-splits (nb / nbs), at most the grid size
+  int ips;           // work items (nbs tiles each) per ring stage
+};
+
+// Arguments of the persistent decode-step kernel (one CTA per SM, cooperative launch).
+struct StepArgs {
+  StepGemv qkv, o;
+  const __nv_bfloat16* x;  // layer input bf16 [B, H]
+  const float* w_in;       // input RMSNorm weight [H]
+  const float* w_q;        // per-head norm weights [hd]
+  const float* w_k;
+  const float2* rope_g;    // [hd/2] (hi, lo) of theta^(-2i/hd) / (2 pi)
+  const int* seq_pos;      // [B]
+  __nv_bfloat16* k_cache;  // [B, nkv, C, hd]
+  __nv_bfloat16* v_cache;
+  float* qkv_part;         // f32 [qkv.S][B][(nh + 2 nkv) hd]: one partial sum per k-split
+  float* ss_part;          // f32 [qkv.S][16]: sum of x^2 over each k-split's columns
+  float* rec;              // f32 [(grid + B nkv)][8][hd + 4]: (O, m, l) per key range
+  float* y_part;           // f32 [o.S][B][H]: one partial o_proj sum per k-split
+  int* row_ticket;         // [H / 16]: zero on entry and on exit
+  unsigned long long* gmax;  // [B * nh]: (step << 32) | ordered(max logit) over the records
+  unsigned step;           // this step's number (nonzero), the high word of gmax
+  unsigned long long* gbar;  // grid barrier arrivals (monotonic, two per CTA per step)
+  unsigned long long gbar_base;  // arrivals before this step: 2 * grid * steps so far
+  unsigned* err;
+  float* q_tap;            // nullable f32 [B, nh, hd] (q after RoPE)
+  float* k_tap;            // nullable f32 [B, nkv, hd]
+  float* v_tap;
+  float* o_tap;            // nullable f32 [B, nh, hd] (attention output)
+  float* out_tap;          // nullable f32 [B, H]
+  __nv_bfloat16* out;      // bf16 [B, H]
+  int B, H, nh, nkv, C, sliding, window, ring, v_unit_norm;
+  long long cache_rows;    // B * nkv * C: rows of the [rows, hd] view of each cache
+  float eps;
+  float qscale;            // scale * log2(e), or scale / softcap with a softcap
+  float cap_log2;          // softcap * log2(e), 0 = no softcap
+};
+
 // Optional per-launch event timing (the layer's hfa_set_kernel_timing); begin/end
 // bracket one kernel launch on `s`.
 struct LaunchTimer {
@@ -89,13 +123,15 @@ void set_thread_error(const char* msg);
 bool encode_bf16_2d(CUtensorMap* map, void* base, int inner, int rows, int box_inner,
                     int box_rows);
 
-cudaError_t launch_repack_q8_0(const uint8_t* src, int rows, int cols, Q8Tiles* dst,
-                               size_t row_offset_rows, cudaStream_t s);
-cudaError_t launch_gemv(int mode, const GemvArgs& a, int grid, int threads, size_t smem,
-                        bool pdl, cudaStream_t s);
-size_t gemv_smem_bytes(int batch, int blocks_per_cta_max);
-int gemv_ntiles(int batch);
-int gemv_items_per_cta();
+cudaError_t launch_repack_q8_0_split(const uint8_t* src, int rows, int cols, uint8_t* dst,
+                                     int row_group0, int R_total, int nbs, cudaStream_t s);
+// the decode step: grid = one CTA per SM (cooperative), ntiles = gemv batch tiles
+cudaError_t launch_step(const StepArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int hd,
+                        int grid, cudaStream_t s);
+size_t step_smem_bytes();
+size_t step_stage_bytes();
+int step_threads();
+int step_batch_tiles(int batch);
 
 cudaError_t launch_attn(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                         int grid, bool pdl, cudaStream_t s);

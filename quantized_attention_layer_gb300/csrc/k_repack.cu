@@ -3,20 +3,23 @@
 // Input: the Q8_0 layout of the Q8_0 lm_head re-quantiser (gemma4/model.rs): per row,
 // cols/32 blocks of 34 bytes = fp16 scale d (little endian) + 32 int8 q.  The 34-byte
 // stride is not 16-byte aligned, so the decode GEMV could not use 128-bit loads on it.
-// Output (values untouched, only moved):
-//   q tiles: tile (row group r, block b) = 512 bytes; lane l = 4g + t owns bytes
-//     [16l, 16l+16): word 0 = row g, word 1 = row g+8 for columns {2t, 2t+1, 2t+8, 2t+9}
-//     of the block's first 16 columns; words 2, 3 the same for columns 16 + {...}.
-//     Each byte stores q + 128 (so the GEMV converts it to fp16 without a sign step).
-//   d tiles: tile (r, b) = 8 half2, entry g = (d[row g], d[row g + 8]).
+// Output (values untouched, only moved): one 544-byte tile per 16 rows x 32 columns,
+//   bytes [0, 512): lane l = 4g + t owns bytes [16l, 16l+16): word 0 = row g, word 1 =
+//     row g+8 for columns {2t, 2t+1, 2t+8, 2t+9} of the block's first 16 columns;
+//     words 2, 3 the same for columns 16 + {...}.  Each byte stores q + 128 (so the GEMV
+//     converts it to fp16 without a sign step).
+//   bytes [512, 544): 8 half2, entry g = (d[row g], d[row g + 8]).
 #include "hfa_common.cuh"
 #include "hfa_internal.h"
 
 namespace hfa {
 
-__global__ void repack_q8_0_kernel(const uint8_t* __restrict__ src, int rows, int cols,
-                                   uint8_t* __restrict__ qdst, __half2* __restrict__ ddst,
-                                   int row0) {
+// Tile (row group r, block b) of a matrix with R_total row groups lands at index
+// ((b / nbs) * R_total + r) * nbs + b % nbs: the row groups of one k-split of nbs blocks
+// are then one contiguous byte range, which the decode-step kernel copies in bulk.
+__global__ void repack_q8_0_split_kernel(const uint8_t* __restrict__ src, int rows, int cols,
+                                         uint8_t* __restrict__ dst, int row_group0, int R_total,
+                                         int nbs) {
   const int nb = cols / 32;
   const long long n = (long long)(rows / 16) * nb * 32;
   for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n;
@@ -42,24 +45,26 @@ __global__ void repack_q8_0_kernel(const uint8_t* __restrict__ src, int rows, in
         w[2 * ks + half] = v;
       }
     }
-    const long long out_tile = (long long)(row0 / 16 + r) * nb + b;
-    reinterpret_cast<uint4*>(qdst)[out_tile * 32 + lane] = make_uint4(w[0], w[1], w[2], w[3]);
+    const long long out_tile =
+        ((long long)(b / nbs) * R_total + (row_group0 + r)) * nbs + (b % nbs);
+    uint8_t* tp = dst + out_tile * kQ8TileBytes;
+    reinterpret_cast<uint4*>(tp)[lane] = make_uint4(w[0], w[1], w[2], w[3]);
     if (t == 0) {
       __half dg = __ushort_as_half((unsigned short)(row_g[0] | (row_g[1] << 8)));
       __half dg8 = __ushort_as_half((unsigned short)(row_g8[0] | (row_g8[1] << 8)));
-      ddst[out_tile * 8 + g] = __halves2half2(dg, dg8);
+      reinterpret_cast<__half2*>(tp + 512)[g] = __halves2half2(dg, dg8);
     }
   }
 }
 
-cudaError_t launch_repack_q8_0(const uint8_t* src, int rows, int cols, Q8Tiles* dst,
-                               size_t row_offset_rows, cudaStream_t s) {
+cudaError_t launch_repack_q8_0_split(const uint8_t* src, int rows, int cols, uint8_t* dst,
+                                     int row_group0, int R_total, int nbs, cudaStream_t s) {
   long long n = (long long)(rows / 16) * (cols / 32) * 32;
   int threads = 256;
   long long blocks = (n + threads - 1) / threads;
   if (blocks > 65535) blocks = 65535;
-  repack_q8_0_kernel<<<(int)blocks, threads, 0, s>>>(src, rows, cols, dst->q, dst->d,
-                                                     (int)row_offset_rows);
+  repack_q8_0_split_kernel<<<(int)blocks, threads, 0, s>>>(src, rows, cols, dst, row_group0,
+                                                           R_total, nbs);
   return cudaGetLastError();
 }
 

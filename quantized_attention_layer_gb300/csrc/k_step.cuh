@@ -1,0 +1,984 @@
+// k_step.cuh -- the decode step of one attention layer as one persistent kernel.
+//
+// One CTA per SM, launched cooperatively so that every CTA is resident and the CTAs may
+// wait for one another at two grid barriers.  Three phases:
+//   A  QKV projection of x (.) w_in with the Q8_0 matrix [Wq; Wk; Wv]
+//      (gemma4/gpu_full_attn.rs, encode_one_layer: "Pre-attention norm", "QKV
+//      projections").  The input norm's 1/rms(x) is a per-row factor, so it is applied
+//      after the projection (phase B), and the projection never waits for it.
+//   B  per (sequence, KV head) unit: q_norm / k_norm, NeoX RoPE and the bf16 KV append
+//      ("Fused per-head RMS norm + RoPE on Q and K", "GPU V norm", dense KV copy), then
+//      the GQA flash-decode over the unit's visible keys ("Dense flash_attn_vec",
+//      FlashAttnVecParams; softcap of dflash/forward.rs).  The key tiles of all units are
+//      dealt out evenly over the CTAs; every CTA writes one (m, l, O) record per unit it
+//      touched.
+//   C  o_proj and the residual ("O-proj"; dflash/forward.rs residual add).  The records
+//      of phase B are combined with log-sum-exp weights while the GEMV operand is built,
+//      so the split-K attention needs no combine pass of its own.
+// Data movement: one producer warp streams everything the CTA reads in bulk -- the weight
+// tiles of phase A, the K/V tiles of phase B, the weight tiles of phase C -- through one
+// ring of shared-memory stages, in that order and as far ahead as the ring allows.  No
+// load waits for a result of the step except the K/V tile holding the slot appended in
+// this step: the producer issues it after the append has been written.
+//
+// Every wait (mbarrier, grid barrier) is bounded in wall time; a CTA that gives up sets
+// an error bit, stops loading and computing, still passes every later barrier so that
+// the others are not held, and drains its copies in flight before it exits.
+#pragma once
+#include "hfa_common.cuh"
+#include "hfa_finish.cuh"
+#include "hfa_internal.h"
+
+namespace hfa {
+namespace step {
+
+constexpr int kCW = 8;                    // consumer warps
+constexpr int kConsumers = kCW * 32;
+constexpr int kThreads = kConsumers + 32; // + the producer warp
+constexpr int kStages = 3;
+constexpr int kStageBytes = 65536;
+constexpr int kUnionBytes = 33792;        // GEMV operand / query rows / merge area
+constexpr int kSmallBytes = 1024;         // barriers, flags, per-row values
+constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kUnionBytes + kSmallBytes;
+constexpr int kKeysPerWarp = 16;
+constexpr int kMaxBatch = 16;
+constexpr int kEarlyTiles = 2;            // K/V tiles prefetched into L2 during phase A
+
+// per batch row: position, visible slots [lo, hi], key tiles, tile of the new slot, slot
+enum { kGeoP = 0, kGeoLo, kGeoHi, kGeoNt, kGeoTn, kGeoSlot, kGeoInts = 8 };
+
+// Attention tile shape: NC key groups of 16 keys per tile; with HD = 256 the 8 consumer
+// warps pair up on a key group (both form S = Q K^T, each accumulates half of O's dims),
+// which halves the O registers of a warp.
+template <int HD>
+struct Attn {
+  static constexpr int NC = HD >= 256 ? 4 : 8;        // key groups of a tile
+  static constexpr int DSPLIT = kCW / NC;             // warps per key group
+  static constexpr int T = NC * kKeysPerWarp;         // keys per tile
+  static constexpr int BOXES = HD / 64;               // 128-byte TMA boxes per row
+  static constexpr int TILE_BYTES = T * HD * 2;       // one of K, V
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+  static constexpr int KS = HD / 16;
+  static constexpr int NTO = HD / 8;                  // n8 tiles of O
+  static constexpr int NTW = NTO / DSPLIT;            // n8 tiles of O per warp
+  static constexpr int RS = HD + 4;                   // record: O[HD], m, l, pad
+  static constexpr int QS_OFF = 8192;                 // query rows (f32) in the union
+  static_assert(STAGE_BYTES <= kStageBytes, "a K/V tile must fit a stage");
+  static_assert(NC * DSPLIT == kCW, "every consumer warp takes part");
+  static_assert(NC * 8 * RS * 4 <= kUnionBytes, "merge area must fit the union");
+  static_assert(KS * 32 * 16 <= QS_OFF && QS_OFF + 8 * HD * 4 <= kUnionBytes, "query rows");
+};
+
+// ------------------------------------------------------------------ small helpers
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_add_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Balanced partition of n items over P parts: part c owns [begin(c), begin(c + 1)).
+__device__ __forceinline__ int part_begin(int c, long long n, int P) {
+  return (int)((long long)c * n / P);
+}
+// the part that owns item t (0 <= t < n): the largest c with begin(c) <= t
+__device__ __forceinline__ int part_of(int t, long long n, int P) {
+  return (int)(((long long)(t + 1) * P - 1) / n);
+}
+
+// Rows of a split-K GEMV owned by CTA c: the CTAs are dealt out over the k-splits, and
+// the CTAs of one split share its row groups evenly.
+struct Slice {
+  int s, r0, r1;
+  bool first;  // first CTA of its split
+};
+__device__ __forceinline__ Slice gemv_slice(const StepGemv& g, int c, int nctas) {
+  Slice sl;
+  sl.s = part_of(c, nctas, g.S);
+  const int c0 = part_begin(sl.s, nctas, g.S), c1 = part_begin(sl.s + 1, nctas, g.S);
+  sl.r0 = part_begin(c - c0, g.R, c1 - c0);
+  sl.r1 = part_begin(c - c0 + 1, g.R, c1 - c0);
+  sl.first = c == c0;
+  return sl;
+}
+
+// Units (sequence b, KV head kvh) in order u = b * nkv + kvh; unit u holds nt_b key tiles.
+// Calls f(b, kvh, lt0, lt1) for the part [lt0, lt1) of each unit inside the global tile
+// range [t0, t1).
+template <typename F>
+__device__ __forceinline__ void for_each_segment(const int* geo, int B, int nkv, int t0, int t1,
+                                                 F&& f) {
+  int base = 0;
+  for (int b = 0; b < B && base < t1; ++b) {
+    const int nt = geo[b * kGeoInts + kGeoNt];
+    const int span = nt * nkv;
+    if (nt > 0 && base + span > t0) {
+      const int kv0 = t0 > base ? (t0 - base) / nt : 0;
+      for (int kvh = kv0; kvh < nkv; ++kvh) {
+        const int ub = base + kvh * nt;
+        if (ub >= t1) break;
+        const int lt0 = t0 > ub ? t0 - ub : 0;
+        const int lt1 = (t1 < ub + nt ? t1 : ub + nt) - ub;
+        if (lt1 > lt0) f(b, kvh, lt0, lt1);
+      }
+    }
+    base += span;
+  }
+}
+// i-th tile of a segment in load order: the tile holding the new slot (tn, if inside
+// [lt0, lt1)) goes last, so that its late load does not hold up the others.
+__device__ __forceinline__ int seg_tile(int i, int lt0, int lt1, int tn) {
+  if (tn < lt0 || tn >= lt1) return lt0 + i;
+  if (i < tn - lt0) return lt0 + i;
+  if (i < lt1 - lt0 - 1) return lt0 + i + 1;
+  return tn;
+}
+
+// Grid barrier of the consumer warps (the producer runs ahead and never joins).  The
+// arrival counter only grows: barrier k (0, 1) of a step completes when it reaches
+// base + (k + 1) * grid, base being the arrivals of all earlier steps.  Arrival is one
+// release reduction (no round trip); a CTA that has given up arrives without waiting, so
+// the count stays exact.
+__device__ __forceinline__ void grid_sync(unsigned long long* gbar, unsigned long long target,
+                                          unsigned* err, volatile int* abort) {
+  consumer_sync();
+  if (threadIdx.x == 0) {
+    const bool given_up = *abort != 0;
+    red_release_add_u64(gbar, 1ull);
+    if (!given_up) {
+      const uint64_t t0 = globaltimer_ns();
+      while ((long long)(ld_acquire_u64(gbar) - target) < 0) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          atomicOr(err, kErrWaitTimeout);
+          *abort = 1;
+          break;
+        }
+      }
+    }
+  }
+  consumer_sync();
+}
+
+// ------------------------------------------------------------------ GEMV pieces
+// One Q8_0 tile (16 rows x 32 columns) times every batch tile of the operand.
+template <int NT>
+__device__ __forceinline__ void q8_tile_mma(float (&acc)[NT][4], const uint4 w, uint32_t dbits,
+                                            const uint4* xrow) {
+  uint32_t A0[4], A1[4];
+  A0[0] = u8x2_to_h2(w.x, kSelLo);
+  A0[1] = u8x2_to_h2(w.y, kSelLo);
+  A0[2] = u8x2_to_h2(w.x, kSelHi);
+  A0[3] = u8x2_to_h2(w.y, kSelHi);
+  A1[0] = u8x2_to_h2(w.z, kSelLo);
+  A1[1] = u8x2_to_h2(w.w, kSelLo);
+  A1[2] = u8x2_to_h2(w.z, kSelHi);
+  A1[3] = u8x2_to_h2(w.w, kSelHi);
+  const __half2 d2 = *reinterpret_cast<const __half2*>(&dbits);
+  const float dg = __low2float(d2), dg8 = __high2float(d2);
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const uint4 xb = xrow[nt * 32];
+    float tmp[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_f16(tmp, A0, xb.x, xb.y);
+    mma_f16(tmp, A1, xb.z, xb.w);
+    acc[nt][0] = fmaf(tmp[0], dg, acc[nt][0]);
+    acc[nt][1] = fmaf(tmp[1], dg, acc[nt][1]);
+    acc[nt][2] = fmaf(tmp[2], dg8, acc[nt][2]);
+    acc[nt][3] = fmaf(tmp[3], dg8, acc[nt][3]);
+  }
+}
+
+// Operand word index of the column pair (cc, cc + 1) of batch row b: block cc / 32,
+// k-step and half of the m16n8k16 B fragment; batch row b in the n8 tile b / 4, as
+// column 2 (b % 4) (fp16 hi) and 2 (b % 4) + 1 (fp16 lo).  The lo word is 16 further.
+template <int NT>
+__device__ __forceinline__ int operand_word(int cc, int b) {
+  const int jb = cc >> 5, w32 = cc & 31;
+  const int ks = w32 >> 4, within = w32 & 15;
+  const int hf = within >> 3, t = (within & 7) >> 1;
+  const int nt = b >> 2, gh = 2 * (b & 3);
+  return ((jb * NT + nt) * 32 + gh * 4 + t) * 4 + 2 * ks + hf;
+}
+
+// power-of-two scale that brings the largest |value| m of a row to [2^14, 2^15)
+__device__ __forceinline__ int scale_exp(unsigned mbits) {
+  if (mbits == 0u) return 0;
+  int e = (int)((mbits >> 23) & 0xffu);
+  if (e == 0) e = 1;  // subnormal
+  int se = 141 - e;   // 14 - (e - 127)
+  return se < -120 ? -120 : (se > 120 ? 120 : se);
+}
+__device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }
+
+// Phase A operand: v = x (.) w_in over the columns of k-split s, for every batch row,
+// scaled per row by a power of two (exact; undone in the flush) and split into fp16
+// hi + lo.  The first CTA of each split also stores the split's part of sum(x^2).
+template <int NT>
+__device__ void build_x_operand(const StepArgs& a, int s, bool add_ss, uint32_t* xw,
+                                unsigned* s_max, float* s_ssq, float* s_inv) {
+  const int tid = threadIdx.x;
+  const int nbs = a.qkv.nbs;
+  const int groups = nbs * 4;  // 8-column groups per batch row
+  const int total = NT * 4 * groups;
+  float v[NT][8];
+#pragma unroll
+  for (int k = 0; k < NT; ++k) {
+    const int e = tid + k * kConsumers;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[k][i] = 0.f;
+    if (e < total) {
+      const int b = e / groups, gi = e - b * groups;
+      if (b < a.B) {
+        const int col = s * nbs * 32 + gi * 8;
+        const uint4 raw = *reinterpret_cast<const uint4*>(a.x + (size_t)b * a.H + col);
+        const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.w_in + col));
+        const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.w_in + col + 4));
+        const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+        float mx = 0.f, ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __bfloat1622float2(h[i]);
+          v[k][2 * i] = f.x * wv[2 * i];
+          v[k][2 * i + 1] = f.y * wv[2 * i + 1];
+          ss += f.x * f.x + f.y * f.y;
+          mx = fmaxf(mx, fmaxf(fabsf(v[k][2 * i]), fabsf(v[k][2 * i + 1])));
+        }
+        atomicMax(&s_max[b], __float_as_uint(mx));
+        if (add_ss) atomicAdd(&s_ssq[b], ss);
+      }
+    }
+  }
+  consumer_sync();
+#pragma unroll
+  for (int k = 0; k < NT; ++k) {
+    const int e = tid + k * kConsumers;
+    if (e < total) {
+      const int b = e / groups, gi = e - b * groups;
+      const float sc = b < a.B ? exp2i(scale_exp(s_max[b])) : 1.f;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        __half h0, l0, h1, l1;
+        split_f16(v[k][2 * t] * sc, h0, l0);
+        split_f16(v[k][2 * t + 1] * sc, h1, l1);
+        const int w = operand_word<NT>(gi * 8 + 2 * t, b);
+        xw[w] = pack_h2(h0, h1);
+        xw[w + 16] = pack_h2(l0, l1);
+      }
+    }
+  }
+  if (tid < a.B) {
+    s_inv[tid] = exp2i(-scale_exp(s_max[tid]));
+    if (add_ss) a.ss_part[s * 16 + tid] = s_ssq[tid];
+  }
+  consumer_sync();
+}
+
+// Epilogue of one o_proj row group once every k-split has stored its partial sums:
+// out = bf16(x + sum over the splits), the splits added in a fixed order.
+__device__ __forceinline__ void finish_rows(const StepArgs& a, int r, int lane) {
+  if (lane == 0) a.row_ticket[r] = 0;
+  for (int i = lane; i < 16 * a.B; i += 32) {
+    const int b = i >> 4, row = r * 16 + (i & 15);
+    const float* p = a.y_part + (size_t)b * a.H + row;
+    const size_t split_stride = (size_t)a.B * a.H;
+    float y = 0.f;
+#pragma unroll 8
+    for (int s = 0; s < a.o.S; ++s) y += __ldcg(p + s * split_stride);
+    const float o = __bfloat162float(a.x[(size_t)b * a.H + row]) + y;
+    a.out[(size_t)b * a.H + row] = __float2bfloat16_rn(o);
+    if (a.out_tap) a.out_tap[(size_t)b * a.H + row] = o;
+  }
+}
+
+// Partial sums of rows [16 r, 16 r + 16) over the nbs tiles of k-split s: stored (no
+// atomics) into the split's slice of the partial-sum buffer.  For o_proj the last of the
+// S items of a row group (ticket) adds the splits up.
+template <int NT, bool OPROJ>
+__device__ __forceinline__ void gemv_flush(const StepArgs& a, const StepGemv& gm,
+                                           float (&acc)[NT][4], int s, int r,
+                                           const float* s_inv, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  const int R16 = gm.R * 16;
+  float* dst = (OPROJ ? a.y_part : a.qkv_part) + (size_t)s * a.B * R16;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int b = nt * 4 + t;
+    if (b < a.B) {
+      const float f = OPROJ ? 1.f : s_inv[b];
+      dst[(size_t)b * R16 + r * 16 + g] = (acc[nt][0] + acc[nt][1]) * f;
+      dst[(size_t)b * R16 + r * 16 + g + 8] = (acc[nt][2] + acc[nt][3]) * f;
+    }
+  }
+  if (OPROJ) {
+    __syncwarp();
+    int done = 0;
+    if (lane == 0) done = atom_add_acq_rel(a.row_ticket + r, 1) + 1 == gm.S;
+    done = __shfl_sync(0xffffffffu, done, 0);
+    if (done) finish_rows(a, r, lane);
+  }
+}
+
+// The work items of one ring stage (n_items items of nbs tiles, row groups r_first ..),
+// one whole item per warp at a time.
+template <int NT, bool OPROJ>
+__device__ void gemv_stage(const StepArgs& a, const StepGemv& gm, int s, const uint8_t* stage,
+                           int n_items, int r_first, const uint4* frag, const float* s_inv,
+                           int warp, int lane) {
+  const int nbs = gm.nbs;
+  const int g = lane >> 2;
+  for (int item = warp; item < n_items; item += kCW) {
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    const uint8_t* tp = stage + (size_t)item * nbs * kQ8TileBytes;
+    const uint4* fr = frag + lane;
+#pragma unroll 4
+    for (int i = 0; i < nbs; ++i) {
+      const uint4 w = *reinterpret_cast<const uint4*>(tp + i * kQ8TileBytes + lane * 16);
+      const uint32_t d = *reinterpret_cast<const uint32_t*>(tp + i * kQ8TileBytes + 512 + g * 4);
+      q8_tile_mma<NT>(acc, w, d, fr + i * NT * 32);
+    }
+    gemv_flush<NT, OPROJ>(a, gm, acc, s, r_first + item, s_inv, lane);
+  }
+}
+
+// ------------------------------------------------------------------ attention pieces
+// byte offset of (row, 16-byte chunk) in a TMA tile written with the 128-byte swizzle
+template <int HD>
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  const int box = chunk >> 3, c = chunk & 7;
+  return (uint32_t)(box * (Attn<HD>::T * 128) + row * 128 + ((c ^ (row & 7)) << 4));
+}
+
+// One head of unit (b, kvh): job < G query head kvh * G + job, G the key, G + 1 the value.
+// Raw projection * 1/rms(x), per-head RMSNorm (q, k; v with the unit-norm flag), RoPE
+// (q, k); queries go to q_s, the key and value row to the cache slot (bf16, RNE).
+template <int HD>
+__device__ void head_job(const StepArgs& a, const int* geo, int b, int kvh, int job, int G,
+                         float* q_s, bool tap_q, int lane) {
+  constexpr int J = HD / 32;
+  const int rows = (a.nh + 2 * a.nkv) * HD;
+  const int kind = job < G ? 0 : (job == G ? 1 : 2);
+  const int row0 = kind == 0 ? (kvh * G + job) * HD
+                             : (kind == 1 ? (a.nh + kvh) * HD : (a.nh + a.nkv + kvh) * HD);
+  // the projection: partial sums of the k-splits added in a fixed order
+  const float* src = a.qkv_part + (size_t)b * rows + row0 + lane;
+  const size_t split_stride = (size_t)a.B * rows;
+  float v[J];
+#pragma unroll
+  for (int j = 0; j < J; ++j) v[j] = 0.f;
+  float ssx = 0.f;
+  for (int s = 0; s < a.qkv.S; ++s) {
+#pragma unroll
+    for (int j = 0; j < J; ++j) v[j] += __ldcg(src + s * split_stride + 32 * j);
+    ssx += __ldcg(a.ss_part + s * 16 + b);
+  }
+  // input RMSNorm factor 1/rms(x) of the row, applied to the projection (linear)
+  const float xinv = rsqrtf(ssx / a.H + a.eps);
+#pragma unroll
+  for (int j = 0; j < J; ++j) v[j] *= xinv;
+  if (kind < 2 || a.v_unit_norm) {
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < J; ++j) ss += v[j] * v[j];
+    ss = warp_sum(ss);
+    const float inv = rsqrtf(ss / HD + a.eps);
+    const float* w = kind == 0 ? a.w_q : (kind == 1 ? a.w_k : nullptr);
+#pragma unroll
+    for (int j = 0; j < J; ++j) v[j] *= inv * (w ? __ldg(w + lane + 32 * j) : 1.0f);
+  }
+  if (kind < 2) {
+    const int P = geo[b * kGeoInts + kGeoP];
+#pragma unroll
+    for (int j = 0; j < J / 2; ++j) {
+      float c, s;
+      rope_cs(P, a.rope_g[lane + 32 * j], c, s);
+      const float x0 = v[j], x1 = v[j + J / 2];
+      v[j] = x0 * c - x1 * s;
+      v[j + J / 2] = x0 * s + x1 * c;
+    }
+  }
+  if (kind == 0) {
+#pragma unroll
+    for (int j = 0; j < J; ++j) q_s[job * HD + lane + 32 * j] = v[j];
+    if (tap_q) {
+      float* qt = a.q_tap + ((size_t)b * a.nh + kvh * G + job) * HD;
+#pragma unroll
+      for (int j = 0; j < J; ++j) qt[lane + 32 * j] = v[j];
+    }
+  } else {
+    const int slot = geo[b * kGeoInts + kGeoSlot];
+    __nv_bfloat16* dst =
+        (kind == 1 ? a.k_cache : a.v_cache) + (((size_t)b * a.nkv + kvh) * a.C + slot) * HD;
+    float* tap = kind == 1 ? a.k_tap : a.v_tap;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      dst[lane + 32 * j] = __float2bfloat16_rn(v[j]);
+      if (tap) tap[((size_t)b * a.nkv + kvh) * HD + lane + 32 * j] = v[j];
+    }
+    // the row is read next by a TMA load (async proxy) of this CTA
+    fence_proxy_async_global();
+  }
+}
+
+// One K/V tile: S = Q K^T for the 16 keys of key group kg (queries of the group as bf16
+// hi rows 0..G-1 and lo rows 8..8+G-1), online softmax in base 2, O += P V with P split
+// hi/lo, for the n8 tiles of O of dim part dh.
+template <int HD>
+__device__ __forceinline__ void attn_tile(uint32_t kb, const uint4* qf, int key0, int k_end,
+                                          float cap_log2, float& m, float& l,
+                                          float (&o)[Attn<HD>::NTW][4], int kg, int dh,
+                                          int lane) {
+  using AC = Attn<HD>;
+  const uint32_t vb = kb + AC::TILE_BYTES;
+  const int krow = kg * kKeysPerWarp;
+  const int t = lane & 3;
+  float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int ks = 0; ks < AC::KS; ++ks) {
+    const uint4 qa = qf[ks * 32 + lane];
+    const uint32_t A[4] = {qa.x, qa.y, qa.z, qa.w};
+    const int mrow = krow + ((lane >> 4) << 3) + (lane & 7);
+    const int mchunk = ks * 2 + ((lane >> 3) & 1);
+    uint32_t b0, b1, b2, b3;
+    ldmatrix_x4(kb + swz<HD>(mrow, mchunk), b0, b1, b2, b3);
+    mma_bf16(s0, A, b0, b1);
+    mma_bf16(s1, A, b2, b3);
+  }
+  float sv[4] = {s0[0] + s0[2], s0[1] + s0[3], s1[0] + s1[2], s1[1] + s1[3]};
+  const int kidx0 = key0 + krow + 2 * t;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int key = kidx0 + (e & 1) + ((e >> 1) << 3);
+    float s = sv[e];
+    if (cap_log2 != 0.f) s = cap_log2 * tanhf(s);
+    sv[e] = key < k_end ? s : -INFINITY;
+  }
+  float mloc = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+  mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
+  mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
+  const float m_new = fmaxf(m, mloc);
+  const float m_use = m_new == -INFINITY ? 0.f : m_new;
+  const float corr = exp2f(m - m_use);
+  float p[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) p[e] = exp2f(sv[e] - m_use);
+  l = l * corr + (p[0] + p[1]) + (p[2] + p[3]);
+  m = m_new;
+#pragma unroll
+  for (int nt = 0; nt < AC::NTW; ++nt) {
+    o[nt][0] *= corr;
+    o[nt][1] *= corr;
+    o[nt][2] *= corr;
+    o[nt][3] *= corr;
+  }
+  uint32_t PA[4];
+  {
+    __nv_bfloat16 h[4], lw[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) split_bf16(p[e], h[e], lw[e]);
+    PA[0] = pack_bf2(h[0], h[1]);
+    PA[1] = pack_bf2(lw[0], lw[1]);
+    PA[2] = pack_bf2(h[2], h[3]);
+    PA[3] = pack_bf2(lw[2], lw[3]);
+  }
+#pragma unroll
+  for (int np = 0; np < AC::NTW / 2; ++np) {
+    const int mrow = krow + (((lane >> 3) & 1) << 3) + (lane & 7);
+    const int mchunk = (dh * (AC::NTW / 2) + np) * 2 + (lane >> 4);
+    uint32_t b0, b1, b2, b3;
+    ldmatrix_x4_trans(vb + swz<HD>(mrow, mchunk), b0, b1, b2, b3);
+    mma_bf16(o[2 * np], PA, b0, b1);
+    mma_bf16(o[2 * np + 1], PA, b2, b3);
+  }
+}
+
+// Order-preserving map of a float to 32 bits (larger float, larger unsigned).
+__device__ __forceinline__ unsigned float_order(float f) {
+  const unsigned u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float order_float(unsigned k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Phase C operand: the attention output over the columns of o_proj k-split s, for every
+// batch row, combined from the records of the CTAs that covered each unit:
+//   o = sum_r 2^(m_r - M) O_r / sum_r 2^(m_r - M) l_r,
+// M the largest m_r of the head (published with atomicMax by the record writers), then
+// split into fp16 hi + lo.  One thread per (batch row, column pair); all of its loads are
+// independent of one another.
+template <int HD, int NT>
+__device__ void build_o_operand(const StepArgs& a, const int* geo, int s, int Nt, bool tap,
+                                uint32_t* xw) {
+  using AC = Attn<HD>;
+  const int nbs = a.o.nbs;
+  const int ncols = nbs * 32, col0 = s * ncols;
+  const int G = a.nh / a.nkv;
+  const int nctas = gridDim.x;
+  const int npair = ncols / 2;
+  for (int i = threadIdx.x; i < nbs * NT * 32 * 4; i += kConsumers) xw[i] = 0u;
+  consumer_sync();
+  for (int e = threadIdx.x; e < a.B * npair; e += kConsumers) {
+    const int b = e / npair, cc = 2 * (e - b * npair);  // column pair (cc, cc + 1) of the split
+    const int col = col0 + cc;
+    const int h = col / HD, d = col - h * HD;
+    const int kvh = h / G, hl = h - kvh * G;
+    const int u = b * a.nkv + kvh;
+    const int nt = geo[b * kGeoInts + kGeoNt];
+    float2 acc = make_float2(0.f, 0.f);
+    float den = 0.f;
+    if (nt > 0) {
+      int pre = kvh * nt;
+      for (int bb = 0; bb < b; ++bb) pre += a.nkv * geo[bb * kGeoInts + kGeoNt];
+      const int cf = part_of(pre, Nt, nctas);
+      const int nrec = part_of(pre + nt - 1, Nt, nctas) - cf + 1;
+      const unsigned long long key = __ldcg(a.gmax + (size_t)b * a.nh + h);
+      const float M = (unsigned)(key >> 32) == a.step ? order_float((unsigned)key) : 0.f;
+      const float* rp = a.rec + ((size_t)(cf + u) * 8 + hl) * AC::RS;
+#pragma unroll 8
+      for (int r = 0; r < nrec; ++r, rp += 8 * AC::RS) {
+        const float mr = __ldcg(rp + HD), lr = __ldcg(rp + HD + 1);
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(rp + d));
+        const float w = exp2f(mr - M);
+        den += w * lr;
+        acc.x += w * v.x;
+        acc.y += w * v.y;
+      }
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    acc.x *= inv;
+    acc.y *= inv;
+    __half hx, lx, hy, ly;
+    split_f16(acc.x, hx, lx);
+    split_f16(acc.y, hy, ly);
+    const int w = operand_word<NT>(cc, b);
+    xw[w] = pack_h2(hx, hy);
+    xw[w + 16] = pack_h2(lx, ly);
+    if (tap) *reinterpret_cast<float2*>(a.o_tap + ((size_t)b * a.nh + h) * HD + d) = acc;
+  }
+  consumer_sync();
+}
+
+// ------------------------------------------------------------------ the load schedule
+// A CTA's loads in order: the stages of its QKV slice (phase A), its K/V tiles (phase B),
+// the stages of its o_proj slice (phase C).  Load j can also be prefetched into L2 by
+// its byte ranges: the first kEarlyTiles K/V tiles go to L2 while phase A still holds the
+// ring, so HBM keeps streaming through the phase A tail and the grid barrier.  Deeper
+// prefetching only lengthens the queues that the step's latency-bound parts (barriers,
+// the head epilogue, the record merge) wait in, and thrashes L2 on long contexts.
+struct Schedule {
+  Slice sa, so;
+  int nA, nB, nC;
+  int t0, t1;  // global key tiles [t0, t1)
+};
+
+__device__ __forceinline__ int gemv_loads(const StepGemv& g, const Slice& sl) {
+  return (sl.r1 - sl.r0 + g.ips - 1) / g.ips;
+}
+
+template <int HD>
+__device__ void prefetch_load(const StepArgs& a, const Schedule& sc, const int* geo, int j) {
+  using AC = Attn<HD>;
+  if (j < sc.nA || j >= sc.nA + sc.nB) {
+    const bool in_a = j < sc.nA;
+    const StepGemv& g = in_a ? a.qkv : a.o;
+    const Slice& sl = in_a ? sc.sa : sc.so;
+    const int r = sl.r0 + (in_a ? j : j - sc.nA - sc.nB) * g.ips;
+    const int n = g.ips < sl.r1 - r ? g.ips : sl.r1 - r;
+    prefetch_bulk_l2(g.w + ((size_t)sl.s * g.R + r) * g.nbs * kQ8TileBytes,
+                     (uint32_t)(n * g.nbs * kQ8TileBytes));
+    return;
+  }
+  int t = sc.t0 + (j - sc.nA);  // global tile -> (b, kvh, tile)
+  for (int b = 0; b < a.B; ++b) {
+    const int nt = geo[b * kGeoInts + kGeoNt];
+    if (t < nt * a.nkv) {
+      const int kvh = t / nt, lt = t - kvh * nt;
+      const long long row = (long long)(b * a.nkv + kvh) * a.C + geo[b * kGeoInts + kGeoLo] +
+                            (long long)lt * AC::T;
+      long long nrow = AC::T;
+      if (row + nrow > a.cache_rows) nrow = a.cache_rows - row;  // last tile of the cache
+      if (nrow > 0) {
+        const uint32_t bytes = (uint32_t)(nrow * HD * 2);
+        prefetch_bulk_l2(a.k_cache + row * HD, bytes);
+        prefetch_bulk_l2(a.v_cache + row * HD, bytes);
+      }
+      return;
+    }
+    t -= nt * a.nkv;
+  }
+}
+
+// ------------------------------------------------------------------ the kernel
+template <int HD, int NT>
+__global__ void __launch_bounds__(kThreads, 1)
+    step_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                const StepArgs a) {
+  using AC = Attn<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~(uintptr_t)1023);
+  uint8_t* ring = smem;
+  uint8_t* uni = smem + kStages * kStageBytes;
+  uint8_t* small = uni + kUnionBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(small);
+  uint64_t* empty = full + kStages;
+  uint64_t* append_bar = empty + kStages;
+  volatile int* s_abort = reinterpret_cast<volatile int*>(small + 64);
+  int* s_issued = reinterpret_cast<int*>(small + 68);
+  unsigned* s_max = reinterpret_cast<unsigned*>(small + 96);
+  float* s_ssq = reinterpret_cast<float*>(small + 160);
+  float* s_inv = reinterpret_cast<float*>(small + 224);
+  int* geo = reinterpret_cast<int*>(small + 512);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c = blockIdx.x, nctas = gridDim.x;
+  const int G = a.nh / a.nkv;
+  if (blockDim.x != kThreads || a.B > kMaxBatch) {
+    if (tid == 0) atomicOr(a.err, kErrBadPlan);
+    return;
+  }
+
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kCW);
+    }
+    mbar_init(append_bar, 1);
+    *s_abort = 0;
+    *s_issued = 0;
+    fence_barrier_init();
+  }
+  if (tid < kMaxBatch) {
+    s_max[tid] = 0u;
+    s_ssq[tid] = 0.f;
+  }
+  __syncthreads();
+
+  if (warp == kCW) {
+    // ============================================================== producer
+    Schedule sc;
+    sc.sa = gemv_slice(a.qkv, c, nctas);
+    sc.so = gemv_slice(a.o, c, nctas);
+    sc.nA = gemv_loads(a.qkv, sc.sa);
+    sc.nC = gemv_loads(a.o, sc.so);
+    uint32_t q = 0;
+    bool ok = true;
+    auto acquire = [&](uint32_t bytes) -> int {
+      const int st = (int)(q % kStages);
+      if (q >= (uint32_t)kStages &&
+          !mbar_wait(&empty[st], ((q / kStages) - 1) & 1, a.err, s_abort)) {
+        *s_abort = 1;
+        return -1;
+      }
+      if (*s_abort) return -1;
+      mbar_arrive_expect_tx(&full[st], bytes);
+      return st;
+    };
+    auto issue_gemv = [&](const StepGemv& g, const Slice& sl, int k) {
+      const int r = sl.r0 + k * g.ips;
+      const int n = g.ips < sl.r1 - r ? g.ips : sl.r1 - r;
+      const uint32_t bytes = (uint32_t)(n * g.nbs * kQ8TileBytes);
+      const int st = acquire(bytes);
+      if (st < 0) {
+        ok = false;
+        return;
+      }
+      bulk_load(ring + st * kStageBytes, g.w + ((size_t)sl.s * g.R + r) * g.nbs * kQ8TileBytes,
+                bytes, &full[st]);
+      ++q;
+    };
+    // phase A depends on nothing of this step: its first stages go out first
+    if (lane == 0) {
+      for (int k = 0; k < sc.nA && k < kStages && ok; ++k) issue_gemv(a.qkv, sc.sa, k);
+      prefetch_tmap(&tmk);
+      prefetch_tmap(&tmv);
+    }
+    __syncwarp();
+    // visible slots and key tiles of each sequence, for both sides (consumers read them
+    // after barrier 2)
+    if (lane < a.B) {
+      const int b = lane;
+      const int P = a.seq_pos[b];
+      const bool bad = P < 0 || (!a.ring && P >= a.C);
+      int lo, hi, slot;
+      if (a.ring) {
+        lo = 0;
+        hi = P < a.C - 1 ? P : a.C - 1;
+        slot = bad ? 0 : P % a.C;
+      } else {
+        lo = a.sliding ? (P - a.window + 1 > 0 ? P - a.window + 1 : 0) : 0;
+        hi = P;
+        slot = P;
+      }
+      int* gb = geo + b * kGeoInts;
+      gb[kGeoP] = P;
+      gb[kGeoLo] = lo;
+      gb[kGeoHi] = hi;
+      gb[kGeoNt] = bad ? 0 : (hi - lo + 1 + AC::T - 1) / AC::T;
+      gb[kGeoTn] = bad ? -1 : (slot - lo) / AC::T;
+      gb[kGeoSlot] = slot;
+      if (bad && c == 0) atomicOr(a.err, kErrBadPosition);
+    }
+    __syncwarp();
+    asm volatile("bar.arrive 2, %0;" ::"n"(kThreads) : "memory");
+    if (lane == 0) {
+      int Nt = 0;
+      for (int b = 0; b < a.B; ++b) Nt += geo[b * kGeoInts + kGeoNt] * a.nkv;
+      sc.t0 = Nt > 0 ? part_begin(c, Nt, nctas) : 0;
+      sc.t1 = Nt > 0 ? part_begin(c + 1, Nt, nctas) : 0;
+      sc.nB = sc.t1 - sc.t0;
+      uint32_t n_app = 0;  // appends waited for (one per unit whose new slot is here)
+      for (int j = 0; j < kEarlyTiles && j < sc.nB; ++j) prefetch_load<HD>(a, sc, geo, sc.nA + j);
+      for (int k = (int)q; k < sc.nA && ok; ++k) issue_gemv(a.qkv, sc.sa, k);
+      for_each_segment(geo, a.B, a.nkv, sc.t0, sc.t1, [&](int b, int kvh, int lt0, int lt1) {
+        const int lo = geo[b * kGeoInts + kGeoLo], tn = geo[b * kGeoInts + kGeoTn];
+        const bool owner = tn >= lt0 && tn < lt1;
+        const int row_base = (b * a.nkv + kvh) * a.C + lo;
+        for (int i = 0; ok && i < lt1 - lt0; ++i) {
+          const int lt = seg_tile(i, lt0, lt1, owner ? tn : -1);
+          if (owner && lt == tn) {
+            // the slot appended in this step: its row is written by this CTA's consumers
+            if (!mbar_wait(append_bar, n_app & 1, a.err, s_abort)) {
+              *s_abort = 1;
+              ok = false;
+              break;
+            }
+            ++n_app;
+          }
+          const int st = acquire(AC::STAGE_BYTES);
+          if (st < 0) {
+            ok = false;
+            break;
+          }
+          uint8_t* kt = ring + st * kStageBytes;
+          uint8_t* vt = kt + AC::TILE_BYTES;
+          const int row = row_base + lt * AC::T;
+#pragma unroll
+          for (int j = 0; j < AC::BOXES; ++j) {
+            tma_load_2d(kt + j * AC::T * 128, &tmk, &full[st], 64 * j, row);
+            tma_load_2d(vt + j * AC::T * 128, &tmv, &full[st], 64 * j, row);
+          }
+          ++q;
+        }
+      });
+      for (int k = 0; k < sc.nC && ok; ++k) issue_gemv(a.o, sc.so, k);
+      *s_issued = (int)q;
+    }
+  } else {
+    // ============================================================== consumers
+    uint32_t q = 0;
+    auto wait_stage = [&]() -> int {
+      const int st = (int)(q % kStages);
+      const bool ok = mbar_wait(&full[st], (q / kStages) & 1, a.err, s_abort);
+      if (!ok) *s_abort = 1;
+      return ok ? st : -1;
+    };
+    auto release_stage = [&]() {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[q % kStages]);
+      ++q;
+    };
+
+    // ---------------------------------------------------------- A: QKV
+    {
+      const Slice sl = gemv_slice(a.qkv, c, nctas);
+      build_x_operand<NT>(a, sl.s, sl.first, reinterpret_cast<uint32_t*>(uni), s_max, s_ssq,
+                          s_inv);
+      for (int r = sl.r0; r < sl.r1; r += a.qkv.ips) {
+        const int n = a.qkv.ips < sl.r1 - r ? a.qkv.ips : sl.r1 - r;
+        const int st = wait_stage();
+        if (st >= 0)
+          gemv_stage<NT, false>(a, a.qkv, sl.s, ring + st * kStageBytes, n, r,
+                                reinterpret_cast<const uint4*>(uni), s_inv, warp, lane);
+        release_stage();
+      }
+    }
+    grid_sync(a.gbar, a.gbar_base + nctas, a.err, s_abort);
+
+    // ---------------------------------------------------------- B: attention
+    asm volatile("bar.sync 2, %0;" ::"n"(kThreads) : "memory");  // geometry is in
+    int Nt = 0;
+    for (int b = 0; b < a.B; ++b) Nt += geo[b * kGeoInts + kGeoNt] * a.nkv;
+    const int t0 = Nt > 0 ? part_begin(c, Nt, nctas) : 0;
+    const int t1 = Nt > 0 ? part_begin(c + 1, Nt, nctas) : 0;
+    {
+      uint4* qf = reinterpret_cast<uint4*>(uni);
+      float* q_s = reinterpret_cast<float*>(uni + AC::QS_OFF);
+      float* red = reinterpret_cast<float*>(uni);  // [key group][8][RS] after the last tile
+      const uint32_t ring_base = smem_u32(ring);
+      for_each_segment(geo, a.B, a.nkv, t0, t1, [&](int b, int kvh, int lt0, int lt1) {
+        const int* gb = geo + b * kGeoInts;
+        const int lo = gb[kGeoLo], hi = gb[kGeoHi], tn = gb[kGeoTn];
+        const bool owner = tn >= lt0 && tn < lt1;
+        const int unit = b * a.nkv + kvh;
+        const int njobs = G + (owner ? 2 : 0);
+        for (int job = warp; job < njobs; job += kCW)
+          head_job<HD>(a, geo, b, kvh, job, G, q_s, lt0 == 0 && a.q_tap != nullptr, lane);
+        consumer_sync();
+        if (owner && tid == 0) mbar_arrive(append_bar);
+        // query fragments: rows 0..G-1 = hi(q * qscale), rows 8..8+G-1 = lo
+        {
+          const int g = lane >> 2, t = lane & 3;
+          for (int ks = warp; ks < AC::KS; ks += kCW) {
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
+            if (g < G) {
+              const float* qr = q_s + g * HD + ks * 16 + 2 * t;
+              __nv_bfloat16 h[4], l[4];
+              split_bf16(qr[0] * a.qscale, h[0], l[0]);
+              split_bf16(qr[1] * a.qscale, h[1], l[1]);
+              split_bf16(qr[8] * a.qscale, h[2], l[2]);
+              split_bf16(qr[9] * a.qscale, h[3], l[3]);
+              w[0] = pack_bf2(h[0], h[1]);
+              w[1] = pack_bf2(l[0], l[1]);
+              w[2] = pack_bf2(h[2], h[3]);
+              w[3] = pack_bf2(l[2], l[3]);
+            }
+            qf[ks * 32 + lane] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        consumer_sync();
+        const int kg = warp % AC::NC, dh = warp / AC::NC;  // key group, dim part
+        float m = -INFINITY, l = 0.f;
+        float o[AC::NTW][4];
+#pragma unroll
+        for (int i = 0; i < AC::NTW; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+        for (int i = 0; i < lt1 - lt0; ++i) {
+          const int lt = seg_tile(i, lt0, lt1, owner ? tn : -1);
+          const int st = wait_stage();
+          if (st >= 0)
+            attn_tile<HD>(ring_base + st * kStageBytes, qf, lo + lt * AC::T, hi + 1, a.cap_log2,
+                          m, l, o, kg, dh, lane);
+          release_stage();
+        }
+        l += __shfl_xor_sync(0xffffffffu, l, 1);
+        l += __shfl_xor_sync(0xffffffffu, l, 2);
+        // combine the warps of this CTA into the unit's record of this CTA
+        consumer_sync();
+        {
+          const int g = lane >> 2, t = lane & 3;
+          float* mine = red + kg * 8 * AC::RS;
+          if (g < G) {
+            if (t == 0 && dh == 0) {
+              mine[g * AC::RS + HD] = m;
+              mine[g * AC::RS + HD + 1] = l;
+            }
+#pragma unroll
+            for (int nt = 0; nt < AC::NTW; ++nt) {
+              const int d = (dh * AC::NTW + nt) * 8 + 2 * t;
+              mine[g * AC::RS + d] = o[nt][0] + o[nt][2];
+              mine[g * AC::RS + d + 1] = o[nt][1] + o[nt][3];
+            }
+          }
+        }
+        consumer_sync();
+        float* rec = a.rec + (size_t)(c + unit) * 8 * AC::RS;
+        for (int e = tid; e < G * (HD + 2); e += kConsumers) {
+          const int h = e / (HD + 2), d = e - h * (HD + 2);
+          float M = -INFINITY;
+#pragma unroll
+          for (int w = 0; w < AC::NC; ++w) M = fmaxf(M, red[(w * 8 + h) * AC::RS + HD]);
+          const float Mu = M == -INFINITY ? 0.f : M;
+          float acc = 0.f;
+          if (d == HD) {
+            acc = M;
+          } else {
+#pragma unroll
+            for (int w = 0; w < AC::NC; ++w)
+              acc += exp2f(red[(w * 8 + h) * AC::RS + HD] - Mu) * red[(w * 8 + h) * AC::RS + d];
+          }
+          rec[h * AC::RS + d] = acc;
+          if (d == HD)
+            atomicMax(a.gmax + (size_t)b * a.nh + kvh * G + h,
+                      ((unsigned long long)a.step << 32) | float_order(M));
+        }
+        consumer_sync();
+      });
+      // A CTA without tiles (fewer tiles than CTAs) that sits inside a unit's run of
+      // CTAs leaves a zero-weight record there, so that the combine reads no stale one.
+      if (t0 == t1 && t0 < Nt) {
+        int t = t0, b = 0;
+        while (t >= geo[b * kGeoInts + kGeoNt] * a.nkv) t -= geo[b++ * kGeoInts + kGeoNt] * a.nkv;
+        const int unit = b * a.nkv + t / geo[b * kGeoInts + kGeoNt];
+        float* rec = a.rec + (size_t)(c + unit) * 8 * AC::RS;
+        for (int e = tid; e < 8 * AC::RS; e += kConsumers) {
+          const int d = e % AC::RS;
+          rec[e] = d == HD ? -INFINITY : 0.f;
+        }
+      }
+    }
+    grid_sync(a.gbar, a.gbar_base + 2ull * nctas, a.err, s_abort);
+
+    // ---------------------------------------------------------- C: o_proj + residual
+    {
+      const Slice sl = gemv_slice(a.o, c, nctas);
+      build_o_operand<HD, NT>(a, geo, sl.s, Nt, sl.first && a.o_tap != nullptr,
+                              reinterpret_cast<uint32_t*>(uni));
+      for (int r = sl.r0; r < sl.r1; r += a.o.ips) {
+        const int n = a.o.ips < sl.r1 - r ? a.o.ips : sl.r1 - r;
+        const int st = wait_stage();
+        if (st >= 0)
+          gemv_stage<NT, true>(a, a.o, sl.s, ring + st * kStageBytes, n, r,
+                               reinterpret_cast<const uint4*>(uni), s_inv, warp, lane);
+        release_stage();
+      }
+    }
+  }
+
+  // drain: after a give-up, copies may still be landing in the ring
+  __syncthreads();
+  if (tid == 0 && *s_abort) {
+    const int issued = *s_issued;
+    for (int st = 0; st < kStages && st < issued; ++st) {
+      const int last = st + ((issued - 1 - st) / kStages) * kStages;
+      mbar_wait(&full[st], (last / kStages) & 1, a.err);
+    }
+  }
+}
+
+template <int HD, int NT>
+cudaError_t launch_step_t(const StepArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                          int grid, cudaStream_t s) {
+  auto kern = step_kernel<HD, NT>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tk, tv, a);
+}
+
+template <int HD>
+cudaError_t launch_step_hd(const StepArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                           int grid, cudaStream_t s) {
+  const int nt = a.B <= 4 ? 1 : (a.B <= 8 ? 2 : 4);
+  if (nt == 1) return launch_step_t<HD, 1>(a, tk, tv, grid, s);
+  if (nt == 2) return launch_step_t<HD, 2>(a, tk, tv, grid, s);
+  return launch_step_t<HD, 4>(a, tk, tv, grid, s);
+}
+
+}  // namespace step
+}  // namespace hfa

@@ -255,8 +255,8 @@ class Layer:
     def hfa_plan_info(self) -> Dict[str, int]:
         v = (ctypes.c_int * 5)()
         lib().hfa_plan_info(self._h, 5, v)
-        return {"attn_splits": v[0], "keys_per_stage": v[1], "gemv_grid": v[2],
-                "attn_grid": v[3], "num_sms": v[4]}
+        return {"attn_tiles": v[0], "keys_per_tile": v[1], "step_grid": v[2],
+                "num_sms": v[4]}
 
     def hfa_destroy(self) -> None:
         if self._h:
