@@ -67,9 +67,7 @@ struct hfa_layer {
   unsigned long long* attn_gmax = nullptr;
   float* o_f32 = nullptr;
   float* y_part = nullptr;
-  int* row_ticket = nullptr;
   unsigned long long* gbar = nullptr;
-  unsigned long long steps_launched = 0;  // decode steps launched (grid barrier epoch)
   float* k_tap = nullptr;
   float* v_tap = nullptr;
   float* out_tap = nullptr;
@@ -379,7 +377,6 @@ extern "C" hfa_status hfa_layer_create(const hfa_layer_desc* desc, const void* w
   LA(L->gbar, 1);
   LA(L->attn_gmax, (size_t)d.max_batch * nh);
   LA(L->o_f32, (size_t)MR * nh * hd);
-  LA(L->row_ticket, H / 16);
   LA(L->err, 1);
   LA(L->x_stage, (size_t)d.max_batch * H);
   LA(L->pos_stage, d.max_batch);
@@ -395,7 +392,6 @@ extern "C" hfa_status hfa_layer_create(const hfa_layer_desc* desc, const void* w
 
   LC(cudaMemsetAsync(L->gbar, 0, 8, s), "memset");
   LC(cudaMemsetAsync(L->attn_gmax, 0, (size_t)d.max_batch * nh * 8, s), "memset");
-  LC(cudaMemsetAsync(L->row_ticket, 0, H / 16 * 4, s), "memset");
   LC(cudaMemsetAsync(L->err, 0, 4, s), "memset");
   if (d.max_verify_len > 0) {
     hfa_status vs = hfa::verify_create(L->d, L->num_sms, &L->verify);
@@ -530,11 +526,8 @@ extern "C" hfa_status hfa_decode_step(hfa_layer* L, void* stream, const void* x,
   sa.ss_part = L->ss_part;
   sa.rec = L->attn_rec;
   sa.y_part = L->y_part;
-  sa.row_ticket = L->row_ticket;
   sa.gbar = L->gbar;
-  sa.gbar_base = 2ull * (unsigned long long)L->num_sms * L->steps_launched;
   sa.gmax = L->attn_gmax;
-  sa.step = (unsigned)(L->steps_launched + 1);
   sa.err = L->err;
   sa.q_tap = taps ? L->q_f32 : nullptr;
   sa.k_tap = L->k_tap;
@@ -572,7 +565,6 @@ extern "C" hfa_status hfa_decode_step(hfa_layer* L, void* stream, const void* x,
   cudaError_t e = launch_step(sa, L->tm_k, L->tm_v, hd, L->num_sms, s);
   timer_end(L, s, &t);
   if (e != cudaSuccess) return cuda_fail(L, e, "decode-step kernel launch");
-  ++L->steps_launched;
   L->last_rows = batch;
   return HFA_OK;
 }
@@ -783,7 +775,6 @@ extern "C" hfa_status hfa_check_device_status(hfa_layer* L, void* stream) {
     CK(L, cudaMemsetAsync(L->attn_gmax, 0, (size_t)L->d.max_batch * L->d.num_heads * 8, s),
        "reset record maxima");
   CK(L, cudaStreamSynchronize(s), "sync");
-  L->steps_launched = 0;
   CK(L, cudaStreamSynchronize(s), "sync");
   return fail(L, HFA_EDEVICE, "device status 0x%x:%s%s%s", v,
               (v & kErrWaitTimeout) ? " a bounded wait gave up;" : "",

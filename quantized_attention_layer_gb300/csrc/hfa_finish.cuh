@@ -44,9 +44,12 @@ static __device__ void finish_head(const GemvArgs& a, int hh, int lane) {
       for (int j = 0; j < J; ++j) ss += v[j] * v[j];
       ss = warp_sum(ss);
       const float inv = rsqrtf(ss / HD + a.eps);
-      const float* w = kind == 0 ? a.w_q : (kind == 1 ? a.w_k : nullptr);
+      const float* w = kind == 0 ? a.w_q : a.w_k;  // a valid address for v too (unused)
 #pragma unroll
-      for (int j = 0; j < J; ++j) v[j] *= inv * (w ? __ldg(w + lane + 32 * j) : 1.0f);
+      for (int j = 0; j < J; ++j) {
+        const float wj = __ldg(w + lane + 32 * j);
+        v[j] *= inv * (kind < 2 ? wj : 1.0f);
+      }
     }
     if (kind < 2) {
 #pragma unroll

@@ -88,11 +88,9 @@ struct StepArgs {
   float* ss_part;          // f32 [qkv.S][16]: sum of x^2 over each k-split's columns
   float* rec;              // f32 [(grid + B nkv)][8][hd + 4]: (O, m, l) per key range
   float* y_part;           // f32 [o.S][B][H]: one partial o_proj sum per k-split
-  int* row_ticket;         // [H / 16]: zero on entry and on exit
   unsigned long long* gmax;  // [B * nh]: (step << 32) | ordered(max logit) over the records
-  unsigned step;           // this step's number (nonzero), the high word of gmax
-  unsigned long long* gbar;  // grid barrier arrivals (monotonic, two per CTA per step)
-  unsigned long long gbar_base;  // arrivals before this step: 2 * grid * steps so far
+  unsigned long long* gbar;  // grid barrier arrivals: only grows, three per CTA per step, so
+                             // it also numbers the steps (graph replays included)
   unsigned* err;
   float* q_tap;            // nullable f32 [B, nh, hd] (q after RoPE)
   float* k_tap;            // nullable f32 [B, nkv, hd]

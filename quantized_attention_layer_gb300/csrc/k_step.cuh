@@ -81,6 +81,22 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
 __device__ __forceinline__ void red_release_add_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
+// L2 loads the compiler keeps in place: never issued ahead of the branch that guards them
+__device__ __forceinline__ float ldcg_pinned(const float* p) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ unsigned long long ldcg_pinned64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.global.cg.u64 %0, [%1];" : "=l"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float2 ldcg_pinned2(const float* p) {
+  float2 v;
+  asm volatile("ld.global.cg.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
+  return v;
+}
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -91,11 +107,16 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 }
 
 // Balanced partition of n items over P parts: part c owns [begin(c), begin(c + 1)).
+// 32-bit arithmetic whenever the products fit (64-bit division is a long software
+// sequence, and every CTA runs these before its first load).
 __device__ __forceinline__ int part_begin(int c, long long n, int P) {
+  if (n < (1ll << 24) && P <= 256) return (int)((unsigned)c * (unsigned)n / (unsigned)P);
   return (int)((long long)c * n / P);
 }
 // the part that owns item t (0 <= t < n): the largest c with begin(c) <= t
 __device__ __forceinline__ int part_of(int t, long long n, int P) {
+  if (n < (1ll << 24) && P <= 256)
+    return (int)(((unsigned)(t + 1) * (unsigned)P - 1u) / (unsigned)n);
   return (int)(((long long)(t + 1) * P - 1) / n);
 }
 
@@ -148,10 +169,11 @@ __device__ __forceinline__ int seg_tile(int i, int lt0, int lt1, int tn) {
 }
 
 // Grid barrier of the consumer warps (the producer runs ahead and never joins).  The
-// arrival counter only grows: barrier k (0, 1) of a step completes when it reaches
-// base + (k + 1) * grid, base being the arrivals of all earlier steps.  Arrival is one
-// release reduction (no round trip); a CTA that has given up arrives without waiting, so
-// the count stays exact.
+// arrival counter only grows: barrier k (0, 1, 2) of a step completes when it reaches
+// base + (k + 1) * grid, base = 3 * grid * (steps before this one), which every CTA reads
+// off the counter at its start (the count is then inside [base, base + 3 grid)).
+// Arrival is one release reduction (no round trip); a CTA that has given up arrives
+// without waiting, so the count stays exact.
 __device__ __forceinline__ void grid_sync(unsigned long long* gbar, unsigned long long target,
                                           unsigned* err, volatile int* abort) {
   consumer_sync();
@@ -233,35 +255,46 @@ __device__ void build_x_operand(const StepArgs& a, int s, bool add_ss, uint32_t*
   const int nbs = a.qkv.nbs;
   const int groups = nbs * 4;  // 8-column groups per batch row
   const int total = NT * 4 * groups;
+  // every load first (x rows and w_in of all NT groups of this thread), then the math
+  uint4 raw[NT];
+  float4 w0[NT], w1[NT];
+#pragma unroll
+  for (int k = 0; k < NT; ++k) {
+    const int e = tid + k * kConsumers;
+    const int b = e / groups, gi = e - b * groups;
+    const bool live = e < total && b < a.B;
+    // addresses stay in range for the lanes without a live group
+    const int bx = live ? b : 0;
+    const int col = s * nbs * 32 + (live ? gi : 0) * 8;
+    raw[k] = *reinterpret_cast<const uint4*>(a.x + (size_t)bx * a.H + col);
+    w0[k] = __ldg(reinterpret_cast<const float4*>(a.w_in + col));
+    w1[k] = __ldg(reinterpret_cast<const float4*>(a.w_in + col + 4));
+  }
   float v[NT][8];
 #pragma unroll
   for (int k = 0; k < NT; ++k) {
     const int e = tid + k * kConsumers;
+    const int b = e / groups;
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[k][i] = 0.f;
-    if (e < total) {
-      const int b = e / groups, gi = e - b * groups;
-      if (b < a.B) {
-        const int col = s * nbs * 32 + gi * 8;
-        const uint4 raw = *reinterpret_cast<const uint4*>(a.x + (size_t)b * a.H + col);
-        const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.w_in + col));
-        const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.w_in + col + 4));
-        const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
-        float mx = 0.f, ss = 0.f;
+    if (e < total && b < a.B) {
+      const float wv[8] = {w0[k].x, w0[k].y, w0[k].z, w0[k].w, w1[k].x, w1[k].y, w1[k].z, w1[k].w};
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[k]);
+      float mx = 0.f, ss = 0.f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = __bfloat1622float2(h[i]);
-          v[k][2 * i] = f.x * wv[2 * i];
-          v[k][2 * i + 1] = f.y * wv[2 * i + 1];
-          ss += f.x * f.x + f.y * f.y;
-          mx = fmaxf(mx, fmaxf(fabsf(v[k][2 * i]), fabsf(v[k][2 * i + 1])));
-        }
-        atomicMax(&s_max[b], __float_as_uint(mx));
-        if (add_ss) atomicAdd(&s_ssq[b], ss);
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        v[k][2 * i] = f.x * wv[2 * i];
+        v[k][2 * i + 1] = f.y * wv[2 * i + 1];
+        ss += f.x * f.x + f.y * f.y;
+        mx = fmaxf(mx, fmaxf(fabsf(v[k][2 * i]), fabsf(v[k][2 * i + 1])));
       }
+      atomicMax(&s_max[b], __float_as_uint(mx));
+      if (add_ss) atomicAdd(&s_ssq[b], ss);
     }
   }
+  // the activations are in registers: the producer may start the weight stream
+  asm volatile("bar.arrive 3, %0;" ::"n"(kThreads) : "memory");
   consumer_sync();
 #pragma unroll
   for (int k = 0; k < NT; ++k) {
@@ -287,26 +320,53 @@ __device__ void build_x_operand(const StepArgs& a, int s, bool add_ss, uint32_t*
   consumer_sync();
 }
 
-// Epilogue of one o_proj row group once every k-split has stored its partial sums:
-// out = bf16(x + sum over the splits), the splits added in a fixed order.
-__device__ __forceinline__ void finish_rows(const StepArgs& a, int r, int lane) {
-  if (lane == 0) a.row_ticket[r] = 0;
-  for (int i = lane; i < 16 * a.B; i += 32) {
-    const int b = i >> 4, row = r * 16 + (i & 15);
-    const float* p = a.y_part + (size_t)b * a.H + row;
-    const size_t split_stride = (size_t)a.B * a.H;
-    float y = 0.f;
-#pragma unroll 8
-    for (int s = 0; s < a.o.S; ++s) y += __ldcg(p + s * split_stride);
-    const float o = __bfloat162float(a.x[(size_t)b * a.H + row]) + y;
-    a.out[(size_t)b * a.H + row] = __float2bfloat16_rn(o);
-    if (a.out_tap) a.out_tap[(size_t)b * a.H + row] = o;
+// Residual epilogue after the last grid barrier: CTA c finishes its share of the B x H
+// outputs, out = bf16(x + sum over the o_proj k-splits), the splits added in a fixed
+// order; each thread issues all of its partial-sum loads before adding.
+__device__ __forceinline__ void finish_outputs(const StepArgs& a, int c, int nctas) {
+  constexpr int kMaxPer = 8;  // outputs per thread per round
+  const long long n = (long long)a.B * a.H;
+  const int i0 = part_begin(c, n, nctas), i1 = part_begin(c + 1, n, nctas);
+  const size_t split_stride = (size_t)a.B * a.H;
+  for (int base = i0; base < i1; base += kMaxPer * kConsumers) {
+    float y[kMaxPer];
+#pragma unroll
+    for (int k = 0; k < kMaxPer; ++k) y[k] = 0.f;
+    for (int s0 = 0; s0 < a.o.S; s0 += 4) {
+      float t[4][kMaxPer];  // every load of four splits issued before the first add
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int s = s0 + u < a.o.S ? s0 + u : a.o.S - 1;
+#pragma unroll
+        for (int k = 0; k < kMaxPer; ++k) {
+          const int i = base + threadIdx.x + k * kConsumers;
+          t[u][k] = __ldcg(a.y_part + s * split_stride + (i < i1 ? i : i1 - 1));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (s0 + u < a.o.S)
+#pragma unroll
+          for (int k = 0; k < kMaxPer; ++k) {
+            const int i = base + threadIdx.x + k * kConsumers;
+            if (i < i1) y[k] += t[u][k];
+          }
+    }
+#pragma unroll
+    for (int k = 0; k < kMaxPer; ++k) {
+      const int i = base + threadIdx.x + k * kConsumers;
+      const float xi = __bfloat162float(a.x[i < i1 ? i : i1 - 1]);
+      if (i < i1) {
+        const float o = xi + y[k];
+        a.out[i] = __float2bfloat16_rn(o);
+        if (a.out_tap) a.out_tap[i] = o;
+      }
+    }
   }
 }
 
 // Partial sums of rows [16 r, 16 r + 16) over the nbs tiles of k-split s: stored (no
-// atomics) into the split's slice of the partial-sum buffer.  For o_proj the last of the
-// S items of a row group (ticket) adds the splits up.
+// atomics) into the split's slice of the partial-sum buffer.
 template <int NT, bool OPROJ>
 __device__ __forceinline__ void gemv_flush(const StepArgs& a, const StepGemv& gm,
                                            float (&acc)[NT][4], int s, int r,
@@ -322,13 +382,6 @@ __device__ __forceinline__ void gemv_flush(const StepArgs& a, const StepGemv& gm
       dst[(size_t)b * R16 + r * 16 + g] = (acc[nt][0] + acc[nt][1]) * f;
       dst[(size_t)b * R16 + r * 16 + g + 8] = (acc[nt][2] + acc[nt][3]) * f;
     }
-  }
-  if (OPROJ) {
-    __syncwarp();
-    int done = 0;
-    if (lane == 0) done = atom_add_acq_rel(a.row_ticket + r, 1) + 1 == gm.S;
-    done = __shfl_sync(0xffffffffu, done, 0);
-    if (done) finish_rows(a, r, lane);
   }
 }
 
@@ -375,17 +428,31 @@ __device__ void head_job(const StepArgs& a, const int* geo, int b, int kvh, int 
   const int kind = job < G ? 0 : (job == G ? 1 : 2);
   const int row0 = kind == 0 ? (kvh * G + job) * HD
                              : (kind == 1 ? (a.nh + kvh) * HD : (a.nh + a.nkv + kvh) * HD);
-  // the projection: partial sums of the k-splits added in a fixed order
+  // the projection: partial sums of the k-splits added in a fixed order, every load of a
+  // group of kSG splits issued before the first add
+  constexpr int kSG = 8;
   const float* src = a.qkv_part + (size_t)b * rows + row0 + lane;
   const size_t split_stride = (size_t)a.B * rows;
   float v[J];
 #pragma unroll
   for (int j = 0; j < J; ++j) v[j] = 0.f;
   float ssx = 0.f;
-  for (int s = 0; s < a.qkv.S; ++s) {
+  for (int s0 = 0; s0 < a.qkv.S; s0 += kSG) {
+    float t[kSG][J], ts[kSG];
 #pragma unroll
-    for (int j = 0; j < J; ++j) v[j] += __ldcg(src + s * split_stride + 32 * j);
-    ssx += __ldcg(a.ss_part + s * 16 + b);
+    for (int i = 0; i < kSG; ++i) {
+      const int s = s0 + i < a.qkv.S ? s0 + i : a.qkv.S - 1;
+#pragma unroll
+      for (int j = 0; j < J; ++j) t[i][j] = __ldcg(src + s * split_stride + 32 * j);
+      ts[i] = __ldcg(a.ss_part + s * 16 + b);
+    }
+#pragma unroll
+    for (int i = 0; i < kSG; ++i)
+      if (s0 + i < a.qkv.S) {
+#pragma unroll
+        for (int j = 0; j < J; ++j) v[j] += t[i][j];
+        ssx += ts[i];
+      }
   }
   // input RMSNorm factor 1/rms(x) of the row, applied to the projection (linear)
   const float xinv = rsqrtf(ssx / a.H + a.eps);
@@ -397,9 +464,12 @@ __device__ void head_job(const StepArgs& a, const int* geo, int b, int kvh, int 
     for (int j = 0; j < J; ++j) ss += v[j] * v[j];
     ss = warp_sum(ss);
     const float inv = rsqrtf(ss / HD + a.eps);
-    const float* w = kind == 0 ? a.w_q : (kind == 1 ? a.w_k : nullptr);
+    const float* w = kind == 0 ? a.w_q : a.w_k;  // a valid address for v too (unused)
 #pragma unroll
-    for (int j = 0; j < J; ++j) v[j] *= inv * (w ? __ldg(w + lane + 32 * j) : 1.0f);
+    for (int j = 0; j < J; ++j) {
+      const float wj = __ldg(w + lane + 32 * j);
+      v[j] *= inv * (kind < 2 ? wj : 1.0f);
+    }
   }
   if (kind < 2) {
     const int P = geo[b * kGeoInts + kGeoP];
@@ -520,56 +590,114 @@ __device__ __forceinline__ float order_float(unsigned k) {
 // batch row, combined from the records of the CTAs that covered each unit:
 //   o = sum_r 2^(m_r - M) O_r / sum_r 2^(m_r - M) l_r,
 // M the largest m_r of the head (published with atomicMax by the record writers), then
-// split into fp16 hi + lo.  One thread per (batch row, column pair); all of its loads are
-// independent of one another.
-template <int HD, int NT>
-__device__ void build_o_operand(const StepArgs& a, const int* geo, int s, int Nt, bool tap,
-                                uint32_t* xw) {
+// split into fp16 hi + lo.  Thread tid owns the E elements (batch row, column pair)
+// tid + k * 256; for each chunk of RCH records every load of all E elements is issued
+// before any of them is used, so a chunk costs one memory round trip.
+template <int HD, int NT, int E>
+__device__ void combine_records(const StepArgs& a, const int* geo, int col0, int npair, int Nt,
+                                unsigned step, bool tap, uint32_t* xw, int k0) {
   using AC = Attn<HD>;
-  const int nbs = a.o.nbs;
-  const int ncols = nbs * 32, col0 = s * ncols;
+  constexpr int RCH = E == 1 ? 24 : (16 / E > 1 ? 16 / E : 1);
   const int G = a.nh / a.nkv;
   const int nctas = gridDim.x;
-  const int npair = ncols / 2;
-  for (int i = threadIdx.x; i < nbs * NT * 32 * 4; i += kConsumers) xw[i] = 0u;
-  consumer_sync();
-  for (int e = threadIdx.x; e < a.B * npair; e += kConsumers) {
-    const int b = e / npair, cc = 2 * (e - b * npair);  // column pair (cc, cc + 1) of the split
-    const int col = col0 + cc;
-    const int h = col / HD, d = col - h * HD;
-    const int kvh = h / G, hl = h - kvh * G;
-    const int u = b * a.nkv + kvh;
-    const int nt = geo[b * kGeoInts + kGeoNt];
-    float2 acc = make_float2(0.f, 0.f);
-    float den = 0.f;
-    if (nt > 0) {
-      int pre = kvh * nt;
-      for (int bb = 0; bb < b; ++bb) pre += a.nkv * geo[bb * kGeoInts + kGeoNt];
-      const int cf = part_of(pre, Nt, nctas);
-      const int nrec = part_of(pre + nt - 1, Nt, nctas) - cf + 1;
-      const unsigned long long key = __ldcg(a.gmax + (size_t)b * a.nh + h);
-      const float M = (unsigned)(key >> 32) == a.step ? order_float((unsigned)key) : 0.f;
-      const float* rp = a.rec + ((size_t)(cf + u) * 8 + hl) * AC::RS;
-#pragma unroll 8
-      for (int r = 0; r < nrec; ++r, rp += 8 * AC::RS) {
-        const float mr = __ldcg(rp + HD), lr = __ldcg(rp + HD + 1);
-        const float2 v = __ldcg(reinterpret_cast<const float2*>(rp + d));
-        const float w = exp2f(mr - M);
-        den += w * lr;
-        acc.x += w * v.x;
-        acc.y += w * v.y;
+  const int nel = a.B * npair;
+  const float* rp[E];
+  int nrec[E], dcol[E];
+  float M[E], den[E];
+  unsigned long long key[E];
+  float2 acc[E];
+  int maxrec = 0;
+#pragma unroll
+  for (int k = 0; k < E; ++k) {
+    const int e0 = threadIdx.x + (k0 + k) * kConsumers;
+    nrec[k] = 0;
+    dcol[k] = 0;
+    den[k] = 0.f;
+    acc[k] = make_float2(0.f, 0.f);
+    rp[k] = a.rec;
+    key[k] = 0ull;
+    if (e0 < nel) {
+      const int e = e0 < nel ? e0 : nel - 1;  // in range even where the test is folded away
+      const int b = e / npair, col = col0 + 2 * (e - b * npair);
+      const int h = col / HD;
+      const int kvh = h / G, hl = h - kvh * G;
+      const int nt = geo[b * kGeoInts + kGeoNt];
+      dcol[k] = col - h * HD;
+      if (nt > 0) {
+        int pre = kvh * nt;
+        for (int bb = 0; bb < b; ++bb) pre += a.nkv * geo[bb * kGeoInts + kGeoNt];
+        const int cf = part_of(pre, Nt, nctas);
+        nrec[k] = part_of(pre + nt - 1, Nt, nctas) - cf + 1;
+        key[k] = ldcg_pinned64(a.gmax + (size_t)b * a.nh + h);  // used after the loop
+        rp[k] = a.rec + ((size_t)(cf + b * a.nkv + kvh) * 8 + hl) * AC::RS;
+        maxrec = nrec[k] > maxrec ? nrec[k] : maxrec;
       }
     }
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-    acc.x *= inv;
-    acc.y *= inv;
-    __half hx, lx, hy, ly;
-    split_f16(acc.x, hx, lx);
-    split_f16(acc.y, hy, ly);
-    const int w = operand_word<NT>(cc, b);
-    xw[w] = pack_h2(hx, hy);
-    xw[w + 16] = pack_h2(lx, ly);
-    if (tap) *reinterpret_cast<float2*>(a.o_tap + ((size_t)b * a.nh + h) * HD + d) = acc;
+  }
+#pragma unroll
+  for (int k = 0; k < E; ++k)
+    M[k] = (unsigned)(key[k] >> 32) == step ? order_float((unsigned)key[k]) : 0.f;
+  for (int r0 = 0; r0 < maxrec; r0 += RCH) {
+    float mr[E][RCH], lr[E][RCH];
+    float2 v[E][RCH];
+#pragma unroll
+    for (int k = 0; k < E; ++k)
+#pragma unroll
+      for (int i = 0; i < RCH; ++i) {
+        mr[k][i] = -INFINITY;
+        lr[k][i] = 0.f;
+        v[k][i] = make_float2(0.f, 0.f);
+        if (r0 + i < nrec[k]) {
+          const float* p = rp[k] + (size_t)(r0 + i) * 8 * AC::RS;
+          mr[k][i] = ldcg_pinned(p + HD);
+          lr[k][i] = ldcg_pinned(p + HD + 1);
+          v[k][i] = ldcg_pinned2(p + dcol[k]);
+        }
+      }
+#pragma unroll
+    for (int k = 0; k < E; ++k)
+#pragma unroll
+      for (int i = 0; i < RCH; ++i) {
+        const float w = exp2f(mr[k][i] - M[k]);
+        den[k] += w * lr[k][i];
+        acc[k].x += w * v[k][i].x;
+        acc[k].y += w * v[k][i].y;
+      }
+  }
+#pragma unroll
+  for (int k = 0; k < E; ++k) {
+    const int e = threadIdx.x + (k0 + k) * kConsumers;
+    if (e < nel) {
+      const int b = e / npair, cc = 2 * (e - b * npair);
+      const int h = (col0 + cc) / HD;
+      const float inv = den[k] > 0.f ? 1.f / den[k] : 0.f;
+      const float2 o = make_float2(acc[k].x * inv, acc[k].y * inv);
+      __half hx, lx, hy, ly;
+      split_f16(o.x, hx, lx);
+      split_f16(o.y, hy, ly);
+      const int w = operand_word<NT>(cc, b);
+      xw[w] = pack_h2(hx, hy);
+      xw[w + 16] = pack_h2(lx, ly);
+      if (tap) *reinterpret_cast<float2*>(a.o_tap + ((size_t)b * a.nh + h) * HD + dcol[k]) = o;
+    }
+  }
+}
+
+template <int HD, int NT>
+__device__ void build_o_operand(const StepArgs& a, const int* geo, int s, int Nt, unsigned step,
+                                bool tap, uint32_t* xw) {
+  const int nbs = a.o.nbs;
+  const int npair = nbs * 16, col0 = s * nbs * 32;
+  for (int i = threadIdx.x; i < nbs * NT * 32 * 4; i += kConsumers) xw[i] = 0u;
+  consumer_sync();
+  const int per = (a.B * npair + kConsumers - 1) / kConsumers;  // <= 4 NT
+  // two shapes only (code size: this runs once per step, from a cold instruction cache)
+  if (per <= 1) {
+    combine_records<HD, NT, 1>(a, geo, col0, npair, Nt, step, tap, xw, 0);
+  } else {
+    constexpr int E = NT >= 2 ? 8 : 4;  // at most 8 elements keep a chunk's loads in registers
+    for (int k0 = 0; k0 < per; k0 += E)
+      combine_records<HD, NT, E>(a, geo, col0, npair, Nt, step, tap, xw, k0);
   }
   consumer_sync();
 }
@@ -628,7 +756,7 @@ __device__ void prefetch_load(const StepArgs& a, const Schedule& sc, const int* 
 template <int HD, int NT>
 __global__ void __launch_bounds__(kThreads, 1)
     step_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                const StepArgs a) {
+                const __grid_constant__ StepArgs a) {
   using AC = Attn<HD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -641,6 +769,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* append_bar = empty + kStages;
   volatile int* s_abort = reinterpret_cast<volatile int*>(small + 64);
   int* s_issued = reinterpret_cast<int*>(small + 68);
+  unsigned* s_step = reinterpret_cast<unsigned*>(small + 72);  // this step's number
+  unsigned long long* s_gbase = reinterpret_cast<unsigned long long*>(small + 80);
   unsigned* s_max = reinterpret_cast<unsigned*>(small + 96);
   float* s_ssq = reinterpret_cast<float*>(small + 160);
   float* s_inv = reinterpret_cast<float*>(small + 224);
@@ -648,11 +778,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, nctas = gridDim.x;
-  const int G = a.nh / a.nkv;
-  if (blockDim.x != kThreads || a.B > kMaxBatch) {
-    if (tid == 0) atomicOr(a.err, kErrBadPlan);
-    return;
-  }
+  if (blockDim.x != kThreads) return;  // the launch always uses kThreads (B <= 16 is checked
+                                       // on the host)
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -670,6 +797,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
+  const int G = a.nh / a.nkv;
   if (warp == kCW) {
     // ============================================================== producer
     Schedule sc;
@@ -703,7 +831,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bytes, &full[st]);
       ++q;
     };
-    // phase A depends on nothing of this step: its first stages go out first
+    // phase A depends on nothing of this step; its copies go out as soon as the consumers
+    // hold their activations (barrier 3), whose loads would otherwise queue behind them
+    asm volatile("bar.sync 3, %0;" ::"n"(kThreads) : "memory");
     if (lane == 0) {
       for (int k = 0; k < sc.nA && k < kStages && ok; ++k) issue_gemv(a.qkv, sc.sa, k);
       prefetch_tmap(&tmk);
@@ -713,7 +843,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // visible slots and key tiles of each sequence, for both sides (consumers read them
     // after barrier 2)
     if (lane < a.B) {
-      const int b = lane;
+      const int b = lane < a.B ? lane : 0;  // in range even where the test is folded away
       const int P = a.seq_pos[b];
       const bool bad = P < 0 || (!a.ring && P >= a.C);
       int lo, hi, slot;
@@ -782,6 +912,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ============================================================== consumers
+    // the barrier count at the start numbers this step (read now, used after phase A)
+    const unsigned long long arrivals0 = tid == 0 ? ldcg_pinned64(a.gbar) : 0ull;
     uint32_t q = 0;
     auto wait_stage = [&]() -> int {
       const int st = (int)(q % kStages);
@@ -800,6 +932,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Slice sl = gemv_slice(a.qkv, c, nctas);
       build_x_operand<NT>(a, sl.s, sl.first, reinterpret_cast<uint32_t*>(uni), s_max, s_ssq,
                           s_inv);
+      if (tid == 0) {
+        const unsigned long long per_step = 3ull * (unsigned)nctas;
+        *s_gbase = arrivals0 / per_step * per_step;       // used by thread 0 only
+        *s_step = (unsigned)(arrivals0 / per_step) + 1u;  // read after the next barrier
+      }
       for (int r = sl.r0; r < sl.r1; r += a.qkv.ips) {
         const int n = a.qkv.ips < sl.r1 - r ? a.qkv.ips : sl.r1 - r;
         const int st = wait_stage();
@@ -809,7 +946,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         release_stage();
       }
     }
-    grid_sync(a.gbar, a.gbar_base + nctas, a.err, s_abort);
+    grid_sync(a.gbar, *s_gbase + nctas, a.err, s_abort);
 
     // ---------------------------------------------------------- B: attention
     asm volatile("bar.sync 2, %0;" ::"n"(kThreads) : "memory");  // geometry is in
@@ -905,7 +1042,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           rec[h * AC::RS + d] = acc;
           if (d == HD)
             atomicMax(a.gmax + (size_t)b * a.nh + kvh * G + h,
-                      ((unsigned long long)a.step << 32) | float_order(M));
+                      ((unsigned long long)*s_step << 32) | float_order(M));
         }
         consumer_sync();
       });
@@ -922,12 +1059,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    grid_sync(a.gbar, a.gbar_base + 2ull * nctas, a.err, s_abort);
+    grid_sync(a.gbar, *s_gbase + 2ull * nctas, a.err, s_abort);
 
     // ---------------------------------------------------------- C: o_proj + residual
     {
       const Slice sl = gemv_slice(a.o, c, nctas);
-      build_o_operand<HD, NT>(a, geo, sl.s, Nt, sl.first && a.o_tap != nullptr,
+      build_o_operand<HD, NT>(a, geo, sl.s, Nt, *s_step, sl.first && a.o_tap != nullptr,
                               reinterpret_cast<uint32_t*>(uni));
       for (int r = sl.r0; r < sl.r1; r += a.o.ips) {
         const int n = a.o.ips < sl.r1 - r ? a.o.ips : sl.r1 - r;
@@ -938,6 +1075,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         release_stage();
       }
     }
+    grid_sync(a.gbar, *s_gbase + 3ull * nctas, a.err, s_abort);
+    finish_outputs(a, c, nctas);
   }
 
   // drain: after a give-up, copies may still be landing in the ring
@@ -955,9 +1094,17 @@ template <int HD, int NT>
 cudaError_t launch_step_t(const StepArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                           int grid, cudaStream_t s) {
   auto kern = step_kernel<HD, NT>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+  // the shared-memory opt-in, once per device (devices 0..63; beyond, every launch)
+  static unsigned long long opted_in = 0ull;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+  if (!(__atomic_load_n(&opted_in, __ATOMIC_ACQUIRE) & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    if (e != cudaSuccess) return e;
+    __atomic_fetch_or(&opted_in, bit, __ATOMIC_RELEASE);
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
