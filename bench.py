@@ -250,6 +250,11 @@ def run_ours(args, rank, world, local):
             layers.append(hfa.Layer(hfa.desc_for(w), dev_w, stream=stream))
             caches.append((kv["k_cache"].cuda(), kv["v_cache"].cuda()))
     del dev_w
+    if R >= 2:
+        # replicas run one after another like the layers of a model: each step prefetches
+        # the next replica's first weights into L2 during its own o_proj phase
+        for r in range(R):
+            layers[r].hfa_set_successor(layers[(r + 1) % R])
     xd = x.cuda()
     posd = torch.from_numpy(pos).cuda()
     out = torch.empty((B, w.hidden), dtype=torch.bfloat16, device="cuda")
@@ -358,6 +363,7 @@ def run_ours(args, rank, world, local):
                        "l2": f"inputs larger than L2: {R} layer replicas rotated, "
                              f"{R * step_bytes / 1e9:.2f} GB"},
             "timing": "CUDA graph of the K steps; ms_per_step_direct = host launches",
+            "successor_prefetch": R >= 2,
             "ms_per_step_direct": ms_direct,
             "step_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
             "step_frac_of_peak": step_bytes / (ms_per_step * 1e-3) / 1e9 / peak,
@@ -366,6 +372,8 @@ def run_ours(args, rank, world, local):
             "gpu_launches": sum(v[1] for v in ktimes.values())}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, weights, x, pos, kv)
+    for L in layers:
+        L.hfa_set_successor(None)
     for L in layers:
         L.hfa_destroy()
     if rank == 0:

@@ -191,6 +191,18 @@ hfa_status hfa_attention_decode_noalloc(const hfa_attn_desc* desc, void* stream,
                                         const void* k_cache_dev, const void* v_cache_dev,
                                         float* o_dev);
 
+/*
+ * Successor hint for decoding through a stack of layers (no counterpart on the pages,
+ * which run one layer at a time).  Once set, each decode step of `layer` prefetches into
+ * L2, during its last phase (o_proj and residual, when HBM is otherwise idle), the Q8_0
+ * QKV weights that the next decode step of `next` reads first.  Results are unchanged.
+ *   next  a layer of the same shape (hidden, heads, kv heads, head dim) with Q8_0
+ *         weights, or NULL to clear the hint.  It must stay alive while it is set: destroy
+ *         or re-point `layer`'s hint before destroying `next`.
+ * Errors: HFA_EINVAL (shapes differ, bf16 weights, NULL layer).
+ */
+hfa_status hfa_set_successor(hfa_layer* layer, const hfa_layer* next);
+
 /* Release the layer and its device memory (synchronises the device first). */
 hfa_status hfa_destroy(hfa_layer* layer);
 

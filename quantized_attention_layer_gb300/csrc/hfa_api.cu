@@ -53,6 +53,7 @@ struct hfa_layer {
   uint8_t* wqkv_t = nullptr;
   uint8_t* wo_t = nullptr;
   StepGemv g_qkv{}, g_o{};
+  const uint8_t* successor_qkv = nullptr;  // QKV tiles of the layer that runs next
   __nv_bfloat16* wqkv_bf16 = nullptr;  // verify path: [(nh + 2 nkv) hd, H]
   __nv_bfloat16* wo_bf16 = nullptr;    // [H, nh hd]
   float* w_in = nullptr;
@@ -61,7 +62,6 @@ struct hfa_layer {
   float2* rope_g = nullptr;
   // scratch
   float* qkv_part = nullptr;
-  float* ss_part = nullptr;
   float* q_f32 = nullptr;
   float* attn_rec = nullptr;
   unsigned long long* attn_gmax = nullptr;
@@ -368,7 +368,6 @@ extern "C" hfa_status hfa_layer_create(const hfa_layer_desc* desc, const void* w
   const int units = d.max_batch * nkv;
   if (!bf16w) {
     LA(L->qkv_part, (size_t)L->g_qkv.S * d.max_batch * L->rows_qkv);
-    LA(L->ss_part, (size_t)L->g_qkv.S * 16);
     LA(L->y_part, (size_t)L->g_o.S * d.max_batch * H);
   }
   LA(L->q_f32, (size_t)MR * nh * hd);
@@ -406,6 +405,22 @@ extern "C" hfa_status hfa_layer_create(const hfa_layer_desc* desc, const void* w
   return HFA_OK;
 #undef LA
 #undef LC
+}
+
+extern "C" hfa_status hfa_set_successor(hfa_layer* L, const hfa_layer* next) {
+  if (!L) return HFA_EINVAL;
+  if (!next) {
+    L->successor_qkv = nullptr;
+    return HFA_OK;
+  }
+  const hfa_layer_desc &a = L->d, &b = next->d;
+  if (!L->wqkv_t || !next->wqkv_t)
+    return fail(L, HFA_EINVAL, "the successor hint needs Q8_0 weights on both layers");
+  if (a.hidden != b.hidden || a.num_heads != b.num_heads || a.num_kv_heads != b.num_kv_heads ||
+      a.head_dim != b.head_dim || next->device != L->device)
+    return fail(L, HFA_EINVAL, "the successor must have the same shape, on the same device");
+  L->successor_qkv = next->wqkv_t;
+  return HFA_OK;
 }
 
 extern "C" hfa_status hfa_destroy(hfa_layer* L) {
@@ -523,7 +538,6 @@ extern "C" hfa_status hfa_decode_step(hfa_layer* L, void* stream, const void* x,
   sa.k_cache = (__nv_bfloat16*)kc;
   sa.v_cache = (__nv_bfloat16*)vc;
   sa.qkv_part = L->qkv_part;
-  sa.ss_part = L->ss_part;
   sa.rec = L->attn_rec;
   sa.y_part = L->y_part;
   sa.gbar = L->gbar;
@@ -535,6 +549,7 @@ extern "C" hfa_status hfa_decode_step(hfa_layer* L, void* stream, const void* x,
   sa.o_tap = taps ? L->o_f32 : nullptr;
   sa.out_tap = L->out_tap;
   sa.out = (__nv_bfloat16*)out;
+  sa.next_qkv_w = L->successor_qkv;
   sa.B = batch;
   sa.H = d.hidden;
   sa.nh = d.num_heads;

@@ -85,7 +85,6 @@ struct StepArgs {
   __nv_bfloat16* k_cache;  // [B, nkv, C, hd]
   __nv_bfloat16* v_cache;
   float* qkv_part;         // f32 [qkv.S][B][(nh + 2 nkv) hd]: one partial sum per k-split
-  float* ss_part;          // f32 [qkv.S][16]: sum of x^2 over each k-split's columns
   float* rec;              // f32 [(grid + B nkv)][8][hd + 4]: (O, m, l) per key range
   float* y_part;           // f32 [o.S][B][H]: one partial o_proj sum per k-split
   unsigned long long* gmax;  // [B * nh]: (step << 32) | ordered(max logit) over the records
@@ -98,6 +97,7 @@ struct StepArgs {
   float* o_tap;            // nullable f32 [B, nh, hd] (attention output)
   float* out_tap;          // nullable f32 [B, H]
   __nv_bfloat16* out;      // bf16 [B, H]
+  const uint8_t* next_qkv_w;  // nullable: QKV tiles (same layout) of the layer that runs next
   int B, H, nh, nkv, C, sliding, window, ring, v_unit_norm;
   long long cache_rows;    // B * nkv * C: rows of the [rows, hd] view of each cache
   float eps;

@@ -247,10 +247,10 @@ __device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) 
 
 // Phase A operand: v = x (.) w_in over the columns of k-split s, for every batch row,
 // scaled per row by a power of two (exact; undone in the flush) and split into fp16
-// hi + lo.  The first CTA of each split also stores the split's part of sum(x^2).
+// hi + lo.
 template <int NT>
-__device__ void build_x_operand(const StepArgs& a, int s, bool add_ss, uint32_t* xw,
-                                unsigned* s_max, float* s_ssq, float* s_inv) {
+__device__ void build_x_operand(const StepArgs& a, int s, uint32_t* xw, unsigned* s_max,
+                                float* s_inv) {
   const int tid = threadIdx.x;
   const int nbs = a.qkv.nbs;
   const int groups = nbs * 4;  // 8-column groups per batch row
@@ -280,17 +280,15 @@ __device__ void build_x_operand(const StepArgs& a, int s, bool add_ss, uint32_t*
     if (e < total && b < a.B) {
       const float wv[8] = {w0[k].x, w0[k].y, w0[k].z, w0[k].w, w1[k].x, w1[k].y, w1[k].z, w1[k].w};
       const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[k]);
-      float mx = 0.f, ss = 0.f;
+      float mx = 0.f;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float2 f = __bfloat1622float2(h[i]);
         v[k][2 * i] = f.x * wv[2 * i];
         v[k][2 * i + 1] = f.y * wv[2 * i + 1];
-        ss += f.x * f.x + f.y * f.y;
         mx = fmaxf(mx, fmaxf(fabsf(v[k][2 * i]), fabsf(v[k][2 * i + 1])));
       }
       atomicMax(&s_max[b], __float_as_uint(mx));
-      if (add_ss) atomicAdd(&s_ssq[b], ss);
     }
   }
   // the activations are in registers: the producer may start the weight stream
@@ -313,10 +311,7 @@ __device__ void build_x_operand(const StepArgs& a, int s, bool add_ss, uint32_t*
       }
     }
   }
-  if (tid < a.B) {
-    s_inv[tid] = exp2i(-scale_exp(s_max[tid]));
-    if (add_ss) a.ss_part[s * 16 + tid] = s_ssq[tid];
-  }
+  if (tid < a.B) s_inv[tid] = exp2i(-scale_exp(s_max[tid]));
   consumer_sync();
 }
 
@@ -436,23 +431,48 @@ __device__ void head_job(const StepArgs& a, const int* geo, int b, int kvh, int 
   float v[J];
 #pragma unroll
   for (int j = 0; j < J; ++j) v[j] = 0.f;
-  float ssx = 0.f;
   for (int s0 = 0; s0 < a.qkv.S; s0 += kSG) {
-    float t[kSG][J], ts[kSG];
+    float t[kSG][J];
 #pragma unroll
     for (int i = 0; i < kSG; ++i) {
       const int s = s0 + i < a.qkv.S ? s0 + i : a.qkv.S - 1;
 #pragma unroll
       for (int j = 0; j < J; ++j) t[i][j] = __ldcg(src + s * split_stride + 32 * j);
-      ts[i] = __ldcg(a.ss_part + s * 16 + b);
     }
 #pragma unroll
     for (int i = 0; i < kSG; ++i)
       if (s0 + i < a.qkv.S) {
 #pragma unroll
         for (int j = 0; j < J; ++j) v[j] += t[i][j];
-        ssx += ts[i];
       }
+  }
+  // sum(x^2) of the layer input row, in a fixed order (each lane in sequence, then a
+  // shuffle tree), 16 loads per lane in flight at a time
+  float ssx = 0.f;
+  {
+    constexpr int kXU = 16;
+    const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)b * a.H);
+    const int nq = a.H / 8;
+    for (int i0 = 0; i0 < nq; i0 += 32 * kXU) {
+      uint4 t[kXU];
+#pragma unroll
+      for (int u = 0; u < kXU; ++u) {
+        const int i = i0 + lane + 32 * u;
+        t[u] = xr[i < nq ? i : nq - 1];
+      }
+#pragma unroll
+      for (int u = 0; u < kXU; ++u)
+        if (i0 + lane + 32 * u < nq) {
+          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&t[u]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(h[e]);
+            ssx = fmaf(f.x, f.x, ssx);
+            ssx = fmaf(f.y, f.y, ssx);
+          }
+        }
+    }
+    ssx = warp_sum(ssx);
   }
   // input RMSNorm factor 1/rms(x) of the row, applied to the projection (linear)
   const float xinv = rsqrtf(ssx / a.H + a.eps);
@@ -767,12 +787,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(small);
   uint64_t* empty = full + kStages;
   uint64_t* append_bar = empty + kStages;
+  uint64_t* next_bar = append_bar + 1;  // consumers passed the second grid barrier
   volatile int* s_abort = reinterpret_cast<volatile int*>(small + 64);
   int* s_issued = reinterpret_cast<int*>(small + 68);
   unsigned* s_step = reinterpret_cast<unsigned*>(small + 72);  // this step's number
   unsigned long long* s_gbase = reinterpret_cast<unsigned long long*>(small + 80);
   unsigned* s_max = reinterpret_cast<unsigned*>(small + 96);
-  float* s_ssq = reinterpret_cast<float*>(small + 160);
   float* s_inv = reinterpret_cast<float*>(small + 224);
   int* geo = reinterpret_cast<int*>(small + 512);
 
@@ -787,14 +807,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&empty[i], kCW);
     }
     mbar_init(append_bar, 1);
+    mbar_init(next_bar, 1);
     *s_abort = 0;
     *s_issued = 0;
     fence_barrier_init();
   }
-  if (tid < kMaxBatch) {
-    s_max[tid] = 0u;
-    s_ssq[tid] = 0.f;
-  }
+  if (tid < kMaxBatch) s_max[tid] = 0u;
   __syncthreads();
 
   const int G = a.nh / a.nkv;
@@ -909,6 +927,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       });
       for (int k = 0; k < sc.nC && ok; ++k) issue_gemv(a.o, sc.so, k);
       *s_issued = (int)q;
+      // the layer that runs next: its first loads (this CTA's QKV slice, same shape) go to
+      // L2 once the attention is over, while the o_proj phase leaves HBM idle
+      if (a.next_qkv_w && ok && mbar_wait(next_bar, 0, a.err, s_abort)) {
+        const uint8_t* src =
+            a.next_qkv_w + ((size_t)sc.sa.s * a.qkv.R + sc.sa.r0) * a.qkv.nbs * kQ8TileBytes;
+        const size_t bytes = (size_t)(sc.sa.r1 - sc.sa.r0) * a.qkv.nbs * kQ8TileBytes;
+        for (size_t off = 0; off < bytes; off += 32768)
+          prefetch_bulk_l2(src + off, (uint32_t)(bytes - off < 32768 ? bytes - off : 32768));
+      }
     }
   } else {
     // ============================================================== consumers
@@ -930,8 +957,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- A: QKV
     {
       const Slice sl = gemv_slice(a.qkv, c, nctas);
-      build_x_operand<NT>(a, sl.s, sl.first, reinterpret_cast<uint32_t*>(uni), s_max, s_ssq,
-                          s_inv);
+      build_x_operand<NT>(a, sl.s, reinterpret_cast<uint32_t*>(uni), s_max, s_inv);
       if (tid == 0) {
         const unsigned long long per_step = 3ull * (unsigned)nctas;
         *s_gbase = arrivals0 / per_step * per_step;       // used by thread 0 only
@@ -1060,6 +1086,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     grid_sync(a.gbar, *s_gbase + 2ull * nctas, a.err, s_abort);
+    if (a.next_qkv_w && tid == 0) mbar_arrive(next_bar);
 
     // ---------------------------------------------------------- C: o_proj + residual
     {
@@ -1090,20 +1117,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+}  // namespace step
+namespace {
+// devices on which a kernel instantiation has its shared-memory opt-in (internal linkage:
+// a function-local static of a template would be merged across every loaded library)
+template <int HD, int NT>
+struct StepOptIn {
+  static unsigned long long mask;
+};
+template <int HD, int NT>
+unsigned long long StepOptIn<HD, NT>::mask = 0ull;
+}  // namespace
+namespace step {
+
 template <int HD, int NT>
 cudaError_t launch_step_t(const StepArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                           int grid, cudaStream_t s) {
   auto kern = step_kernel<HD, NT>;
   // the shared-memory opt-in, once per device (devices 0..63; beyond, every launch)
-  static unsigned long long opted_in = 0ull;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
-  if (!(__atomic_load_n(&opted_in, __ATOMIC_ACQUIRE) & bit)) {
+  unsigned long long* opted_in = &StepOptIn<HD, NT>::mask;
+  if (!bit || !(__atomic_load_n(opted_in, __ATOMIC_ACQUIRE) & bit)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     if (e != cudaSuccess) return e;
-    __atomic_fetch_or(&opted_in, bit, __ATOMIC_RELEASE);
+    __atomic_fetch_or(opted_in, bit, __ATOMIC_RELEASE);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);

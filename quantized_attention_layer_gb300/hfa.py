@@ -84,6 +84,8 @@ def lib():
         L.hfa_verify_block.argtypes = [P, P, P, I, I, P, P, P]
         L.hfa_destroy.restype = C
         L.hfa_destroy.argtypes = [P]
+        L.hfa_set_successor.restype = C
+        L.hfa_set_successor.argtypes = [P, P]
         L.hfa_last_error.restype = ctypes.c_char_p
         L.hfa_last_error.argtypes = [P]
         L.hfa_debug_taps.restype = C
@@ -240,6 +242,9 @@ class Layer:
 
     def hfa_check_device_status(self, stream=None) -> None:
         self._check(lib().hfa_check_device_status(self._h, _stream_ptr(stream)))
+
+    def hfa_set_successor(self, next_layer: Optional["Layer"]) -> None:
+        self._check(lib().hfa_set_successor(self._h, next_layer._h if next_layer else None))
 
     def hfa_set_kernel_timing(self, enable: bool) -> None:
         lib().hfa_set_kernel_timing(self._h, int(bool(enable)))
