@@ -64,7 +64,8 @@ struct hfa_layer {
   float* qkv_part = nullptr;
   float* q_f32 = nullptr;
   float* attn_rec = nullptr;
-  unsigned long long* attn_gmax = nullptr;
+  int* unit_ticket = nullptr;
+  uint32_t* o_operand = nullptr;  // o_proj operand slices (fragment order, 4 batch tiles max)
   float* o_f32 = nullptr;
   float* y_part = nullptr;
   unsigned long long* gbar = nullptr;
@@ -369,12 +370,13 @@ extern "C" hfa_status hfa_layer_create(const hfa_layer_desc* desc, const void* w
   if (!bf16w) {
     LA(L->qkv_part, (size_t)L->g_qkv.S * d.max_batch * L->rows_qkv);
     LA(L->y_part, (size_t)L->g_o.S * d.max_batch * H);
+    LA(L->o_operand, (size_t)L->g_o.S * L->g_o.nbs * 4 * 128);
   }
   LA(L->q_f32, (size_t)MR * nh * hd);
   // one (m, l, O) record per (CTA, unit) pair of the step kernel: ids c + u are unique
   LA(L->attn_rec, (size_t)(L->num_sms + units) * attn_record_floats(hd));
   LA(L->gbar, 1);
-  LA(L->attn_gmax, (size_t)d.max_batch * nh);
+  LA(L->unit_ticket, (size_t)d.max_batch * nkv);
   LA(L->o_f32, (size_t)MR * nh * hd);
   LA(L->err, 1);
   LA(L->x_stage, (size_t)d.max_batch * H);
@@ -390,7 +392,7 @@ extern "C" hfa_status hfa_layer_create(const hfa_layer_desc* desc, const void* w
   }
 
   LC(cudaMemsetAsync(L->gbar, 0, 8, s), "memset");
-  LC(cudaMemsetAsync(L->attn_gmax, 0, (size_t)d.max_batch * nh * 8, s), "memset");
+  LC(cudaMemsetAsync(L->unit_ticket, 0, (size_t)d.max_batch * nkv * 4, s), "memset");
   LC(cudaMemsetAsync(L->err, 0, 4, s), "memset");
   if (d.max_verify_len > 0) {
     hfa_status vs = hfa::verify_create(L->d, L->num_sms, &L->verify);
@@ -541,12 +543,13 @@ extern "C" hfa_status hfa_decode_step(hfa_layer* L, void* stream, const void* x,
   sa.rec = L->attn_rec;
   sa.y_part = L->y_part;
   sa.gbar = L->gbar;
-  sa.gmax = L->attn_gmax;
+  sa.unit_ticket = L->unit_ticket;
+  sa.o_attn = L->o_f32;  // also the attention tap
+  sa.o_operand = L->o_operand;
   sa.err = L->err;
   sa.q_tap = taps ? L->q_f32 : nullptr;
   sa.k_tap = L->k_tap;
   sa.v_tap = L->v_tap;
-  sa.o_tap = taps ? L->o_f32 : nullptr;
   sa.out_tap = L->out_tap;
   sa.out = (__nv_bfloat16*)out;
   sa.next_qkv_w = L->successor_qkv;
@@ -786,9 +789,9 @@ extern "C" hfa_status hfa_check_device_status(hfa_layer* L, void* stream) {
   CK(L, cudaMemsetAsync(L->err, 0, 4, s), "clear status");
   // a step that gave up may have left the grid barrier mid-count
   CK(L, cudaMemsetAsync(L->gbar, 0, 8, s), "reset grid barrier");
-  if (L->attn_gmax)
-    CK(L, cudaMemsetAsync(L->attn_gmax, 0, (size_t)L->d.max_batch * L->d.num_heads * 8, s),
-       "reset record maxima");
+  if (L->unit_ticket)
+    CK(L, cudaMemsetAsync(L->unit_ticket, 0, (size_t)L->d.max_batch * L->d.num_kv_heads * 4, s),
+       "reset unit tickets");
   CK(L, cudaStreamSynchronize(s), "sync");
   CK(L, cudaStreamSynchronize(s), "sync");
   return fail(L, HFA_EDEVICE, "device status 0x%x:%s%s%s", v,

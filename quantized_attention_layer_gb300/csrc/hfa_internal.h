@@ -87,14 +87,15 @@ struct StepArgs {
   float* qkv_part;         // f32 [qkv.S][B][(nh + 2 nkv) hd]: one partial sum per k-split
   float* rec;              // f32 [(grid + B nkv)][8][hd + 4]: (O, m, l) per key range
   float* y_part;           // f32 [o.S][B][H]: one partial o_proj sum per k-split
-  unsigned long long* gmax;  // [B * nh]: (step << 32) | ordered(max logit) over the records
+  int* unit_ticket;        // [B * nkv]: records written per (sequence, KV head); zero between steps
+  float* o_attn;           // f32 [B, nh, hd]: attention output (combined records)
+  uint32_t* o_operand;     // [o.S][o.nbs * NT * 128] words: o_proj operand, fragment order
   unsigned long long* gbar;  // grid barrier arrivals: only grows, three per CTA per step, so
                              // it also numbers the steps (graph replays included)
   unsigned* err;
   float* q_tap;            // nullable f32 [B, nh, hd] (q after RoPE)
   float* k_tap;            // nullable f32 [B, nkv, hd]
   float* v_tap;
-  float* o_tap;            // nullable f32 [B, nh, hd] (attention output)
   float* out_tap;          // nullable f32 [B, H]
   __nv_bfloat16* out;      // bf16 [B, H]
   const uint8_t* next_qkv_w;  // nullable: QKV tiles (same layout) of the layer that runs next

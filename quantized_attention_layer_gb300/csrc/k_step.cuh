@@ -174,24 +174,29 @@ __device__ __forceinline__ int seg_tile(int i, int lt0, int lt1, int tn) {
 // off the counter at its start (the count is then inside [base, base + 3 grid)).
 // Arrival is one release reduction (no round trip); a CTA that has given up arrives
 // without waiting, so the count stays exact.
-__device__ __forceinline__ void grid_sync(unsigned long long* gbar, unsigned long long target,
-                                          unsigned* err, volatile int* abort) {
+// Split in two so that a CTA can do work of its own between its arrival and the wait.
+__device__ __forceinline__ void grid_arrive(unsigned long long* gbar) {
   consumer_sync();
-  if (threadIdx.x == 0) {
-    const bool given_up = *abort != 0;
-    red_release_add_u64(gbar, 1ull);
-    if (!given_up) {
-      const uint64_t t0 = globaltimer_ns();
-      while ((long long)(ld_acquire_u64(gbar) - target) < 0) {
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-          atomicOr(err, kErrWaitTimeout);
-          *abort = 1;
-          break;
-        }
+  if (threadIdx.x == 0) red_release_add_u64(gbar, 1ull);
+}
+__device__ __forceinline__ void grid_wait(const unsigned long long* gbar, unsigned long long target,
+                                          unsigned* err, volatile int* abort) {
+  if (threadIdx.x == 0 && !*abort) {
+    const uint64_t t0 = globaltimer_ns();
+    while ((long long)(ld_acquire_u64(gbar) - target) < 0) {
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        atomicOr(err, kErrWaitTimeout);
+        *abort = 1;
+        break;
       }
     }
   }
   consumer_sync();
+}
+__device__ __forceinline__ void grid_sync(unsigned long long* gbar, unsigned long long target,
+                                          unsigned* err, volatile int* abort) {
+  grid_arrive(gbar);
+  grid_wait(gbar, target, err, abort);
 }
 
 // ------------------------------------------------------------------ GEMV pieces
@@ -319,7 +324,7 @@ __device__ void build_x_operand(const StepArgs& a, int s, uint32_t* xw, unsigned
 // outputs, out = bf16(x + sum over the o_proj k-splits), the splits added in a fixed
 // order; each thread issues all of its partial-sum loads before adding.
 __device__ __forceinline__ void finish_outputs(const StepArgs& a, int c, int nctas) {
-  constexpr int kMaxPer = 8;  // outputs per thread per round
+  constexpr int kMaxPer = 2;  // outputs per thread per round
   const long long n = (long long)a.B * a.H;
   const int i0 = part_begin(c, n, nctas), i1 = part_begin(c + 1, n, nctas);
   const size_t split_stride = (size_t)a.B * a.H;
@@ -360,34 +365,20 @@ __device__ __forceinline__ void finish_outputs(const StepArgs& a, int c, int nct
   }
 }
 
-// Partial sums of rows [16 r, 16 r + 16) over the nbs tiles of k-split s: stored (no
-// atomics) into the split's slice of the partial-sum buffer.
-template <int NT, bool OPROJ>
-__device__ __forceinline__ void gemv_flush(const StepArgs& a, const StepGemv& gm,
-                                           float (&acc)[NT][4], int s, int r,
-                                           const float* s_inv, int lane) {
+// The work items of one ring stage (n_items items of nbs tiles, row groups r_first ..),
+// one whole item per warp at a time.  The partial sums of rows [16 r, 16 r + 16) over an
+// item's tiles are stored (no atomics) into the k-split's slice of `part`, times the
+// batch row's factor `scale` (nullable: 1).  One out-of-line copy serves both GEMVs, so
+// the o_proj phase runs code the QKV phase already brought into the instruction cache.
+template <int NT>
+__device__ __noinline__ void gemv_stage(const StepGemv& gm, int B, float* part, int s,
+                                        const uint8_t* stage, int n_items, int r_first,
+                                        const uint4* frag, const float* scale, int warp,
+                                        int lane) {
+  const int nbs = gm.nbs;
   const int g = lane >> 2, t = lane & 3;
   const int R16 = gm.R * 16;
-  float* dst = (OPROJ ? a.y_part : a.qkv_part) + (size_t)s * a.B * R16;
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int b = nt * 4 + t;
-    if (b < a.B) {
-      const float f = OPROJ ? 1.f : s_inv[b];
-      dst[(size_t)b * R16 + r * 16 + g] = (acc[nt][0] + acc[nt][1]) * f;
-      dst[(size_t)b * R16 + r * 16 + g + 8] = (acc[nt][2] + acc[nt][3]) * f;
-    }
-  }
-}
-
-// The work items of one ring stage (n_items items of nbs tiles, row groups r_first ..),
-// one whole item per warp at a time.
-template <int NT, bool OPROJ>
-__device__ void gemv_stage(const StepArgs& a, const StepGemv& gm, int s, const uint8_t* stage,
-                           int n_items, int r_first, const uint4* frag, const float* s_inv,
-                           int warp, int lane) {
-  const int nbs = gm.nbs;
-  const int g = lane >> 2;
+  float* dst = part + (size_t)s * B * R16;
   for (int item = warp; item < n_items; item += kCW) {
     float acc[NT][4];
 #pragma unroll
@@ -400,7 +391,16 @@ __device__ void gemv_stage(const StepArgs& a, const StepGemv& gm, int s, const u
       const uint32_t d = *reinterpret_cast<const uint32_t*>(tp + i * kQ8TileBytes + 512 + g * 4);
       q8_tile_mma<NT>(acc, w, d, fr + i * NT * 32);
     }
-    gemv_flush<NT, OPROJ>(a, gm, acc, s, r_first + item, s_inv, lane);
+    const int r = r_first + item;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int b = nt * 4 + t;
+      if (b < B) {
+        const float f = scale ? scale[b] : 1.f;
+        dst[(size_t)b * R16 + r * 16 + g] = (acc[nt][0] + acc[nt][1]) * f;
+        dst[(size_t)b * R16 + r * 16 + g + 8] = (acc[nt][2] + acc[nt][3]) * f;
+      }
+    }
   }
 }
 
@@ -415,9 +415,16 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 // One head of unit (b, kvh): job < G query head kvh * G + job, G the key, G + 1 the value.
 // Raw projection * 1/rms(x), per-head RMSNorm (q, k; v with the unit-norm flag), RoPE
 // (q, k); queries go to q_s, the key and value row to the cache slot (bf16, RNE).
+// the RoPE rotation of one pair, out of line: one copy of the sin/cos code serves all
+static __device__ __noinline__ float2 rope_rotate(int P, float2 g, float x0, float x1) {
+  float c, s;
+  rope_cs(P, g, c, s);
+  return make_float2(x0 * c - x1 * s, x0 * s + x1 * c);
+}
+
 template <int HD>
 __device__ void head_job(const StepArgs& a, const int* geo, int b, int kvh, int job, int G,
-                         float* q_s, bool tap_q, int lane) {
+                         float xss, float* q_s, bool tap_q, int lane) {
   constexpr int J = HD / 32;
   const int rows = (a.nh + 2 * a.nkv) * HD;
   const int kind = job < G ? 0 : (job == G ? 1 : 2);
@@ -446,36 +453,8 @@ __device__ void head_job(const StepArgs& a, const int* geo, int b, int kvh, int 
         for (int j = 0; j < J; ++j) v[j] += t[i][j];
       }
   }
-  // sum(x^2) of the layer input row, in a fixed order (each lane in sequence, then a
-  // shuffle tree), 16 loads per lane in flight at a time
-  float ssx = 0.f;
-  {
-    constexpr int kXU = 16;
-    const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)b * a.H);
-    const int nq = a.H / 8;
-    for (int i0 = 0; i0 < nq; i0 += 32 * kXU) {
-      uint4 t[kXU];
-#pragma unroll
-      for (int u = 0; u < kXU; ++u) {
-        const int i = i0 + lane + 32 * u;
-        t[u] = xr[i < nq ? i : nq - 1];
-      }
-#pragma unroll
-      for (int u = 0; u < kXU; ++u)
-        if (i0 + lane + 32 * u < nq) {
-          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&t[u]);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = __bfloat1622float2(h[e]);
-            ssx = fmaf(f.x, f.x, ssx);
-            ssx = fmaf(f.y, f.y, ssx);
-          }
-        }
-    }
-    ssx = warp_sum(ssx);
-  }
   // input RMSNorm factor 1/rms(x) of the row, applied to the projection (linear)
-  const float xinv = rsqrtf(ssx / a.H + a.eps);
+  const float xinv = rsqrtf(xss / a.H + a.eps);
 #pragma unroll
   for (int j = 0; j < J; ++j) v[j] *= xinv;
   if (kind < 2 || a.v_unit_norm) {
@@ -495,11 +474,9 @@ __device__ void head_job(const StepArgs& a, const int* geo, int b, int kvh, int 
     const int P = geo[b * kGeoInts + kGeoP];
 #pragma unroll
     for (int j = 0; j < J / 2; ++j) {
-      float c, s;
-      rope_cs(P, a.rope_g[lane + 32 * j], c, s);
-      const float x0 = v[j], x1 = v[j + J / 2];
-      v[j] = x0 * c - x1 * s;
-      v[j + J / 2] = x0 * s + x1 * c;
+      const float2 r = rope_rotate(P, a.rope_g[lane + 32 * j], v[j], v[j + J / 2]);
+      v[j] = r.x;
+      v[j + J / 2] = r.y;
     }
   }
   if (kind == 0) {
@@ -597,127 +574,106 @@ __device__ __forceinline__ void attn_tile(uint32_t kb, const uint4* qf, int key0
   }
 }
 
-// Order-preserving map of a float to 32 bits (larger float, larger unsigned).
-__device__ __forceinline__ unsigned float_order(float f) {
-  const unsigned u = __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float order_float(unsigned k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+// CTAs that hold a record of unit u (its tiles, plus CTAs without tiles sitting inside
+// that run): [first, first + count).
+__device__ __forceinline__ void unit_ctas(const int* geo, int nkv, int b, int kvh, int Nt,
+                                          int nctas, int* first, int* count) {
+  const int nt = geo[b * kGeoInts + kGeoNt];
+  int pre = kvh * nt;
+  for (int bb = 0; bb < b; ++bb) pre += nkv * geo[bb * kGeoInts + kGeoNt];
+  *first = part_of(pre, Nt, nctas);
+  *count = part_of(pre + nt - 1, Nt, nctas) - *first + 1;
 }
 
-// Phase C operand: the attention output over the columns of o_proj k-split s, for every
-// batch row, combined from the records of the CTAs that covered each unit:
-//   o = sum_r 2^(m_r - M) O_r / sum_r 2^(m_r - M) l_r,
-// M the largest m_r of the head (published with atomicMax by the record writers), then
-// split into fp16 hi + lo.  Thread tid owns the E elements (batch row, column pair)
-// tid + k * 256; for each chunk of RCH records every load of all E elements is issued
-// before any of them is used, so a chunk costs one memory round trip.
-template <int HD, int NT, int E>
-__device__ void combine_records(const StepArgs& a, const int* geo, int col0, int npair, int Nt,
-                                unsigned step, bool tap, uint32_t* xw, int k0) {
+// Combine of one unit's records (run by the CTA whose record came last): for every query
+// head h of the group and column pair (d, d + 1),
+//   o = sum_r 2^(m_r - M) O_r / sum_r 2^(m_r - M) l_r,   M = max_r m_r,
+// written as the attention output (fp32) and, as fp16 hi + lo, straight into the o_proj
+// operand in MMA fragment order (one slice per k-split; sequence 0 also zeroes the batch
+// slots past B).  Each thread issues the loads of up to kRch records before using any.
+template <int HD, int NT>
+__device__ void merge_unit(const StepArgs& a, int b, int kvh, int G, int cf, int nrec) {
   using AC = Attn<HD>;
-  constexpr int RCH = E == 1 ? 24 : (16 / E > 1 ? 16 / E : 1);
-  const int G = a.nh / a.nkv;
-  const int nctas = gridDim.x;
-  const int nel = a.B * npair;
-  const float* rp[E];
-  int nrec[E], dcol[E];
-  float M[E], den[E];
-  unsigned long long key[E];
-  float2 acc[E];
-  int maxrec = 0;
+  constexpr int kRch = 16;
+  const int unit = b * a.nkv + kvh;
+  const float* base = a.rec + (size_t)(cf + unit) * 8 * AC::RS;
+  for (int p = threadIdx.x; p < G * HD / 2; p += kConsumers) {
+    const int h = (2 * p) / HD, d = 2 * p - h * HD;
+    const float* rh = base + h * AC::RS;
+    float M = -INFINITY, den = 0.f;
+    float2 acc = make_float2(0.f, 0.f);
+    for (int r0 = 0; r0 < nrec; r0 += kRch) {
+      float mr[kRch], lr[kRch];
+      float2 v[kRch];
 #pragma unroll
-  for (int k = 0; k < E; ++k) {
-    const int e0 = threadIdx.x + (k0 + k) * kConsumers;
-    nrec[k] = 0;
-    dcol[k] = 0;
-    den[k] = 0.f;
-    acc[k] = make_float2(0.f, 0.f);
-    rp[k] = a.rec;
-    key[k] = 0ull;
-    if (e0 < nel) {
-      const int e = e0 < nel ? e0 : nel - 1;  // in range even where the test is folded away
-      const int b = e / npair, col = col0 + 2 * (e - b * npair);
-      const int h = col / HD;
-      const int kvh = h / G, hl = h - kvh * G;
-      const int nt = geo[b * kGeoInts + kGeoNt];
-      dcol[k] = col - h * HD;
-      if (nt > 0) {
-        int pre = kvh * nt;
-        for (int bb = 0; bb < b; ++bb) pre += a.nkv * geo[bb * kGeoInts + kGeoNt];
-        const int cf = part_of(pre, Nt, nctas);
-        nrec[k] = part_of(pre + nt - 1, Nt, nctas) - cf + 1;
-        key[k] = ldcg_pinned64(a.gmax + (size_t)b * a.nh + h);  // used after the loop
-        rp[k] = a.rec + ((size_t)(cf + b * a.nkv + kvh) * 8 + hl) * AC::RS;
-        maxrec = nrec[k] > maxrec ? nrec[k] : maxrec;
-      }
-    }
-  }
-#pragma unroll
-  for (int k = 0; k < E; ++k)
-    M[k] = (unsigned)(key[k] >> 32) == step ? order_float((unsigned)key[k]) : 0.f;
-  for (int r0 = 0; r0 < maxrec; r0 += RCH) {
-    float mr[E][RCH], lr[E][RCH];
-    float2 v[E][RCH];
-#pragma unroll
-    for (int k = 0; k < E; ++k)
-#pragma unroll
-      for (int i = 0; i < RCH; ++i) {
-        mr[k][i] = -INFINITY;
-        lr[k][i] = 0.f;
-        v[k][i] = make_float2(0.f, 0.f);
-        if (r0 + i < nrec[k]) {
-          const float* p = rp[k] + (size_t)(r0 + i) * 8 * AC::RS;
-          mr[k][i] = ldcg_pinned(p + HD);
-          lr[k][i] = ldcg_pinned(p + HD + 1);
-          v[k][i] = ldcg_pinned2(p + dcol[k]);
+      for (int i = 0; i < kRch; ++i) {
+        mr[i] = -INFINITY;
+        lr[i] = 0.f;
+        v[i] = make_float2(0.f, 0.f);
+        if (r0 + i < nrec) {
+          const float* q = rh + (size_t)(r0 + i) * 8 * AC::RS;
+          mr[i] = ldcg_pinned(q + HD);
+          lr[i] = ldcg_pinned(q + HD + 1);
+          v[i] = ldcg_pinned2(q + d);
         }
       }
+      float Mc = mr[0];
 #pragma unroll
-    for (int k = 0; k < E; ++k)
+      for (int i = 1; i < kRch; ++i) Mc = fmaxf(Mc, mr[i]);
+      const float Mn = fmaxf(M, Mc);
+      const float Mu = Mn == -INFINITY ? 0.f : Mn;
+      const float f = exp2f(M - Mu);  // rescale what earlier chunks summed
+      den *= f;
+      acc.x *= f;
+      acc.y *= f;
 #pragma unroll
-      for (int i = 0; i < RCH; ++i) {
-        const float w = exp2f(mr[k][i] - M[k]);
-        den[k] += w * lr[k][i];
-        acc[k].x += w * v[k][i].x;
-        acc[k].y += w * v[k][i].y;
+      for (int i = 0; i < kRch; ++i) {
+        const float w = exp2f(mr[i] - Mu);
+        den += w * lr[i];
+        acc.x += w * v[i].x;
+        acc.y += w * v[i].y;
+      }
+      M = Mn;
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    const float2 o = make_float2(acc.x * inv, acc.y * inv);
+    *reinterpret_cast<float2*>(a.o_attn + ((size_t)b * a.nh + kvh * G + h) * HD + d) = o;
+    const int col = (kvh * G + h) * HD + d, ncols = a.o.nbs * 32;
+    const int sp = col / ncols, cc = col - sp * ncols;
+    uint32_t* xw = a.o_operand + (size_t)sp * a.o.nbs * NT * 128;
+    __half hx, lx, hy, ly;
+    split_f16(o.x, hx, lx);
+    split_f16(o.y, hy, ly);
+    const int w = operand_word<NT>(cc, b);
+    xw[w] = pack_h2(hx, hy);
+    xw[w + 16] = pack_h2(lx, ly);
+    if (b == 0)
+      for (int bz = a.B; bz < 4 * NT; ++bz) {
+        const int wz = operand_word<NT>(cc, bz);
+        xw[wz] = 0u;
+        xw[wz + 16] = 0u;
       }
   }
-#pragma unroll
-  for (int k = 0; k < E; ++k) {
-    const int e = threadIdx.x + (k0 + k) * kConsumers;
-    if (e < nel) {
-      const int b = e / npair, cc = 2 * (e - b * npair);
-      const int h = (col0 + cc) / HD;
-      const float inv = den[k] > 0.f ? 1.f / den[k] : 0.f;
-      const float2 o = make_float2(acc[k].x * inv, acc[k].y * inv);
-      __half hx, lx, hy, ly;
-      split_f16(o.x, hx, lx);
-      split_f16(o.y, hy, ly);
-      const int w = operand_word<NT>(cc, b);
-      xw[w] = pack_h2(hx, hy);
-      xw[w + 16] = pack_h2(lx, ly);
-      if (tap) *reinterpret_cast<float2*>(a.o_tap + ((size_t)b * a.nh + h) * HD + dcol[k]) = o;
-    }
-  }
+  fence_proxy_async_global();  // the operand is read next by bulk copies (async proxy)
 }
 
+// Record of this CTA for unit (b, kvh) is written (all consumer threads past a barrier):
+// take the unit's ticket; the CTA that completes it combines the unit's records.
 template <int HD, int NT>
-__device__ void build_o_operand(const StepArgs& a, const int* geo, int s, int Nt, unsigned step,
-                                bool tap, uint32_t* xw) {
-  const int nbs = a.o.nbs;
-  const int npair = nbs * 16, col0 = s * nbs * 32;
-  for (int i = threadIdx.x; i < nbs * NT * 32 * 4; i += kConsumers) xw[i] = 0u;
+__device__ __noinline__ void finish_unit(const StepArgs& a, const int* geo, int b, int kvh, int G, int Nt,
+                            volatile int* s_last) {
+  int cf, n;
+  unit_ctas(geo, a.nkv, b, kvh, Nt, gridDim.x, &cf, &n);
+  const int unit = b * a.nkv + kvh;
+  if (threadIdx.x == 0) {
+    __threadfence();  // the record before the ticket
+    *s_last = atomicAdd(a.unit_ticket + unit, 1) == n - 1;
+  }
   consumer_sync();
-  const int per = (a.B * npair + kConsumers - 1) / kConsumers;  // <= 4 NT
-  // two shapes only (code size: this runs once per step, from a cold instruction cache)
-  if (per <= 1) {
-    combine_records<HD, NT, 1>(a, geo, col0, npair, Nt, step, tap, xw, 0);
-  } else {
-    constexpr int E = NT >= 2 ? 8 : 4;  // at most 8 elements keep a chunk's loads in registers
-    for (int k0 = 0; k0 < per; k0 += E)
-      combine_records<HD, NT, E>(a, geo, col0, npair, Nt, step, tap, xw, k0);
+  if (*s_last) {
+    __threadfence();
+    merge_unit<HD, NT>(a, b, kvh, G, cf, n);
+    if (threadIdx.x == 0) a.unit_ticket[unit] = 0;
   }
   consumer_sync();
 }
@@ -788,12 +744,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + kStages;
   uint64_t* append_bar = empty + kStages;
   uint64_t* next_bar = append_bar + 1;  // consumers passed the second grid barrier
+  uint64_t* op_bar = reinterpret_cast<uint64_t*>(small + 88);  // o_proj operand copy
   volatile int* s_abort = reinterpret_cast<volatile int*>(small + 64);
   int* s_issued = reinterpret_cast<int*>(small + 68);
-  unsigned* s_step = reinterpret_cast<unsigned*>(small + 72);  // this step's number
+  volatile int* s_last = reinterpret_cast<volatile int*>(small + 72);  // ticket completed
   unsigned long long* s_gbase = reinterpret_cast<unsigned long long*>(small + 80);
+  // small + 88: op_bar
   unsigned* s_max = reinterpret_cast<unsigned*>(small + 96);
-  float* s_inv = reinterpret_cast<float*>(small + 224);
+  float* s_xss = reinterpret_cast<float*>(small + 160);  // sum(x^2) per batch row
+  float* s_inv = reinterpret_cast<float*>(small + 224);  // [16] + 8 warp partials after
   int* geo = reinterpret_cast<int*>(small + 512);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -808,6 +767,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(append_bar, 1);
     mbar_init(next_bar, 1);
+    mbar_init(op_bar, 1);
     *s_abort = 0;
     *s_issued = 0;
     fence_barrier_init();
@@ -960,26 +920,64 @@ __global__ void __launch_bounds__(kThreads, 1)
       build_x_operand<NT>(a, sl.s, reinterpret_cast<uint32_t*>(uni), s_max, s_inv);
       if (tid == 0) {
         const unsigned long long per_step = 3ull * (unsigned)nctas;
-        *s_gbase = arrivals0 / per_step * per_step;       // used by thread 0 only
-        *s_step = (unsigned)(arrivals0 / per_step) + 1u;  // read after the next barrier
+        *s_gbase = arrivals0 / per_step * per_step;  // used by thread 0 only
       }
       for (int r = sl.r0; r < sl.r1; r += a.qkv.ips) {
         const int n = a.qkv.ips < sl.r1 - r ? a.qkv.ips : sl.r1 - r;
         const int st = wait_stage();
         if (st >= 0)
-          gemv_stage<NT, false>(a, a.qkv, sl.s, ring + st * kStageBytes, n, r,
-                                reinterpret_cast<const uint4*>(uni), s_inv, warp, lane);
+          gemv_stage<NT>(a.qkv, a.B, a.qkv_part, sl.s, ring + st * kStageBytes, n, r,
+                         reinterpret_cast<const uint4*>(uni), s_inv, warp, lane);
         release_stage();
       }
     }
-    grid_sync(a.gbar, *s_gbase + nctas, a.err, s_abort);
-
-    // ---------------------------------------------------------- B: attention
+    grid_arrive(a.gbar);
+    // while the other CTAs finish phase A: sum(x^2) of the input rows this CTA's key
+    // tiles belong to, in a fixed order (the input norm's statistic)
     asm volatile("bar.sync 2, %0;" ::"n"(kThreads) : "memory");  // geometry is in
     int Nt = 0;
     for (int b = 0; b < a.B; ++b) Nt += geo[b * kGeoInts + kGeoNt] * a.nkv;
     const int t0 = Nt > 0 ? part_begin(c, Nt, nctas) : 0;
     const int t1 = Nt > 0 ? part_begin(c + 1, Nt, nctas) : 0;
+    {
+      int b0 = a.B, b1 = -1, base = 0;  // batch rows of tiles [t0, t1]
+      for (int b = 0; b < a.B; ++b) {
+        const int span = geo[b * kGeoInts + kGeoNt] * a.nkv;
+        if (span > 0 && base + span > t0 && base <= t1) {
+          b0 = b < b0 ? b : b0;
+          b1 = b;
+        }
+        base += span;
+      }
+      float* s_wred = s_inv + kMaxBatch;  // 8 warp partials (free after phase A)
+      for (int b = b0; b <= b1; ++b) {
+        const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)b * a.H);
+        float acc = 0.f;
+#pragma unroll 2
+        for (int i = tid; i < a.H / 8; i += kConsumers) {
+          const uint4 t = xr[i];
+          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&t);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(h[e]);
+            acc = fmaf(f.x, f.x, acc);
+            acc = fmaf(f.y, f.y, acc);
+          }
+        }
+        acc = warp_sum(acc);
+        if (lane == 0) s_wred[warp] = acc;
+        consumer_sync();
+        if (tid == 0) {
+          float t = 0.f;
+          for (int w = 0; w < kCW; ++w) t += s_wred[w];
+          s_xss[b] = t;
+        }
+        consumer_sync();
+      }
+    }
+    grid_wait(a.gbar, *s_gbase + nctas, a.err, s_abort);
+
+    // ---------------------------------------------------------- B: attention
     {
       uint4* qf = reinterpret_cast<uint4*>(uni);
       float* q_s = reinterpret_cast<float*>(uni + AC::QS_OFF);
@@ -992,7 +990,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int unit = b * a.nkv + kvh;
         const int njobs = G + (owner ? 2 : 0);
         for (int job = warp; job < njobs; job += kCW)
-          head_job<HD>(a, geo, b, kvh, job, G, q_s, lt0 == 0 && a.q_tap != nullptr, lane);
+          head_job<HD>(a, geo, b, kvh, job, G, s_xss[b], q_s, lt0 == 0 && a.q_tap != nullptr,
+                       lane);
         consumer_sync();
         if (owner && tid == 0) mbar_arrive(append_bar);
         // query fragments: rows 0..G-1 = hi(q * qscale), rows 8..8+G-1 = lo
@@ -1066,23 +1065,27 @@ __global__ void __launch_bounds__(kThreads, 1)
               acc += exp2f(red[(w * 8 + h) * AC::RS + HD] - Mu) * red[(w * 8 + h) * AC::RS + d];
           }
           rec[h * AC::RS + d] = acc;
-          if (d == HD)
-            atomicMax(a.gmax + (size_t)b * a.nh + kvh * G + h,
-                      ((unsigned long long)*s_step << 32) | float_order(M));
         }
         consumer_sync();
+        finish_unit<HD, NT>(a, geo, b, kvh, G, Nt, s_last);
       });
       // A CTA without tiles (fewer tiles than CTAs) that sits inside a unit's run of
-      // CTAs leaves a zero-weight record there, so that the combine reads no stale one.
-      if (t0 == t1 && t0 < Nt) {
-        int t = t0, b = 0;
-        while (t >= geo[b * kGeoInts + kGeoNt] * a.nkv) t -= geo[b++ * kGeoInts + kGeoNt] * a.nkv;
-        const int unit = b * a.nkv + t / geo[b * kGeoInts + kGeoNt];
-        float* rec = a.rec + (size_t)(c + unit) * 8 * AC::RS;
+      // CTAs -- its position t0 is a tile of the unit other than the first -- leaves a
+      // zero-weight record there and takes the unit's ticket like the others.
+      int tin = t0, bin = 0;
+      if (t0 == t1 && t0 < Nt)
+        while (tin >= geo[bin * kGeoInts + kGeoNt] * a.nkv)
+          tin -= geo[bin++ * kGeoInts + kGeoNt] * a.nkv;
+      if (t0 == t1 && t0 < Nt && tin % geo[bin * kGeoInts + kGeoNt] != 0) {
+        const int b = bin;
+        const int kvh = tin / geo[b * kGeoInts + kGeoNt];
+        float* rec = a.rec + (size_t)(c + b * a.nkv + kvh) * 8 * AC::RS;
         for (int e = tid; e < 8 * AC::RS; e += kConsumers) {
           const int d = e % AC::RS;
           rec[e] = d == HD ? -INFINITY : 0.f;
         }
+        consumer_sync();
+        finish_unit<HD, NT>(a, geo, b, kvh, G, Nt, s_last);
       }
     }
     grid_sync(a.gbar, *s_gbase + 2ull * nctas, a.err, s_abort);
@@ -1091,14 +1094,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- C: o_proj + residual
     {
       const Slice sl = gemv_slice(a.o, c, nctas);
-      build_o_operand<HD, NT>(a, geo, sl.s, Nt, *s_step, sl.first && a.o_tap != nullptr,
-                              reinterpret_cast<uint32_t*>(uni));
+      // the operand slice of this k-split, written in fragment order by the unit merges
+      if (tid == 0) {
+        const uint32_t bytes = (uint32_t)(a.o.nbs * NT * 512);
+        fence_proxy_async_global();
+        mbar_arrive_expect_tx(op_bar, bytes);
+        bulk_load(uni, a.o_operand + (size_t)sl.s * a.o.nbs * NT * 128, bytes, op_bar);
+      }
+      mbar_wait(op_bar, 0, a.err, s_abort);
       for (int r = sl.r0; r < sl.r1; r += a.o.ips) {
         const int n = a.o.ips < sl.r1 - r ? a.o.ips : sl.r1 - r;
         const int st = wait_stage();
         if (st >= 0)
-          gemv_stage<NT, true>(a, a.o, sl.s, ring + st * kStageBytes, n, r,
-                               reinterpret_cast<const uint4*>(uni), s_inv, warp, lane);
+          gemv_stage<NT>(a.o, a.B, a.y_part, sl.s, ring + st * kStageBytes, n, r,
+                         reinterpret_cast<const uint4*>(uni), nullptr, warp, lane);
         release_stage();
       }
     }

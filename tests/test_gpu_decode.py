@@ -70,6 +70,15 @@ def test_other_head_dims_sliding_linear(hd):
     _case(w, pos=[150, 613])
 
 
+def test_fewer_key_tiles_than_ctas_with_many_units():
+    # 16 sequences of 1..6 key tiles (104 tiles for 152 CTAs): CTAs without tiles sit both
+    # inside units and on their first tiles; every unit's records must combine exactly once
+    w = wl.Workload(name="units16", hidden=512, num_heads=4, num_kv_heads=2, head_dim=64,
+                    layer_type=wl.FULL, window=0, kv_capacity=700, ring=False, batch=16,
+                    rope_theta=1e6, seed=45, seq_pos_range=(0, 699))
+    _case(w, pos=[0, 130, 260, 390, 520, 650, 3, 140, 300, 450, 600, 699, 77, 255, 256, 511])
+
+
 def test_ring_before_and_after_wrap():
     w = wl.Workload(name="ring", hidden=256, num_heads=4, num_kv_heads=1, head_dim=64,
                     layer_type=wl.SLIDING, window=256, kv_capacity=256, ring=True, batch=4,
