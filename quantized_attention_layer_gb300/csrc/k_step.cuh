@@ -594,7 +594,7 @@ __device__ __forceinline__ void unit_ctas(const int* geo, int nkv, int b, int kv
 template <int HD, int NT>
 __device__ void merge_unit(const StepArgs& a, int b, int kvh, int G, int cf, int nrec) {
   using AC = Attn<HD>;
-  constexpr int kRch = 16;
+  constexpr int kRch = 24;
   const int unit = b * a.nkv + kvh;
   const float* base = a.rec + (size_t)(cf + unit) * 8 * AC::RS;
   for (int p = threadIdx.x; p < G * HD / 2; p += kConsumers) {
@@ -665,13 +665,11 @@ __device__ __noinline__ void finish_unit(const StepArgs& a, const int* geo, int 
   int cf, n;
   unit_ctas(geo, a.nkv, b, kvh, Nt, gridDim.x, &cf, &n);
   const int unit = b * a.nkv + kvh;
-  if (threadIdx.x == 0) {
-    __threadfence();  // the record before the ticket
-    *s_last = atomicAdd(a.unit_ticket + unit, 1) == n - 1;
-  }
+  // acquire-release: this CTA's record (ordered by the barrier before) is visible to the
+  // CTA that completes the ticket, and that CTA sees every record
+  if (threadIdx.x == 0) *s_last = atom_add_acq_rel(a.unit_ticket + unit, 1) == n - 1;
   consumer_sync();
   if (*s_last) {
-    __threadfence();
     merge_unit<HD, NT>(a, b, kvh, G, cf, n);
     if (threadIdx.x == 0) a.unit_ticket[unit] = 0;
   }
