@@ -64,8 +64,6 @@ struct hfa_layer {
   float* qkv_part = nullptr;
   float* q_f32 = nullptr;
   float* attn_rec = nullptr;
-  int* unit_ticket = nullptr;
-  uint32_t* o_operand = nullptr;  // o_proj operand slices (fragment order, 4 batch tiles max)
   float* o_f32 = nullptr;
   float* y_part = nullptr;
   unsigned long long* gbar = nullptr;
@@ -199,8 +197,9 @@ static bool is_pow2_hd(int hd) { return hd == 64 || hd == 128 || hd == 256; }
 
 static hfa_status validate_desc(const hfa_layer_desc* d) {
   if (!d) return fail(nullptr, HFA_EINVAL, "desc is NULL");
-  if (d->hidden <= 0 || d->hidden % 64)
-    return fail(nullptr, HFA_EINVAL, "hidden=%d must be a positive multiple of 64", d->hidden);
+  if (d->hidden <= 0 || d->hidden % 64 || d->hidden > 65536)
+    return fail(nullptr, HFA_EINVAL, "hidden=%d must be a positive multiple of 64, at most 65536",
+                d->hidden);
   if (d->num_heads <= 0 || d->num_kv_heads <= 0 || d->num_heads % d->num_kv_heads)
     return fail(nullptr, HFA_EINVAL, "num_heads=%d must be a positive multiple of num_kv_heads=%d",
                 d->num_heads, d->num_kv_heads);
@@ -277,6 +276,9 @@ extern "C" hfa_status hfa_layer_create(const hfa_layer_desc* desc, const void* w
     return fail(nullptr, HFA_EDEVICE, "device %s is sm_%d%d; libhfa is built for sm_103a only",
                 prop.name, prop.major, prop.minor);
   if (!encode_fn()) return fail(nullptr, HFA_EDEVICE, "cuTensorMapEncodeTiled unavailable");
+  if (prop.multiProcessorCount > 256)  // the step kernel's partitions: 32-bit products
+    return fail(nullptr, HFA_EUNSUPPORTED, "%d SMs: at most 256 supported",
+                prop.multiProcessorCount);
 
   hfa_layer* L = new hfa_layer();
   L->d = *desc;
@@ -370,13 +372,11 @@ extern "C" hfa_status hfa_layer_create(const hfa_layer_desc* desc, const void* w
   if (!bf16w) {
     LA(L->qkv_part, (size_t)L->g_qkv.S * d.max_batch * L->rows_qkv);
     LA(L->y_part, (size_t)L->g_o.S * d.max_batch * H);
-    LA(L->o_operand, (size_t)L->g_o.S * L->g_o.nbs * 4 * 128);
   }
   LA(L->q_f32, (size_t)MR * nh * hd);
   // one (m, l, O) record per (CTA, unit) pair of the step kernel: ids c + u are unique
   LA(L->attn_rec, (size_t)(L->num_sms + units) * attn_record_floats(hd));
   LA(L->gbar, 1);
-  LA(L->unit_ticket, (size_t)d.max_batch * nkv);
   LA(L->o_f32, (size_t)MR * nh * hd);
   LA(L->err, 1);
   LA(L->x_stage, (size_t)d.max_batch * H);
@@ -392,7 +392,6 @@ extern "C" hfa_status hfa_layer_create(const hfa_layer_desc* desc, const void* w
   }
 
   LC(cudaMemsetAsync(L->gbar, 0, 8, s), "memset");
-  LC(cudaMemsetAsync(L->unit_ticket, 0, (size_t)d.max_batch * nkv * 4, s), "memset");
   LC(cudaMemsetAsync(L->err, 0, 4, s), "memset");
   if (d.max_verify_len > 0) {
     hfa_status vs = hfa::verify_create(L->d, L->num_sms, &L->verify);
@@ -524,6 +523,9 @@ extern "C" hfa_status hfa_decode_step(hfa_layer* L, void* stream, const void* x,
   const long long rows = (long long)batch * nkv * d.kv_capacity;
   if (rows + 256 >= (1ll << 31))
     return fail(L, HFA_EUNSUPPORTED, "cache too large for 32-bit TMA rows");
+  // the step kernel's key-tile partition (64 keys per tile at least) in 32-bit arithmetic
+  if (rows / 64 + (long long)batch * nkv >= (1ll << 24))
+    return fail(L, HFA_EUNSUPPORTED, "cache too large: 2^24 key tiles or more");
   hfa_status st = ensure_maps(L, kc, vc, (int)rows);
   if (st != HFA_OK) return st;
 
@@ -543,9 +545,7 @@ extern "C" hfa_status hfa_decode_step(hfa_layer* L, void* stream, const void* x,
   sa.rec = L->attn_rec;
   sa.y_part = L->y_part;
   sa.gbar = L->gbar;
-  sa.unit_ticket = L->unit_ticket;
   sa.o_attn = L->o_f32;  // also the attention tap
-  sa.o_operand = L->o_operand;
   sa.err = L->err;
   sa.q_tap = taps ? L->q_f32 : nullptr;
   sa.k_tap = L->k_tap;
@@ -789,10 +789,6 @@ extern "C" hfa_status hfa_check_device_status(hfa_layer* L, void* stream) {
   CK(L, cudaMemsetAsync(L->err, 0, 4, s), "clear status");
   // a step that gave up may have left the grid barrier mid-count
   CK(L, cudaMemsetAsync(L->gbar, 0, 8, s), "reset grid barrier");
-  if (L->unit_ticket)
-    CK(L, cudaMemsetAsync(L->unit_ticket, 0, (size_t)L->d.max_batch * L->d.num_kv_heads * 4, s),
-       "reset unit tickets");
-  CK(L, cudaStreamSynchronize(s), "sync");
   CK(L, cudaStreamSynchronize(s), "sync");
   return fail(L, HFA_EDEVICE, "device status 0x%x:%s%s%s", v,
               (v & kErrWaitTimeout) ? " a bounded wait gave up;" : "",

@@ -87,9 +87,7 @@ struct StepArgs {
   float* qkv_part;         // f32 [qkv.S][B][(nh + 2 nkv) hd]: one partial sum per k-split
   float* rec;              // f32 [(grid + B nkv)][8][hd + 4]: (O, m, l) per key range
   float* y_part;           // f32 [o.S][B][H]: one partial o_proj sum per k-split
-  int* unit_ticket;        // [B * nkv]: records written per (sequence, KV head); zero between steps
   float* o_attn;           // f32 [B, nh, hd]: attention output (combined records)
-  uint32_t* o_operand;     // [o.S][o.nbs * NT * 128] words: o_proj operand, fragment order
   unsigned long long* gbar;  // grid barrier arrivals: only grows, three per CTA per step, so
                              // it also numbers the steps (graph replays included)
   unsigned* err;

@@ -45,7 +45,7 @@ constexpr int kMaxBatch = 16;
 constexpr int kEarlyTiles = 2;            // K/V tiles prefetched into L2 during phase A
 
 // per batch row: position, visible slots [lo, hi], key tiles, tile of the new slot, slot
-enum { kGeoP = 0, kGeoLo, kGeoHi, kGeoNt, kGeoTn, kGeoSlot, kGeoInts = 8 };
+enum { kGeoP = 0, kGeoLo, kGeoHi, kGeoNt, kGeoTn, kGeoSlot, kGeoPre, kGeoInts = 8 };
 
 // Attention tile shape: NC key groups of 16 keys per tile; with HD = 256 the 8 consumer
 // warps pair up on a key group (both form S = Q K^T, each accumulates half of O's dims),
@@ -107,17 +107,14 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 }
 
 // Balanced partition of n items over P parts: part c owns [begin(c), begin(c + 1)).
-// 32-bit arithmetic whenever the products fit (64-bit division is a long software
-// sequence, and every CTA runs these before its first load).
-__device__ __forceinline__ int part_begin(int c, long long n, int P) {
-  if (n < (1ll << 24) && P <= 256) return (int)((unsigned)c * (unsigned)n / (unsigned)P);
-  return (int)((long long)c * n / P);
+// 32-bit products: the host keeps every partitioned count below 2^24 (key tiles, B x H
+// outputs, row groups) and the grid at most 256 CTAs.
+__device__ __forceinline__ int part_begin(int c, int n, int P) {
+  return (int)((unsigned)c * (unsigned)n / (unsigned)P);
 }
 // the part that owns item t (0 <= t < n): the largest c with begin(c) <= t
-__device__ __forceinline__ int part_of(int t, long long n, int P) {
-  if (n < (1ll << 24) && P <= 256)
-    return (int)(((unsigned)(t + 1) * (unsigned)P - 1u) / (unsigned)n);
-  return (int)(((long long)(t + 1) * P - 1) / n);
+__device__ __forceinline__ int part_of(int t, int n, int P) {
+  return (int)(((unsigned)(t + 1) * (unsigned)P - 1u) / (unsigned)n);
 }
 
 // Rows of a split-K GEMV owned by CTA c: the CTAs are dealt out over the k-splits, and
@@ -320,48 +317,44 @@ __device__ void build_x_operand(const StepArgs& a, int s, uint32_t* xw, unsigned
   consumer_sync();
 }
 
-// Residual epilogue after the last grid barrier: CTA c finishes its share of the B x H
-// outputs, out = bf16(x + sum over the o_proj k-splits), the splits added in a fixed
-// order; each thread issues all of its partial-sum loads before adding.
-__device__ __forceinline__ void finish_outputs(const StepArgs& a, int c, int nctas) {
-  constexpr int kMaxPer = 2;  // outputs per thread per round
-  const long long n = (long long)a.B * a.H;
+// Residual epilogue after the last grid barrier: CTA c finishes its share [i0, i1) of the
+// B x H outputs, out = bf16(x + sum over the o_proj k-splits), the splits added in order
+// 0, 1, ..., S - 1.  A round covers kPer * per outputs (per = 256 / S): thread (k, sp)
+// loads split sp of outputs k, k + per, ... (all in flight together) into shared memory,
+// then one thread per output adds its S partial sums.
+static __device__ void finish_outputs(const StepArgs& a, int c, int nctas, float* red) {
+  constexpr int kPer = 8;
+  const int S = a.o.S;  // <= grid <= 256
+  const int n = a.B * a.H;
   const int i0 = part_begin(c, n, nctas), i1 = part_begin(c + 1, n, nctas);
   const size_t split_stride = (size_t)a.B * a.H;
-  for (int base = i0; base < i1; base += kMaxPer * kConsumers) {
-    float y[kMaxPer];
+  const int tid = threadIdx.x;
+  const int per = kConsumers / S, k = tid / S, sp = tid - k * S;
+  const float* ys = a.y_part + sp * split_stride;
+#pragma unroll 1
+  for (int base = i0; base < i1; base += kPer * per) {
+    if (k < per) {
+      float v[kPer];
 #pragma unroll
-    for (int k = 0; k < kMaxPer; ++k) y[k] = 0.f;
-    for (int s0 = 0; s0 < a.o.S; s0 += 4) {
-      float t[4][kMaxPer];  // every load of four splits issued before the first add
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int s = s0 + u < a.o.S ? s0 + u : a.o.S - 1;
-#pragma unroll
-        for (int k = 0; k < kMaxPer; ++k) {
-          const int i = base + threadIdx.x + k * kConsumers;
-          t[u][k] = __ldcg(a.y_part + s * split_stride + (i < i1 ? i : i1 - 1));
-        }
+      for (int u = 0; u < kPer; ++u) {
+        const int i = base + u * per + k;
+        v[u] = __ldcg(ys + (i < i1 ? i : i1 - 1));
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (s0 + u < a.o.S)
-#pragma unroll
-          for (int k = 0; k < kMaxPer; ++k) {
-            const int i = base + threadIdx.x + k * kConsumers;
-            if (i < i1) y[k] += t[u][k];
-          }
+      for (int u = 0; u < kPer; ++u) red[(u * per + k) * S + sp] = v[u];
     }
-#pragma unroll
-    for (int k = 0; k < kMaxPer; ++k) {
-      const int i = base + threadIdx.x + k * kConsumers;
-      const float xi = __bfloat162float(a.x[i < i1 ? i : i1 - 1]);
-      if (i < i1) {
-        const float o = xi + y[k];
-        a.out[i] = __float2bfloat16_rn(o);
-        if (a.out_tap) a.out_tap[i] = o;
-      }
+    consumer_sync();
+#pragma unroll 1
+    for (int o = tid; o < kPer * per && base + o < i1; o += kConsumers) {
+      const int i = base + o;
+      float y = 0.f;
+#pragma unroll 1
+      for (int t = 0; t < S; ++t) y += red[o * S + t];
+      const float r = __bfloat162float(a.x[i]) + y;
+      a.out[i] = __float2bfloat16_rn(r);
+      if (a.out_tap) a.out_tap[i] = r;
     }
+    consumer_sync();
   }
 }
 
@@ -540,10 +533,10 @@ __device__ __forceinline__ void attn_tile(uint32_t kb, const uint4* qf, int key0
   mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
   const float m_new = fmaxf(m, mloc);
   const float m_use = m_new == -INFINITY ? 0.f : m_new;
-  const float corr = exp2f(m - m_use);
+  const float corr = ex2_approx(m - m_use);
   float p[4];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) p[e] = exp2f(sv[e] - m_use);
+  for (int e = 0; e < 4; ++e) p[e] = ex2_approx(sv[e] - m_use);
   l = l * corr + (p[0] + p[1]) + (p[2] + p[3]);
   m = m_new;
 #pragma unroll
@@ -574,106 +567,147 @@ __device__ __forceinline__ void attn_tile(uint32_t kb, const uint4* qf, int key0
   }
 }
 
-// CTAs that hold a record of unit u (its tiles, plus CTAs without tiles sitting inside
-// that run): [first, first + count).
-__device__ __forceinline__ void unit_ctas(const int* geo, int nkv, int b, int kvh, int Nt,
-                                          int nctas, int* first, int* count) {
-  const int nt = geo[b * kGeoInts + kGeoNt];
-  int pre = kvh * nt;
-  for (int bb = 0; bb < b; ++bb) pre += nkv * geo[bb * kGeoInts + kGeoNt];
-  *first = part_of(pre, Nt, nctas);
-  *count = part_of(pre + nt - 1, Nt, nctas) - *first + 1;
-}
-
-// Combine of one unit's records (run by the CTA whose record came last): for every query
-// head h of the group and column pair (d, d + 1),
+// The o_proj operand of k-split s, merged from the attention records after the second
+// grid barrier by every CTA that multiplies that split (each merges what it needs; no
+// CTA waits on another's merge).  For batch row b and column pair (d, d + 1) of query
+// head h, over the records r of h's unit (one per CTA that attended over its key tiles):
 //   o = sum_r 2^(m_r - M) O_r / sum_r 2^(m_r - M) l_r,   M = max_r m_r,
-// written as the attention output (fp32) and, as fp16 hi + lo, straight into the o_proj
-// operand in MMA fragment order (one slice per k-split; sequence 0 also zeroes the batch
-// slots past B).  Each thread issues the loads of up to kRch records before using any.
-template <int HD, int NT>
-__device__ void merge_unit(const StepArgs& a, int b, int kvh, int G, int cf, int nrec) {
+// stored as fp16 hi + lo in MMA fragment order.  The first CTA of the split also writes o
+// as the fp32 attention output.  A thread owns one column pair and takes JG of its batch
+// rows at a time, with the loads of RU records of each in flight together.
+// units[b * nk + kvh - kvh0] = first record slot | record count << 16 (merge_operand).
+template <int HD, int NT, int JG, int RU>
+__device__ void merge_jobs(const StepArgs& a, int G, int s, bool write_attn, uint32_t* xw,
+                           const unsigned* units, int nk, int kvh0) {
   using AC = Attn<HD>;
-  constexpr int kRch = 24;
-  const int unit = b * a.nkv + kvh;
-  const float* base = a.rec + (size_t)(cf + unit) * 8 * AC::RS;
-  for (int p = threadIdx.x; p < G * HD / 2; p += kConsumers) {
-    const int h = (2 * p) / HD, d = 2 * p - h * HD;
-    const float* rh = base + h * AC::RS;
-    float M = -INFINITY, den = 0.f;
-    float2 acc = make_float2(0.f, 0.f);
-    for (int r0 = 0; r0 < nrec; r0 += kRch) {
-      float mr[kRch], lr[kRch];
-      float2 v[kRch];
+  const int npairs = a.o.nbs * 16;  // <= 256: bstep batch rows per column pair
+  int pair = threadIdx.x, b0 = 0, bstep = 0;
+  while (pair >= npairs) {
+    pair -= npairs;
+    ++b0;
+  }
+  for (int t = npairs; t <= kConsumers; t += npairs) ++bstep;
+  if (b0 >= bstep) return;
+  const int col = s * 2 * npairs + 2 * pair;
+  const int hq = col / HD, d = col % HD;
+  const int kvh = hq / G;
+  const float* row0 = a.rec + (size_t)(hq - kvh * G) * AC::RS;
+  const unsigned* ut = units + (kvh - kvh0);
+  for (int bg = b0; bg < a.B; bg += JG * bstep) {
+    const float* row[JG];
+    int cnt[JG], maxc = 0;
 #pragma unroll
-      for (int i = 0; i < kRch; ++i) {
-        mr[i] = -INFINITY;
-        lr[i] = 0.f;
-        v[i] = make_float2(0.f, 0.f);
-        if (r0 + i < nrec) {
-          const float* q = rh + (size_t)(r0 + i) * 8 * AC::RS;
-          mr[i] = ldcg_pinned(q + HD);
-          lr[i] = ldcg_pinned(q + HD + 1);
-          v[i] = ldcg_pinned2(q + d);
+    for (int g = 0; g < JG; ++g) {
+      const int b = bg + g * bstep;
+      const unsigned u = b < a.B ? ut[b * nk] : 0u;
+      cnt[g] = (int)(u >> 16);
+      maxc = cnt[g] > maxc ? cnt[g] : maxc;
+      row[g] = row0 + (size_t)(u & 0xffffu) * 8 * AC::RS;
+    }
+    float M[JG], den[JG];
+    float2 acc[JG];
+#pragma unroll
+    for (int g = 0; g < JG; ++g) {
+      M[g] = -INFINITY;
+      den[g] = 0.f;
+      acc[g] = make_float2(0.f, 0.f);
+    }
+#pragma unroll 1
+    for (int r0 = 0; r0 < maxc; r0 += RU) {
+      float2 ml[JG][RU], v[JG][RU];
+#pragma unroll
+      for (int g = 0; g < JG; ++g) {
+        const int last = cnt[g] > 0 ? cnt[g] - 1 : 0;
+#pragma unroll
+        for (int i = 0; i < RU; ++i) {
+          // clamped to a record of the job (in range); slots past its count weigh 0
+          const float* q = row[g] + min(r0 + i, last) * (8 * AC::RS);
+          ml[g][i] = __ldcg(reinterpret_cast<const float2*>(q + HD));
+          v[g][i] = __ldcg(reinterpret_cast<const float2*>(q + d));
         }
       }
-      float Mc = mr[0];
 #pragma unroll
-      for (int i = 1; i < kRch; ++i) Mc = fmaxf(Mc, mr[i]);
-      const float Mn = fmaxf(M, Mc);
-      const float Mu = Mn == -INFINITY ? 0.f : Mn;
-      const float f = exp2f(M - Mu);  // rescale what earlier chunks summed
-      den *= f;
-      acc.x *= f;
-      acc.y *= f;
+      for (int g = 0; g < JG; ++g) {
+        float Mc = M[g];
 #pragma unroll
-      for (int i = 0; i < kRch; ++i) {
-        const float w = exp2f(mr[i] - Mu);
-        den += w * lr[i];
-        acc.x += w * v[i].x;
-        acc.y += w * v[i].y;
+        for (int i = 0; i < RU; ++i) {
+          if (r0 + i >= cnt[g]) {  // weight 0, and nothing of a record outside the run
+            ml[g][i] = make_float2(-INFINITY, 0.f);
+            v[g][i] = make_float2(0.f, 0.f);
+          }
+          Mc = fmaxf(Mc, ml[g][i].x);
+        }
+        const float Mu = Mc == -INFINITY ? 0.f : Mc;
+        const float f = ex2_approx(M[g] - Mu);  // rescales what earlier chunks summed
+        den[g] *= f;
+        acc[g].x *= f;
+        acc[g].y *= f;
+#pragma unroll
+        for (int i = 0; i < RU; ++i) {
+          const float w = ex2_approx(ml[g][i].x - Mu);
+          den[g] = fmaf(w, ml[g][i].y, den[g]);
+          acc[g].x = fmaf(w, v[g][i].x, acc[g].x);
+          acc[g].y = fmaf(w, v[g][i].y, acc[g].y);
+        }
+        M[g] = Mc;
       }
-      M = Mn;
     }
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-    const float2 o = make_float2(acc.x * inv, acc.y * inv);
-    *reinterpret_cast<float2*>(a.o_attn + ((size_t)b * a.nh + kvh * G + h) * HD + d) = o;
-    const int col = (kvh * G + h) * HD + d, ncols = a.o.nbs * 32;
-    const int sp = col / ncols, cc = col - sp * ncols;
-    uint32_t* xw = a.o_operand + (size_t)sp * a.o.nbs * NT * 128;
-    __half hx, lx, hy, ly;
-    split_f16(o.x, hx, lx);
-    split_f16(o.y, hy, ly);
-    const int w = operand_word<NT>(cc, b);
-    xw[w] = pack_h2(hx, hy);
-    xw[w + 16] = pack_h2(lx, ly);
-    if (b == 0)
-      for (int bz = a.B; bz < 4 * NT; ++bz) {
-        const int wz = operand_word<NT>(cc, bz);
-        xw[wz] = 0u;
-        xw[wz + 16] = 0u;
+#pragma unroll
+    for (int g = 0; g < JG; ++g) {
+      const int b = bg + g * bstep;
+      if (b < a.B) {
+        const float inv = den[g] > 0.f ? rcp_approx(den[g]) : 0.f;
+        const float2 o = make_float2(acc[g].x * inv, acc[g].y * inv);
+        if (write_attn) *reinterpret_cast<float2*>(a.o_attn + (size_t)b * a.nh * HD + col) = o;
+        __half hx, lx, hy, ly;
+        split_f16(o.x, hx, lx);
+        split_f16(o.y, hy, ly);
+        const int w = operand_word<NT>(2 * pair, b);
+        xw[w] = pack_h2(hx, hy);
+        xw[w + 16] = pack_h2(lx, ly);
       }
+    }
   }
-  fence_proxy_async_global();  // the operand is read next by bulk copies (async proxy)
 }
 
-// Record of this CTA for unit (b, kvh) is written (all consumer threads past a barrier):
-// take the unit's ticket; the CTA that completes it combines the unit's records.
+constexpr int kOperandBytes = 16 * 4 * 512;  // o_proj operand: nbs <= 16 blocks, NT <= 4
+static_assert(kOperandBytes + kMaxBatch * 9 * 4 <= kUnionBytes, "unit table after the operand");
+
+// Builds the o_proj operand of k-split s in xw (the union): zero columns for the batch
+// slots past B, a table of the record runs of the units the split reads, then the merge.
+// The host keeps the grid-wide key-tile count below 2^24 and the grid at most 256 CTAs,
+// so the CTA that owns tile t, ((t + 1) P - 1) / Nt, is exact in 32-bit arithmetic.
 template <int HD, int NT>
-__device__ __noinline__ void finish_unit(const StepArgs& a, const int* geo, int b, int kvh, int G, int Nt,
-                            volatile int* s_last) {
-  int cf, n;
-  unit_ctas(geo, a.nkv, b, kvh, Nt, gridDim.x, &cf, &n);
-  const int unit = b * a.nkv + kvh;
-  // acquire-release: this CTA's record (ordered by the barrier before) is visible to the
-  // CTA that completes the ticket, and that CTA sees every record
-  if (threadIdx.x == 0) *s_last = atom_add_acq_rel(a.unit_ticket + unit, 1) == n - 1;
-  consumer_sync();
-  if (*s_last) {
-    merge_unit<HD, NT>(a, b, kvh, G, cf, n);
-    if (threadIdx.x == 0) a.unit_ticket[unit] = 0;
+__device__ __noinline__ void merge_operand(const StepArgs& a, const int* geo, int Nt, int G,
+                                           int s, bool write_attn, uint32_t* xw) {
+  const int npairs = a.o.nbs * 16;
+  const int tid = threadIdx.x;
+  for (int e = tid; e < (4 * NT - a.B) * npairs; e += kConsumers) {
+    const int b = a.B + e / npairs, cc = 2 * (e % npairs);
+    const int w = operand_word<NT>(cc, b);
+    xw[w] = 0u;
+    xw[w + 16] = 0u;
+  }
+  // KV heads whose query heads own the split's columns [s W, s W + W): at most 9
+  const int W = 2 * npairs;
+  const int kvh0 = s * W / HD / G, nk = (s * W + W - 1) / HD / G - kvh0 + 1;
+  unsigned* units = reinterpret_cast<unsigned*>(reinterpret_cast<uint8_t*>(xw) + kOperandBytes);
+  if (tid < a.B * nk) {
+    const int b = tid / nk, kvh = kvh0 + tid - b * nk;
+    const int nt = geo[b * kGeoInts + kGeoNt];
+    const int pre = geo[b * kGeoInts + kGeoPre] + kvh * nt;  // the unit's first tile
+    const unsigned P = gridDim.x;
+    const int first = nt > 0 ? (int)(((unsigned)(pre + 1) * P - 1u) / (unsigned)Nt) : 0;
+    const int last = nt > 0 ? (int)(((unsigned)(pre + nt) * P - 1u) / (unsigned)Nt) : -1;
+    // the record of CTA first + r for unit u sits in slot first + r + u
+    units[tid] = (unsigned)(first + b * a.nkv + kvh) | ((unsigned)(last - first + 1) << 16);
   }
   consumer_sync();
+  // a thread with one batch row: many records; several batch rows: few records each
+  if (a.B * npairs <= kConsumers)
+    merge_jobs<HD, NT, 1, 12>(a, G, s, write_attn, xw, units, nk, kvh0);
+  else
+    merge_jobs<HD, NT, 4, 3>(a, G, s, write_attn, xw, units, nk, kvh0);
 }
 
 // ------------------------------------------------------------------ the load schedule
@@ -742,12 +776,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + kStages;
   uint64_t* append_bar = empty + kStages;
   uint64_t* next_bar = append_bar + 1;  // consumers passed the second grid barrier
-  uint64_t* op_bar = reinterpret_cast<uint64_t*>(small + 88);  // o_proj operand copy
   volatile int* s_abort = reinterpret_cast<volatile int*>(small + 64);
   int* s_issued = reinterpret_cast<int*>(small + 68);
-  volatile int* s_last = reinterpret_cast<volatile int*>(small + 72);  // ticket completed
   unsigned long long* s_gbase = reinterpret_cast<unsigned long long*>(small + 80);
-  // small + 88: op_bar
   unsigned* s_max = reinterpret_cast<unsigned*>(small + 96);
   float* s_xss = reinterpret_cast<float*>(small + 160);  // sum(x^2) per batch row
   float* s_inv = reinterpret_cast<float*>(small + 224);  // [16] + 8 warp partials after
@@ -765,7 +796,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(append_bar, 1);
     mbar_init(next_bar, 1);
-    mbar_init(op_bar, 1);
     *s_abort = 0;
     *s_issued = 0;
     fence_barrier_init();
@@ -818,6 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     // visible slots and key tiles of each sequence, for both sides (consumers read them
     // after barrier 2)
+    int span = 0;  // key tiles of this lane's sequence over all KV heads
     if (lane < a.B) {
       const int b = lane < a.B ? lane : 0;  // in range even where the test is folded away
       const int P = a.seq_pos[b];
@@ -839,8 +870,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       gb[kGeoNt] = bad ? 0 : (hi - lo + 1 + AC::T - 1) / AC::T;
       gb[kGeoTn] = bad ? -1 : (slot - lo) / AC::T;
       gb[kGeoSlot] = slot;
+      span = gb[kGeoNt] * a.nkv;
       if (bad && c == 0) atomicOr(a.err, kErrBadPosition);
     }
+    int incl = span;  // inclusive prefix over the sequences
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane < a.B) geo[lane * kGeoInts + kGeoPre] = incl - span;
     __syncwarp();
     asm volatile("bar.arrive 2, %0;" ::"n"(kThreads) : "memory");
     if (lane == 0) {
@@ -850,6 +889,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       sc.t1 = Nt > 0 ? part_begin(c + 1, Nt, nctas) : 0;
       sc.nB = sc.t1 - sc.t0;
       uint32_t n_app = 0;  // appends waited for (one per unit whose new slot is here)
+      const uint64_t kv_policy = l2_policy_evict_first();  // the cache is read once a step
       for (int j = 0; j < kEarlyTiles && j < sc.nB; ++j) prefetch_load<HD>(a, sc, geo, sc.nA + j);
       for (int k = (int)q; k < sc.nA && ok; ++k) issue_gemv(a.qkv, sc.sa, k);
       for_each_segment(geo, a.B, a.nkv, sc.t0, sc.t1, [&](int b, int kvh, int lt0, int lt1) {
@@ -877,8 +917,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int row = row_base + lt * AC::T;
 #pragma unroll
           for (int j = 0; j < AC::BOXES; ++j) {
-            tma_load_2d(kt + j * AC::T * 128, &tmk, &full[st], 64 * j, row);
-            tma_load_2d(vt + j * AC::T * 128, &tmv, &full[st], 64 * j, row);
+            tma_load_2d_hint(kt + j * AC::T * 128, &tmk, &full[st], 64 * j, row, kv_policy);
+            tma_load_2d_hint(vt + j * AC::T * 128, &tmv, &full[st], 64 * j, row, kv_policy);
           }
           ++q;
         }
@@ -1060,16 +1100,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
 #pragma unroll
             for (int w = 0; w < AC::NC; ++w)
-              acc += exp2f(red[(w * 8 + h) * AC::RS + HD] - Mu) * red[(w * 8 + h) * AC::RS + d];
+              acc += ex2_approx(red[(w * 8 + h) * AC::RS + HD] - Mu) * red[(w * 8 + h) * AC::RS + d];
           }
           rec[h * AC::RS + d] = acc;
         }
-        consumer_sync();
-        finish_unit<HD, NT>(a, geo, b, kvh, G, Nt, s_last);
+        consumer_sync();  // the next segment's queries overwrite the merge area
       });
       // A CTA without tiles (fewer tiles than CTAs) that sits inside a unit's run of
       // CTAs -- its position t0 is a tile of the unit other than the first -- leaves a
-      // zero-weight record there and takes the unit's ticket like the others.
+      // zero-weight record there, so that the unit's records fill one run of slots.
       int tin = t0, bin = 0;
       if (t0 == t1 && t0 < Nt)
         while (tin >= geo[bin * kGeoInts + kGeoNt] * a.nkv)
@@ -1082,8 +1121,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int d = e % AC::RS;
           rec[e] = d == HD ? -INFINITY : 0.f;
         }
-        consumer_sync();
-        finish_unit<HD, NT>(a, geo, b, kvh, G, Nt, s_last);
       }
     }
     grid_sync(a.gbar, *s_gbase + 2ull * nctas, a.err, s_abort);
@@ -1092,14 +1129,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- C: o_proj + residual
     {
       const Slice sl = gemv_slice(a.o, c, nctas);
-      // the operand slice of this k-split, written in fragment order by the unit merges
-      if (tid == 0) {
-        const uint32_t bytes = (uint32_t)(a.o.nbs * NT * 512);
-        fence_proxy_async_global();
-        mbar_arrive_expect_tx(op_bar, bytes);
-        bulk_load(uni, a.o_operand + (size_t)sl.s * a.o.nbs * NT * 128, bytes, op_bar);
-      }
-      mbar_wait(op_bar, 0, a.err, s_abort);
+      merge_operand<HD, NT>(a, geo, Nt, G, sl.s, sl.first, reinterpret_cast<uint32_t*>(uni));
+      consumer_sync();
       for (int r = sl.r0; r < sl.r1; r += a.o.ips) {
         const int n = a.o.ips < sl.r1 - r ? a.o.ips : sl.r1 - r;
         const int st = wait_stage();
@@ -1110,7 +1141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     grid_sync(a.gbar, *s_gbase + 3ull * nctas, a.err, s_abort);
-    finish_outputs(a, c, nctas);
+    finish_outputs(a, c, nctas, reinterpret_cast<float*>(uni));
   }
 
   // drain: after a give-up, copies may still be landing in the ring
