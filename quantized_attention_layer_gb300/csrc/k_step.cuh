@@ -200,7 +200,7 @@ __device__ __forceinline__ void grid_sync(unsigned long long* gbar, unsigned lon
 // One Q8_0 tile (16 rows x 32 columns) times every batch tile of the operand.
 template <int NT>
 __device__ __forceinline__ void q8_tile_mma(float (&acc)[NT][4], const uint4 w, uint32_t dbits,
-                                            const uint4* xrow) {
+                                            uint32_t xrow) {
   uint32_t A0[4], A1[4];
   A0[0] = u8x2_to_h2(w.x, kSelLo);
   A0[1] = u8x2_to_h2(w.y, kSelLo);
@@ -214,7 +214,7 @@ __device__ __forceinline__ void q8_tile_mma(float (&acc)[NT][4], const uint4 w, 
   const float dg = __low2float(d2), dg8 = __high2float(d2);
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const uint4 xb = xrow[nt * 32];
+    const uint4 xb = lds128(xrow + nt * 512);
     float tmp[4] = {0.f, 0.f, 0.f, 0.f};
     mma_f16(tmp, A0, xb.x, xb.y);
     mma_f16(tmp, A1, xb.z, xb.w);
@@ -317,6 +317,34 @@ __device__ void build_x_operand(const StepArgs& a, int s, uint32_t* xw, unsigned
   consumer_sync();
 }
 
+// sum(x^2) of one input row over its H columns, by one warp in a fixed order: 16-byte
+// loads strided over the lanes (16 in flight per lane), then the warp tree.
+__device__ __forceinline__ float row_sumsq(const __nv_bfloat16* x, int H, int lane) {
+  const uint4* xr = reinterpret_cast<const uint4*>(x);
+  const int n = H / 8;
+  float acc = 0.f;
+  for (int i0 = 0; i0 < n; i0 += 32 * 16) {
+    uint4 u[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const int i = i0 + k * 32 + lane;
+      u[k] = xr[i < n ? i : n - 1];  // in range; lanes past the row add nothing
+      if (i >= n) u[k] = make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u[k]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(h[e]);
+        acc = fmaf(f.x, f.x, acc);
+        acc = fmaf(f.y, f.y, acc);
+      }
+    }
+  }
+  return warp_sum(acc);
+}
+
 // Residual epilogue after the last grid barrier: CTA c finishes its share [i0, i1) of the
 // B x H outputs, out = bf16(x + sum over the o_proj k-splits), the splits added in order
 // 0, 1, ..., S - 1.  A round covers kPer * per outputs (per = 256 / S): thread (k, sp)
@@ -362,12 +390,12 @@ static __device__ void finish_outputs(const StepArgs& a, int c, int nctas, float
 // one whole item per warp at a time.  The partial sums of rows [16 r, 16 r + 16) over an
 // item's tiles are stored (no atomics) into the k-split's slice of `part`, times the
 // batch row's factor `scale` (nullable: 1).  One out-of-line copy serves both GEMVs, so
-// the o_proj phase runs code the QKV phase already brought into the instruction cache.
+// the o_proj phase runs code the QKV phase already brought into the instruction cache;
+// the stage and the operand fragments come as shared-window addresses (ld.shared).
 template <int NT>
 __device__ __noinline__ void gemv_stage(const StepGemv& gm, int B, float* part, int s,
-                                        const uint8_t* stage, int n_items, int r_first,
-                                        const uint4* frag, const float* scale, int warp,
-                                        int lane) {
+                                        uint32_t stage, int n_items, int r_first, uint32_t frag,
+                                        const float* scale, int warp, int lane) {
   const int nbs = gm.nbs;
   const int g = lane >> 2, t = lane & 3;
   const int R16 = gm.R * 16;
@@ -376,13 +404,13 @@ __device__ __noinline__ void gemv_stage(const StepGemv& gm, int B, float* part, 
     float acc[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-    const uint8_t* tp = stage + (size_t)item * nbs * kQ8TileBytes;
-    const uint4* fr = frag + lane;
+    const uint32_t tp = stage + (uint32_t)(item * nbs * kQ8TileBytes);
+    const uint32_t fr = frag + lane * 16;
 #pragma unroll 4
     for (int i = 0; i < nbs; ++i) {
-      const uint4 w = *reinterpret_cast<const uint4*>(tp + i * kQ8TileBytes + lane * 16);
-      const uint32_t d = *reinterpret_cast<const uint32_t*>(tp + i * kQ8TileBytes + 512 + g * 4);
-      q8_tile_mma<NT>(acc, w, d, fr + i * NT * 32);
+      const uint4 w = lds128(tp + i * kQ8TileBytes + lane * 16);
+      const uint32_t d = lds32(tp + i * kQ8TileBytes + 512 + g * 4);
+      q8_tile_mma<NT>(acc, w, d, fr + i * NT * 512);
     }
     const int r = r_first + item;
 #pragma unroll
@@ -569,61 +597,68 @@ __device__ __forceinline__ void attn_tile(uint32_t kb, const uint4* qf, int key0
 
 // The o_proj operand of k-split s, merged from the attention records after the second
 // grid barrier by every CTA that multiplies that split (each merges what it needs; no
-// CTA waits on another's merge).  For batch row b and column pair (d, d + 1) of query
-// head h, over the records r of h's unit (one per CTA that attended over its key tiles):
+// CTA waits on another's merge).  For batch row b and columns d .. d + 3 of query head h,
+// over the records r of h's unit (one per CTA that attended over its key tiles):
 //   o = sum_r 2^(m_r - M) O_r / sum_r 2^(m_r - M) l_r,   M = max_r m_r,
 // stored as fp16 hi + lo in MMA fragment order.  The first CTA of the split also writes o
-// as the fp32 attention output.  A thread owns one column pair and takes JG of its batch
-// rows at a time, with the loads of RU records of each in flight together.
-// units[b * nk + kvh - kvh0] = first record slot | record count << 16 (merge_operand).
+// as the fp32 attention output.  A job is a column quad of one batch row.  With at most
+// 256 jobs, RL = 256 / jobs (a power of two) lanes share a job, lane k taking records
+// k, k + RL, ..., and their partial (M, den, acc) combine over a fixed butterfly; with
+// more jobs, a thread takes JG of them at a time.  Each lane keeps the loads of RU records
+// of each of its jobs in flight together.
+// units[b * nk + kvh - kvh0] = first record slot | record count << 16 (build_unit_table).
 template <int HD, int NT, int JG, int RU>
 __device__ void merge_jobs(const StepArgs& a, int G, int s, bool write_attn, uint32_t* xw,
                            const unsigned* units, int nk, int kvh0) {
   using AC = Attn<HD>;
-  const int npairs = a.o.nbs * 16;  // <= 256: bstep batch rows per column pair
-  int pair = threadIdx.x, b0 = 0, bstep = 0;
-  while (pair >= npairs) {
-    pair -= npairs;
-    ++b0;
-  }
-  for (int t = npairs; t <= kConsumers; t += npairs) ++bstep;
-  if (b0 >= bstep) return;
-  const int col = s * 2 * npairs + 2 * pair;
-  const int hq = col / HD, d = col % HD;
-  const int kvh = hq / G;
-  const float* row0 = a.rec + (size_t)(hq - kvh * G) * AC::RS;
-  const unsigned* ut = units + (kvh - kvh0);
-  for (int bg = b0; bg < a.B; bg += JG * bstep) {
+  const int nq = a.o.nbs * 8;  // column quads of the split (<= 128)
+  const int jobs = a.B * nq;
+  int RL = 1;
+  while (JG == 1 && RL < 32 && jobs * RL * 2 <= kConsumers) RL *= 2;
+  const int sub = threadIdx.x & (RL - 1);
+  const int jstep = kConsumers / RL;
+  // JG == 1: one pass for every thread (jobs <= jstep), so that all lanes of a warp reach
+  // the butterfly's shuffles
+  const int npass = JG == 1 ? 1 : (jobs + JG * jstep - 1) / (JG * jstep);
+  for (int pass = 0; pass < npass; ++pass) {
+    const int j0 = threadIdx.x / RL + pass * JG * jstep;
     const float* row[JG];
-    int cnt[JG], maxc = 0;
+    int cnt[JG], dd[JG], maxc = 0;
 #pragma unroll
     for (int g = 0; g < JG; ++g) {
-      const int b = bg + g * bstep;
-      const unsigned u = b < a.B ? ut[b * nk] : 0u;
-      cnt[g] = (int)(u >> 16);
+      const int j = j0 + g * jstep;
+      const int jj = j < jobs ? j : 0;  // a job past the end reads job 0's table (unused)
+      const int b = jj / nq, col = s * 4 * nq + 4 * (jj - b * nq);
+      const int hq = col / HD, kvh = hq / G;
+      dd[g] = col % HD;
+      const unsigned u = units[b * nk + kvh - kvh0];
+      const int n = j < jobs ? (int)(u >> 16) : 0;
+      cnt[g] = n > sub ? (n - sub + RL - 1) / RL : 0;  // this lane's records
       maxc = cnt[g] > maxc ? cnt[g] : maxc;
-      row[g] = row0 + (size_t)(u & 0xffffu) * 8 * AC::RS;
+      row[g] = a.rec + ((size_t)(u & 0xffffu) * 8 + (hq - kvh * G)) * AC::RS +
+               (size_t)sub * 8 * AC::RS;
     }
     float M[JG], den[JG];
-    float2 acc[JG];
+    float4 acc[JG];
 #pragma unroll
     for (int g = 0; g < JG; ++g) {
       M[g] = -INFINITY;
       den[g] = 0.f;
-      acc[g] = make_float2(0.f, 0.f);
+      acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll 1
     for (int r0 = 0; r0 < maxc; r0 += RU) {
-      float2 ml[JG][RU], v[JG][RU];
+      float2 ml[JG][RU];
+      float4 v[JG][RU];
 #pragma unroll
       for (int g = 0; g < JG; ++g) {
         const int last = cnt[g] > 0 ? cnt[g] - 1 : 0;
 #pragma unroll
         for (int i = 0; i < RU; ++i) {
-          // clamped to a record of the job (in range); slots past its count weigh 0
-          const float* q = row[g] + min(r0 + i, last) * (8 * AC::RS);
+          // clamped to a record of the lane (in range); slots past its count weigh 0
+          const float* q = row[g] + min(r0 + i, last) * (RL * 8 * AC::RS);
           ml[g][i] = __ldcg(reinterpret_cast<const float2*>(q + HD));
-          v[g][i] = __ldcg(reinterpret_cast<const float2*>(q + d));
+          v[g][i] = __ldcg(reinterpret_cast<const float4*>(q + dd[g]));
         }
       }
 #pragma unroll
@@ -633,7 +668,7 @@ __device__ void merge_jobs(const StepArgs& a, int G, int s, bool write_attn, uin
         for (int i = 0; i < RU; ++i) {
           if (r0 + i >= cnt[g]) {  // weight 0, and nothing of a record outside the run
             ml[g][i] = make_float2(-INFINITY, 0.f);
-            v[g][i] = make_float2(0.f, 0.f);
+            v[g][i] = make_float4(0.f, 0.f, 0.f, 0.f);
           }
           Mc = fmaxf(Mc, ml[g][i].x);
         }
@@ -642,29 +677,53 @@ __device__ void merge_jobs(const StepArgs& a, int G, int s, bool write_attn, uin
         den[g] *= f;
         acc[g].x *= f;
         acc[g].y *= f;
+        acc[g].z *= f;
+        acc[g].w *= f;
 #pragma unroll
         for (int i = 0; i < RU; ++i) {
           const float w = ex2_approx(ml[g][i].x - Mu);
           den[g] = fmaf(w, ml[g][i].y, den[g]);
           acc[g].x = fmaf(w, v[g][i].x, acc[g].x);
           acc[g].y = fmaf(w, v[g][i].y, acc[g].y);
+          acc[g].z = fmaf(w, v[g][i].z, acc[g].z);
+          acc[g].w = fmaf(w, v[g][i].w, acc[g].w);
         }
         M[g] = Mc;
       }
     }
+    // the lanes of a job: butterfly over their partial states (a fixed order)
+    for (int o = 1; o < RL; o <<= 1) {
+      const float Mo = __shfl_xor_sync(0xffffffffu, M[0], o);
+      const float Mn = fmaxf(M[0], Mo);
+      const float Mu = Mn == -INFINITY ? 0.f : Mn;
+      const float fa = ex2_approx(M[0] - Mu), fb = ex2_approx(Mo - Mu);
+      den[0] = den[0] * fa + __shfl_xor_sync(0xffffffffu, den[0], o) * fb;
+      acc[0].x = acc[0].x * fa + __shfl_xor_sync(0xffffffffu, acc[0].x, o) * fb;
+      acc[0].y = acc[0].y * fa + __shfl_xor_sync(0xffffffffu, acc[0].y, o) * fb;
+      acc[0].z = acc[0].z * fa + __shfl_xor_sync(0xffffffffu, acc[0].z, o) * fb;
+      acc[0].w = acc[0].w * fa + __shfl_xor_sync(0xffffffffu, acc[0].w, o) * fb;
+      M[0] = Mn;
+    }
 #pragma unroll
     for (int g = 0; g < JG; ++g) {
-      const int b = bg + g * bstep;
-      if (b < a.B) {
+      const int j = j0 + g * jstep;
+      if (j < jobs && sub == 0) {
+        const int b = j / nq, cq = 4 * (j - b * nq);
         const float inv = den[g] > 0.f ? rcp_approx(den[g]) : 0.f;
-        const float2 o = make_float2(acc[g].x * inv, acc[g].y * inv);
-        if (write_attn) *reinterpret_cast<float2*>(a.o_attn + (size_t)b * a.nh * HD + col) = o;
-        __half hx, lx, hy, ly;
-        split_f16(o.x, hx, lx);
-        split_f16(o.y, hy, ly);
-        const int w = operand_word<NT>(2 * pair, b);
-        xw[w] = pack_h2(hx, hy);
-        xw[w + 16] = pack_h2(lx, ly);
+        const float4 o = make_float4(acc[g].x * inv, acc[g].y * inv, acc[g].z * inv, acc[g].w * inv);
+        if (write_attn)
+          *reinterpret_cast<float4*>(a.o_attn + (size_t)b * a.nh * HD + s * 4 * nq + cq) = o;
+        __half h0, l0, h1, l1;
+        split_f16(o.x, h0, l0);
+        split_f16(o.y, h1, l1);
+        int w = operand_word<NT>(cq, b);
+        xw[w] = pack_h2(h0, h1);
+        xw[w + 16] = pack_h2(l0, l1);
+        split_f16(o.z, h0, l0);
+        split_f16(o.w, h1, l1);
+        w = operand_word<NT>(cq + 2, b);
+        xw[w] = pack_h2(h0, h1);
+        xw[w + 16] = pack_h2(l0, l1);
       }
     }
   }
@@ -673,25 +732,18 @@ __device__ void merge_jobs(const StepArgs& a, int G, int s, bool write_attn, uin
 constexpr int kOperandBytes = 16 * 4 * 512;  // o_proj operand: nbs <= 16 blocks, NT <= 4
 static_assert(kOperandBytes + kMaxBatch * 9 * 4 <= kUnionBytes, "unit table after the operand");
 
-// Builds the o_proj operand of k-split s in xw (the union): zero columns for the batch
-// slots past B, a table of the record runs of the units the split reads, then the merge.
-// The host keeps the grid-wide key-tile count below 2^24 and the grid at most 256 CTAs,
-// so the CTA that owns tile t, ((t + 1) P - 1) / Nt, is exact in 32-bit arithmetic.
-template <int HD, int NT>
-__device__ __noinline__ void merge_operand(const StepArgs& a, const int* geo, int Nt, int G,
-                                           int s, bool write_attn, uint32_t* xw) {
-  const int npairs = a.o.nbs * 16;
-  const int tid = threadIdx.x;
-  for (int e = tid; e < (4 * NT - a.B) * npairs; e += kConsumers) {
-    const int b = a.B + e / npairs, cc = 2 * (e % npairs);
-    const int w = operand_word<NT>(cc, b);
-    xw[w] = 0u;
-    xw[w + 16] = 0u;
-  }
-  // KV heads whose query heads own the split's columns [s W, s W + W): at most 9
-  const int W = 2 * npairs;
+// The record runs of the units whose query heads own the o_proj split s's columns
+// [s W, s W + W) (at most 9 KV heads): units[b * nk + kvh - kvh0] = first record slot |
+// record count << 16.  Depends on the geometry only, so it is built while the CTA waits
+// at the second grid barrier.  The host keeps the grid-wide key-tile count below 2^24 and
+// the grid at most 256 CTAs: the CTA that owns tile t, ((t + 1) P - 1) / Nt, is exact in
+// 32-bit arithmetic.
+template <int HD>
+__device__ __forceinline__ void build_unit_table(const StepArgs& a, const int* geo, int Nt, int G,
+                                                 int s, unsigned* units) {
+  const int W = a.o.nbs * 32;
   const int kvh0 = s * W / HD / G, nk = (s * W + W - 1) / HD / G - kvh0 + 1;
-  unsigned* units = reinterpret_cast<unsigned*>(reinterpret_cast<uint8_t*>(xw) + kOperandBytes);
+  const int tid = threadIdx.x;
   if (tid < a.B * nk) {
     const int b = tid / nk, kvh = kvh0 + tid - b * nk;
     const int nt = geo[b * kGeoInts + kGeoNt];
@@ -702,10 +754,20 @@ __device__ __noinline__ void merge_operand(const StepArgs& a, const int* geo, in
     // the record of CTA first + r for unit u sits in slot first + r + u
     units[tid] = (unsigned)(first + b * a.nkv + kvh) | ((unsigned)(last - first + 1) << 16);
   }
-  consumer_sync();
-  // a thread with one batch row: many records; several batch rows: few records each
-  if (a.B * npairs <= kConsumers)
-    merge_jobs<HD, NT, 1, 12>(a, G, s, write_attn, xw, units, nk, kvh0);
+}
+
+// Builds the o_proj operand of k-split s in xw (the union) from the records.  Batch slots
+// past B are left as they are: their MMA columns never reach a stored output.
+template <int HD, int NT>
+__device__ __noinline__ void merge_operand(const StepArgs& a, int G, int s, bool write_attn,
+                                           uint32_t* xw) {
+  const int W = a.o.nbs * 32;
+  const int kvh0 = s * W / HD / G, nk = (s * W + W - 1) / HD / G - kvh0 + 1;
+  const unsigned* units =
+      reinterpret_cast<const unsigned*>(reinterpret_cast<const uint8_t*>(xw) + kOperandBytes);
+  // up to 256 column quads: lanes share a job's records; more: several jobs per thread
+  if (a.B * W / 4 <= kConsumers)
+    merge_jobs<HD, NT, 1, 10>(a, G, s, write_attn, xw, units, nk, kvh0);
   else
     merge_jobs<HD, NT, 4, 3>(a, G, s, write_attn, xw, units, nk, kvh0);
 }
@@ -781,7 +843,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned long long* s_gbase = reinterpret_cast<unsigned long long*>(small + 80);
   unsigned* s_max = reinterpret_cast<unsigned*>(small + 96);
   float* s_xss = reinterpret_cast<float*>(small + 160);  // sum(x^2) per batch row
-  float* s_inv = reinterpret_cast<float*>(small + 224);  // [16] + 8 warp partials after
+  float* s_inv = reinterpret_cast<float*>(small + 224);  // [16]: 2^-scale per batch row
   int* geo = reinterpret_cast<int*>(small + 512);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -881,16 +943,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (lane < a.B) geo[lane * kGeoInts + kGeoPre] = incl - span;
     __syncwarp();
-    asm volatile("bar.arrive 2, %0;" ::"n"(kThreads) : "memory");
-    if (lane == 0) {
+    {
       int Nt = 0;
       for (int b = 0; b < a.B; ++b) Nt += geo[b * kGeoInts + kGeoNt] * a.nkv;
       sc.t0 = Nt > 0 ? part_begin(c, Nt, nctas) : 0;
       sc.t1 = Nt > 0 ? part_begin(c + 1, Nt, nctas) : 0;
       sc.nB = sc.t1 - sc.t0;
+    }
+    if (lane == 0)
+      for (int j = 0; j < kEarlyTiles && j < sc.nB; ++j) prefetch_load<HD>(a, sc, geo, sc.nA + j);
+    // while the consumers run phase A: sum(x^2) of the input rows whose key tiles this CTA
+    // attends over (the input norm's statistic, read in phase B)
+    {
+      int base = 0;
+      for (int b = 0; b < a.B; ++b) {
+        const int span_b = geo[b * kGeoInts + kGeoNt] * a.nkv;
+        if (span_b > 0 && base < sc.t1 && base + span_b > sc.t0) {
+          const float ss = row_sumsq(a.x + (size_t)b * a.H, a.H, lane);
+          if (lane == 0) s_xss[b] = ss;
+        }
+        base += span_b;
+      }
+    }
+    __syncwarp();
+    asm volatile("bar.arrive 2, %0;" ::"n"(kThreads) : "memory");  // geometry, statistics
+    if (lane == 0) {
       uint32_t n_app = 0;  // appends waited for (one per unit whose new slot is here)
       const uint64_t kv_policy = l2_policy_evict_first();  // the cache is read once a step
-      for (int j = 0; j < kEarlyTiles && j < sc.nB; ++j) prefetch_load<HD>(a, sc, geo, sc.nA + j);
       for (int k = (int)q; k < sc.nA && ok; ++k) issue_gemv(a.qkv, sc.sa, k);
       for_each_segment(geo, a.B, a.nkv, sc.t0, sc.t1, [&](int b, int kvh, int lt0, int lt1) {
         const int lo = geo[b * kGeoInts + kGeoLo], tn = geo[b * kGeoInts + kGeoTn];
@@ -964,55 +1043,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = a.qkv.ips < sl.r1 - r ? a.qkv.ips : sl.r1 - r;
         const int st = wait_stage();
         if (st >= 0)
-          gemv_stage<NT>(a.qkv, a.B, a.qkv_part, sl.s, ring + st * kStageBytes, n, r,
-                         reinterpret_cast<const uint4*>(uni), s_inv, warp, lane);
+          gemv_stage<NT>(a.qkv, a.B, a.qkv_part, sl.s, smem_u32(ring + st * kStageBytes), n, r,
+                         smem_u32(uni), s_inv, warp, lane);
         release_stage();
       }
     }
     grid_arrive(a.gbar);
-    // while the other CTAs finish phase A: sum(x^2) of the input rows this CTA's key
-    // tiles belong to, in a fixed order (the input norm's statistic)
-    asm volatile("bar.sync 2, %0;" ::"n"(kThreads) : "memory");  // geometry is in
+    asm volatile("bar.sync 2, %0;" ::"n"(kThreads) : "memory");  // geometry, statistics
     int Nt = 0;
     for (int b = 0; b < a.B; ++b) Nt += geo[b * kGeoInts + kGeoNt] * a.nkv;
     const int t0 = Nt > 0 ? part_begin(c, Nt, nctas) : 0;
     const int t1 = Nt > 0 ? part_begin(c + 1, Nt, nctas) : 0;
-    {
-      int b0 = a.B, b1 = -1, base = 0;  // batch rows of tiles [t0, t1]
-      for (int b = 0; b < a.B; ++b) {
-        const int span = geo[b * kGeoInts + kGeoNt] * a.nkv;
-        if (span > 0 && base + span > t0 && base <= t1) {
-          b0 = b < b0 ? b : b0;
-          b1 = b;
-        }
-        base += span;
-      }
-      float* s_wred = s_inv + kMaxBatch;  // 8 warp partials (free after phase A)
-      for (int b = b0; b <= b1; ++b) {
-        const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)b * a.H);
-        float acc = 0.f;
-#pragma unroll 2
-        for (int i = tid; i < a.H / 8; i += kConsumers) {
-          const uint4 t = xr[i];
-          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&t);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = __bfloat1622float2(h[e]);
-            acc = fmaf(f.x, f.x, acc);
-            acc = fmaf(f.y, f.y, acc);
-          }
-        }
-        acc = warp_sum(acc);
-        if (lane == 0) s_wred[warp] = acc;
-        consumer_sync();
-        if (tid == 0) {
-          float t = 0.f;
-          for (int w = 0; w < kCW; ++w) t += s_wred[w];
-          s_xss[b] = t;
-        }
-        consumer_sync();
-      }
-    }
     grid_wait(a.gbar, *s_gbase + nctas, a.err, s_abort);
 
     // ---------------------------------------------------------- B: attention
@@ -1123,20 +1164,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    grid_sync(a.gbar, *s_gbase + 2ull * nctas, a.err, s_abort);
+    const Slice sl = gemv_slice(a.o, c, nctas);
+    grid_arrive(a.gbar);
+    build_unit_table<HD>(a, geo, Nt, G, sl.s,
+                         reinterpret_cast<unsigned*>(uni + kOperandBytes));  // while waiting
+    grid_wait(a.gbar, *s_gbase + 2ull * nctas, a.err, s_abort);
     if (a.next_qkv_w && tid == 0) mbar_arrive(next_bar);
 
     // ---------------------------------------------------------- C: o_proj + residual
     {
-      const Slice sl = gemv_slice(a.o, c, nctas);
-      merge_operand<HD, NT>(a, geo, Nt, G, sl.s, sl.first, reinterpret_cast<uint32_t*>(uni));
+      merge_operand<HD, NT>(a, G, sl.s, sl.first, reinterpret_cast<uint32_t*>(uni));
       consumer_sync();
       for (int r = sl.r0; r < sl.r1; r += a.o.ips) {
         const int n = a.o.ips < sl.r1 - r ? a.o.ips : sl.r1 - r;
         const int st = wait_stage();
         if (st >= 0)
-          gemv_stage<NT>(a.o, a.B, a.y_part, sl.s, ring + st * kStageBytes, n, r,
-                         reinterpret_cast<const uint4*>(uni), nullptr, warp, lane);
+          gemv_stage<NT>(a.o, a.B, a.y_part, sl.s, smem_u32(ring + st * kStageBytes), n, r,
+                         smem_u32(uni), nullptr, warp, lane);
         release_stage();
       }
     }
