@@ -61,11 +61,11 @@ struct hfa_layer {
   float* w_k = nullptr;
   float2* rope_g = nullptr;
   // scratch
-  float* qkv_part = nullptr;
+  unsigned long long* qkv_part = nullptr;  // tagged partial sums (value | step << 32)
   float* q_f32 = nullptr;
   float* attn_rec = nullptr;
   float* o_f32 = nullptr;
-  float* y_part = nullptr;
+  unsigned long long* y_part = nullptr;
   unsigned long long* gbar = nullptr;
   float* k_tap = nullptr;
   float* v_tap = nullptr;
@@ -387,11 +387,12 @@ extern "C" hfa_status hfa_layer_create(const hfa_layer_desc* desc, const void* w
     LA(L->v_tap, (size_t)MR * nkv * hd);
     LA(L->out_tap, (size_t)MR * H);
   }
-  for (void* p : L->allocations) {
-    (void)p;
-  }
-
   LC(cudaMemsetAsync(L->gbar, 0, 8, s), "memset");
+  if (!bf16w) {  // tag 0 never matches a step (tags start at 1)
+    LC(cudaMemsetAsync(L->qkv_part, 0, (size_t)L->g_qkv.S * d.max_batch * L->rows_qkv * 8, s),
+       "memset");
+    LC(cudaMemsetAsync(L->y_part, 0, (size_t)L->g_o.S * d.max_batch * H * 8, s), "memset");
+  }
   LC(cudaMemsetAsync(L->err, 0, 4, s), "memset");
   if (d.max_verify_len > 0) {
     hfa_status vs = hfa::verify_create(L->d, L->num_sms, &L->verify);
@@ -787,8 +788,15 @@ extern "C" hfa_status hfa_check_device_status(hfa_layer* L, void* stream) {
   CK(L, cudaStreamSynchronize(s), "sync");
   if (v == 0) return HFA_OK;
   CK(L, cudaMemsetAsync(L->err, 0, 4, s), "clear status");
-  // a step that gave up may have left the grid barrier mid-count
+  // a step that gave up may have left the grid barrier mid-count; the step numbers start
+  // again, so the tagged partial sums of earlier steps are cleared with it
   CK(L, cudaMemsetAsync(L->gbar, 0, 8, s), "reset grid barrier");
+  if (L->qkv_part)
+    CK(L, cudaMemsetAsync(L->qkv_part, 0,
+                          (size_t)L->g_qkv.S * L->d.max_batch * L->rows_qkv * 8, s), "reset");
+  if (L->y_part)
+    CK(L, cudaMemsetAsync(L->y_part, 0, (size_t)L->g_o.S * L->d.max_batch * L->d.hidden * 8, s),
+       "reset");
   CK(L, cudaStreamSynchronize(s), "sync");
   return fail(L, HFA_EDEVICE, "device status 0x%x:%s%s%s", v,
               (v & kErrWaitTimeout) ? " a bounded wait gave up;" : "",

@@ -84,11 +84,11 @@ struct StepArgs {
   const int* seq_pos;      // [B]
   __nv_bfloat16* k_cache;  // [B, nkv, C, hd]
   __nv_bfloat16* v_cache;
-  float* qkv_part;         // f32 [qkv.S][B][(nh + 2 nkv) hd]: one partial sum per k-split
+  unsigned long long* qkv_part;  // [qkv.S][B][(nh + 2 nkv) hd]: f32 bits | step tag << 32
   float* rec;              // f32 [(grid + B nkv)][8][hd + 4]: (O, m, l) per key range
-  float* y_part;           // f32 [o.S][B][H]: one partial o_proj sum per k-split
+  unsigned long long* y_part;    // [o.S][B][H]: f32 bits | step tag << 32
   float* o_attn;           // f32 [B, nh, hd]: attention output (combined records)
-  unsigned long long* gbar;  // grid barrier arrivals: only grows, three per CTA per step, so
+  unsigned long long* gbar;  // grid barrier arrivals: only grows, one per CTA per step, so
                              // it also numbers the steps (graph replays included)
   unsigned* err;
   float* q_tap;            // nullable f32 [B, nh, hd] (q after RoPE)

@@ -97,6 +97,21 @@ __device__ __forceinline__ float2 ldcg_pinned2(const float* p) {
   asm volatile("ld.global.cg.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
   return v;
 }
+// Tagged partial sums: 8 bytes (f32 bits | step tag << 32) stored and loaded as one
+// morally strong 64-bit access, so that a reader sees a value together with the step it
+// belongs to and needs no fence or barrier to know that it is there.
+__device__ __forceinline__ void st_tagged(unsigned long long* p, float v, uint32_t tag) {
+  const unsigned long long w = ((unsigned long long)tag << 32) | __float_as_uint(v);
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_tagged(const unsigned long long* p) {
+  unsigned long long w;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+  return w;
+}
+__device__ __forceinline__ float tagged_value(unsigned long long w) {
+  return __uint_as_float((uint32_t)w);
+}
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -165,10 +180,12 @@ __device__ __forceinline__ int seg_tile(int i, int lt0, int lt1, int tn) {
   return tn;
 }
 
-// Grid barrier of the consumer warps (the producer runs ahead and never joins).  The
-// arrival counter only grows: barrier k (0, 1, 2) of a step completes when it reaches
-// base + (k + 1) * grid, base = 3 * grid * (steps before this one), which every CTA reads
-// off the counter at its start (the count is then inside [base, base + 3 grid)).
+// Grid barrier of the consumer warps (the producer runs ahead and never joins), once a
+// step, before the attention records are merged.  The arrival counter only grows: the
+// barrier of a step completes when it reaches base + grid, base = grid * (steps before
+// this one), which every CTA reads off the counter at its start (the count is then inside
+// [base, base + grid)); the same number tags the step's partial sums, which the readers
+// poll instead of waiting at barriers of their own.
 // Arrival is one release reduction (no round trip); a CTA that has given up arrives
 // without waiting, so the count stays exact.
 // Split in two so that a CTA can do work of its own between its arrival and the wait.
@@ -189,11 +206,6 @@ __device__ __forceinline__ void grid_wait(const unsigned long long* gbar, unsign
     }
   }
   consumer_sync();
-}
-__device__ __forceinline__ void grid_sync(unsigned long long* gbar, unsigned long long target,
-                                          unsigned* err, volatile int* abort) {
-  grid_arrive(gbar);
-  grid_wait(gbar, target, err, abort);
 }
 
 // ------------------------------------------------------------------ GEMV pieces
@@ -252,7 +264,8 @@ __device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) 
 // hi + lo.
 template <int NT>
 __device__ void build_x_operand(const StepArgs& a, int s, uint32_t* xw, unsigned* s_max,
-                                float* s_inv) {
+                                float* s_inv, unsigned long long arrivals0,
+                                unsigned long long* s_gbase, uint32_t* s_tag) {
   const int tid = threadIdx.x;
   const int nbs = a.qkv.nbs;
   const int groups = nbs * 4;  // 8-column groups per batch row
@@ -295,6 +308,11 @@ __device__ void build_x_operand(const StepArgs& a, int s, uint32_t* xw, unsigned
   }
   // the activations are in registers: the producer may start the weight stream
   asm volatile("bar.arrive 3, %0;" ::"n"(kThreads) : "memory");
+  if (tid == 0) {
+    // this step's number: one grid barrier a step, counted since the layer was created
+    *s_gbase = arrivals0 / gridDim.x * gridDim.x;     // used by thread 0 only
+    *s_tag = (uint32_t)(arrivals0 / gridDim.x) + 1u;  // 0 marks "never written"
+  }
   consumer_sync();
 #pragma unroll
   for (int k = 0; k < NT; ++k) {
@@ -345,12 +363,14 @@ __device__ __forceinline__ float row_sumsq(const __nv_bfloat16* x, int H, int la
   return warp_sum(acc);
 }
 
-// Residual epilogue after the last grid barrier: CTA c finishes its share [i0, i1) of the
-// B x H outputs, out = bf16(x + sum over the o_proj k-splits), the splits added in order
-// 0, 1, ..., S - 1.  A round covers kPer * per outputs (per = 256 / S): thread (k, sp)
-// loads split sp of outputs k, k + per, ... (all in flight together) into shared memory,
-// then one thread per output adds its S partial sums.
-static __device__ void finish_outputs(const StepArgs& a, int c, int nctas, float* red) {
+// Residual epilogue: CTA c finishes its share [i0, i1) of the B x H outputs,
+// out = bf16(x + sum over the o_proj k-splits), the splits added in order 0, 1, ..., S - 1.
+// A round covers kPer * per outputs (per = 256 / S): thread (k, sp) loads split sp of
+// outputs k, k + per, ... (all in flight together; again, after a short pause, until every
+// tag is this step's) into shared memory, then one thread per output adds its S partial
+// sums.  No grid barrier: each partial sum carries its step tag.
+static __device__ void finish_outputs(const StepArgs& a, int c, int nctas, float* red,
+                                      uint32_t tag, volatile int* abort) {
   constexpr int kPer = 8;
   const int S = a.o.S;  // <= grid <= 256
   const int n = a.B * a.H;
@@ -358,18 +378,30 @@ static __device__ void finish_outputs(const StepArgs& a, int c, int nctas, float
   const size_t split_stride = (size_t)a.B * a.H;
   const int tid = threadIdx.x;
   const int per = kConsumers / S, k = tid / S, sp = tid - k * S;
-  const float* ys = a.y_part + sp * split_stride;
+  const unsigned long long* ys = a.y_part + sp * split_stride;
 #pragma unroll 1
   for (int base = i0; base < i1; base += kPer * per) {
     if (k < per) {
-      float v[kPer];
+      unsigned long long w[kPer];
+      const uint64_t t0 = globaltimer_ns();
+      for (;;) {
+        bool ready = true;
 #pragma unroll
-      for (int u = 0; u < kPer; ++u) {
-        const int i = base + u * per + k;
-        v[u] = __ldcg(ys + (i < i1 ? i : i1 - 1));
+        for (int u = 0; u < kPer; ++u) {
+          const int i = base + u * per + k;
+          w[u] = ld_tagged(ys + (i < i1 ? i : i1 - 1));
+          ready = ready && (uint32_t)(w[u] >> 32) == tag;
+        }
+        if (ready) break;
+        if (*abort || globaltimer_ns() - t0 > kWaitLimitNs) {
+          atomicOr(a.err, kErrWaitTimeout);
+          *abort = 1;
+          break;
+        }
+        __nanosleep(64);
       }
 #pragma unroll
-      for (int u = 0; u < kPer; ++u) red[(u * per + k) * S + sp] = v[u];
+      for (int u = 0; u < kPer; ++u) red[(u * per + k) * S + sp] = tagged_value(w[u]);
     }
     consumer_sync();
 #pragma unroll 1
@@ -388,18 +420,19 @@ static __device__ void finish_outputs(const StepArgs& a, int c, int nctas, float
 
 // The work items of one ring stage (n_items items of nbs tiles, row groups r_first ..),
 // one whole item per warp at a time.  The partial sums of rows [16 r, 16 r + 16) over an
-// item's tiles are stored (no atomics) into the k-split's slice of `part`, times the
-// batch row's factor `scale` (nullable: 1).  One out-of-line copy serves both GEMVs, so
+// item's tiles are stored (no atomics, tagged with the step) into the k-split's slice of
+// `part`, times the batch row's factor `scale` (nullable: 1).  One out-of-line copy serves both GEMVs, so
 // the o_proj phase runs code the QKV phase already brought into the instruction cache;
 // the stage and the operand fragments come as shared-window addresses (ld.shared).
 template <int NT>
-__device__ __noinline__ void gemv_stage(const StepGemv& gm, int B, float* part, int s,
-                                        uint32_t stage, int n_items, int r_first, uint32_t frag,
-                                        const float* scale, int warp, int lane) {
+__device__ __noinline__ void gemv_stage(const StepGemv& gm, int B, unsigned long long* part,
+                                        int s, uint32_t stage, int n_items, int r_first,
+                                        uint32_t frag, const float* scale, uint32_t tag, int warp,
+                                        int lane) {
   const int nbs = gm.nbs;
   const int g = lane >> 2, t = lane & 3;
   const int R16 = gm.R * 16;
-  float* dst = part + (size_t)s * B * R16;
+  unsigned long long* dst = part + (size_t)s * B * R16;
   for (int item = warp; item < n_items; item += kCW) {
     float acc[NT][4];
 #pragma unroll
@@ -418,8 +451,8 @@ __device__ __noinline__ void gemv_stage(const StepGemv& gm, int B, float* part, 
       const int b = nt * 4 + t;
       if (b < B) {
         const float f = scale ? scale[b] : 1.f;
-        dst[(size_t)b * R16 + r * 16 + g] = (acc[nt][0] + acc[nt][1]) * f;
-        dst[(size_t)b * R16 + r * 16 + g + 8] = (acc[nt][2] + acc[nt][3]) * f;
+        st_tagged(dst + (size_t)b * R16 + r * 16 + g, (acc[nt][0] + acc[nt][1]) * f, tag);
+        st_tagged(dst + (size_t)b * R16 + r * 16 + g + 8, (acc[nt][2] + acc[nt][3]) * f, tag);
       }
     }
   }
@@ -445,27 +478,44 @@ static __device__ __noinline__ float2 rope_rotate(int P, float2 g, float x0, flo
 
 template <int HD>
 __device__ void head_job(const StepArgs& a, const int* geo, int b, int kvh, int job, int G,
-                         float xss, float* q_s, bool tap_q, int lane) {
+                         float xss, float* q_s, bool tap_q, uint32_t tag, volatile int* abort,
+                         int lane) {
   constexpr int J = HD / 32;
   const int rows = (a.nh + 2 * a.nkv) * HD;
   const int kind = job < G ? 0 : (job == G ? 1 : 2);
   const int row0 = kind == 0 ? (kvh * G + job) * HD
                              : (kind == 1 ? (a.nh + kvh) * HD : (a.nh + a.nkv + kvh) * HD);
   // the projection: partial sums of the k-splits added in a fixed order, every load of a
-  // group of kSG splits issued before the first add
+  // group of kSG splits issued before the first add, and issued again (after a short
+  // pause) until every one carries this step's tag: no grid barrier orders them
   constexpr int kSG = 8;
-  const float* src = a.qkv_part + (size_t)b * rows + row0 + lane;
+  const unsigned long long* src = a.qkv_part + (size_t)b * rows + row0 + lane;
   const size_t split_stride = (size_t)a.B * rows;
   float v[J];
 #pragma unroll
   for (int j = 0; j < J; ++j) v[j] = 0.f;
+  const uint64_t t_start = globaltimer_ns();
   for (int s0 = 0; s0 < a.qkv.S; s0 += kSG) {
     float t[kSG][J];
+    for (;;) {
+      bool ready = true;
 #pragma unroll
-    for (int i = 0; i < kSG; ++i) {
-      const int s = s0 + i < a.qkv.S ? s0 + i : a.qkv.S - 1;
+      for (int i = 0; i < kSG; ++i) {
+        const int s = s0 + i < a.qkv.S ? s0 + i : a.qkv.S - 1;
 #pragma unroll
-      for (int j = 0; j < J; ++j) t[i][j] = __ldcg(src + s * split_stride + 32 * j);
+        for (int j = 0; j < J; ++j) {
+          const unsigned long long w = ld_tagged(src + s * split_stride + 32 * j);
+          ready = ready && (uint32_t)(w >> 32) == tag;
+          t[i][j] = tagged_value(w);
+        }
+      }
+      if (ready) break;
+      if (*abort || globaltimer_ns() - t_start > kWaitLimitNs) {
+        atomicOr(a.err, kErrWaitTimeout);
+        *abort = 1;
+        break;
+      }
+      __nanosleep(32);
     }
 #pragma unroll
     for (int i = 0; i < kSG; ++i)
@@ -837,9 +887,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(small);
   uint64_t* empty = full + kStages;
   uint64_t* append_bar = empty + kStages;
-  uint64_t* next_bar = append_bar + 1;  // consumers passed the second grid barrier
+  uint64_t* next_bar = append_bar + 1;  // consumers passed the grid barrier
   volatile int* s_abort = reinterpret_cast<volatile int*>(small + 64);
   int* s_issued = reinterpret_cast<int*>(small + 68);
+  uint32_t* s_tag = reinterpret_cast<uint32_t*>(small + 72);  // this step's partial-sum tag
   unsigned long long* s_gbase = reinterpret_cast<unsigned long long*>(small + 80);
   unsigned* s_max = reinterpret_cast<unsigned*>(small + 96);
   float* s_xss = reinterpret_cast<float*>(small + 160);  // sum(x^2) per batch row
@@ -1034,27 +1085,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- A: QKV
     {
       const Slice sl = gemv_slice(a.qkv, c, nctas);
-      build_x_operand<NT>(a, sl.s, reinterpret_cast<uint32_t*>(uni), s_max, s_inv);
-      if (tid == 0) {
-        const unsigned long long per_step = 3ull * (unsigned)nctas;
-        *s_gbase = arrivals0 / per_step * per_step;  // used by thread 0 only
-      }
+      build_x_operand<NT>(a, sl.s, reinterpret_cast<uint32_t*>(uni), s_max, s_inv, arrivals0,
+                          s_gbase, s_tag);
+      const uint32_t tag = *s_tag;
       for (int r = sl.r0; r < sl.r1; r += a.qkv.ips) {
         const int n = a.qkv.ips < sl.r1 - r ? a.qkv.ips : sl.r1 - r;
         const int st = wait_stage();
         if (st >= 0)
           gemv_stage<NT>(a.qkv, a.B, a.qkv_part, sl.s, smem_u32(ring + st * kStageBytes), n, r,
-                         smem_u32(uni), s_inv, warp, lane);
+                         smem_u32(uni), s_inv, tag, warp, lane);
         release_stage();
       }
     }
-    grid_arrive(a.gbar);
     asm volatile("bar.sync 2, %0;" ::"n"(kThreads) : "memory");  // geometry, statistics
     int Nt = 0;
     for (int b = 0; b < a.B; ++b) Nt += geo[b * kGeoInts + kGeoNt] * a.nkv;
     const int t0 = Nt > 0 ? part_begin(c, Nt, nctas) : 0;
     const int t1 = Nt > 0 ? part_begin(c + 1, Nt, nctas) : 0;
-    grid_wait(a.gbar, *s_gbase + nctas, a.err, s_abort);
 
     // ---------------------------------------------------------- B: attention
     {
@@ -1070,7 +1117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int njobs = G + (owner ? 2 : 0);
         for (int job = warp; job < njobs; job += kCW)
           head_job<HD>(a, geo, b, kvh, job, G, s_xss[b], q_s, lt0 == 0 && a.q_tap != nullptr,
-                       lane);
+                       *s_tag, s_abort, lane);
         consumer_sync();
         if (owner && tid == 0) mbar_arrive(append_bar);
         // query fragments: rows 0..G-1 = hi(q * qscale), rows 8..8+G-1 = lo
@@ -1168,7 +1215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     grid_arrive(a.gbar);
     build_unit_table<HD>(a, geo, Nt, G, sl.s,
                          reinterpret_cast<unsigned*>(uni + kOperandBytes));  // while waiting
-    grid_wait(a.gbar, *s_gbase + 2ull * nctas, a.err, s_abort);
+    grid_wait(a.gbar, *s_gbase + (unsigned long long)nctas, a.err, s_abort);
     if (a.next_qkv_w && tid == 0) mbar_arrive(next_bar);
 
     // ---------------------------------------------------------- C: o_proj + residual
@@ -1180,12 +1227,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = wait_stage();
         if (st >= 0)
           gemv_stage<NT>(a.o, a.B, a.y_part, sl.s, smem_u32(ring + st * kStageBytes), n, r,
-                         smem_u32(uni), nullptr, warp, lane);
+                         smem_u32(uni), nullptr, *s_tag, warp, lane);
         release_stage();
       }
     }
-    grid_sync(a.gbar, *s_gbase + 3ull * nctas, a.err, s_abort);
-    finish_outputs(a, c, nctas, reinterpret_cast<float*>(uni));
+    consumer_sync();  // the union (operand) is free for the epilogue
+    finish_outputs(a, c, nctas, reinterpret_cast<float*>(uni), *s_tag, s_abort);
   }
 
   // drain: after a give-up, copies may still be landing in the ring
