@@ -43,6 +43,8 @@ constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kUnionBytes + kS
 constexpr int kKeysPerWarp = 16;
 constexpr int kMaxBatch = 16;
 constexpr int kEarlyTiles = 2;            // K/V tiles prefetched into L2 during phase A
+constexpr uint32_t kSuccChunk = 16384;    // next layer's weights: L2 prefetch chunk ...
+constexpr unsigned kSuccPauseNs = 400;    // ... and the pause after each
 
 // per batch row: position, visible slots [lo, hi], key tiles, tile of the new slot, slot
 enum { kGeoP = 0, kGeoLo, kGeoHi, kGeoNt, kGeoTn, kGeoSlot, kGeoPre, kGeoInts = 8 };
@@ -888,6 +890,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + kStages;
   uint64_t* append_bar = empty + kStages;
   uint64_t* next_bar = append_bar + 1;  // consumers passed the grid barrier
+  uint64_t* arrived_bar = reinterpret_cast<uint64_t*>(small + 88);  // ... arrived at it
   volatile int* s_abort = reinterpret_cast<volatile int*>(small + 64);
   int* s_issued = reinterpret_cast<int*>(small + 68);
   uint32_t* s_tag = reinterpret_cast<uint32_t*>(small + 72);  // this step's partial-sum tag
@@ -909,6 +912,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(append_bar, 1);
     mbar_init(next_bar, 1);
+    mbar_init(arrived_bar, 1);
     *s_abort = 0;
     *s_issued = 0;
     fence_barrier_init();
@@ -1053,16 +1057,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++q;
         }
       });
+      // the o_proj slice goes out once the consumers have arrived at the grid barrier: the
+      // arrival's release waits for this SM's copies in flight, so they come after it
+      if (sc.nC > 0 && ok && !mbar_wait(arrived_bar, 0, a.err, s_abort)) ok = false;
       for (int k = 0; k < sc.nC && ok; ++k) issue_gemv(a.o, sc.so, k);
       *s_issued = (int)q;
       // the layer that runs next: its first loads (this CTA's QKV slice, same shape) go to
-      // L2 once the attention is over, while the o_proj phase leaves HBM idle
+      // L2 once the attention is over, while the o_proj phase leaves HBM idle; paced, so
+      // that the latency-bound tail of this step does not queue behind them
       if (a.next_qkv_w && ok && mbar_wait(next_bar, 0, a.err, s_abort)) {
         const uint8_t* src =
             a.next_qkv_w + ((size_t)sc.sa.s * a.qkv.R + sc.sa.r0) * a.qkv.nbs * kQ8TileBytes;
         const size_t bytes = (size_t)(sc.sa.r1 - sc.sa.r0) * a.qkv.nbs * kQ8TileBytes;
-        for (size_t off = 0; off < bytes; off += 32768)
-          prefetch_bulk_l2(src + off, (uint32_t)(bytes - off < 32768 ? bytes - off : 32768));
+        for (size_t off = 0; off < bytes; off += kSuccChunk) {
+          prefetch_bulk_l2(src + off, (uint32_t)(bytes - off < kSuccChunk ? bytes - off : kSuccChunk));
+          __nanosleep(kSuccPauseNs);
+        }
       }
     }
   } else {
@@ -1213,6 +1223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const Slice sl = gemv_slice(a.o, c, nctas);
     grid_arrive(a.gbar);
+    if (tid == 0) mbar_arrive(arrived_bar);
     build_unit_table<HD>(a, geo, Nt, G, sl.s,
                          reinterpret_cast<unsigned*>(uni + kOperandBytes));  // while waiting
     grid_wait(a.gbar, *s_gbase + (unsigned long long)nctas, a.err, s_abort);
