@@ -224,7 +224,8 @@ hfa_status hfa_debug_taps(hfa_layer* layer, void* stream, float* q_dev, float* k
  * Device-side status of earlier steps: bounded waits that gave up, or positions the
  * kernels refused.  Synchronises `stream`; returns HFA_OK, or HFA_EDEVICE with the
  * reason in hfa_last_error, and clears the record (and, after a give-up, resets the
- * step kernel's grid barrier so that later steps start clean).
+ * step kernel's grid-barrier counter and clears its step-tagged partial sums, so that
+ * later steps start clean).
  */
 hfa_status hfa_check_device_status(hfa_layer* layer, void* stream);
 
