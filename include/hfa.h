@@ -203,6 +203,16 @@ hfa_status hfa_attention_decode_noalloc(const hfa_attn_desc* desc, void* stream,
  */
 hfa_status hfa_set_successor(hfa_layer* layer, const hfa_layer* next);
 
+/*
+ * Test hook for the failure path: in the next decode step of `layer`, the consumer warps
+ * of CTA 0 wait on an mbarrier that nothing completes.  The wait gives up after its bound
+ * (about 1 s of the GPU clock), the step's other waits give up in turn, and the step ends
+ * with its error word set: hfa_check_device_status then reports HFA_EDEVICE ("a bounded
+ * wait gave up") and resets the step kernel's state.  No fault, trap or unbounded wait is
+ * involved; the outputs of that one step are undefined.  Errors: HFA_EINVAL (NULL layer).
+ */
+hfa_status hfa_debug_stall_next_step(hfa_layer* layer);
+
 /* Release the layer and its device memory (synchronises the device first). */
 hfa_status hfa_destroy(hfa_layer* layer);
 

@@ -54,6 +54,7 @@ struct hfa_layer {
   uint8_t* wo_t = nullptr;
   StepGemv g_qkv{}, g_o{};
   const uint8_t* successor_qkv = nullptr;  // QKV tiles of the layer that runs next
+  int stall_next = 0;  // test hook (hfa_debug_stall_next_step), one step
   __nv_bfloat16* wqkv_bf16 = nullptr;  // verify path: [(nh + 2 nkv) hd, H]
   __nv_bfloat16* wo_bf16 = nullptr;    // [H, nh hd]
   float* w_in = nullptr;
@@ -425,6 +426,12 @@ extern "C" hfa_status hfa_set_successor(hfa_layer* L, const hfa_layer* next) {
   return HFA_OK;
 }
 
+extern "C" hfa_status hfa_debug_stall_next_step(hfa_layer* L) {
+  if (!L) return HFA_EINVAL;
+  L->stall_next = 1;
+  return HFA_OK;
+}
+
 extern "C" hfa_status hfa_destroy(hfa_layer* L) {
   if (!L) return HFA_EINVAL;
   cudaDeviceSynchronize();
@@ -554,6 +561,8 @@ extern "C" hfa_status hfa_decode_step(hfa_layer* L, void* stream, const void* x,
   sa.out_tap = L->out_tap;
   sa.out = (__nv_bfloat16*)out;
   sa.next_qkv_w = L->successor_qkv;
+  sa.stall = L->stall_next;
+  L->stall_next = 0;
   sa.B = batch;
   sa.H = d.hidden;
   sa.nh = d.num_heads;

@@ -97,6 +97,7 @@ struct StepArgs {
   float* out_tap;          // nullable f32 [B, H]
   __nv_bfloat16* out;      // bf16 [B, H]
   const uint8_t* next_qkv_w;  // nullable: QKV tiles (same layout) of the layer that runs next
+  int stall;               // test hook: CTA 0's consumers wait on a barrier nothing completes
   int B, H, nh, nkv, C, sliding, window, ring, v_unit_norm;
   long long cache_rows;    // B * nkv * C: rows of the [rows, hd] view of each cache
   float eps;

@@ -891,6 +891,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* append_bar = empty + kStages;
   uint64_t* next_bar = append_bar + 1;  // consumers passed the grid barrier
   uint64_t* arrived_bar = reinterpret_cast<uint64_t*>(small + 88);  // ... arrived at it
+  uint64_t* stall_bar = reinterpret_cast<uint64_t*>(small + 288);  // test hook: never completes
   volatile int* s_abort = reinterpret_cast<volatile int*>(small + 64);
   int* s_issued = reinterpret_cast<int*>(small + 68);
   uint32_t* s_tag = reinterpret_cast<uint32_t*>(small + 72);  // this step's partial-sum tag
@@ -913,6 +914,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(append_bar, 1);
     mbar_init(next_bar, 1);
     mbar_init(arrived_bar, 1);
+    mbar_init(stall_bar, 1);
     *s_abort = 0;
     *s_issued = 0;
     fence_barrier_init();
@@ -1098,6 +1100,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       build_x_operand<NT>(a, sl.s, reinterpret_cast<uint32_t*>(uni), s_max, s_inv, arrivals0,
                           s_gbase, s_tag);
       const uint32_t tag = *s_tag;
+      // test hook of the failure path: a bounded wait that runs out
+      if (a.stall && c == 0 && !mbar_wait(stall_bar, 0, a.err, s_abort)) *s_abort = 1;
       for (int r = sl.r0; r < sl.r1; r += a.qkv.ips) {
         const int n = a.qkv.ips < sl.r1 - r ? a.qkv.ips : sl.r1 - r;
         const int st = wait_stage();

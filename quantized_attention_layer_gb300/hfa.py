@@ -86,6 +86,8 @@ def lib():
         L.hfa_destroy.argtypes = [P]
         L.hfa_set_successor.restype = C
         L.hfa_set_successor.argtypes = [P, P]
+        L.hfa_debug_stall_next_step.restype = C
+        L.hfa_debug_stall_next_step.argtypes = [P]
         L.hfa_last_error.restype = ctypes.c_char_p
         L.hfa_last_error.argtypes = [P]
         L.hfa_debug_taps.restype = C
@@ -242,6 +244,9 @@ class Layer:
 
     def hfa_check_device_status(self, stream=None) -> None:
         self._check(lib().hfa_check_device_status(self._h, _stream_ptr(stream)))
+
+    def hfa_debug_stall_next_step(self) -> None:
+        self._check(lib().hfa_debug_stall_next_step(self._h))
 
     def hfa_set_successor(self, next_layer: Optional["Layer"]) -> None:
         self._check(lib().hfa_set_successor(self._h, next_layer._h if next_layer else None))

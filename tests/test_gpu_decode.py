@@ -179,3 +179,31 @@ def test_rejected_calls_touch_nothing():
     assert torch.count_nonzero(out).item() == 0
     layer.hfa_check_device_status()
     layer.hfa_destroy()
+
+
+def test_bounded_wait_gives_up_reports_and_recovers():
+    # the failure path without a fault: CTA 0's consumers wait on a barrier nothing
+    # completes; the wait gives up after its bound, the step ends with its error word
+    # set, hfa_check_device_status reports it and resets, and the next step is correct
+    w = SMALL.replace(batch=2)
+    weights = wl.make_weights(w)
+    layer = hfa.Layer(hfa.desc_for(w, debug_taps=True), hfa.weights_to_device(w, weights))
+    x = wl.make_x(w)
+    pos = np.array([100, 999], dtype=np.int32)
+    kv = wl.make_kv_cache(w)
+    before = run_gpu_decode(w, weights, x, pos, kv, debug_taps=True, layer=layer)
+    kc, vc = kv["k_cache"].cuda(), kv["v_cache"].cuda()
+    out = torch.empty((len(pos), w.hidden), dtype=torch.bfloat16, device="cuda")
+    layer.hfa_debug_stall_next_step()
+    layer.hfa_decode_step(x.cuda(), torch.from_numpy(pos).cuda(), pos, kc, vc, out)
+    with pytest.raises(hfa.HfaError) as e:
+        layer.hfa_check_device_status()
+    assert e.value.status == hfa.HFA_EDEVICE
+    assert "bounded wait" in str(e.value)
+    layer.hfa_check_device_status()  # the record was cleared
+    # steps after the reset: the same result as before the stall, bit for bit
+    for _ in range(2):
+        after = run_gpu_decode(w, weights, x, pos, kv, debug_taps=True, layer=layer)
+        for key in ("out_bf16", "attn", "out"):
+            assert torch.equal(after[key], before[key]), key
+    layer.hfa_destroy()
