@@ -380,9 +380,19 @@ static __device__ void finish_outputs(const StepArgs& a, int c, int nctas, float
   const size_t split_stride = (size_t)a.B * a.H;
   const int tid = threadIdx.x;
   const int per = kConsumers / S, k = tid / S, sp = tid - k * S;
+  // outputs of a round: at most 2 per thread, so that the residual inputs of a thread's
+  // outputs (tid, tid + 256) are loaded ahead of the wait
+  const int nu = kPer < 2 * kConsumers / per ? kPer : 2 * kConsumers / per;
+  const int round = nu * per;
   const unsigned long long* ys = a.y_part + sp * split_stride;
 #pragma unroll 1
-  for (int base = i0; base < i1; base += kPer * per) {
+  for (int base = i0; base < i1; base += round) {
+    float xo[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int i = base + tid + j * kConsumers;
+      xo[j] = __bfloat162float(a.x[i < i1 ? i : i1 - 1]);
+    }
     if (k < per) {
       unsigned long long w[kPer];
       const uint64_t t0 = globaltimer_ns();
@@ -390,7 +400,7 @@ static __device__ void finish_outputs(const StepArgs& a, int c, int nctas, float
         bool ready = true;
 #pragma unroll
         for (int u = 0; u < kPer; ++u) {
-          const int i = base + u * per + k;
+          const int i = u < nu ? base + u * per + k : i1;
           w[u] = ld_tagged(ys + (i < i1 ? i : i1 - 1));
           ready = ready && (uint32_t)(w[u] >> 32) == tag;
         }
@@ -403,18 +413,22 @@ static __device__ void finish_outputs(const StepArgs& a, int c, int nctas, float
         __nanosleep(64);
       }
 #pragma unroll
-      for (int u = 0; u < kPer; ++u) red[(u * per + k) * S + sp] = tagged_value(w[u]);
+      for (int u = 0; u < kPer; ++u)
+        if (u < nu) red[(u * per + k) * S + sp] = tagged_value(w[u]);
     }
     consumer_sync();
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int o = tid + j * kConsumers;
+      if (o < round && base + o < i1) {
+        const int i = base + o;
+        float y = 0.f;
 #pragma unroll 1
-    for (int o = tid; o < kPer * per && base + o < i1; o += kConsumers) {
-      const int i = base + o;
-      float y = 0.f;
-#pragma unroll 1
-      for (int t = 0; t < S; ++t) y += red[o * S + t];
-      const float r = __bfloat162float(a.x[i]) + y;
-      a.out[i] = __float2bfloat16_rn(r);
-      if (a.out_tap) a.out_tap[i] = r;
+        for (int t = 0; t < S; ++t) y += red[o * S + t];
+        const float r = xo[j] + y;
+        a.out[i] = __float2bfloat16_rn(r);
+        if (a.out_tap) a.out_tap[i] = r;
+      }
     }
     consumer_sync();
   }
