@@ -58,6 +58,8 @@ class OrcDesc(ctypes.Structure):
         ("attn_scale", ctypes.c_double), ("softcap", ctypes.c_double),
         ("kv_capacity", ctypes.c_int), ("ring", ctypes.c_int),
         ("v_unit_norm", ctypes.c_int), ("weights_bf16", ctypes.c_int),
+        ("k_eq_v", ctypes.c_int), ("rope_freq_factors", ctypes.c_void_p),
+        ("w_post", ctypes.c_void_p),
     ]
 
 
@@ -79,6 +81,7 @@ def lib():
             L.orc_bf16_matvec.argtypes = [P, ctypes.c_int, ctypes.c_int, P, P]
             L.orc_rmsnorm.argtypes = [P, P, ctypes.c_int, ctypes.c_double, P]
             L.orc_rope_neox.argtypes = [P, ctypes.c_int, ctypes.c_double, ctypes.c_double]
+            L.orc_rope_neox_ff.argtypes = [P, ctypes.c_int, ctypes.c_double, ctypes.c_double, P]
             L.orc_kv_slot.restype = ctypes.c_long
             L.orc_kv_slot.argtypes = [ctypes.c_long, ctypes.c_long, ctypes.c_int]
             L.orc_key_visible.restype = ctypes.c_int
@@ -127,15 +130,30 @@ def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
     return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def desc_from(w) -> OrcDesc:
+def desc_from(w, weights: Optional[Dict] = None, keep: Optional[list] = None) -> OrcDesc:
+    """The oracle's layer description; the variant tables of `weights` (frequency factors,
+    post-attention norm weight) are referenced by pointer, their arrays appended to `keep`
+    so that they outlive the call."""
+    ff = wp = None
+    if weights is not None:
+        if weights.get("rope_ff") is not None:
+            ff = as_np(weights["rope_ff"], np.float32)
+        if weights.get("w_post") is not None:
+            wp = as_np(weights["w_post"], np.float32)
+    if keep is not None:
+        keep.extend([ff, wp])
     return OrcDesc(hidden=w.hidden, num_heads=w.num_heads, num_kv_heads=w.num_kv_heads,
                    head_dim=w.head_dim, layer_type=w.layer_type, window=w.window, eps=w.eps,
                    rope_theta=w.rope_theta, attn_scale=w.attn_scale, softcap=w.softcap,
                    kv_capacity=w.kv_capacity, ring=int(w.ring), v_unit_norm=int(w.v_unit_norm),
-                   weights_bf16=int(w.weights_bf16))
+                   weights_bf16=int(w.weights_bf16), k_eq_v=int(getattr(w, "k_eq_v", False)),
+                   rope_freq_factors=None if ff is None else ff.ctypes.data,
+                   w_post=None if wp is None else wp.ctypes.data)
 
 
 def _weight_np(w, t):
+    if t is None:
+        return None
     return as_np(t, np.uint16) if w.weights_bf16 else as_np(t, np.uint8)
 
 
@@ -187,9 +205,13 @@ def rmsnorm(x, w=None, eps=1e-6) -> np.ndarray:
     return y
 
 
-def rope_neox(u, pos, theta) -> np.ndarray:
+def rope_neox(u, pos, theta, freq_factors=None) -> np.ndarray:
     u = np.array(u, dtype=np.float64, copy=True)
-    lib().orc_rope_neox(_ptr(u), u.size, float(pos), float(theta))
+    if freq_factors is None:
+        lib().orc_rope_neox(_ptr(u), u.size, float(pos), float(theta))
+    else:
+        ff = np.ascontiguousarray(np.asarray(freq_factors, dtype=np.float32))
+        lib().orc_rope_neox_ff(_ptr(u), u.size, float(pos), float(theta), _ptr(ff))
     return u
 
 
@@ -223,7 +245,8 @@ def attend(q, k_rows_bf16, v_rows_bf16, rows, scale=1.0, softcap=0.0):
 
 def decode_step(w, weights: Dict, x, seq_pos, k_cache, v_cache) -> Dict[str, np.ndarray]:
     """Run the oracle decode step on copies of the caches; returns every tap."""
-    d = desc_from(w)
+    keep: list = []
+    d = desc_from(w, weights, keep)
     B = int(np.asarray(seq_pos).size)
     H, nh, nkv, hd = w.hidden, w.num_heads, w.num_kv_heads, w.head_dim
     xb = bf16_bits(x).reshape(B, H)
@@ -246,7 +269,8 @@ def decode_step(w, weights: Dict, x, seq_pos, k_cache, v_cache) -> Dict[str, np.
 
 
 def verify_block(w, weights: Dict, x, base_pos, k_cache, v_cache) -> Dict[str, np.ndarray]:
-    d = desc_from(w)
+    keep: list = []
+    d = desc_from(w, weights, keep)
     H, nh, nkv, hd = w.hidden, w.num_heads, w.num_kv_heads, w.head_dim
     xb = bf16_bits(x).reshape(-1, H)
     L = xb.shape[0]

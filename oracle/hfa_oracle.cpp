@@ -131,10 +131,15 @@ void orc_rmsnorm(const double* x, const float* w, int n, double eps, double* y) 
 }
 
 void orc_rope_neox(double* u, int hd, double pos, double theta) {
+  orc_rope_neox_ff(u, hd, pos, theta, nullptr);
+}
+
+void orc_rope_neox_ff(double* u, int hd, double pos, double theta, const float* ff) {
   int half = hd / 2;
   for (int i = 0; i < half; ++i) {
     double inv_freq = std::pow(theta, -2.0 * i / hd);
     double phi = pos * inv_freq;
+    if (ff) phi /= (double)ff[i];  // frequency factor of the pair (global layers)
     double c = std::cos(phi), s = std::sin(phi);
     double a = u[i], b = u[i + half];
     u[i] = a * c - b * s;
@@ -207,18 +212,21 @@ static void project_token(const orc_desc* d, const void* wq, const void* wk, con
   orc_rmsnorm(xd.data(), w_in, H, d->eps, n.data());                 // [P1] pre-attn norm
   matvec(d, wq, nh * hd, H, n.data(), q);                            // [P1] QKV projections
   matvec(d, wk, nkv * hd, H, n.data(), k);
-  matvec(d, wv, nkv * hd, H, n.data(), v);
+  if (d->k_eq_v)                                  // [P2] no v_proj: V comes from the raw K
+    std::memcpy(v, k, (size_t)nkv * hd * sizeof(double));
+  else
+    matvec(d, wv, nkv * hd, H, n.data(), v);
   std::vector<double> t(hd);
   for (int h = 0; h < nh; ++h) {                                     // [P1] q_norm + RoPE
     orc_rmsnorm(q + h * hd, w_q, hd, d->eps, t.data());
     std::memcpy(q + h * hd, t.data(), hd * sizeof(double));
-    orc_rope_neox(q + h * hd, hd, (double)P, d->rope_theta);
+    orc_rope_neox_ff(q + h * hd, hd, (double)P, d->rope_theta, d->rope_freq_factors);
   }
   for (int h = 0; h < nkv; ++h) {                                    // [P1] k_norm + RoPE
     orc_rmsnorm(k + h * hd, w_k, hd, d->eps, t.data());
     std::memcpy(k + h * hd, t.data(), hd * sizeof(double));
-    orc_rope_neox(k + h * hd, hd, (double)P, d->rope_theta);
-    if (d->v_unit_norm) {                                            // [P1] GPU V norm
+    orc_rope_neox_ff(k + h * hd, hd, (double)P, d->rope_theta, d->rope_freq_factors);
+    if (d->v_unit_norm || d->k_eq_v) {                               // [P1] GPU V norm
       orc_rmsnorm(v + h * hd, nullptr, hd, d->eps, t.data());
       std::memcpy(v + h * hd, t.data(), hd * sizeof(double));
     }
@@ -267,6 +275,11 @@ static void output_token(const orc_desc* d, const void* wo, const uint16_t* x_ro
   int H = d->hidden;
   std::vector<double> y(H);
   matvec(d, wo, H, d->num_heads * d->head_dim, o, y.data());  // [P1] O-proj
+  if (d->w_post) {                              // [P1] fused post-attention norm + add
+    std::vector<double> t(H);
+    orc_rmsnorm(y.data(), d->w_post, H, d->eps, t.data());
+    y = t;
+  }
   for (int i = 0; i < H; ++i) {                                 // [P3] residual add
     double r = orc_bf16_to_f64(x_row[i]) + y[i];
     if (out) out[i] = r;

@@ -38,6 +38,12 @@ typedef struct {
   int ring;            /* 1: slot = pos % capacity; 0: slot = pos */
   int v_unit_norm;     /* 1: V is RMS-normalised per head with unit weight */
   int weights_bf16;    /* 0: Q/K/V/O are Q8_0 blocks; 1: dense bf16 [out, in] */
+  /* Gemma decode variants [P1 fused head norm + RoPE with freq factors on global layers,
+   * GPU V norm, fused post-attention norm + residual add; P2 v_proj None when k_eq_v,
+   * rope_freqs.weight, post_attention_norm.weight]: */
+  int k_eq_v;                      /* 1: no V projection; V = unit RMSNorm of the raw K */
+  const float* rope_freq_factors;  /* NULL, or [hd/2]: phi_i = pos * theta^(-2i/hd) / f_i */
+  const float* w_post;             /* NULL, or [hidden]: out = x + RMSNorm(y) * w_post */
 } orc_desc;
 
 /* ---- scalar formats ---- */
@@ -63,6 +69,8 @@ void orc_rmsnorm(const double* x, const float* w, int n, double eps, double* y);
 /* ---- RoPE, NeoX pairing (i, i + hd/2) [P1 fused head norm + RoPE (half_rope = hd/2);
  *      P3 dispatch_dflash_rope]: phi_i = pos * theta^(-2i/hd) ---- */
 void orc_rope_neox(double* u, int hd, double pos, double theta);
+/* the same with per-pair frequency factors (NULL: none): phi_i = pos * theta^(-2i/hd) / f_i */
+void orc_rope_neox_ff(double* u, int hd, double pos, double theta, const float* ff);
 
 /* ---- KV slots and visibility [P1 dense decode SDPA: write_slot and kv_seq_len] ---- */
 long orc_kv_slot(long pos, long capacity, int ring);

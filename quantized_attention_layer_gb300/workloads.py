@@ -34,6 +34,7 @@ FULL = 1
 F_V_UNIT_NORM = 1 << 0
 F_WEIGHTS_BF16 = 1 << 1
 F_RING = 1 << 2
+F_K_EQ_V = 1 << 4
 
 
 @dataclasses.dataclass(frozen=True)
@@ -61,6 +62,11 @@ class Workload:
     seq_pos: Optional[int] = None        # decode: one position for every sequence
     seq_pos_range: Optional[tuple] = None  # decode: per-sequence U[lo, hi]
     v_unit_norm: bool = False
+    # Gemma decode variants: no V projection (V = unit-normed raw K), per-pair RoPE
+    # frequency factors, RMSNorm of the o_proj output before the residual add
+    k_eq_v: bool = False
+    rope_freq_factors: bool = False
+    post_norm: bool = False
 
     @property
     def group(self) -> int:
@@ -83,6 +89,8 @@ class Workload:
             f |= F_WEIGHTS_BF16
         if self.ring:
             f |= F_RING
+        if self.k_eq_v:
+            f |= F_K_EQ_V
         return f
 
     def replace(self, **kw) -> "Workload":
@@ -157,13 +165,19 @@ def make_weights(w: Workload) -> Dict[str, object]:
     shapes = {"wq": (qr, H), "wk": (kr, H), "wv": (kr, H), "wo": (H, qr)}
     for i, (name, (r, c)) in enumerate(shapes.items()):
         g = _gen(w.seed, 10 + i)
-        if w.weights_bf16:
+        if name == "wv" and w.k_eq_v:
+            out[name] = None  # the layer has no V projection
+        elif w.weights_bf16:
             out[name] = bf16_normal((r, c), g, std=0.02)
         else:
             out[name] = q8_0_blocks(r, c, g)
     out["w_in"] = norm_weight(H, _gen(w.seed, 20))
     out["w_q"] = norm_weight(w.head_dim, _gen(w.seed, 21))
     out["w_k"] = norm_weight(w.head_dim, _gen(w.seed, 22))
+    # per-pair RoPE frequency factors, U[1, 4] (the pages load them from the model file)
+    out["rope_ff"] = (torch.rand((w.head_dim // 2,), generator=_gen(w.seed, 23),
+                                 dtype=torch.float32) * 3.0 + 1.0) if w.rope_freq_factors else None
+    out["w_post"] = norm_weight(H, _gen(w.seed, 24)) if w.post_norm else None
     return out
 
 
