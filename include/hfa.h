@@ -56,6 +56,8 @@ typedef enum { HFA_SLIDING = 0, HFA_FULL = 1 } hfa_layer_type;
 #define HFA_F_WEIGHTS_BF16 0x2u /* Q/K/V/O are dense bf16 [out, in] instead of Q8_0 */
 #define HFA_F_RING 0x4u         /* sliding ring buffer: slot = pos % kv_capacity */
 #define HFA_F_DEBUG_TAPS 0x8u   /* keep fp32 copies of q, k, v, attention and output */
+#define HFA_F_K_EQ_V 0x10u      /* no V projection: V = per-head unit RMSNorm of the raw K
+                                   (Gemma global layers; model.rs, v_proj None when k_eq_v) */
 
 typedef struct {
   int hidden;       /* H, multiple of 64 */
@@ -79,7 +81,8 @@ typedef struct {
  * for coalesced loads; the values are untouched) into library-owned memory, so the
  * caller may free them when the call returns.  The call synchronises `stream`.
  *
- *   wq_dev [nh*hd, H], wk_dev [nkv*hd, H], wv_dev [nkv*hd, H], wo_dev [H, nh*hd]:
+ *   wq_dev [nh*hd, H], wk_dev [nkv*hd, H], wv_dev [nkv*hd, H], wo_dev [H, nh*hd]
+ *     (wv_dev is ignored, and may be NULL, with HFA_F_K_EQ_V):
  *     Q8_0: rows of H/32 (resp. nh*hd/32) blocks of 34 bytes -- fp16 scale d (little
  *     endian) then 32 int8 q, value = d * q (Q8_0 lm_head re-quantiser, model.rs).
  *     With HFA_F_WEIGHTS_BF16: dense bf16, row-major [out, in].
@@ -99,7 +102,7 @@ hfa_status hfa_layer_create(const hfa_layer_desc* desc, const void* wq_dev, cons
  *   n = RMSNorm(x) ; [q;k;v] = W n ; q,k = per-head RMSNorm + RoPE at seq_pos ;
  *   append bf16(k), bf16(v) at slot seq_pos (linear) or seq_pos % C (ring) ;
  *   o = softmax(scale * q K^T [softcap] [window mask]) V over the visible keys ;
- *   out = x + Wo o.
+ *   out = x + Wo o   (x + RMSNorm(Wo o) * w_post with hfa_set_post_norm).
  *
  *   x_dev        bf16 [batch, H]
  *   seq_pos_dev  int32 [batch], device copy read by the kernels
@@ -212,6 +215,26 @@ hfa_status hfa_set_successor(hfa_layer* layer, const hfa_layer* next);
  * involved; the outputs of that one step are undefined.  Errors: HFA_EINVAL (NULL layer).
  */
 hfa_status hfa_debug_stall_next_step(hfa_layer* layer);
+
+/*
+ * RoPE frequency factors of a global layer (gpu_full_attn.rs passes them to the fused
+ * head norm + RoPE of full layers; model.rs loads rope_freqs.weight): each pair's angle
+ * becomes phi_i = P * theta^(-2i/hd) / f_i, for decode steps and verify blocks alike.
+ *   factors_host  f32 [hd/2] in host memory, each finite and > 0; NULL restores
+ *                 phi_i = P * theta^(-2i/hd).
+ * Enqueued on `stream` (the table is updated in stream order).  Errors: HFA_EINVAL.
+ */
+hfa_status hfa_set_rope_freq_factors(hfa_layer* layer, const float* factors_host, void* stream);
+
+/*
+ * Post-attention RMSNorm (gpu_full_attn.rs, fused post-attention norm + residual add):
+ * the output becomes out = x + y * w_post / sqrt(mean(y^2) + eps), y = Wo o, for decode
+ * steps and verify blocks.
+ *   w_post_dev  f32 [H] in device memory, copied (the caller may free it); NULL turns the
+ *               norm off again.
+ * Enqueued on `stream`.  Errors: HFA_EINVAL, HFA_ENOMEM, HFA_ECUDA.
+ */
+hfa_status hfa_set_post_norm(hfa_layer* layer, const float* w_post_dev, void* stream);
 
 /* Release the layer and its device memory (synchronises the device first). */
 hfa_status hfa_destroy(hfa_layer* layer);

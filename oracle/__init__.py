@@ -135,10 +135,10 @@ def desc_from(w, weights: Optional[Dict] = None, keep: Optional[list] = None) ->
     post-attention norm weight) are referenced by pointer, their arrays appended to `keep`
     so that they outlive the call."""
     ff = wp = None
-    if weights is not None:
-        if weights.get("rope_ff") is not None:
+    if weights is not None:  # only the variants the workload turns on
+        if getattr(w, "rope_freq_factors", False) and weights.get("rope_ff") is not None:
             ff = as_np(weights["rope_ff"], np.float32)
-        if weights.get("w_post") is not None:
+        if getattr(w, "post_norm", False) and weights.get("w_post") is not None:
             wp = as_np(weights["w_post"], np.float32)
     if keep is not None:
         keep.extend([ff, wp])

@@ -61,6 +61,10 @@ struct hfa_layer {
   float* w_q = nullptr;
   float* w_k = nullptr;
   float2* rope_g = nullptr;
+  std::vector<float2> rope_host;  // source of the last table upload (stream-ordered)
+  float* w_post = nullptr;        // post-attention RMSNorm weight [H] (allocated on first use)
+  bool w_post_on = false;         // the norm is applied
+  unsigned long long* post_part = nullptr;  // [grid][2] tagged partial sum(y^2) per CTA
   // scratch
   unsigned long long* qkv_part = nullptr;  // tagged partial sums (value | step << 32)
   float* q_f32 = nullptr;
@@ -222,7 +226,8 @@ static hfa_status validate_desc(const hfa_layer_desc* d) {
     return fail(nullptr, HFA_EUNSUPPORTED, "max_verify_len=%d outside [0, 16]", d->max_verify_len);
   if (!(d->eps >= 0.f) || !(d->rope_theta > 0.f) || !(d->attn_scale > 0.f) || !(d->softcap >= 0.f))
     return fail(nullptr, HFA_EINVAL, "eps, rope_theta, attn_scale, softcap out of range");
-  if (d->flags & ~(HFA_F_V_UNIT_NORM | HFA_F_WEIGHTS_BF16 | HFA_F_RING | HFA_F_DEBUG_TAPS))
+  if (d->flags &
+      ~(HFA_F_V_UNIT_NORM | HFA_F_WEIGHTS_BF16 | HFA_F_RING | HFA_F_DEBUG_TAPS | HFA_F_K_EQ_V))
     return fail(nullptr, HFA_EINVAL, "unknown flags 0x%x", d->flags);
   return HFA_OK;
 }
@@ -242,6 +247,22 @@ static void plan_step_gemv(StepGemv* g, int rows, int cols) {
   g->S = g->nb / g->nbs;
   g->ips = (int)(step_stage_bytes() / ((size_t)g->nbs * kQ8TileBytes));
   g->w = nullptr;
+}
+
+// RoPE table: theta^(-2i/hd) / (2 pi) / f_i in double (f_i = 1 without frequency factors),
+// stored as an fp32 (hi, lo) pair per pair i; the kernels reduce P * g exactly enough.
+// The host copy lives in the layer, so that the asynchronous upload can read it later.
+static cudaError_t upload_rope_table(hfa_layer* L, const float* ff, cudaStream_t s) {
+  const int hd = L->d.head_dim;
+  L->rope_host.resize(hd / 2);
+  for (int i = 0; i < hd / 2; ++i) {
+    double v = pow((double)L->d.rope_theta, -2.0 * i / hd) / (2.0 * M_PI);
+    if (ff) v /= (double)ff[i];
+    const float hi = (float)v;
+    L->rope_host[i] = make_float2(hi, (float)(v - (double)hi));
+  }
+  return cudaMemcpyAsync(L->rope_g, L->rope_host.data(), (size_t)hd / 2 * sizeof(float2),
+                         cudaMemcpyHostToDevice, s);
 }
 
 // ------------------------------------------------------------------ create / destroy
@@ -265,7 +286,7 @@ extern "C" hfa_status hfa_layer_create(const hfa_layer_desc* desc, const void* w
   *out = nullptr;
   hfa_status st = validate_desc(desc);
   if (st != HFA_OK) return st;
-  if (!wq || !wk || !wv || !wo || !w_in || !w_q || !w_k)
+  if (!wq || !wk || (!wv && !(desc->flags & HFA_F_K_EQ_V)) || !wo || !w_in || !w_q || !w_k)
     return fail(nullptr, HFA_EINVAL, "a weight pointer is NULL");
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -288,7 +309,7 @@ extern "C" hfa_status hfa_layer_create(const hfa_layer_desc* desc, const void* w
   const hfa_layer_desc& d = L->d;
   const int H = d.hidden, nh = d.num_heads, nkv = d.num_kv_heads, hd = d.head_dim;
   L->G = nh / nkv;
-  L->rows_qkv = (nh + 2 * nkv) * hd;
+  L->rows_qkv = qkv_rows(d);  // no V rows with k_eq_v
   L->max_rows = d.max_batch > d.max_verify_len ? d.max_batch : d.max_verify_len;
   const int MR = L->max_rows;
   cudaStream_t s = (cudaStream_t)stream;
@@ -333,9 +354,10 @@ extern "C" hfa_status hfa_layer_create(const hfa_layer_desc* desc, const void* w
     LC(launch_repack_q8_0_split((const uint8_t*)wk, nkv * hd, H, L->wqkv_t, nh * hd / 16, Rq, nbq,
                                 s),
        "repack wk");
-    LC(launch_repack_q8_0_split((const uint8_t*)wv, nkv * hd, H, L->wqkv_t, (nh + nkv) * hd / 16,
-                                Rq, nbq, s),
-       "repack wv");
+    if (!(d.flags & HFA_F_K_EQ_V))
+      LC(launch_repack_q8_0_split((const uint8_t*)wv, nkv * hd, H, L->wqkv_t,
+                                  (nh + nkv) * hd / 16, Rq, nbq, s),
+         "repack wv");
     LC(launch_repack_q8_0_split((const uint8_t*)wo, H, nh * hd, L->wo_t, 0, H / 16, nbo, s),
        "repack wo");
   } else {
@@ -344,8 +366,9 @@ extern "C" hfa_status hfa_layer_create(const hfa_layer_desc* desc, const void* w
     const size_t qb = (size_t)nh * hd * H * 2, kb = (size_t)nkv * hd * H * 2;
     LC(cudaMemcpyAsync(L->wqkv_bf16, wq, qb, cudaMemcpyDeviceToDevice, s), "copy wq");
     LC(cudaMemcpyAsync((char*)L->wqkv_bf16 + qb, wk, kb, cudaMemcpyDeviceToDevice, s), "copy wk");
-    LC(cudaMemcpyAsync((char*)L->wqkv_bf16 + qb + kb, wv, kb, cudaMemcpyDeviceToDevice, s),
-       "copy wv");
+    if (!(d.flags & HFA_F_K_EQ_V))
+      LC(cudaMemcpyAsync((char*)L->wqkv_bf16 + qb + kb, wv, kb, cudaMemcpyDeviceToDevice, s),
+         "copy wv");
     LC(cudaMemcpyAsync(L->wo_bf16, wo, (size_t)H * nh * hd * 2, cudaMemcpyDeviceToDevice, s),
        "copy wo");
   }
@@ -355,19 +378,9 @@ extern "C" hfa_status hfa_layer_create(const hfa_layer_desc* desc, const void* w
   LC(cudaMemcpyAsync(L->w_in, w_in, H * 4, cudaMemcpyDeviceToDevice, s), "copy w_in");
   LC(cudaMemcpyAsync(L->w_q, w_q, hd * 4, cudaMemcpyDeviceToDevice, s), "copy w_q");
   LC(cudaMemcpyAsync(L->w_k, w_k, hd * 4, cudaMemcpyDeviceToDevice, s), "copy w_k");
-  {
-    // theta^(-2i/hd) / (2 pi) in double, stored as an fp32 (hi, lo) pair
-    std::vector<float2> g(hd / 2);
-    for (int i = 0; i < hd / 2; ++i) {
-      double v = pow((double)d.rope_theta, -2.0 * i / hd) / (2.0 * M_PI);
-      float hi = (float)v;
-      g[i] = make_float2(hi, (float)(v - (double)hi));
-    }
-    LA(L->rope_g, hd / 2);
-    LC(cudaMemcpyAsync(L->rope_g, g.data(), g.size() * sizeof(float2), cudaMemcpyHostToDevice, s),
-       "copy rope table");
-    LC(cudaStreamSynchronize(s), "create sync");
-  }
+  LA(L->rope_g, hd / 2);
+  LC(upload_rope_table(L, nullptr, s), "copy rope table");
+  LC(cudaStreamSynchronize(s), "create sync");
   // scratch
   const int units = d.max_batch * nkv;
   if (!bf16w) {
@@ -423,6 +436,44 @@ extern "C" hfa_status hfa_set_successor(hfa_layer* L, const hfa_layer* next) {
       a.head_dim != b.head_dim || next->device != L->device)
     return fail(L, HFA_EINVAL, "the successor must have the same shape, on the same device");
   L->successor_qkv = next->wqkv_t;
+  return HFA_OK;
+}
+
+extern "C" hfa_status hfa_set_rope_freq_factors(hfa_layer* L, const float* ff, void* stream) {
+  if (!L) return HFA_EINVAL;
+  const int hd = L->d.head_dim;
+  if (ff)
+    for (int i = 0; i < hd / 2; ++i)
+      if (!(ff[i] > 0.f) || !isfinite(ff[i]))
+        return fail(L, HFA_EINVAL, "frequency factor %d is %g (need finite and > 0)", i,
+                    (double)ff[i]);
+  cudaStream_t s = (cudaStream_t)stream;
+  CK(L, upload_rope_table(L, ff, s), "copy rope table");
+  return HFA_OK;
+}
+
+extern "C" hfa_status hfa_set_post_norm(hfa_layer* L, const float* w_post, void* stream) {
+  if (!L) return HFA_EINVAL;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (!w_post) {
+    L->w_post_on = false;
+    return HFA_OK;
+  }
+  if (!L->w_post) {
+    cudaError_t e = cudaMalloc(&L->w_post, (size_t)L->d.hidden * sizeof(float));
+    if (e == cudaSuccess) L->allocations.push_back(L->w_post);
+    else L->w_post = nullptr;
+    if (e == cudaSuccess) {
+      e = cudaMalloc(&L->post_part, (size_t)L->num_sms * 2 * sizeof(unsigned long long));
+      if (e == cudaSuccess) L->allocations.push_back(L->post_part);
+      else L->post_part = nullptr;
+    }
+    if (e != cudaSuccess) return fail(L, HFA_ENOMEM, "cudaMalloc: %s", cudaGetErrorString(e));
+    CK(L, cudaMemsetAsync(L->post_part, 0, (size_t)L->num_sms * 2 * 8, s), "memset");
+  }
+  CK(L, cudaMemcpyAsync(L->w_post, w_post, (size_t)L->d.hidden * sizeof(float),
+                        cudaMemcpyDeviceToDevice, s), "copy w_post");
+  L->w_post_on = true;
   return HFA_OK;
 }
 
@@ -562,6 +613,9 @@ extern "C" hfa_status hfa_decode_step(hfa_layer* L, void* stream, const void* x,
   sa.out = (__nv_bfloat16*)out;
   sa.next_qkv_w = L->successor_qkv;
   sa.stall = L->stall_next;
+  sa.w_post = L->w_post_on ? L->w_post : nullptr;
+  sa.post_part = L->post_part;
+  sa.k_eq_v = (d.flags & HFA_F_K_EQ_V) ? 1 : 0;
   L->stall_next = 0;
   sa.B = batch;
   sa.H = d.hidden;
@@ -753,6 +807,7 @@ extern "C" hfa_status hfa_verify_block(hfa_layer* L, void* stream, const void* x
   c.rope_g = L->rope_g;
   c.q_f32 = L->q_f32;
   c.o_f32 = L->o_f32;
+  c.w_post = L->w_post_on ? L->w_post : nullptr;
   c.k_tap = L->k_tap;
   c.v_tap = L->v_tap;
   c.out_tap = L->out_tap;
@@ -806,6 +861,8 @@ extern "C" hfa_status hfa_check_device_status(hfa_layer* L, void* stream) {
   if (L->y_part)
     CK(L, cudaMemsetAsync(L->y_part, 0, (size_t)L->g_o.S * L->d.max_batch * L->d.hidden * 8, s),
        "reset");
+  if (L->post_part)
+    CK(L, cudaMemsetAsync(L->post_part, 0, (size_t)L->num_sms * 2 * 8, s), "reset");
   CK(L, cudaStreamSynchronize(s), "sync");
   return fail(L, HFA_EDEVICE, "device status 0x%x:%s%s%s", v,
               (v & kErrWaitTimeout) ? " a bounded wait gave up;" : "",

@@ -38,6 +38,21 @@ static __device__ void finish_head(const GemvArgs& a, int hh, int lane) {
     }
     const int seq = a.rows_are_tokens ? 0 : b;
     const int P = a.rows_are_tokens ? a.base_pos + b : a.seq_pos[b];
+    if (kind == 1 && a.k_eq_v && P >= 0 && (a.ring || P < a.C)) {
+      // no V projection: V is the raw K, RMS-normalised per head with unit weight
+      float ss = 0.f;
+#pragma unroll
+      for (int j = 0; j < J; ++j) ss += v[j] * v[j];
+      const float inv = rsqrtf(warp_sum(ss) / HD + a.eps);
+      const int kvh = hh - a.nh;
+      const int slot = a.ring ? P % a.C : P;
+      __nv_bfloat16* dst = a.v_cache + (((size_t)seq * a.nkv + kvh) * a.C + slot) * HD;
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        dst[lane + 32 * j] = __float2bfloat16_rn(v[j] * inv);
+        if (a.v_tap) a.v_tap[((size_t)b * a.nkv + kvh) * HD + lane + 32 * j] = v[j] * inv;
+      }
+    }
     if (kind < 2 || a.v_unit_norm) {
       float ss = 0.f;
 #pragma unroll
@@ -84,7 +99,8 @@ static __device__ void finish_head(const GemvArgs& a, int hh, int lane) {
   }
 }
 
-// Epilogue of one row group (o_proj mode): out = bf16(x + y).
+// Epilogue of one row group (o_proj mode): out = bf16(x + y), or y kept in y_post for the
+// post-attention norm pass (which needs the whole row's mean of y^2 first).
 static __device__ void finish_rowgroup(const GemvArgs& a, int r, int lane) {
   const int R16 = a.R * 16;
   for (int i = lane; i < 16 * a.batch; i += 32) {
@@ -92,6 +108,10 @@ static __device__ void finish_rowgroup(const GemvArgs& a, int r, int lane) {
     float* p = a.acc + (size_t)b * R16 + row;
     const float y = ld_cg_f32(p);
     *p = 0.0f;
+    if (a.y_post) {  // the post-attention norm pass writes the output
+      a.y_post[(size_t)b * R16 + row] = y;
+      continue;
+    }
     const float o = __bfloat162float(a.x[(size_t)b * R16 + row]) + y;
     a.out[(size_t)b * R16 + row] = __float2bfloat16_rn(o);
     if (a.out_tap) a.out_tap[(size_t)b * R16 + row] = o;

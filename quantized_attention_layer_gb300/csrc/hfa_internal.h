@@ -10,6 +10,12 @@
 
 namespace hfa {
 
+// Rows of the concatenated QKV projection: q, k and (without k_eq_v) v heads.
+inline int qkv_rows(const hfa_layer_desc& d) {
+  const int kv = (d.flags & HFA_F_K_EQ_V) ? 1 : 2;
+  return (d.num_heads + kv * d.num_kv_heads) * d.head_dim;
+}
+
 // Epilogue arguments of the verify-block GEMMs (per-head norm + RoPE + KV append, and
 // the residual), shared with the finishers of hfa_finish.cuh.
 struct GemvArgs {
@@ -29,6 +35,7 @@ struct GemvArgs {
   const float2* rope_g;    // [hd/2] (hi, lo) of theta^(-2i/hd) / (2 pi)
   const int* seq_pos;      // [B]
   int v_unit_norm;
+  int k_eq_v;              // the key finisher also writes V = unit RMSNorm of the raw K
   float* q_out;            // f32 [B, nh, hd]
   __nv_bfloat16* k_cache;  // [B, nkv, C, hd]
   __nv_bfloat16* v_cache;
@@ -37,6 +44,7 @@ struct GemvArgs {
   // OPROJ finisher
   __nv_bfloat16* out;      // bf16 [B, R*16]
   float* out_tap;          // nullable f32 [B, R*16]
+  float* y_post;           // nullable f32 [B, R*16]: y kept for the post-attention norm pass
   // verify rows: row b of the GEMV is token b of sequence 0 at position base_pos + b
   int rows_are_tokens;
   int base_pos;
@@ -98,7 +106,10 @@ struct StepArgs {
   __nv_bfloat16* out;      // bf16 [B, H]
   const uint8_t* next_qkv_w;  // nullable: QKV tiles (same layout) of the layer that runs next
   int stall;               // test hook: CTA 0's consumers wait on a barrier nothing completes
+  const float* w_post;     // nullable f32 [H]: post-attention RMSNorm of the o_proj output
+  unsigned long long* post_part;  // [grid][2] tagged partial sum(y^2) (with w_post)
   int B, H, nh, nkv, C, sliding, window, ring, v_unit_norm;
+  int k_eq_v;              // no V rows: the K job also writes V = unit RMSNorm of raw K
   long long cache_rows;    // B * nkv * C: rows of the [rows, hd] view of each cache
   float eps;
   float qscale;            // scale * log2(e), or scale / softcap with a softcap

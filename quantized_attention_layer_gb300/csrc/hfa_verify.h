@@ -18,7 +18,7 @@ struct VerifyCall {
   __nv_bfloat16* k_cache;  // [1, nkv, C, hd]
   __nv_bfloat16* v_cache;
   __nv_bfloat16* out;      // [L, H]
-  const __nv_bfloat16* wqkv;  // [(nh + 2 nkv) hd, H]
+  const __nv_bfloat16* wqkv;  // [qkv_rows(d), H]: q, k and (without k_eq_v) v rows
   const __nv_bfloat16* wo;    // [H, nh hd]
   const float* w_in;
   const float* w_q;
@@ -29,6 +29,7 @@ struct VerifyCall {
   float* k_tap;   // nullable [L, nkv, hd]
   float* v_tap;
   float* out_tap; // nullable [L, H]
+  const float* w_post;  // nullable [H]: out = x + RMSNorm(y) * w_post
   unsigned* err;
   int num_sms;
   LaunchTimer* timer;  // nullable; when set, launches are timed and not PDL-chained

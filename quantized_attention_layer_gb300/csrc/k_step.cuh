@@ -434,6 +434,111 @@ static __device__ void finish_outputs(const StepArgs& a, int c, int nctas, float
   }
 }
 
+// Post-attention RMSNorm variant of the residual epilogue: out = x + y * w_post * r_b,
+// r_b = 1 / sqrt(mean over the row b of y^2 + eps).  A CTA's share [i0, i1) of the B x H
+// outputs spans at most two batch rows (share <= H).  The CTA sums its splits into y (kept
+// in `ybuf`, shared memory), publishes sum(y^2) of its part of each row (tagged, slot 0 for
+// its first row, 1 for the second), then adds up, in CTA order, the parts of the CTAs that
+// share each of its rows, and writes its outputs.
+static __device__ __noinline__ void finish_outputs_post(const StepArgs& a, int c, int nctas,
+                                                        float* red, float* ybuf, uint32_t tag,
+                                                        volatile int* abort) {
+  const int S = a.o.S;
+  const int n = a.B * a.H;
+  const int i0 = part_begin(c, n, nctas), i1 = part_begin(c + 1, n, nctas);
+  const size_t split_stride = (size_t)a.B * a.H;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = kConsumers / S, k = tid / S, sp = tid - k * S;
+  const int round = per;  // one output per (k, all splits) per round
+  const unsigned long long* ys = a.y_part + sp * split_stride;
+  float* wred = red + kConsumers * 8;  // [8 warps][2]
+  float* s_inv = wred + 16;            // [2]
+  const int b_lo = i0 < i1 ? i0 / a.H : 0;
+  float ps[2] = {0.f, 0.f};  // this thread's part of sum(y^2) of rows b_lo, b_lo + 1
+#pragma unroll 1
+  for (int base = i0; base < i1; base += round) {
+    if (k < per) {
+      const int i = base + k;
+      const uint64_t t0 = globaltimer_ns();
+      unsigned long long w;
+      for (;;) {
+        w = ld_tagged(ys + (i < i1 ? i : i1 - 1));
+        if ((uint32_t)(w >> 32) == tag) break;
+        if (*abort || globaltimer_ns() - t0 > kWaitLimitNs) {
+          atomicOr(a.err, kErrWaitTimeout);
+          *abort = 1;
+          break;
+        }
+        __nanosleep(64);
+      }
+      red[k * S + sp] = tagged_value(w);
+    }
+    consumer_sync();
+    if (tid < round && base + tid < i1) {
+      const int i = base + tid;
+      float y = 0.f;
+#pragma unroll 1
+      for (int t = 0; t < S; ++t) y += red[tid * S + t];
+      ybuf[i - i0] = y;
+      ps[i / a.H - b_lo] += y * y;
+    }
+    consumer_sync();
+  }
+  // this CTA's parts of sum(y^2): warp trees, then the warps in order
+  {
+    const float t0 = warp_sum(ps[0]), t1 = warp_sum(ps[1]);
+    if (lane == 0) {
+      wred[warp * 2] = t0;
+      wred[warp * 2 + 1] = t1;
+    }
+  }
+  consumer_sync();
+  if (tid < 2 && i0 < i1 && b_lo + tid <= (i1 - 1) / a.H) {
+    float t = 0.f;
+    for (int w = 0; w < kCW; ++w) t += wred[w * 2 + tid];
+    st_tagged(a.post_part + 2 * c + tid, t, tag);
+  }
+  // the parts of every CTA that shares a row with this one, added in CTA order
+  if (i0 < i1) {
+#pragma unroll 1
+    for (int r = 0; r < 2 && b_lo + r <= (i1 - 1) / a.H; ++r) {
+      const int b = b_lo + r;
+      const int cf = part_of(b * a.H, n, nctas), cl = part_of((b + 1) * a.H - 1, n, nctas);
+#pragma unroll 1
+      for (int cc = cf + tid; cc <= cl; cc += kConsumers) {
+        const int slot = b - part_begin(cc, n, nctas) / a.H;
+        const uint64_t t0 = globaltimer_ns();
+        unsigned long long w;
+        for (;;) {
+          w = ld_tagged(a.post_part + 2 * cc + slot);
+          if ((uint32_t)(w >> 32) == tag) break;
+          if (*abort || globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(a.err, kErrWaitTimeout);
+            *abort = 1;
+            break;
+          }
+          __nanosleep(64);
+        }
+        red[cc - cf] = tagged_value(w);
+      }
+      consumer_sync();
+      if (tid == 0) {
+        float t = 0.f;
+        for (int cc = cf; cc <= cl; ++cc) t += red[cc - cf];
+        s_inv[r] = rsqrtf(t / a.H + a.eps);
+      }
+      consumer_sync();
+    }
+  }
+#pragma unroll 1
+  for (int i = i0 + tid; i < i1; i += kConsumers) {
+    const int col = i % a.H;
+    const float r = __bfloat162float(a.x[i]) + ybuf[i - i0] * a.w_post[col] * s_inv[i / a.H - b_lo];
+    a.out[i] = __float2bfloat16_rn(r);
+    if (a.out_tap) a.out_tap[i] = r;
+  }
+}
+
 // The work items of one ring stage (n_items items of nbs tiles, row groups r_first ..),
 // one whole item per warp at a time.  The partial sums of rows [16 r, 16 r + 16) over an
 // item's tiles are stored (no atomics, tagged with the step) into the k-split's slice of
@@ -482,7 +587,8 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return (uint32_t)(box * (Attn<HD>::T * 128) + row * 128 + ((c ^ (row & 7)) << 4));
 }
 
-// One head of unit (b, kvh): job < G query head kvh * G + job, G the key, G + 1 the value.
+// One head of unit (b, kvh): job < G query head kvh * G + job, G the key, G + 1 the value
+// (with k_eq_v there is no value job: the key job writes V = unit RMSNorm of the raw K).
 // Raw projection * 1/rms(x), per-head RMSNorm (q, k; v with the unit-norm flag), RoPE
 // (q, k); queries go to q_s, the key and value row to the cache slot (bf16, RNE).
 // the RoPE rotation of one pair, out of line: one copy of the sin/cos code serves all
@@ -497,7 +603,7 @@ __device__ void head_job(const StepArgs& a, const int* geo, int b, int kvh, int 
                          float xss, float* q_s, bool tap_q, uint32_t tag, volatile int* abort,
                          int lane) {
   constexpr int J = HD / 32;
-  const int rows = (a.nh + 2 * a.nkv) * HD;
+  const int rows = a.qkv.R * 16;  // q, k and (without k_eq_v) v heads
   const int kind = job < G ? 0 : (job == G ? 1 : 2);
   const int row0 = kind == 0 ? (kvh * G + job) * HD
                              : (kind == 1 ? (a.nh + kvh) * HD : (a.nh + a.nkv + kvh) * HD);
@@ -544,6 +650,20 @@ __device__ void head_job(const StepArgs& a, const int* geo, int b, int kvh, int 
   const float xinv = rsqrtf(xss / a.H + a.eps);
 #pragma unroll
   for (int j = 0; j < J; ++j) v[j] *= xinv;
+  const int slot = geo[b * kGeoInts + kGeoSlot];
+  if (kind == 1 && a.k_eq_v) {
+    // no V projection: V is the raw K, RMS-normalised per head with unit weight
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < J; ++j) ss += v[j] * v[j];
+    const float inv = rsqrtf(warp_sum(ss) / HD + a.eps);
+    __nv_bfloat16* dst = a.v_cache + (((size_t)b * a.nkv + kvh) * a.C + slot) * HD;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      dst[lane + 32 * j] = __float2bfloat16_rn(v[j] * inv);
+      if (a.v_tap) a.v_tap[((size_t)b * a.nkv + kvh) * HD + lane + 32 * j] = v[j] * inv;
+    }
+  }
   if (kind < 2 || a.v_unit_norm) {
     float ss = 0.f;
 #pragma unroll
@@ -575,7 +695,6 @@ __device__ void head_job(const StepArgs& a, const int* geo, int b, int kvh, int 
       for (int j = 0; j < J; ++j) qt[lane + 32 * j] = v[j];
     }
   } else {
-    const int slot = geo[b * kGeoInts + kGeoSlot];
     __nv_bfloat16* dst =
         (kind == 1 ? a.k_cache : a.v_cache) + (((size_t)b * a.nkv + kvh) * a.C + slot) * HD;
     float* tap = kind == 1 ? a.k_tap : a.v_tap;
@@ -1142,7 +1261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lo = gb[kGeoLo], hi = gb[kGeoHi], tn = gb[kGeoTn];
         const bool owner = tn >= lt0 && tn < lt1;
         const int unit = b * a.nkv + kvh;
-        const int njobs = G + (owner ? 2 : 0);
+        const int njobs = G + (owner ? (a.k_eq_v ? 1 : 2) : 0);  // q heads, k, v
         for (int job = warp; job < njobs; job += kCW)
           head_job<HD>(a, geo, b, kvh, job, G, s_xss[b], q_s, lt0 == 0 && a.q_tap != nullptr,
                        *s_tag, s_abort, lane);
@@ -1261,7 +1380,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     consumer_sync();  // the union (operand) is free for the epilogue
-    finish_outputs(a, c, nctas, reinterpret_cast<float*>(uni), *s_tag, s_abort);
+    if (a.w_post)
+      finish_outputs_post(a, c, nctas, reinterpret_cast<float*>(uni),
+                          reinterpret_cast<float*>(ring), *s_tag, s_abort);
+    else
+      finish_outputs(a, c, nctas, reinterpret_cast<float*>(uni), *s_tag, s_abort);
   }
 
   // drain: after a give-up, copies may still be landing in the ring

@@ -547,6 +547,31 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
   }
 }
 
+// Post-attention RMSNorm of the verify block, one CTA per token row: sum(y^2) in a fixed
+// order (thread strides, warp trees, warps in order), then out = bf16(x + y w r).
+__global__ void __launch_bounds__(256) post_norm_rows_kernel(const float* __restrict__ y,
+                                                             const __nv_bfloat16* __restrict__ x,
+                                                             const float* __restrict__ w, int H,
+                                                             float eps, __nv_bfloat16* out,
+                                                             float* out_tap) {
+  __shared__ float s_w[8];
+  const int row = blockIdx.x, tid = threadIdx.x;
+  const float* yr = y + (size_t)row * H;
+  float ss = 0.f;
+  for (int i = tid; i < H; i += 256) ss += yr[i] * yr[i];
+  ss = warp_sum(ss);
+  if ((tid & 31) == 0) s_w[tid >> 5] = ss;
+  __syncthreads();
+  float t = 0.f;
+  for (int k = 0; k < 8; ++k) t += s_w[k];
+  const float r = rsqrtf(t / H + eps);
+  for (int i = tid; i < H; i += 256) {
+    const float o = __bfloat162float(x[(size_t)row * H + i]) + yr[i] * w[i] * r;
+    out[(size_t)row * H + i] = __float2bfloat16_rn(o);
+    if (out_tap) out_tap[(size_t)row * H + i] = o;
+  }
+}
+
 // ------------------------------------------------------------------ host side
 struct VerifyState {
   CUtensorMap tm_wqkv, tm_wo;
@@ -557,6 +582,7 @@ struct VerifyState {
   float* part = nullptr;        // [max(SMs, nkv)][64][hd + 2]
   float* qkv_acc = nullptr;     // [16][rows_qkv]
   float* y_acc = nullptr;       // [16][H]
+  float* y_post = nullptr;      // [16][H]: o_proj output kept for the post-attention norm
   uint8_t* bq = nullptr;        // QKV activation operand [H / 64][32][128 B]
   uint8_t* bo = nullptr;        // o_proj activation operand [nh hd / 64][32][128 B]
   size_t part_records = 0;
@@ -571,7 +597,7 @@ hfa_status verify_create(const hfa_layer_desc& d, int num_sms, VerifyState** out
     *out = new VerifyState();  // a Q8_0 layer has no verify block: nothing to allocate
     return HFA_OK;
   }
-  const int rows_qkv = (d.num_heads + 2 * d.num_kv_heads) * d.head_dim;
+  const int rows_qkv = qkv_rows(d);
   if (rows_qkv % kVM || d.hidden % kVM || d.hidden % kVK || (d.num_heads * d.head_dim) % kVK) {
     snprintf(g_verify_error, sizeof g_verify_error,
              "verify GEMM needs projection sizes that are multiples of 128");
@@ -592,6 +618,7 @@ hfa_status verify_create(const hfa_layer_desc& d, int num_sms, VerifyState** out
     e = cudaMemset(v->bo, 0, (size_t)(d.num_heads * d.head_dim / kVK) * kBChunkBytes);
   if (e == cudaSuccess) e = cudaMalloc(&v->qkv_acc, (size_t)16 * rows_qkv * sizeof(float));
   if (e == cudaSuccess) e = cudaMalloc(&v->y_acc, (size_t)16 * d.hidden * sizeof(float));
+  if (e == cudaSuccess) e = cudaMalloc(&v->y_post, (size_t)16 * d.hidden * sizeof(float));
   if (e == cudaSuccess) e = cudaMemset(v->head_ticket, 0, (d.num_heads + 2 * nkv) * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(v->tile_ticket, 0, (d.hidden / kVM) * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(v->attn_ticket, 0, nkv * sizeof(int));
@@ -614,6 +641,7 @@ void verify_free(VerifyState* v) {
   cudaFree(v->part);
   cudaFree(v->qkv_acc);
   cudaFree(v->y_acc);
+  cudaFree(v->y_post);
   cudaFree(v->bq);
   cudaFree(v->bo);
   delete v;
@@ -651,7 +679,7 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   const hfa_layer_desc& d = *c.d;
   const int H = d.hidden, nh = d.num_heads, nkv = d.num_kv_heads, hd = d.head_dim;
   const int G = nh / nkv;
-  const int rows_qkv = (nh + 2 * nkv) * hd;
+  const int rows_qkv = qkv_rows(d);
   if (!(d.flags & HFA_F_WEIGHTS_BF16) || !v->part) {
     snprintf(msg, n, "verify is built for bf16 weights");
     return HFA_EUNSUPPORTED;
@@ -709,6 +737,7 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   qa.g.w_k = c.w_k;
   qa.g.rope_g = c.rope_g;
   qa.g.v_unit_norm = (d.flags & HFA_F_V_UNIT_NORM) ? 1 : 0;
+  qa.g.k_eq_v = (d.flags & HFA_F_K_EQ_V) ? 1 : 0;
   qa.g.q_out = c.q_f32;
   qa.g.k_cache = c.k_cache;
   qa.g.v_cache = c.v_cache;
@@ -797,6 +826,7 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   oa.g.err = c.err;
   oa.g.out = c.out;
   oa.g.out_tap = c.out_tap;
+  oa.g.y_post = c.w_post ? v->y_post : nullptr;
   oa.rows = H;
   oa.K = nh * hd;
   oa.chunks = oa.K / kVK;
@@ -810,6 +840,18 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   if (e != cudaSuccess) {
     snprintf(msg, n, "verify o_proj launch: %s", cudaGetErrorString(e));
     return HFA_ECUDA;
+  }
+  if (c.w_post) {
+    // (4) post-attention norm: out = x + y * w_post / sqrt(mean(y^2) + eps), one CTA a row
+    tb("verify_post_norm");
+    post_norm_rows_kernel<<<c.L, 256, 0, s>>>(v->y_post, c.x, c.w_post, d.hidden, d.eps, c.out,
+                                              c.out_tap);
+    e = cudaGetLastError();
+    te();
+    if (e != cudaSuccess) {
+      snprintf(msg, n, "verify post-norm launch: %s", cudaGetErrorString(e));
+      return HFA_ECUDA;
+    }
   }
   return HFA_OK;
 }

@@ -29,6 +29,7 @@ HFA_F_V_UNIT_NORM = 0x1
 HFA_F_WEIGHTS_BF16 = 0x2
 HFA_F_RING = 0x4
 HFA_F_DEBUG_TAPS = 0x8
+HFA_F_K_EQ_V = 0x10
 
 
 class HfaError(RuntimeError):
@@ -88,6 +89,10 @@ def lib():
         L.hfa_set_successor.argtypes = [P, P]
         L.hfa_debug_stall_next_step.restype = C
         L.hfa_debug_stall_next_step.argtypes = [P]
+        L.hfa_set_rope_freq_factors.restype = C
+        L.hfa_set_rope_freq_factors.argtypes = [P, P, P]
+        L.hfa_set_post_norm.restype = C
+        L.hfa_set_post_norm.argtypes = [P, P, P]
         L.hfa_last_error.restype = ctypes.c_char_p
         L.hfa_last_error.argtypes = [P]
         L.hfa_debug_taps.restype = C
@@ -178,6 +183,9 @@ def desc_for(w: wl.Workload, max_batch: Optional[int] = None, max_verify_len: Op
 def weights_to_device(w: wl.Workload, weights: Dict, device="cuda") -> Dict[str, torch.Tensor]:
     out = {}
     for k, v in weights.items():
+        if v is None:  # an absent tensor (no V projection, no variant table)
+            out[k] = None
+            continue
         if isinstance(v, np.ndarray):
             v = torch.from_numpy(np.ascontiguousarray(v))
         out[k] = v.to(device).contiguous()
@@ -197,6 +205,11 @@ class Layer:
             ctypes.byref(self._h))
         if st != HFA_OK:
             raise HfaError(st, lib().hfa_last_error(None).decode())
+        # the Gemma variants the weights carry: RoPE frequency factors, post-attention norm
+        if dev_weights.get("rope_ff") is not None:
+            self.hfa_set_rope_freq_factors(dev_weights["rope_ff"].cpu().numpy(), stream)
+        if dev_weights.get("w_post") is not None:
+            self.hfa_set_post_norm(dev_weights["w_post"], stream)
 
     @property
     def handle(self) -> ctypes.c_void_p:
@@ -244,6 +257,15 @@ class Layer:
 
     def hfa_check_device_status(self, stream=None) -> None:
         self._check(lib().hfa_check_device_status(self._h, _stream_ptr(stream)))
+
+    def hfa_set_rope_freq_factors(self, factors: Optional[np.ndarray], stream=None) -> None:
+        ff = None if factors is None else np.ascontiguousarray(factors, dtype=np.float32)
+        self._check(lib().hfa_set_rope_freq_factors(
+            self._h, None if ff is None else ctypes.c_void_p(ff.ctypes.data), _stream_ptr(stream)))
+
+    def hfa_set_post_norm(self, w_post: Optional[torch.Tensor], stream=None) -> None:
+        self._check(lib().hfa_set_post_norm(self._h, None if w_post is None else _ptr(w_post),
+                                            _stream_ptr(stream)))
 
     def hfa_debug_stall_next_step(self) -> None:
         self._check(lib().hfa_debug_stall_next_step(self._h))

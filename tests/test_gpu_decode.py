@@ -207,3 +207,39 @@ def test_bounded_wait_gives_up_reports_and_recovers():
         for key in ("out_bf16", "attn", "out"):
             assert torch.equal(after[key], before[key]), key
     layer.hfa_destroy()
+
+
+@pytest.mark.parametrize("k_eq_v,ff,post", [(True, True, True), (True, False, False),
+                                           (False, True, False), (False, False, True)],
+                         ids=["all", "keqv", "ff", "post"])
+def test_gemma_variants_full_layer(k_eq_v, ff, post):
+    # no V projection (V = unit-normed raw K), RoPE frequency factors, post-attention
+    # RMSNorm: the pages' global-layer variants, each against the oracle
+    w = SMALL.replace(name="small_var", k_eq_v=k_eq_v, rope_freq_factors=ff, post_norm=post)
+    _case(w, pos=[0, 77, 999])
+
+
+def test_post_norm_batch_of_sixteen_sliding_ring():
+    # 16 rows: every CTA's share of the outputs straddles rows, so the row statistic is
+    # summed over the CTAs that share each row
+    w = wl.SLIDING_B16.replace(name="b16_post", post_norm=True, rope_freq_factors=True)
+    _case(w)
+
+
+def test_post_norm_off_again_and_factors_cleared():
+    w = SMALL.replace(name="small_toggle", post_norm=True, rope_freq_factors=True)
+    weights = wl.make_weights(w)
+    layer = hfa.Layer(hfa.desc_for(w, debug_taps=True), hfa.weights_to_device(w, weights))
+    x = wl.make_x(w)
+    pos = np.array([5, 600, 999], dtype=np.int32)
+    kv = wl.make_kv_cache(w)
+    layer.hfa_set_post_norm(None)
+    layer.hfa_set_rope_freq_factors(None)
+    gpu = run_gpu_decode(w, weights, x, pos, kv, debug_taps=True, layer=layer)
+    plain = SMALL.replace(name="small_plain")
+    ref = oracle.decode_step(plain, weights, x, pos, kv["k_cache"], kv["v_cache"])
+    check_decode(plain, pos, gpu, ref, kv)
+    with pytest.raises(hfa.HfaError) as e:
+        layer.hfa_set_rope_freq_factors(np.zeros(w.head_dim // 2, dtype=np.float32))
+    assert e.value.status == hfa.HFA_EINVAL
+    layer.hfa_destroy()

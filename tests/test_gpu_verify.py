@@ -54,3 +54,15 @@ def test_verify_block_at_position_zero():
                     layer_type=wl.FULL, window=0, kv_capacity=64, ring=False, batch=1,
                     rope_theta=1e6, seed=96, weights_bf16=True, verify_len=16, base_pos=0)
     _case(w, 16, 0)
+
+
+@pytest.mark.parametrize("k_eq_v,ff,post", [(True, True, True), (False, False, True),
+                                           (True, False, False)], ids=["all", "post", "keqv"])
+def test_verify_block_gemma_variants(k_eq_v, ff, post):
+    # no V projection, RoPE frequency factors, post-attention RMSNorm (the pages' global
+    # layer), each against the oracle
+    w = wl.Workload(name="ver_var", hidden=1024, num_heads=8, num_kv_heads=2, head_dim=128,
+                    layer_type=wl.FULL, window=0, kv_capacity=700, ring=False, batch=1,
+                    rope_theta=1e6, seed=97, weights_bf16=True, verify_len=16, base_pos=0,
+                    k_eq_v=k_eq_v, rope_freq_factors=ff, post_norm=post)
+    _case(w, 13, 400)
