@@ -454,7 +454,8 @@ static __device__ __noinline__ void finish_outputs_post(const StepArgs& a, int c
   float* wred = red + kConsumers * 8;  // [8 warps][2]
   float* s_inv = wred + 16;            // [2]
   const int b_lo = i0 < i1 ? i0 / a.H : 0;
-  float ps[2] = {0.f, 0.f};  // this thread's part of sum(y^2) of rows b_lo, b_lo + 1
+  float ps0 = 0.f, ps1 = 0.f;  // this thread's part of sum(y^2) of rows b_lo, b_lo + 1
+  const int split_i = (b_lo + 1) * a.H;  // first output of the second row
 #pragma unroll 1
   for (int base = i0; base < i1; base += round) {
     if (k < per) {
@@ -480,13 +481,14 @@ static __device__ __noinline__ void finish_outputs_post(const StepArgs& a, int c
 #pragma unroll 1
       for (int t = 0; t < S; ++t) y += red[tid * S + t];
       ybuf[i - i0] = y;
-      ps[i / a.H - b_lo] += y * y;
+      if (i < split_i) ps0 += y * y;
+      else ps1 += y * y;
     }
     consumer_sync();
   }
   // this CTA's parts of sum(y^2): warp trees, then the warps in order
   {
-    const float t0 = warp_sum(ps[0]), t1 = warp_sum(ps[1]);
+    const float t0 = warp_sum(ps0), t1 = warp_sum(ps1);
     if (lane == 0) {
       wred[warp * 2] = t0;
       wred[warp * 2 + 1] = t1;
@@ -532,8 +534,9 @@ static __device__ __noinline__ void finish_outputs_post(const StepArgs& a, int c
   }
 #pragma unroll 1
   for (int i = i0 + tid; i < i1; i += kConsumers) {
-    const int col = i % a.H;
-    const float r = __bfloat162float(a.x[i]) + ybuf[i - i0] * a.w_post[col] * s_inv[i / a.H - b_lo];
+    const bool second = i >= split_i;
+    const int col = second ? i - split_i : i - b_lo * a.H;
+    const float r = __bfloat162float(a.x[i]) + ybuf[i - i0] * a.w_post[col] * s_inv[second ? 1 : 0];
     a.out[i] = __float2bfloat16_rn(r);
     if (a.out_tap) a.out_tap[i] = r;
   }
