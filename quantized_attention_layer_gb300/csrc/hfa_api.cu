@@ -55,8 +55,8 @@ struct hfa_layer {
   StepGemv g_qkv{}, g_o{};
   const uint8_t* successor_qkv = nullptr;  // QKV tiles of the layer that runs next
   int stall_next = 0;  // test hook (hfa_debug_stall_next_step), one step
-  __nv_bfloat16* wqkv_bf16 = nullptr;  // verify path: [(nh + 2 nkv) hd, H]
-  __nv_bfloat16* wo_bf16 = nullptr;    // [H, nh hd]
+  __nv_bfloat16* wqkv_bf16 = nullptr;  // verify path: [(nh + 2 nkv) hd, H] as 128 x 64 tiles
+  __nv_bfloat16* wo_bf16 = nullptr;    // [H, nh hd] as 128 x 64 tiles
   float* w_in = nullptr;
   float* w_q = nullptr;
   float* w_k = nullptr;
@@ -159,19 +159,6 @@ hfa_status hfa_encode_kv_map(CUtensorMap* map, void* base, int rows, int hd, int
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? HFA_OK : HFA_EINVAL;
-}
-
-bool hfa::encode_bf16_2d(CUtensorMap* map, void* base, int inner, int rows, int box_inner,
-                         int box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
-  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // ------------------------------------------------------------------ timing
@@ -363,14 +350,17 @@ extern "C" hfa_status hfa_layer_create(const hfa_layer_desc* desc, const void* w
   } else {
     LA(L->wqkv_bf16, (size_t)L->rows_qkv * H);
     LA(L->wo_bf16, (size_t)H * nh * hd);
-    const size_t qb = (size_t)nh * hd * H * 2, kb = (size_t)nkv * hd * H * 2;
-    LC(cudaMemcpyAsync(L->wqkv_bf16, wq, qb, cudaMemcpyDeviceToDevice, s), "copy wq");
-    LC(cudaMemcpyAsync((char*)L->wqkv_bf16 + qb, wk, kb, cudaMemcpyDeviceToDevice, s), "copy wk");
-    if (!(d.flags & HFA_F_K_EQ_V))
-      LC(cudaMemcpyAsync((char*)L->wqkv_bf16 + qb + kb, wv, kb, cudaMemcpyDeviceToDevice, s),
-         "copy wv");
-    LC(cudaMemcpyAsync(L->wo_bf16, wo, (size_t)H * nh * hd * 2, cudaMemcpyDeviceToDevice, s),
-       "copy wo");
+    if (L->rows_qkv % 128 == 0 && H % 128 == 0 && H % 64 == 0 && (nh * hd) % 64 == 0) {
+      const bool kv1 = d.flags & HFA_F_K_EQ_V;
+      LC(launch_repack_bf16_tiles((const __nv_bfloat16*)wq, nh * hd, (const __nv_bfloat16*)wk,
+                                  kv1 ? L->rows_qkv - nh * hd : nkv * hd,
+                                  (const __nv_bfloat16*)(kv1 ? wk : wv), L->rows_qkv, H,
+                                  (uint8_t*)L->wqkv_bf16, s),
+         "repack wqkv");
+      LC(launch_repack_bf16_tiles((const __nv_bfloat16*)wo, H, (const __nv_bfloat16*)wo, 0,
+                                  (const __nv_bfloat16*)wo, H, nh * hd, (uint8_t*)L->wo_bf16, s),
+         "repack wo");
+    }
   }
   LA(L->w_in, H);
   LA(L->w_q, hd);
@@ -897,9 +887,9 @@ extern "C" int hfa_kernel_times(hfa_layer* L, int n, const char** names, float* 
     L->event_pool.push_back(t.stop);
   }
   L->pending.clear();
-  static const char* kNames[] = {"decode_step", "flash_decode",
-                                 "verify_prep", "verify_qkv_gemm", "verify_norm_rope_append", "verify_attention",
-                                 "verify_oproj_gemm", "verify_residual"};
+  static const char* kNames[] = {"decode_step",       "flash_decode",      "verify_prep",
+                                 "verify_qkv_gemm",   "verify_attention",  "verify_attn_merge",
+                                 "verify_oproj_gemm", "verify_post_norm"};
   int k = 0;
   for (size_t i = 0; i < L->slot_names.size() && k < n; ++i, ++k) {
     const char* nm = "?";

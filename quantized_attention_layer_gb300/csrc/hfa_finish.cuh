@@ -22,99 +22,140 @@ __device__ __forceinline__ void rope_cs(int P, float2 gpair, float& c, float& s)
   sincospif(2.0f * r, &s, &c);
 }
 
-// Epilogue of one attention head (QKV mode): rows [hh*hd, hh*hd + hd) of the QKV output.
+// Epilogue of one token row b of one attention head (QKV mode): v holds rows
+// [hh*hd, hh*hd + hd) of the QKV output for that token, lane + 32 j in v[j].
 template <int HD>
-static __device__ void finish_head(const GemvArgs& a, int hh, int lane) {
+static __device__ __forceinline__ void finish_head_row(const GemvArgs& a, int hh, int b, float (&v)[HD / 32],
+                                       int lane) {
   constexpr int J = HD / 32;   // values per lane; pairs (j, j + J/2) are RoPE partners
-  const int R16 = a.R * 16;
   const int kind = hh < a.nh ? 0 : (hh < a.nh + a.nkv ? 1 : 2);  // q, k, v
-  for (int b = 0; b < a.batch; ++b) {
-    float v[J];
+  const int seq = a.rows_are_tokens ? 0 : b;
+  const int P = a.rows_are_tokens ? a.base_pos + b : a.seq_pos[b];
+  if (kind == 1 && a.k_eq_v && P >= 0 && (a.ring || P < a.C)) {
+    // no V projection: V is the raw K, RMS-normalised per head with unit weight
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < J; ++j) ss += v[j] * v[j];
+    const float inv = rsqrtf(warp_sum(ss) / HD + a.eps);
+    const int kvh = hh - a.nh;
+    const int slot = a.ring ? P % a.C : P;
+    __nv_bfloat16* dst = a.v_cache + (((size_t)seq * a.nkv + kvh) * a.C + slot) * HD;
 #pragma unroll
     for (int j = 0; j < J; ++j) {
-      float* p = a.acc + (size_t)b * R16 + (size_t)hh * HD + lane + 32 * j;
-      v[j] = ld_cg_f32(p);
-      *p = 0.0f;
+      dst[lane + 32 * j] = __float2bfloat16_rn(v[j] * inv);
+      if (a.v_tap) a.v_tap[((size_t)b * a.nkv + kvh) * HD + lane + 32 * j] = v[j] * inv;
     }
-    const int seq = a.rows_are_tokens ? 0 : b;
-    const int P = a.rows_are_tokens ? a.base_pos + b : a.seq_pos[b];
-    if (kind == 1 && a.k_eq_v && P >= 0 && (a.ring || P < a.C)) {
-      // no V projection: V is the raw K, RMS-normalised per head with unit weight
-      float ss = 0.f;
+  }
+  if (kind < 2 || a.v_unit_norm) {
+    float ss = 0.f;
 #pragma unroll
-      for (int j = 0; j < J; ++j) ss += v[j] * v[j];
-      const float inv = rsqrtf(warp_sum(ss) / HD + a.eps);
-      const int kvh = hh - a.nh;
-      const int slot = a.ring ? P % a.C : P;
-      __nv_bfloat16* dst = a.v_cache + (((size_t)seq * a.nkv + kvh) * a.C + slot) * HD;
+    for (int j = 0; j < J; ++j) ss += v[j] * v[j];
+    ss = warp_sum(ss);
+    const float inv = rsqrtf(ss / HD + a.eps);
+    const float* w = kind == 0 ? a.w_q : a.w_k;  // a valid address for v too (unused)
 #pragma unroll
-      for (int j = 0; j < J; ++j) {
-        dst[lane + 32 * j] = __float2bfloat16_rn(v[j] * inv);
-        if (a.v_tap) a.v_tap[((size_t)b * a.nkv + kvh) * HD + lane + 32 * j] = v[j] * inv;
-      }
+    for (int j = 0; j < J; ++j) {
+      const float wj = __ldg(w + lane + 32 * j);
+      v[j] *= inv * (kind < 2 ? wj : 1.0f);
     }
-    if (kind < 2 || a.v_unit_norm) {
-      float ss = 0.f;
+  }
+  if (kind < 2) {
 #pragma unroll
-      for (int j = 0; j < J; ++j) ss += v[j] * v[j];
-      ss = warp_sum(ss);
-      const float inv = rsqrtf(ss / HD + a.eps);
-      const float* w = kind == 0 ? a.w_q : a.w_k;  // a valid address for v too (unused)
-#pragma unroll
-      for (int j = 0; j < J; ++j) {
-        const float wj = __ldg(w + lane + 32 * j);
-        v[j] *= inv * (kind < 2 ? wj : 1.0f);
-      }
+    for (int j = 0; j < J / 2; ++j) {
+      float c, s;
+      rope_cs(P, a.rope_g[lane + 32 * j], c, s);
+      const float x0 = v[j], x1 = v[j + J / 2];
+      v[j] = x0 * c - x1 * s;
+      v[j + J / 2] = x0 * s + x1 * c;
     }
-    if (kind < 2) {
+  }
+  if (kind == 0) {
+    float* q = a.q_out + ((size_t)b * a.nh + hh) * HD;
 #pragma unroll
-      for (int j = 0; j < J / 2; ++j) {
-        float c, s;
-        rope_cs(P, a.rope_g[lane + 32 * j], c, s);
-        const float x0 = v[j], x1 = v[j + J / 2];
-        v[j] = x0 * c - x1 * s;
-        v[j + J / 2] = x0 * s + x1 * c;
-      }
+    for (int j = 0; j < J; ++j) q[lane + 32 * j] = v[j];
+  } else {
+    const int kvh = kind == 1 ? hh - a.nh : hh - a.nh - a.nkv;
+    if (P < 0 || (!a.ring && P >= a.C)) {
+      if (lane == 0) atomicOr(a.err, kErrBadPosition);
+      return;
     }
-    if (kind == 0) {
-      float* q = a.q_out + ((size_t)b * a.nh + hh) * HD;
+    const int slot = a.ring ? P % a.C : P;
+    __nv_bfloat16* cache = kind == 1 ? a.k_cache : a.v_cache;
+    __nv_bfloat16* dst = cache + (((size_t)seq * a.nkv + kvh) * a.C + slot) * HD;
+    float* tap = kind == 1 ? a.k_tap : a.v_tap;
 #pragma unroll
-      for (int j = 0; j < J; ++j) q[lane + 32 * j] = v[j];
-    } else {
-      const int kvh = kind == 1 ? hh - a.nh : hh - a.nh - a.nkv;
-      if (P < 0 || (!a.ring && P >= a.C)) {
-        if (lane == 0) atomicOr(a.err, kErrBadPosition);
-        continue;
-      }
-      const int slot = a.ring ? P % a.C : P;
-      __nv_bfloat16* cache = kind == 1 ? a.k_cache : a.v_cache;
-      __nv_bfloat16* dst = cache + (((size_t)seq * a.nkv + kvh) * a.C + slot) * HD;
-      float* tap = kind == 1 ? a.k_tap : a.v_tap;
-#pragma unroll
-      for (int j = 0; j < J; ++j) {
-        dst[lane + 32 * j] = __float2bfloat16_rn(v[j]);
-        if (tap) tap[((size_t)b * a.nkv + kvh) * HD + lane + 32 * j] = v[j];
-      }
+    for (int j = 0; j < J; ++j) {
+      dst[lane + 32 * j] = __float2bfloat16_rn(v[j]);
+      if (tap) tap[((size_t)b * a.nkv + kvh) * HD + lane + 32 * j] = v[j];
     }
   }
 }
 
-// Epilogue of one row group (o_proj mode): out = bf16(x + y), or y kept in y_post for the
-// post-attention norm pass (which needs the whole row's mean of y^2 first).
-static __device__ void finish_rowgroup(const GemvArgs& a, int r, int lane) {
+// Epilogue of one attention head (QKV mode) for the token rows b0, b0 + bstep, ...: the
+// accumulators of four such rows are loaded together (and zeroed for the next call),
+// then each row is finished.
+template <int HD>
+static __device__ void finish_head(const GemvArgs& a, int hh, int lane, int b0, int bstep) {
+  constexpr int J = HD / 32;
+  constexpr int TB = 4;
   const int R16 = a.R * 16;
-  for (int i = lane; i < 16 * a.batch; i += 32) {
-    const int b = i >> 4, row = r * 16 + (i & 15);
-    float* p = a.acc + (size_t)b * R16 + row;
-    const float y = ld_cg_f32(p);
-    *p = 0.0f;
-    if (a.y_post) {  // the post-attention norm pass writes the output
-      a.y_post[(size_t)b * R16 + row] = y;
-      continue;
+  for (int bb = b0; bb < a.batch; bb += TB * bstep) {
+    float v[TB][J];
+#pragma unroll
+    for (int u = 0; u < TB; ++u) {
+      const int b = bb + u * bstep;
+#pragma unroll
+      for (int j = 0; j < J; ++j)
+        v[u][j] = b < a.batch
+                      ? ld_cg_f32(a.acc + (size_t)b * R16 + (size_t)hh * HD + lane + 32 * j)
+                      : 0.f;
     }
-    const float o = __bfloat162float(a.x[(size_t)b * R16 + row]) + y;
-    a.out[(size_t)b * R16 + row] = __float2bfloat16_rn(o);
-    if (a.out_tap) a.out_tap[(size_t)b * R16 + row] = o;
+#pragma unroll
+    for (int u = 0; u < TB; ++u) {
+      const int b = bb + u * bstep;
+      if (b >= a.batch) break;
+#pragma unroll
+      for (int j = 0; j < J; ++j) a.acc[(size_t)b * R16 + (size_t)hh * HD + lane + 32 * j] = 0.f;
+      finish_head_row<HD>(a, hh, b, v[u], lane);
+    }
+  }
+}
+
+// Epilogue of output rows [row0, row0 + nrows) for every token (o_proj mode), items
+// spread over nthr threads with sixteen accumulator loads in flight per thread:
+// out = bf16(x + y), or y kept in y_post for the post-attention norm pass (which needs
+// the whole row's mean of y^2 first).
+static __device__ void finish_rows(const GemvArgs& a, int row0, int nrows, int tid, int nthr) {
+  constexpr int U = 16;
+  const int R16 = a.R * 16;
+  const int n = nrows * a.batch;
+  for (int i0 = tid; i0 < n; i0 += U * nthr) {
+    float y[U], xv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + u * nthr;
+      y[u] = xv[u] = 0.f;
+      if (i < n) {
+        const int b = i / nrows, row = row0 + i - b * nrows;
+        y[u] = ld_cg_f32(a.acc + (size_t)b * R16 + row);
+        if (!a.y_post) xv[u] = __bfloat162float(a.x[(size_t)b * R16 + row]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + u * nthr;
+      if (i >= n) break;
+      const int b = i / nrows, row = row0 + i - b * nrows;
+      const size_t off = (size_t)b * R16 + row;
+      a.acc[off] = 0.0f;
+      if (a.y_post) {  // the post-attention norm pass writes the output
+        a.y_post[off] = y[u];
+        continue;
+      }
+      const float o = xv[u] + y[u];
+      a.out[off] = __float2bfloat16_rn(o);
+      if (a.out_tap) a.out_tap[off] = o;
+    }
   }
 }
 

@@ -127,13 +127,13 @@ struct LaunchTimer {
 // message returned by hfa_last_error(NULL) on this thread
 void set_thread_error(const char* msg);
 
-// TMA descriptor of a row-major bf16 matrix [rows, inner] with boxes of
-// box_inner x box_rows and the 128-byte swizzle (box_inner * 2 must be 128)
-bool encode_bf16_2d(CUtensorMap* map, void* base, int inner, int rows, int box_inner,
-                    int box_rows);
-
 cudaError_t launch_repack_q8_0_split(const uint8_t* src, int rows, int cols, uint8_t* dst,
                                      int row_group0, int R_total, int nbs, cudaStream_t s);
+// bf16 [rows, K] (rows from s0, then s1, then s2) -> 128 x 64 tiles of 16 KB in the
+// 128-byte-swizzled order of the verify GEMM's shared-memory stages
+cudaError_t launch_repack_bf16_tiles(const __nv_bfloat16* s0, int n0, const __nv_bfloat16* s1,
+                                     int n1, const __nv_bfloat16* s2, int rows, int K,
+                                     uint8_t* dst, cudaStream_t s);
 // the decode step: grid = one CTA per SM (cooperative), ntiles = gemv batch tiles
 cudaError_t launch_step(const StepArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int hd,
                         int grid, cudaStream_t s);

@@ -18,8 +18,9 @@ struct VerifyCall {
   __nv_bfloat16* k_cache;  // [1, nkv, C, hd]
   __nv_bfloat16* v_cache;
   __nv_bfloat16* out;      // [L, H]
-  const __nv_bfloat16* wqkv;  // [qkv_rows(d), H]: q, k and (without k_eq_v) v rows
-  const __nv_bfloat16* wo;    // [H, nh hd]
+  const __nv_bfloat16* wqkv;  // [qkv_rows(d), H]: q, k and (without k_eq_v) v rows, as
+                              // 128 x 64 tiles (launch_repack_bf16_tiles)
+  const __nv_bfloat16* wo;    // [H, nh hd], as 128 x 64 tiles
   const float* w_in;
   const float* w_q;
   const float* w_k;

@@ -1,4 +1,4 @@
-// k_repack.cu -- Q8_0 blocks -> MMA-ready tiles (run once at layer creation).
+// k_repack.cu -- weights -> MMA-ready tiles (run once at layer creation).
 //
 // Input: the Q8_0 layout of the Q8_0 lm_head re-quantiser (gemma4/model.rs): per row,
 // cols/32 blocks of 34 bytes = fp16 scale d (little endian) + 32 int8 q.  The 34-byte
@@ -65,6 +65,40 @@ cudaError_t launch_repack_q8_0_split(const uint8_t* src, int rows, int cols, uin
   if (blocks > 65535) blocks = 65535;
   repack_q8_0_split_kernel<<<(int)blocks, threads, 0, s>>>(src, rows, cols, dst, row_group0,
                                                            R_total, nbs);
+  return cudaGetLastError();
+}
+
+// bf16 matrix [rows, K] (rows 0 .. n0-1 from s0, the next n1 from s1, the rest from
+// s2) -> the shared-memory image of the verify GEMM's A stages: tile (m, c) of 128 rows x
+// 64 columns is 16 KB at ((m * K / 64) + c) * 16 KB, row r of the tile at r * 128 bytes,
+// its 16-byte group j at position j XOR (r mod 8) -- the 128-byte swizzle the tensor-core
+// descriptors read.  The row tiles of one matrix stream as one contiguous range each.
+__global__ void repack_bf16_tiles_kernel(const __nv_bfloat16* __restrict__ s0, int n0,
+                                         const __nv_bfloat16* __restrict__ s1, int n1,
+                                         const __nv_bfloat16* __restrict__ s2, int rows, int K,
+                                         uint8_t* __restrict__ dst) {
+  const int g8 = K / 8;  // 16-byte groups per row
+  const long long n = (long long)rows * g8;
+  for (long long u = blockIdx.x * (long long)blockDim.x + threadIdx.x; u < n;
+       u += (long long)gridDim.x * blockDim.x) {
+    const int row = (int)(u / g8), j8 = (int)(u - (long long)row * g8);
+    const __nv_bfloat16* src = row < n0        ? s0 + (size_t)row * K
+                               : row < n0 + n1 ? s1 + (size_t)(row - n0) * K
+                                               : s2 + (size_t)(row - n0 - n1) * K;
+    const uint4 v = *reinterpret_cast<const uint4*>(src + j8 * 8);
+    const int m = row >> 7, r = row & 127, c = j8 >> 3, j = j8 & 7;
+    const size_t off = (((size_t)m * (K / 64) + c) * 128 + r) * 128 + ((j ^ (r & 7)) << 4);
+    *reinterpret_cast<uint4*>(dst + off) = v;
+  }
+}
+
+cudaError_t launch_repack_bf16_tiles(const __nv_bfloat16* s0, int n0, const __nv_bfloat16* s1,
+                                     int n1, const __nv_bfloat16* s2, int rows, int K,
+                                     uint8_t* dst, cudaStream_t s) {
+  const long long n = (long long)rows * (K / 8);
+  long long blocks = (n + 255) / 256;
+  if (blocks > 65535) blocks = 65535;
+  repack_bf16_tiles_kernel<<<(int)blocks, 256, 0, s>>>(s0, n0, s1, n1, s2, rows, K, dst);
   return cudaGetLastError();
 }
 

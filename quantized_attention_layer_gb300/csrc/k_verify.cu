@@ -8,15 +8,20 @@
 //
 //  * verify_gemm_kernel (tcgen05): swap-AB -- the weight rows are the MMA's M = 128, the
 //    activations its N = 32 (16 tokens x fp32 split into bf16 hi and lo, so the product
-//    keeps ~16 bits of the activation), K in 64-element stages.  A TMA producer thread
-//    streams 128x64 weight tiles (128-byte swizzle) into a 4-stage mbarrier ring; one
+//    keeps ~16 bits of the activation), K in 64-element stages.  A producer thread
+//    streams 128x64 weight tiles -- repacked at layer creation into the 128-byte-swizzled
+//    shared-memory image, so each is one 16 KB bulk copy -- into a 6-stage ring; one
 //    thread issues tcgen05.mma into a 128x32 fp32 TMEM accumulator and releases stages
 //    with tcgen05.commit; the four warps read the accumulator back (tcgen05.ld) and add
 //    their partial sums (k-split) into an fp32 accumulator.  The CTA whose chunks
 //    complete a head / row tile runs the same epilogue as the decode GEMV.
 //  * attn_verify_kernel: one CTA per (KV head, key chunk); a TMA producer warp streams K
 //    and V tiles, each consumer warp owns 8 query rows (bf16 hi/lo in MMA rows g and
-//    g + 8) and sweeps every key of the stage with the causal mask of its rows.
+//    g + 8) and takes every 64-key stage in one online-softmax update (the stage's
+//    scores, then O += P V), with the causal / window mask of its rows.  Each CTA
+//    writes one (O, m, l) record per query row.
+//  * attn_verify_merge_kernel: the records of a KV head's chunks combined, a few query
+//    rows per CTA, into the f32 output and the o_proj activation operand.
 #include <stdio.h>
 
 #include "hfa_common.cuh"
@@ -52,15 +57,15 @@ __device__ __forceinline__ void store_bop_group(uint8_t* bops, int t, int e, con
 constexpr int kVM = 128;         // weight rows per CTA = MMA M
 constexpr int kVN = 32;          // MMA N: 16 tokens x (hi, lo)
 constexpr int kVK = 64;          // K elements per stage (one 128-byte swizzled row)
-constexpr int kVStages = 4;
-constexpr int kVMaxChunks = 24;  // K stages per CTA whose activation tile stays resident
-constexpr int kAStageBytes = kVM * kVK * 2;  // 16 KB
-constexpr int kBChunkBytes = kVN * kVK * 2;  // 4 KB
-constexpr size_t kVGemmSmem =
-    1024 + (size_t)kVStages * kAStageBytes + (size_t)kVMaxChunks * kBChunkBytes + 256;
+constexpr int kVStages = 10;     // ring depth: 200 KB of copies in flight per SM
+constexpr int kAStageBytes = kVM * kVK * 2;  // 16 KB weight tile
+constexpr int kBChunkBytes = kVN * kVK * 2;  // 4 KB activation chunk
+constexpr int kVStageBytes = kAStageBytes + kBChunkBytes;
+constexpr size_t kVGemmSmem = 1024 + (size_t)kVStages * kVStageBytes + 256;
 
 struct VGemmArgs {
   GemvArgs g;        // epilogue arguments (accumulator, tickets, norms, caches, ...)
+  const uint8_t* wt;    // weights as 16 KB tiles [rows / 128][K / 64] (launch_repack_bf16_tiles)
   const uint8_t* bops;  // activation operand, [K / 64 chunks][32 rows][128 B], swizzled
   int rows;          // output features
   int K;             // input features
@@ -81,6 +86,8 @@ __global__ void __launch_bounds__(256) verify_prep_kernel(const __nv_bfloat16* _
   __shared__ float s_red[8];
   const int t = blockIdx.x;
   const int ngroups = K / 8;
+  if (t < L)  // the input row into L2 while the previous kernel finishes
+    for (int e = threadIdx.x; e < K / 64; e += blockDim.x) prefetch_l2(x + (size_t)t * K + e * 64);
   pdl_wait();
   float inv = 0.f;
   if (t < L) {
@@ -125,19 +132,16 @@ __global__ void __launch_bounds__(256) verify_prep_kernel(const __nv_bfloat16* _
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(128) verify_gemm_kernel(const __grid_constant__ CUtensorMap tw,
-                                                          const VGemmArgs a) {
+__global__ void __launch_bounds__(128, 1) verify_gemm_kernel(const VGemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
-  uint8_t* sa = smem;                                   // A stages
-  uint8_t* sb = smem + kVStages * kAStageBytes;         // B chunks of this CTA
-  uint64_t* full = reinterpret_cast<uint64_t*>(sb + kVMaxChunks * kBChunkBytes);
+  uint8_t* ring = smem;  // stage i: weight tile (16 KB), then activation chunk (4 KB)
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + kVStages * kVStageBytes);
   uint64_t* empty = full + kVStages;
   uint64_t* done = empty + kVStages;
-  uint64_t* bready = done + 1;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bready + 1);
-  int* s_fin = reinterpret_cast<int*>(s_tmem + 1);      // [0..3] finished heads / tile flag
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(done + 1);
+  int* s_fin = reinterpret_cast<int*>(s_tmem + 1);      // [0..3] finished heads, [4] count
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = blockIdx.x / a.splits, sp = blockIdx.x - mt * a.splits;
   const int c0 = a.chunks * sp / a.splits, c1 = a.chunks * (sp + 1) / a.splits;
@@ -147,58 +151,72 @@ __global__ void __launch_bounds__(128) verify_gemm_kernel(const __grid_constant_
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kVStages; ++i) {
-      mbar_init(&full[i], 1);
+      mbar_init(&full[i], 2);  // one arrival with the weight copy, one with the activation's
       mbar_init(&empty[i], 1);
     }
     mbar_init(done, 1);
-    mbar_init(bready, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
     tmem_alloc(s_tmem, kVN);
     tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) prefetch_tmap(&tw);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
-  // the weights never depend on an earlier kernel: fill the ring right away
+  // the weights never depend on an earlier kernel: fill the ring's weight tiles right
+  // away.  The CTA's tiles (m, c0 .. c1 - 1) are one contiguous range, 16 KB a stage;
+  // the activation chunks (laid out in shared-memory order by verify_prep_kernel or
+  // the attention merge) follow once the previous kernel has finished.
+  const uint8_t* wsrc = a.wt + ((size_t)mt * a.chunks + c0) * kAStageBytes;
+  const uint8_t* bsrc = a.bops + (size_t)c0 * kBChunkBytes;
   const int npre = nch < kVStages ? nch : kVStages;
   if (warp == 0 && lane == 0) {
     for (int i = 0; i < npre; ++i) {
       mbar_arrive_expect_tx(&full[i], kAStageBytes);
-      tma_load_2d(sa + i * kAStageBytes, &tw, &full[i], (c0 + i) * kVK, m0);
+      bulk_load(ring + i * kVStageBytes, wsrc + (size_t)i * kAStageBytes, kAStageBytes, &full[i]);
+    }
+  }
+  if (warp == 2) {
+    // the lines the epilogue reads (the accumulator rows of this tile, and the residual
+    // in o_proj mode) into L2, where the weight stream would otherwise have left them cold
+    const int R16 = a.g.R * 16;
+    for (int q = lane; q < 4 * L; q += 32) {
+      const int t = q >> 2, part = q & 3;
+      prefetch_l2(a.g.acc + (size_t)t * R16 + m0 + part * 32);
+      if (MODE == kModeOProj) prefetch_l2(a.g.x + (size_t)t * R16 + m0 + part * 32);
     }
   }
   pdl_wait();
-  // B operand: the chunks [c0, c1) of the activation operand that verify_prep_kernel
-  // (or the block attention's merge) laid out in shared-memory order, one bulk copy
-  if (warp == 1 && lane == 0) {
-    mbar_arrive_expect_tx(bready, (uint32_t)nch * kBChunkBytes);
-    bulk_load(sb, a.bops + (size_t)c0 * kBChunkBytes, (uint32_t)nch * kBChunkBytes, bready);
-  }
   pdl_launch_dependents();
 
   if (warp == 0 && lane == 0) {
-    // ---- TMA producer
+    // ---- producer
+    for (int i = 0; i < npre; ++i) {
+      mbar_arrive_expect_tx(&full[i], kBChunkBytes);
+      bulk_load(ring + i * kVStageBytes + kAStageBytes, bsrc + (size_t)i * kBChunkBytes,
+                kBChunkBytes, &full[i]);
+    }
     for (int i = npre; i < nch; ++i) {
       const int st = i % kVStages;
-      if (i >= kVStages && !mbar_wait(&empty[st], ((i / kVStages) - 1) & 1, a.g.err)) break;
+      if (!mbar_wait(&empty[st], ((i / kVStages) - 1) & 1, a.g.err)) break;
+      uint8_t* stage = ring + st * kVStageBytes;
       mbar_arrive_expect_tx(&full[st], kAStageBytes);
-      tma_load_2d(sa + st * kAStageBytes, &tw, &full[st], (c0 + i) * kVK, m0);
+      bulk_load(stage, wsrc + (size_t)i * kAStageBytes, kAStageBytes, &full[st]);
+      mbar_arrive_expect_tx(&full[st], kBChunkBytes);
+      bulk_load(stage + kAStageBytes, bsrc + (size_t)i * kBChunkBytes, kBChunkBytes, &full[st]);
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer
     constexpr uint32_t idesc = idesc_bf16_f32(kVM, kVN);
-    const bool bok = mbar_wait(bready, 0, a.g.err);
-    for (int i = 0; bok && i < nch; ++i) {
+    for (int i = 0; i < nch; ++i) {
       const int st = i % kVStages;
       if (!mbar_wait(&full[st], (i / kVStages) & 1, a.g.err)) break;
       tc_fence_after();
-      const uint32_t abase = smem_u32(sa + st * kAStageBytes);
-      const uint32_t bbase = smem_u32(sb + i * kBChunkBytes);
+      const uint32_t abase = smem_u32(ring + st * kVStageBytes);
+      const uint32_t bbase = abase + kAStageBytes;
 #pragma unroll
       for (int kk = 0; kk < kVK / 16; ++kk)
         tc_mma_f16(tmem, smem_desc_sw128(abase + kk * 32), smem_desc_sw128(bbase + kk * 32),
@@ -229,27 +247,30 @@ __global__ void __launch_bounds__(128) verify_gemm_kernel(const __grid_constant_
 
   // ---- completion tickets and epilogues
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 4; ++i) s_fin[i] = -1;
+    int nf = 0;
     if (MODE == kModeQKV) {
       const int h0 = m0 / a.g.hd, h1 = (m0 + kVM - 1) / a.g.hd;
-      for (int h = h0, j = 0; h <= h1 && j < 4; ++h, ++j)
-        if (atomicAdd(a.g.ticket + h, nch) + nch == a.need) s_fin[j] = h;
+      for (int h = h0; h <= h1 && nf < 4; ++h)
+        if (atomicAdd(a.g.ticket + h, nch) + nch == a.need) s_fin[nf++] = h;
     } else {
-      if (atomicAdd(a.g.ticket + mt, nch) + nch == a.need) s_fin[0] = mt;
+      if (atomicAdd(a.g.ticket + mt, nch) + nch == a.need) s_fin[nf++] = mt;
     }
+    for (int i = 0; i < nf; ++i) a.g.ticket[s_fin[i]] = 0;
+    s_fin[4] = nf;
   }
   __syncthreads();
+  const int nf = s_fin[4];
+  if (nf == 0) return;
   __threadfence();
   if (MODE == kModeQKV) {
-    if (s_fin[warp] >= 0) {
-      if (lane == 0) a.g.ticket[s_fin[warp]] = 0;
-      if (a.g.hd == 64) finish_head<64>(a.g, s_fin[warp], lane);
-      else if (a.g.hd == 128) finish_head<128>(a.g, s_fin[warp], lane);
-      else finish_head<256>(a.g, s_fin[warp], lane);
+    // every warp takes the token rows warp, warp + 4, ... of each completed head
+    for (int f = 0; f < nf; ++f) {
+      if (a.g.hd == 64) finish_head<64>(a.g, s_fin[f], lane, warp, 4);
+      else if (a.g.hd == 128) finish_head<128>(a.g, s_fin[f], lane, warp, 4);
+      else finish_head<256>(a.g, s_fin[f], lane, warp, 4);
     }
-  } else if (s_fin[0] >= 0) {
-    if (threadIdx.x == 0) a.g.ticket[mt] = 0;
-    for (int r = warp; r < kVM / 16; r += 4) finish_rowgroup(a.g, m0 / 16 + r, lane);
+  } else {
+    finish_rows(a.g, m0, kVM, threadIdx.x, blockDim.x);
   }
 }
 
@@ -263,7 +284,6 @@ struct VAttnArgs {
   int splits, chunk, klo, khi;  // keys [klo, khi] are read by some row
   float* part;                  // [nkv][splits][64 rows][hd + 4]: O[hd], m, l, pad
   uint8_t* bops;                // o_proj activation operand (see store_bop_group)
-  int* ticket;                  // [nkv]
   float* o;                     // [L, nh, hd]
   unsigned* err;
 };
@@ -275,6 +295,7 @@ struct VACfg {
   static constexpr int STAGE = 2 * TILE;
   static constexpr int KS = HD / 16;
   static constexpr int NTO = HD / 8;
+  static constexpr int KB = HD >= 256 ? 16 : 64;  // keys per online-softmax update (registers)
   static constexpr size_t SMEM = 1024 + (size_t)NS * STAGE + 8 * KS * 32 * 16 + 256;
 };
 
@@ -290,6 +311,7 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
                                                           const VAttnArgs a) {
   using Cfg = VACfg<HD>;
   constexpr int NS = Cfg::NS;
+  constexpr int KB = Cfg::KB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
@@ -315,7 +337,6 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
     fence_barrier_init();
   }
   __syncthreads();
-  pdl_wait();
 
   const int k_begin = a.klo + split * a.chunk;
   int k_end = k_begin + a.chunk;
@@ -328,9 +349,16 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
 
   if (warp == nc) {
     if (lane == 0) {
+      // keys before the block's first position are not written by the QKV kernel: the
+      // first stages of such keys are requested before waiting for it
       int issued = 0;
+      bool waited = false;
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % NS;
+        if (!waited && (i >= NS || k_begin + (i + 1) * kVT > a.base)) {
+          pdl_wait();
+          waited = true;
+        }
         if (i >= NS && !mbar_wait(&empty[st], ((i / NS) - 1) & 1, a.err, &s_flags[0])) {
           atomicExch(&s_flags[0], 1);
           break;
@@ -345,9 +373,13 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
         }
         issued = i + 1;
       }
+      if (!waited) pdl_wait();
       s_flags[1] = issued;
     }
+    pdl_launch_dependents();
   } else {
+    pdl_wait();
+    pdl_launch_dependents();
     // query rows of this warp: q = 8 warp + g  ->  token q / G, head kvh G + q % G
     const int qrow = 8 * warp + g;
     const bool qvalid = qrow < NQ;
@@ -384,44 +416,69 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
         atomicExch(&s_flags[0], 1);
         break;
       }
-      const uint32_t kb = stage_base + st * Cfg::STAGE;
-      const uint32_t vb = kb + Cfg::TILE;
-      for (int kg = 0; kg < kVT / 16; ++kg) {
-        const int krow = kg * 16;
-        const int key0 = k_begin + i * kVT + krow;
-        if (key0 >= k_end) break;
-        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint32_t kb0 = stage_base + st * Cfg::STAGE;
+      const uint32_t vb0 = kb0 + Cfg::TILE;
+#pragma unroll 1
+      for (int hb = 0; hb < kVT; hb += KB) {
+      const int key_lo = k_begin + i * kVT + hb, key_hi = key_lo + KB - 1;
+      if (key_lo >= k_end) break;
+      // scores of KB keys, KB / 8 independent accumulator chains: n-tile j holds keys
+      // 8j .. 8j + 7, rows g (q hi) and g + 8 (q lo)
+      float s[KB / 8][4];
 #pragma unroll
-        for (int ks = 0; ks < Cfg::KS; ++ks) {
-          const uint4 qa = myq[ks * 32 + lane];
-          const uint32_t A[4] = {qa.x, qa.y, qa.z, qa.w};
-          const int mrow = krow + ((lane >> 4) << 3) + (lane & 7);
+      for (int j = 0; j < KB / 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < Cfg::KS; ++ks) {
+        const uint4 qa = myq[ks * 32 + lane];
+        const uint32_t A[4] = {qa.x, qa.y, qa.z, qa.w};
+#pragma unroll
+        for (int kg = 0; kg < KB / 16; ++kg) {
+          const int mrow = hb + kg * 16 + ((lane >> 4) << 3) + (lane & 7);
           const int mchunk = ks * 2 + ((lane >> 3) & 1);
           uint32_t b0, b1, b2, b3;
-          ldmatrix_x4(kb + vswz<HD>(mrow, mchunk), b0, b1, b2, b3);
-          mma_bf16(s0, A, b0, b1);
-          mma_bf16(s1, A, b2, b3);
+          ldmatrix_x4(kb0 + vswz<HD>(mrow, mchunk), b0, b1, b2, b3);
+          mma_bf16(s[2 * kg], A, b0, b1);
+          mma_bf16(s[2 * kg + 1], A, b2, b3);
         }
-        float sv[4] = {s0[0] + s0[2], s0[1] + s0[3], s1[0] + s1[2], s1[1] + s1[3]};
+      }
+      // this lane's KB / 4 scores: keys key_lo + 8 (e / 2) + 2 t + e % 2
+      constexpr int NE = KB / 4;
+      float sc[NE];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int key = key0 + 2 * t + (e & 1) + ((e >> 1) << 3);
-          float s = sv[e];
-          if (a.cap_log2 != 0.f) s = a.cap_log2 * tanhf(s);
+      for (int j = 0; j < KB / 8; ++j) {
+        sc[2 * j] = s[j][0] + s[j][2];
+        sc[2 * j + 1] = s[j][1] + s[j][3];
+      }
+      if (a.cap_log2 != 0.f) {
+#pragma unroll
+        for (int e = 0; e < NE; ++e) sc[e] = a.cap_log2 * tanhf(sc[e]);
+      }
+      // keys past the chunk, after this row's position or before its window: masked
+      if (!(key_hi < k_end && key_hi <= limit && (!a.sliding || key_lo > limit - a.window))) {
+#pragma unroll
+        for (int e = 0; e < NE; ++e) {
+          const int key = key_lo + 8 * (e >> 1) + 2 * t + (e & 1);
           const bool vis = key < k_end && key <= limit && (!a.sliding || key > limit - a.window);
-          sv[e] = vis ? s : -INFINITY;
+          if (!vis) sc[e] = -INFINITY;
         }
-        float mloc = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
-        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
-        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
-        const float m_new = fmaxf(m, mloc);
-        const float m_use = m_new == -INFINITY ? 0.f : m_new;
-        const float corr = exp2f(m - m_use);
-        float p[4];
+      }
+      float mloc = sc[0];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) p[e] = exp2f(sv[e] - m_use);
-        l = l * corr + (p[0] + p[1]) + (p[2] + p[3]);
-        m = m_new;
+      for (int e = 1; e < NE; ++e) mloc = fmaxf(mloc, sc[e]);
+      mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
+      mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
+      const float m_new = fmaxf(m, mloc);
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
+      const float corr = ex2_approx(m - m_use);
+      m = m_new;
+      float psum = 0.f;
+#pragma unroll
+      for (int e = 0; e < NE; ++e) {
+        sc[e] = ex2_approx(sc[e] - m_use);
+        psum += sc[e];
+      }
+      l = l * corr + psum;
+      if (__any_sync(0xffffffffu, corr != 1.f)) {  // else every factor is exactly 1
 #pragma unroll
         for (int nt = 0; nt < Cfg::NTO; ++nt) {
           o[nt][0] *= corr;
@@ -429,25 +486,42 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
           o[nt][2] *= corr;
           o[nt][3] *= corr;
         }
+      }
+      // O += P V in 16-key steps; P (hi in rows g, lo in rows g + 8) is the A operand.
+      // Rows of the last stage past the chunk may hold any bits (a NaN times a zero
+      // weight is NaN): their V elements are zeroed in the fragments.
+      const bool tail = key_hi >= k_end;
+#pragma unroll
+      for (int kk = 0; kk < KB / 16; ++kk) {
         uint32_t PA[4];
         {
           __nv_bfloat16 h[4], lw[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) split_bf16(p[e], h[e], lw[e]);
+          for (int e = 0; e < 4; ++e) split_bf16(sc[4 * kk + e], h[e], lw[e]);
           PA[0] = pack_bf2(h[0], h[1]);
           PA[1] = pack_bf2(lw[0], lw[1]);
           PA[2] = pack_bf2(h[2], h[3]);
           PA[3] = pack_bf2(lw[2], lw[3]);
         }
+        const int kv0 = key_lo + kk * 16 + 2 * t;
+        const uint32_t mlo = (kv0 < k_end ? 0xffffu : 0u) | (kv0 + 1 < k_end ? 0xffff0000u : 0u);
+        const uint32_t mhi = (kv0 + 8 < k_end ? 0xffffu : 0u) | (kv0 + 9 < k_end ? 0xffff0000u : 0u);
 #pragma unroll
         for (int np = 0; np < Cfg::NTO / 2; ++np) {
-          const int mrow = krow + (((lane >> 3) & 1) << 3) + (lane & 7);
+          const int mrow = hb + kk * 16 + (((lane >> 3) & 1) << 3) + (lane & 7);
           const int mchunk = np * 2 + (lane >> 4);
           uint32_t b0, b1, b2, b3;
-          ldmatrix_x4_trans(vb + vswz<HD>(mrow, mchunk), b0, b1, b2, b3);
+          ldmatrix_x4_trans(vb0 + vswz<HD>(mrow, mchunk), b0, b1, b2, b3);
+          if (tail) {
+            b0 &= mlo;
+            b2 &= mlo;
+            b1 &= mhi;
+            b3 &= mhi;
+          }
           mma_bf16(o[2 * np], PA, b0, b1);
           mma_bf16(o[2 * np + 1], PA, b2, b3);
         }
+      }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
@@ -456,15 +530,11 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
     l += __shfl_xor_sync(0xffffffffu, l, 2);
     if (qvalid) {
       float* pr = part + (size_t)qrow * RS;
-      if (t == 0) {
-        pr[HD] = m;
-        pr[HD + 1] = l;
-      }
+      if (t == 0) *reinterpret_cast<float2*>(pr + HD) = make_float2(m, l);
 #pragma unroll
-      for (int nt = 0; nt < Cfg::NTO; ++nt) {
-        pr[nt * 8 + 2 * t] = o[nt][0] + o[nt][2];
-        pr[nt * 8 + 2 * t + 1] = o[nt][1] + o[nt][3];
-      }
+      for (int nt = 0; nt < Cfg::NTO; ++nt)
+        *reinterpret_cast<float2*>(pr + nt * 8 + 2 * t) =
+            make_float2(o[nt][0] + o[nt][2], o[nt][1] + o[nt][3]);
     }
   }
 
@@ -476,75 +546,111 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
       mbar_wait(&full[st], (last / NS) & 1, a.err);
     }
   }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_flags[2] = (atomicAdd(a.ticket + kvh, 1) == a.splits - 1);
-  __syncthreads();
-  if (!s_flags[2]) return;
-  __threadfence();
-  if (threadIdx.x == 0) a.ticket[kvh] = 0;
-  const float* up = a.part + (size_t)kvh * a.splits * 64 * RS;
-  float* wsm = reinterpret_cast<float*>(stages);  // [64 rows][splits]
-  const int nwarps = blockDim.x >> 5;
-  for (int r = warp; r < NQ; r += nwarps) {
-    float M = -INFINITY;
-    for (int sp = lane; sp < a.splits; sp += 32)
-      M = fmaxf(M, ld_cg_f32(up + ((size_t)sp * 64 + r) * RS + HD));
+}
+
+// Combination of the block attention's split records, one CTA per RPW = 256 / HD query
+// rows of one KV head (the lanes of a row own 8 output columns each):
+//   M = max_s m_s,  w_s = 2^(m_s - M),  o = sum_s w_s O_s / sum_s w_s l_s.
+// The (m, l) pairs go through shared memory; the four warps each sum a quarter of the
+// splits (their records loaded in the same round as the pairs) and the partial sums are
+// added in warp order, so the result does not depend on timing.  The output is written twice: f32 o, and the o_proj GEMM's activation operand.
+template <int HD>
+__global__ void __launch_bounds__(128) attn_verify_merge_kernel(const VAttnArgs a) {
+  constexpr int LPR = HD / 8;    // lanes per query row
+  constexpr int RPW = 32 / LPR;  // query rows per CTA
+  constexpr int RS = HD + 4;
+  __shared__ float4 s_acc[4][32][2];
+  extern __shared__ float2 s_ml[];  // [RPW][splits]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kvh = blockIdx.y;
+  const int NQ = a.L * a.G;
+  const int S = a.splits;
+  const int sub = lane / LPR, d8 = lane - sub * LPR;
+  const int r = blockIdx.x * RPW + sub;
+  const int rr = r < NQ ? r : NQ - 1;
+  const float* up = a.part + (size_t)kvh * S * 64 * RS;
+  pdl_wait();
+  pdl_launch_dependents();
+  // every load in one round: the (m, l) pairs into shared memory, and this warp's first
+  // MB records (splits warp, warp + 4, ...) into registers
+  constexpr int MB = 8;
+  for (int it = threadIdx.x; it < RPW * S; it += blockDim.x) {
+    const int row = it / S, sp = it - row * S;
+    const int qr = blockIdx.x * RPW + row < NQ ? blockIdx.x * RPW + row : NQ - 1;
+    s_ml[it] = __ldcg(reinterpret_cast<const float2*>(up + ((size_t)sp * 64 + qr) * RS + HD));
+  }
+  const float* base = up + (size_t)rr * RS + 8 * d8;
+  float4 v[2 * MB];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    const float Mu = M == -INFINITY ? 0.f : M;
-    float den = 0.f;
-    for (int sp = lane; sp < a.splits; sp += 32) {
-      const float* ps = up + ((size_t)sp * 64 + r) * RS;
-      const float f = exp2f(ld_cg_f32(ps + HD) - Mu);
-      wsm[r * a.splits + sp] = f;
-      den += f * ld_cg_f32(ps + HD + 1);
+  for (int j = 0; j < MB; ++j) {
+    const int sp = warp + 4 * j;
+    if (sp < S) {
+      const float4* src = reinterpret_cast<const float4*>(base + (size_t)sp * 64 * RS);
+      v[2 * j] = __ldcg(src);
+      v[2 * j + 1] = __ldcg(src + 1);
     }
-    den = warp_sum(den);
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-    __syncwarp();
-    for (int sp = lane; sp < a.splits; sp += 32) wsm[r * a.splits + sp] *= inv;
   }
   __syncthreads();
-  // one item = 8 consecutive output columns of one query row; chunks summed with
-  // independent 16-byte loads, four chunks at a time
-  constexpr int G8 = HD / 8;
-  for (int it = threadIdx.x; it < NQ * G8; it += blockDim.x) {
-    const int r = it / G8, d8 = it - r * G8;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    int sp = 0;
-    for (; sp + 4 <= a.splits; sp += 4) {
-      float4 v[8];
+  const float2* ml = s_ml + sub * S;
+  float M = -INFINITY;
+  for (int sp = d8; sp < S; sp += LPR) M = fmaxf(M, ml[sp].x);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float4* src =
-            reinterpret_cast<const float4*>(up + ((size_t)(sp + u) * 64 + r) * RS) + 2 * d8;
-        v[2 * u] = __ldcg(src);
-        v[2 * u + 1] = __ldcg(src + 1);
-      }
+  for (int off = LPR / 2; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  const float Mu = M == -INFINITY ? 0.f : M;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int sp0 = warp;; sp0 += 4 * MB) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float w = wsm[r * a.splits + sp + u];
-        acc[0] += w * v[2 * u].x; acc[1] += w * v[2 * u].y;
-        acc[2] += w * v[2 * u].z; acc[3] += w * v[2 * u].w;
-        acc[4] += w * v[2 * u + 1].x; acc[5] += w * v[2 * u + 1].y;
-        acc[6] += w * v[2 * u + 1].z; acc[7] += w * v[2 * u + 1].w;
+    for (int j = 0; j < MB; ++j) {
+      const int sp = sp0 + 4 * j;
+      if (sp < S) {
+        const float w = ex2_approx(ml[sp].x - Mu);
+        acc[0] += w * v[2 * j].x; acc[1] += w * v[2 * j].y;
+        acc[2] += w * v[2 * j].z; acc[3] += w * v[2 * j].w;
+        acc[4] += w * v[2 * j + 1].x; acc[5] += w * v[2 * j + 1].y;
+        acc[6] += w * v[2 * j + 1].z; acc[7] += w * v[2 * j + 1].w;
       }
     }
-    for (; sp < a.splits; ++sp) {
-      const float4* src = reinterpret_cast<const float4*>(up + ((size_t)sp * 64 + r) * RS) + 2 * d8;
-      const float4 v0 = __ldcg(src), v1 = __ldcg(src + 1);
-      const float w = wsm[r * a.splits + sp];
-      acc[0] += w * v0.x; acc[1] += w * v0.y; acc[2] += w * v0.z; acc[3] += w * v0.w;
-      acc[4] += w * v1.x; acc[5] += w * v1.y; acc[6] += w * v1.z; acc[7] += w * v1.w;
+    if (sp0 + 4 * MB >= S) break;
+#pragma unroll
+    for (int j = 0; j < MB; ++j) {  // more than 4 MB splits: the next batch
+      const int sp = sp0 + 4 * MB + 4 * j;
+      if (sp < S) {
+        const float4* src = reinterpret_cast<const float4*>(base + (size_t)sp * 64 * RS);
+        v[2 * j] = __ldcg(src);
+        v[2 * j + 1] = __ldcg(src + 1);
+      }
     }
-    const int tok = r / a.G, h = kvh * a.G + r % a.G;
-    float4* dst = reinterpret_cast<float4*>(a.o + ((size_t)tok * a.nh + h) * HD) + 2 * d8;
-    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-    // the same values as the o_proj GEMM's activation operand (column h * HD + 8 d8)
-    store_bop_group(a.bops, tok, (h * HD) / 8 + d8, acc);
   }
+  s_acc[warp][lane][0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  s_acc[warp][lane][1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  __syncthreads();
+  if (warp != 0) return;
+  float den = 0.f;
+  for (int q = d8; q < S; q += LPR) den += ex2_approx(ml[q].x - Mu) * ml[q].y;
+#pragma unroll
+  for (int off = LPR / 2; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  float out[8];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float4 t0 = s_acc[0][lane][h];
+#pragma unroll
+    for (int w = 1; w < 4; ++w) {
+      const float4 tw = s_acc[w][lane][h];
+      t0.x += tw.x; t0.y += tw.y; t0.z += tw.z; t0.w += tw.w;
+    }
+    out[4 * h] = t0.x * inv;
+    out[4 * h + 1] = t0.y * inv;
+    out[4 * h + 2] = t0.z * inv;
+    out[4 * h + 3] = t0.w * inv;
+  }
+  if (r >= NQ) return;
+  const int tok = r / a.G, h = kvh * a.G + r % a.G;
+  float4* dst = reinterpret_cast<float4*>(a.o + ((size_t)tok * a.nh + h) * HD) + 2 * d8;
+  dst[0] = make_float4(out[0], out[1], out[2], out[3]);
+  dst[1] = make_float4(out[4], out[5], out[6], out[7]);
+  // the same values as the o_proj GEMM's activation operand (column h * HD + 8 d8)
+  store_bop_group(a.bops, tok, (h * HD) / 8 + d8, out);
 }
 
 // Post-attention RMSNorm of the verify block, one CTA per token row: sum(y^2) in a fixed
@@ -574,12 +680,9 @@ __global__ void __launch_bounds__(256) post_norm_rows_kernel(const float* __rest
 
 // ------------------------------------------------------------------ host side
 struct VerifyState {
-  CUtensorMap tm_wqkv, tm_wo;
-  const void* tm_wqkv_ptr = nullptr;
   int* head_ticket = nullptr;   // [nh + 2 nkv]
   int* tile_ticket = nullptr;   // [H / 128]
-  int* attn_ticket = nullptr;   // [nkv]
-  float* part = nullptr;        // [max(SMs, nkv)][64][hd + 2]
+  float* part = nullptr;        // [max(SMs, nkv)][64][hd + 4]
   float* qkv_acc = nullptr;     // [16][rows_qkv]
   float* y_acc = nullptr;       // [16][H]
   float* y_post = nullptr;      // [16][H]: o_proj output kept for the post-attention norm
@@ -608,7 +711,6 @@ hfa_status verify_create(const hfa_layer_desc& d, int num_sms, VerifyState** out
   v->part_records = (size_t)(num_sms > nkv ? num_sms : nkv);
   cudaError_t e = cudaMalloc(&v->head_ticket, (d.num_heads + 2 * nkv) * sizeof(int));
   if (e == cudaSuccess) e = cudaMalloc(&v->tile_ticket, (d.hidden / kVM) * sizeof(int));
-  if (e == cudaSuccess) e = cudaMalloc(&v->attn_ticket, nkv * sizeof(int));
   if (e == cudaSuccess)
     e = cudaMalloc(&v->part, v->part_records * 64 * (d.head_dim + 4) * sizeof(float));
   if (e == cudaSuccess) e = cudaMalloc(&v->bq, (size_t)(d.hidden / kVK) * kBChunkBytes);
@@ -621,7 +723,6 @@ hfa_status verify_create(const hfa_layer_desc& d, int num_sms, VerifyState** out
   if (e == cudaSuccess) e = cudaMalloc(&v->y_post, (size_t)16 * d.hidden * sizeof(float));
   if (e == cudaSuccess) e = cudaMemset(v->head_ticket, 0, (d.num_heads + 2 * nkv) * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(v->tile_ticket, 0, (d.hidden / kVM) * sizeof(int));
-  if (e == cudaSuccess) e = cudaMemset(v->attn_ticket, 0, nkv * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(v->qkv_acc, 0, (size_t)16 * rows_qkv * sizeof(float));
   if (e == cudaSuccess) e = cudaMemset(v->y_acc, 0, (size_t)16 * d.hidden * sizeof(float));
   if (e != cudaSuccess) {
@@ -637,7 +738,6 @@ void verify_free(VerifyState* v) {
   if (!v) return;
   cudaFree(v->head_ticket);
   cudaFree(v->tile_ticket);
-  cudaFree(v->attn_ticket);
   cudaFree(v->part);
   cudaFree(v->qkv_acc);
   cudaFree(v->y_acc);
@@ -648,13 +748,13 @@ void verify_free(VerifyState* v) {
 }
 
 template <typename Kern, typename... Args>
-static cudaError_t launch_ex(Kern kern, int grid, int threads, size_t smem, bool pdl,
-                             cudaStream_t s, Args... args) {
+static cudaError_t launch_ex2(Kern kern, dim3 grid, int threads, size_t smem, bool pdl,
+                              cudaStream_t s, Args... args) {
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
+  cfg.gridDim = grid;
   cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -666,11 +766,15 @@ static cudaError_t launch_ex(Kern kern, int grid, int threads, size_t smem, bool
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+template <typename Kern, typename... Args>
+static cudaError_t launch_ex(Kern kern, int grid, int threads, size_t smem, bool pdl,
+                             cudaStream_t s, Args... args) {
+  return launch_ex2(kern, dim3(grid), threads, smem, pdl, s, args...);
+}
+
 static int gemm_splits(int tiles, int chunks, int num_sms) {
   int S = num_sms / tiles;
   if (S < 1) S = 1;
-  const int min_s = (chunks + kVMaxChunks - 1) / kVMaxChunks;
-  if (S < min_s) S = min_s;
   if (S > chunks) S = chunks;
   return S;
 }
@@ -688,14 +792,7 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
     snprintf(msg, n, "L * (num_heads / num_kv_heads) = %d > 64 query rows per KV head", c.L * G);
     return HFA_EUNSUPPORTED;
   }
-  if (v->tm_wqkv_ptr != c.wqkv) {
-    if (!encode_bf16_2d(&v->tm_wqkv, (void*)c.wqkv, H, rows_qkv, kVK, kVM) ||
-        !encode_bf16_2d(&v->tm_wo, (void*)c.wo, nh * hd, H, kVK, kVM)) {
-      snprintf(msg, n, "cannot describe the weights to the TMA unit");
-      return HFA_EINVAL;
-    }
-    v->tm_wqkv_ptr = c.wqkv;
-  }
+
   CUtensorMap tk, tv;
   if (hfa_encode_kv_map(&tk, c.k_cache, nkv * d.kv_capacity, hd, kVT) != HFA_OK ||
       hfa_encode_kv_map(&tv, c.v_cache, nkv * d.kv_capacity, hd, kVT) != HFA_OK) {
@@ -720,6 +817,7 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   // (1) QKV projection + per-head norms + RoPE + append of all L rows
   VGemmArgs qa{};
   qa.bops = v->bq;
+  qa.wt = reinterpret_cast<const uint8_t*>(c.wqkv);
   qa.g.batch = c.L;
   qa.g.x = c.x;
   qa.g.w_in = c.w_in;
@@ -752,8 +850,7 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   qa.splits = gemm_splits(qtiles, qa.chunks, c.num_sms);
   qa.need = qa.chunks * (hd > kVM ? hd / kVM : 1);
   tb("verify_qkv_gemm");
-  e = launch_ex(verify_gemm_kernel<kModeQKV>, qtiles * qa.splits, 128, kVGemmSmem, pdl, s,
-                v->tm_wqkv, qa);
+  e = launch_ex(verify_gemm_kernel<kModeQKV>, qtiles * qa.splits, 128, kVGemmSmem, pdl, s, qa);
   te();
   if (e != cudaSuccess) {
     snprintf(msg, n, "verify QKV launch: %s", cudaGetErrorString(e));
@@ -794,7 +891,6 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   aa.chunk = chunk;
   aa.part = v->part;
   aa.bops = v->bo;
-  aa.ticket = v->attn_ticket;
   aa.o = c.o_f32;
   aa.err = c.err;
   const int nq_warps = (c.L * G + 7) / 8;
@@ -813,10 +909,26 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
     snprintf(msg, n, "verify attention launch: %s", cudaGetErrorString(e));
     return HFA_ECUDA;
   }
+  // (2b) combination of the split records
+  const size_t msmem = (size_t)(256 / hd) * S * sizeof(float2);
+  const int mgrid = (c.L * G + 256 / hd - 1) / (256 / hd);
+  tb("verify_attn_merge");
+  if (hd == 64)
+    e = launch_ex2(attn_verify_merge_kernel<64>, dim3(mgrid, nkv), 128, msmem, pdl, s, aa);
+  else if (hd == 128)
+    e = launch_ex2(attn_verify_merge_kernel<128>, dim3(mgrid, nkv), 128, msmem, pdl, s, aa);
+  else
+    e = launch_ex2(attn_verify_merge_kernel<256>, dim3(mgrid, nkv), 128, msmem, pdl, s, aa);
+  te();
+  if (e != cudaSuccess) {
+    snprintf(msg, n, "verify attention merge launch: %s", cudaGetErrorString(e));
+    return HFA_ECUDA;
+  }
 
   // (3) o_proj + residual
   VGemmArgs oa{};
   oa.bops = v->bo;
+  oa.wt = reinterpret_cast<const uint8_t*>(c.wo);
   oa.g.batch = c.L;
   oa.g.x = c.x;
   oa.g.xin = c.o_f32;
@@ -834,8 +946,7 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   oa.splits = gemm_splits(otiles, oa.chunks, c.num_sms);
   oa.need = oa.chunks;
   tb("verify_oproj_gemm");
-  e = launch_ex(verify_gemm_kernel<kModeOProj>, otiles * oa.splits, 128, kVGemmSmem, pdl, s,
-                v->tm_wo, oa);
+  e = launch_ex(verify_gemm_kernel<kModeOProj>, otiles * oa.splits, 128, kVGemmSmem, pdl, s, oa);
   te();
   if (e != cudaSuccess) {
     snprintf(msg, n, "verify o_proj launch: %s", cudaGetErrorString(e));
