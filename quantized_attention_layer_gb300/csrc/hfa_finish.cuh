@@ -2,7 +2,6 @@
 // projection is complete: per-head RMSNorm, NeoX RoPE and the bf16 KV append
 // (gemma4/gpu_full_attn.rs, encode_one_layer: fused per-head norm + RoPE, GPU V norm,
 // dense KV copy), and the residual add (dflash/forward.rs, dispatch_dflash_residual_add).
-// Shared by the decode GEMV and the verify-block GEMM.
 #pragma once
 #include "hfa_common.cuh"
 #include "hfa_internal.h"
@@ -24,6 +23,7 @@ __device__ __forceinline__ void rope_cs(int P, float2 gpair, float& c, float& s)
 
 // Epilogue of one token row b of one attention head (QKV mode): v holds rows
 // [hh*hd, hh*hd + hd) of the QKV output for that token, lane + 32 j in v[j].
+// Used by the verify-block GEMM once the k-split partial sums are added.
 template <int HD>
 static __device__ __forceinline__ void finish_head_row(const GemvArgs& a, int hh, int b, float (&v)[HD / 32],
                                        int lane) {
@@ -91,72 +91,19 @@ static __device__ __forceinline__ void finish_head_row(const GemvArgs& a, int hh
   }
 }
 
-// Epilogue of one attention head (QKV mode) for the token rows b0, b0 + bstep, ...: the
-// accumulators of four such rows are loaded together (and zeroed for the next call),
-// then each row is finished.
-template <int HD>
-static __device__ void finish_head(const GemvArgs& a, int hh, int lane, int b0, int bstep) {
-  constexpr int J = HD / 32;
-  constexpr int TB = 4;
-  const int R16 = a.R * 16;
-  for (int bb = b0; bb < a.batch; bb += TB * bstep) {
-    float v[TB][J];
-#pragma unroll
-    for (int u = 0; u < TB; ++u) {
-      const int b = bb + u * bstep;
-#pragma unroll
-      for (int j = 0; j < J; ++j)
-        v[u][j] = b < a.batch
-                      ? ld_cg_f32(a.acc + (size_t)b * R16 + (size_t)hh * HD + lane + 32 * j)
-                      : 0.f;
-    }
-#pragma unroll
-    for (int u = 0; u < TB; ++u) {
-      const int b = bb + u * bstep;
-      if (b >= a.batch) break;
-#pragma unroll
-      for (int j = 0; j < J; ++j) a.acc[(size_t)b * R16 + (size_t)hh * HD + lane + 32 * j] = 0.f;
-      finish_head_row<HD>(a, hh, b, v[u], lane);
-    }
+// Epilogue of one output (o_proj mode): token row b, output feature `row`, projection
+// value y: out = bf16(x + y), or y kept in y_post for the post-attention norm pass (which
+// needs the whole row's mean of y^2 first).
+static __device__ __forceinline__ void finish_row_item(const GemvArgs& a, int b, int row,
+                                                       float y) {
+  const size_t off = (size_t)b * a.R * 16 + row;
+  if (a.y_post) {
+    a.y_post[off] = y;
+    return;
   }
-}
-
-// Epilogue of output rows [row0, row0 + nrows) for every token (o_proj mode), items
-// spread over nthr threads with sixteen accumulator loads in flight per thread:
-// out = bf16(x + y), or y kept in y_post for the post-attention norm pass (which needs
-// the whole row's mean of y^2 first).
-static __device__ void finish_rows(const GemvArgs& a, int row0, int nrows, int tid, int nthr) {
-  constexpr int U = 16;
-  const int R16 = a.R * 16;
-  const int n = nrows * a.batch;
-  for (int i0 = tid; i0 < n; i0 += U * nthr) {
-    float y[U], xv[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int i = i0 + u * nthr;
-      y[u] = xv[u] = 0.f;
-      if (i < n) {
-        const int b = i / nrows, row = row0 + i - b * nrows;
-        y[u] = ld_cg_f32(a.acc + (size_t)b * R16 + row);
-        if (!a.y_post) xv[u] = __bfloat162float(a.x[(size_t)b * R16 + row]);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int i = i0 + u * nthr;
-      if (i >= n) break;
-      const int b = i / nrows, row = row0 + i - b * nrows;
-      const size_t off = (size_t)b * R16 + row;
-      a.acc[off] = 0.0f;
-      if (a.y_post) {  // the post-attention norm pass writes the output
-        a.y_post[off] = y[u];
-        continue;
-      }
-      const float o = xv[u] + y[u];
-      a.out[off] = __float2bfloat16_rn(o);
-      if (a.out_tap) a.out_tap[off] = o;
-    }
-  }
+  const float o = __bfloat162float(a.x[off]) + y;
+  a.out[off] = __float2bfloat16_rn(o);
+  if (a.out_tap) a.out_tap[off] = o;
 }
 
 }  // namespace hfa

@@ -25,8 +25,6 @@ struct GemvArgs {
   const float* w_in;       // QKV: input RMSNorm weight [cols]
   const float* xin;        // OPROJ: attention output f32 [B, cols]
   float eps;
-  float* acc;              // f32 [B, R*16], zero between launches
-  int* ticket;             // QKV: per head; OPROJ: per row group
   unsigned* err;
   // QKV finisher
   int nh, nkv, hd, C, ring;

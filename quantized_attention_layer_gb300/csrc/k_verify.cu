@@ -22,6 +22,7 @@
 //    writes one (O, m, l) record per query row.
 //  * attn_verify_merge_kernel: the records of a KV head's chunks combined, a few query
 //    rows per CTA, into the f32 output and the o_proj activation operand.
+#include <cooperative_groups.h>
 #include <stdio.h>
 
 #include "hfa_common.cuh"
@@ -64,14 +65,14 @@ constexpr int kVStageBytes = kAStageBytes + kBChunkBytes;
 constexpr size_t kVGemmSmem = 1024 + (size_t)kVStages * kVStageBytes + 256;
 
 struct VGemmArgs {
-  GemvArgs g;        // epilogue arguments (accumulator, tickets, norms, caches, ...)
+  GemvArgs g;        // epilogue arguments (norms, RoPE, caches, residual, ...)
   const uint8_t* wt;    // weights as 16 KB tiles [rows / 128][K / 64] (launch_repack_bf16_tiles)
   const uint8_t* bops;  // activation operand, [K / 64 chunks][32 rows][128 B], swizzled
   int rows;          // output features
   int K;             // input features
   int chunks;        // K / 64
   int splits;        // k-splits per row tile
-  int need;          // chunk contributions that complete a head (QKV) / row tile (o_proj)
+  int tpc;           // row tiles per cluster: hd / 128 for QKV heads wider than a tile, else 1
 };
 
 // Activation operand of the verify GEMMs, built once per call: row t of the block
@@ -141,7 +142,6 @@ __global__ void __launch_bounds__(128, 1) verify_gemm_kernel(const VGemmArgs a) 
   uint64_t* empty = full + kVStages;
   uint64_t* done = empty + kVStages;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(done + 1);
-  int* s_fin = reinterpret_cast<int*>(s_tmem + 1);      // [0..3] finished heads, [4] count
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = blockIdx.x / a.splits, sp = blockIdx.x - mt * a.splits;
   const int c0 = a.chunks * sp / a.splits, c1 = a.chunks * (sp + 1) / a.splits;
@@ -180,13 +180,16 @@ __global__ void __launch_bounds__(128, 1) verify_gemm_kernel(const VGemmArgs a) 
     }
   }
   if (warp == 2) {
-    // the lines the epilogue reads (the accumulator rows of this tile, and the residual
-    // in o_proj mode) into L2, where the weight stream would otherwise have left them cold
-    const int R16 = a.g.R * 16;
-    for (int q = lane; q < 4 * L; q += 32) {
-      const int t = q >> 2, part = q & 3;
-      prefetch_l2(a.g.acc + (size_t)t * R16 + m0 + part * 32);
-      if (MODE == kModeOProj) prefetch_l2(a.g.x + (size_t)t * R16 + m0 + part * 32);
+    // the lines the epilogue reads (the residual in o_proj mode, the norm weights and
+    // RoPE table in QKV mode) into L2, where the weight stream would have left them cold
+    if (MODE == kModeOProj) {
+      const int R16 = a.g.R * 16;
+      for (int q = lane; q < 4 * L; q += 32)
+        prefetch_l2(a.g.x + (size_t)(q >> 2) * R16 + m0 + (q & 3) * 32);
+    } else if (lane < 3) {  // each of the three is hd * 4 bytes
+      const void* p = lane == 0 ? (const void*)a.g.w_q : lane == 1 ? (const void*)a.g.w_k
+                                                                   : (const void*)a.g.rope_g;
+      prefetch_bulk_l2(p, (uint32_t)a.g.hd * 4u);
     }
   }
   pdl_wait();
@@ -226,52 +229,91 @@ __global__ void __launch_bounds__(128, 1) verify_gemm_kernel(const VGemmArgs a) 
     tc_commit(done);
   }
   __syncwarp();
-  // ---- epilogue: accumulator rows 32w..32w+31, columns 0..15 hi, 16..31 lo
+  // ---- epilogue: accumulator rows 32w..32w+31, columns 0..15 hi, 16..31 lo.  The CTA's
+  // partial sums go to its own shared memory (the ring is drained: every copy has been
+  // consumed by the MMAs that `done` waited for) as [16 tokens][128 rows] f32.
   const bool ok = mbar_wait(done, 0, a.g.err);
   tc_fence_after();
-  if (ok) {
+  float* psum = reinterpret_cast<float*>(ring);
+  {
     float hi[16], lo[16];
-    const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16);
-    tmem_ld_32x32b_x16(taddr, hi);
-    tmem_ld_32x32b_x16(taddr + 16, lo);
-    const int row = m0 + 32 * warp + lane;
-    const int R16 = a.g.R * 16;
+    if (ok) {
+      const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16);
+      tmem_ld_32x32b_x16(taddr, hi);
+      tmem_ld_32x32b_x16(taddr + 16, lo);
+    }
 #pragma unroll
-    for (int t = 0; t < 16; ++t)
-      if (t < L) red_add_f32(a.g.acc + (size_t)t * R16 + row, hi[t] + lo[t]);
+    for (int t = 0; t < 16; ++t) psum[t * kVM + 32 * warp + lane] = ok ? hi[t] + lo[t] : 0.f;
   }
   tc_fence_before();
-  __threadfence();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, kVN);
 
-  // ---- completion tickets and epilogues
-  if (threadIdx.x == 0) {
-    int nf = 0;
-    if (MODE == kModeQKV) {
-      const int h0 = m0 / a.g.hd, h1 = (m0 + kVM - 1) / a.g.hd;
-      for (int h = h0; h <= h1 && nf < 4; ++h)
-        if (atomicAdd(a.g.ticket + h, nch) + nch == a.need) s_fin[nf++] = h;
-    } else {
-      if (atomicAdd(a.g.ticket + mt, nch) + nch == a.need) s_fin[nf++] = mt;
-    }
-    for (int i = 0; i < nf; ++i) a.g.ticket[s_fin[i]] = 0;
-    s_fin[4] = nf;
-  }
-  __syncthreads();
-  const int nf = s_fin[4];
-  if (nf == 0) return;
-  __threadfence();
+  // ---- k-split reduction through distributed shared memory: the cluster is the
+  // a.splits CTAs of a.tpc consecutive row tiles (rank = tile-in-cluster * splits + split).
+  // Each output is summed over the splits in rank order, so the result does not depend
+  // on timing.
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  cluster.sync();  // every CTA's partial sums are visible
+  const int S = a.splits;
+  const int rank = (int)cluster.block_rank(), cs = S * a.tpc;
   if (MODE == kModeQKV) {
-    // every warp takes the token rows warp, warp + 4, ... of each completed head
-    for (int f = 0; f < nf; ++f) {
-      if (a.g.hd == 64) finish_head<64>(a.g, s_fin[f], lane, warp, 4);
-      else if (a.g.hd == 128) finish_head<128>(a.g, s_fin[f], lane, warp, 4);
-      else finish_head<256>(a.g, s_fin[f], lane, warp, 4);
+    // items (head, token) of the cluster's rows, one warp each
+    const int hd = a.g.hd;
+    const int tile0 = m0 / kVM - (rank / S);  // first row tile of the cluster
+    const int rows0 = tile0 * kVM;
+    const int nheads = a.tpc * kVM / hd;
+    const int nitems = nheads * L;
+    for (int it = rank * 4 + warp; it < nitems; it += cs * 4) {
+      const int hl = it / L, t = it - hl * L;
+      const int hh = rows0 / hd + hl;
+      if (hd == 64) {
+        float v[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int r = hl * 64 + lane + 32 * j;  // row within the cluster's rows
+          float acc = 0.f;
+          for (int c = 0; c < S; ++c)
+            acc += cluster.map_shared_rank(psum, (r >> 7) * S + c)[t * kVM + (r & 127)];
+          v[j] = acc;
+        }
+        finish_head_row<64>(a.g, hh, t, v, lane);
+      } else if (hd == 128) {
+        float v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = hl * 128 + lane + 32 * j;
+          float acc = 0.f;
+          for (int c = 0; c < S; ++c)
+            acc += cluster.map_shared_rank(psum, (r >> 7) * S + c)[t * kVM + (r & 127)];
+          v[j] = acc;
+        }
+        finish_head_row<128>(a.g, hh, t, v, lane);
+      } else {
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int r = hl * 256 + lane + 32 * j;
+          float acc = 0.f;
+          for (int c = 0; c < S; ++c)
+            acc += cluster.map_shared_rank(psum, (r >> 7) * S + c)[t * kVM + (r & 127)];
+          v[j] = acc;
+        }
+        finish_head_row<256>(a.g, hh, t, v, lane);
+      }
     }
   } else {
-    finish_rows(a.g, m0, kVM, threadIdx.x, blockDim.x);
+    // items (token, row) of the tile, a contiguous range per rank
+    const int n = L * kVM;
+    const int i0 = n * rank / S, i1 = n * (rank + 1) / S;
+    for (int i = i0 + (int)threadIdx.x; i < i1; i += blockDim.x) {
+      float y = 0.f;
+      for (int c = 0; c < S; ++c) y += cluster.map_shared_rank(psum, c)[i];
+      finish_row_item(a.g, i >> 7, m0 + (i & 127), y);
+    }
   }
+  cluster.sync();  // no CTA leaves while another still reads its shared memory
 }
 
 // ------------------------------------------------------------------ block attention
@@ -680,15 +722,12 @@ __global__ void __launch_bounds__(256) post_norm_rows_kernel(const float* __rest
 
 // ------------------------------------------------------------------ host side
 struct VerifyState {
-  int* head_ticket = nullptr;   // [nh + 2 nkv]
-  int* tile_ticket = nullptr;   // [H / 128]
   float* part = nullptr;        // [max(SMs, nkv)][64][hd + 4]
-  float* qkv_acc = nullptr;     // [16][rows_qkv]
-  float* y_acc = nullptr;       // [16][H]
   float* y_post = nullptr;      // [16][H]: o_proj output kept for the post-attention norm
   uint8_t* bq = nullptr;        // QKV activation operand [H / 64][32][128 B]
   uint8_t* bo = nullptr;        // o_proj activation operand [nh hd / 64][32][128 B]
   size_t part_records = 0;
+  int max_clusters[9] = {};     // co-resident GEMM clusters of n CTAs (index n)
 };
 
 static char g_verify_error[256];
@@ -709,26 +748,42 @@ hfa_status verify_create(const hfa_layer_desc& d, int num_sms, VerifyState** out
   VerifyState* v = new VerifyState();
   const int nkv = d.num_kv_heads;
   v->part_records = (size_t)(num_sms > nkv ? num_sms : nkv);
-  cudaError_t e = cudaMalloc(&v->head_ticket, (d.num_heads + 2 * nkv) * sizeof(int));
-  if (e == cudaSuccess) e = cudaMalloc(&v->tile_ticket, (d.hidden / kVM) * sizeof(int));
-  if (e == cudaSuccess)
-    e = cudaMalloc(&v->part, v->part_records * 64 * (d.head_dim + 4) * sizeof(float));
+  cudaError_t e = cudaMalloc(&v->part, v->part_records * 64 * (d.head_dim + 4) * sizeof(float));
   if (e == cudaSuccess) e = cudaMalloc(&v->bq, (size_t)(d.hidden / kVK) * kBChunkBytes);
   if (e == cudaSuccess)
     e = cudaMalloc(&v->bo, (size_t)(d.num_heads * d.head_dim / kVK) * kBChunkBytes);
   if (e == cudaSuccess)
     e = cudaMemset(v->bo, 0, (size_t)(d.num_heads * d.head_dim / kVK) * kBChunkBytes);
-  if (e == cudaSuccess) e = cudaMalloc(&v->qkv_acc, (size_t)16 * rows_qkv * sizeof(float));
-  if (e == cudaSuccess) e = cudaMalloc(&v->y_acc, (size_t)16 * d.hidden * sizeof(float));
   if (e == cudaSuccess) e = cudaMalloc(&v->y_post, (size_t)16 * d.hidden * sizeof(float));
-  if (e == cudaSuccess) e = cudaMemset(v->head_ticket, 0, (d.num_heads + 2 * nkv) * sizeof(int));
-  if (e == cudaSuccess) e = cudaMemset(v->tile_ticket, 0, (d.hidden / kVM) * sizeof(int));
-  if (e == cudaSuccess) e = cudaMemset(v->qkv_acc, 0, (size_t)16 * rows_qkv * sizeof(float));
-  if (e == cudaSuccess) e = cudaMemset(v->y_acc, 0, (size_t)16 * d.hidden * sizeof(float));
   if (e != cudaSuccess) {
     snprintf(g_verify_error, sizeof g_verify_error, "%s", cudaGetErrorString(e));
     verify_free(v);
     return HFA_ENOMEM;
+  }
+  // how many GEMM clusters of each size fit on the GPU at once (GPCs hold different
+  // numbers of SMs, so this is not num_sms / n)
+  e = cudaFuncSetAttribute(verify_gemm_kernel<kModeQKV>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kVGemmSmem);
+  v->max_clusters[1] = num_sms;
+  for (int n = 2; n <= 8 && e == cudaSuccess; ++n) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = kVGemmSmem;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)n;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    e = cudaOccupancyMaxActiveClusters(&v->max_clusters[n], verify_gemm_kernel<kModeQKV>, &cfg);
+  }
+  if (e != cudaSuccess) {
+    snprintf(g_verify_error, sizeof g_verify_error, "cluster occupancy: %s",
+             cudaGetErrorString(e));
+    verify_free(v);
+    return HFA_ECUDA;
   }
   *out = v;
   return HFA_OK;
@@ -736,11 +791,7 @@ hfa_status verify_create(const hfa_layer_desc& d, int num_sms, VerifyState** out
 
 void verify_free(VerifyState* v) {
   if (!v) return;
-  cudaFree(v->head_ticket);
-  cudaFree(v->tile_ticket);
   cudaFree(v->part);
-  cudaFree(v->qkv_acc);
-  cudaFree(v->y_acc);
   cudaFree(v->y_post);
   cudaFree(v->bq);
   cudaFree(v->bo);
@@ -749,7 +800,7 @@ void verify_free(VerifyState* v) {
 
 template <typename Kern, typename... Args>
 static cudaError_t launch_ex2(Kern kern, dim3 grid, int threads, size_t smem, bool pdl,
-                              cudaStream_t s, Args... args) {
+                              cudaStream_t s, int cluster, Args... args) {
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -758,24 +809,38 @@ static cudaError_t launch_ex2(Kern kern, dim3 grid, int threads, size_t smem, bo
   cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na++].val.programmaticStreamSerializationAllowed = 1;
+  }
+  if (cluster > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = (unsigned)cluster;
+    attr[na].val.clusterDim.y = 1;
+    attr[na++].val.clusterDim.z = 1;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 template <typename Kern, typename... Args>
 static cudaError_t launch_ex(Kern kern, int grid, int threads, size_t smem, bool pdl,
                              cudaStream_t s, Args... args) {
-  return launch_ex2(kern, dim3(grid), threads, smem, pdl, s, args...);
+  return launch_ex2(kern, dim3(grid), threads, smem, pdl, s, 1, args...);
 }
 
-static int gemm_splits(int tiles, int chunks, int num_sms) {
+// k-splits per row tile: the SMs shared out over the tiles, with every cluster of
+// tpc tiles x splits CTAs (at most 8, reducing through distributed shared memory)
+// resident at once -- max_clusters[n] is how many clusters of n CTAs the GPU holds.
+static int gemm_splits(int tiles, int chunks, int num_sms, int tpc, const int* max_clusters) {
   int S = num_sms / tiles;
-  if (S < 1) S = 1;
+  if (S > 8 / tpc) S = 8 / tpc;
   if (S > chunks) S = chunks;
+  while (S > 1 && tiles / tpc > max_clusters[S * tpc]) --S;
+  if (S < 1) S = 1;
   return S;
 }
 
@@ -823,8 +888,6 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   qa.g.w_in = c.w_in;
   qa.g.eps = d.eps;
   qa.g.R = rows_qkv / 16;
-  qa.g.acc = v->qkv_acc;
-  qa.g.ticket = v->head_ticket;
   qa.g.err = c.err;
   qa.g.nh = nh;
   qa.g.nkv = nkv;
@@ -847,10 +910,11 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   qa.K = H;
   qa.chunks = H / kVK;
   const int qtiles = rows_qkv / kVM;
-  qa.splits = gemm_splits(qtiles, qa.chunks, c.num_sms);
-  qa.need = qa.chunks * (hd > kVM ? hd / kVM : 1);
+  qa.tpc = hd > kVM ? hd / kVM : 1;
+  qa.splits = gemm_splits(qtiles, qa.chunks, c.num_sms, qa.tpc, v->max_clusters);
   tb("verify_qkv_gemm");
-  e = launch_ex(verify_gemm_kernel<kModeQKV>, qtiles * qa.splits, 128, kVGemmSmem, pdl, s, qa);
+  e = launch_ex2(verify_gemm_kernel<kModeQKV>, dim3(qtiles * qa.splits), 128, kVGemmSmem, pdl, s,
+                 qa.splits * qa.tpc, qa);
   te();
   if (e != cudaSuccess) {
     snprintf(msg, n, "verify QKV launch: %s", cudaGetErrorString(e));
@@ -914,11 +978,11 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   const int mgrid = (c.L * G + 256 / hd - 1) / (256 / hd);
   tb("verify_attn_merge");
   if (hd == 64)
-    e = launch_ex2(attn_verify_merge_kernel<64>, dim3(mgrid, nkv), 128, msmem, pdl, s, aa);
+    e = launch_ex2(attn_verify_merge_kernel<64>, dim3(mgrid, nkv), 128, msmem, pdl, s, 1, aa);
   else if (hd == 128)
-    e = launch_ex2(attn_verify_merge_kernel<128>, dim3(mgrid, nkv), 128, msmem, pdl, s, aa);
+    e = launch_ex2(attn_verify_merge_kernel<128>, dim3(mgrid, nkv), 128, msmem, pdl, s, 1, aa);
   else
-    e = launch_ex2(attn_verify_merge_kernel<256>, dim3(mgrid, nkv), 128, msmem, pdl, s, aa);
+    e = launch_ex2(attn_verify_merge_kernel<256>, dim3(mgrid, nkv), 128, msmem, pdl, s, 1, aa);
   te();
   if (e != cudaSuccess) {
     snprintf(msg, n, "verify attention merge launch: %s", cudaGetErrorString(e));
@@ -933,8 +997,6 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   oa.g.x = c.x;
   oa.g.xin = c.o_f32;
   oa.g.R = H / 16;
-  oa.g.acc = v->y_acc;
-  oa.g.ticket = v->tile_ticket;
   oa.g.err = c.err;
   oa.g.out = c.out;
   oa.g.out_tap = c.out_tap;
@@ -943,10 +1005,11 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   oa.K = nh * hd;
   oa.chunks = oa.K / kVK;
   const int otiles = H / kVM;
-  oa.splits = gemm_splits(otiles, oa.chunks, c.num_sms);
-  oa.need = oa.chunks;
+  oa.tpc = 1;
+  oa.splits = gemm_splits(otiles, oa.chunks, c.num_sms, 1, v->max_clusters);
   tb("verify_oproj_gemm");
-  e = launch_ex(verify_gemm_kernel<kModeOProj>, otiles * oa.splits, 128, kVGemmSmem, pdl, s, oa);
+  e = launch_ex2(verify_gemm_kernel<kModeOProj>, dim3(otiles * oa.splits), 128, kVGemmSmem, pdl,
+                 s, oa.splits, oa);
   te();
   if (e != cudaSuccess) {
     snprintf(msg, n, "verify o_proj launch: %s", cudaGetErrorString(e));
