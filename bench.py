@@ -464,7 +464,8 @@ def run_verify(args, rank, world, w):
             "step_bytes": step_bytes,
             "roofline": {"bound": "hbm", "kernel": "verify_qkv_gemm", "achieved": wqkv_bytes / (g_us * 1e-6) / 1e9,
                          "peak": peak, "unit": "GB/s", "frac": wqkv_bytes / (g_us * 1e-6) / 1e9 / peak,
-                         "traffic": None, "useful_tflops": flops / (g_us * 1e-6) / 1e12,
+                         "traffic": ncu_traffic("k_verify.cu", f"verify_block_{w.name}.md"),
+                         "useful_tflops": flops / (g_us * 1e-6) / 1e12,
                          "peak_source": src},
             "kernels": {k: {"avg_us": v[0] / max(v[1], 1) * 1e3, "launches": v[1]} for k, v in kt.items()},
             "clocks": clk.summary(), "gpu_launches": sum(v[1] for v in kt.values())}

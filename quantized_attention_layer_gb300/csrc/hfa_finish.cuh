@@ -55,7 +55,7 @@ static __device__ __forceinline__ void finish_head_row(const GemvArgs& a, int hh
     const float* w = kind == 0 ? a.w_q : a.w_k;  // a valid address for v too (unused)
 #pragma unroll
     for (int j = 0; j < J; ++j) {
-      const float wj = __ldg(w + lane + 32 * j);
+      const float wj = w[lane + 32 * j];
       v[j] *= inv * (kind < 2 ? wj : 1.0f);
     }
   }

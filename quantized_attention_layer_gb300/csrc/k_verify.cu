@@ -62,7 +62,8 @@ constexpr int kVStages = 10;     // ring depth: 200 KB of copies in flight per S
 constexpr int kAStageBytes = kVM * kVK * 2;  // 16 KB weight tile
 constexpr int kBChunkBytes = kVN * kVK * 2;  // 4 KB activation chunk
 constexpr int kVStageBytes = kAStageBytes + kBChunkBytes;
-constexpr size_t kVGemmSmem = 1024 + (size_t)kVStages * kVStageBytes + 256;
+constexpr int kVTableBytes = 3 * 256 * 4;  // QKV epilogue: w_q, w_k, RoPE table (hd <= 256)
+constexpr size_t kVGemmSmem = 1024 + (size_t)kVStages * kVStageBytes + 256 + kVTableBytes;
 
 struct VGemmArgs {
   GemvArgs g;        // epilogue arguments (norms, RoPE, caches, residual, ...)
@@ -142,6 +143,7 @@ __global__ void __launch_bounds__(128, 1) verify_gemm_kernel(const VGemmArgs a) 
   uint64_t* empty = full + kVStages;
   uint64_t* done = empty + kVStages;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(done + 1);
+  float* s_tab = reinterpret_cast<float*>(ring + kVStages * kVStageBytes + 256);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = blockIdx.x / a.splits, sp = blockIdx.x - mt * a.splits;
   const int c0 = a.chunks * sp / a.splits, c1 = a.chunks * (sp + 1) / a.splits;
@@ -186,10 +188,17 @@ __global__ void __launch_bounds__(128, 1) verify_gemm_kernel(const VGemmArgs a) 
       const int R16 = a.g.R * 16;
       for (int q = lane; q < 4 * L; q += 32)
         prefetch_l2(a.g.x + (size_t)(q >> 2) * R16 + m0 + (q & 3) * 32);
-    } else if (lane < 3) {  // each of the three is hd * 4 bytes
-      const void* p = lane == 0 ? (const void*)a.g.w_q : lane == 1 ? (const void*)a.g.w_k
-                                                                   : (const void*)a.g.rope_g;
-      prefetch_bulk_l2(p, (uint32_t)a.g.hd * 4u);
+    } else {
+      // the epilogue's tables into shared memory: w_q, w_k (hd floats each), then the
+      // RoPE table (hd / 2 float2); written by this warp, read after the __syncthreads
+      // that precedes the epilogue
+      const int hd = a.g.hd;
+      const float* rg = reinterpret_cast<const float*>(a.g.rope_g);
+      for (int i = lane; i < hd; i += 32) {
+        s_tab[i] = a.g.w_q[i];
+        s_tab[hd + i] = a.g.w_k[i];
+        s_tab[2 * hd + i] = rg[i];
+      }
     }
   }
   pdl_wait();
@@ -255,6 +264,12 @@ __global__ void __launch_bounds__(128, 1) verify_gemm_kernel(const VGemmArgs a) 
   // on timing.
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
+  GemvArgs g = a.g;
+  if (MODE == kModeQKV) {
+    g.w_q = s_tab;
+    g.w_k = s_tab + a.g.hd;
+    g.rope_g = reinterpret_cast<const float2*>(s_tab + 2 * a.g.hd);
+  }
   cluster.sync();  // every CTA's partial sums are visible
   const int S = a.splits;
   const int rank = (int)cluster.block_rank(), cs = S * a.tpc;
@@ -278,7 +293,7 @@ __global__ void __launch_bounds__(128, 1) verify_gemm_kernel(const VGemmArgs a) 
             acc += cluster.map_shared_rank(psum, (r >> 7) * S + c)[t * kVM + (r & 127)];
           v[j] = acc;
         }
-        finish_head_row<64>(a.g, hh, t, v, lane);
+        finish_head_row<64>(g, hh, t, v, lane);
       } else if (hd == 128) {
         float v[4];
 #pragma unroll
@@ -289,7 +304,7 @@ __global__ void __launch_bounds__(128, 1) verify_gemm_kernel(const VGemmArgs a) 
             acc += cluster.map_shared_rank(psum, (r >> 7) * S + c)[t * kVM + (r & 127)];
           v[j] = acc;
         }
-        finish_head_row<128>(a.g, hh, t, v, lane);
+        finish_head_row<128>(g, hh, t, v, lane);
       } else {
         float v[8];
 #pragma unroll
@@ -300,7 +315,7 @@ __global__ void __launch_bounds__(128, 1) verify_gemm_kernel(const VGemmArgs a) 
             acc += cluster.map_shared_rank(psum, (r >> 7) * S + c)[t * kVM + (r & 127)];
           v[j] = acc;
         }
-        finish_head_row<256>(a.g, hh, t, v, lane);
+        finish_head_row<256>(g, hh, t, v, lane);
       }
     }
   } else {
@@ -310,7 +325,7 @@ __global__ void __launch_bounds__(128, 1) verify_gemm_kernel(const VGemmArgs a) 
     for (int i = i0 + (int)threadIdx.x; i < i1; i += blockDim.x) {
       float y = 0.f;
       for (int c = 0; c < S; ++c) y += cluster.map_shared_rank(psum, c)[i];
-      finish_row_item(a.g, i >> 7, m0 + (i & 127), y);
+      finish_row_item(g, i >> 7, m0 + (i & 127), y);
     }
   }
   cluster.sync();  // no CTA leaves while another still reads its shared memory
@@ -615,7 +630,7 @@ __global__ void __launch_bounds__(128) attn_verify_merge_kernel(const VAttnArgs 
   pdl_launch_dependents();
   // every load in one round: the (m, l) pairs into shared memory, and this warp's first
   // MB records (splits warp, warp + 4, ...) into registers
-  constexpr int MB = 8;
+  constexpr int MB = 12;
   for (int it = threadIdx.x; it < RPW * S; it += blockDim.x) {
     const int row = it / S, sp = it - row * S;
     const int qr = blockIdx.x * RPW + row < NQ ? blockIdx.x * RPW + row : NQ - 1;
