@@ -66,3 +66,20 @@ def test_verify_block_gemma_variants(k_eq_v, ff, post):
                     rope_theta=1e6, seed=97, weights_bf16=True, verify_len=16, base_pos=0,
                     k_eq_v=k_eq_v, rope_freq_factors=ff, post_norm=post)
     _case(w, 13, 400)
+
+
+def test_verify_block_hd256_cluster_across_row_tiles():
+    # a 256-wide head spans two 128-row GEMM tiles: the k-split cluster holds both tiles'
+    # splits, and the head epilogue adds rows from either tile's CTAs
+    w = wl.Workload(name="ver256", hidden=1024, num_heads=8, num_kv_heads=2, head_dim=256,
+                    layer_type=wl.FULL, window=0, kv_capacity=600, ring=False, batch=1,
+                    rope_theta=1e6, seed=98, weights_bf16=True, verify_len=16, base_pos=0)
+    _case(w, 16, 500)
+
+
+def test_verify_block_sliding_hd256_softcap_short_block():
+    w = wl.Workload(name="ver256s", hidden=512, num_heads=4, num_kv_heads=1, head_dim=256,
+                    layer_type=wl.SLIDING, window=200, kv_capacity=900, ring=False, batch=1,
+                    rope_theta=1e4, seed=99, weights_bf16=True, verify_len=16, base_pos=0,
+                    softcap=30.0)
+    _case(w, 7, 850)
