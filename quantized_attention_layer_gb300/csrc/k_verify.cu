@@ -356,11 +356,6 @@ struct VACfg {
   static constexpr size_t SMEM = 1024 + (size_t)NS * STAGE + 8 * KS * 32 * 16 + 256;
 };
 
-template <int HD>
-__device__ __forceinline__ uint32_t vswz(int row, int chunk) {
-  const int box = chunk >> 3, c = chunk & 7;
-  return (uint32_t)(box * (kVT * 128) + row * 128 + ((c ^ (row & 7)) << 4));
-}
 
 template <int HD>
 __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant__ CUtensorMap tmk,
@@ -466,6 +461,25 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
 #pragma unroll
     for (int i = 0; i < Cfg::NTO; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     const uint32_t stage_base = smem_u32(stages);
+    // A K or V stage holds HD / 64 boxes of 64 keys x 128 bytes: 16-byte chunk c of key
+    // row r sits at (c / 8) * 8 KB + r * 128 + ((c % 8) XOR (r % 8)) * 16.  The lane parts
+    // of the ldmatrix addresses (the compile-time row and chunk terms split off): the K
+    // fragments read row 16 kg + (lane / 16) 8 + lane % 8,
+    // chunk 2 ks + (lane / 8) % 2; the V fragments row 16 kk + ((lane / 8) % 2) 8 + lane % 8,
+    // chunk 2 np + lane / 16.  Rows are multiples of 8 apart, so row % 8 = lane % 8 and the
+    // XOR term depends on the chunk only through (chunk % 8) / 2: four offsets per operand.
+    uint32_t swk[4], swv[4];
+    {
+      const int l7 = lane & 7;
+      const int xk = ((lane >> 3) & 1) ^ l7, xv = (lane >> 4) ^ l7;
+      const uint32_t rk = (uint32_t)((((lane >> 4) << 3) + l7) * 128);
+      const uint32_t rv = (uint32_t)(((((lane >> 3) & 1) << 3) + l7) * 128);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        swk[j] = rk + (uint32_t)(((2 * j) ^ xk) << 4);
+        swv[j] = rv + (uint32_t)(((2 * j) ^ xv) << 4);
+      }
+    }
     for (int i = 0; i < ntiles; ++i) {
       const int st = i % NS;
       if (*(volatile int*)&s_flags[0]) break;
@@ -490,10 +504,9 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
         const uint32_t A[4] = {qa.x, qa.y, qa.z, qa.w};
 #pragma unroll
         for (int kg = 0; kg < KB / 16; ++kg) {
-          const int mrow = hb + kg * 16 + ((lane >> 4) << 3) + (lane & 7);
-          const int mchunk = ks * 2 + ((lane >> 3) & 1);
           uint32_t b0, b1, b2, b3;
-          ldmatrix_x4(kb0 + vswz<HD>(mrow, mchunk), b0, b1, b2, b3);
+          ldmatrix_x4(kb0 + swk[ks & 3] + (uint32_t)((ks >> 2) * (kVT * 128) + (hb + kg * 16) * 128),
+                      b0, b1, b2, b3);
           mma_bf16(s[2 * kg], A, b0, b1);
           mma_bf16(s[2 * kg + 1], A, b2, b3);
         }
@@ -565,10 +578,10 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
         const uint32_t mhi = (kv0 + 8 < k_end ? 0xffffu : 0u) | (kv0 + 9 < k_end ? 0xffff0000u : 0u);
 #pragma unroll
         for (int np = 0; np < Cfg::NTO / 2; ++np) {
-          const int mrow = hb + kk * 16 + (((lane >> 3) & 1) << 3) + (lane & 7);
-          const int mchunk = np * 2 + (lane >> 4);
           uint32_t b0, b1, b2, b3;
-          ldmatrix_x4_trans(vb0 + vswz<HD>(mrow, mchunk), b0, b1, b2, b3);
+          ldmatrix_x4_trans(
+              vb0 + swv[np & 3] + (uint32_t)((np >> 2) * (kVT * 128) + (hb + kk * 16) * 128),
+              b0, b1, b2, b3);
           if (tail) {
             b0 &= mlo;
             b2 &= mlo;
