@@ -73,6 +73,23 @@ static __device__ __forceinline__ void finish_head_row(const GemvArgs& a, int hh
     float* q = a.q_out + ((size_t)b * a.nh + hh) * HD;
 #pragma unroll
     for (int j = 0; j < J; ++j) q[lane + 32 * j] = v[j];
+    if (HD == 128 && a.qx) {
+      // the tensor-core operand of the verify attention: query row qr = b G + hh % G of
+      // KV head hh / G, scaled, bf16 hi in row qr and lo in row qr + 64, dims in two
+      // 64-wide boxes, 16-byte chunk c of row r at (c XOR (r % 8))
+      const int qr = b * a.G + hh % a.G;
+      uint8_t* img = a.qx + (size_t)(hh / a.G) * 32768;
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        const int d = lane + 32 * j;
+        __nv_bfloat16 h, lo;
+        split_bf16(v[j] * a.qscale, h, lo);
+        const int box = d >> 6, c = (d & 63) >> 3, e = d & 7;
+        const int rh = qr, rl = qr + 64;
+        *reinterpret_cast<__nv_bfloat16*>(img + box * 16384 + rh * 128 + ((c ^ (rh & 7)) << 4) + 2 * e) = h;
+        *reinterpret_cast<__nv_bfloat16*>(img + box * 16384 + rl * 128 + ((c ^ (rl & 7)) << 4) + 2 * e) = lo;
+      }
+    }
   } else {
     const int kvh = kind == 1 ? hh - a.nh : hh - a.nh - a.nkv;
     if (P < 0 || (!a.ring && P >= a.C)) {

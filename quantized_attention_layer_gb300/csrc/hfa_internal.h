@@ -35,6 +35,10 @@ struct GemvArgs {
   int v_unit_norm;
   int k_eq_v;              // the key finisher also writes V = unit RMSNorm of the raw K
   float* q_out;            // f32 [B, nh, hd]
+  uint8_t* qx;             // nullable: the scaled q as the verify attention's tensor-core
+                           // operand, [nkv][2 boxes][128 rows][128 B] (see finish_head_row)
+  float qscale;            // scale folded into qx
+  int G;                   // query heads per KV head
   __nv_bfloat16* k_cache;  // [B, nkv, C, hd]
   __nv_bfloat16* v_cache;
   float* k_tap;            // nullable f32 [B, nkv, hd]

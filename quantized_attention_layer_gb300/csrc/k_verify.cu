@@ -341,6 +341,7 @@ struct VAttnArgs {
   int splits, chunk, klo, khi;  // keys [klo, khi] are read by some row
   float* part;                  // [nkv][splits][64 rows][hd + 4]: O[hd], m, l, pad
   uint8_t* bops;                // o_proj activation operand (see store_bop_group)
+  const uint8_t* qx;            // head_dim 128: the scaled q as an MMA operand image per KV head
   float* o;                     // [L, nh, hd]
   unsigned* err;
 };
@@ -618,6 +619,377 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
   }
 }
 
+// ------------------------------------------------------------------ block attention (tcgen05)
+// The same records as attn_verify_kernel, for head_dim 128, with both products on the
+// 5th-generation tensor cores.  Per CTA (KV head, key chunk) and 64-key stage i:
+//   S_i = Qx K^T   M = 128 rows (queries 0..63 as bf16 hi, then the same queries as lo),
+//                  N = 64 keys, K = 128: the score of query q is S[q] + S[q + 64];
+//                  two TMEM buffers, so S_{i+1} is computed while stage i's softmax runs;
+//   O  += Px Vt    M = 128 rows (P hi for rows 0..63, P lo for 64..127), N = 128 dims,
+//                  K = 64 keys, accumulated in TMEM; Vt is the stage's V transposed in
+//                  shared memory.  Query q's O is O[q] + O[q + 64].
+// Eight consumer warps: warps w and w + 4 share TMEM lane quadrant w (rows 32w .. 32w+31),
+// one per half of the columns.  The four threads of query q (rows q and q + 64, two
+// column halves) split the stage's keys 16 each, exchanging score parts and maxima through
+// shared memory, and each writes P (hi and lo) for its keys; the warps also transpose V
+// (ldmatrix + stmatrix.trans, keys past the chunk zeroed).  When a query's running
+// maximum moves, its O rows are rescaled in TMEM before the next O += P V.  One thread of
+// warp 8 streams K/V stages with TMA and issues the MMAs.
+namespace vtc {
+constexpr int NS = 3;                          // K/V stages of 64 keys
+constexpr int STAGE = 2 * kVT * 128 * 2;       // K (2 boxes) + V (2 boxes): 32 KB
+constexpr int QX_OFF = NS * STAGE;             // Qx: 2 boxes x 128 rows x 128 B
+constexpr int PX_OFF = QX_OFF + 32768;         // Px: 128 rows x 128 B
+constexpr int VT_OFF = PX_OFF + 16384;         // Vt: 128 rows (dims) x 128 B (64 keys)
+constexpr int SL_OFF = VT_OFF + 16384;         // lo-row scores f32 [64][64]
+constexpr int CR_OFF = SL_OFF + 16384;         // corrections f32 [64]
+constexpr int MX_OFF = CR_OFF + 256;           // stage maxima (then partial sums) f32 [64][4]
+constexpr int BAR_OFF = MX_OFF + 1024;
+constexpr size_t SMEM = 1024 + BAR_OFF + 256;
+constexpr int THREADS = 288;                 // 8 consumer warps + the producer warp
+constexpr int NCW = 8;
+}  // namespace vtc
+
+__global__ void __launch_bounds__(vtc::THREADS, 1)
+    attn_verify_tc_kernel(const __grid_constant__ CUtensorMap tmk,
+                          const __grid_constant__ CUtensorMap tmv, const VAttnArgs a) {
+  using namespace vtc;
+  constexpr int HD = 128;
+  constexpr int RS = HD + 4;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~(uintptr_t)1023);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + BAR_OFF);  // [NS]
+  uint64_t* s_bar = full + NS;    // [2] S of stage i in TMEM buffer i % 2
+  uint64_t* p_bar = s_bar + 2;    // Px, Vt written and O rescaled (one arrival per warp)
+  uint64_t* pv_bar = p_bar + 1;   // O += P V of the stage done (Px, Vt free again)
+  uint64_t* qx_bar = pv_bar + 1;  // Qx landed
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(qx_bar + 1);
+  int* s_abort = reinterpret_cast<int*>(s_tmem + 1);
+  int* s_issued = s_abort + 1;
+  float* corr_s = reinterpret_cast<float*>(smem + CR_OFF);
+  float* mx_s = reinterpret_cast<float*>(smem + MX_OFF);
+  float4* slo = reinterpret_cast<float4*>(smem + SL_OFF);  // [64 queries][16] swizzled
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kvh = blockIdx.x / a.splits, split = blockIdx.x - kvh * a.splits;
+  const int NQ = a.L * a.G;
+  const int k_begin = a.klo + split * a.chunk;
+  int k_end = k_begin + a.chunk;
+  if (k_end > a.khi + 1) k_end = a.khi + 1;
+  const int nkeys = k_end > k_begin ? k_end - k_begin : 0;
+  const int ntiles = (nkeys + kVT - 1) / kVT;
+  const int row0 = kvh * a.C + k_begin;
+  const uint32_t sbase = smem_u32(smem);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) mbar_init(&full[i], 1);
+    mbar_init(&s_bar[0], 1);
+    mbar_init(&s_bar[1], 1);
+    mbar_init(p_bar, NCW);
+    mbar_init(pv_bar, 1);
+    mbar_init(qx_bar, 1);
+    *s_abort = 0;
+    *s_issued = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(s_tmem, 256);  // S in columns [0, 64) and [64, 128), O in [128, 256)
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const uint32_t tO = tmem + 128;
+
+  if (warp == NCW) {
+    if (lane == 0) {
+      // ---- producer and MMA issuer
+      auto issue = [&](int i) {
+        uint8_t* st = smem + (i % NS) * STAGE;
+        mbar_arrive_expect_tx(&full[i % NS], STAGE);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          tma_load_2d(st + j * kVT * 128, &tmk, &full[i % NS], 64 * j, row0 + i * kVT);
+          tma_load_2d(st + 2 * kVT * 128 + j * kVT * 128, &tmv, &full[i % NS], 64 * j,
+                      row0 + i * kVT);
+        }
+      };
+      constexpr uint32_t idS = idesc_bf16_f32(128, 64), idPV = idesc_bf16_f32(128, 128);
+      auto mma_s = [&](int i) {  // S_i into buffer i % 2 (its stage has landed)
+        const uint32_t kb = sbase + (i % NS) * STAGE;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma_f16(tmem + (i & 1) * 64,
+                     smem_desc_sw128(sbase + QX_OFF + (kk >> 2) * 16384 + (kk & 3) * 32),
+                     smem_desc_sw128(kb + (kk >> 2) * 8192 + (kk & 3) * 32), idS, kk != 0);
+        tc_commit(&s_bar[i & 1]);
+      };
+      // keys before the block's first position are not written by the QKV kernel
+      int n0 = 0;
+      for (; n0 < NS && n0 < ntiles && k_begin + (n0 + 1) * kVT <= a.base; ++n0) issue(n0);
+      pdl_wait();
+      for (; n0 < NS && n0 < ntiles; ++n0) issue(n0);
+      int issued = n0;
+      // the queries, written by the QKV kernel's head epilogue in operand form
+      mbar_arrive_expect_tx(qx_bar, 32768);
+      bulk_load(smem + QX_OFF, a.qx + (size_t)kvh * 32768, 32768, qx_bar);
+      bool ok = mbar_wait(qx_bar, 0, a.err, s_abort);
+      if (ok && ntiles > 0) {
+        ok = mbar_wait(&full[0], 0, a.err, s_abort);
+        tc_fence_after();
+        if (ok) mma_s(0);
+      }
+      for (int i = 0; ok && i < ntiles; ++i) {
+        if (i + 1 < ntiles) {  // the next scores while this stage's softmax runs
+          if (!mbar_wait(&full[(i + 1) % NS], ((i + 1) / NS) & 1, a.err, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mma_s(i + 1);
+        }
+        if (!mbar_wait(p_bar, i & 1, a.err, s_abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma_f16(tO, smem_desc_sw128(sbase + PX_OFF + kk * 32),
+                     smem_desc_sw128(sbase + VT_OFF + kk * 32), idPV, (i | kk) != 0);
+        tc_commit(pv_bar);
+        if (i + NS < ntiles) {  // K went into S_i, V into Vt: the stage is free
+          issue(i + NS);
+          ++issued;
+        }
+      }
+      if (!ok) *(volatile int*)s_abort = 1;
+      *s_issued = issued;
+    } else {
+      pdl_wait();
+    }
+    pdl_launch_dependents();
+  } else {
+    pdl_wait();
+    pdl_launch_dependents();
+    // consumer warp w: TMEM lane quadrant w % 4 (row r), column half hf = w / 4
+    const int hf = warp >> 2;
+    const int r = 32 * (warp & 3) + lane;  // TMEM lane / operand row
+    const int q = r & 63;                  // query of the row
+    const int lo = r >= 64 ? 1 : 0;        // row holds the lo part
+    const bool qvalid = q < NQ;
+    const int tok = qvalid ? q / a.G : 0;
+    const int limit = a.base + tok;
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    const int part = 2 * hf + lo;          // this thread's 16 keys of the stage: 16 part ..
+    float m = -INFINITY, l = 0.f;
+    // every consumer runs every stage's named barriers, also after a give-up (a bounded
+    // wait that runs out sets the abort flag; later waits return at once), so no thread is
+    // left at a barrier the others skipped; the result is agreed across the warp, as what
+    // follows are .sync.aligned instructions
+    bool dead = false;
+    auto wait_ok = [&](uint64_t* bar, uint32_t parity) {
+      if (!dead && !mbar_wait(bar, parity, a.err, s_abort)) {
+        dead = true;
+        *(volatile int*)s_abort = 1;
+      }
+      dead = !__all_sync(0xffffffffu, !dead);
+      return !dead;
+    };
+    for (int i = 0; i < ntiles; ++i) {
+      const int st = i % NS;
+      const int key_lo = k_begin + i * kVT;
+      // the four threads of query q (rows q and q + 64, column halves 0 and 1) hold its
+      // scores' hi or lo part for 32 keys; each takes 16 of them, swapping the other 16
+      // with its partner row through shared memory
+      float sv[32];
+      if (wait_ok(&s_bar[i & 1], (i >> 1) & 1)) {
+        tc_fence_after();
+        uint32_t t[2][16];
+        tmem_ld16_nowait(tmem + (i & 1) * 64 + lane_off + 32 * hf, t[0]);
+        tmem_ld16_nowait(tmem + (i & 1) * 64 + lane_off + 32 * hf + 16, t[1]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          sv[e] = __uint_as_float(t[0][e]);
+          sv[16 + e] = __uint_as_float(t[1][e]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) sv[c] = 0.f;
+      }
+      // Px, Vt and O are free once O += P V of the previous stage is done (that MMA was
+      // issued after this stage's S, so the S barrier does not cover it)
+      if (i > 0) wait_ok(pv_bar, (i - 1) & 1);
+      float sc[16], give[16];  // (selected with fixed indices: no local memory)
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        sc[c] = lo ? sv[16 + c] : sv[c];
+        give[c] = lo ? sv[c] : sv[16 + c];
+      }
+      // keys 32 hf + 16 (1 - lo) .. go to the partner row, in float4 slot (key / 4)
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const int kc = 8 * hf + 4 * (1 - lo) + c4;
+        slo[q * 16 + (kc ^ (q & 15))] =
+            make_float4(give[4 * c4], give[4 * c4 + 1], give[4 * c4 + 2], give[4 * c4 + 3]);
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");  // score parts out
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const int kc = 4 * part + c4;
+        const float4 v = slo[q * 16 + (kc ^ (q & 15))];
+        sc[4 * c4] += v.x;
+        sc[4 * c4 + 1] += v.y;
+        sc[4 * c4 + 2] += v.z;
+        sc[4 * c4 + 3] += v.w;
+      }
+      if (a.cap_log2 != 0.f) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) sc[c] = a.cap_log2 * tanhf(sc[c]);
+      }
+      const int klo = key_lo + 16 * part;  // first key of this thread's part
+      if (!(klo + 15 < k_end && klo + 15 <= limit && (!a.sliding || klo > limit - a.window))) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int key = klo + c;
+          const bool vis = key < k_end && key <= limit && (!a.sliding || key > limit - a.window);
+          if (!vis) sc[c] = -INFINITY;
+        }
+      }
+      float mx[4] = {sc[0], sc[1], sc[2], sc[3]};  // four independent chains
+#pragma unroll
+      for (int c = 4; c < 16; ++c) mx[c & 3] = fmaxf(mx[c & 3], sc[c]);
+      mx_s[4 * q + part] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      asm volatile("bar.sync 1, 256;" ::: "memory");  // maxima out
+      const float4 mq = *reinterpret_cast<const float4*>(mx_s + 4 * q);
+      const float m_new = fmaxf(m, fmaxf(fmaxf(mq.x, mq.y), fmaxf(mq.z, mq.w)));
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
+      const float corr = ex2_approx(m - m_use);
+      m = m_new;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c8 = 0; c8 < 2; ++c8) {  // P hi (row q) and lo (row q + 64) of the part
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float p0 = ex2_approx(sc[8 * c8 + 2 * e] - m_use);
+          const float p1 = ex2_approx(sc[8 * c8 + 2 * e + 1] - m_use);
+          ps[e] += p0 + p1;
+          __nv_bfloat16 h0, l0, h1, l1;
+          split_bf16(p0, h0, l0);
+          split_bf16(p1, h1, l1);
+          hw[e] = pack_bf2(h0, h1);
+          lw[e] = pack_bf2(l0, l1);
+        }
+        const int chunk = 2 * part + c8;
+        const uint32_t sw = (uint32_t)((chunk ^ (q & 7)) << 4);
+        *reinterpret_cast<uint4*>(smem + PX_OFF + q * 128 + sw) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4*>(smem + PX_OFF + (q + 64) * 128 + sw) =
+            make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      }
+      l = l * corr + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+      if (part == 0) corr_s[q] = corr;
+      // the transposed V of the stage, an eighth per warp: 8 key blocks x 16 dim blocks
+      // of 8x8, one x4 taking 4 dim blocks of a key block
+      {
+        const bool vin = wait_ok(&full[st], (i / NS) & 1);
+        const uint32_t vb = sbase + st * STAGE + 2 * kVT * 128;
+        for (int blk = warp; vin && blk < 32; blk += NCW) {
+          const int ka = blk >> 2, b0 = (blk & 3) * 4;  // key block, first dim block
+          const int mj = lane >> 3, j = lane & 7;        // matrix, row within it
+          const int bb = b0 + mj;                        // this lane's dim block
+          const int key = 8 * ka + j;
+          const uint32_t src = vb + (bb >> 3) * 8192 + key * 128 + (((bb & 7) ^ (key & 7)) << 4);
+          uint32_t v0, v1, v2, v3;
+          ldmatrix_x4(src, v0, v1, v2, v3);
+          if (key_lo + 8 * ka + (lane >> 2) >= k_end) v0 = v1 = v2 = v3 = 0u;  // held key
+          const int dim = 8 * bb + j;
+          const uint32_t dst = sbase + VT_OFF + dim * 128 + ((ka ^ (dim & 7)) << 4);
+          stmatrix_x4_trans(dst, v0, v1, v2, v3);
+        }
+      }
+      fence_proxy_async_smem();
+      asm volatile("bar.sync 1, 256;" ::: "memory");  // P, Vt and corrections out
+      // O rows of a query whose maximum moved are rescaled before O += P V of this stage
+      // (stage 0's MMA overwrites: nothing to scale); each thread its row's column half
+      const float cr = corr_s[q];
+      if (i > 0 && !dead && __any_sync(0xffffffffu, cr != 1.f)) {
+        uint32_t t[4][16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld16_nowait(tO + lane_off + 64 * hf + 16 * c, t[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) t[c][e] = __float_as_uint(__uint_as_float(t[c][e]) * cr);
+          tmem_st16(tO + lane_off + 64 * hf + 16 * c, t[c]);
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_bar);
+    }
+    // O: wait for the last O += P V; each thread loads its row's column half, and the two
+    // parts of each query are added through shared memory (the ring is idle)
+    float o[64];
+    if (ntiles > 0 && wait_ok(pv_bar, (ntiles - 1) & 1)) {
+      tc_fence_after();
+      uint32_t t[4][16];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld16_nowait(tO + lane_off + 64 * hf + 16 * c, t[c]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 16; ++e) o[16 * c + e] = __uint_as_float(t[c][e]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 64; ++j) o[j] = 0.f;
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    mx_s[4 * q + part] = l;  // the four partial sums of the query
+    float4* ox = reinterpret_cast<float4*>(smem);  // [64 queries][32] swizzled
+    if (lo) {
+#pragma unroll
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const int k4 = 16 * hf + c4;
+        ox[q * 32 + (k4 ^ (q & 31))] = make_float4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]);
+      }
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    if (!lo && qvalid && !*(volatile int*)s_abort) {
+      float* pr = a.part + ((size_t)kvh * a.splits + split) * 64 * RS + (size_t)q * RS;
+#pragma unroll
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const int k4 = 16 * hf + c4;
+        const float4 v = ox[q * 32 + (k4 ^ (q & 31))];
+        *reinterpret_cast<float4*>(pr + 4 * k4) =
+            make_float4(o[4 * c4] + v.x, o[4 * c4 + 1] + v.y, o[4 * c4 + 2] + v.z, o[4 * c4 + 3] + v.w);
+      }
+      if (hf == 0) {
+        const float4 lq = *reinterpret_cast<const float4*>(mx_s + 4 * q);
+        *reinterpret_cast<float2*>(pr + HD) = make_float2(m, (lq.x + lq.y) + (lq.z + lq.w));
+      }
+    }
+  }
+  // drain: copies may still be landing after a give-up; then TMEM back
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int issued = *s_issued;
+    for (int st = 0; st < NS && st < issued; ++st) {
+      const int last = st + ((issued - 1 - st) / NS) * NS;
+      mbar_wait(&full[st], (last / NS) & 1, a.err);
+    }
+  }
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
 // Combination of the block attention's split records, one CTA per RPW = 256 / HD query
 // rows of one KV head (the lanes of a row own 8 output columns each):
 //   M = max_s m_s,  w_s = 2^(m_s - M),  o = sum_s w_s O_s / sum_s w_s l_s.
@@ -754,6 +1126,7 @@ struct VerifyState {
   float* y_post = nullptr;      // [16][H]: o_proj output kept for the post-attention norm
   uint8_t* bq = nullptr;        // QKV activation operand [H / 64][32][128 B]
   uint8_t* bo = nullptr;        // o_proj activation operand [nh hd / 64][32][128 B]
+  uint8_t* qx = nullptr;        // head_dim 128: attention query operand [nkv][32 KB]
   size_t part_records = 0;
   int max_clusters[9] = {};     // co-resident GEMM clusters of n CTAs (index n)
 };
@@ -782,6 +1155,10 @@ hfa_status verify_create(const hfa_layer_desc& d, int num_sms, VerifyState** out
     e = cudaMalloc(&v->bo, (size_t)(d.num_heads * d.head_dim / kVK) * kBChunkBytes);
   if (e == cudaSuccess)
     e = cudaMemset(v->bo, 0, (size_t)(d.num_heads * d.head_dim / kVK) * kBChunkBytes);
+  if (e == cudaSuccess && d.head_dim == 128) {  // rows past L * G stay zero
+    e = cudaMalloc(&v->qx, (size_t)nkv * 32768);
+    if (e == cudaSuccess) e = cudaMemset(v->qx, 0, (size_t)nkv * 32768);
+  }
   if (e == cudaSuccess) e = cudaMalloc(&v->y_post, (size_t)16 * d.hidden * sizeof(float));
   if (e != cudaSuccess) {
     snprintf(g_verify_error, sizeof g_verify_error, "%s", cudaGetErrorString(e));
@@ -823,6 +1200,7 @@ void verify_free(VerifyState* v) {
   cudaFree(v->y_post);
   cudaFree(v->bq);
   cudaFree(v->bo);
+  cudaFree(v->qx);
   delete v;
 }
 
@@ -928,6 +1306,9 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   qa.g.v_unit_norm = (d.flags & HFA_F_V_UNIT_NORM) ? 1 : 0;
   qa.g.k_eq_v = (d.flags & HFA_F_K_EQ_V) ? 1 : 0;
   qa.g.q_out = c.q_f32;
+  qa.g.qx = v->qx;  // head_dim 128 only (else null)
+  qa.g.qscale = d.softcap > 0.f ? d.attn_scale / d.softcap : d.attn_scale * 1.4426950408889634f;
+  qa.g.G = G;
   qa.g.k_cache = c.k_cache;
   qa.g.v_cache = c.v_cache;
   qa.g.k_tap = c.k_tap;
@@ -983,6 +1364,7 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   aa.chunk = chunk;
   aa.part = v->part;
   aa.bops = v->bo;
+  aa.qx = v->qx;
   aa.o = c.o_f32;
   aa.err = c.err;
   const int nq_warps = (c.L * G + 7) / 8;
@@ -990,9 +1372,8 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   tb("verify_attention");
   if (hd == 64)
     e = launch_ex(attn_verify_kernel<64>, nkv * S, athreads, VACfg<64>::SMEM, pdl, s, tk, tv, aa);
-  else if (hd == 128)
-    e = launch_ex(attn_verify_kernel<128>, nkv * S, athreads, VACfg<128>::SMEM, pdl, s, tk, tv,
-                  aa);
+  else if (hd == 128)  // both products on the tensor cores (TMEM accumulators)
+    e = launch_ex(attn_verify_tc_kernel, nkv * S, vtc::THREADS, vtc::SMEM, pdl, s, tk, tv, aa);
   else
     e = launch_ex(attn_verify_kernel<256>, nkv * S, athreads, VACfg<256>::SMEM, pdl, s, tk, tv,
                   aa);
