@@ -627,7 +627,8 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
 //                  two TMEM buffers, so S_{i+1} is computed while stage i's softmax runs;
 //   O  += Px Vt    M = 128 rows (P hi for rows 0..63, P lo for 64..127), N = 128 dims,
 //                  K = 64 keys, accumulated in TMEM; Vt is the stage's V transposed in
-//                  shared memory.  Query q's O is O[q] + O[q + 64].
+//                  shared memory.  Px and Vt are double-buffered, so the next stage's
+//                  softmax does not wait for this MMA.  Query q's O is O[q] + O[q + 64].
 // Eight consumer warps: warps w and w + 4 share TMEM lane quadrant w (rows 32w .. 32w+31),
 // one per half of the columns.  The four threads of query q (rows q and q + 64, two
 // column halves) split the stage's keys 16 each, exchanging score parts and maxima through
@@ -639,9 +640,9 @@ namespace vtc {
 constexpr int NS = 3;                          // K/V stages of 64 keys
 constexpr int STAGE = 2 * kVT * 128 * 2;       // K (2 boxes) + V (2 boxes): 32 KB
 constexpr int QX_OFF = NS * STAGE;             // Qx: 2 boxes x 128 rows x 128 B
-constexpr int PX_OFF = QX_OFF + 32768;         // Px: 128 rows x 128 B
-constexpr int VT_OFF = PX_OFF + 16384;         // Vt: 128 rows (dims) x 128 B (64 keys)
-constexpr int SL_OFF = VT_OFF + 16384;         // lo-row scores f32 [64][64]
+constexpr int PX_OFF = QX_OFF + 32768;         // Px [2]: 128 rows x 128 B each
+constexpr int VT_OFF = PX_OFF + 32768;         // Vt [2]: 128 rows (dims) x 128 B (64 keys)
+constexpr int SL_OFF = VT_OFF + 32768;         // score parts f32 [64][64]
 constexpr int CR_OFF = SL_OFF + 16384;         // corrections f32 [64]
 constexpr int MX_OFF = CR_OFF + 256;           // stage maxima (then partial sums) f32 [64][4]
 constexpr int BAR_OFF = MX_OFF + 1024;
@@ -662,8 +663,8 @@ __global__ void __launch_bounds__(vtc::THREADS, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + BAR_OFF);  // [NS]
   uint64_t* s_bar = full + NS;    // [2] S of stage i in TMEM buffer i % 2
   uint64_t* p_bar = s_bar + 2;    // Px, Vt written and O rescaled (one arrival per warp)
-  uint64_t* pv_bar = p_bar + 1;   // O += P V of the stage done (Px, Vt free again)
-  uint64_t* qx_bar = pv_bar + 1;  // Qx landed
+  uint64_t* pv_bar = p_bar + 1;   // [2] O += P V of stage i done: Px, Vt buffer i % 2 free
+  uint64_t* qx_bar = pv_bar + 2;  // Qx landed
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(qx_bar + 1);
   int* s_abort = reinterpret_cast<int*>(s_tmem + 1);
   int* s_issued = s_abort + 1;
@@ -687,7 +688,8 @@ __global__ void __launch_bounds__(vtc::THREADS, 1)
     mbar_init(&s_bar[0], 1);
     mbar_init(&s_bar[1], 1);
     mbar_init(p_bar, NCW);
-    mbar_init(pv_bar, 1);
+    mbar_init(&pv_bar[0], 1);
+    mbar_init(&pv_bar[1], 1);
     mbar_init(qx_bar, 1);
     *s_abort = 0;
     *s_issued = 0;
@@ -755,11 +757,12 @@ __global__ void __launch_bounds__(vtc::THREADS, 1)
           break;
         }
         tc_fence_after();
+        const uint32_t pb = (uint32_t)(i & 1) * 16384;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          tc_mma_f16(tO, smem_desc_sw128(sbase + PX_OFF + kk * 32),
-                     smem_desc_sw128(sbase + VT_OFF + kk * 32), idPV, (i | kk) != 0);
-        tc_commit(pv_bar);
+          tc_mma_f16(tO, smem_desc_sw128(sbase + PX_OFF + pb + kk * 32),
+                     smem_desc_sw128(sbase + VT_OFF + pb + kk * 32), idPV, (i | kk) != 0);
+        tc_commit(&pv_bar[i & 1]);
         if (i + NS < ntiles) {  // K went into S_i, V into Vt: the stage is free
           issue(i + NS);
           ++issued;
@@ -820,9 +823,10 @@ __global__ void __launch_bounds__(vtc::THREADS, 1)
 #pragma unroll
         for (int c = 0; c < 32; ++c) sv[c] = 0.f;
       }
-      // Px, Vt and O are free once O += P V of the previous stage is done (that MMA was
-      // issued after this stage's S, so the S barrier does not cover it)
-      if (i > 0) wait_ok(pv_bar, (i - 1) & 1);
+      // Px, Vt buffer i % 2 is free once O += P V of stage i - 2 is done (the S barrier
+      // does not cover MMAs issued after S)
+      const uint32_t pb = (uint32_t)(i & 1) * 16384;
+      if (i >= 2) wait_ok(&pv_bar[i & 1], ((i - 2) >> 1) & 1);
       float sc[16], give[16];  // (selected with fixed indices: no local memory)
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
@@ -886,8 +890,9 @@ __global__ void __launch_bounds__(vtc::THREADS, 1)
         }
         const int chunk = 2 * part + c8;
         const uint32_t sw = (uint32_t)((chunk ^ (q & 7)) << 4);
-        *reinterpret_cast<uint4*>(smem + PX_OFF + q * 128 + sw) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        *reinterpret_cast<uint4*>(smem + PX_OFF + (q + 64) * 128 + sw) =
+        *reinterpret_cast<uint4*>(smem + PX_OFF + pb + q * 128 + sw) =
+            make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4*>(smem + PX_OFF + pb + (q + 64) * 128 + sw) =
             make_uint4(lw[0], lw[1], lw[2], lw[3]);
       }
       l = l * corr + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
@@ -907,16 +912,19 @@ __global__ void __launch_bounds__(vtc::THREADS, 1)
           ldmatrix_x4(src, v0, v1, v2, v3);
           if (key_lo + 8 * ka + (lane >> 2) >= k_end) v0 = v1 = v2 = v3 = 0u;  // held key
           const int dim = 8 * bb + j;
-          const uint32_t dst = sbase + VT_OFF + dim * 128 + ((ka ^ (dim & 7)) << 4);
+          const uint32_t dst = sbase + VT_OFF + pb + dim * 128 + ((ka ^ (dim & 7)) << 4);
           stmatrix_x4_trans(dst, v0, v1, v2, v3);
         }
       }
       fence_proxy_async_smem();
       asm volatile("bar.sync 1, 256;" ::: "memory");  // P, Vt and corrections out
-      // O rows of a query whose maximum moved are rescaled before O += P V of this stage
-      // (stage 0's MMA overwrites: nothing to scale); each thread its row's column half
+      // O rows of a query whose maximum moved are rescaled before O += P V of this stage,
+      // once the previous one is done (stage 0's MMA overwrites: nothing to scale); each
+      // thread its row's column half
       const float cr = corr_s[q];
-      if (i > 0 && !dead && __any_sync(0xffffffffu, cr != 1.f)) {
+      if (i > 0 && !dead && __any_sync(0xffffffffu, cr != 1.f) &&
+          wait_ok(&pv_bar[(i - 1) & 1], ((i - 1) >> 1) & 1)) {
+        tc_fence_after();
         uint32_t t[4][16];
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld16_nowait(tO + lane_off + 64 * hf + 16 * c, t[c]);
@@ -936,7 +944,7 @@ __global__ void __launch_bounds__(vtc::THREADS, 1)
     // O: wait for the last O += P V; each thread loads its row's column half, and the two
     // parts of each query are added through shared memory (the ring is idle)
     float o[64];
-    if (ntiles > 0 && wait_ok(pv_bar, (ntiles - 1) & 1)) {
+    if (ntiles > 0 && wait_ok(&pv_bar[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1)) {
       tc_fence_after();
       uint32_t t[4][16];
 #pragma unroll
