@@ -10,16 +10,20 @@
 //    activations its N = 32 (16 tokens x fp32 split into bf16 hi and lo, so the product
 //    keeps ~16 bits of the activation), K in 64-element stages.  A producer thread
 //    streams 128x64 weight tiles -- repacked at layer creation into the 128-byte-swizzled
-//    shared-memory image, so each is one 16 KB bulk copy -- into a 6-stage ring; one
-//    thread issues tcgen05.mma into a 128x32 fp32 TMEM accumulator and releases stages
-//    with tcgen05.commit; the four warps read the accumulator back (tcgen05.ld) and add
-//    their partial sums (k-split) into an fp32 accumulator.  The CTA whose chunks
-//    complete a head / row tile runs the same epilogue as the decode GEMV.
-//  * attn_verify_kernel: one CTA per (KV head, key chunk); a TMA producer warp streams K
-//    and V tiles, each consumer warp owns 8 query rows (bf16 hi/lo in MMA rows g and
-//    g + 8) and takes every 64-key stage in one online-softmax update (the stage's
-//    scores, then O += P V), with the causal / window mask of its rows.  Each CTA
-//    writes one (O, m, l) record per query row.
+//    shared-memory image, so each is one 16 KB bulk copy -- with the matching 4 KB
+//    activation chunk into a 10-stage ring; one thread issues tcgen05.mma into a 128x32
+//    fp32 TMEM accumulator and releases stages with tcgen05.commit.  The k-splits of a
+//    row tile form a cluster and add their partial sums through distributed shared
+//    memory; then the head epilogue (norms, RoPE, KV append; the query also as the
+//    attention's operand image) or the residual epilogue runs on the complete rows.
+//  * attn_verify_tc_kernel (head_dim 128, tcgen05): one CTA per (KV head, key chunk);
+//    S = Qx K^T and O += Px Vt on the tensor cores with TMEM accumulators, the online
+//    softmax of each query split over the four threads that hold its two TMEM rows.
+//  * attn_verify_kernel (head_dim 64, 256; mma.sync): one CTA per (KV head, key chunk); a
+//    TMA producer warp streams K and V tiles, each consumer warp owns 8 query rows (bf16
+//    hi/lo in MMA rows g and g + 8) and takes every 64-key stage in one online-softmax
+//    update, with the causal / window mask of its rows.
+//    Both attention kernels write one (O, m, l) record per query row and CTA.
 //  * attn_verify_merge_kernel: the records of a KV head's chunks combined, a few query
 //    rows per CTA, into the f32 output and the o_proj activation operand.
 #include <cooperative_groups.h>
