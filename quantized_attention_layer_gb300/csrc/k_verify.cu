@@ -647,8 +647,7 @@ constexpr int QX_OFF = NS * STAGE;             // Qx: 2 boxes x 128 rows x 128 B
 constexpr int PX_OFF = QX_OFF + 32768;         // Px [2]: 128 rows x 128 B each
 constexpr int VT_OFF = PX_OFF + 32768;         // Vt [2]: 128 rows (dims) x 128 B (64 keys)
 constexpr int SL_OFF = VT_OFF + 32768;         // score parts f32 [64][64]
-constexpr int CR_OFF = SL_OFF + 16384;         // corrections f32 [64]
-constexpr int MX_OFF = CR_OFF + 256;           // stage maxima (then partial sums) f32 [64][4]
+constexpr int MX_OFF = SL_OFF + 16384;         // stage maxima (then partial sums) f32 [64][4]
 constexpr int BAR_OFF = MX_OFF + 1024;
 constexpr size_t SMEM = 1024 + BAR_OFF + 256;
 constexpr int THREADS = 288;                 // 8 consumer warps + the producer warp
@@ -672,7 +671,6 @@ __global__ void __launch_bounds__(vtc::THREADS, 1)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(qx_bar + 1);
   int* s_abort = reinterpret_cast<int*>(s_tmem + 1);
   int* s_issued = s_abort + 1;
-  float* corr_s = reinterpret_cast<float*>(smem + CR_OFF);
   float* mx_s = reinterpret_cast<float*>(smem + MX_OFF);
   float4* slo = reinterpret_cast<float4*>(smem + SL_OFF);  // [64 queries][16] swizzled
 
@@ -900,7 +898,6 @@ __global__ void __launch_bounds__(vtc::THREADS, 1)
             make_uint4(lw[0], lw[1], lw[2], lw[3]);
       }
       l = l * corr + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
-      if (part == 0) corr_s[q] = corr;
       // the transposed V of the stage, an eighth per warp: 8 key blocks x 16 dim blocks
       // of 8x8, one x4 taking 4 dim blocks of a key block
       {
@@ -921,11 +918,12 @@ __global__ void __launch_bounds__(vtc::THREADS, 1)
         }
       }
       fence_proxy_async_smem();
-      asm volatile("bar.sync 1, 256;" ::: "memory");  // P, Vt and corrections out
       // O rows of a query whose maximum moved are rescaled before O += P V of this stage,
       // once the previous one is done (stage 0's MMA overwrites: nothing to scale); each
-      // thread its row's column half
-      const float cr = corr_s[q];
+      // thread its row's column half, by the correction it computed itself (the four
+      // threads of a query hold the same maxima); each warp then reports its P and Vt
+      // writes and its rescale on p_bar
+      const float cr = corr;
       if (i > 0 && !dead && __any_sync(0xffffffffu, cr != 1.f) &&
           wait_ok(&pv_bar[(i - 1) & 1], ((i - 1) >> 1) & 1)) {
         tc_fence_after();
