@@ -83,3 +83,14 @@ def test_verify_block_sliding_hd256_softcap_short_block():
                     rope_theta=1e4, seed=99, weights_bf16=True, verify_len=16, base_pos=0,
                     softcap=30.0)
     _case(w, 7, 850)
+
+
+@pytest.mark.parametrize("window,softcap", [(100, 30.0), (40, 0.0)], ids=["w100cap", "w40"])
+def test_verify_block_hd128_sliding(window, softcap):
+    # head_dim 128 runs the tensor-core attention: window starts inside a 64-key stage,
+    # keys before the window and after each row's position masked, with and without softcap
+    w = wl.Workload(name=f"ver128s{window}", hidden=1024, num_heads=8, num_kv_heads=2,
+                    head_dim=128, layer_type=wl.SLIDING, window=window, kv_capacity=700,
+                    ring=False, batch=1, rope_theta=1e4, seed=101, weights_bf16=True,
+                    verify_len=16, base_pos=0, softcap=softcap)
+    _case(w, 11, 517)
