@@ -94,3 +94,15 @@ def test_verify_block_hd128_sliding(window, softcap):
                     ring=False, batch=1, rope_theta=1e4, seed=101, weights_bf16=True,
                     verify_len=16, base_pos=0, softcap=softcap)
     _case(w, 11, 517)
+
+
+def test_verify_block_repeats_bit_for_bit():
+    # no atomics on the data path: two runs on the same inputs agree in every bit
+    w = wl.VERIFY_L16
+    weights = wl.make_weights(w)
+    x = wl.make_x(w, rows=w.verify_len)
+    kv = wl.make_kv_cache(w)
+    a = run_gpu_verify(w, weights, x, w.base_pos, kv)
+    b = run_gpu_verify(w, weights, x, w.base_pos, kv)
+    for key in ("out_bf16", "q", "k", "v", "attn", "out"):
+        assert torch.equal(a[key], b[key]), key
