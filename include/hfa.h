@@ -45,7 +45,7 @@ typedef enum {
   HFA_ERANGE = -2,       /* a position outside the cache or the layer's limits */
   HFA_ENOMEM = -3,       /* device allocation failed (hfa_layer_create only) */
   HFA_ECUDA = -4,        /* a CUDA call failed; hfa_last_error has the CUDA message */
-  HFA_EUNSUPPORTED = -5, /* valid request this build does not implement */
+  HFA_EUNSUPPORTED = -5, /* valid request this library does not implement */
   HFA_EDEVICE = -6,      /* no usable sm_103 device, or a device-side check failed */
 } hfa_status;
 
@@ -88,7 +88,7 @@ typedef struct {
  *     With HFA_F_WEIGHTS_BF16: dense bf16, row-major [out, in].
  *   w_in_dev f32 [H], w_q_dev f32 [hd], w_k_dev f32 [hd]: RMSNorm weights, used as
  *     y = x * w / sqrt(mean(x^2) + eps).
- * Errors: HFA_EINVAL (shape, flags), HFA_EUNSUPPORTED (a shape this build does not
+ * Errors: HFA_EINVAL (shape, flags), HFA_EUNSUPPORTED (a shape this library does not
  * cover), HFA_EDEVICE (no sm_103 device), HFA_ENOMEM, HFA_ECUDA.  *out is NULL on
  * error.
  */
