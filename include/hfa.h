@@ -141,6 +141,13 @@ hfa_status hfa_decode_step_host(hfa_layer* layer, void* stream, const void* x_ho
  * is the caller's business.
  *   x_dev bf16 [L, H]; k_cache_dev, v_cache_dev bf16 [1, nkv, C, hd]; out_dev bf16 [L, H].
  * Needs a linear cache with base_pos + L <= C and 1 <= L <= max_verify_len.
+ * Errors: HFA_EINVAL for NULL or unaligned (16-byte) pointers, for L outside
+ * [1, max_verify_len] or a layer made with max_verify_len = 0; HFA_ERANGE for positions
+ * past the cache; HFA_EUNSUPPORTED for a ring cache, a Q8_0 layer (the block runs on
+ * bf16 weights, HFA_F_WEIGHTS_BF16) or L * (nh / nkv) > 64 query rows per KV head.  At
+ * create, max_verify_len > 16 and projection sizes that are not multiples of 128 rows
+ * are HFA_EUNSUPPORTED.  The post-attention norm, RoPE frequency factors and
+ * HFA_F_K_EQ_V apply as in the decode step.
  */
 hfa_status hfa_verify_block(hfa_layer* layer, void* stream, const void* x_dev, int L,
                             int base_pos, void* k_cache_dev, void* v_cache_dev, void* out_dev);
