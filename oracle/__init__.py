@@ -15,7 +15,8 @@ Parity status per function (pins live in ``tests/test_oracle_*.py``):
 * slots / visibility / attention: pinned (brute-force explicit mask, permutation,
   one key, softcap bound, ring == linear window)
 * decode step / verify block: pinned by a closed-form layer (permutation weights at
-  position 0) and by consistency (verify of L tokens == L decode steps; batch ==
+  position 0), by the q and k heads in closed form at later positions (permutation Wq
+  and Wk, distinct norm weights, power-of-two RoPE angles), and by consistency (verify of L tokens == L decode steps; batch ==
   independent sequences).  The pages print no whole-layer values.
 """
 from __future__ import annotations

@@ -1,6 +1,10 @@
 """Whole-layer pins of the oracle (CPU only).
 
 * a closed-form layer: permutation Q8_0 weights at position 0 with one visible key;
+* the q and k heads in closed form at a later position: distinct permutation Wq and Wk,
+  distinct q_norm / k_norm weights, RoPE angles that are exact powers of two applied as
+  complex rotations (so a swapped projection, a norm applied after RoPE, or RoPE left off
+  one of q and k all fail);
 * the verify block of L tokens equals L decode steps one after another;
 * a batch of sequences equals the sequences stepped one by one.
 """
@@ -55,6 +59,48 @@ def test_closed_form_layer_with_permutation_weights(orc, v_unit_norm):
     vc = r["v_cache"].reshape(2, 4, 16)
     assert np.array_equal(oracle.bf16_to_f64(vc[:, 0, :]), v_b)
     assert np.array_equal(vc[:, 1:, :], oracle.bf16_bits(kv["v_cache"]).reshape(2, 4, 16)[:, 1:, :])
+
+
+@pytest.mark.parametrize("P", [5, 77])
+def test_closed_form_q_and_k_heads_at_a_later_position(orc, P):
+    # theta = 2^8 with head_dim 16: inverse frequencies 256^(-2i/16) = 2^-i exactly, so the
+    # angle of pair i is P * 2^-i.  The rotation of the NeoX pair (u_i, u_{i+8}) is the
+    # complex product (u_i + j u_{i+8}) * e^{j phi_i}.
+    hd, nh, nkv, H = 16, 4, 2, 64
+    w = wl.Workload(name="qkpin", hidden=H, num_heads=nh, num_kv_heads=nkv, head_dim=hd,
+                    layer_type=wl.FULL, window=0, kv_capacity=P + 3, ring=False, batch=1,
+                    rope_theta=256.0, seed=31, seq_pos=P)
+    rng = np.random.default_rng(31)
+    pq = rng.permutation(H)             # Wq: 64 rows, each picks one input column
+    pk = rng.permutation(H)[:nkv * hd]  # Wk: 32 rows, a different choice of columns
+    weights = wl.make_weights(w)
+    weights["wq"] = _perm_q8_0(pq, H)
+    weights["wk"] = _perm_q8_0(pk, H)
+    w_q = weights["w_q"].to(torch.float64).numpy()
+    w_k = weights["w_k"].to(torch.float64).numpy()
+    assert np.min(np.abs(w_q - w_k)) > 0  # a swap of the two norm weights shows
+    x = wl.make_x(w)
+    kv = wl.make_kv_cache(w)
+    r = orc.decode_step(w, weights, x, [P], kv["k_cache"], kv["v_cache"])
+
+    xd = x.to(torch.float64).numpy()[0]
+    w_in = weights["w_in"].to(torch.float64).numpy()
+    n = xd * w_in / np.sqrt(np.mean(xd * xd) + w.eps)
+    rot = np.exp(1j * P * np.ldexp(1.0, -np.arange(hd // 2)))
+
+    def head(t, wn):
+        u = t * wn / np.sqrt(np.mean(t * t) + w.eps)  # per-head RMSNorm, then RoPE
+        z = (u[:hd // 2] + 1j * u[hd // 2:]) * rot
+        return np.concatenate([z.real, z.imag])
+
+    q = np.stack([head(n[pq[h * hd:(h + 1) * hd]], w_q) for h in range(nh)])
+    k = np.stack([head(n[pk[h * hd:(h + 1) * hd]], w_k) for h in range(nkv)])
+    assert np.max(np.abs(r["q"][0] - q)) <= 1e-13
+    assert np.max(np.abs(r["k"][0] - k)) <= 1e-13
+    # the key row lands at slot P as the bf16 rounding of k
+    kc = r["k_cache"].reshape(nkv, w.kv_capacity, hd)
+    kb = np.array([[oracle.f64_to_bf16(t) for t in row] for row in k], dtype=np.uint16)
+    assert np.array_equal(kc[:, P, :], kb)
 
 
 def test_verify_block_equals_sequential_decode_steps(orc):
