@@ -60,7 +60,8 @@ typedef enum { HFA_SLIDING = 0, HFA_FULL = 1 } hfa_layer_type;
                                    (Gemma global layers; model.rs, v_proj None when k_eq_v) */
 
 typedef struct {
-  int hidden;       /* H, multiple of 64 */
+  int hidden;       /* H: a multiple of 32 (whole Q8_0 blocks; HFA_EINVAL otherwise);
+                       multiples of 64 are supported (HFA_EUNSUPPORTED otherwise) */
   int num_heads;    /* query heads nh */
   int num_kv_heads; /* key/value heads nkv; nh % nkv == 0 and nh / nkv <= 8 */
   int head_dim;     /* hd in {64, 128, 256} */
@@ -146,7 +147,8 @@ hfa_status hfa_decode_step_host(hfa_layer* layer, void* stream, const void* x_ho
  * past the cache; HFA_EUNSUPPORTED for a ring cache, a Q8_0 layer (the block runs on
  * bf16 weights, HFA_F_WEIGHTS_BF16) or L * (nh / nkv) > 64 query rows per KV head.  At
  * create, max_verify_len > 16 and projection sizes that are not multiples of 128 rows
- * are HFA_EUNSUPPORTED.  The post-attention norm, RoPE frequency factors and
+ * are HFA_EUNSUPPORTED, and so is a cache of nkv * kv_capacity + 256 >= 2^31 rows (the
+ * kernels address it in 32-bit rows).  The post-attention norm, RoPE frequency factors and
  * HFA_F_K_EQ_V apply as in the decode step.
  */
 hfa_status hfa_verify_block(hfa_layer* layer, void* stream, const void* x_dev, int L,
@@ -193,7 +195,13 @@ hfa_status hfa_attention_decode(const hfa_attn_desc* desc, void* stream, const f
  * HFA_ERANGE.  The first call on each device looks up the array's address (make it
  * before any stream capture).  Each call clears the array's counters on `stream`; all
  * calls share the array, so calls that overlap on the GPU race and must not be issued.
- * Device-side wait timeouts of this variant are not reported.  Allocates nothing.
+ * Neither device-side condition that hfa_attention_decode records in its status word (a
+ * bounded wait that gave up, a position refused on the device, e.g. seq_pos_dev
+ * disagreeing with seq_pos_host) is reported by this variant: the next call clears the
+ * word, and the output of such a call is wrong without notice.  Callers that need that
+ * check use hfa_attention_decode and read word 0 of their workspace.  The cached address
+ * belongs to the device's context: after cudaDeviceReset (or any reset of the primary
+ * context) this entry point must not be called again in the process.  Allocates nothing.
  */
 hfa_status hfa_attention_decode_noalloc(const hfa_attn_desc* desc, void* stream,
                                         const float* q_dev, const int32_t* seq_pos_dev,

@@ -189,8 +189,11 @@ static bool is_pow2_hd(int hd) { return hd == 64 || hd == 128 || hd == 256; }
 
 static hfa_status validate_desc(const hfa_layer_desc* d) {
   if (!d) return fail(nullptr, HFA_EINVAL, "desc is NULL");
-  if (d->hidden <= 0 || d->hidden % 64 || d->hidden > 65536)
-    return fail(nullptr, HFA_EINVAL, "hidden=%d must be a positive multiple of 64, at most 65536",
+  if (d->hidden <= 0 || d->hidden % 32 || d->hidden > 65536)
+    return fail(nullptr, HFA_EINVAL, "hidden=%d must be a positive multiple of 32, at most 65536",
+                d->hidden);
+  if (d->hidden % 64)  // a valid Q8_0 row length (whole 32-value blocks) not covered here
+    return fail(nullptr, HFA_EUNSUPPORTED, "hidden=%d: only multiples of 64 are supported",
                 d->hidden);
   if (d->num_heads <= 0 || d->num_kv_heads <= 0 || d->num_heads % d->num_kv_heads)
     return fail(nullptr, HFA_EINVAL, "num_heads=%d must be a positive multiple of num_kv_heads=%d",
@@ -211,6 +214,9 @@ static hfa_status validate_desc(const hfa_layer_desc* d) {
     return fail(nullptr, HFA_EUNSUPPORTED, "max_batch=%d outside [1, 16]", d->max_batch);
   if (d->max_verify_len < 0 || d->max_verify_len > 16)
     return fail(nullptr, HFA_EUNSUPPORTED, "max_verify_len=%d outside [0, 16]", d->max_verify_len);
+  // the verify kernels address each cache as [nkv * C, hd] rows with 32-bit TMA rows
+  if (d->max_verify_len > 0 && (long long)d->num_kv_heads * d->kv_capacity + 256 >= (1ll << 31))
+    return fail(nullptr, HFA_EUNSUPPORTED, "verify: cache too large for 32-bit TMA rows");
   if (!(d->eps >= 0.f) || !(d->rope_theta > 0.f) || !(d->attn_scale > 0.f) || !(d->softcap >= 0.f))
     return fail(nullptr, HFA_EINVAL, "eps, rope_theta, attn_scale, softcap out of range");
   if (d->flags &
@@ -780,6 +786,8 @@ extern "C" hfa_status hfa_verify_block(hfa_layer* L, void* stream, const void* x
     return fail(L, HFA_EINVAL, "x, caches and out must be 16-byte aligned");
   if (!(d.flags & HFA_F_WEIGHTS_BF16))
     return fail(L, HFA_EUNSUPPORTED, "verify is built for bf16 weights");
+  if ((long long)d.num_kv_heads * d.kv_capacity + 256 >= (1ll << 31))
+    return fail(L, HFA_EUNSUPPORTED, "cache too large for 32-bit TMA rows");
   hfa::VerifyCall c{};
   c.d = &L->d;
   c.stream = (cudaStream_t)stream;

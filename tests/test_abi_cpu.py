@@ -32,7 +32,7 @@ def test_library_exports_every_declared_symbol(libhfa):
 def test_create_rejects_bad_descriptors_before_touching_a_device(libhfa):
     from quantized_attention_layer_gb300 import workloads as wl
     bad = [
-        dict(hidden=100),             # not a multiple of 64
+        dict(hidden=100),             # not a multiple of 32
         dict(head_dim=96),            # unsupported head_dim
         dict(num_kv_heads=3),         # nh % nkv != 0
         dict(max_batch=17),
@@ -49,6 +49,35 @@ def test_create_rejects_bad_descriptors_before_touching_a_device(libhfa):
         assert st in (hfa.HFA_EINVAL, hfa.HFA_EUNSUPPORTED), (kw, st)
         assert not h.value
         assert libhfa.hfa_last_error(None)
+
+
+def _create_status(libhfa, d):
+    h = ctypes.c_void_p()
+    dummy = ctypes.c_void_p(16)
+    st = libhfa.hfa_layer_create(ctypes.byref(d), dummy, dummy, dummy, dummy, dummy, dummy, dummy,
+                                 None, ctypes.byref(h))
+    assert not h.value
+    return st
+
+
+def test_hidden_statuses_follow_the_block_format(libhfa):
+    from quantized_attention_layer_gb300 import workloads as wl
+    d = hfa.desc_for(wl.TINY_SLIDING)
+    d.hidden = 100  # not whole 32-value blocks: an invalid layer
+    assert _create_status(libhfa, d) == hfa.HFA_EINVAL
+    d.hidden = 96   # whole Q8_0 blocks, but not a multiple of 64: valid, not covered
+    assert _create_status(libhfa, d) == hfa.HFA_EUNSUPPORTED
+    assert b"multiples of 64" in libhfa.hfa_last_error(None)
+
+
+def test_verify_refuses_caches_past_32_bit_rows(libhfa):
+    from quantized_attention_layer_gb300 import workloads as wl
+    d = hfa.desc_for(wl.VERIFY_L16)
+    d.num_kv_heads = 256
+    d.num_heads = 256
+    d.kv_capacity = (1 << 23) + 1  # 256 x (2^23 + 1) rows: past 2^31
+    assert _create_status(libhfa, d) == hfa.HFA_EUNSUPPORTED
+    assert b"32-bit" in libhfa.hfa_last_error(None)
 
 
 def test_ring_needs_capacity_equal_to_window(libhfa):

@@ -70,3 +70,21 @@ def test_noalloc_refuses_a_batch_beyond_its_static_scratch():
         hfa.hfa_attention_decode_noalloc(desc, q, torch.from_numpy(pos).cuda(), pos, kc, kc, o)
     assert e.value.status == hfa.HFA_ERANGE
     assert "static scratch" in str(e.value)
+
+
+def test_noalloc_allocates_nothing_after_its_first_call():
+    # the first call on a device looks up the static array (and may load the module that
+    # holds it); after that, free device memory must not move across calls
+    w = wl.FULL_32K.replace(kv_capacity=4096, seq_pos=4095)
+    desc = hfa.attn_desc_for(w)
+    pos = [4095]
+    q, posd, kc, vc = _inputs(w, pos, seed=7)
+    o = torch.empty_like(q)
+    hfa.hfa_attention_decode_noalloc(desc, q, posd, pos, kc, vc, o)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(3):
+        hfa.hfa_attention_decode_noalloc(desc, q, posd, pos, kc, vc, o)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert torch.isfinite(o).all()
