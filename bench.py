@@ -1,19 +1,27 @@
 """Benchmark of the single-token decode step of one attention layer on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload full_b1_32k] [--replicas R]
+                    [--workload full_b1_32k] [--replicas R] [--extra all|none|name,...]
 
 One step = one pass of the whole decode path (input norm + QKV + norms + RoPE + KV append
 -> flash-decode -> o_proj + residual) over one batch of the workload: one launch of the
-persistent decode-step kernel.  Every timed step
-runs on a different layer replica (distinct weights and caches in HBM, R replicas of
-~179 MB for the 32K full-attention layer), so the inputs of a step are never L2-resident:
-together they are far larger than the 129 MB L2.
+persistent decode-step kernel.  Every timed step runs on a different layer replica (distinct
+weights and caches in HBM, R replicas of ~179 MB for the 32K full-attention layer), so the
+inputs of a step are never L2-resident: together they are far larger than the 129 MB L2.
+The replicas are chained like the layers of a model (each step prefetches the next
+replica's first weights during its own tail).
 
-Printed (one JSON line, rank 0): steps/s for the whole job, ms per step, the roofline of
-the step kernel (algorithmic bytes of the step -- Q8_0 weights, visible K/V rows,
-activations -- over its CUDA-event duration, against the measured HBM copy bandwidth), the end-to-end rate through the host-buffer entry point,
-the CPU oracle baseline, SM clocks sampled during the timed region, and the launch count.
+Printed (one JSON line, rank 0): steps/s for the whole job on the headline workload (the
+32K full-attention layer at batch 1), ms per step, the roofline of the step kernel
+(algorithmic bytes of the step -- Q8_0 weights, visible K/V rows, activations -- over its
+CUDA-event duration, against the measured HBM copy bandwidth), the kernel's own duration
+from its device timer stamps, the end-to-end rate through the host-buffer entry point, the
+CPU oracle baseline, SM clocks sampled during the timed region, the launch count, and under
+"workloads" the same figures for the other four workloads (the tiny sliding layer, the
+batch-16 sliding ring, the 128K batch-4 layer with softcap, and the 16-token verify block).
+
+The K timed steps are one CUDA graph whose first and last nodes record the timing events,
+so the timed region is exactly the K steps on the device (no host launch latency).
 
 --impl reference times the CPU oracle (the plain fp64 implementation the tests check the
 library against) on the host cores, same workload, metric and unit.
@@ -24,6 +32,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import re
 import statistics
 import subprocess
@@ -40,6 +49,8 @@ import torch  # noqa: E402
 METRIC = "decode steps/sec per layer at 1 GB300; achieved HBM GB/s as % of peak"
 UNIT = "steps/s"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0
+EXTRA = ("tiny_sliding", "sliding_b16_ring1024", "full_b4_128k_softcap", "verify_l16_8k")
 
 
 def parse():
@@ -50,6 +61,8 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="full_b1_32k")
     p.add_argument("--replicas", type=int, default=8)
+    p.add_argument("--extra", default="all",
+                   help="other workloads measured in the same run: all, none, or names")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
 
@@ -91,10 +104,26 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def cpu_info():
+    """CPU model and logical core count of this host."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        m = re.search(r"Model name:\s*(.+)", out)
+        model = m.group(1).strip() if m else None
+    except Exception:
+        pass
+    if not model and os.path.exists("/proc/cpuinfo"):
+        m = re.search(r"model name\s*:\s*(.+)", open("/proc/cpuinfo").read())
+        model = m.group(1).strip() if m else None
+    return {"cpu_model": model or platform.processor() or platform.machine(),
+            "nproc": os.cpu_count()}
+
+
 def workload_bytes(w, pos):
     """Algorithmic bytes of one step: Q8_0 weights at 34/32 B per weight, the visible
     bf16 K and V rows, activations in and out, the appended K/V row."""
-    H, nh, nkv, hd = w.hidden, w.num_heads, w.num_kv_heads, w.head_dim
+    H, nkv, hd = w.hidden, w.num_kv_heads, w.head_dim
     wbytes = (w.q_rows + 2 * w.kv_rows) * H * 34 // 32 + H * w.q_rows * 34 // 32
     kv = 0
     for P in pos:
@@ -182,18 +211,32 @@ def ncu_traffic(kernel_file, summary_name):
 
 
 def cpu_baseline(w, weights, x, pos, kv, budget_s=15.0):
+    """The oracle on the host cores: all cores for ~2/3 of the budget, one core for the rest."""
     import oracle
     oracle.build()
-    n, t0 = 0, time.perf_counter()
-    while True:
-        oracle.decode_step(w, weights, x, pos, kv["k_cache"], kv["v_cache"])
-        n += 1
-        if time.perf_counter() - t0 >= budget_s:
-            break
-    dt = time.perf_counter() - t0
-    return {"value": n / dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+    all_threads = oracle.num_threads()
+
+    def rate(seconds):
+        n, t0 = 0, time.perf_counter()
+        while True:
+            oracle.decode_step(w, weights, x, pos, kv["k_cache"], kv["v_cache"])
+            n += 1
+            if time.perf_counter() - t0 >= seconds:
+                break
+        return n, time.perf_counter() - t0
+
+    n, dt = rate(budget_s * 2 / 3)
+    oracle.set_num_threads(1)
+    try:
+        n1, dt1 = rate(budget_s / 3)
+    finally:
+        oracle.set_num_threads(all_threads)
+    info = cpu_info()
+    return {"value": n / dt, "unit": UNIT, "cores": all_threads, "kind": "oracle",
             "sample": f"{n} full oracle decode steps of {w.name} (batch {len(pos)}), fp64, "
-                      f"{dt:.1f} s on the host cores"}
+                      f"{dt:.1f} s on {all_threads} threads; {n1} steps in {dt1:.1f} s on 1 thread",
+            "single_thread": {"value": n1 / dt1, "unit": UNIT, "cores": 1},
+            **info}
 
 
 def run_reference(args, rank, world):
@@ -213,7 +256,7 @@ def run_reference(args, rank, world):
     for _ in range(args.steps):
         oracle.decode_step(w, weights, x, pos, kv["k_cache"], kv["v_cache"])
     dt = time.perf_counter() - t0
-    value = args.steps * len(pos) / dt / len(pos)
+    value = args.steps / dt
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -223,30 +266,64 @@ def run_reference(args, rank, world):
                        "context": int(pos.max()) + 1, "weights": "q8_0"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
                              "kind": "oracle",
-                             "sample": f"{args.steps} full oracle decode steps of {w.name}"},
+                             "sample": f"{args.steps} full oracle decode steps of {w.name}",
+                             **cpu_info()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, rank, world, local):
-    from quantized_attention_layer_gb300 import build, hfa, workloads as wl
-    build.build()
-    assert torch.cuda.is_available(), "bench.py needs a CUDA device"
-    torch.cuda.set_device(local)
-    w = wl.BY_NAME[args.workload]
-    if w.verify_len:
-        return run_verify(args, rank, world, w)
+def timed_graph(stream, steps_fn, K):
+    """A CUDA graph of K steps whose first and last nodes record timing events (events made
+    with external=True become record nodes of the graph, replayed with it)."""
+    ev0 = torch.cuda.Event(enable_timing=True, external=True)
+    ev1 = torch.cuda.Event(enable_timing=True, external=True)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        ev0.record(stream)
+        steps_fn()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    return g, ev0, ev1
+
+
+def time_replays(graph, ev0, ev1, stream, world):
+    """Replays the graph under load for ~0.5 s, then times one replay between a barrier and a
+    synchronize on both sides; the sampler sees the same load.  Returns (ms, clocks)."""
+    with torch.cuda.stream(stream):
+        graph.replay()
+    torch.cuda.synchronize()
+    per_replay_s = max(ev0.elapsed_time(ev1) * 1e-3, 1e-5)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        with torch.cuda.stream(stream):
+            for _ in range(max(1, int(0.5 / per_replay_s))):
+                graph.replay()
+        barrier(world)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            graph.replay()
+        torch.cuda.synchronize()
+        ms = ev0.elapsed_time(ev1)
+        with torch.cuda.stream(stream):
+            for _ in range(max(1, int(0.2 / per_replay_s))):
+                graph.replay()
+        torch.cuda.synchronize()
+        barrier(world)
+    return max_over_ranks(ms, world), clk.summary()
+
+
+def decode_workload(w, K, W, R, world, want_cpu=False):
+    """Measures the decode step of workload `w`; returns the figures and the launch count."""
+    from quantized_attention_layer_gb300 import hfa, workloads as wl
     weights = wl.make_weights(w)
     x = wl.make_x(w)
     pos = wl.make_positions(w)
     kv = wl.make_kv_cache(w)
     B = len(pos)
     dev_w = hfa.weights_to_device(w, weights)
-    R = max(1, args.replicas)
     stream = torch.cuda.Stream()
     layers, caches = [], []
     with torch.cuda.stream(stream):
-        for r in range(R):
+        for _ in range(R):
             layers.append(hfa.Layer(hfa.desc_for(w), dev_w, stream=stream))
             caches.append((kv["k_cache"].cuda(), kv["v_cache"].cuda()))
     del dev_w
@@ -264,92 +341,55 @@ def run_ours(args, rank, world, local):
         kc, vc = caches[i % R]
         layers[i % R].hfa_decode_step(xd, posd, pos, kc, vc, out, stream=stream)
 
-    for i in range(max(3, args.warmup)):
+    for i in range(max(3, W)):
         step(i)
     torch.cuda.synchronize()
     for L in layers:
         L.hfa_check_device_status(stream=stream)
 
-    # the K timed steps as one CUDA graph (one kernel node per step, replicas rotated), so
-    # that the host's per-launch cost does not pace the GPU
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for i in range(args.steps):
+    def steps():
+        for i in range(K):
             step(i)
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    graph, ev0, ev1 = timed_graph(stream, steps, K)
+    ms, clocks = time_replays(graph, ev0, ev1, stream, world)
+    ms_per_step = ms / K
+    for L in layers:
+        L.hfa_check_device_status(stream=stream)
+    del graph
+
+    # the kernel's own duration from its timer stamps (a separate, untimed replay)
+    rows = layers[0].hfa_step_stamp_rows()
+    stamps = torch.zeros((K, rows, 16), dtype=torch.int64, device="cuda")
+
+    def stamped_steps():
+        for i in range(K):
+            L = layers[i % R]
+            L.hfa_set_step_stamps(stamps[i])
+            step(i)
+            L.hfa_set_step_stamps(None)
+
+    g2, e0, e1 = timed_graph(stream, stamped_steps, K)
     with torch.cuda.stream(stream):
-        ev0.record(stream)
-        graph.replay()  # one untimed replay, which also sizes the load around the timed one
-        ev1.record(stream)
+        g2.replay()
+        g2.replay()
     torch.cuda.synchronize()
-    per_replay_s = max(ev0.elapsed_time(ev1) * 1e-3, 1e-4)
+    del g2
+    s = stamps.cpu().numpy()
+    spans = (s[:, :, 9].max(1) - s[:, :, 13].min(1)) / 1e3  # exit - dependency wait, us
+    kernel_us = float(np.mean(spans[1:])) if K > 1 else float(spans[0])
 
-    # ---------------------------------------------------------------- timed region
-    # The clock sampler (nvidia-smi, 50 ms) sees the GPU under this same load: untimed
-    # replays of the graph run for ~0.5 s before the timed replay and ~0.2 s after it.
-    with ClockSampler(torch.cuda.current_device()) as clk:
-        with torch.cuda.stream(stream):
-            for _ in range(max(1, int(0.5 / per_replay_s))):
-                graph.replay()
-        barrier(world)
-        torch.cuda.synchronize()
-        with torch.cuda.stream(stream):
-            ev0.record(stream)
-            graph.replay()
-            ev1.record(stream)
-            for _ in range(max(1, int(0.2 / per_replay_s))):
-                graph.replay()
-        torch.cuda.synchronize()
-        barrier(world)
-    ms = ev0.elapsed_time(ev1)
-    ms = max_over_ranks(ms, world)
-    clocks = clk.summary()
-    ms_per_step = ms / args.steps
-    for L in layers:
-        L.hfa_check_device_status(stream=stream)
-
-    # the same steps launched one by one from the host (for reference)
-    torch.cuda.synchronize()
-    ev0.record(stream)
-    for i in range(args.steps):
-        step(i)
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    ms_direct = max_over_ranks(ev0.elapsed_time(ev1), world) / args.steps
-    value = world * B * args.steps / (ms / 1e3) / B  # steps/s over the whole job
-    for L in layers:
-        L.hfa_check_device_status(stream=stream)
-
-    # ---------------------------------------------------------------- per-kernel events
-    for L in layers:
-        L.hfa_set_kernel_timing(True)
-        L.hfa_kernel_times()
-    torch.cuda.synchronize()
-    for i in range(args.steps):
-        step(i)
-    torch.cuda.synchronize()
-    ktimes = {}
-    for L in layers:
-        for name, (kms, cnt) in L.hfa_kernel_times().items():
-            a = ktimes.setdefault(name, [0.0, 0])
-            a[0] += kms
-            a[1] += cnt
-        L.hfa_set_kernel_timing(False)
     wbytes, kvbytes, actbytes = workload_bytes(w, pos)
     peak, peak_src = measured_peaks()
     step_bytes = wbytes + kvbytes + actbytes
-    # one kernel per step: its average duration over the timed region is ms_per_step
-    k_avg_ms = ms_per_step
-    k_gbs = step_bytes / (k_avg_ms * 1e-3) / 1e9
-    traffic = ncu_traffic("k_step.cuh", f"decode_step_{w.name}.md")
-    roofline = {"bound": "hbm", "achieved": k_gbs, "peak": peak, "unit": "GB/s",
-                "frac": k_gbs / peak, "traffic": traffic, "kernel": "decode_step",
-                "algorithmic_bytes_per_launch": step_bytes, "peak_source": peak_src,
-                "duration": "timed region (CUDA graph) / K launches"}
-    kernels = {k: {"avg_us": v[0] / max(v[1], 1) * 1e3, "launches": v[1]} for k, v in ktimes.items()}
+    gbs = step_bytes / (ms_per_step * 1e-3) / 1e9
+    res = {"ms_per_step": ms_per_step, "steps_per_s": world * 1e3 / ms_per_step,
+           "step_bytes": step_bytes, "step_gbs": gbs, "frac": gbs / peak,
+           "frac_of_nominal": gbs / NOMINAL_HBM_GBS, "peak": peak, "peak_source": peak_src,
+           "kernel_us": kernel_us, "clocks": clocks, "launches": K, "batch": B,
+           "context": int(pos.max()) + 1, "successor_prefetch": R >= 2, "replicas": R}
 
-    # ---------------------------------------------------------------- end to end
+    # end to end: the host-buffer entry point (pinned input and output copies in every step)
     x_h = x.pin_memory()
     out_h = torch.empty((B, w.hidden), dtype=torch.bfloat16).pin_memory()
     for i in range(3):
@@ -357,50 +397,33 @@ def run_ours(args, rank, world, local):
         layers[i % R].hfa_decode_step_host(x_h, pos, kc, vc, out_h, stream=stream)
     barrier(world)
     t0 = time.perf_counter()
-    for i in range(args.steps):
+    for i in range(K):
         kc, vc = caches[i % R]
         layers[i % R].hfa_decode_step_host(x_h, pos, kc, vc, out_h, stream=stream)
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
-    e2e = {"value": world * args.steps / e2e_s, "unit": UNIT,
-           "h2d_bytes_per_step": B * w.hidden * 2 + B * 4, "d2h_bytes_per_step": B * w.hidden * 2}
-
-    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": w.name, "batch": B, "hidden": w.hidden,
-                       "heads": f"{w.num_heads}/{w.num_kv_heads}", "head_dim": w.head_dim,
-                       "context": int(pos.max()) + 1, "weights": "q8_0",
-                       "kv": "bf16", "parallelism": f"replicas x{world}",
-                       "l2": f"inputs larger than L2: {R} layer replicas rotated, "
-                             f"{R * step_bytes / 1e9:.2f} GB"},
-            "timing": "CUDA graph of the K steps; ms_per_step_direct = host launches",
-            "successor_prefetch": R >= 2,
-            "ms_per_step_direct": ms_direct,
-            "step_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
-            "step_frac_of_peak": step_bytes / (ms_per_step * 1e-3) / 1e9 / peak,
-            "step_bytes": step_bytes,
-            "roofline": roofline, "kernels": kernels, "e2e": e2e, "clocks": clocks,
-            "gpu_launches": sum(v[1] for v in ktimes.values())}
-    if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, weights, x, pos, kv)
+    res["e2e"] = {"value": world * K / e2e_s, "unit": UNIT,
+                  "h2d_bytes_per_step": B * w.hidden * 2 + B * 4, "d2h_bytes_per_step": B * w.hidden * 2}
+    if want_cpu:
+        res["cpu_inputs"] = (weights, x, pos, kv)
     for L in layers:
+        L.hfa_check_device_status(stream=stream)
         L.hfa_set_successor(None)
     for L in layers:
         L.hfa_destroy()
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    del caches
+    torch.cuda.empty_cache()
+    return res
 
 
-def run_verify(args, rank, world, w):
+def verify_workload(w, K, W, R, world):
     """The multi-token verify block (L tokens through one layer, bf16 weights): blocks/s,
-    and the roofline of its QKV projection (tcgen05 GEMM) against HBM and tensor peaks."""
+    and the roofline of its QKV projection (tcgen05 GEMM)."""
     from quantized_attention_layer_gb300 import hfa, workloads as wl
     weights = wl.make_weights(w)
     x = wl.make_x(w)
     kv = wl.make_kv_cache(w)
     L, base = w.verify_len, w.base_pos
     dev_w = hfa.weights_to_device(w, weights)
-    R = max(1, args.replicas)
     stream = torch.cuda.Stream()
     layers, caches = [], []
     with torch.cuda.stream(stream):
@@ -416,25 +439,22 @@ def run_verify(args, rank, world, w):
         kc, vc = caches[i % R]
         layers[i % R].hfa_verify_block(xd, base, kc, vc, out, stream=stream)
 
-    for i in range(max(3, args.warmup)):
+    for i in range(max(3, W)):
         step(i)
     torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(torch.cuda.current_device()) as clk:
-        barrier(world)
-        torch.cuda.synchronize()
-        ev0.record(stream)
-        for i in range(args.steps):
+
+    def steps():
+        for i in range(K):
             step(i)
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        barrier(world)
-    ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+
+    graph, ev0, ev1 = timed_graph(stream, steps, K)
+    ms, clocks = time_replays(graph, ev0, ev1, stream, world)
+    del graph
     for Lr in layers:
         Lr.hfa_check_device_status(stream=stream)
         Lr.hfa_set_kernel_timing(True)
         Lr.hfa_kernel_times()
-    for i in range(args.steps):
+    for i in range(K):
         step(i)
     torch.cuda.synchronize()
     kt = {}
@@ -453,24 +473,96 @@ def run_verify(args, rank, world, w):
     g = kt.get("verify_qkv_gemm", [float("nan"), 1])
     g_us = g[0] / max(g[1], 1) * 1e3
     flops = 2.0 * L * (qr + 2 * kr) * H
-    line = {"metric": "verify blocks/sec per layer (L tokens, bf16 weights)", "value": world * args.steps / (ms / 1e3),
-            "unit": "blocks/s", "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup),
-            "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": w.name, "tokens": L, "prior": base, "hidden": H,
-                       "heads": f"{w.num_heads}/{w.num_kv_heads}", "head_dim": w.head_dim,
-                       "weights": "bf16", "l2": f"{R} layer replicas rotated"},
-            "step_gbs": step_bytes / (ms / args.steps * 1e-3) / 1e9,
-            "step_bytes": step_bytes,
-            "roofline": {"bound": "hbm", "kernel": "verify_qkv_gemm", "achieved": wqkv_bytes / (g_us * 1e-6) / 1e9,
-                         "peak": peak, "unit": "GB/s", "frac": wqkv_bytes / (g_us * 1e-6) / 1e9 / peak,
-                         "traffic": ncu_traffic("k_verify.cu", f"verify_block_{w.name}.md"),
-                         "useful_tflops": flops / (g_us * 1e-6) / 1e12,
-                         "peak_source": src},
-            "kernels": {k: {"avg_us": v[0] / max(v[1], 1) * 1e3, "launches": v[1]} for k, v in kt.items()},
-            "clocks": clk.summary(), "gpu_launches": sum(v[1] for v in kt.values())}
+    ms_per_step = ms / K
+    res = {"ms_per_step": ms_per_step, "blocks_per_s": world * 1e3 / ms_per_step,
+           "step_bytes": step_bytes, "step_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
+           "frac": step_bytes / (ms_per_step * 1e-3) / 1e9 / peak, "tokens": L, "prior": base,
+           "qkv_gemm": {"avg_us": g_us, "gbs": wqkv_bytes / (g_us * 1e-6) / 1e9,
+                        "frac": wqkv_bytes / (g_us * 1e-6) / 1e9 / peak,
+                        "useful_tflops": flops / (g_us * 1e-6) / 1e12,
+                        "traffic": ncu_traffic("k_verify.cu", f"verify_block_{w.name}.md")},
+           "kernels": {k: {"avg_us": v[0] / max(v[1], 1) * 1e3, "launches": v[1],
+                           "timing": "events around each host-launched kernel (no overlap)"}
+                       for k, v in kt.items()},
+           "clocks": clocks, "launches": 5 * K, "peak": peak, "peak_source": src}
     for Lr in layers:
         Lr.hfa_destroy()
+    del caches
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args, rank, world, local):
+    from quantized_attention_layer_gb300 import build, workloads as wl
+    build.build()
+    assert torch.cuda.is_available(), "bench.py needs a CUDA device"
+    torch.cuda.set_device(local)
+    w = wl.BY_NAME[args.workload]
+    K, W = args.steps, max(3, args.warmup)
+    if w.verify_len:
+        r = verify_workload(w, K, W, max(1, args.replicas), world)
+        line = {"metric": "verify blocks/sec per layer (L tokens, bf16 weights)", "value": r["blocks_per_s"],
+                "unit": "blocks/s", "n_gpus": world, "steps": K, "warmup": W,
+                "ms_per_step": r["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": {"workload": w.name, "tokens": w.verify_len, "prior": w.base_pos},
+                **{k: v for k, v in r.items() if k not in ("ms_per_step", "blocks_per_s")}}
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return
+
+    R = max(1, args.replicas)
+    main = decode_workload(w, K, W, R, world, want_cpu=rank == 0 and not args.no_cpu_baseline)
+    cpu_inputs = main.pop("cpu_inputs", None)
+    roofline = {"bound": "hbm", "achieved": main["step_gbs"], "peak": main["peak"], "unit": "GB/s",
+                "frac": main["frac"], "frac_of_nominal_8tbs": main["frac_of_nominal"],
+                "traffic": ncu_traffic("k_step.cuh", f"decode_step_{w.name}.md"),
+                "kernel": "decode_step", "algorithmic_bytes_per_launch": main["step_bytes"],
+                "peak_source": main["peak_source"],
+                "duration": "CUDA events around the K steps on the device (first and last graph "
+                            "nodes) / K launches"}
+    line = {"metric": METRIC, "value": main["steps_per_s"], "unit": UNIT, "n_gpus": world,
+            "steps": K, "warmup": W, "ms_per_step": main["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "batch": main["batch"], "hidden": w.hidden,
+                       "heads": f"{w.num_heads}/{w.num_kv_heads}", "head_dim": w.head_dim,
+                       "context": main["context"], "weights": "q8_0", "kv": "bf16",
+                       "parallelism": f"replicas x{world}",
+                       "l2": f"inputs larger than L2: {R} layer replicas rotated, "
+                             f"{R * main['step_bytes'] / 1e9:.2f} GB"},
+            "timing": "one CUDA graph of the K steps, timing events recorded by its first and "
+                      "last nodes; kernel duration from the kernel's own timer stamps",
+            "successor_prefetch": main["successor_prefetch"],
+            "step_gbs": main["step_gbs"], "step_frac_of_peak": main["frac"],
+            "step_bytes": main["step_bytes"], "roofline": roofline,
+            "kernels": {"decode_step": {"avg_us": main["kernel_us"], "launches": K,
+                                        "source": "device timer stamps: last CTA end - "
+                                                  "dependency wait, mean over the K steps"}},
+            "e2e": main["e2e"], "clocks": main["clocks"]}
+    extra = EXTRA if args.extra == "all" else (() if args.extra == "none" else
+                                               tuple(n for n in args.extra.split(",") if n))
+    wls = {}
+    for name in extra:
+        if name == w.name:
+            continue
+        we = wl.BY_NAME[name]
+        if we.verify_len:
+            r = verify_workload(we, K, W, 2, world)
+            wls[name] = {"unit": "blocks/s", "value": r["blocks_per_s"], "ms_per_step": r["ms_per_step"],
+                         "step_bytes": r["step_bytes"], "frac": r["frac"], "qkv_gemm": r["qkv_gemm"],
+                         "kernels": r["kernels"], "clocks": r["clocks"]}
+        else:
+            Re = 2 if we.batch >= 4 else R  # the 128K batch-4 layer holds 2.2 GB of K/V per replica
+            r = decode_workload(we, K, W, Re, world)
+            wls[name] = {"unit": UNIT, "value": r["steps_per_s"], "ms_per_step": r["ms_per_step"],
+                         "step_bytes": r["step_bytes"], "frac": r["frac"], "kernel_us": r["kernel_us"],
+                         "e2e": r["e2e"], "replicas": Re, "clocks": r["clocks"]}
+    if wls:
+        line["workloads"] = wls
+    line["gpu_launches"] = K  # one decode-step kernel per timed step
+    if cpu_inputs is not None:
+        weights, x, pos, kv = cpu_inputs
+        line["cpu_baseline"] = cpu_baseline(w, weights, x, pos, kv)
     if rank == 0:
         print(json.dumps(line), flush=True)
 

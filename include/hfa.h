@@ -115,7 +115,10 @@ hfa_status hfa_layer_create(const hfa_layer_desc* desc, const void* wq_dev, cons
  * The cache must hold the earlier positions of each sequence: positions
  * max(0, P-W+1) .. P-1 (sliding) or 0 .. P-1 (full).
  * The step is one cooperative launch of one CTA per SM; it fails with HFA_ECUDA when the
- * device cannot hold that grid at once (e.g. SMs taken by another context).  Steps on
+ * device cannot hold that grid at once (e.g. SMs taken by another context).  It is
+ * launched with programmatic dependent launch: it may start while the previous kernel on
+ * `stream` finishes, reads nothing but the layer's own weights until that kernel has
+ * completed, and lets the next kernel on `stream` start the same way.  Steps on
  * one layer handle must not overlap on the GPU (they share the layer's scratch).
  */
 hfa_status hfa_decode_step(hfa_layer* layer, void* stream, const void* x_dev,
@@ -220,6 +223,26 @@ hfa_status hfa_attention_decode_noalloc(const hfa_attn_desc* desc, void* stream,
  * Errors: HFA_EINVAL (shapes differ, bf16 weights, NULL layer).
  */
 hfa_status hfa_set_successor(hfa_layer* layer, const hfa_layer* next);
+
+/*
+ * Instrumentation of the decode step (no counterpart on the pages): with a buffer set,
+ * every later decode step of `layer` writes, per CTA c (one CTA per SM), the GPU's
+ * nanosecond timer (%globaltimer) at fixed points into stamps_dev[c * 16 + k]:
+ *   k = 0 CTA start, 1 activations loaded, 2 QKV projection done, 3 first queries ready,
+ *   4 last key tile consumed, 5 attention records written, 6 grid barrier passed,
+ *   7 o_proj operand merged, 8 o_proj done, 9 residual written (CTA end);
+ *   10 first QKV copy issued, 11 last key tile issued, 12 o_proj copies issued,
+ *   13 the wait for the previous kernel on the stream returned.
+ * Slots 14 and 15 are unused.  A step may start (slot 0) while the previous kernel on the
+ * stream is still finishing (programmatic dependent launch); from slot 13 on it runs alone.
+ * max over c of slot 9 minus min over c of slot 13 is the kernel's own duration.  Results
+ * are unchanged; the stores cost a few instructions.
+ *   stamps_dev  u64 device buffer of hfa_step_stamp_rows(layer) * 16 entries, 8-byte
+ *               aligned, owned by the caller; NULL turns the stamps off.
+ * Errors: HFA_EINVAL (NULL layer, misaligned buffer).
+ */
+hfa_status hfa_set_step_stamps(hfa_layer* layer, unsigned long long* stamps_dev);
+int hfa_step_stamp_rows(const hfa_layer* layer); /* CTAs of a step: rows of the stamp buffer */
 
 /*
  * Test hook for the failure path: in the next decode step of `layer`, the consumer warps

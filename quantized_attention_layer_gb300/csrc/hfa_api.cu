@@ -54,6 +54,7 @@ struct hfa_layer {
   uint8_t* wo_t = nullptr;
   StepGemv g_qkv{}, g_o{};
   const uint8_t* successor_qkv = nullptr;  // QKV tiles of the layer that runs next
+  unsigned long long* stamps = nullptr;     // caller's [SMs][16] timer stamps, or NULL
   int stall_next = 0;  // test hook (hfa_debug_stall_next_step), one step
   __nv_bfloat16* wqkv_bf16 = nullptr;  // verify path: [(nh + 2 nkv) hd, H] as 128 x 64 tiles
   __nv_bfloat16* wo_bf16 = nullptr;    // [H, nh hd] as 128 x 64 tiles
@@ -473,6 +474,16 @@ extern "C" hfa_status hfa_set_post_norm(hfa_layer* L, const float* w_post, void*
   return HFA_OK;
 }
 
+extern "C" hfa_status hfa_set_step_stamps(hfa_layer* L, unsigned long long* stamps) {
+  if (!L) return HFA_EINVAL;
+  if (stamps && ((uintptr_t)stamps & 7))
+    return fail(L, HFA_EINVAL, "the stamp buffer must be 8-byte aligned");
+  L->stamps = stamps;
+  return HFA_OK;
+}
+
+extern "C" int hfa_step_stamp_rows(const hfa_layer* L) { return L ? L->num_sms : 0; }
+
 extern "C" hfa_status hfa_debug_stall_next_step(hfa_layer* L) {
   if (!L) return HFA_EINVAL;
   L->stall_next = 1;
@@ -611,6 +622,7 @@ extern "C" hfa_status hfa_decode_step(hfa_layer* L, void* stream, const void* x,
   sa.stall = L->stall_next;
   sa.w_post = L->w_post_on ? L->w_post : nullptr;
   sa.post_part = L->post_part;
+  sa.stamps = L->stamps;
   sa.k_eq_v = (d.flags & HFA_F_K_EQ_V) ? 1 : 0;
   L->stall_next = 0;
   sa.B = batch;

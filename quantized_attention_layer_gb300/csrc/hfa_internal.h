@@ -110,6 +110,7 @@ struct StepArgs {
   int stall;               // test hook: CTA 0's consumers wait on a barrier nothing completes
   const float* w_post;     // nullable f32 [H]: post-attention RMSNorm of the o_proj output
   unsigned long long* post_part;  // [grid][2] tagged partial sum(y^2) (with w_post)
+  unsigned long long* stamps;  // nullable [grid][16]: %globaltimer at fixed points (see kStamp*)
   int B, H, nh, nkv, C, sliding, window, ring, v_unit_norm;
   int k_eq_v;              // no V rows: the K job also writes V = unit RMSNorm of raw K
   long long cache_rows;    // B * nkv * C: rows of the [rows, hd] view of each cache

@@ -42,9 +42,38 @@ constexpr int kSmallBytes = 1024;         // barriers, flags, per-row values
 constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kUnionBytes + kSmallBytes;
 constexpr int kKeysPerWarp = 16;
 constexpr int kMaxBatch = 16;
-constexpr int kEarlyTiles = 2;            // K/V tiles prefetched into L2 during phase A
+// K/V tiles prefetched into L2 during phase A, and the most K/V tiles brought into the ring
+// before the queries of the first unit are formed (0: no limit).  With one batch tile the
+// head epilogue's loads of the QKV partial sums would otherwise queue behind the ring fill;
+// with more batch tiles phase A is long enough that the fill is over before they are issued.
+template <int NT> struct Fill {
+  static constexpr int kEarlyTiles = NT == 1 ? 3 : 2;
+  static constexpr int kBeforeQueries = NT == 1 ? 2 : 0;
+};
 constexpr uint32_t kSuccChunk = 16384;    // next layer's weights: L2 prefetch chunk ...
 constexpr unsigned kSuccPauseNs = 400;    // ... and the pause after each
+
+// Instrumentation (hfa_set_step_stamps): with a stamp buffer set, thread 0 of each CTA and
+// the producer's lane 0 record %globaltimer at these points of every step.
+enum {
+  kStampEntry = 0,   // CTA start, barriers initialised
+  kStampOperand,     // phase A operand built (activations loaded)
+  kStampGemvA,       // phase A GEMV done
+  kStampAttn,        // first key tile's queries ready
+  kStampStream,      // last key tile consumed
+  kStampRecords,     // attention records written
+  kStampBarrier,     // grid barrier passed
+  kStampMerge,       // o_proj operand merged
+  kStampGemvC,       // o_proj GEMV done
+  kStampExit,        // residual written
+  kStampProdA,       // producer: first QKV copy issued
+  kStampProdKV,      // producer: last key tile issued
+  kStampProdC,       // producer: o_proj copies issued
+  kStampWait,        // the wait for the previous kernel on the stream returned
+  kStampSlots = 16
+};
+#define HFA_STAMP(a, k) \
+  do { if ((a).stamps) (a).stamps[blockIdx.x * kStampSlots + (k)] = globaltimer_ns(); } while (0)
 
 // per batch row: position, visible slots [lo, hi], key tiles, tile of the new slot, slot
 enum { kGeoP = 0, kGeoLo, kGeoHi, kGeoNt, kGeoTn, kGeoSlot, kGeoPre, kGeoInts = 8 };
@@ -548,7 +577,7 @@ static __device__ __noinline__ void finish_outputs_post(const StepArgs& a, int c
 // `part`, times the batch row's factor `scale` (nullable: 1).  One out-of-line copy serves both GEMVs, so
 // the o_proj phase runs code the QKV phase already brought into the instruction cache;
 // the stage and the operand fragments come as shared-window addresses (ld.shared).
-template <int NT>
+template <int NT, int UNR = 4>
 __device__ __noinline__ void gemv_stage(const StepGemv& gm, int B, unsigned long long* part,
                                         int s, uint32_t stage, int n_items, int r_first,
                                         uint32_t frag, const float* scale, uint32_t tag, int warp,
@@ -563,7 +592,7 @@ __device__ __noinline__ void gemv_stage(const StepGemv& gm, int B, unsigned long
     for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
     const uint32_t tp = stage + (uint32_t)(item * nbs * kQ8TileBytes);
     const uint32_t fr = frag + lane * 16;
-#pragma unroll 4
+#pragma unroll UNR
     for (int i = 0; i < nbs; ++i) {
       const uint4 w = lds128(tp + i * kQ8TileBytes + lane * 16);
       const uint32_t d = lds32(tp + i * kQ8TileBytes + 512 + g * 4);
@@ -616,6 +645,17 @@ __device__ void head_job(const StepArgs& a, const int* geo, int b, int kvh, int 
   constexpr int kSG = 8;
   const unsigned long long* src = a.qkv_part + (size_t)b * rows + row0 + lane;
   const size_t split_stride = (size_t)a.B * rows;
+  // the per-head norm weight and the RoPE angles are constants: loaded before the wait for
+  // the partial sums, so that no dependent global load follows it
+  float wn[J];
+  float2 rg[J / 2];
+  {
+    const float* w = kind == 0 ? a.w_q : a.w_k;  // a valid address for v too (unused)
+#pragma unroll
+    for (int j = 0; j < J; ++j) wn[j] = __ldg(w + lane + 32 * j);
+#pragma unroll
+    for (int j = 0; j < J / 2; ++j) rg[j] = __ldg(a.rope_g + lane + 32 * j);
+  }
   float v[J];
 #pragma unroll
   for (int j = 0; j < J; ++j) v[j] = 0.f;
@@ -673,18 +713,14 @@ __device__ void head_job(const StepArgs& a, const int* geo, int b, int kvh, int 
     for (int j = 0; j < J; ++j) ss += v[j] * v[j];
     ss = warp_sum(ss);
     const float inv = rsqrtf(ss / HD + a.eps);
-    const float* w = kind == 0 ? a.w_q : a.w_k;  // a valid address for v too (unused)
 #pragma unroll
-    for (int j = 0; j < J; ++j) {
-      const float wj = __ldg(w + lane + 32 * j);
-      v[j] *= inv * (kind < 2 ? wj : 1.0f);
-    }
+    for (int j = 0; j < J; ++j) v[j] *= inv * (kind < 2 ? wn[j] : 1.0f);
   }
   if (kind < 2) {
     const int P = geo[b * kGeoInts + kGeoP];
 #pragma unroll
     for (int j = 0; j < J / 2; ++j) {
-      const float2 r = rope_rotate(P, a.rope_g[lane + 32 * j], v[j], v[j + J / 2]);
+      const float2 r = rope_rotate(P, rg[j], v[j], v[j + J / 2]);
       v[j] = r.x;
       v[j + J / 2] = r.y;
     }
@@ -1028,6 +1064,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* next_bar = append_bar + 1;  // consumers passed the grid barrier
   uint64_t* arrived_bar = reinterpret_cast<uint64_t*>(small + 88);  // ... arrived at it
   uint64_t* stall_bar = reinterpret_cast<uint64_t*>(small + 288);  // test hook: never completes
+  uint64_t* polled_bar = reinterpret_cast<uint64_t*>(small + 296);  // first queries formed
   volatile int* s_abort = reinterpret_cast<volatile int*>(small + 64);
   int* s_issued = reinterpret_cast<int*>(small + 68);
   uint32_t* s_tag = reinterpret_cast<uint32_t*>(small + 72);  // this step's partial-sum tag
@@ -1051,12 +1088,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(next_bar, 1);
     mbar_init(arrived_bar, 1);
     mbar_init(stall_bar, 1);
+    mbar_init(polled_bar, 1);
     *s_abort = 0;
     *s_issued = 0;
     fence_barrier_init();
   }
   if (tid < kMaxBatch) s_max[tid] = 0u;
   __syncthreads();
+  if (tid == 0) HFA_STAMP(a, kStampEntry);
+  // Programmatic dependent launch: the next kernel on the stream may be scheduled now (its
+  // CTAs take over the SMs as these exit).  Nothing this kernel reads or writes in global
+  // memory is touched before the wait for the previous kernel, except what no kernel
+  // writes: the weights, loaded here into the first ring stages with a single batch tile
+  // (with more, the activation loads would queue behind them).
+  constexpr bool early_qkv = NT == 1;
+  {
+    pdl_launch_dependents();
+    if (early_qkv && warp == kCW && lane == 0) {
+      const Slice sa0 = gemv_slice(a.qkv, c, nctas);
+      const int nA0 = (sa0.r1 - sa0.r0 + a.qkv.ips - 1) / a.qkv.ips;
+      for (int k = 0; k < nA0 && k < kStages; ++k) {
+        const int r = sa0.r0 + k * a.qkv.ips;
+        const int n = a.qkv.ips < sa0.r1 - r ? a.qkv.ips : sa0.r1 - r;
+        const uint32_t bytes = (uint32_t)(n * a.qkv.nbs * kQ8TileBytes);
+        mbar_arrive_expect_tx(&full[k], bytes);
+        bulk_load(ring + k * kStageBytes, a.qkv.w + ((size_t)sa0.s * a.qkv.R + r) * a.qkv.nbs * kQ8TileBytes,
+                  bytes, &full[k]);
+      }
+      prefetch_tmap(&tmk);
+      prefetch_tmap(&tmv);
+    }
+    pdl_wait();
+    if (tid == 0) HFA_STAMP(a, kStampWait);
+  }
 
   const int G = a.nh / a.nkv;
   if (warp == kCW) {
@@ -1096,9 +1160,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // hold their activations (barrier 3), whose loads would otherwise queue behind them
     asm volatile("bar.sync 3, %0;" ::"n"(kThreads) : "memory");
     if (lane == 0) {
-      for (int k = 0; k < sc.nA && k < kStages && ok; ++k) issue_gemv(a.qkv, sc.sa, k);
-      prefetch_tmap(&tmk);
-      prefetch_tmap(&tmv);
+      if (early_qkv) {
+        q = (uint32_t)(sc.nA < kStages ? sc.nA : kStages);  // issued before the wait
+      } else {
+        for (int k = 0; k < sc.nA && k < kStages && ok; ++k) issue_gemv(a.qkv, sc.sa, k);
+        prefetch_tmap(&tmk);
+        prefetch_tmap(&tmv);
+      }
+      HFA_STAMP(a, kStampProdA);
     }
     __syncwarp();
     // visible slots and key tiles of each sequence, for both sides (consumers read them
@@ -1144,7 +1213,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       sc.nB = sc.t1 - sc.t0;
     }
     if (lane == 0)
-      for (int j = 0; j < kEarlyTiles && j < sc.nB; ++j) prefetch_load<HD>(a, sc, geo, sc.nA + j);
+      for (int j = 0; j < Fill<NT>::kEarlyTiles && j < sc.nB; ++j)
+        prefetch_load<HD>(a, sc, geo, sc.nA + j);
     // while the consumers run phase A: sum(x^2) of the input rows whose key tiles this CTA
     // attends over (the input norm's statistic, read in phase B)
     {
@@ -1164,6 +1234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t n_app = 0;  // appends waited for (one per unit whose new slot is here)
       const uint64_t kv_policy = l2_policy_evict_first();  // the cache is read once a step
       for (int k = (int)q; k < sc.nA && ok; ++k) issue_gemv(a.qkv, sc.sa, k);
+      int kv_issued = 0;  // K/V tiles issued so far (for the fill limit)
       for_each_segment(geo, a.B, a.nkv, sc.t0, sc.t1, [&](int b, int kvh, int lt0, int lt1) {
         const int lo = geo[b * kGeoInts + kGeoLo], tn = geo[b * kGeoInts + kGeoTn];
         const bool owner = tn >= lt0 && tn < lt1;
@@ -1179,6 +1250,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++n_app;
           }
+          if (Fill<NT>::kBeforeQueries > 0 && kv_issued == Fill<NT>::kBeforeQueries &&
+              !mbar_wait(polled_bar, 0, a.err, s_abort)) {
+            ok = false;
+            break;
+          }
+          ++kv_issued;
           const int st = acquire(AC::STAGE_BYTES);
           if (st < 0) {
             ok = false;
@@ -1197,8 +1274,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       });
       // the o_proj slice goes out once the consumers have arrived at the grid barrier: the
       // arrival's release waits for this SM's copies in flight, so they come after it
+      HFA_STAMP(a, kStampProdKV);
       if (sc.nC > 0 && ok && !mbar_wait(arrived_bar, 0, a.err, s_abort)) ok = false;
       for (int k = 0; k < sc.nC && ok; ++k) issue_gemv(a.o, sc.so, k);
+      HFA_STAMP(a, kStampProdC);
       *s_issued = (int)q;
       // the layer that runs next: its first loads (this CTA's QKV slice, same shape) go to
       // L2 once the attention is over, while the o_proj phase leaves HBM idle; paced, so
@@ -1235,6 +1314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Slice sl = gemv_slice(a.qkv, c, nctas);
       build_x_operand<NT>(a, sl.s, reinterpret_cast<uint32_t*>(uni), s_max, s_inv, arrivals0,
                           s_gbase, s_tag);
+      if (tid == 0) HFA_STAMP(a, kStampOperand);
       const uint32_t tag = *s_tag;
       // test hook of the failure path: a bounded wait that runs out
       if (a.stall && c == 0 && !mbar_wait(stall_bar, 0, a.err, s_abort)) *s_abort = 1;
@@ -1247,6 +1327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         release_stage();
       }
     }
+    if (tid == 0) HFA_STAMP(a, kStampGemvA);
     asm volatile("bar.sync 2, %0;" ::"n"(kThreads) : "memory");  // geometry, statistics
     int Nt = 0;
     for (int b = 0; b < a.B; ++b) Nt += geo[b * kGeoInts + kGeoNt] * a.nkv;
@@ -1259,6 +1340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* q_s = reinterpret_cast<float*>(uni + AC::QS_OFF);
       float* red = reinterpret_cast<float*>(uni);  // [key group][8][RS] after the last tile
       const uint32_t ring_base = smem_u32(ring);
+      bool first_segment = true;  // stamps: queries of the CTA's first segment ready
       for_each_segment(geo, a.B, a.nkv, t0, t1, [&](int b, int kvh, int lt0, int lt1) {
         const int* gb = geo + b * kGeoInts;
         const int lo = gb[kGeoLo], hi = gb[kGeoHi], tn = gb[kGeoTn];
@@ -1269,6 +1351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           head_job<HD>(a, geo, b, kvh, job, G, s_xss[b], q_s, lt0 == 0 && a.q_tap != nullptr,
                        *s_tag, s_abort, lane);
         consumer_sync();
+        if (tid == 0 && first_segment) mbar_arrive(polled_bar);
         if (owner && tid == 0) mbar_arrive(append_bar);
         // query fragments: rows 0..G-1 = hi(q * qscale), rows 8..8+G-1 = lo
         {
@@ -1291,6 +1374,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         consumer_sync();
+        if (tid == 0 && first_segment) HFA_STAMP(a, kStampAttn);
+        first_segment = false;
         const int kg = warp % AC::NC, dh = warp / AC::NC;  // key group, dim part
         float m = -INFINITY, l = 0.f;
         float o[AC::NTW][4];
@@ -1304,6 +1389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           m, l, o, kg, dh, lane);
           release_stage();
         }
+        if (tid == 0) HFA_STAMP(a, kStampStream);
         l += __shfl_xor_sync(0xffffffffu, l, 1);
         l += __shfl_xor_sync(0xffffffffu, l, 2);
         // combine the warps of this CTA into the unit's record of this CTA
@@ -1362,17 +1448,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     const Slice sl = gemv_slice(a.o, c, nctas);
+    if (tid == 0) HFA_STAMP(a, kStampRecords);
     grid_arrive(a.gbar);
     if (tid == 0) mbar_arrive(arrived_bar);
     build_unit_table<HD>(a, geo, Nt, G, sl.s,
                          reinterpret_cast<unsigned*>(uni + kOperandBytes));  // while waiting
     grid_wait(a.gbar, *s_gbase + (unsigned long long)nctas, a.err, s_abort);
+    if (tid == 0) HFA_STAMP(a, kStampBarrier);
     if (a.next_qkv_w && tid == 0) mbar_arrive(next_bar);
 
     // ---------------------------------------------------------- C: o_proj + residual
     {
       merge_operand<HD, NT>(a, G, sl.s, sl.first, reinterpret_cast<uint32_t*>(uni));
       consumer_sync();
+      if (tid == 0) HFA_STAMP(a, kStampMerge);
       for (int r = sl.r0; r < sl.r1; r += a.o.ips) {
         const int n = a.o.ips < sl.r1 - r ? a.o.ips : sl.r1 - r;
         const int st = wait_stage();
@@ -1383,11 +1472,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     consumer_sync();  // the union (operand) is free for the epilogue
+    if (tid == 0) HFA_STAMP(a, kStampGemvC);
     if (a.w_post)
       finish_outputs_post(a, c, nctas, reinterpret_cast<float*>(uni),
                           reinterpret_cast<float*>(ring), *s_tag, s_abort);
     else
       finish_outputs(a, c, nctas, reinterpret_cast<float*>(uni), *s_tag, s_abort);
+    if (tid == 0) HFA_STAMP(a, kStampExit);
   }
 
   // drain: after a give-up, copies may still be landing in the ring
@@ -1434,11 +1525,13 @@ cudaError_t launch_step_t(const StepArgs& a, const CUtensorMap& tk, const CUtens
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, tk, tv, a);
 }
 

@@ -87,6 +87,10 @@ def lib():
         L.hfa_destroy.argtypes = [P]
         L.hfa_set_successor.restype = C
         L.hfa_set_successor.argtypes = [P, P]
+        L.hfa_set_step_stamps.restype = C
+        L.hfa_set_step_stamps.argtypes = [P, P]
+        L.hfa_step_stamp_rows.restype = C
+        L.hfa_step_stamp_rows.argtypes = [P]
         L.hfa_debug_stall_next_step.restype = C
         L.hfa_debug_stall_next_step.argtypes = [P]
         L.hfa_set_rope_freq_factors.restype = C
@@ -266,6 +270,13 @@ class Layer:
     def hfa_set_post_norm(self, w_post: Optional[torch.Tensor], stream=None) -> None:
         self._check(lib().hfa_set_post_norm(self._h, None if w_post is None else _ptr(w_post),
                                             _stream_ptr(stream)))
+
+    def hfa_set_step_stamps(self, stamps: Optional[torch.Tensor]) -> None:
+        """Timer stamps of later decode steps into `stamps` (int64 [rows, 16], device), or off."""
+        self._check(lib().hfa_set_step_stamps(self._h, _ptr(stamps)))
+
+    def hfa_step_stamp_rows(self) -> int:
+        return int(lib().hfa_step_stamp_rows(self._h))
 
     def hfa_debug_stall_next_step(self) -> None:
         self._check(lib().hfa_debug_stall_next_step(self._h))
