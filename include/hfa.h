@@ -274,6 +274,28 @@ hfa_status hfa_set_rope_freq_factors(hfa_layer* layer, const float* factors_host
  */
 hfa_status hfa_set_post_norm(hfa_layer* layer, const float* w_post_dev, void* stream);
 
+/*
+ * Copy of the library-owned weight tiles, for checking the re-layout done at create
+ * (the values are moved, never changed).  `which` selects the buffer:
+ *   0  Q8_0 [Wq; Wk; Wv] tiles, 1  Q8_0 Wo tiles: 544-byte tiles of 16 rows x 32 columns
+ *      ordered (k-split s, row group r, block bb), a k-split being nbs consecutive
+ *      32-column blocks, nbs the largest divisor of the row's block count up to 16.
+ *      Tile bytes [0, 512): lane l = 4g + t holds four little-endian words at 16 l:
+ *      word 2 ks + h = row g + 8 h, columns 16 ks + {2t, 2t+1, 2t+8, 2t+9} (byte e of the
+ *      word for the e-th of those columns), each byte q + 128; bytes [512, 544): eight
+ *      (fp16 d of row g, fp16 d of row g + 8) pairs, g = 0..7.
+ *   2  bf16 [Wq; Wk; Wv] tiles, 3  bf16 Wo tiles (HFA_F_WEIGHTS_BF16 layers): 16 KB tiles
+ *      of 128 rows x 64 columns, tile (m, c) at (m * K / 64 + c) * 16 KB, row r at
+ *      r * 128 bytes, its 16-byte group j at (j XOR (r mod 8)) * 16.
+ * hfa_weight_tile_bytes returns the size of the selected buffer (0: the layer has none).
+ * hfa_debug_weight_tiles copies it to dst_dev (at least that many bytes) on `stream`.
+ * Errors: HFA_EINVAL (NULL layer or pointer, a buffer the layer does not have, dst too
+ * small), HFA_ECUDA.
+ */
+size_t hfa_weight_tile_bytes(const hfa_layer* layer, int which);
+hfa_status hfa_debug_weight_tiles(hfa_layer* layer, int which, void* dst_dev, size_t dst_bytes,
+                                  void* stream);
+
 /* Release the layer and its device memory (synchronises the device first). */
 hfa_status hfa_destroy(hfa_layer* layer);
 

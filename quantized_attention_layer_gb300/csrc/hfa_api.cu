@@ -484,6 +484,47 @@ extern "C" hfa_status hfa_set_step_stamps(hfa_layer* L, unsigned long long* stam
 
 extern "C" int hfa_step_stamp_rows(const hfa_layer* L) { return L ? L->num_sms : 0; }
 
+static size_t weight_tile_bytes(const hfa_layer* L, int which, const void** src) {
+  *src = nullptr;
+  if (!L) return 0;
+  const hfa_layer_desc& d = L->d;
+  const int H = d.hidden, qo = d.num_heads * d.head_dim;
+  switch (which) {
+    case 0:
+      *src = L->wqkv_t;
+      return L->wqkv_t ? (size_t)(L->rows_qkv / 16) * L->g_qkv.nb * kQ8TileBytes : 0;
+    case 1:
+      *src = L->wo_t;
+      return L->wo_t ? (size_t)(H / 16) * L->g_o.nb * kQ8TileBytes : 0;
+    case 2:
+      *src = L->wqkv_bf16;
+      return L->wqkv_bf16 ? (size_t)L->rows_qkv * H * 2 : 0;
+    case 3:
+      *src = L->wo_bf16;
+      return L->wo_bf16 ? (size_t)H * qo * 2 : 0;
+    default:
+      return 0;
+  }
+}
+
+extern "C" size_t hfa_weight_tile_bytes(const hfa_layer* L, int which) {
+  const void* src;
+  return weight_tile_bytes(L, which, &src);
+}
+
+extern "C" hfa_status hfa_debug_weight_tiles(hfa_layer* L, int which, void* dst, size_t dst_bytes,
+                                             void* stream) {
+  if (!L) return HFA_EINVAL;
+  const void* src;
+  const size_t n = weight_tile_bytes(L, which, &src);
+  if (!n || !src) return fail(L, HFA_EINVAL, "the layer has no weight buffer %d", which);
+  if (!dst || dst_bytes < n)
+    return fail(L, HFA_EINVAL, "destination of %zu bytes, %zu needed", dst_bytes, n);
+  CK(L, cudaMemcpyAsync(dst, src, n, cudaMemcpyDeviceToDevice, (cudaStream_t)stream),
+     "copy weight tiles");
+  return HFA_OK;
+}
+
 extern "C" hfa_status hfa_debug_stall_next_step(hfa_layer* L) {
   if (!L) return HFA_EINVAL;
   L->stall_next = 1;

@@ -91,6 +91,10 @@ def lib():
         L.hfa_set_step_stamps.argtypes = [P, P]
         L.hfa_step_stamp_rows.restype = C
         L.hfa_step_stamp_rows.argtypes = [P]
+        L.hfa_weight_tile_bytes.restype = ctypes.c_size_t
+        L.hfa_weight_tile_bytes.argtypes = [P, I]
+        L.hfa_debug_weight_tiles.restype = C
+        L.hfa_debug_weight_tiles.argtypes = [P, I, P, ctypes.c_size_t, P]
         L.hfa_debug_stall_next_step.restype = C
         L.hfa_debug_stall_next_step.argtypes = [P]
         L.hfa_set_rope_freq_factors.restype = C
@@ -277,6 +281,16 @@ class Layer:
 
     def hfa_step_stamp_rows(self) -> int:
         return int(lib().hfa_step_stamp_rows(self._h))
+
+    def hfa_debug_weight_tiles(self, which: int, stream=None) -> torch.Tensor:
+        """The library's copy of weight buffer `which` (see hfa.h) as a uint8 device tensor."""
+        n = int(lib().hfa_weight_tile_bytes(self._h, int(which)))
+        if n == 0:
+            raise HfaError(HFA_EINVAL, f"the layer has no weight buffer {which}")
+        dst = torch.empty(n, dtype=torch.uint8, device="cuda")
+        self._check(lib().hfa_debug_weight_tiles(self._h, int(which), _ptr(dst), n,
+                                                 _stream_ptr(stream)))
+        return dst
 
     def hfa_debug_stall_next_step(self) -> None:
         self._check(lib().hfa_debug_stall_next_step(self._h))
