@@ -187,6 +187,8 @@ static void timer_end(hfa_layer* L, cudaStream_t s, KernelTimer* t) {
 
 // ------------------------------------------------------------------ validation
 static bool is_pow2_hd(int hd) { return hd == 64 || hd == 128 || hd == 256; }
+// the decode step also covers the 512-wide heads of the pages' global layers
+static bool step_hd(int hd) { return is_pow2_hd(hd) || hd == 512; }
 
 static hfa_status validate_desc(const hfa_layer_desc* d) {
   if (!d) return fail(nullptr, HFA_EINVAL, "desc is NULL");
@@ -201,8 +203,11 @@ static hfa_status validate_desc(const hfa_layer_desc* d) {
                 d->num_heads, d->num_kv_heads);
   if (d->num_heads / d->num_kv_heads > 8)
     return fail(nullptr, HFA_EUNSUPPORTED, "GQA group %d > 8", d->num_heads / d->num_kv_heads);
-  if (!is_pow2_hd(d->head_dim))
-    return fail(nullptr, HFA_EUNSUPPORTED, "head_dim=%d (supported: 64, 128, 256)", d->head_dim);
+  if (!step_hd(d->head_dim))
+    return fail(nullptr, HFA_EUNSUPPORTED, "head_dim=%d (supported: 64, 128, 256, 512)",
+                d->head_dim);
+  if (d->head_dim == 512 && d->max_verify_len > 0)
+    return fail(nullptr, HFA_EUNSUPPORTED, "head_dim=512: decode steps only (max_verify_len 0)");
   if (d->layer_type != HFA_SLIDING && d->layer_type != HFA_FULL)
     return fail(nullptr, HFA_EINVAL, "layer_type=%d", d->layer_type);
   if (d->layer_type == HFA_SLIDING && d->window <= 0)
@@ -547,7 +552,7 @@ static bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 
 static hfa_status ensure_maps(hfa_layer* L, void* kc, void* vc, int rows) {
   if (L->tm_k_ptr == kc && L->tm_v_ptr == vc && L->tm_rows == rows) return HFA_OK;
-  const int T = attn_keys_per_stage(L->d.head_dim);
+  const int T = step_keys_per_tile(L->d.head_dim);
   if (hfa_encode_kv_map(&L->tm_k, kc, rows, L->d.head_dim, T) != HFA_OK ||
       hfa_encode_kv_map(&L->tm_v, vc, rows, L->d.head_dim, T) != HFA_OK)
     return fail(L, HFA_EINVAL, "cannot describe the KV cache to the TMA unit");
@@ -630,8 +635,8 @@ extern "C" hfa_status hfa_decode_step(hfa_layer* L, void* stream, const void* x,
   const long long rows = (long long)batch * nkv * d.kv_capacity;
   if (rows + 256 >= (1ll << 31))
     return fail(L, HFA_EUNSUPPORTED, "cache too large for 32-bit TMA rows");
-  // the step kernel's key-tile partition (64 keys per tile at least) in 32-bit arithmetic
-  if (rows / 64 + (long long)batch * nkv >= (1ll << 24))
+  // the step kernel's key-tile partition in 32-bit arithmetic
+  if (rows / step_keys_per_tile(hd) + (long long)batch * nkv >= (1ll << 24))
     return fail(L, HFA_EUNSUPPORTED, "cache too large: 2^24 key tiles or more");
   hfa_status st = ensure_maps(L, kc, vc, (int)rows);
   if (st != HFA_OK) return st;
@@ -685,7 +690,7 @@ extern "C" hfa_status hfa_decode_step(hfa_layer* L, void* stream, const void* x,
     sa.qscale = d.attn_scale * log2e;
     sa.cap_log2 = 0.f;
   }
-  const int T = attn_keys_per_stage(hd);
+  const int T = step_keys_per_tile(hd);
   int tiles = 0;
   for (int b = 0; b < batch; ++b) tiles += (visible_keys(d, pos_host[b]) + T - 1) / T * nkv;
   L->last_splits = tiles;
@@ -968,7 +973,7 @@ extern "C" int hfa_kernel_times(hfa_layer* L, int n, const char** names, float* 
 
 extern "C" int hfa_plan_info(const hfa_layer* L, int n, int* v) {
   if (!L || !v) return -1;
-  const int vals[5] = {L->last_splits, attn_keys_per_stage(L->d.head_dim), L->last_gemv_grid,
+  const int vals[5] = {L->last_splits, step_keys_per_tile(L->d.head_dim), L->last_gemv_grid,
                        L->last_attn_grid, L->num_sms};
   int k = n < 5 ? n : 5;
   for (int i = 0; i < k; ++i) v[i] = vals[i];

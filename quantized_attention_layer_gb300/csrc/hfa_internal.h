@@ -141,6 +141,7 @@ cudaError_t launch_repack_bf16_tiles(const __nv_bfloat16* s0, int n0, const __nv
 cudaError_t launch_step(const StepArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int hd,
                         int grid, cudaStream_t s);
 size_t step_smem_bytes();
+int step_keys_per_tile(int hd);  // keys of one K/V tile of the decode-step kernel
 size_t step_stage_bytes();
 int step_threads();
 int step_batch_tiles(int batch);

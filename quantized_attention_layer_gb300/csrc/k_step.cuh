@@ -80,10 +80,11 @@ enum { kGeoP = 0, kGeoLo, kGeoHi, kGeoNt, kGeoTn, kGeoSlot, kGeoPre, kGeoInts = 
 
 // Attention tile shape: NC key groups of 16 keys per tile; with HD = 256 the 8 consumer
 // warps pair up on a key group (both form S = Q K^T, each accumulates half of O's dims),
-// which halves the O registers of a warp.
+// which halves the O registers of a warp; with HD = 512 four warps share a key group (a
+// 32-key tile of K and V is then one 64 KB stage).
 template <int HD>
 struct Attn {
-  static constexpr int NC = HD >= 256 ? 4 : 8;        // key groups of a tile
+  static constexpr int NC = HD >= 512 ? 2 : (HD >= 256 ? 4 : 8);  // key groups of a tile
   static constexpr int DSPLIT = kCW / NC;             // warps per key group
   static constexpr int T = NC * kKeysPerWarp;         // keys per tile
   static constexpr int BOXES = HD / 64;               // 128-byte TMA boxes per row
@@ -93,7 +94,7 @@ struct Attn {
   static constexpr int NTO = HD / 8;                  // n8 tiles of O
   static constexpr int NTW = NTO / DSPLIT;            // n8 tiles of O per warp
   static constexpr int RS = HD + 4;                   // record: O[HD], m, l, pad
-  static constexpr int QS_OFF = 8192;                 // query rows (f32) in the union
+  static constexpr int QS_OFF = KS * 32 * 16 > 8192 ? KS * 32 * 16 : 8192;  // query rows (f32)
   static_assert(STAGE_BYTES <= kStageBytes, "a K/V tile must fit a stage");
   static_assert(NC * DSPLIT == kCW, "every consumer warp takes part");
   static_assert(NC * 8 * RS * 4 <= kUnionBytes, "merge area must fit the union");
@@ -642,7 +643,7 @@ __device__ void head_job(const StepArgs& a, const int* geo, int b, int kvh, int 
   // the projection: partial sums of the k-splits added in a fixed order, every load of a
   // group of kSG splits issued before the first add, and issued again (after a short
   // pause) until every one carries this step's tag: no grid barrier orders them
-  constexpr int kSG = 8;
+  constexpr int kSG = HD >= 512 ? 2 : 8;  // J values of kSG splits per load round
   const unsigned long long* src = a.qkv_part + (size_t)b * rows + row0 + lane;
   const size_t split_stride = (size_t)a.B * rows;
   // the per-head norm weight and the RoPE angles are constants: loaded before the wait for

@@ -8,12 +8,22 @@ cudaError_t launch_step_64(const StepArgs& a, const CUtensorMap& tk, const CUten
                            int grid, cudaStream_t s);
 cudaError_t launch_step_256(const StepArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                             int grid, cudaStream_t s);
+cudaError_t launch_step_512(const StepArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                            int grid, cudaStream_t s);
 
 cudaError_t launch_step(const StepArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int hd,
                         int grid, cudaStream_t s) {
   if (hd == 64) return launch_step_64(a, tk, tv, grid, s);
   if (hd == 128) return step::launch_step_hd<128>(a, tk, tv, grid, s);
+  if (hd == 512) return launch_step_512(a, tk, tv, grid, s);
   return launch_step_256(a, tk, tv, grid, s);
+}
+
+int step_keys_per_tile(int hd) {
+  return hd == 64    ? step::Attn<64>::T
+         : hd == 128 ? step::Attn<128>::T
+         : hd == 256 ? step::Attn<256>::T
+                     : step::Attn<512>::T;
 }
 
 size_t step_smem_bytes() { return step::kSmem; }

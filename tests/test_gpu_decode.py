@@ -70,6 +70,27 @@ def test_other_head_dims_sliding_linear(hd):
     _case(w, pos=[150, 613])
 
 
+# The pages' global layer: 16 query heads of 512 dims over 2 KV heads (GQA group 8), full
+# attention, no V projection (V = unit-normed raw K), RoPE frequency factors and the
+# post-attention norm; hidden 2816 splits the QKV rows into k-splits of 11 blocks.
+GLOBAL_32K = wl.Workload(name="global_hd512_32k", hidden=2816, num_heads=16, num_kv_heads=2,
+                         head_dim=512, layer_type=wl.FULL, window=0, kv_capacity=32768,
+                         ring=False, batch=1, rope_theta=1e6, seed=70, seq_pos=32767,
+                         k_eq_v=True, rope_freq_factors=True, post_norm=True)
+
+
+def test_global_layer_hd512_32k_context():
+    _case(GLOBAL_32K)
+
+
+def test_hd512_ragged_batch_plain_layer():
+    # three sequences of 1, 7 and 40 key tiles of 32 keys, with V projected and no variants
+    w = GLOBAL_32K.replace(name="hd512_b3", hidden=1024, kv_capacity=1300, batch=3,
+                           k_eq_v=False, rope_freq_factors=False, post_norm=False,
+                           seq_pos=None, softcap=30.0)
+    _case(w, pos=[0, 200, 1279])
+
+
 def test_fewer_key_tiles_than_ctas_with_many_units():
     # 16 sequences of 1..6 key tiles (104 tiles for 152 CTAs): CTAs without tiles sit both
     # inside units and on their first tiles; every unit's records must combine exactly once
