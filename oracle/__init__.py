@@ -14,6 +14,10 @@ Parity status per function (pins live in ``tests/test_oracle_*.py``):
 * RoPE: pinned (hand-computed angles, norm, composition, relative position)
 * slots / visibility / attention: pinned (brute-force explicit mask, permutation,
   one key, softcap bound, ring == linear window)
+* quantised KV cache (Lloyd-Max codebook, FWHT rotation, encode / decode, attention
+  over codes): pinned (textbook Lloyd-Max values and closed forms, the Hadamard matrix
+  from its popcount definition, brute-force nearest centroid, attention over codes ==
+  attention over the dequantised cache)
 * decode step / verify block: pinned by a closed-form layer (permutation weights at
   position 0), by the q and k heads in closed form at later positions (permutation Wq
   and Wk, distinct norm weights, power-of-two RoPE angles), and by consistency (verify of L tokens == L decode steps; batch ==
@@ -32,6 +36,8 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "hfa_oracle.cpp")
+_SRCS = [_SRC, os.path.join(_HERE, "tq_oracle.cpp")]
+_HDRS = [os.path.join(_HERE, "hfa_oracle.h"), os.path.join(_HERE, "tq_oracle.h")]
 _LIB_PATH = os.path.join(_HERE, "liborc.so")
 _lock = threading.Lock()
 _lib = None
@@ -40,11 +46,10 @@ _lib = None
 def build(force: bool = False) -> str:
     """Compile the oracle with g++ (OpenMP when available)."""
     if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= max(os.path.getmtime(_SRC),
-                                                   os.path.getmtime(os.path.join(_HERE, "hfa_oracle.h")))):
+            and os.path.getmtime(_LIB_PATH) >= max(os.path.getmtime(f) for f in _SRCS + _HDRS)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-fopenmp", _SRC, "-o", tmp]
+    cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-fopenmp"] + _SRCS + ["-o", tmp]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -97,6 +102,21 @@ def lib():
             L.orc_verify_block.restype = ctypes.c_int
             L.orc_verify_block.argtypes = step_args + [ctypes.c_int, ctypes.c_int, P, P, P, P, P,
                                                        P, P, P]
+            L.orc_lloyd_max_normal.restype = ctypes.c_int
+            L.orc_lloyd_max_normal.argtypes = [ctypes.c_int, P, P]
+            L.orc_lloyd_max_mse.restype = ctypes.c_double
+            L.orc_lloyd_max_mse.argtypes = [ctypes.c_int, P, P]
+            L.orc_fwht.argtypes = [P, ctypes.c_int]
+            L.orc_tq_rotate.argtypes = [P, ctypes.c_int, P]
+            L.orc_tq_unrotate.argtypes = [P, ctypes.c_int, P]
+            L.orc_tq_code_bytes.restype = ctypes.c_int
+            L.orc_tq_code_bytes.argtypes = [ctypes.c_int, ctypes.c_int]
+            L.orc_tq_blocks.restype = ctypes.c_int
+            L.orc_tq_blocks.argtypes = [ctypes.c_int]
+            L.orc_tq_encode_row.argtypes = [P, ctypes.c_int, P, ctypes.c_int, P, P, P]
+            L.orc_tq_decode_row.argtypes = [P, P, ctypes.c_int, ctypes.c_int, P, P]
+            L.orc_attend_tq.argtypes = [P, ctypes.c_int, ctypes.c_int, P, P, P, P, P, P, P, P,
+                                        ctypes.c_long, ctypes.c_double, ctypes.c_double, P]
             L.orc_num_threads.restype = ctypes.c_int
             L.orc_set_num_threads.argtypes = [ctypes.c_int]
             _lib = L
@@ -298,3 +318,97 @@ def num_threads() -> int:
 
 def set_num_threads(n: int) -> None:
     lib().orc_set_num_threads(int(n))
+
+
+# ------------------------------------------------------------------ quantised KV cache
+
+def lloyd_max_normal(bits: int):
+    """(centroids [2^bits], boundaries [2^bits + 1], rounds) of the N(0,1) Lloyd-Max quantiser."""
+    levels = 1 << bits
+    c = np.empty(levels, dtype=np.float64)
+    b = np.empty(levels + 1, dtype=np.float64)
+    rounds = lib().orc_lloyd_max_normal(levels, _ptr(c), _ptr(b))
+    return c, b, int(rounds)
+
+
+def lloyd_max_mse(centroids, boundaries) -> float:
+    c = np.ascontiguousarray(centroids, dtype=np.float64)
+    b = np.ascontiguousarray(boundaries, dtype=np.float64)
+    return float(lib().orc_lloyd_max_mse(c.size, _ptr(c), _ptr(b)))
+
+
+def fwht(x) -> np.ndarray:
+    x = np.array(x, dtype=np.float64, copy=True)
+    lib().orc_fwht(_ptr(x), x.size)
+    return x
+
+
+def tq_rotate(x, signs) -> np.ndarray:
+    x = np.array(x, dtype=np.float64, copy=True)
+    s = np.ascontiguousarray(signs, dtype=np.int8)
+    lib().orc_tq_rotate(_ptr(x), x.size, _ptr(s))
+    return x
+
+
+def tq_unrotate(x, signs) -> np.ndarray:
+    x = np.array(x, dtype=np.float64, copy=True)
+    s = np.ascontiguousarray(signs, dtype=np.int8)
+    lib().orc_tq_unrotate(_ptr(x), x.size, _ptr(s))
+    return x
+
+
+def tq_code_bytes(hd: int, bits: int) -> int:
+    return int(lib().orc_tq_code_bytes(hd, bits))
+
+
+def tq_blocks(hd: int) -> int:
+    return int(lib().orc_tq_blocks(hd))
+
+
+def tq_encode_rows(x, signs, bits, boundaries):
+    """Encode rows x [..., hd] -> (codes uint8 [..., code_bytes], norms f32 [..., blocks])."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    hd = x.shape[-1]
+    rows = x.reshape(-1, hd)
+    s = np.ascontiguousarray(signs, dtype=np.int8)
+    b = np.ascontiguousarray(boundaries, dtype=np.float64)
+    cb, nb = tq_code_bytes(hd, bits), tq_blocks(hd)
+    codes = np.empty((rows.shape[0], cb), dtype=np.uint8)
+    norms = np.empty((rows.shape[0], nb), dtype=np.float32)
+    for r in range(rows.shape[0]):
+        lib().orc_tq_encode_row(_ptr(rows[r]), hd, _ptr(s), int(bits), _ptr(b), _ptr(codes[r]),
+                                _ptr(norms[r]))
+    return codes.reshape(x.shape[:-1] + (cb,)), norms.reshape(x.shape[:-1] + (nb,))
+
+
+def tq_decode_rows(codes, norms, hd, bits, centroids) -> np.ndarray:
+    """Decode rows into the rotated domain: [..., hd] float64."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    norms = np.ascontiguousarray(norms, dtype=np.float32)
+    c = np.ascontiguousarray(centroids, dtype=np.float64)
+    cr = codes.reshape(-1, codes.shape[-1])
+    nr = norms.reshape(-1, norms.shape[-1])
+    out = np.empty((cr.shape[0], hd), dtype=np.float64)
+    for r in range(cr.shape[0]):
+        lib().orc_tq_decode_row(_ptr(cr[r]), _ptr(nr[r]), hd, int(bits), _ptr(c), _ptr(out[r]))
+    return out.reshape(codes.shape[:-1] + (hd,))
+
+
+def attend_tq(q, signs, bits, centroids, k_codes, k_norms, v_codes, v_norms, rows,
+              scale=1.0, softcap=0.0, k_bf16=None) -> np.ndarray:
+    """Attention of one query over rows of a TQ cache (k_codes None: hybrid, raw bf16 keys)."""
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    hd = q.size
+    s = np.ascontiguousarray(signs, dtype=np.int8)
+    c = np.ascontiguousarray(centroids, dtype=np.float64)
+    kc = None if k_codes is None else np.ascontiguousarray(k_codes, dtype=np.uint8)
+    kn = None if k_norms is None else np.ascontiguousarray(k_norms, dtype=np.float32)
+    kb = None if k_bf16 is None else as_np(k_bf16, np.uint16)
+    vc = np.ascontiguousarray(v_codes, dtype=np.uint8)
+    vn = np.ascontiguousarray(v_norms, dtype=np.float32)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    o = np.empty(hd, dtype=np.float64)
+    lib().orc_attend_tq(_ptr(q), hd, int(bits), _ptr(s), _ptr(c), _ptr(kc), _ptr(kn), _ptr(kb),
+                        _ptr(vc), _ptr(vn), _ptr(rows), rows.size, float(scale), float(softcap),
+                        _ptr(o))
+    return o
