@@ -214,6 +214,66 @@ hfa_status hfa_attention_decode_noalloc(const hfa_attn_desc* desc, void* stream,
                                         float* o_dev);
 
 /*
+ * Quantised KV cache (TurboQuant): gpu_full_attn.rs, encode_one_layer -- the
+ * Hadamard-quantize KV encode (sign pre-multiply, normalised FWHT, a norm per 256-dim
+ * block, Lloyd-Max codes packed as 4-bit nibbles or one byte per value), the attention
+ * over codes (the query pre-rotated, the output sign-undone) and the hybrid layout (raw
+ * keys, coded values); model.rs, the cache buffers.
+ * A format fixes head_dim, the code width and the sign pre-multiply.  Rows are coded in
+ * blocks of B = min(head_dim, 256) values: u = H (s . x) / sqrt(B) (H the Sylvester
+ * Hadamard matrix), norm = sqrt(mean(u^2)) stored as f32, and each u_i / norm coded by the
+ * cell of the Lloyd-Max quantiser of N(0, 1) with 2^bits levels that holds it (a value on
+ * a boundary takes the upper cell; the library computes the quantiser when the format is
+ * created).  bits 8: one byte per value; bits 4: value 2j in the low nibble of byte j,
+ * 2j+1 in the high nibble.  A coded value decodes to centroid[code] * norm (rotated).
+ *   head_dim in {64, 128, 256, 512}; bits in {4, 8};
+ *   signs_host int8 [head_dim], each +1 or -1, copied.
+ * Errors: HFA_EINVAL, HFA_EUNSUPPORTED, HFA_EDEVICE, HFA_ENOMEM.
+ */
+typedef struct hfa_tq hfa_tq;
+hfa_status hfa_tq_create(int head_dim, int bits, const int8_t* signs_host, hfa_tq** out);
+hfa_status hfa_tq_destroy(hfa_tq* fmt);
+int hfa_tq_code_bytes(const hfa_tq* fmt); /* bytes of one row's codes: head_dim * bits / 8 */
+int hfa_tq_blocks(const hfa_tq* fmt);     /* norms per row: head_dim / B */
+/* copies up to n centroids (ascending) to centroids_host; returns the level count */
+int hfa_tq_codebook(const hfa_tq* fmt, float* centroids_host, int n);
+
+/*
+ * The KV append of a coded cache: row (b, h) of x_dev f32 [batch, nkv, head_dim] is coded
+ * into slot seq_pos[b] (linear) or seq_pos[b] % capacity (ring) of codes_dev
+ * [batch, nkv, capacity, code_bytes] and norms_dev f32 [batch, nkv, capacity, blocks];
+ * every other slot is left as it is.  The decisions (the norm, the cells) are taken in
+ * double precision from the f32 inputs.  x_dev 16-byte aligned.
+ * Errors: HFA_EINVAL, HFA_ERANGE (a position outside a linear cache), HFA_ECUDA.
+ */
+hfa_status hfa_tq_append(const hfa_tq* fmt, void* stream, const float* x_dev,
+                         const int32_t* seq_pos_dev, const int32_t* seq_pos_host, int batch,
+                         int nkv, int capacity, int ring, uint8_t* codes_dev, float* norms_dev);
+
+/*
+ * Attention over a coded cache: as hfa_attention_decode (same descriptor, positions, masks,
+ * scale and softcap), with the keys given by k_codes_dev / k_norms_dev in the format, or,
+ * when k_codes_dev is NULL, by raw bf16 keys k_raw_dev [batch, nkv, capacity, head_dim]
+ * (the hybrid layout), and the values always coded (v_codes_dev, v_norms_dev).  Scores
+ * with coded keys use the rotated query (the rotation is orthogonal, so they equal q . k
+ * over the decoded keys); the weighted sum of the decoded values is rotated back.
+ *   workspace_dev  at least hfa_attention_tq_workspace_bytes(desc, batch, max_keys)
+ *                  bytes, max_keys the most visible keys of any sequence of the call,
+ *                  16-byte aligned, zero before its first use; each call leaves it ready
+ *                  for the next.  Calls sharing a workspace must not overlap on the GPU.
+ * fmt->head_dim must equal desc->head_dim.  q, o, the workspace and the code arrays
+ * 16-byte aligned.  Errors as hfa_attention_decode (message via hfa_last_error(NULL)).
+ */
+size_t hfa_attention_tq_workspace_bytes(const hfa_attn_desc* desc, int batch, int max_keys);
+hfa_status hfa_attention_decode_tq(const hfa_attn_desc* desc, const hfa_tq* fmt, void* stream,
+                                   const float* q_dev, const int32_t* seq_pos_dev,
+                                   const int32_t* seq_pos_host, int batch,
+                                   const uint8_t* k_codes_dev, const float* k_norms_dev,
+                                   const void* k_raw_dev, const uint8_t* v_codes_dev,
+                                   const float* v_norms_dev, void* workspace_dev,
+                                   size_t workspace_bytes, float* o_dev);
+
+/*
  * Successor hint for decoding through a stack of layers (no counterpart on the pages,
  * which run one layer at a time).  Once set, each decode step of `layer` prefetches into
  * L2, during its last phase (o_proj and residual, when HBM is otherwise idle), the Q8_0

@@ -122,6 +122,23 @@ def lib():
         L.hfa_attention_decode_noalloc.restype = C
         L.hfa_attention_decode_noalloc.argtypes = [ctypes.POINTER(hfa_attn_desc), P, P, P, P, I,
                                                    P, P, P]
+        L.hfa_tq_create.restype = C
+        L.hfa_tq_create.argtypes = [I, I, P, ctypes.POINTER(P)]
+        L.hfa_tq_destroy.restype = C
+        L.hfa_tq_destroy.argtypes = [P]
+        L.hfa_tq_code_bytes.restype = I
+        L.hfa_tq_code_bytes.argtypes = [P]
+        L.hfa_tq_blocks.restype = I
+        L.hfa_tq_blocks.argtypes = [P]
+        L.hfa_tq_codebook.restype = I
+        L.hfa_tq_codebook.argtypes = [P, P, I]
+        L.hfa_tq_append.restype = C
+        L.hfa_tq_append.argtypes = [P, P, P, P, P, I, I, I, I, P, P]
+        L.hfa_attention_tq_workspace_bytes.restype = ctypes.c_size_t
+        L.hfa_attention_tq_workspace_bytes.argtypes = [ctypes.POINTER(hfa_attn_desc), I, I]
+        L.hfa_attention_decode_tq.restype = C
+        L.hfa_attention_decode_tq.argtypes = [ctypes.POINTER(hfa_attn_desc), P, P, P, P, P, I,
+                                              P, P, P, P, P, P, ctypes.c_size_t, P]
         _lib = L
     return _lib
 
@@ -173,6 +190,70 @@ def hfa_attention_decode_noalloc(desc: hfa_attn_desc, q: torch.Tensor, seq_pos_d
     if st != HFA_OK:
         raise HfaError(st, lib().hfa_last_error(None).decode())
     return o
+
+
+class TqFormat:
+    """A quantised-KV format (hfa_tq_create ... hfa_tq_destroy)."""
+
+    def __init__(self, head_dim: int, bits: int, signs: np.ndarray):
+        self.head_dim, self.bits = int(head_dim), int(bits)
+        self._signs = np.ascontiguousarray(signs, dtype=np.int8)
+        self._h = ctypes.c_void_p()
+        st = lib().hfa_tq_create(self.head_dim, self.bits, ctypes.c_void_p(self._signs.ctypes.data),
+                                 ctypes.byref(self._h))
+        if st != HFA_OK:
+            raise HfaError(st, lib().hfa_last_error(None).decode())
+
+    @property
+    def code_bytes(self) -> int:
+        return int(lib().hfa_tq_code_bytes(self._h))
+
+    @property
+    def blocks(self) -> int:
+        return int(lib().hfa_tq_blocks(self._h))
+
+    def codebook(self) -> np.ndarray:
+        c = np.empty(1 << self.bits, dtype=np.float32)
+        n = lib().hfa_tq_codebook(self._h, ctypes.c_void_p(c.ctypes.data), c.size)
+        return c[:n]
+
+    def hfa_tq_append(self, x: torch.Tensor, seq_pos_dev: torch.Tensor, seq_pos_host, nkv: int,
+                      capacity: int, ring: bool, codes: torch.Tensor, norms: torch.Tensor,
+                      stream=None) -> None:
+        pos_h = np.ascontiguousarray(seq_pos_host, dtype=np.int32)
+        st = lib().hfa_tq_append(self._h, _stream_ptr(stream), _ptr(x), _ptr(seq_pos_dev),
+                                 ctypes.c_void_p(pos_h.ctypes.data), int(pos_h.size), int(nkv),
+                                 int(capacity), int(bool(ring)), _ptr(codes), _ptr(norms))
+        if st != HFA_OK:
+            raise HfaError(st, lib().hfa_last_error(None).decode())
+
+    def hfa_attention_decode_tq(self, desc: hfa_attn_desc, q: torch.Tensor, seq_pos_dev: torch.Tensor,
+                                seq_pos_host, k_codes, k_norms, k_raw, v_codes, v_norms,
+                                workspace: torch.Tensor, o: torch.Tensor, stream=None) -> torch.Tensor:
+        pos_h = np.ascontiguousarray(seq_pos_host, dtype=np.int32)
+        st = lib().hfa_attention_decode_tq(
+            ctypes.byref(desc), self._h, _stream_ptr(stream), _ptr(q), _ptr(seq_pos_dev),
+            ctypes.c_void_p(pos_h.ctypes.data), int(pos_h.size), _ptr(k_codes), _ptr(k_norms),
+            _ptr(k_raw), _ptr(v_codes), _ptr(v_norms), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _ptr(o))
+        if st != HFA_OK:
+            raise HfaError(st, lib().hfa_last_error(None).decode())
+        return o
+
+    def destroy(self) -> None:
+        if self._h:
+            lib().hfa_tq_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+def hfa_attention_tq_workspace_bytes(desc: hfa_attn_desc, batch: int, max_keys: int) -> int:
+    return int(lib().hfa_attention_tq_workspace_bytes(ctypes.byref(desc), int(batch), int(max_keys)))
 
 
 def desc_for(w: wl.Workload, max_batch: Optional[int] = None, max_verify_len: Optional[int] = None,

@@ -94,3 +94,18 @@ def test_ring_needs_capacity_equal_to_window(libhfa):
 def test_null_handle_is_rejected(libhfa):
     assert libhfa.hfa_decode_step(None, None, None, None, None, 1, None, None, None) == hfa.HFA_EINVAL
     assert libhfa.hfa_destroy(None) == hfa.HFA_EINVAL
+
+
+def test_quantised_kv_format_rejects_bad_arguments_before_any_device_call(libhfa):
+    import numpy as np
+    h = ctypes.c_void_p()
+    ok = np.ones(128, dtype=np.int8)
+    bad = ok.copy()
+    bad[5] = 0
+    P = lambda a: ctypes.c_void_p(a.ctypes.data)  # noqa: E731
+    assert libhfa.hfa_tq_create(128, 3, P(ok), ctypes.byref(h)) == hfa.HFA_EUNSUPPORTED
+    assert libhfa.hfa_tq_create(96, 8, P(ok), ctypes.byref(h)) == hfa.HFA_EUNSUPPORTED
+    assert libhfa.hfa_tq_create(128, 8, P(bad), ctypes.byref(h)) == hfa.HFA_EINVAL
+    assert b"signs[5]" in libhfa.hfa_last_error(None)
+    assert libhfa.hfa_tq_create(128, 8, None, ctypes.byref(h)) == hfa.HFA_EINVAL
+    assert not h.value
