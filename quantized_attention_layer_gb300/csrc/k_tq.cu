@@ -102,6 +102,7 @@ const Codebook& codebook(int bits) {
 
 constexpr int kTqThreads = 256;  // attention CTA: 8 warps; a tile is 256 keys
 constexpr int kTqMaxG = 8;
+constexpr int kTqMaxSplits = 256;  // the merge's weight table: kTqMaxG * 256 floats
 
 // ------------------------------------------------------------------ encode (device)
 struct TqAppendArgs {
@@ -221,8 +222,9 @@ struct TqCfg {
   static constexpr int BLK = HD < 256 ? HD : 256;
   static constexpr int NB = HD / BLK;
   static constexpr int RS = HD + 4;
-  static constexpr int NKS = HD >= kTqThreads ? 1 : kTqThreads / HD;  // key subsets, phase 2
-  static constexpr int DPT = HD > kTqThreads ? HD / kTqThreads : 1;   // dims per thread
+  // phase 2: four dimensions per thread, HD / 4 threads per key row, NKS key subsets
+  static constexpr int TPR = HD / 4;
+  static constexpr int NKS = kTqThreads / TPR;
 };
 
 // shared-memory normalised FWHT of n values (n <= 256) at v, all threads of the CTA
@@ -251,30 +253,49 @@ __device__ void smem_fwht_rows(float* v, int count, int stride, int n, int row_l
   __syncthreads();
 }
 
-template <int HD, int BITS, bool KRAW>
+// GM: the most query heads per KV head this instantiation handles (G rounded up to 2, 4, 8)
+template <int HD, int BITS, bool KRAW, int GM>
+struct TqSmem {
+  static constexpr int LEVELS = 1 << BITS;
+  static constexpr int NB = TqCfg<HD>::NB;
+  // the centroid table with one copy per bank (entry c of lane l at c * 32 + l), so the
+  // lookups of a warp never collide; the queries; the per-tile scores / weights; V norms
+  static constexpr size_t TAB = (size_t)LEVELS * 32 * 4;
+  static constexpr size_t Q = (size_t)GM * HD * 4;
+  static constexpr size_t PB = (size_t)kTqMaxG * kTqThreads * 4;
+  static constexpr size_t VN = (size_t)kTqThreads * NB * 4;
+  static constexpr size_t BYTES = TAB + Q + PB + VN + 3 * kTqMaxG * 4 + 16;
+};
+
+template <int HD, int BITS, bool KRAW, int GM>
 __global__ void __launch_bounds__(kTqThreads) tq_attn_kernel(const TqAttnArgs a) {
   using Cfg = TqCfg<HD>;
+  using SM = TqSmem<HD, BITS, KRAW, GM>;
   constexpr int RS = Cfg::RS;
   constexpr int NB = Cfg::NB;
   constexpr int BLK = Cfg::BLK;
   constexpr int CB = HD * BITS / 8;  // code bytes of a row
   constexpr int NKS = Cfg::NKS;
-  constexpr int DPT = Cfg::DPT;
-  __shared__ float s_cent[256];
-  __shared__ __align__(16) float s_q[kTqMaxG * HD];      // rotated (or raw, hybrid) queries
-  __shared__ float s_p[kTqMaxG * kTqThreads];             // scores, then weights, per tile
-  __shared__ float s_vn[kTqThreads * NB];                 // V norms of the tile's keys
-  __shared__ float s_corr[kTqMaxG], s_m[kTqMaxG], s_l[kTqMaxG];
-  __shared__ int s_last;
+  constexpr int TPR = Cfg::TPR;
+  constexpr int LEVELS = 1 << BITS;
+  extern __shared__ __align__(16) uint8_t tq_smem[];
+  float* s_tab = reinterpret_cast<float*>(tq_smem);
+  float* s_q = reinterpret_cast<float*>(tq_smem + SM::TAB);   // [GM][HD]
+  float* s_p = reinterpret_cast<float*>(tq_smem + SM::TAB + SM::Q);  // [8][256]
+  float* s_vn = reinterpret_cast<float*>(tq_smem + SM::TAB + SM::Q + SM::PB);  // [256][NB]
+  float* s_corr = reinterpret_cast<float*>(tq_smem + SM::TAB + SM::Q + SM::PB + SM::VN);
+  float* s_m = s_corr + kTqMaxG;
+  float* s_l = s_m + kTqMaxG;
+  int* s_last = reinterpret_cast<int*>(s_l + kTqMaxG);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int G = a.nh / a.nkv;
+  const int G = a.nh / a.nkv;  // <= GM
   const int unit = blockIdx.x / a.splits, split = blockIdx.x - unit * a.splits;
   const int b = unit / a.nkv, kvh = unit - b * a.nkv;
-  for (int i = tid; i < a.levels; i += kTqThreads) s_cent[i] = a.centroids[i];
-  for (int e = tid; e < G * HD; e += kTqThreads) {
+  for (int i = tid; i < LEVELS * 32; i += kTqThreads) s_tab[i] = a.centroids[i >> 5];
+  for (int e = tid; e < GM * HD; e += kTqThreads) {
     const int h = e / HD, i = e - h * HD;
-    const float qv = a.q[((size_t)b * a.nh + kvh * G + h) * HD + i] * a.qscale;
+    const float qv = h < G ? a.q[((size_t)b * a.nh + kvh * G + h) * HD + i] * a.qscale : 0.f;
     s_q[h * HD + i] = KRAW ? qv : qv * a.signs[i];
   }
   if (tid < kTqMaxG) {
@@ -282,7 +303,7 @@ __global__ void __launch_bounds__(kTqThreads) tq_attn_kernel(const TqAttnArgs a)
     s_l[tid] = 0.f;
   }
   __syncthreads();
-  if (!KRAW) smem_fwht_rows(s_q, G, HD, BLK, HD);  // the query in the keys' rotated domain
+  if (!KRAW) smem_fwht_rows(s_q, GM, HD, BLK, HD);  // the query in the keys' rotated domain
 
   const int P = a.seq_pos[b];
   int lo, hi;
@@ -301,39 +322,45 @@ __global__ void __launch_bounds__(kTqThreads) tq_attn_kernel(const TqAttnArgs a)
   if (bad) k_end = k_begin;
   const size_t row0 = (size_t)unit * a.C;  // cache row of slot 0 of this unit
 
-  float acc[DPT][kTqMaxG];
+  // phase 2 accumulators: dims 4 (tid % TPR) .. + 3 for every query head
+  const int ks = tid / TPR, d0 = 4 * (tid - ks * TPR);
+  float acc[4][GM];
 #pragma unroll
-  for (int d = 0; d < DPT; ++d)
+  for (int d = 0; d < 4; ++d)
 #pragma unroll
-    for (int h = 0; h < kTqMaxG; ++h) acc[d][h] = 0.f;
+    for (int h = 0; h < GM; ++h) acc[d][h] = 0.f;
 
   for (int t0 = k_begin; t0 < k_end; t0 += kTqThreads) {
-    // ---- phase 1: one key per thread, its score for every query head
+    // ---- phase 1: one key per thread, its score for every query head (every lane reads
+    // the same query element at a time: a broadcast); eight 16-byte loads in flight
     {
       const int key = t0 + tid;
-      float sc[kTqMaxG];
+      float sc[GM];
 #pragma unroll
-      for (int h = 0; h < kTqMaxG; ++h) sc[h] = 0.f;
+      for (int h = 0; h < GM; ++h) sc[h] = 0.f;
       if (key < k_end) {
         const size_t r = row0 + key;
         if (KRAW) {
           const uint4* kr = reinterpret_cast<const uint4*>(a.k_raw + r * HD);
-#pragma unroll 2
-          for (int c8 = 0; c8 < HD / 8; ++c8) {
-            const uint4 w = __ldg(kr + c8);
-            const __nv_bfloat162* kp = reinterpret_cast<const __nv_bfloat162*>(&w);
-            float kv[8];
+          for (int c0 = 0; c0 < HD / 8; c0 += 8) {
+            uint4 w8[8];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = __bfloat1622float2(kp[e]);
-              kv[2 * e] = f.x;
-              kv[2 * e + 1] = f.y;
-            }
+            for (int u = 0; u < 8; ++u) w8[u] = __ldg(kr + c0 + u);
 #pragma unroll
-            for (int h = 0; h < kTqMaxG; ++h) {
-              if (h < G) {
-                const float4 qa = *reinterpret_cast<const float4*>(s_q + h * HD + c8 * 8);
-                const float4 qb = *reinterpret_cast<const float4*>(s_q + h * HD + c8 * 8 + 4);
+            for (int u = 0; u < 8; ++u) {
+              const __nv_bfloat162* kp = reinterpret_cast<const __nv_bfloat162*>(&w8[u]);
+              float kv[8];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(kp[e]);
+                kv[2 * e] = f.x;
+                kv[2 * e + 1] = f.y;
+              }
+              const int i0 = (c0 + u) * 8;
+#pragma unroll
+              for (int h = 0; h < GM; ++h) {
+                const float4 qa = *reinterpret_cast<const float4*>(s_q + h * HD + i0);
+                const float4 qb = *reinterpret_cast<const float4*>(s_q + h * HD + i0 + 4);
                 sc[h] += qa.x * kv[0] + qa.y * kv[1] + qa.z * kv[2] + qa.w * kv[3] +
                          qb.x * kv[4] + qb.y * kv[5] + qb.z * kv[6] + qb.w * kv[7];
               }
@@ -341,30 +368,34 @@ __global__ void __launch_bounds__(kTqThreads) tq_attn_kernel(const TqAttnArgs a)
           }
         } else {
           const uint4* kc = reinterpret_cast<const uint4*>(a.k_codes + r * CB);
-          constexpr int VPC = 128 / BITS;  // values per 16-byte chunk
+          constexpr int VPC = 128 / BITS;        // values per 16-byte chunk
+          constexpr int CPB = BLK / VPC;         // chunks per block
+          constexpr int CG = CPB < 8 ? CPB : 8;  // chunks loaded together
 #pragma unroll
           for (int k = 0; k < NB; ++k) {
-            float part[kTqMaxG];
+            float part[GM];
 #pragma unroll
-            for (int h = 0; h < kTqMaxG; ++h) part[h] = 0.f;
-#pragma unroll 2
-            for (int c16 = k * (BLK / VPC); c16 < (k + 1) * (BLK / VPC); ++c16) {
-              const uint4 w = __ldg(kc + c16);
-              const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+            for (int h = 0; h < GM; ++h) part[h] = 0.f;
+            for (int c0 = k * CPB; c0 < (k + 1) * CPB; c0 += CG) {
+              uint4 w8[CG];
 #pragma unroll
-              for (int q4 = 0; q4 < VPC / 4; ++q4) {
-                float kv[4];
+              for (int u = 0; u < CG; ++u) w8[u] = __ldg(kc + c0 + u);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const int vi = q4 * 4 + e;  // value index inside the chunk
-                  const uint32_t word = ws[vi / (32 / BITS)];
-                  const int code = (word >> ((vi % (32 / BITS)) * BITS)) & ((1 << BITS) - 1);
-                  kv[e] = s_cent[code];
-                }
-                const int i0 = c16 * VPC + q4 * 4;
+              for (int u = 0; u < CG; ++u) {
+                const uint32_t ws[4] = {w8[u].x, w8[u].y, w8[u].z, w8[u].w};
 #pragma unroll
-                for (int h = 0; h < kTqMaxG; ++h) {
-                  if (h < G) {
+                for (int q4 = 0; q4 < VPC / 4; ++q4) {
+                  float kv[4];
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    const int vi = q4 * 4 + e;
+                    const uint32_t word = ws[vi / (32 / BITS)];
+                    const int code = (word >> ((vi % (32 / BITS)) * BITS)) & (LEVELS - 1);
+                    kv[e] = s_tab[code * 32 + lane];
+                  }
+                  const int i0 = (c0 + u) * VPC + q4 * 4;
+#pragma unroll
+                  for (int h = 0; h < GM; ++h) {
                     const float4 qa = *reinterpret_cast<const float4*>(s_q + h * HD + i0);
                     part[h] += qa.x * kv[0] + qa.y * kv[1] + qa.z * kv[2] + qa.w * kv[3];
                   }
@@ -373,18 +404,18 @@ __global__ void __launch_bounds__(kTqThreads) tq_attn_kernel(const TqAttnArgs a)
             }
             const float kn = __ldg(a.k_norms + r * NB + k);
 #pragma unroll
-            for (int h = 0; h < kTqMaxG; ++h) sc[h] += part[h] * kn;
+            for (int h = 0; h < GM; ++h) sc[h] += part[h] * kn;
           }
         }
 #pragma unroll
         for (int k = 0; k < NB; ++k) s_vn[tid * NB + k] = __ldg(a.v_norms + r * NB + k);
       }
 #pragma unroll
-      for (int h = 0; h < kTqMaxG; ++h) {
+      for (int h = 0; h < GM; ++h) {
         if (h < G) {
-          float s = sc[h];
-          if (a.cap_log2 != 0.f) s = a.cap_log2 * tanhf(s);
-          s_p[h * kTqThreads + tid] = key < k_end ? s : -INFINITY;
+          float sv = sc[h];
+          if (a.cap_log2 != 0.f) sv = a.cap_log2 * tanhf(sv);
+          s_p[h * kTqThreads + tid] = key < k_end ? sv : -INFINITY;
         }
       }
     }
@@ -415,56 +446,73 @@ __global__ void __launch_bounds__(kTqThreads) tq_attn_kernel(const TqAttnArgs a)
       }
     }
     __syncthreads();
-    // ---- phase 2: one dimension per thread (DPT of them with HD = 512), the keys of its
-    // subset; the weighted sum of the decoded values in the rotated domain
+    // ---- phase 2: four dimensions per thread, the keys of its subset (four keys' codes
+    // loaded together); the weighted sum of the decoded values in the rotated domain
     {
-      const int ks = tid / (HD >= kTqThreads ? kTqThreads : HD);
+      float corr[GM];
 #pragma unroll
-      for (int d = 0; d < DPT; ++d)
+      for (int h = 0; h < GM; ++h) corr[h] = h < G ? s_corr[h] : 0.f;
 #pragma unroll
-        for (int h = 0; h < kTqMaxG; ++h) acc[d][h] *= h < G ? s_corr[h] : 1.f;
+      for (int d = 0; d < 4; ++d)
+#pragma unroll
+        for (int h = 0; h < GM; ++h) acc[d][h] *= corr[h];
       const int nk = k_end - t0 < kTqThreads ? k_end - t0 : kTqThreads;
-      for (int j = ks; j < nk; j += NKS) {
-        const size_t r = row0 + t0 + j;
+      const int blk = d0 / BLK;
+      for (int j0 = ks; j0 < nk; j0 += 4 * NKS) {
+        uint32_t cw[4];
 #pragma unroll
-        for (int d = 0; d < DPT; ++d) {
-          const int i = (HD >= kTqThreads ? tid : tid % HD) + d * kTqThreads;
-          int code;
-          if (BITS == 8) code = __ldg(a.v_codes + r * CB + i);
-          else code = (__ldg(a.v_codes + r * CB + i / 2) >> ((i & 1) * 4)) & 15;
-          const float val = s_cent[code] * s_vn[j * NB + i / BLK];
+        for (int u = 0; u < 4; ++u) {
+          const int j = j0 + u * NKS;
+          const size_t r = row0 + t0 + (j < nk ? j : j0);  // in range
+          if (BITS == 8)
+            cw[u] = __ldg(reinterpret_cast<const uint32_t*>(a.v_codes + r * CB + d0));
+          else
+            cw[u] = __ldg(reinterpret_cast<const uint16_t*>(a.v_codes + r * CB + d0 / 2));
+        }
 #pragma unroll
-          for (int h = 0; h < kTqMaxG; ++h)
-            if (h < G) acc[d][h] = fmaf(s_p[h * kTqThreads + j], val, acc[d][h]);
+        for (int u = 0; u < 4; ++u) {
+          const int j = j0 + u * NKS;
+          if (j < nk) {
+            const float vn = s_vn[j * NB + blk];
+            float val[4];
+#pragma unroll
+            for (int d = 0; d < 4; ++d) val[d] = s_tab[((cw[u] >> (d * BITS)) & (LEVELS - 1)) * 32 + lane] * vn;
+#pragma unroll
+            for (int h = 0; h < GM; ++h) {
+              const float p = s_p[h * kTqThreads + j];
+#pragma unroll
+              for (int d = 0; d < 4; ++d) acc[d][h] = fmaf(p, val[d], acc[d][h]);
+            }
+          }
         }
       }
     }
     __syncthreads();
   }
 
-  // ---- the chunk's record: the key subsets added in order (through s_p), then m and l
+  // ---- the chunk's record: the key subsets added in order, then m and l
   float* rec = a.part + ((size_t)unit * a.splits + split) * 8 * RS;
   {
-    // [NKS][G][HD] floats: NKS * G * HD <= 8 * max(HD, 256), which the query area
-    // (8 HD floats) holds for HD >= 256 and the score area (8 * 256) for HD < 256; neither
-    // is read again by this CTA's key loop
-    float* red = HD >= kTqThreads ? s_q : s_p;
-    static_assert(NKS * kTqMaxG * HD <= (HD >= kTqThreads ? kTqMaxG * HD : kTqMaxG * kTqThreads),
-                  "the subset reduction must fit its buffer");
-    const int ks = tid / (HD >= kTqThreads ? kTqThreads : HD);
+    // [NKS][GM][HD] floats = 4 * 256 * GM: the query area (8 HD floats) holds it for
+    // HD >= 4 * 32 GM / 8..., the score area (8 * 256) always does for GM <= 2; use whichever
+    // fits, else two halves through the score area
+    float* red = s_p;
+    static_assert(NKS * HD == 4 * kTqThreads, "four dims per thread");
+    constexpr int HALF = GM * 4 * kTqThreads <= kTqMaxG * kTqThreads ? GM : kTqMaxG / 4;
+    for (int h0 = 0; h0 < GM; h0 += HALF) {
 #pragma unroll
-    for (int d = 0; d < DPT; ++d) {
-      const int i = (HD >= kTqThreads ? tid : tid % HD) + d * kTqThreads;
+      for (int d = 0; d < 4; ++d)
 #pragma unroll
-      for (int h = 0; h < kTqMaxG; ++h)
-        if (h < G) red[(ks * G + h) * HD + i] = acc[d][h];
-    }
-    __syncthreads();
-    for (int e = tid; e < G * HD; e += kTqThreads) {
-      const int h = e / HD, i = e - h * HD;
-      float sum = 0.f;
-      for (int s = 0; s < NKS; ++s) sum += red[(s * G + h) * HD + i];
-      rec[h * RS + i] = sum;
+        for (int h = 0; h < GM; ++h)
+          if (h >= h0 && h < h0 + HALF) red[((h - h0) * NKS + ks) * HD + d0 + d] = acc[d][h];
+      __syncthreads();
+      for (int e = tid; e < HALF * HD; e += kTqThreads) {
+        const int hh = e / HD, i = e - hh * HD;
+        float sum = 0.f;
+        for (int k2 = 0; k2 < NKS; ++k2) sum += red[(hh * NKS + k2) * HD + i];
+        if (h0 + hh < G) rec[(h0 + hh) * RS + i] = sum;
+      }
+      __syncthreads();
     }
     if (tid < G) {
       rec[tid * RS + HD] = s_m[tid];
@@ -475,13 +523,14 @@ __global__ void __launch_bounds__(kTqThreads) tq_attn_kernel(const TqAttnArgs a)
   // ---- the last chunk of the unit merges the records and undoes the rotation
   __threadfence();
   __syncthreads();
-  if (tid == 0) s_last = atomicAdd(a.ticket + unit, 1) == a.splits - 1;
+  if (tid == 0) *s_last = atomicAdd(a.ticket + unit, 1) == a.splits - 1;
   __syncthreads();
-  if (!s_last) return;
+  if (!*s_last) return;
   __threadfence();
   if (tid == 0) a.ticket[unit] = 0;
   const float* up = a.part + (size_t)unit * a.splits * 8 * RS;
-  float* s_o = s_q;  // [G][HD]: the merged output, rotated
+  // weight of chunk sp for head h: 2^(m_sp - M) / sum_sp' 2^(m_sp' - M) l_sp'
+  float* wsm = s_p;  // [G][splits]: kTqMaxG * kTqMaxSplits floats = the score area
   for (int h = warp; h < G; h += kTqThreads / 32) {
     float M = -INFINITY;
     for (int sp = lane; sp < a.splits; sp += 32) M = fmaxf(M, __ldcg(up + (sp * 8 + h) * RS + HD));
@@ -489,19 +538,45 @@ __global__ void __launch_bounds__(kTqThreads) tq_attn_kernel(const TqAttnArgs a)
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float Mu = M == -INFINITY ? 0.f : M;
     float den = 0.f;
-    for (int sp = lane; sp < a.splits; sp += 32)
-      den += exp2f(__ldcg(up + (sp * 8 + h) * RS + HD) - Mu) * __ldcg(up + (sp * 8 + h) * RS + HD + 1);
+    for (int sp = lane; sp < a.splits; sp += 32) {
+      const float f = exp2f(__ldcg(up + (sp * 8 + h) * RS + HD) - Mu);
+      wsm[h * a.splits + sp] = f;
+      den += f * __ldcg(up + (sp * 8 + h) * RS + HD + 1);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
     const float inv = den > 0.f ? 1.f / den : 0.f;
-    for (int i = lane; i < HD; i += 32) {
-      float v = 0.f;
-      for (int sp = 0; sp < a.splits; ++sp) {
-        const float w = exp2f(__ldcg(up + (sp * 8 + h) * RS + HD) - Mu);
-        v += w * __ldcg(up + (sp * 8 + h) * RS + i);
+    __syncwarp();
+    for (int sp = lane; sp < a.splits; sp += 32) wsm[h * a.splits + sp] *= inv;
+  }
+  __syncthreads();
+  // o[h][i] = sum_sp w[h][sp] O_sp[h][i]: one float4 column per thread, the chunks added
+  // in order, eight loads in flight at a time
+  float* s_o = s_q;  // [G][HD]: the merged output, rotated
+  constexpr int Q4 = HD / 4;
+  const int ncol = G * Q4;
+  for (int c = tid; c < ncol; c += kTqThreads) {
+    const int h = c / Q4, d4 = c - h * Q4;
+    float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sp0 = 0; sp0 < a.splits; sp0 += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int sp = sp0 + u < a.splits ? sp0 + u : a.splits - 1;  // in range
+        v[u] = __ldcg(reinterpret_cast<const float4*>(up + (sp * 8 + h) * RS) + d4);
       }
-      s_o[h * HD + i] = v * inv;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (sp0 + u < a.splits) {
+          const float w = wsm[h * a.splits + sp0 + u];
+          acc4.x = fmaf(w, v[u].x, acc4.x);
+          acc4.y = fmaf(w, v[u].y, acc4.y);
+          acc4.z = fmaf(w, v[u].z, acc4.z);
+          acc4.w = fmaf(w, v[u].w, acc4.w);
+        }
+      }
     }
+    reinterpret_cast<float4*>(s_o)[c] = acc4;
   }
   __syncthreads();
   smem_fwht_rows(s_o, G, HD, BLK, HD);  // the normalised FWHT is its own inverse
@@ -517,10 +592,22 @@ cudaError_t launch_append_t(const TqAppendArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+template <int HD, int BITS, bool KRAW, int GM>
+cudaError_t launch_gm(const TqAttnArgs& a, int grid, cudaStream_t s) {
+  auto kern = tq_attn_kernel<HD, BITS, KRAW, GM>;
+  const size_t smem = TqSmem<HD, BITS, KRAW, GM>::BYTES;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kTqThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
 template <int HD, int BITS, bool KRAW>
 cudaError_t launch_attn_t(const TqAttnArgs& a, int grid, cudaStream_t s) {
-  tq_attn_kernel<HD, BITS, KRAW><<<grid, kTqThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  const int G = a.nh / a.nkv;
+  if (G <= 2) return launch_gm<HD, BITS, KRAW, 2>(a, grid, s);
+  if (G <= 4) return launch_gm<HD, BITS, KRAW, 4>(a, grid, s);
+  return launch_gm<HD, BITS, KRAW, 8>(a, grid, s);
 }
 
 template <int HD>
@@ -657,7 +744,8 @@ namespace {
 // workspace: [status word + tickets, 256-byte aligned][records]
 size_t tq_ws_head(int units) { return ((size_t)(units + 1) * 4 + 255) / 256 * 256; }
 int tq_splits(int units, int max_keys, int sms) {
-  int S = (4 * sms + units - 1) / units;
+  int S = (8 * sms + units - 1) / units;  // many CTAs: the per-key work is latency-bound
+  if (S > kTqMaxSplits) S = kTqMaxSplits;
   const int tiles = (max_keys + kTqThreads - 1) / kTqThreads;
   if (S > tiles) S = tiles;
   if (S < 1) S = 1;
