@@ -65,7 +65,7 @@ class OrcDesc(ctypes.Structure):
         ("kv_capacity", ctypes.c_int), ("ring", ctypes.c_int),
         ("v_unit_norm", ctypes.c_int), ("weights_bf16", ctypes.c_int),
         ("k_eq_v", ctypes.c_int), ("rope_freq_factors", ctypes.c_void_p),
-        ("w_post", ctypes.c_void_p),
+        ("w_post", ctypes.c_void_p), ("block_bidir", ctypes.c_int),
     ]
 
 
@@ -117,6 +117,9 @@ def lib():
             L.orc_tq_decode_row.argtypes = [P, P, ctypes.c_int, ctypes.c_int, P, P]
             L.orc_attend_tq.argtypes = [P, ctypes.c_int, ctypes.c_int, P, P, P, P, P, P, P, P,
                                         ctypes.c_long, ctypes.c_double, ctypes.c_double, P]
+            L.orc_ctx_append.restype = ctypes.c_int
+            L.orc_ctx_append.argtypes = [ctypes.POINTER(OrcDesc), P, P, P, P, ctypes.c_int,
+                                         ctypes.c_int, P, P, P, P]
             L.orc_num_threads.restype = ctypes.c_int
             L.orc_set_num_threads.argtypes = [ctypes.c_int]
             _lib = L
@@ -169,7 +172,8 @@ def desc_from(w, weights: Optional[Dict] = None, keep: Optional[list] = None) ->
                    kv_capacity=w.kv_capacity, ring=int(w.ring), v_unit_norm=int(w.v_unit_norm),
                    weights_bf16=int(w.weights_bf16), k_eq_v=int(getattr(w, "k_eq_v", False)),
                    rope_freq_factors=None if ff is None else ff.ctypes.data,
-                   w_post=None if wp is None else wp.ctypes.data)
+                   w_post=None if wp is None else wp.ctypes.data,
+                   block_bidir=int(getattr(w, "block_bidir", False)))
 
 
 def _weight_np(w, t):
@@ -308,6 +312,26 @@ def verify_block(w, weights: Dict, x, base_pos, k_cache, v_cache) -> Dict[str, n
                                 _ptr(out["attn"]), _ptr(out["out"]), _ptr(out["out_bf16"]))
     if rc != 0:
         raise ValueError("oracle verify_block rejected its arguments")
+    out["k_cache"], out["v_cache"] = kc, vc
+    return out
+
+
+def ctx_append(w, weights: Dict, x_ctx, base_pos, k_cache, v_cache) -> Dict[str, np.ndarray]:
+    """The drafter's context rows appended to copies of the caches; returns k, v and caches."""
+    keep: list = []
+    d = desc_from(w, weights, keep)
+    H, nkv, hd = w.hidden, w.num_kv_heads, w.head_dim
+    xb = bf16_bits(x_ctx).reshape(-1, H)
+    S = xb.shape[0]
+    kc = bf16_bits(k_cache).copy()
+    vc = bf16_bits(v_cache).copy()
+    out = {"k": np.empty((S, nkv, hd)), "v": np.empty((S, nkv, hd))}
+    wk, wv = _weight_np(w, weights["wk"]), _weight_np(w, weights["wv"])
+    rc = lib().orc_ctx_append(ctypes.byref(d), _ptr(wk), _ptr(wv),
+                              _ptr(as_np(weights["w_k"], np.float32)), _ptr(xb), S, int(base_pos),
+                              _ptr(kc), _ptr(vc), _ptr(out["k"]), _ptr(out["v"]))
+    if rc != 0:
+        raise ValueError("oracle ctx_append rejected its arguments")
     out["k_cache"], out["v_cache"] = kc, vc
     return out
 

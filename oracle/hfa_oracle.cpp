@@ -337,9 +337,12 @@ int orc_verify_block(const orc_desc* d, const void* wq, const void* wk, const vo
   for (int i = 0; i < L; ++i)
     append_kv(d, k_cache, v_cache, base_pos + i, &k[(size_t)i * nkv * hd],
               &v[(size_t)i * nkv * hd]);
+  // row i sees positions <= base_pos + i (causal), or the whole block on a full layer of
+  // a bidirectional block [P3]
+  const bool bidir = d->block_bidir && d->layer_type == 1;
   for (int i = 0; i < L; ++i)
-    attend_token(d, k_cache, v_cache, base_pos + i, last, &q[(size_t)i * nh * hd],
-                 &o[(size_t)i * nh * hd]);
+    attend_token(d, k_cache, v_cache, bidir ? last : base_pos + i, last,
+                 &q[(size_t)i * nh * hd], &o[(size_t)i * nh * hd]);
   for (int i = 0; i < L; ++i)
     output_token(d, wo, x + (size_t)i * H, &o[(size_t)i * nh * hd],
                  out ? out + (size_t)i * H : nullptr,
@@ -348,6 +351,35 @@ int orc_verify_block(const orc_desc* d, const void* wq, const void* wk, const vo
   if (k_out) std::memcpy(k_out, k.data(), k.size() * sizeof(double));
   if (v_out) std::memcpy(v_out, v.data(), v.size() * sizeof(double));
   if (attn_out) std::memcpy(attn_out, o.data(), o.size() * sizeof(double));
+  return 0;
+}
+
+int orc_ctx_append(const orc_desc* d, const void* wk, const void* wv, const float* w_k,
+                   const uint16_t* x_ctx, int S, int base_pos, uint16_t* k_cache,
+                   uint16_t* v_cache, double* k_out, double* v_out) {
+  if (check_desc(d) || S <= 0 || base_pos < 0 || !x_ctx || !k_cache || !v_cache) return -1;
+  if (d->ring || (long)base_pos + S > d->kv_capacity) return -1;
+  int H = d->hidden, nkv = d->num_kv_heads, hd = d->head_dim;
+  std::vector<double> n(H), k((size_t)nkv * hd), v((size_t)nkv * hd), t(hd);
+  for (int r = 0; r < S; ++r) {
+    const long P = base_pos + r;
+    for (int i = 0; i < H; ++i) n[i] = orc_bf16_to_f64(x_ctx[(size_t)r * H + i]);  // no norm
+    matvec(d, wk, nkv * hd, H, n.data(), k.data());                             // [P3] k_proj
+    if (d->k_eq_v) std::memcpy(v.data(), k.data(), k.size() * sizeof(double));
+    else matvec(d, wv, nkv * hd, H, n.data(), v.data());                        // [P3] v_proj
+    for (int h = 0; h < nkv; ++h) {
+      orc_rmsnorm(&k[(size_t)h * hd], w_k, hd, d->eps, t.data());               // k_norm
+      std::memcpy(&k[(size_t)h * hd], t.data(), hd * sizeof(double));
+      orc_rope_neox_ff(&k[(size_t)h * hd], hd, (double)P, d->rope_theta, d->rope_freq_factors);
+      if (d->v_unit_norm || d->k_eq_v) {
+        orc_rmsnorm(&v[(size_t)h * hd], nullptr, hd, d->eps, t.data());
+        std::memcpy(&v[(size_t)h * hd], t.data(), hd * sizeof(double));
+      }
+    }
+    append_kv(d, k_cache, v_cache, P, k.data(), v.data());
+    if (k_out) std::memcpy(k_out + (size_t)r * nkv * hd, k.data(), k.size() * sizeof(double));
+    if (v_out) std::memcpy(v_out + (size_t)r * nkv * hd, v.data(), v.size() * sizeof(double));
+  }
   return 0;
 }
 

@@ -44,6 +44,10 @@ typedef struct {
   int k_eq_v;                      /* 1: no V projection; V = unit RMSNorm of the raw K */
   const float* rope_freq_factors;  /* NULL, or [hd/2]: phi_i = pos * theta^(-2i/hd) / f_i */
   const float* w_post;             /* NULL, or [hidden]: out = x + RMSNorm(y) * w_post */
+  /* [P3 dispatch_dflash_decoder_layer_attention: bidirectional within the block on full
+   * layers, causal + window on sliding ones]: 1 = every row of a verify block sees the
+   * whole block on a full layer */
+  int block_bidir;
 } orc_desc;
 
 /* ---- scalar formats ---- */
@@ -107,6 +111,15 @@ int orc_verify_block(const orc_desc* d, const void* wq, const void* wk, const vo
                      const uint16_t* x, int L, int base_pos, uint16_t* k_cache,
                      uint16_t* v_cache, double* q_out, double* k_out, double* v_out,
                      double* attn_out, double* out, uint16_t* out_bf16);
+
+/* ---- the drafter's context rows [P3 dispatch_dflash_decoder_layer_attention]: S rows
+ * x_ctx bf16 [S, H] (already normalised by the model: no input RMSNorm) projected by Wk
+ * and Wv only, k_norm + RoPE on k at positions base_pos .. base_pos+S-1, V as in the decode
+ * step (unit-normed with v_unit_norm or k_eq_v, the raw K with k_eq_v), appended as bf16.
+ * k_out, v_out (nullable) [S, nkv, hd] before rounding.  Returns 0, -1 on bad arguments. */
+int orc_ctx_append(const orc_desc* d, const void* wk, const void* wv, const float* w_k,
+                   const uint16_t* x_ctx, int S, int base_pos, uint16_t* k_cache,
+                   uint16_t* v_cache, double* k_out, double* v_out);
 
 /* number of OpenMP threads the oracle uses (1 when built without OpenMP) */
 int orc_num_threads(void);

@@ -67,6 +67,9 @@ class Workload:
     k_eq_v: bool = False
     rope_freq_factors: bool = False
     post_norm: bool = False
+    # the drafter's block attention: every row of a verify block sees the whole block on a
+    # full layer (sliding layers stay causal)
+    block_bidir: bool = False
 
     @property
     def group(self) -> int:
