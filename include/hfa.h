@@ -58,6 +58,9 @@ typedef enum { HFA_SLIDING = 0, HFA_FULL = 1 } hfa_layer_type;
 #define HFA_F_DEBUG_TAPS 0x8u   /* keep fp32 copies of q, k, v, attention and output */
 #define HFA_F_K_EQ_V 0x10u      /* no V projection: V = per-head unit RMSNorm of the raw K
                                    (Gemma global layers; model.rs, v_proj None when k_eq_v) */
+#define HFA_F_BLOCK_BIDIR 0x20u /* verify blocks of a FULL layer attend bidirectionally
+                                   within the block (the drafter's full-attention layers,
+                                   dflash/forward.rs); sliding layers stay causal */
 
 typedef struct {
   int hidden;       /* H: a multiple of 32 (whole Q8_0 blocks; HFA_EINVAL otherwise);
@@ -157,6 +160,22 @@ hfa_status hfa_decode_step_host(hfa_layer* layer, void* stream, const void* x_ho
  */
 hfa_status hfa_verify_block(hfa_layer* layer, void* stream, const void* x_dev, int L,
                             int base_pos, void* k_cache_dev, void* v_cache_dev, void* out_dev);
+
+/*
+ * The drafter's context rows (spec_decode/dflash/forward.rs,
+ * dispatch_dflash_decoder_layer_attention: k_ctx, v_ctx and their cache append): S rows
+ * x_ctx_dev bf16 [S, H], already normalised by the drafter model (no input RMSNorm here),
+ * projected by Wk and Wv only, k_norm and RoPE at positions base_pos .. base_pos+S-1, V as
+ * in the block (unit-normed with HFA_F_V_UNIT_NORM or HFA_F_K_EQ_V), appended as bf16 at
+ * those slots.  A drafter step is this call followed by hfa_verify_block of the L block
+ * rows at base_pos + S (their K/V land past the committed context, in the slack the
+ * caller does not commit), on a layer with HFA_F_BLOCK_BIDIR if it is a full layer, and
+ * attn_scale 1/sqrt(hd).  Needs a bf16-weight layer (as hfa_verify_block) and
+ * 1 <= S <= max_verify_len, base_pos + S <= kv_capacity.
+ * Errors: HFA_EINVAL, HFA_ERANGE, HFA_EUNSUPPORTED (ring cache, Q8_0 layer), HFA_ECUDA.
+ */
+hfa_status hfa_ctx_append(hfa_layer* layer, void* stream, const void* x_ctx_dev, int S,
+                          int base_pos, void* k_cache_dev, void* v_cache_dev);
 
 /*
  * The attention step alone ("Dense flash_attn_vec" of encode_one_layer), for callers

@@ -225,8 +225,8 @@ static hfa_status validate_desc(const hfa_layer_desc* d) {
     return fail(nullptr, HFA_EUNSUPPORTED, "verify: cache too large for 32-bit TMA rows");
   if (!(d->eps >= 0.f) || !(d->rope_theta > 0.f) || !(d->attn_scale > 0.f) || !(d->softcap >= 0.f))
     return fail(nullptr, HFA_EINVAL, "eps, rope_theta, attn_scale, softcap out of range");
-  if (d->flags &
-      ~(HFA_F_V_UNIT_NORM | HFA_F_WEIGHTS_BF16 | HFA_F_RING | HFA_F_DEBUG_TAPS | HFA_F_K_EQ_V))
+  if (d->flags & ~(HFA_F_V_UNIT_NORM | HFA_F_WEIGHTS_BF16 | HFA_F_RING | HFA_F_DEBUG_TAPS |
+                   HFA_F_K_EQ_V | HFA_F_BLOCK_BIDIR))
     return fail(nullptr, HFA_EINVAL, "unknown flags 0x%x", d->flags);
   return HFA_OK;
 }
@@ -869,6 +869,7 @@ extern "C" hfa_status hfa_verify_block(hfa_layer* L, void* stream, const void* x
   c.out_tap = L->out_tap;
   c.err = L->err;
   c.num_sms = L->num_sms;
+  c.bidir = (d.flags & HFA_F_BLOCK_BIDIR) ? 1 : 0;
   LayerTimer lt;
   lt.L = L;
   c.timer = L->timing ? &lt : nullptr;
@@ -876,6 +877,50 @@ extern "C" hfa_status hfa_verify_block(hfa_layer* L, void* stream, const void* x
   hfa_status st = hfa::verify_run(L->verify, c, msg, sizeof msg);
   if (st != HFA_OK) return fail(L, st, "%s", msg);
   L->last_rows = Lt;
+  return HFA_OK;
+}
+
+extern "C" hfa_status hfa_ctx_append(hfa_layer* L, void* stream, const void* x, int S, int base_pos,
+                                     void* kc, void* vc) {
+  if (!L) return HFA_EINVAL;
+  const hfa_layer_desc& d = L->d;
+  if (d.max_verify_len <= 0 || !L->verify)
+    return fail(L, HFA_EINVAL, "layer created with max_verify_len = 0");
+  if (!x || !kc || !vc) return fail(L, HFA_EINVAL, "a pointer argument is NULL");
+  if (S < 1 || S > d.max_verify_len)
+    return fail(L, HFA_EINVAL, "S=%d outside [1, max_verify_len=%d]", S, d.max_verify_len);
+  if (d.flags & HFA_F_RING) return fail(L, HFA_EUNSUPPORTED, "context rows need a linear cache");
+  if (base_pos < 0 || (long long)base_pos + S > d.kv_capacity)
+    return fail(L, HFA_ERANGE, "positions %d..%d outside the cache (capacity %d)", base_pos,
+                base_pos + S - 1, d.kv_capacity);
+  if (!aligned16(x) || !aligned16(kc) || !aligned16(vc))
+    return fail(L, HFA_EINVAL, "x_ctx and the caches must be 16-byte aligned");
+  if (!(d.flags & HFA_F_WEIGHTS_BF16))
+    return fail(L, HFA_EUNSUPPORTED, "context rows need bf16 weights");
+  hfa::VerifyCall c{};
+  c.d = &L->d;
+  c.stream = (cudaStream_t)stream;
+  c.x = (const __nv_bfloat16*)x;
+  c.L = S;
+  c.base_pos = base_pos;
+  c.k_cache = (__nv_bfloat16*)kc;
+  c.v_cache = (__nv_bfloat16*)vc;
+  c.wqkv = L->wqkv_bf16;
+  c.w_q = L->w_q;
+  c.w_k = L->w_k;
+  c.rope_g = L->rope_g;
+  c.q_f32 = L->q_f32;
+  c.k_tap = L->k_tap;
+  c.v_tap = L->v_tap;
+  c.err = L->err;
+  c.num_sms = L->num_sms;
+  LayerTimer lt;
+  lt.L = L;
+  c.timer = L->timing ? &lt : nullptr;
+  char msg[256] = {0};
+  hfa_status st = hfa::verify_ctx_append(L->verify, c, msg, sizeof msg);
+  if (st != HFA_OK) return fail(L, st, "%s", msg);
+  L->last_rows = S;
   return HFA_OK;
 }
 

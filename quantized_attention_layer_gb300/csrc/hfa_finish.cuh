@@ -29,6 +29,7 @@ static __device__ __forceinline__ void finish_head_row(const GemvArgs& a, int hh
                                        int lane) {
   constexpr int J = HD / 32;   // values per lane; pairs (j, j + J/2) are RoPE partners
   const int kind = hh < a.nh ? 0 : (hh < a.nh + a.nkv ? 1 : 2);  // q, k, v
+  if (kind == 0 && a.kv_only) return;
   const int seq = a.rows_are_tokens ? 0 : b;
   const int P = a.rows_are_tokens ? a.base_pos + b : a.seq_pos[b];
   if (kind == 1 && a.k_eq_v && P >= 0 && (a.ring || P < a.C)) {

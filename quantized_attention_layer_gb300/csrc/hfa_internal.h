@@ -34,6 +34,7 @@ struct GemvArgs {
   const int* seq_pos;      // [B]
   int v_unit_norm;
   int k_eq_v;              // the key finisher also writes V = unit RMSNorm of the raw K
+  int kv_only;             // rows of query heads are skipped (context rows: K and V only)
   float* q_out;            // f32 [B, nh, hd]
   uint8_t* qx;             // nullable: the scaled q as the verify attention's tensor-core
                            // operand, [nkv][2 boxes][128 rows][128 B] (see finish_head_row)

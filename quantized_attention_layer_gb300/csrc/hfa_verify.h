@@ -34,11 +34,15 @@ struct VerifyCall {
   unsigned* err;
   int num_sms;
   LaunchTimer* timer;  // nullable; when set, launches are timed and not PDL-chained
+  int bidir;           // full layer: every row sees the whole block (the drafter's blocks)
 };
 
 hfa_status verify_create(const hfa_layer_desc& d, int num_sms, VerifyState** out);
 void verify_free(VerifyState* v);
 const char* verify_error();
 hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int msg_len);
+// the drafter's context rows: c.x holds c.L rows, projected by Wk and Wv only (no input
+// norm), k_norm + RoPE, appended at c.base_pos ..; q, attention and o_proj are not run
+hfa_status verify_ctx_append(VerifyState* v, const VerifyCall& c, char* msg, int msg_len);
 
 }  // namespace hfa

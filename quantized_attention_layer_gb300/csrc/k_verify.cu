@@ -78,6 +78,7 @@ struct VGemmArgs {
   int chunks;        // K / 64
   int splits;        // k-splits per row tile
   int tpc;           // row tiles per cluster: hd / 128 for QKV heads wider than a tile, else 1
+  int tile_base;     // first row tile (the context rows start at the key rows' tile)
 };
 
 // Activation operand of the verify GEMMs, built once per call: row t of the block
@@ -112,14 +113,15 @@ __global__ void __launch_bounds__(256) verify_prep_kernel(const __nv_bfloat16* _
     __syncthreads();
     float tot = 0.f;
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += s_red[w];
-    inv = rsqrtf(tot / K + eps);
+    inv = w_in ? rsqrtf(tot / K + eps) : 1.f;  // context rows (w_in NULL): no input norm
   }
   for (int e = threadIdx.x; e < ngroups; e += blockDim.x) {
     float v[8];
     if (t < L) {
       const uint4 raw = *reinterpret_cast<const uint4*>(x + (size_t)t * K + e * 8);
-      const float4 w0 = __ldg(reinterpret_cast<const float4*>(w_in + e * 8));
-      const float4 w1 = __ldg(reinterpret_cast<const float4*>(w_in + e * 8 + 4));
+      const float4 one = make_float4(1.f, 1.f, 1.f, 1.f);
+      const float4 w0 = w_in ? __ldg(reinterpret_cast<const float4*>(w_in + e * 8)) : one;
+      const float4 w1 = w_in ? __ldg(reinterpret_cast<const float4*>(w_in + e * 8 + 4)) : one;
       const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
       const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
@@ -149,7 +151,7 @@ __global__ void __launch_bounds__(128, 1) verify_gemm_kernel(const VGemmArgs a) 
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(done + 1);
   float* s_tab = reinterpret_cast<float*>(ring + kVStages * kVStageBytes + 256);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mt = blockIdx.x / a.splits, sp = blockIdx.x - mt * a.splits;
+  const int mt = a.tile_base + blockIdx.x / a.splits, sp = blockIdx.x % a.splits;
   const int c0 = a.chunks * sp / a.splits, c1 = a.chunks * (sp + 1) / a.splits;
   const int nch = c1 - c0;
   const int m0 = mt * kVM;
@@ -341,6 +343,7 @@ constexpr int kVT = 64;  // keys per stage
 struct VAttnArgs {
   const float* q;  // [L, nh, hd]
   int L, nh, nkv, G, C, base, sliding, window;
+  int bidir;       // every row sees the whole block (full layers of the drafter)
   float qscale, cap_log2;
   int splits, chunk, klo, khi;  // keys [klo, khi] are read by some row
   float* part;                  // [nkv][splits][64 rows][hd + 4]: O[hd], m, l, pad
@@ -441,7 +444,7 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
     const int qrow = 8 * warp + g;
     const bool qvalid = qrow < NQ;
     const int tok = qvalid ? qrow / a.G : 0;
-    const int limit = a.base + tok;  // last visible position of this row
+    const int limit = a.bidir ? a.base + a.L - 1 : a.base + tok;  // last visible position
     uint4* myq = qf + warp * Cfg::KS * 32;
     for (int ks = 0; ks < Cfg::KS; ++ks) {
       uint32_t w[4] = {0u, 0u, 0u, 0u};
@@ -786,7 +789,7 @@ __global__ void __launch_bounds__(vtc::THREADS, 1)
     const int lo = r >= 64 ? 1 : 0;        // row holds the lo part
     const bool qvalid = q < NQ;
     const int tok = qvalid ? q / a.G : 0;
-    const int limit = a.base + tok;
+    const int limit = a.bidir ? a.base + a.L - 1 : a.base + tok;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const int part = 2 * hf + lo;          // this thread's 16 keys of the stage: 16 part ..
     float m = -INFINITY, l = 0.f;
@@ -1260,6 +1263,72 @@ static int gemm_splits(int tiles, int chunks, int num_sms, int tpc, const int* m
   return S;
 }
 
+hfa_status verify_ctx_append(VerifyState* v, const VerifyCall& c, char* msg, int n) {
+  const hfa_layer_desc& d = *c.d;
+  const int H = d.hidden, nh = d.num_heads, nkv = d.num_kv_heads, hd = d.head_dim;
+  const int rows_qkv = qkv_rows(d);
+  if (!(d.flags & HFA_F_WEIGHTS_BF16) || !v->part) {
+    snprintf(msg, n, "context rows need the bf16 (verify) weights");
+    return HFA_EUNSUPPORTED;
+  }
+  cudaStream_t s = c.stream;
+  const bool pdl = c.timer == nullptr;
+  auto tb = [&](const char* nm) { if (c.timer) c.timer->begin(s, nm); };
+  auto te = [&]() { if (c.timer) c.timer->end(s); };
+  // (0) the rows as they are (w_in NULL: no input norm), bf16 hi/lo operand
+  tb("ctx_prep");
+  cudaError_t e = launch_ex(verify_prep_kernel, 16, 256, 0, pdl, s, c.x, (const float*)nullptr,
+                            d.eps, c.L, H, v->bq);
+  te();
+  if (e != cudaSuccess) {
+    snprintf(msg, n, "context prep launch: %s", cudaGetErrorString(e));
+    return HFA_ECUDA;
+  }
+  // (1) the K and V rows only: row tiles from the one holding the first key row
+  VGemmArgs qa{};
+  qa.bops = v->bq;
+  qa.wt = reinterpret_cast<const uint8_t*>(c.wqkv);
+  qa.g.batch = c.L;
+  qa.g.x = c.x;
+  qa.g.eps = d.eps;
+  qa.g.R = rows_qkv / 16;
+  qa.g.err = c.err;
+  qa.g.nh = nh;
+  qa.g.nkv = nkv;
+  qa.g.hd = hd;
+  qa.g.C = d.kv_capacity;
+  qa.g.w_q = c.w_q;
+  qa.g.w_k = c.w_k;
+  qa.g.rope_g = c.rope_g;
+  qa.g.v_unit_norm = (d.flags & HFA_F_V_UNIT_NORM) ? 1 : 0;
+  qa.g.k_eq_v = (d.flags & HFA_F_K_EQ_V) ? 1 : 0;
+  qa.g.kv_only = 1;
+  qa.g.q_out = c.q_f32;
+  qa.g.G = nh / nkv;
+  qa.g.k_cache = c.k_cache;
+  qa.g.v_cache = c.v_cache;
+  qa.g.k_tap = c.k_tap;
+  qa.g.v_tap = c.v_tap;
+  qa.g.rows_are_tokens = 1;
+  qa.g.base_pos = c.base_pos;
+  qa.rows = rows_qkv;
+  qa.K = H;
+  qa.chunks = H / kVK;
+  qa.tpc = hd > kVM ? hd / kVM : 1;
+  qa.tile_base = (nh * hd / kVM) / qa.tpc * qa.tpc;  // aligned to the clusters of a head
+  const int ktiles = rows_qkv / kVM - qa.tile_base;
+  qa.splits = gemm_splits(ktiles, qa.chunks, c.num_sms, qa.tpc, v->max_clusters);
+  tb("ctx_kv_gemm");
+  e = launch_ex2(verify_gemm_kernel<kModeQKV>, dim3(ktiles * qa.splits), 128, kVGemmSmem, pdl, s,
+                 qa.splits * qa.tpc, qa);
+  te();
+  if (e != cudaSuccess) {
+    snprintf(msg, n, "context K/V launch: %s", cudaGetErrorString(e));
+    return HFA_ECUDA;
+  }
+  return HFA_OK;
+}
+
 hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   const hfa_layer_desc& d = *c.d;
   const int H = d.hidden, nh = d.num_heads, nkv = d.num_kv_heads, hd = d.head_dim;
@@ -1350,6 +1419,7 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   aa.C = d.kv_capacity;
   aa.base = c.base_pos;
   aa.sliding = d.layer_type == HFA_SLIDING;
+  aa.bidir = c.bidir && d.layer_type == HFA_FULL;
   aa.window = d.window;
   const float log2e = 1.4426950408889634f;
   if (d.softcap > 0.f) {

@@ -30,6 +30,7 @@ HFA_F_WEIGHTS_BF16 = 0x2
 HFA_F_RING = 0x4
 HFA_F_DEBUG_TAPS = 0x8
 HFA_F_K_EQ_V = 0x10
+HFA_F_BLOCK_BIDIR = 0x20
 
 
 class HfaError(RuntimeError):
@@ -83,6 +84,8 @@ def lib():
         L.hfa_decode_step_host.argtypes = [P, P, P, P, I, P, P, P]
         L.hfa_verify_block.restype = C
         L.hfa_verify_block.argtypes = [P, P, P, I, I, P, P, P]
+        L.hfa_ctx_append.restype = C
+        L.hfa_ctx_append.argtypes = [P, P, P, I, I, P, P]
         L.hfa_destroy.restype = C
         L.hfa_destroy.argtypes = [P]
         L.hfa_set_successor.restype = C
@@ -331,6 +334,12 @@ class Layer:
         self._check(lib().hfa_verify_block(self._h, _stream_ptr(stream), _ptr(x), int(x.shape[0]),
                                            int(base_pos), _ptr(k_cache), _ptr(v_cache), _ptr(out)))
         return out
+
+    def hfa_ctx_append(self, x_ctx: torch.Tensor, base_pos: int, k_cache: torch.Tensor,
+                       v_cache: torch.Tensor, stream=None) -> None:
+        self._check(lib().hfa_ctx_append(self._h, _stream_ptr(stream), _ptr(x_ctx),
+                                         int(x_ctx.shape[0]), int(base_pos), _ptr(k_cache),
+                                         _ptr(v_cache)))
 
     def hfa_debug_taps(self, rows: int, stream=None) -> Dict[str, torch.Tensor]:
         d = self.desc

@@ -35,6 +35,7 @@ F_V_UNIT_NORM = 1 << 0
 F_WEIGHTS_BF16 = 1 << 1
 F_RING = 1 << 2
 F_K_EQ_V = 1 << 4
+F_BLOCK_BIDIR = 1 << 5
 
 
 @dataclasses.dataclass(frozen=True)
@@ -94,6 +95,8 @@ class Workload:
             f |= F_RING
         if self.k_eq_v:
             f |= F_K_EQ_V
+        if self.block_bidir:
+            f |= F_BLOCK_BIDIR
         return f
 
     def replace(self, **kw) -> "Workload":

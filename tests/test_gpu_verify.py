@@ -1,9 +1,10 @@
 """GPU parity of the multi-token verify block (tcgen05 projections) against the oracle."""
+import numpy as np
 import pytest
 import torch
 
 import oracle
-from quantized_attention_layer_gb300 import workloads as wl
+from quantized_attention_layer_gb300 import hfa, workloads as wl
 
 from parity import check_verify, run_gpu_verify
 
@@ -106,3 +107,77 @@ def test_verify_block_repeats_bit_for_bit():
     b = run_gpu_verify(w, weights, x, w.base_pos, kv)
     for key in ("out_bf16", "q", "k", "v", "attn", "out"):
         assert torch.equal(a[key], b[key]), key
+
+
+# ---------------------------------------------------------------- the drafter's blocks
+
+def test_bidirectional_block_full_size():
+    w = wl.VERIFY_L16.replace(name="ver_bidir", block_bidir=True)
+    _case(w, w.verify_len, w.base_pos)
+
+
+@pytest.mark.parametrize("hd", [64, 128, 256])
+def test_bidirectional_block_head_dims(hd):
+    w = wl.Workload(name=f"bidir{hd}", hidden=1024, num_heads=8, num_kv_heads=2, head_dim=hd,
+                    layer_type=wl.FULL, window=0, kv_capacity=700, ring=False, batch=1,
+                    rope_theta=1e6, seed=99, weights_bf16=True, verify_len=16, base_pos=0,
+                    block_bidir=True)
+    _case(w, 11, 350)
+
+
+def _drafter_step(w, S, L, base):
+    """Context rows then the block, on the GPU and in the oracle; both checked."""
+    from parity import bits_of, check_verify, flip_bound, rel_l2
+    weights = wl.make_weights(w)
+    g = torch.Generator().manual_seed(w.seed + 5)
+    x_ctx = wl.bf16_normal((S, w.hidden), g)
+    x = wl.make_x(w, rows=L)
+    kv = wl.make_kv_cache(w)
+    layer = hfa.Layer(hfa.desc_for(w, debug_taps=True), hfa.weights_to_device(w, weights))
+    kc, vc = kv["k_cache"].cuda(), kv["v_cache"].cuda()
+    layer.hfa_ctx_append(x_ctx.cuda(), base, kc, vc)
+    taps = layer.hfa_debug_taps(S)
+    torch.cuda.synchronize()
+    ref_ctx = oracle.ctx_append(w, weights, x_ctx, base, kv["k_cache"], kv["v_cache"])
+    n_flip, expected = 0, 0.0
+    for key in ("k", "v"):
+        got = taps[key].cpu().numpy()
+        assert rel_l2(got, ref_ctx[key]) <= 2e-3
+        cache = bits_of((kc if key == "k" else vc).cpu()).reshape(w.num_kv_heads, w.kv_capacity, w.head_dim)
+        own = np.array([oracle.f64_to_bf16(float(t)) for t in got.ravel()], dtype=np.uint16)
+        rows = cache[:, base:base + S, :].transpose(1, 0, 2).ravel()
+        assert np.array_equal(rows, own), "context bytes are not the RNE of the kernel's fp32"
+        ref_rows = ref_ctx[key + "_cache"].reshape(cache.shape)[:, base:base + S, :].transpose(1, 0, 2).ravel()
+        n_flip += int((rows != ref_rows).sum())
+        expected += flip_bound(got, ref_ctx[key])[0]
+    assert n_flip <= expected + 4 * np.sqrt(expected) + 4
+    kv_mid = {"k_cache": kc.cpu(), "v_cache": vc.cpu()}
+    out = torch.empty((L, w.hidden), dtype=torch.bfloat16, device="cuda")
+    layer.hfa_verify_block(x.cuda(), base + S, kc, vc, out)
+    layer.hfa_check_device_status()
+    gpu = {"out_bf16": out, "k_cache": kc, "v_cache": vc}
+    gpu.update(layer.hfa_debug_taps(L))
+    torch.cuda.synchronize()
+    gpu = {k: v.cpu() for k, v in gpu.items()}
+    layer.hfa_destroy()
+    kc_ref = torch.from_numpy(ref_ctx["k_cache"].view(np.int16)).view(torch.bfloat16)
+    vc_ref = torch.from_numpy(ref_ctx["v_cache"].view(np.int16)).view(torch.bfloat16)
+    ref = oracle.verify_block(w, weights, x, base + S, kc_ref, vc_ref)
+    return check_verify(w, base + S, gpu, ref, kv_mid)
+
+
+def test_drafter_step_full_layer():
+    # context rows, then a bidirectional block with the drafter's 1/sqrt(hd) scale
+    w = wl.Workload(name="draft_full", hidden=1024, num_heads=8, num_kv_heads=2, head_dim=128,
+                    layer_type=wl.FULL, window=0, kv_capacity=600, ring=False, batch=1,
+                    rope_theta=1e6, seed=101, weights_bf16=True, verify_len=16, base_pos=0,
+                    block_bidir=True, attn_scale=128 ** -0.5)
+    _drafter_step(w, S=5, L=8, base=300)
+
+
+def test_drafter_step_sliding_layer_stays_causal():
+    w = wl.Workload(name="draft_sl", hidden=1024, num_heads=8, num_kv_heads=4, head_dim=256,
+                    layer_type=wl.SLIDING, window=64, kv_capacity=500, ring=False, batch=1,
+                    rope_theta=1e4, seed=102, weights_bf16=True, verify_len=16, base_pos=0,
+                    block_bidir=True, attn_scale=256 ** -0.5)
+    _drafter_step(w, S=16, L=8, base=200)
