@@ -120,6 +120,11 @@ def lib():
             L.orc_ctx_append.restype = ctypes.c_int
             L.orc_ctx_append.argtypes = [ctypes.POINTER(OrcDesc), P, P, P, P, ctypes.c_int,
                                          ctypes.c_int, P, P, P, P]
+            L.orc_gelu_tanh.restype = ctypes.c_double
+            L.orc_gelu_tanh.argtypes = [ctypes.c_double]
+            L.orc_ffn_step.restype = ctypes.c_int
+            L.orc_ffn_step.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_double, P, P, P, P, P,
+                                       P, ctypes.c_int, P, ctypes.c_int, P, P, P]
             L.orc_num_threads.restype = ctypes.c_int
             L.orc_set_num_threads.argtypes = [ctypes.c_int]
             _lib = L
@@ -333,6 +338,26 @@ def ctx_append(w, weights: Dict, x_ctx, base_pos, k_cache, v_cache) -> Dict[str,
     if rc != 0:
         raise ValueError("oracle ctx_append rejected its arguments")
     out["k_cache"], out["v_cache"] = kc, vc
+    return out
+
+
+def gelu_tanh(x: float) -> float:
+    return float(lib().orc_gelu_tanh(float(x)))
+
+
+def ffn_step(f, weights: Dict, h) -> Dict[str, np.ndarray]:
+    """The dense FFN half for the rows of h (bf16 [B, H]); returns a, out and out_bf16."""
+    H, I = f.hidden, f.intermediate
+    hb = bf16_bits(h).reshape(-1, H)
+    B = hb.shape[0]
+    out = {"a": np.empty((B, I)), "out": np.empty((B, H)), "out_bf16": np.empty((B, H), dtype=np.uint16)}
+    wg, wu, wd = (as_np(weights[n], np.uint8) for n in ("w_gate", "w_up", "w_down"))
+    norms = [as_np(weights[n], np.float32) for n in ("w_pre", "w_post", "scalar")]
+    rc = lib().orc_ffn_step(H, I, float(f.eps), _ptr(wg), _ptr(wu), _ptr(wd), _ptr(norms[0]),
+                            _ptr(norms[1]), _ptr(norms[2]), norms[2].size, _ptr(hb), B,
+                            _ptr(out["a"]), _ptr(out["out"]), _ptr(out["out_bf16"]))
+    if rc != 0:
+        raise ValueError("oracle ffn_step rejected its arguments")
     return out
 
 

@@ -383,6 +383,38 @@ int orc_ctx_append(const orc_desc* d, const void* wk, const void* wv, const floa
   return 0;
 }
 
+double orc_gelu_tanh(double x) {
+  const double c = std::sqrt(2.0 / M_PI);
+  return 0.5 * x * (1.0 + std::tanh(c * (x + 0.044715 * x * x * x)));
+}
+
+int orc_ffn_step(int H, int I, double eps, const uint8_t* wg, const uint8_t* wu,
+                 const uint8_t* wd, const float* w_pre, const float* w_post,
+                 const float* scalar, int scalar_len, const uint16_t* h, int B, double* a_out,
+                 double* out, uint16_t* out_bf16) {
+  if (H <= 0 || I <= 0 || H % 32 || I % 32 || B <= 0 || !wg || !wu || !wd || !w_pre ||
+      !w_post || !scalar || (scalar_len != 1 && scalar_len != H) || !h)
+    return -1;
+  std::vector<double> x(H), n(H), g(I), u(I), a(I), d(H);
+  for (int b = 0; b < B; ++b) {
+    for (int i = 0; i < H; ++i) x[i] = orc_bf16_to_f64(h[(size_t)b * H + i]);
+    orc_rmsnorm(x.data(), w_pre, H, eps, n.data());            // [P1] pre-FF norm
+    orc_q8_0_matvec(wg, I, H, n.data(), g.data());             // [P1] dense gate
+    orc_q8_0_matvec(wu, I, H, n.data(), u.data());             // [P1] dense up
+    for (int i = 0; i < I; ++i) a[i] = orc_gelu_tanh(g[i]) * u[i];  // [P1] fused_gelu_mul
+    orc_q8_0_matvec(wd, H, I, a.data(), d.data());             // [P1] dense down
+    std::vector<double> dn(H);
+    orc_rmsnorm(d.data(), w_post, H, eps, dn.data());          // [P1] post-FF norm
+    for (int i = 0; i < H; ++i) {                              // [P1] end of layer
+      const double r = (x[i] + dn[i]) * (double)scalar[scalar_len == 1 ? 0 : i];
+      if (out) out[(size_t)b * H + i] = r;
+      if (out_bf16) out_bf16[(size_t)b * H + i] = orc_f64_to_bf16(r);
+    }
+    if (a_out) std::memcpy(a_out + (size_t)b * I, a.data(), I * sizeof(double));
+  }
+  return 0;
+}
+
 int orc_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

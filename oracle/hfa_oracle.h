@@ -121,6 +121,20 @@ int orc_ctx_append(const orc_desc* d, const void* wk, const void* wv, const floa
                    const uint16_t* x_ctx, int S, int base_pos, uint16_t* k_cache,
                    uint16_t* v_cache, double* k_out, double* v_out);
 
+/* ---- the dense FFN half of the layer [P1 encode_one_layer, groups B8-B11 and the
+ * end-of-layer norm: pre-FF RMSNorm, dense gate and up projections, fused_gelu_mul, the
+ * down projection, the post-FF RMSNorm added to the residual, the layer scalar]:
+ *   n = h * w_pre / sqrt(mean(h^2) + eps);  a = gelu(Wg n) * (Wu n);  d = Wd a;
+ *   out = (h + d * w_post / sqrt(mean(d^2) + eps)) * s,
+ * gelu(x) = x/2 (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))), s the layer scalar (one value,
+ * or one per channel when scalar_len == H).  Wg, Wu Q8_0 [I, H]; Wd Q8_0 [H, I];
+ * h bf16 [B, H].  Outputs (nullable): a [B, I], out [B, H] and its bf16 rounding. */
+double orc_gelu_tanh(double x);
+int orc_ffn_step(int H, int I, double eps, const uint8_t* wg, const uint8_t* wu,
+                 const uint8_t* wd, const float* w_pre, const float* w_post,
+                 const float* scalar, int scalar_len, const uint16_t* h, int B, double* a_out,
+                 double* out, uint16_t* out_bf16);
+
 /* number of OpenMP threads the oracle uses (1 when built without OpenMP) */
 int orc_num_threads(void);
 void orc_set_num_threads(int n);

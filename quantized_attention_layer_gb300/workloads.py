@@ -137,16 +137,18 @@ def _gen(seed: int, stream: int) -> torch.Generator:
     return torch.Generator().manual_seed(seed * 1000 + stream)
 
 
-def q8_0_blocks(rows: int, cols: int, g: torch.Generator) -> np.ndarray:
+def q8_0_blocks(rows: int, cols: int, g: torch.Generator, d_mean: Optional[float] = None) -> np.ndarray:
     """Random Q8_0 matrix ``[rows, cols]`` as raw bytes ``uint8 [rows, cols/32*34]``.
 
     Byte layout per 32-value block: bytes 0-1 the fp16 scale (little endian),
-    bytes 2..33 the 32 signed 8-bit values in column order.
+    bytes 2..33 the 32 signed 8-bit values in column order.  Scales ~U[0.001, 0.02], or
+    ~U[0.5, 1.5] * d_mean when d_mean is given.
     """
     assert cols % 32 == 0
     nb = cols // 32
     q = torch.randint(-127, 128, (rows, nb, 32), generator=g, dtype=torch.int8)
-    d = (torch.rand((rows, nb), generator=g, dtype=torch.float32) * 0.019 + 0.001).to(torch.float16)
+    u = torch.rand((rows, nb), generator=g, dtype=torch.float32)
+    d = (u * 0.019 + 0.001 if d_mean is None else (u + 0.5) * d_mean).to(torch.float16)
     out = np.empty((rows, nb, 34), dtype=np.uint8)
     out[:, :, 0:2] = d.numpy().view(np.uint8).reshape(rows, nb, 2)
     out[:, :, 2:] = q.numpy().view(np.uint8)
@@ -224,3 +226,46 @@ def make_tq_signs(head_dim: int, seed: int) -> np.ndarray:
     """The +-1 sign pre-multiply of a quantised-KV format (int8 [head_dim]), seeded."""
     g = _gen(seed, 60)
     return (torch.randint(0, 2, (head_dim,), generator=g, dtype=torch.int8) * 2 - 1).numpy()
+
+
+@dataclasses.dataclass(frozen=True)
+class FfnWorkload:
+    """The dense FFN half of a layer: hidden H, intermediate I, batch rows."""
+
+    name: str
+    hidden: int
+    intermediate: int
+    batch: int
+    seed: int
+    eps: float = 1e-6
+    scalar_per_channel: bool = False
+
+    def replace(self, **kw) -> "FfnWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+# the dense MLP of the pages' decode (2816 -> 5760 gate and up, back to 2816), batch 1
+FFN_B1 = FfnWorkload(name="ffn_b1", hidden=2816, intermediate=5760, batch=1, seed=6)
+
+
+def make_ffn_weights(f: FfnWorkload) -> Dict[str, object]:
+    """Q8_0 gate, up [I, H] and down [H, I], f32 norm weights ~U[0.5, 1.5], the layer
+    scalar ~U[0.5, 1.5] (one value or one per channel).  The Q8_0 scales are sized so that
+    each weight has standard deviation about 1/sqrt(fan-in) (q ~U{-127..127} has standard
+    deviation ~73.3): the gate pre-activations are then O(1), where GELU is not linear."""
+    H, I = f.hidden, f.intermediate
+    q_std = 73.3
+    out: Dict[str, object] = {
+        "w_gate": q8_0_blocks(I, H, _gen(f.seed, 70), d_mean=1.0 / (q_std * H ** 0.5)),
+        "w_up": q8_0_blocks(I, H, _gen(f.seed, 71), d_mean=1.0 / (q_std * H ** 0.5)),
+        "w_down": q8_0_blocks(H, I, _gen(f.seed, 72), d_mean=1.0 / (q_std * I ** 0.5)),
+        "w_pre": norm_weight(H, _gen(f.seed, 73)),
+        "w_post": norm_weight(H, _gen(f.seed, 74)),
+        "scalar": norm_weight(H if f.scalar_per_channel else 1, _gen(f.seed, 75)),
+    }
+    return out
+
+
+def make_ffn_input(f: FfnWorkload, rows: Optional[int] = None) -> torch.Tensor:
+    """The FFN input h (the attention half's output), bf16 [rows, H] ~N(0, 1)."""
+    return bf16_normal((rows or f.batch, f.hidden), _gen(f.seed, 76))
