@@ -293,6 +293,69 @@ hfa_status hfa_attention_decode_tq(const hfa_attn_desc* desc, const hfa_tq* fmt,
                                    size_t workspace_bytes, float* o_dev);
 
 /*
+ * ---- The dense feed-forward half of a layer (gemma4/gpu_full_attn.rs, encode_one_layer:
+ * the dense MLP -- pre-feed-forward RMSNorm, gate and up projections, fused_gelu_mul,
+ * down projection -- and the end of the layer: RMSNorm of the down output with
+ * post_feedforward_layernorm, residual add, layer_scalar).  For each batch row h:
+ *   n = h * w_pre / sqrt(mean(h^2) + eps) ;  a = gelu(Wg n) * (Wu n) ;  d = Wd a ;
+ *   out = (h + d * w_post / sqrt(mean(d^2) + eps)) * s,
+ * gelu(x) = x/2 (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) (the tanh form; the pages name
+ * the fused kernel without printing its formula), s the layer scalar: one value or one
+ * per channel.  The MoE branch of the pages' 26B model is not part of this object.
+ */
+typedef struct hfa_ffn hfa_ffn; /* opaque; owned by the library */
+typedef struct {
+  int hidden;       /* H: a positive multiple of 32 (HFA_EINVAL otherwise) */
+  int intermediate; /* I: a positive multiple of 32 (HFA_EINVAL otherwise) */
+  float eps;        /* RMSNorm epsilon of both norms, >= 0 */
+  int scalar_len;   /* 1 (one layer scalar) or H (one per channel) */
+  int max_batch;    /* largest batch of hfa_ffn_step, 1..16; sizes the scratch and the
+                       weights' tile order (HFA_EUNSUPPORTED outside) */
+} hfa_ffn_desc;
+
+/*
+ * Create the FFN half.  Weights are read from device memory and copied (Q8_0 re-laid out
+ * in MMA tiles; the values are untouched) into library-owned memory; the caller may free
+ * them when the call returns.  Synchronises `stream`; allocates (the only FFN call that
+ * does).
+ *   w_gate_dev, w_up_dev  Q8_0 [I, H] (rows of H/32 blocks of 34 bytes: fp16 scale d,
+ *                         little endian, then 32 int8 q; value = d * q)
+ *   w_down_dev            Q8_0 [H, I]
+ *   w_pre_dev, w_post_dev f32 [H];  scalar_dev f32 [scalar_len]
+ * Errors: HFA_EINVAL (shape, NULL pointer), HFA_EUNSUPPORTED (max_batch, a shape the
+ * kernel's buffers cannot plan), HFA_EDEVICE (no sm_103 device), HFA_ENOMEM, HFA_ECUDA.
+ * Messages via hfa_ffn_last_error(NULL).  *out is NULL on error.
+ */
+hfa_status hfa_ffn_create(const hfa_ffn_desc* desc, const void* w_gate_dev, const void* w_up_dev,
+                          const void* w_down_dev, const float* w_pre_dev, const float* w_post_dev,
+                          const float* scalar_dev, void* stream, hfa_ffn** out);
+hfa_status hfa_ffn_destroy(hfa_ffn* ffn);
+
+/*
+ * One FFN step for `batch` rows (1..max_batch), one cooperative launch of one CTA per SM
+ * with programmatic dependent launch (as hfa_decode_step: only the weights are read
+ * before the previous kernel on `stream` has completed).  Steps on one object must not
+ * overlap on the GPU (they share its scratch).
+ *   h_dev        bf16 [batch, H]: the FFN input, also the residual (the attention half's
+ *                output)
+ *   out_dev      bf16 [batch, H]: the layer output, round to nearest even
+ *   out_f32_dev  nullable f32 [batch, H]: the same before rounding
+ *   a_dev        nullable f32 [batch, I]: gelu(gate) * up, for tests
+ * Every buffer 16-byte aligned (HFA_EINVAL otherwise).  Errors: HFA_EINVAL, HFA_EDEVICE
+ * (another current device), HFA_ECUDA (launch; e.g. the SMs cannot all hold a CTA).
+ */
+hfa_status hfa_ffn_step(hfa_ffn* ffn, void* stream, const void* h_dev, int batch, void* out_dev,
+                        float* out_f32_dev, float* a_dev);
+/* Reads (synchronising `stream`) and clears the device error word: HFA_OK, or HFA_EDEVICE
+ * when a bounded wait of an earlier step gave up (its outputs are then invalid; the step
+ * count and partial sums restart). */
+hfa_status hfa_ffn_check_status(hfa_ffn* ffn, void* stream);
+const char* hfa_ffn_last_error(const hfa_ffn* ffn); /* NULL: this thread's last create error */
+/* the work plan: grid, batch tiles, then (k-splits, blocks per split, row groups per
+ * stage, stages) of the gate/up and of the down projection; returns the count (10) */
+int hfa_ffn_plan_info(const hfa_ffn* ffn, int n, int* values);
+
+/*
  * Successor hint for decoding through a stack of layers (no counterpart on the pages,
  * which run one layer at a time).  Once set, each decode step of `layer` prefetches into
  * L2, during its last phase (o_proj and residual, when HBM is otherwise idle), the Q8_0

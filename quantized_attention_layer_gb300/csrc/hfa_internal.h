@@ -120,6 +120,38 @@ struct StepArgs {
   float cap_log2;          // softcap * log2(e), 0 = no softcap
 };
 
+// One GEMV of the persistent FFN kernel: Q8_0 tiles in the order [k-split][row group]
+// [block] (see launch_repack_q8_0_split), streamed in ring stages of `rgs` row groups of
+// one k-split.
+struct FfnPhase {
+  const uint8_t* w;  // tiles
+  int R;             // row groups of 16 rows (phase 1: gate and up interleaved, 2 I / 16)
+  int nbs;           // blocks (tiles) per k-split
+  int S;             // k-splits
+  int rgs;           // row groups per ring stage: 1, 2, 4 or 8 (even in phase 1)
+  int stages;        // S * ceil(R / rgs)
+};
+
+// Arguments of the persistent FFN kernel (one CTA per SM, cooperative launch).
+struct FfnArgs {
+  FfnPhase p1, p2;               // [Wg; Wu] (interleaved row groups) and Wd
+  const __nv_bfloat16* h;        // bf16 [B, H]: the FFN input and the residual
+  const float* w_pre;            // f32 [H]: pre-FF RMSNorm weight
+  const float* w_post;           // f32 [H]: post-FF RMSNorm weight
+  const float* scalar;           // f32 [scalar_len]: the layer scalar
+  int scalar_len;                // 1 or H
+  unsigned long long* part1;     // [p1.S][B][2 I]: gate rows, then up rows (tagged f32)
+  unsigned long long* part2;     // [p2.S][B][H] (tagged f32)
+  unsigned long long* post_part; // [grid][2]: tagged partial sum(d^2)
+  unsigned long long* ctr;       // launches x grid: numbers the steps (tags)
+  unsigned* err;
+  __nv_bfloat16* out;            // bf16 [B, H]
+  float* out_f32;                // nullable f32 [B, H]
+  float* a_tap;                  // nullable f32 [B, I]: GELU(gate) * up
+  int B, H, I;
+  float eps;
+};
+
 // Optional per-launch event timing (the layer's hfa_set_kernel_timing); begin/end
 // bracket one kernel launch on `s`.
 struct LaunchTimer {
@@ -132,7 +164,8 @@ struct LaunchTimer {
 void set_thread_error(const char* msg);
 
 cudaError_t launch_repack_q8_0_split(const uint8_t* src, int rows, int cols, uint8_t* dst,
-                                     int row_group0, int R_total, int nbs, cudaStream_t s);
+                                     int row_group0, int R_total, int nbs, cudaStream_t s,
+                                     int rg_stride = 1);
 // bf16 [rows, K] (rows from s0, then s1, then s2) -> 128 x 64 tiles of 16 KB in the
 // 128-byte-swizzled order of the verify GEMM's shared-memory stages
 cudaError_t launch_repack_bf16_tiles(const __nv_bfloat16* s0, int n0, const __nv_bfloat16* s1,
@@ -146,6 +179,12 @@ int step_keys_per_tile(int hd);  // keys of one K/V tile of the decode-step kern
 size_t step_stage_bytes();
 int step_threads();
 int step_batch_tiles(int batch);
+
+// the FFN step: grid = one CTA per SM (cooperative); the plan of one GEMV phase for
+// batches up to 4 * nt_max rows, false when no plan fits the kernel's buffers
+bool plan_ffn_phase(FfnPhase* p, int R, int nb, bool pairs, int nt_max, int grid);
+cudaError_t launch_ffn(const FfnArgs& a, int grid, cudaStream_t s);
+int ffn_max_outputs_per_cta();  // B * H / grid must not exceed it
 
 cudaError_t launch_attn(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                         int grid, bool pdl, cudaStream_t s);

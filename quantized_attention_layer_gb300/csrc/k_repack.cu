@@ -15,11 +15,12 @@
 namespace hfa {
 
 // Tile (row group r, block b) of a matrix with R_total row groups lands at index
-// ((b / nbs) * R_total + r) * nbs + b % nbs: the row groups of one k-split of nbs blocks
-// are then one contiguous byte range, which the decode-step kernel copies in bulk.
+// ((b / nbs) * R_total + rg) * nbs + b % nbs, rg = row_group0 + r * rg_stride: the row
+// groups of one k-split of nbs blocks are then one contiguous byte range, which the
+// persistent kernels copy in bulk (rg_stride 2 interleaves two matrices' row groups).
 __global__ void repack_q8_0_split_kernel(const uint8_t* __restrict__ src, int rows, int cols,
-                                         uint8_t* __restrict__ dst, int row_group0, int R_total,
-                                         int nbs) {
+                                         uint8_t* __restrict__ dst, int row_group0, int rg_stride,
+                                         int R_total, int nbs) {
   const int nb = cols / 32;
   const long long n = (long long)(rows / 16) * nb * 32;
   for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n;
@@ -46,7 +47,7 @@ __global__ void repack_q8_0_split_kernel(const uint8_t* __restrict__ src, int ro
       }
     }
     const long long out_tile =
-        ((long long)(b / nbs) * R_total + (row_group0 + r)) * nbs + (b % nbs);
+        ((long long)(b / nbs) * R_total + (row_group0 + (long long)r * rg_stride)) * nbs + (b % nbs);
     uint8_t* tp = dst + out_tile * kQ8TileBytes;
     reinterpret_cast<uint4*>(tp)[lane] = make_uint4(w[0], w[1], w[2], w[3]);
     if (t == 0) {
@@ -58,13 +59,14 @@ __global__ void repack_q8_0_split_kernel(const uint8_t* __restrict__ src, int ro
 }
 
 cudaError_t launch_repack_q8_0_split(const uint8_t* src, int rows, int cols, uint8_t* dst,
-                                     int row_group0, int R_total, int nbs, cudaStream_t s) {
+                                     int row_group0, int R_total, int nbs, cudaStream_t s,
+                                     int rg_stride) {
   long long n = (long long)(rows / 16) * (cols / 32) * 32;
   int threads = 256;
   long long blocks = (n + threads - 1) / threads;
   if (blocks > 65535) blocks = 65535;
   repack_q8_0_split_kernel<<<(int)blocks, threads, 0, s>>>(src, rows, cols, dst, row_group0,
-                                                           R_total, nbs);
+                                                           rg_stride, R_total, nbs);
   return cudaGetLastError();
 }
 

@@ -57,6 +57,11 @@ class hfa_attn_desc(ctypes.Structure):
                 ("flags", ctypes.c_uint)]
 
 
+class hfa_ffn_desc(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int), ("intermediate", ctypes.c_int), ("eps", ctypes.c_float),
+                ("scalar_len", ctypes.c_int), ("max_batch", ctypes.c_int)]
+
+
 def attn_desc_for(w: wl.Workload) -> hfa_attn_desc:
     return hfa_attn_desc(num_heads=w.num_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
                          layer_type=w.layer_type, window=w.window, kv_capacity=w.kv_capacity,
@@ -142,6 +147,19 @@ def lib():
         L.hfa_attention_decode_tq.restype = C
         L.hfa_attention_decode_tq.argtypes = [ctypes.POINTER(hfa_attn_desc), P, P, P, P, P, I,
                                               P, P, P, P, P, P, ctypes.c_size_t, P]
+        L.hfa_ffn_create.restype = C
+        L.hfa_ffn_create.argtypes = [ctypes.POINTER(hfa_ffn_desc), P, P, P, P, P, P, P,
+                                     ctypes.POINTER(P)]
+        L.hfa_ffn_destroy.restype = C
+        L.hfa_ffn_destroy.argtypes = [P]
+        L.hfa_ffn_step.restype = C
+        L.hfa_ffn_step.argtypes = [P, P, P, I, P, P, P]
+        L.hfa_ffn_check_status.restype = C
+        L.hfa_ffn_check_status.argtypes = [P, P]
+        L.hfa_ffn_last_error.restype = ctypes.c_char_p
+        L.hfa_ffn_last_error.argtypes = [P]
+        L.hfa_ffn_plan_info.restype = C
+        L.hfa_ffn_plan_info.argtypes = [P, I, ctypes.POINTER(ctypes.c_int)]
         _lib = L
     return _lib
 
@@ -415,5 +433,64 @@ class Layer:
     def __del__(self):
         try:
             self.hfa_destroy()
+        except Exception:
+            pass
+
+
+def ffn_desc_for(f: wl.FfnWorkload, max_batch: Optional[int] = None) -> hfa_ffn_desc:
+    return hfa_ffn_desc(hidden=f.hidden, intermediate=f.intermediate, eps=f.eps,
+                        scalar_len=f.hidden if f.scalar_per_channel else 1,
+                        max_batch=int(max_batch or f.batch))
+
+
+def ffn_weights_to_device(weights: Dict, device="cuda") -> Dict[str, torch.Tensor]:
+    out = {}
+    for k in ("w_gate", "w_up", "w_down"):
+        out[k] = torch.from_numpy(np.ascontiguousarray(weights[k])).to(device)
+    for k in ("w_pre", "w_post", "scalar"):
+        out[k] = torch.as_tensor(weights[k], dtype=torch.float32).contiguous().to(device)
+    return out
+
+
+class Ffn:
+    """The dense FFN half (hfa_ffn_create ... hfa_ffn_destroy)."""
+
+    def __init__(self, desc: hfa_ffn_desc, dev_weights: Dict[str, torch.Tensor], stream=None):
+        self.desc = desc
+        self._h = ctypes.c_void_p()
+        w = dev_weights
+        st = lib().hfa_ffn_create(ctypes.byref(desc), _ptr(w["w_gate"]), _ptr(w["w_up"]),
+                                  _ptr(w["w_down"]), _ptr(w["w_pre"]), _ptr(w["w_post"]),
+                                  _ptr(w["scalar"]), _stream_ptr(stream), ctypes.byref(self._h))
+        if st != HFA_OK:
+            raise HfaError(st, lib().hfa_ffn_last_error(None).decode())
+
+    def _check(self, st: int):
+        if st != HFA_OK:
+            raise HfaError(st, lib().hfa_ffn_last_error(self._h).decode())
+
+    def hfa_ffn_step(self, h: torch.Tensor, out: torch.Tensor, out_f32: Optional[torch.Tensor] = None,
+                     a: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        self._check(lib().hfa_ffn_step(self._h, _stream_ptr(stream), _ptr(h), int(h.shape[0]),
+                                       _ptr(out), _ptr(out_f32), _ptr(a)))
+        return out
+
+    def hfa_ffn_check_status(self, stream=None) -> None:
+        self._check(lib().hfa_ffn_check_status(self._h, _stream_ptr(stream)))
+
+    def hfa_ffn_plan_info(self) -> Dict[str, int]:
+        v = (ctypes.c_int * 16)()
+        n = lib().hfa_ffn_plan_info(self._h, 16, v)
+        names = ["grid", "nt_max", "s1", "nbs1", "rgs1", "stages1", "s2", "nbs2", "rgs2", "stages2"]
+        return {names[i]: int(v[i]) for i in range(min(n, len(names)))}
+
+    def hfa_ffn_destroy(self) -> None:
+        if self._h:
+            lib().hfa_ffn_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.hfa_ffn_destroy()
         except Exception:
             pass

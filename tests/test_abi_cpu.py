@@ -109,3 +109,29 @@ def test_quantised_kv_format_rejects_bad_arguments_before_any_device_call(libhfa
     assert b"signs[5]" in libhfa.hfa_last_error(None)
     assert libhfa.hfa_tq_create(128, 8, None, ctypes.byref(h)) == hfa.HFA_EINVAL
     assert not h.value
+
+
+def test_ffn_create_rejects_bad_descriptors_before_any_device_call(libhfa):
+    h = ctypes.c_void_p()
+    dummy = ctypes.c_void_p(16)  # never dereferenced: every case fails validation first
+
+    def create(**kw):
+        base = dict(hidden=256, intermediate=512, eps=1e-6, scalar_len=1, max_batch=1)
+        base.update(kw)
+        d = hfa.hfa_ffn_desc(**base)
+        return libhfa.hfa_ffn_create(ctypes.byref(d), dummy, dummy, dummy, dummy, dummy, dummy,
+                                     None, ctypes.byref(h))
+
+    assert create(hidden=48) == hfa.HFA_EINVAL          # not whole Q8_0 blocks
+    assert create(intermediate=0) == hfa.HFA_EINVAL
+    assert create(scalar_len=7) == hfa.HFA_EINVAL       # one scalar or one per channel
+    assert create(max_batch=17) == hfa.HFA_EUNSUPPORTED
+    assert create(max_batch=0) == hfa.HFA_EUNSUPPORTED
+    assert create(eps=-1.0) == hfa.HFA_EINVAL
+    assert b"eps" in libhfa.hfa_ffn_last_error(None)
+    d = hfa.hfa_ffn_desc(hidden=256, intermediate=512, eps=1e-6, scalar_len=1, max_batch=1)
+    assert libhfa.hfa_ffn_create(ctypes.byref(d), None, dummy, dummy, dummy, dummy, dummy, None,
+                                 ctypes.byref(h)) == hfa.HFA_EINVAL
+    assert not h.value
+    assert libhfa.hfa_ffn_step(None, None, None, 1, None, None, None) == hfa.HFA_EINVAL
+    assert libhfa.hfa_ffn_destroy(None) == hfa.HFA_EINVAL
