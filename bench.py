@@ -17,8 +17,9 @@ Printed (one JSON line, rank 0): steps/s for the whole job on the headline workl
 CUDA-event duration, against the measured HBM copy bandwidth), the kernel's own duration
 from its device timer stamps, the end-to-end rate through the host-buffer entry point, the
 CPU oracle baseline, SM clocks sampled during the timed region, the launch count, and under
-"workloads" the same figures for the other four workloads (the tiny sliding layer, the
-batch-16 sliding ring, the 128K batch-4 layer with softcap, and the 16-token verify block).
+"workloads" the same figures for the other workloads (the tiny sliding layer, the
+batch-16 sliding ring, the 128K batch-4 layer with softcap, the 16-token verify block, and
+the layer's dense FFN half at batch 1 and 16).
 
 The K timed steps are one CUDA graph whose first and last nodes record the timing events,
 so the timed region is exactly the K steps on the device (no host launch latency).
@@ -50,7 +51,11 @@ METRIC = "decode steps/sec per layer at 1 GB300; achieved HBM GB/s as % of peak"
 UNIT = "steps/s"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0
-EXTRA = ("tiny_sliding", "sliding_b16_ring1024", "full_b4_128k_softcap", "verify_l16_8k")
+EXTRA = ("tiny_sliding", "sliding_b16_ring1024", "full_b4_128k_softcap", "verify_l16_8k", "ffn_b1",
+         "ffn_b16", "tq8_full_b1_32k", "tq4_full_b1_32k")
+# attention over a quantised (TurboQuant) KV cache: bits, and the attention shape of the
+# headline layer (batch 1, 32/8 heads, head dim 128, 32768 visible keys)
+TQ = {"tq8_full_b1_32k": 8, "tq4_full_b1_32k": 4}
 
 
 def parse():
@@ -492,6 +497,122 @@ def verify_workload(w, K, W, R, world):
     return res
 
 
+def ffn_workload(f, K, W, R, world):
+    """The dense FFN half (one persistent kernel per step): steps/s and its HBM roofline."""
+    from quantized_attention_layer_gb300 import hfa, workloads as wl
+    weights = wl.make_ffn_weights(f)
+    h = wl.make_ffn_input(f).cuda()
+    dev_w = hfa.ffn_weights_to_device(weights)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        ffns = [hfa.Ffn(hfa.ffn_desc_for(f), dev_w, stream=stream) for _ in range(R)]
+    del dev_w
+    B, H, I = f.batch, f.hidden, f.intermediate
+    out = torch.empty((B, H), dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
+
+    def step(i):
+        ffns[i % R].hfa_ffn_step(h, out, stream=stream)
+
+    for i in range(max(3, W)):
+        step(i)
+    torch.cuda.synchronize()
+
+    def steps():
+        for i in range(K):
+            step(i)
+
+    graph, ev0, ev1 = timed_graph(stream, steps, K)
+    ms, clocks = time_replays(graph, ev0, ev1, stream, world)
+    del graph
+    for F in ffns:
+        F.hfa_ffn_check_status(stream=stream)
+    wbytes = 3 * I * H // 32 * 34               # Q8_0 gate, up and down
+    step_bytes = wbytes + 2 * B * H * 2 + 2 * H * 4 + (H if f.scalar_per_channel else 1) * 4
+    peak, src = measured_peaks()
+    ms_per_step = ms / K
+    gbs = step_bytes / (ms_per_step * 1e-3) / 1e9
+    res = {"unit": UNIT, "value": world * 1e3 / ms_per_step, "ms_per_step": ms_per_step,
+           "step_bytes": step_bytes, "step_gbs": gbs, "frac": gbs / peak,
+           "frac_of_nominal": gbs / NOMINAL_HBM_GBS, "peak_source": src, "batch": B,
+           "shape": f"{H}->{I}->{H}", "replicas": R, "plan": ffns[0].hfa_ffn_plan_info(),
+           "traffic": ncu_traffic("k_ffn.cu", f"ffn_step_{f.name}.md"), "clocks": clocks,
+           "l2": f"inputs larger than L2: {R} replicas, {R * step_bytes / 1e9:.2f} GB"}
+    for F in ffns:
+        F.hfa_ffn_destroy()
+    torch.cuda.empty_cache()
+    return res
+
+
+def tq_workload(bits, K, W, world):
+    """Flash-decode over a coded KV cache (4- or 8-bit codes + f32 block norms for K and V;
+    hfa_attention_decode_tq), and the bf16 attention of the same shape for comparison."""
+    from quantized_attention_layer_gb300 import hfa, workloads as wl
+    B, nh, nkv, hd, C = 1, 32, 8, 128, 32768
+    w = wl.Workload(name="tq", hidden=256, num_heads=nh, num_kv_heads=nkv, head_dim=hd,
+                    layer_type=wl.FULL, window=0, kv_capacity=C, ring=False, batch=B,
+                    rope_theta=1e6, seed=11)
+    desc = hfa.attn_desc_for(w)
+    pos = np.full(B, C - 1, dtype=np.int32)
+    posd = torch.from_numpy(pos).cuda()
+    g = torch.Generator(device="cuda").manual_seed(11)
+    q = torch.randn((B, nh, hd), device="cuda", generator=g)
+    o = torch.empty_like(q)
+    fmt = hfa.TqFormat(hd, bits, wl.make_tq_signs(hd, 3))
+    cb, nb = fmt.code_bytes, fmt.blocks
+    step_bytes = B * nkv * C * (cb + nb * 4) * 2 + 2 * q.numel() * 4
+    R = max(2, -(-300_000_000 // step_bytes))  # replicas: together larger than L2
+    caches = []
+    for _ in range(R):
+        caches.append(tuple(
+            torch.randint(0, 256, (B, nkv, C, cb), dtype=torch.uint8, device="cuda", generator=g)
+            if k % 2 == 0 else torch.rand((B, nkv, C, nb), device="cuda", generator=g) + 0.5
+            for k in range(4)))
+    ws = torch.zeros(hfa.hfa_attention_tq_workspace_bytes(desc, B, C), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    def step(i):
+        kc, kn, vc, vn = caches[i % R]
+        fmt.hfa_attention_decode_tq(desc, q, posd, pos, kc, kn, None, vc, vn, ws, o, stream=stream)
+
+    for i in range(max(3, W)):
+        step(i)
+    torch.cuda.synchronize()
+    graph, ev0, ev1 = timed_graph(stream, lambda: [step(i) for i in range(K)], K)
+    ms, clocks = time_replays(graph, ev0, ev1, stream, world)
+    del graph, caches
+    # the same attention over a dense bf16 cache
+    dense_bytes = B * nkv * C * hd * 2 * 2 + 2 * q.numel() * 4
+    Rd = max(2, -(-300_000_000 // dense_bytes))
+    kvs = [(torch.randn((B, nkv, C, hd), device="cuda", generator=g).to(torch.bfloat16),
+            torch.randn((B, nkv, C, hd), device="cuda", generator=g).to(torch.bfloat16)) for _ in range(Rd)]
+    wsd = torch.zeros(hfa.hfa_attention_workspace_bytes(desc, B), dtype=torch.uint8, device="cuda")
+
+    def dstep(i):
+        kc, vc = kvs[i % Rd]
+        hfa.hfa_attention_decode(desc, q, posd, pos, kc, vc, wsd, o, stream=stream)
+
+    for i in range(3):
+        dstep(i)
+    torch.cuda.synchronize()
+    graph, ev0, ev1 = timed_graph(stream, lambda: [dstep(i) for i in range(K)], K)
+    dms, _ = time_replays(graph, ev0, ev1, stream, world)
+    del graph, kvs
+    fmt.destroy()
+    torch.cuda.empty_cache()
+    peak, src = measured_peaks()
+    ms_per_step = ms / K
+    gbs = step_bytes / (ms_per_step * 1e-3) / 1e9
+    dgbs = dense_bytes / (dms / K * 1e-3) / 1e9
+    return {"unit": "attention calls/s", "value": world * 1e3 / ms_per_step, "ms_per_step": ms_per_step,
+            "step_bytes": step_bytes, "step_gbs": gbs, "frac": gbs / peak, "peak_source": src,
+            "bits": bits, "shape": f"batch {B}, {nh}/{nkv} heads, hd {hd}, {C} keys",
+            "replicas": R, "clocks": clocks,
+            "dense_bf16": {"ms_per_step": dms / K, "step_bytes": dense_bytes, "step_gbs": dgbs,
+                           "frac": dgbs / peak}}
+
+
 def run_ours(args, rank, world, local):
     from quantized_attention_layer_gb300 import build, workloads as wl
     build.build()
@@ -544,6 +665,12 @@ def run_ours(args, rank, world, local):
     wls = {}
     for name in extra:
         if name == w.name:
+            continue
+        if name in TQ:
+            wls[name] = tq_workload(TQ[name], K, W, world)
+            continue
+        if name in wl.FFN_BY_NAME:
+            wls[name] = ffn_workload(wl.FFN_BY_NAME[name], K, W, 8, world)
             continue
         we = wl.BY_NAME[name]
         if we.verify_len:

@@ -1,6 +1,7 @@
 /*
  * hfa.h -- C ABI of libhfa: the single-token decode step and the multi-token verify
- * block of one Gemma-style attention layer on an NVIDIA GB300 (sm_103a).
+ * block of one Gemma-style attention layer on an NVIDIA GB300 (sm_103a), attention over
+ * a quantised KV cache, and the layer's dense feed-forward half.
  *
  * Sources of the operation (hf2q documentation pages):
  *   "gemma4/gpu_full_attn.rs", encode_one_layer: the per-layer decode encoder --
@@ -12,6 +13,9 @@
  *   "gemma4/model.rs": the Q8_0 block format (Q8_0 lm_head re-quantiser), the dense
  *     KV buffer layout [n_kv_heads, capacity, head_dim] with sliding layers as rings
  *     of capacity = sliding window, and the dense tree-verify entry point.
+ *   "gemma4/gpu_full_attn.rs", encode_one_layer, the dense MLP and the end of the
+ *     layer: pre- and post-feed-forward RMSNorm, gate/up/down projections, GELU(gate) *
+ *     up, the residual add and the layer scalar (hfa_ffn_*).
  *   "spec_decode/dflash/forward.rs": per-head RMSNorm over rows = L * n_heads, NeoX
  *     RoPE with a position offset, the logit softcap tanh(s / cap) * cap, the residual
  *     add, and SDPA of an L-row block over the cache (all rows of the block appended).
@@ -24,7 +28,8 @@
  *   - All argument checks run on the host before anything is launched; a rejected
  *     call launches nothing and touches no device memory.  The reason is available
  *     from hfa_last_error().
- *   - No entry point allocates device memory except hfa_layer_create.
+ *   - No entry point allocates device memory except the create functions
+ *     (hfa_layer_create, hfa_tq_create, hfa_ffn_create).
  *   - bf16 = IEEE bfloat16 bit pattern (uint16), row-major, densely packed.
  */
 #ifndef HFA_H
@@ -43,7 +48,7 @@ typedef enum {
   HFA_OK = 0,
   HFA_EINVAL = -1,       /* bad argument: null pointer, shape, flag combination */
   HFA_ERANGE = -2,       /* a position outside the cache or the layer's limits */
-  HFA_ENOMEM = -3,       /* device allocation failed (hfa_layer_create only) */
+  HFA_ENOMEM = -3,       /* device allocation failed (the create functions only) */
   HFA_ECUDA = -4,        /* a CUDA call failed; hfa_last_error has the CUDA message */
   HFA_EUNSUPPORTED = -5, /* valid request this library does not implement */
   HFA_EDEVICE = -6,      /* no usable sm_103 device, or a device-side check failed */
@@ -351,6 +356,16 @@ hfa_status hfa_ffn_step(hfa_ffn* ffn, void* stream, const void* h_dev, int batch
  * count and partial sums restart). */
 hfa_status hfa_ffn_check_status(hfa_ffn* ffn, void* stream);
 const char* hfa_ffn_last_error(const hfa_ffn* ffn); /* NULL: this thread's last create error */
+/* Instrumentation (no counterpart on the pages): with a buffer set, every later step writes
+ * per CTA c the GPU's nanosecond timer into stamps_dev[c * 32 + k], k = 0 entry, 1 the
+ * previous kernel completed, 2 first gate/up operand built, 3 first stage computed, 4 last
+ * gate/up stage stored, 5 first down operand built, 6 last down stage stored, 7 down sums
+ * of the CTA's outputs added, 8 post-FF norm known, 9 exit, 10 last weight stage issued,
+ * 11..18 ring stages 0..7 arrived, 19..26 loads 4..11 issued (slots a CTA does not reach
+ * keep their old value).  The buffer (int64 [rows][32], rows = hfa_ffn_stamp_rows) must
+ * stay valid while set; NULL clears.  Results are unchanged. */
+hfa_status hfa_ffn_set_stamps(hfa_ffn* ffn, unsigned long long* stamps_dev);
+int hfa_ffn_stamp_rows(const hfa_ffn* ffn);
 /* the work plan: grid, batch tiles, then (k-splits, blocks per split, row groups per
  * stage, stages) of the gate/up and of the down projection; returns the count (10) */
 int hfa_ffn_plan_info(const hfa_ffn* ffn, int n, int* values);

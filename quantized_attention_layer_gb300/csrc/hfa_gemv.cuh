@@ -74,6 +74,52 @@ __device__ __forceinline__ void q8_tile_mma(float (&acc)[NT][4], const uint4 w, 
   }
 }
 
+// Two tiles at once: the same as two q8_tile_mma calls, with the two tiles' MMAs
+// interleaved so that each one's latency hides behind the other's.
+template <int NT>
+__device__ __forceinline__ void q8_tile2_mma(float (&acc)[NT][4], const uint4 wa, uint32_t da,
+                                             uint32_t xa, const uint4 wb, uint32_t db,
+                                             uint32_t xb) {
+  uint32_t A0[4], A1[4], B0[4], B1[4];
+  A0[0] = u8x2_to_h2(wa.x, kSelLo);
+  A0[1] = u8x2_to_h2(wa.y, kSelLo);
+  A0[2] = u8x2_to_h2(wa.x, kSelHi);
+  A0[3] = u8x2_to_h2(wa.y, kSelHi);
+  A1[0] = u8x2_to_h2(wa.z, kSelLo);
+  A1[1] = u8x2_to_h2(wa.w, kSelLo);
+  A1[2] = u8x2_to_h2(wa.z, kSelHi);
+  A1[3] = u8x2_to_h2(wa.w, kSelHi);
+  B0[0] = u8x2_to_h2(wb.x, kSelLo);
+  B0[1] = u8x2_to_h2(wb.y, kSelLo);
+  B0[2] = u8x2_to_h2(wb.x, kSelHi);
+  B0[3] = u8x2_to_h2(wb.y, kSelHi);
+  B1[0] = u8x2_to_h2(wb.z, kSelLo);
+  B1[1] = u8x2_to_h2(wb.w, kSelLo);
+  B1[2] = u8x2_to_h2(wb.z, kSelHi);
+  B1[3] = u8x2_to_h2(wb.w, kSelHi);
+  const __half2 d2a = *reinterpret_cast<const __half2*>(&da);
+  const __half2 d2b = *reinterpret_cast<const __half2*>(&db);
+  const float ga = __low2float(d2a), ga8 = __high2float(d2a);
+  const float gb = __low2float(d2b), gb8 = __high2float(d2b);
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const uint4 xva = lds128(xa + nt * 512), xvb = lds128(xb + nt * 512);
+    float ta[4] = {0.f, 0.f, 0.f, 0.f}, tb[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_f16(ta, A0, xva.x, xva.y);
+    mma_f16(tb, B0, xvb.x, xvb.y);
+    mma_f16(ta, A1, xva.z, xva.w);
+    mma_f16(tb, B1, xvb.z, xvb.w);
+    acc[nt][0] = fmaf(ta[0], ga, acc[nt][0]);
+    acc[nt][1] = fmaf(ta[1], ga, acc[nt][1]);
+    acc[nt][2] = fmaf(ta[2], ga8, acc[nt][2]);
+    acc[nt][3] = fmaf(ta[3], ga8, acc[nt][3]);
+    acc[nt][0] = fmaf(tb[0], gb, acc[nt][0]);
+    acc[nt][1] = fmaf(tb[1], gb, acc[nt][1]);
+    acc[nt][2] = fmaf(tb[2], gb8, acc[nt][2]);
+    acc[nt][3] = fmaf(tb[3], gb8, acc[nt][3]);
+  }
+}
+
 // Operand word index of the column pair (cc, cc + 1) of batch row b: block cc / 32,
 // k-step and half of the m16n8k16 B fragment; batch row b in the n8 tile b / 4, as
 // column 2 (b % 4) (fp16 hi) and 2 (b % 4) + 1 (fp16 lo).  The lo word is 16 further.

@@ -148,6 +148,7 @@ struct FfnArgs {
   __nv_bfloat16* out;            // bf16 [B, H]
   float* out_f32;                // nullable f32 [B, H]
   float* a_tap;                  // nullable f32 [B, I]: GELU(gate) * up
+  unsigned long long* stamps;    // nullable [grid][16]: %globaltimer at fixed points
   int B, H, I;
   float eps;
 };
@@ -183,6 +184,7 @@ int step_batch_tiles(int batch);
 // the FFN step: grid = one CTA per SM (cooperative); the plan of one GEMV phase for
 // batches up to 4 * nt_max rows, false when no plan fits the kernel's buffers
 bool plan_ffn_phase(FfnPhase* p, int R, int nb, bool pairs, int nt_max, int grid);
+bool ffn_plan_fits(const FfnPhase& p, int nt);  // the kernel for nt batch tiles holds it
 cudaError_t launch_ffn(const FfnArgs& a, int grid, cudaStream_t s);
 int ffn_max_outputs_per_cta();  // B * H / grid must not exceed it
 

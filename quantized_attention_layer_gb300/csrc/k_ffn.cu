@@ -19,9 +19,17 @@
 //      columns: g, u summed over the k-splits and times 1/rms(h), a = gelu(g) u.
 //   3  the end of the layer: d summed over the phase-2 k-splits, sum(d^2) per row exchanged
 //      between the CTAs that share the row (tagged), out = (h + d w_post / rms(d)) s.
-// One producer warp streams every weight tile of both phases through the ring, phase 2's
-// as soon as stages free up: they depend on nothing of the step, so HBM keeps streaming
-// while the consumers wait for the phase-1 sums.
+// A producer warp streams every weight tile of both phases through a ring of shared-memory
+// stages with 1-D bulk copies: a stage is reloaded as soon as every consumer warp has read
+// its tiles, phase 2's stages included -- they depend on nothing of the step, so HBM keeps
+// streaming while the consumers wait for the phase-1 sums.  The ring fill starts once the
+// activations of the first operand are in, whose loads would otherwise queue behind it.
+//
+// The GEMV is latency-bound on the warp MMA, so there are 16 consumer warps (8 with four
+// batch tiles, whose registers allow no more) and each runs two tiles' MMAs interleaved.
+// The warps that share a row group of a stage add their sums through shared memory (one
+// of two buffers, alternating) behind a named barrier of their own, each warp storing a
+// share of the results: no barrier spans the CTA within a phase.
 //
 // Every wait is bounded in wall time; a CTA that gives up sets an error bit, skips its
 // remaining work (every barrier is still passed) and drains its copies in flight.
@@ -36,24 +44,65 @@
 namespace hfa {
 namespace ffn {
 
-constexpr int kCW = 8;                     // consumer warps
-constexpr int kConsumers = kCW * 32;
-constexpr int kThreads = kConsumers + 32;  // + the producer warp
-constexpr int kStages = 4;
 constexpr int kStageBytes = 49152;
-constexpr int kOpBytes = 24576;            // GEMV operand (nbs x NT x 512 bytes)
-constexpr int kRedBytes = 8192;            // warp sums of a stage / d of phase 3
 constexpr int kSmallBytes = 1024;
-constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kOpBytes + kRedBytes + kSmallBytes;
 constexpr int kMaxBatch = 16;
-constexpr int kMaxS1 = 16;                 // k-splits of phase 1 (read per phase-2 operand)
-constexpr int kMaxS2 = 32;                 // k-splits of phase 2 (read per output)
+constexpr int kMaxS1 = 16;  // k-splits of phase 1 (read per phase-2 operand)
+constexpr int kMaxS2 = 32;  // k-splits of phase 2 (read per output)
 constexpr int kMaxGrid = 256;
-static_assert(kCW * 4 * 32 * 2 * 4 <= kRedBytes, "warp sums of a stage");
+constexpr int kMaxOutputsPerCta = 2048;  // phase 3 keeps d of its outputs in the sums area
 
+// Instrumentation (hfa_ffn_set_stamps): thread 0 of each CTA (the producer's lane 0 for
+// kStampIssued) records %globaltimer at these points of every step.
+enum {
+  kStampEntry = 0,  // barriers initialised
+  kStampWait,       // the previous kernel has completed
+  kStampOp1,        // first phase-1 operand built
+  kStampFirst,      // first stage computed (warp 0)
+  kStampPh1,        // last phase-1 stage stored
+  kStampOp2,        // first phase-2 operand built (phase-1 sums of its columns in)
+  kStampPh2,        // last phase-2 stage stored
+  kStampD,          // d of this CTA's outputs summed
+  kStampNorm,       // 1/rms(d) of its rows known
+  kStampExit,       // outputs written
+  kStampIssued,     // producer: last stage issued
+  kStampArrived = 11,  // [8]: stages 0..7 computed (warp 0: its wait and its tiles)
+  kStampIssue = 19,    // [8]: producer: loads kStages..kStages+7 issued (their slot free)
+  kStampSlots = 32,
+};
+#define FFN_STAMP(a, k)                                                        \
+  do {                                                                         \
+    if ((a).stamps) (a).stamps[blockIdx.x * kStampSlots + (k)] = globaltimer_ns(); \
+  } while (0)
+
+// GEMV operand bytes (nbs x NT x 512) the kernel for `nt` batch tiles holds
+__host__ __device__ constexpr int op_bytes(int nt) { return nt == 1 ? 24576 : (nt == 2 ? 16384 : 49152); }
+
+template <int NT>
+struct Cfg {
+  static constexpr int kCW = NT == 4 ? 8 : 16;  // consumer warps
+  static constexpr int kConsumers = kCW * 32;
+  static constexpr int kThreads = kConsumers + 32;  // + the producer warp
+  static constexpr int kStages = NT == 4 ? 3 : 4;
+  static constexpr int kOpBytes = op_bytes(NT);
+  static constexpr int kRedHalf = kCW * NT * 32 * 2 * 4;  // warp sums of one stage
+  static constexpr int kRedBytes = 2 * kRedHalf;
+  static constexpr size_t kSmem =
+      1024 + (size_t)kStages * kStageBytes + kOpBytes + kRedBytes + kSmallBytes;
+  static_assert(kMaxOutputsPerCta * 4 <= kRedBytes, "phase-3 outputs in the sums area");
+  static_assert(kSmem <= 232448, "shared memory per CTA");
+};
+
+// Named barriers: 1 all consumers, 2 consumers + producer (first activations in),
+// 3 + j the consumer warps of row group j of a stage.
+template <int NT>
 __device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(Cfg<NT>::kConsumers) : "memory");
 }
+__device__ __forceinline__ void group_sync(int j, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(3 + j), "r"(threads) : "memory");
+}
+
 // balanced partition of n items over P parts (n < 2^24, P <= kMaxGrid)
 __device__ __forceinline__ int part_begin(int c, int n, int P) {
   return (int)((unsigned)c * (unsigned)n / (unsigned)P);
@@ -97,116 +146,169 @@ __device__ __forceinline__ bool poll_expired(uint64_t t0, unsigned* err, volatil
   return false;
 }
 
+// Largest |v| of batch row b over a warp whose 32 consecutive items cover at most three
+// consecutive rows (every row has at least 16 items): one warp reduction per row, one
+// shared atomic per row and warp.
+__device__ __forceinline__ void warp_row_max(unsigned* s_max, int b, unsigned m, int lane) {
+  const int b0 = __shfl_sync(0xffffffffu, b, 0);
+  const int b1 = __shfl_sync(0xffffffffu, b, 31);
+#pragma unroll
+  for (int d = 0; d < 3; ++d) {
+    const unsigned r = __reduce_max_sync(0xffffffffu, b == b0 + d ? m : 0u);
+    if (lane == 0 && b0 + d <= b1 && r) atomicMax(&s_max[b0 + d], r);
+  }
+}
+
 // The operand words hold f32 values (hi word: column cc, lo word: column cc + 1); this
 // pass scales each batch row by the power of two of its largest |value| and splits it
-// into fp16 hi + lo, and zeroes the batch columns past B.  s_inv gets the scales' inverse.
+// into fp16 hi + lo.  The words of batch columns past B are left as they are: the MMA
+// keeps columns apart, and the sums of those columns are never read.  s_inv gets the
+// scales' inverse.
 template <int NT>
 __device__ void finish_operand(uint32_t* op, const unsigned* s_max, float* s_inv, int B,
                                int pairs) {
+  constexpr int C = Cfg<NT>::kConsumers;
   const int tid = threadIdx.x;
-  for (int e = tid; e < NT * 4 * pairs; e += kConsumers) {
-    const int b = e / pairs, cc = 2 * (e - b * pairs);
-    const int wd = operand_word<NT>(cc, b);
-    uint32_t hi = 0u, lo = 0u;
-    if (b < B) {
-      const float sc = exp2i(scale_exp(s_max[b]));
+  for (int b = 0; b < B; ++b) {
+    const float sc = exp2i(scale_exp(s_max[b]));
+    for (int p = tid; p < pairs; p += C) {
+      const int wd = operand_word<NT>(2 * p, b);
       __half h0, l0, h1, l1;
       split_f16(__uint_as_float(op[wd]) * sc, h0, l0);
       split_f16(__uint_as_float(op[wd + 16]) * sc, h1, l1);
-      hi = pack_h2(h0, h1);
-      lo = pack_h2(l0, l1);
+      op[wd] = pack_h2(h0, h1);
+      op[wd + 16] = pack_h2(l0, l1);
     }
-    op[wd] = hi;
-    op[wd + 16] = lo;
   }
   if (tid < B) s_inv[tid] = exp2i(-scale_exp(s_max[tid]));
-  consumer_sync();
+  consumer_sync<NT>();
 }
 
-// Phase-1 operand of k-split s: v = h (.) w_pre over the split's columns.
+// Phase-1 operand of k-split s: v = h (.) w_pre over the split's columns.  With `signal`,
+// the consumers release the producer (barrier 2) once their first activations are in.
 template <int NT>
-__device__ void build_op1(const FfnArgs& a, int s, uint32_t* op, unsigned* s_max, float* s_inv) {
-  const int tid = threadIdx.x;
-  const int ncols = a.p1.nbs * 32, c0 = s * ncols, pairs = ncols / 2;
+__device__ void build_op1(const FfnArgs& a, int s, uint32_t* op, unsigned* s_max, float* s_inv,
+                          bool signal) {
+  constexpr int C = Cfg<NT>::kConsumers;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int ncols = a.p1.nbs * 32, c0 = s * ncols, pairs = ncols / 2, total = a.B * pairs;
   if (tid < kMaxBatch) s_max[tid] = 0u;
-  consumer_sync();
-  for (int e = tid; e < a.B * pairs; e += kConsumers) {
-    const int b = e / pairs, cc = 2 * (e - b * pairs), col = c0 + cc;
-    const float2 hf = __bfloat1622float2(
-        *reinterpret_cast<const __nv_bfloat162*>(a.h + (size_t)b * a.H + col));
-    const float2 w = __ldg(reinterpret_cast<const float2*>(a.w_pre + col));
-    const float v0 = hf.x * w.x, v1 = hf.y * w.y;
-    const int wd = operand_word<NT>(cc, b);
-    op[wd] = __float_as_uint(v0);
-    op[wd + 16] = __float_as_uint(v1);
-    atomicMax(&s_max[b], __float_as_uint(fmaxf(fabsf(v0), fabsf(v1))));
+  consumer_sync<NT>();
+  for (int base = 0; base < total; base += 4 * C) {
+    float2 hv[4], wv[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {  // every load of the round first
+      const int e = base + k * C + tid, ee = e < total ? e : total - 1;
+      const int b = ee / pairs, col = c0 + 2 * (ee - b * pairs);
+      hv[k] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(a.h + (size_t)b * a.H + col));
+      wv[k] = __ldg(reinterpret_cast<const float2*>(a.w_pre + col));
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int e = base + k * C + tid, ee = e < total ? e : total - 1;
+      const int b = ee / pairs, cc = 2 * (ee - b * pairs);
+      const float v0 = hv[k].x * wv[k].x, v1 = hv[k].y * wv[k].y;
+      if (e < total) {
+        const int wd = operand_word<NT>(cc, b);
+        op[wd] = __float_as_uint(v0);
+        op[wd + 16] = __float_as_uint(v1);
+      }
+      warp_row_max(s_max, b, e < total ? __float_as_uint(fmaxf(fabsf(v0), fabsf(v1))) : 0u, lane);
+    }
+    if (signal && base == 0)  // the values are used: their loads have completed
+      asm volatile("bar.arrive 2, %0;" ::"n"(Cfg<NT>::kThreads) : "memory");
   }
-  consumer_sync();
+  consumer_sync<NT>();
   finish_operand<NT>(op, s_max, s_inv, a.B, pairs);
 }
 
 // Phase-2 operand of k-split s: for each column x of the split, g and u = the phase-1
 // partial sums added in k-split order, times 1/rms(h); a = gelu(g) u (written to the tap
-// by the one CTA that loads the split's first stage).
+// by the one CTA that loads the split's first stage).  Each thread polls two columns
+// pairs at once, every load of a round issued before the first tag is checked.
 template <int NT>
 __device__ void build_op2(const FfnArgs& a, int s, uint32_t* op, unsigned* s_max, float* s_inv,
                           const float* s_hinv, bool tap, uint32_t tag, volatile int* abort) {
-  const int tid = threadIdx.x;
-  const int ncols = a.p2.nbs * 32, c0 = s * ncols, pairs = ncols / 2;
+  constexpr int C = Cfg<NT>::kConsumers;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int ncols = a.p2.nbs * 32, c0 = s * ncols, pairs = ncols / 2, total = a.B * pairs;
   const size_t sstride = (size_t)a.B * 2 * a.I;
   if (tid < kMaxBatch) s_max[tid] = 0u;
-  consumer_sync();
-  for (int e = tid; e < a.B * pairs; e += kConsumers) {
-    const int b = e / pairs, cc = 2 * (e - b * pairs), col = c0 + cc;
-    const unsigned long long* src = a.part1 + (size_t)b * 2 * a.I + col;
-    float g0 = 0.f, g1 = 0.f, u0 = 0.f, u1 = 0.f;
-    for (int s0 = 0; s0 < a.p1.S; s0 += 4) {
-      unsigned long long w[4][4];
+  consumer_sync<NT>();
+  for (int base = 0; base < total; base += 2 * C) {
+    float g[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, u[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    const unsigned long long* src[2];
+    int bb[2], cc[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int e = base + k * C + tid, ee = e < total ? e : total - 1;
+      bb[k] = ee / pairs;
+      cc[k] = 2 * (ee - bb[k] * pairs);
+      src[k] = a.part1 + (size_t)bb[k] * 2 * a.I + c0 + cc[k];
+    }
+    for (int s0 = 0; s0 < a.p1.S; s0 += 2) {
+      unsigned long long w[2][2][4];
       const uint64_t t0 = globaltimer_ns();
       for (;;) {
         bool ready = true;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int sx = s0 + i < a.p1.S ? s0 + i : a.p1.S - 1;
-          const unsigned long long* p = src + sx * sstride;
-          w[i][0] = ld_tagged(p);
-          w[i][1] = ld_tagged(p + 1);
-          w[i][2] = ld_tagged(p + a.I);
-          w[i][3] = ld_tagged(p + a.I + 1);
+        for (int k = 0; k < 2; ++k)
 #pragma unroll
-          for (int k = 0; k < 4; ++k) ready = ready && (uint32_t)(w[i][k] >> 32) == tag;
-        }
+          for (int i = 0; i < 2; ++i) {
+            const int sx = s0 + i < a.p1.S ? s0 + i : a.p1.S - 1;
+            const unsigned long long* p = src[k] + sx * sstride;
+            w[k][i][0] = ld_tagged(p);
+            w[k][i][1] = ld_tagged(p + 1);
+            w[k][i][2] = ld_tagged(p + a.I);
+            w[k][i][3] = ld_tagged(p + a.I + 1);
+          }
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int m = 0; m < 4; ++m) ready = ready && (uint32_t)(w[k][i][m] >> 32) == tag;
         if (ready || poll_expired(t0, a.err, abort)) break;
         __nanosleep(32);
       }
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (s0 + i < a.p1.S) {
-          g0 += tagged_value(w[i][0]);
-          g1 += tagged_value(w[i][1]);
-          u0 += tagged_value(w[i][2]);
-          u1 += tagged_value(w[i][3]);
+      for (int k = 0; k < 2; ++k)
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+          if (s0 + i < a.p1.S) {
+            g[k][0] += tagged_value(w[k][i][0]);
+            g[k][1] += tagged_value(w[k][i][1]);
+            u[k][0] += tagged_value(w[k][i][2]);
+            u[k][1] += tagged_value(w[k][i][3]);
+          }
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int e = base + k * C + tid;
+      const float hinv = s_hinv[bb[k]];
+      const float a0 = gelu_tanh(g[k][0] * hinv) * (u[k][0] * hinv);
+      const float a1 = gelu_tanh(g[k][1] * hinv) * (u[k][1] * hinv);
+      if (e < total) {
+        if (tap) {
+          a.a_tap[(size_t)bb[k] * a.I + c0 + cc[k]] = a0;
+          a.a_tap[(size_t)bb[k] * a.I + c0 + cc[k] + 1] = a1;
         }
+        const int wd = operand_word<NT>(cc[k], bb[k]);
+        op[wd] = __float_as_uint(a0);
+        op[wd + 16] = __float_as_uint(a1);
+      }
+      warp_row_max(s_max, bb[k], e < total ? __float_as_uint(fmaxf(fabsf(a0), fabsf(a1))) : 0u,
+                   lane);
     }
-    const float hinv = s_hinv[b];
-    const float a0 = gelu_tanh(g0 * hinv) * (u0 * hinv);
-    const float a1 = gelu_tanh(g1 * hinv) * (u1 * hinv);
-    if (tap) {
-      a.a_tap[(size_t)b * a.I + col] = a0;
-      a.a_tap[(size_t)b * a.I + col + 1] = a1;
-    }
-    const int wd = operand_word<NT>(cc, b);
-    op[wd] = __float_as_uint(a0);
-    op[wd + 16] = __float_as_uint(a1);
-    atomicMax(&s_max[b], __float_as_uint(fmaxf(fabsf(a0), fabsf(a1))));
   }
-  consumer_sync();
+  consumer_sync<NT>();
   finish_operand<NT>(op, s_max, s_inv, a.B, pairs);
 }
 
 // 1/rms(h) of every batch row: one warp per row, 16-byte loads, the warp tree.
+template <int NT>
 __device__ void h_inv_rms(const FfnArgs& a, float* s_hinv, int warp, int lane) {
-  for (int b = warp; b < a.B; b += kCW) {
+  for (int b = warp; b < a.B; b += Cfg<NT>::kCW) {
     const uint4* row = reinterpret_cast<const uint4*>(a.h + (size_t)b * a.H);
     float ss = 0.f;
     for (int i = lane; i < a.H / 8; i += 32) {
@@ -225,14 +327,16 @@ __device__ void h_inv_rms(const FfnArgs& a, float* s_hinv, int warp, int lane) {
 }
 
 template <int NT>
-__global__ void __launch_bounds__(kThreads, 1) ffn_kernel(const __grid_constant__ FfnArgs a) {
+__global__ void __launch_bounds__(Cfg<NT>::kThreads, 1) ffn_kernel(const __grid_constant__ FfnArgs a) {
+  using K = Cfg<NT>;
+  constexpr int kCW = K::kCW, kConsumers = K::kConsumers, kStages = K::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
   uint8_t* ring = smem;
   uint32_t* op = reinterpret_cast<uint32_t*>(smem + kStages * kStageBytes);
-  float* red = reinterpret_cast<float*>(smem + kStages * kStageBytes + kOpBytes);
-  uint8_t* small = smem + kStages * kStageBytes + kOpBytes + kRedBytes;
+  float* red = reinterpret_cast<float*>(smem + kStages * kStageBytes + K::kOpBytes);
+  uint8_t* small = smem + kStages * kStageBytes + K::kOpBytes + K::kRedBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(small);
   uint64_t* empty = full + kStages;
   volatile int* s_abort = reinterpret_cast<volatile int*>(small + 64);
@@ -241,11 +345,11 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_kernel(const __grid_constant_
   float* s_inv = reinterpret_cast<float*>(small + 192);        // [16] operand scale undo
   float* s_hinv = reinterpret_cast<float*>(small + 256);       // [16] 1/rms(h)
   float* s_dinv = reinterpret_cast<float*>(small + 320);       // [2] 1/rms(d)
-  float* wred = reinterpret_cast<float*>(small + 384);         // [8 warps][2]
+  float* wred = reinterpret_cast<float*>(small + 384);         // [16 warps][2]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, nctas = gridDim.x;
-  if (blockDim.x != kThreads) return;  // the host always launches kThreads
+  if (blockDim.x != K::kThreads) return;  // the host always launches kThreads
   const int k10 = part_begin(c, a.p1.stages, nctas), k11 = part_begin(c + 1, a.p1.stages, nctas);
   const int k20 = part_begin(c, a.p2.stages, nctas), k21 = part_begin(c + 1, a.p2.stages, nctas);
   const int n1 = k11 - k10, nld = n1 + (k21 - k20);
@@ -259,17 +363,10 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_kernel(const __grid_constant_
     fence_barrier_init();
   }
   __syncthreads();
-  // Programmatic dependent launch: the next kernel may be scheduled now.  The weights are
-  // written by no kernel, so their first stages load before the wait for the previous one.
+  if (tid == 0) FFN_STAMP(a, kStampEntry);
+  // Programmatic dependent launch: the next kernel may be scheduled now; nothing is read
+  // before the previous kernel has completed.
   pdl_launch_dependents();
-  const int early = nld < kStages ? nld : kStages;
-  if (warp == kCW && lane == 0) {
-    for (int i = 0; i < early; ++i) {
-      const StageGeo g = i < n1 ? stage_geo(a.p1, k10 + i) : stage_geo(a.p2, k20 + i - n1);
-      mbar_arrive_expect_tx(&full[i], g.bytes);
-      bulk_load(ring + i * kStageBytes, (i < n1 ? a.p1.w : a.p2.w) + g.off, g.bytes, &full[i]);
-    }
-  }
   pdl_wait();
   if (tid == 0) {
     // the step's number: every CTA of a launch reads the counter before its own increment
@@ -277,24 +374,29 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_kernel(const __grid_constant_
     const unsigned long long v = ld_acquire_u64(a.ctr);
     *s_tag = (uint32_t)(v / (unsigned long long)nctas) + 1u;  // 0 marks "never written"
     red_release_add_u64(a.ctr, 1ull);
+    FFN_STAMP(a, kStampWait);
   }
   __syncthreads();
   const uint32_t tag = *s_tag;
 
   if (warp == kCW) {
     // ================================================================ producer
+    // the first operand's activations go out before the ring fill (barrier 2)
+    if (n1 > 0) asm volatile("bar.sync 2, %0;" ::"n"(K::kThreads) : "memory");
     if (lane == 0) {
-      int i = early;
+      int i = 0;
       for (; i < nld; ++i) {
         const int st = i % kStages;
-        if (!mbar_wait(&empty[st], ((i / kStages) - 1) & 1, a.err, s_abort)) {
+        if (i >= kStages && !mbar_wait(&empty[st], ((i / kStages) - 1) & 1, a.err, s_abort)) {
           *s_abort = 1;
           break;
         }
         const StageGeo g = i < n1 ? stage_geo(a.p1, k10 + i) : stage_geo(a.p2, k20 + i - n1);
         mbar_arrive_expect_tx(&full[st], g.bytes);
         bulk_load(ring + st * kStageBytes, (i < n1 ? a.p1.w : a.p2.w) + g.off, g.bytes, &full[st]);
+        if (i >= kStages && i - kStages < 8) FFN_STAMP(a, kStampIssue + i - kStages);
       }
+      FFN_STAMP(a, kStampIssued);
       // every copy in flight lands before the CTA exits (the last use of each slot)
       for (int j = i > kStages ? i - kStages : 0; j < i; ++j)
         mbar_wait(&full[j % kStages], (j / kStages) & 1, a.err);
@@ -313,16 +415,18 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_kernel(const __grid_constant_
     const int key = (ph1 ? 0 : 65536) + g.s;
     if (key != cur) {
       if (!ph1 && !have_hinv) {
-        h_inv_rms(a, s_hinv, warp, lane);
+        h_inv_rms<NT>(a, s_hinv, warp, lane);
         have_hinv = true;
       }
-      consumer_sync();  // the previous operand is no longer read; s_hinv is visible
+      consumer_sync<NT>();  // the previous operand is no longer read; s_hinv is visible
       if (ph1) {
-        build_op1<NT>(a, g.s, op, s_max, s_inv);
+        build_op1<NT>(a, g.s, op, s_max, s_inv, i == 0);
+        if (tid == 0 && i == 0) FFN_STAMP(a, kStampOp1);
       } else {
         const int first = g.s * nps2;  // the split's first stage
         const bool tap = a.a_tap && first >= k20 && first < k21;
         build_op2<NT>(a, g.s, op, s_max, s_inv, s_hinv, tap, tag, s_abort);
+        if (tid == 0 && i == n1) FFN_STAMP(a, kStampOp2);
       }
       cur = key;
     }
@@ -331,52 +435,69 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_kernel(const __grid_constant_
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
     const int wpr = kCW / P.rgs;  // warps per row group
+    const int j = warp / wpr, qw = warp - j * wpr;
     if (mbar_wait(&full[st], (i / kStages) & 1, a.err, s_abort) && !*s_abort) {
-      const int j = warp / wpr, q = warp - j * wpr;
       if (j < g.nrg) {
-        const int t0 = q * P.nbs / wpr, t1 = (q + 1) * P.nbs / wpr;
+        const int t0 = qw * P.nbs / wpr, t1 = (qw + 1) * P.nbs / wpr;
         const uint32_t tp = smem_u32(ring + st * kStageBytes) + (uint32_t)(j * P.nbs * kQ8TileBytes);
         const uint32_t fr = smem_u32(op) + lane * 16;
-#pragma unroll 4
-        for (int t = t0; t < t1; ++t) {
-          const uint4 w = lds128(tp + t * kQ8TileBytes + lane * 16);
-          const uint32_t d = lds32(tp + t * kQ8TileBytes + 512 + (lane >> 2) * 4);
-          q8_tile_mma<NT>(acc, w, d, fr + t * NT * 512);
+        const uint32_t dl = 512 + (lane >> 2) * 4;
+        int t = t0;
+#pragma unroll 2
+        for (; t + 1 < t1; t += 2) {
+          const uint32_t pa = tp + t * kQ8TileBytes, pb = pa + kQ8TileBytes;
+          q8_tile2_mma<NT>(acc, lds128(pa + lane * 16), lds32(pa + dl), fr + t * NT * 512,
+                           lds128(pb + lane * 16), lds32(pb + dl), fr + (t + 1) * NT * 512);
+        }
+        if (t < t1) {
+          const uint32_t pa = tp + t * kQ8TileBytes;
+          q8_tile_mma<NT>(acc, lds128(pa + lane * 16), lds32(pa + dl), fr + t * NT * 512);
         }
       }
     } else {
       *s_abort = 1;
     }
+    if (tid == 0 && i < 8) FFN_STAMP(a, kStampArrived + i);
+    if (tid == 0 && i == 0) FFN_STAMP(a, kStampFirst);
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);
+    if (lane == 0) mbar_arrive(&empty[st]);  // this warp is done with the slot
+    if (j < g.nrg) {
+      // the row group's sums: its warps' parts through shared memory (the buffer of this
+      // stage's parity: a group writes it again two of its stages later, after its barrier
+      // of the stage in between, which every warp of the group passes after its reads)
+      float* rb = red + (i & 1) * (K::kRedHalf / 4);
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      float2 v;
-      v.x = acc[nt][0] + acc[nt][1];  // row g, batch 4 nt + t (hi + lo columns)
-      v.y = acc[nt][2] + acc[nt][3];  // row g + 8
-      reinterpret_cast<float2*>(red)[(warp * NT + nt) * 32 + lane] = v;
-    }
-    consumer_sync();
-    // the row groups' sums: the warps of a row group added in order, then tagged stores
-    const int n_out = g.nrg * a.B * 16;
-    for (int e = tid; e < n_out; e += kConsumers) {
-      const int row = e & 15, jb = e >> 4;
-      const int j = jb / a.B, b = jb - j * a.B;
-      const int nt = b >> 2, src_lane = (row & 7) * 4 + (b & 3), half = row >> 3;
-      float v = 0.f;
-      for (int q = 0; q < wpr; ++q) v += red[(((j * wpr + q) * NT + nt) * 32 + src_lane) * 2 + half];
-      v *= s_inv[b];
+      for (int nt = 0; nt < NT; ++nt) {
+        float2 v;
+        v.x = acc[nt][0] + acc[nt][1];  // row g, batch 4 nt + t (hi + lo columns)
+        v.y = acc[nt][2] + acc[nt][3];  // row g + 8
+        reinterpret_cast<float2*>(rb)[(warp * NT + nt) * 32 + lane] = v;
+      }
+      group_sync(j, wpr * 32);
+      // outputs (b, row) of the group spread over its warps: output e -> warp e % wpr
       const int rg = g.rg0 + j;
-      unsigned long long* dst =
-          ph1 ? a.part1 + ((size_t)g.s * a.B + b) * (2 * (size_t)a.I) + (rg & 1) * (size_t)a.I +
-                    (rg >> 1) * 16 + row
-              : a.part2 + ((size_t)g.s * a.B + b) * a.H + rg * 16 + row;
-      st_tagged(dst, v, tag);
+      for (int e = lane * wpr + qw; e < a.B * 16; e += 32 * wpr) {
+        const int b = e >> 4, row = e & 15;
+        const int nt = b >> 2, src_lane = (row & 7) * 4 + (b & 3), half = row >> 3;
+        const float* rp = rb + ((j * wpr * NT + nt) * 32 + src_lane) * 2 + half;
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kCW; ++w)
+          if (w < wpr) v += rp[w * NT * 64];
+        v *= s_inv[b];
+        unsigned long long* dst =
+            ph1 ? a.part1 + ((size_t)g.s * a.B + b) * (2 * (size_t)a.I) + (rg & 1) * (size_t)a.I +
+                      (rg >> 1) * 16 + row
+                : a.part2 + ((size_t)g.s * a.B + b) * a.H + rg * 16 + row;
+        st_tagged(dst, v, tag);
+      }
     }
-    consumer_sync();
+    if (tid == 0 && i == n1 - 1) FFN_STAMP(a, kStampPh1);
+    if (tid == 0 && i == nld - 1) FFN_STAMP(a, kStampPh2);
   }
 
   // ================================================================== phase 3
+  consumer_sync<NT>();  // every stage's sums are read: the sums area holds d from here
   const int N = a.B * a.H;
   const int e0 = part_begin(c, N, nctas), e1 = part_begin(c + 1, N, nctas);
   const int b_lo = e0 < e1 ? e0 / a.H : 0;
@@ -394,8 +515,9 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_kernel(const __grid_constant_
         for (int k = 0; k < 8; ++k) {
           const int sx = s0 + k < a.p2.S ? s0 + k : a.p2.S - 1;
           w[k] = ld_tagged(a.part2 + sx * s2stride + e);
-          ready = ready && (uint32_t)(w[k] >> 32) == tag;
         }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) ready = ready && (uint32_t)(w[k] >> 32) == tag;
         if (ready || poll_expired(t0, a.err, s_abort)) break;
         __nanosleep(32);
       }
@@ -414,7 +536,8 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_kernel(const __grid_constant_
       wred[warp * 2 + 1] = t1;
     }
   }
-  consumer_sync();
+  consumer_sync<NT>();
+  if (tid == 0) FFN_STAMP(a, kStampD);
   if (tid < 2 && e0 < e1 && b_lo + tid <= (e1 - 1) / a.H) {
     float t = 0.f;
     for (int w = 0; w < kCW; ++w) t += wred[w * 2 + tid];
@@ -442,15 +565,16 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_kernel(const __grid_constant_
         }
         gath[cc - cf] = v;
       }
-      consumer_sync();
+      consumer_sync<NT>();
       if (tid == 0) {
         float t = 0.f;
         for (int cc = cf; cc <= cl; ++cc) t += gath[cc - cf];
         s_dinv[r] = rsqrtf(t / a.H + a.eps);
       }
-      consumer_sync();
+      consumer_sync<NT>();
     }
   }
+  if (tid == 0) FFN_STAMP(a, kStampNorm);
   for (int e = e0 + tid; e < e1; e += kConsumers) {
     const int second = e >= split_e ? 1 : 0;
     const int i = e - (b_lo + second) * a.H;
@@ -460,21 +584,37 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_kernel(const __grid_constant_
     a.out[e] = __float2bfloat16_rn(r);
     if (a.out_f32) a.out_f32[e] = r;
   }
+  if (tid == 0) FFN_STAMP(a, kStampExit);
 }
 
 }  // namespace ffn
 
-int ffn_max_outputs_per_cta() { return ffn::kRedBytes / 4; }
+int ffn_max_outputs_per_cta() { return ffn::kMaxOutputsPerCta; }
+
+// largest k-split (blocks) whose operand every kernel up to nt_max batch tiles holds
+static int max_blocks_per_split(int nt_max) {
+  int m = 1 << 30;
+  for (int nt = 1; nt <= nt_max; nt *= 2) {
+    const int v = ffn::op_bytes(nt) / (nt * 512);
+    m = v < m ? v : m;
+  }
+  return m;
+}
+
+bool ffn_plan_fits(const FfnPhase& p, int nt) {
+  return p.nbs * nt * 512 <= ffn::op_bytes(nt) &&
+         (long long)p.rgs * p.nbs * kQ8TileBytes <= ffn::kStageBytes;
+}
 
 bool plan_ffn_phase(FfnPhase* p, int R, int nb, bool pairs, int nt_max, int grid) {
-  // cost: the bytes of the busiest CTA, plus a charge per stage (its two barriers and
+  // cost: the bytes of the busiest CTA, plus a charge per stage (its barrier and
   // reduction) and per k-split (phase 1's splits are all read by every phase-2 operand)
   long long best = -1;
   const int maxS = pairs ? ffn::kMaxS1 : ffn::kMaxS2;
   for (int S = 1; S <= nb && S <= maxS; ++S) {
     if (nb % S) continue;
     const int nbs = nb / S;
-    if (nbs * nt_max * 512 > ffn::kOpBytes) continue;
+    if (nbs > max_blocks_per_split(nt_max)) continue;
     for (int rgs = 1; rgs <= 8; rgs *= 2) {
       if (pairs && (rgs & 1)) continue;
       const long long sb = (long long)rgs * nbs * kQ8TileBytes;
@@ -505,6 +645,7 @@ unsigned long long FfnOptIn<NT>::mask = 0ull;
 
 template <int NT>
 cudaError_t launch_ffn_t(const FfnArgs& a, int grid, cudaStream_t s) {
+  using K = ffn::Cfg<NT>;
   auto kern = ffn::ffn_kernel<NT>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -512,14 +653,14 @@ cudaError_t launch_ffn_t(const FfnArgs& a, int grid, cudaStream_t s) {
   const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
   unsigned long long* opted_in = &FfnOptIn<NT>::mask;
   if (!bit || !(__atomic_load_n(opted_in, __ATOMIC_ACQUIRE) & bit)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ffn::kSmem);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K::kSmem);
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(opted_in, bit, __ATOMIC_RELEASE);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(ffn::kThreads);
-  cfg.dynamicSmemBytes = ffn::kSmem;
+  cfg.blockDim = dim3(K::kThreads);
+  cfg.dynamicSmemBytes = K::kSmem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -559,6 +700,7 @@ struct hfa_ffn {
   unsigned long long* post_part = nullptr;
   unsigned long long* ctr = nullptr;
   unsigned* err = nullptr;
+  unsigned long long* stamps = nullptr;
   char msg[256] = {0};
 };
 
@@ -719,14 +861,26 @@ extern "C" hfa_status hfa_ffn_step(hfa_ffn* F, void* stream, const void* h, int 
   a.out = (__nv_bfloat16*)out;
   a.out_f32 = out_f32;
   a.a_tap = a_tap;
+  a.stamps = F->stamps;
   a.B = batch;
   a.H = F->d.hidden;
   a.I = F->d.intermediate;
   a.eps = F->d.eps;
+  const int nt = batch <= 4 ? 1 : (batch <= 8 ? 2 : 4);
+  if (!ffn_plan_fits(F->p1, nt) || !ffn_plan_fits(F->p2, nt))
+    return ffn_fail(F, HFA_EUNSUPPORTED, "the plan does not fit the kernel for batch %d", batch);
   const cudaError_t e = launch_ffn(a, F->grid, (cudaStream_t)stream);
   if (e != cudaSuccess) return ffn_fail(F, HFA_ECUDA, "FFN launch: %s", cudaGetErrorString(e));
   return HFA_OK;
 }
+
+extern "C" hfa_status hfa_ffn_set_stamps(hfa_ffn* F, unsigned long long* stamps) {
+  if (!F) return ffn_fail(nullptr, HFA_EINVAL, "ffn is NULL");
+  F->stamps = stamps;
+  return HFA_OK;
+}
+
+extern "C" int hfa_ffn_stamp_rows(const hfa_ffn* F) { return F ? F->grid : 0; }
 
 extern "C" hfa_status hfa_ffn_check_status(hfa_ffn* F, void* stream) {
   if (!F) return ffn_fail(nullptr, HFA_EINVAL, "ffn is NULL");

@@ -158,6 +158,10 @@ def lib():
         L.hfa_ffn_check_status.argtypes = [P, P]
         L.hfa_ffn_last_error.restype = ctypes.c_char_p
         L.hfa_ffn_last_error.argtypes = [P]
+        L.hfa_ffn_set_stamps.restype = C
+        L.hfa_ffn_set_stamps.argtypes = [P, P]
+        L.hfa_ffn_stamp_rows.restype = C
+        L.hfa_ffn_stamp_rows.argtypes = [P]
         L.hfa_ffn_plan_info.restype = C
         L.hfa_ffn_plan_info.argtypes = [P, I, ctypes.POINTER(ctypes.c_int)]
         _lib = L
@@ -477,6 +481,12 @@ class Ffn:
 
     def hfa_ffn_check_status(self, stream=None) -> None:
         self._check(lib().hfa_ffn_check_status(self._h, _stream_ptr(stream)))
+
+    def hfa_ffn_set_stamps(self, stamps: Optional[torch.Tensor]) -> None:
+        self._check(lib().hfa_ffn_set_stamps(self._h, _ptr(stamps)))
+
+    def hfa_ffn_stamp_rows(self) -> int:
+        return int(lib().hfa_ffn_stamp_rows(self._h))
 
     def hfa_ffn_plan_info(self) -> Dict[str, int]:
         v = (ctypes.c_int * 16)()

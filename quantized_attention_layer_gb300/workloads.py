@@ -246,6 +246,8 @@ class FfnWorkload:
 
 # the dense MLP of the pages' decode (2816 -> 5760 gate and up, back to 2816), batch 1
 FFN_B1 = FfnWorkload(name="ffn_b1", hidden=2816, intermediate=5760, batch=1, seed=6)
+FFN_B16 = FfnWorkload(name="ffn_b16", hidden=2816, intermediate=5760, batch=16, seed=7)
+FFN_BY_NAME: Dict[str, FfnWorkload] = {f.name: f for f in (FFN_B1, FFN_B16)}
 
 
 def make_ffn_weights(f: FfnWorkload) -> Dict[str, object]:
