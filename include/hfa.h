@@ -123,7 +123,8 @@ hfa_status hfa_layer_create(const hfa_layer_desc* desc, const void* wq_dev, cons
  * Linear caches need 0 <= seq_pos < C (HFA_ERANGE otherwise).  Requires Q8_0 weights.
  * The cache must hold the earlier positions of each sequence: positions
  * max(0, P-W+1) .. P-1 (sliding) or 0 .. P-1 (full).
- * The step is one cooperative launch of one CTA per SM; it fails with HFA_ECUDA when the
+ * The step is one cooperative launch of at most one CTA per SM (one per SM unless the
+ * layer's largest step has less work: a tiny layer runs on a few); it fails with HFA_ECUDA when the
  * device cannot hold that grid at once (e.g. SMs taken by another context).  It is
  * launched with programmatic dependent launch: it may start while the previous kernel on
  * `stream` finishes, reads nothing but the layer's own weights until that kernel has
@@ -384,7 +385,7 @@ hfa_status hfa_set_successor(hfa_layer* layer, const hfa_layer* next);
 
 /*
  * Instrumentation of the decode step (no counterpart on the pages): with a buffer set,
- * every later decode step of `layer` writes, per CTA c (one CTA per SM), the GPU's
+ * every later decode step of `layer` writes, per CTA c (at most one per SM), the GPU's
  * nanosecond timer (%globaltimer) at fixed points into stamps_dev[c * 16 + k]:
  *   k = 0 CTA start, 1 activations loaded, 2 QKV projection done, 3 first queries ready,
  *   4 last key tile consumed, 5 attention records written, 6 grid barrier passed,

@@ -46,6 +46,7 @@ struct hfa_layer {
   hfa_layer_desc d{};
   int device = 0;
   int num_sms = 0;
+  int grid = 0;  // CTAs of a decode step: fixed per layer (the step tags count launches x grid)
   int G = 0;
   int rows_qkv = 0;
   int max_rows = 0;
@@ -234,6 +235,8 @@ static hfa_status validate_desc(const hfa_layer_desc* d) {
 // Split-K shape of a decode-step GEMV: k-splits of nbs 32-column blocks, nbs the largest
 // divisor of the block count up to 16 (512 columns), and as many nbs-tile work items per
 // 64 KiB ring stage as fit.
+static int step_grid(const hfa_layer_desc& d, const StepGemv& qkv, const StepGemv& o, int sms);
+
 static void plan_step_gemv(StepGemv* g, int rows, int cols) {
   g->R = rows / 16;
   g->nb = cols / 32;
@@ -343,6 +346,7 @@ extern "C" hfa_status hfa_layer_create(const hfa_layer_desc* desc, const void* w
       return HFA_EUNSUPPORTED;
     }
     const int Rq = L->rows_qkv / 16;
+    L->grid = step_grid(*desc, L->g_qkv, L->g_o, L->num_sms);
     LA(L->wqkv_t, (size_t)Rq * L->g_qkv.nb * kQ8TileBytes);
     LA(L->wo_t, (size_t)(H / 16) * L->g_o.nb * kQ8TileBytes);
     L->g_qkv.w = L->wqkv_t;
@@ -487,7 +491,7 @@ extern "C" hfa_status hfa_set_step_stamps(hfa_layer* L, unsigned long long* stam
   return HFA_OK;
 }
 
-extern "C" int hfa_step_stamp_rows(const hfa_layer* L) { return L ? L->num_sms : 0; }
+extern "C" int hfa_step_stamp_rows(const hfa_layer* L) { return L ? L->grid : 0; }
 
 static size_t weight_tile_bytes(const hfa_layer* L, int which, const void** src) {
   *src = nullptr;
@@ -600,6 +604,24 @@ static void fill_attn(AttnArgs& aa, int nh, int nkv, int hd, int C, int layer_ty
   *S_out = S;
 }
 
+// CTAs of a layer's decode step: one per SM, or fewer for a layer whose largest step has
+// less work than SMs (the QKV and o_proj row groups two to a CTA, and the key tiles of the
+// most visible keys at max_batch), never fewer than the GEMVs' k-splits.  Fixed per layer:
+// the step tags are launches x grid.
+static int step_grid(const hfa_layer_desc& d, const StepGemv& qkv, const StepGemv& o, int sms) {
+  const int T = step_keys_per_tile(d.head_dim);
+  const bool ring = d.flags & HFA_F_RING;
+  const int vis = (d.layer_type == HFA_SLIDING && !ring && d.window < d.kv_capacity) ? d.window
+                                                                                     : d.kv_capacity;
+  const long long tiles = (long long)d.max_batch * d.num_kv_heads * ((vis + T - 1) / T + 1);
+  long long work = tiles;
+  if ((qkv.R + 1) / 2 > work) work = (qkv.R + 1) / 2;
+  if ((o.R + 1) / 2 > work) work = (o.R + 1) / 2;
+  if (work > d.hidden) work = d.hidden;  // every CTA keeps outputs of a batch-1 step
+  const int lo = qkv.S > o.S ? qkv.S : o.S;
+  return (int)(work > sms ? sms : (work < lo ? lo : work));
+}
+
 static int visible_keys(const hfa_layer_desc& d, int P) {
   const bool ring = d.flags & HFA_F_RING;
   if (ring) return (P < d.kv_capacity - 1 ? P : d.kv_capacity - 1) + 1;
@@ -694,11 +716,11 @@ extern "C" hfa_status hfa_decode_step(hfa_layer* L, void* stream, const void* x,
   int tiles = 0;
   for (int b = 0; b < batch; ++b) tiles += (visible_keys(d, pos_host[b]) + T - 1) / T * nkv;
   L->last_splits = tiles;
-  L->last_gemv_grid = L->num_sms;
-  L->last_attn_grid = L->num_sms;
+  L->last_gemv_grid = L->grid;
+  L->last_attn_grid = L->grid;
   KernelTimer t;
   timer_begin(L, s, "decode_step", &t);
-  cudaError_t e = launch_step(sa, L->tm_k, L->tm_v, hd, L->num_sms, s);
+  cudaError_t e = launch_step(sa, L->tm_k, L->tm_v, hd, L->grid, s);
   timer_end(L, s, &t);
   if (e != cudaSuccess) return cuda_fail(L, e, "decode-step kernel launch");
   L->last_rows = batch;

@@ -450,7 +450,12 @@ static __device__ __noinline__ void finish_outputs_post(const StepArgs& a, int c
       const int cf = part_of(b * a.H, n, nctas), cl = part_of((b + 1) * a.H - 1, n, nctas);
 #pragma unroll 1
       for (int cc = cf + tid; cc <= cl; cc += kConsumers) {
-        const int slot = b - part_begin(cc, n, nctas) / a.H;
+        const int beg = part_begin(cc, n, nctas);
+        if (beg == part_begin(cc + 1, n, nctas)) {  // a CTA without outputs adds nothing
+          red[cc - cf] = 0.f;
+          continue;
+        }
+        const int slot = b - beg / a.H;
         const uint64_t t0 = globaltimer_ns();
         unsigned long long w;
         for (;;) {
