@@ -111,7 +111,8 @@ void orc_tq_unrotate(double* x, int hd, const int8_t* signs) {
   for (int i = 0; i < hd; ++i) x[i] *= (double)signs[i];  // sign undo
 }
 
-int orc_tq_code_bytes(int hd, int bits) { return hd * bits / 8; }
+// 4-bit codes two to a byte; 5-, 6- and 8-bit codes one to a byte (the byte-packed form)
+int orc_tq_code_bytes(int hd, int bits) { return bits == 4 ? hd / 2 : hd; }
 int orc_tq_blocks(int hd) { return hd / block_dims(hd); }
 
 void orc_tq_encode_row(const double* x, int hd, const int8_t* signs, int bits,
@@ -128,7 +129,7 @@ void orc_tq_encode_row(const double* x, int hd, const int8_t* signs, int bits,
     for (int i = k; i < k + B; ++i)
       code[i] = cell_of(norm > 0.0 ? u[i] / norm : 0.0, boundaries, levels);
   }
-  if (bits == 8) {
+  if (bits != 4) {
     for (int i = 0; i < hd; ++i) codes[i] = (uint8_t)code[i];
   } else {
     for (int j = 0; j < hd / 2; ++j) codes[j] = (uint8_t)(code[2 * j] | (code[2 * j + 1] << 4));
@@ -139,7 +140,7 @@ void orc_tq_decode_row(const uint8_t* codes, const float* norms, int hd, int bit
                        const double* centroids, double* u) {
   const int B = block_dims(hd);
   for (int i = 0; i < hd; ++i) {
-    const int c = bits == 8 ? codes[i] : ((codes[i / 2] >> (4 * (i & 1))) & 15);
+    const int c = bits != 4 ? codes[i] : ((codes[i / 2] >> (4 * (i & 1))) & 15);
     u[i] = centroids[c] * (double)norms[i / B];
   }
 }

@@ -8,7 +8,7 @@
  * Source: hf2q documentation page "gemma4/gpu_full_attn.rs", encode_one_layer: the
  * Hadamard-quantize KV encode (hadamard_quantize_kv, _hb: sign pre-multiply, normalised
  * FWHT, a per-block norm -- one per 256 dims, two for a 512-wide head -- and Lloyd-Max
- * codes, 4-bit nibble-packed or one byte per element), the TQ attention
+ * codes, 4-bit nibble-packed, or one byte per element at 5, 6 and 8 bits), the TQ attention
  * (flash_attn_vec_tq / _tq_hb: Q pre-rotated by the same sign pre-multiply and FWHT,
  * scores and the weighted sum of V in the rotated domain, the output sign-undone), and
  * the hybrid layout (K stored raw, V TQ-coded); "gemma4/model.rs": the cache buffers
@@ -50,11 +50,11 @@ void orc_fwht(double* x, int n);
 void orc_tq_rotate(double* x, int hd, const int8_t* signs);
 void orc_tq_unrotate(double* x, int hd, const int8_t* signs);
 
-/* bytes of one row's codes, and norms per row */
+/* bytes of one row's codes (hd / 2 at 4 bits, hd at 5, 6 and 8 bits), and norms per row */
 int orc_tq_code_bytes(int hd, int bits);
 int orc_tq_blocks(int hd);
 
-/* encode one head row x [hd] (the appended K or V row) with `bits` in {4, 8}: rotate,
+/* encode one head row x [hd] (the appended K or V row) with `bits` in {4, 5, 6, 8}: rotate,
  * norm = sqrt(mean of the rotated block's squares), code of each element = the cell of
  * u / norm (0 when norm is 0); codes [orc_tq_code_bytes], norms [orc_tq_blocks] (f32). */
 void orc_tq_encode_row(const double* x, int hd, const int8_t* signs, int bits,

@@ -3,10 +3,12 @@
 * the Lloyd-Max quantiser of N(0,1): the 2-level closed form (centroids +-sqrt(2/pi),
   mean squared error 1 - 2/pi), the published 4- and 8-level tables (Max, "Quantizing for
   minimum distortion", IRE Trans. Inform. Theory, 1960: levels, thresholds and error to
-  the printed digits), and for 16 and 256 levels the two optimality conditions checked
-  with scipy's truncated-normal mean;
+  the printed digits), for 16, 32, 64 and 256 levels the two optimality conditions checked
+  with scipy's truncated-normal mean, and the Panter-Dite high-resolution error
+  (sqrt(3) pi / 2) 4^-bits approached from below as the bit count grows;
 * the normalised FWHT against the Hadamard matrix built from its popcount definition;
-* the encoder against a brute-force nearest-centroid search in the documented packing;
+* the encoder against a brute-force nearest-centroid search in the documented packing (4-bit
+  nibbles; 5-, 6- and 8-bit codes one byte per element);
 * attention over codes against attention over the dequantised, un-rotated cache, written
   out here in the original domain (orthogonality of the rotation and the sign undo).
 """
@@ -49,7 +51,7 @@ def test_published_quantiser_tables(orc, bits, levels, thresholds, mse):
     assert abs(oracle.lloyd_max_mse(c, b) - mse) < 1e-4
 
 
-@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
 def test_optimality_conditions(orc, bits):
     from scipy.stats import norm, truncnorm
     c, b, _ = oracle.lloyd_max_normal(bits)
@@ -62,6 +64,17 @@ def test_optimality_conditions(orc, bits):
     # mean squared error against direct numerical integration of the cell errors
     num = sum(norm.expect(lambda x, ci=c[i]: (x - ci) ** 2, lb=b[i], ub=b[i + 1]) for i in range(n))
     assert abs(num - oracle.lloyd_max_mse(c, b)) < 1e-9
+
+
+def test_high_resolution_asymptote(orc):
+    # Panter-Dite: the optimal b-bit quantiser of N(0, 1) has mean squared error
+    # (sqrt(3) pi / 2) 4^-b as b grows; the exact quantisers approach it from below
+    r = []
+    for bits in (4, 5, 6, 7, 8):
+        c, b, _ = oracle.lloyd_max_normal(bits)
+        r.append(oracle.lloyd_max_mse(c, b) * 4.0 ** bits / (math.sqrt(3.0) * math.pi / 2.0))
+    assert all(0.85 < x < 1.0 for x in r) and all(x < y for x, y in zip(r, r[1:]))
+    assert r[-1] > 0.99
 
 
 # ------------------------------------------------------------------ rotation
@@ -87,13 +100,13 @@ def test_rotation_blocks_and_inverse(orc, hd):
 # ------------------------------------------------------------------ encoder
 
 def unpack(codes, hd, bits):
-    if bits == 8:
+    if bits != 4:  # 5-, 6- and 8-bit codes: one byte per element
         return codes.astype(np.int64)
     lo, hi = codes & 15, codes >> 4
     return np.stack([lo, hi], axis=-1).reshape(codes.shape[:-1] + (hd,)).astype(np.int64)
 
 
-@pytest.mark.parametrize("hd,bits", [(64, 4), (128, 8), (256, 4), (512, 8)])
+@pytest.mark.parametrize("hd,bits", [(64, 4), (128, 8), (256, 4), (512, 8), (128, 5), (256, 6)])
 def test_encoder_is_the_nearest_centroid(orc, hd, bits):
     s = signs_for(hd, 7)
     c, b, _ = oracle.lloyd_max_normal(bits)
@@ -123,7 +136,7 @@ def test_encoder_scale_invariance_and_zero_row(orc):
     assert nz[0, 0] == 0.0 and np.all(unpack(cz, hd, bits) == len(b) // 2)  # 0 -> upper cell
 
 
-@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
 def test_round_trip_error_matches_the_quantiser(orc, bits):
     hd = 256
     s = signs_for(hd, 10)
@@ -149,7 +162,8 @@ def softmax_attention(q, K, V, scale, softcap):
     return (p / p.sum()) @ V
 
 
-@pytest.mark.parametrize("hd,bits,softcap", [(128, 8, 0.0), (256, 4, 30.0), (512, 8, 0.0)])
+@pytest.mark.parametrize("hd,bits,softcap", [(128, 8, 0.0), (256, 4, 30.0), (512, 8, 0.0),
+                                             (128, 6, 0.0), (64, 5, 20.0)])
 def test_attention_over_codes_is_attention_over_the_dequantised_cache(orc, hd, bits, softcap):
     rng = np.random.default_rng(hd + bits)
     s = signs_for(hd, 12)
