@@ -241,7 +241,8 @@ hfa_status hfa_attention_decode_noalloc(const hfa_attn_desc* desc, void* stream,
 /*
  * Quantised KV cache (TurboQuant): gpu_full_attn.rs, encode_one_layer -- the
  * Hadamard-quantize KV encode (sign pre-multiply, normalised FWHT, a norm per 256-dim
- * block, Lloyd-Max codes packed as 4-bit nibbles or one byte per value), the attention
+ * block, Lloyd-Max codes packed as 4-bit nibbles or, at 5, 6 and 8 bits, one byte per
+ * value), the attention
  * over codes (the query pre-rotated, the output sign-undone) and the hybrid layout (raw
  * keys, coded values); model.rs, the cache buffers.
  * A format fixes head_dim, the code width and the sign pre-multiply.  Rows are coded in
@@ -249,16 +250,17 @@ hfa_status hfa_attention_decode_noalloc(const hfa_attn_desc* desc, void* stream,
  * Hadamard matrix), norm = sqrt(mean(u^2)) stored as f32, and each u_i / norm coded by the
  * cell of the Lloyd-Max quantiser of N(0, 1) with 2^bits levels that holds it (a value on
  * a boundary takes the upper cell; the library computes the quantiser when the format is
- * created).  bits 8: one byte per value; bits 4: value 2j in the low nibble of byte j,
- * 2j+1 in the high nibble.  A coded value decodes to centroid[code] * norm (rotated).
- *   head_dim in {64, 128, 256, 512}; bits in {4, 8};
+ * created).  bits 5, 6, 8: one byte per value; bits 4: value 2j in the low nibble of byte
+ * j, 2j+1 in the high nibble.  A coded value decodes to centroid[code] * norm (rotated).
+ *   head_dim in {64, 128, 256, 512}; bits in {4, 5, 6, 8};
  *   signs_host int8 [head_dim], each +1 or -1, copied.
  * Errors: HFA_EINVAL, HFA_EUNSUPPORTED, HFA_EDEVICE, HFA_ENOMEM.
  */
 typedef struct hfa_tq hfa_tq;
 hfa_status hfa_tq_create(int head_dim, int bits, const int8_t* signs_host, hfa_tq** out);
 hfa_status hfa_tq_destroy(hfa_tq* fmt);
-int hfa_tq_code_bytes(const hfa_tq* fmt); /* bytes of one row's codes: head_dim * bits / 8 */
+int hfa_tq_code_bytes(const hfa_tq* fmt); /* bytes of one row's codes: head_dim / 2 at 4 bits,
+                                             head_dim at 5, 6 and 8 bits */
 int hfa_tq_blocks(const hfa_tq* fmt);     /* norms per row: head_dim / B */
 /* copies up to n centroids (ascending) to centroids_host; returns the level count */
 int hfa_tq_codebook(const hfa_tq* fmt, float* centroids_host, int n);

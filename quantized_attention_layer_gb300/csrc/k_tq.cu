@@ -36,7 +36,7 @@
 #include "hfa_internal.h"
 
 struct hfa_tq {
-  int hd, bits, levels, blocks, code_bytes, device;
+  int hd, bits, sbits, levels, blocks, code_bytes, device;  // sbits: bits stored per code
   float* centroids = nullptr;  // device [levels]
   double* bounds = nullptr;    // device [levels - 1]: the interior cell boundaries, ascending
   float* signs = nullptr;      // device [hd]: +-1
@@ -292,7 +292,9 @@ __global__ void __launch_bounds__(kTqThreads) tq_attn_kernel(const TqAttnArgs a)
   const int G = a.nh / a.nkv;  // <= GM
   const int unit = blockIdx.x / a.splits, split = blockIdx.x - unit * a.splits;
   const int b = unit / a.nkv, kvh = unit - b * a.nkv;
-  for (int i = tid; i < LEVELS * 32; i += kTqThreads) s_tab[i] = a.centroids[i >> 5];
+  // the table has room for 2^BITS levels; a byte-coded format may use fewer (5, 6 bits)
+  for (int i = tid; i < LEVELS * 32; i += kTqThreads)
+    s_tab[i] = (i >> 5) < a.levels ? a.centroids[i >> 5] : 0.f;
   for (int e = tid; e < GM * HD; e += kTqThreads) {
     const int h = e / HD, i = e - h * HD;
     const float qv = h < G ? a.q[((size_t)b * a.nh + kvh * G + h) * HD + i] * a.qscale : 0.f;
@@ -639,7 +641,8 @@ extern "C" hfa_status hfa_tq_create(int head_dim, int bits, const int8_t* signs,
   *out = nullptr;
   if (head_dim != 64 && head_dim != 128 && head_dim != 256 && head_dim != 512)
     return tq_fail(HFA_EUNSUPPORTED, "head_dim=%d (supported: 64, 128, 256, 512)", head_dim);
-  if (bits != 4 && bits != 8) return tq_fail(HFA_EUNSUPPORTED, "bits=%d (supported: 4, 8)", bits);
+  if (bits != 4 && bits != 5 && bits != 6 && bits != 8)
+    return tq_fail(HFA_EUNSUPPORTED, "bits=%d (supported: 4, 5, 6, 8)", bits);
   if (!signs) return tq_fail(HFA_EINVAL, "signs is NULL");
   for (int i = 0; i < head_dim; ++i)
     if (signs[i] != 1 && signs[i] != -1) return tq_fail(HFA_EINVAL, "signs[%d]=%d is not +-1", i, signs[i]);
@@ -652,7 +655,8 @@ extern "C" hfa_status hfa_tq_create(int head_dim, int bits, const int8_t* signs,
   t->bits = bits;
   t->levels = 1 << bits;
   t->blocks = head_dim / (head_dim < 256 ? head_dim : 256);
-  t->code_bytes = head_dim * bits / 8;
+  t->sbits = bits == 4 ? 4 : 8;  // 5- and 6-bit codes are stored one per byte
+  t->code_bytes = head_dim * t->sbits / 8;
   t->device = dev;
   t->centroids_host.assign(cb.cent.begin(), cb.cent.end());
   std::vector<float> sg(head_dim);
@@ -726,7 +730,7 @@ extern "C" hfa_status hfa_tq_append(const hfa_tq* t, void* stream, const float* 
   a.levels = t->levels;
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e;
-  switch (t->hd * 16 + t->bits) {
+  switch (t->hd * 16 + t->sbits) {
     case 64 * 16 + 4: e = launch_append_t<64, 4>(a, s); break;
     case 64 * 16 + 8: e = launch_append_t<64, 8>(a, s); break;
     case 128 * 16 + 4: e = launch_append_t<128, 4>(a, s); break;
@@ -856,10 +860,10 @@ extern "C" hfa_status hfa_attention_decode_tq(const hfa_attn_desc* d, const hfa_
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e;
   const int grid = units * S;
-  if (hd == 64) e = launch_attn_hd<64>(a, t->bits, kraw, grid, s);
-  else if (hd == 128) e = launch_attn_hd<128>(a, t->bits, kraw, grid, s);
-  else if (hd == 256) e = launch_attn_hd<256>(a, t->bits, kraw, grid, s);
-  else e = launch_attn_hd<512>(a, t->bits, kraw, grid, s);
+  if (hd == 64) e = launch_attn_hd<64>(a, t->sbits, kraw, grid, s);
+  else if (hd == 128) e = launch_attn_hd<128>(a, t->sbits, kraw, grid, s);
+  else if (hd == 256) e = launch_attn_hd<256>(a, t->sbits, kraw, grid, s);
+  else e = launch_attn_hd<512>(a, t->sbits, kraw, grid, s);
   if (e != cudaSuccess) return tq_fail(HFA_ECUDA, "attention launch: %s", cudaGetErrorString(e));
   return HFA_OK;
 }

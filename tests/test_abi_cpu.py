@@ -104,6 +104,7 @@ def test_quantised_kv_format_rejects_bad_arguments_before_any_device_call(libhfa
     bad[5] = 0
     P = lambda a: ctypes.c_void_p(a.ctypes.data)  # noqa: E731
     assert libhfa.hfa_tq_create(128, 3, P(ok), ctypes.byref(h)) == hfa.HFA_EUNSUPPORTED
+    assert libhfa.hfa_tq_create(128, 7, P(ok), ctypes.byref(h)) == hfa.HFA_EUNSUPPORTED
     assert libhfa.hfa_tq_create(96, 8, P(ok), ctypes.byref(h)) == hfa.HFA_EUNSUPPORTED
     assert libhfa.hfa_tq_create(128, 8, P(bad), ctypes.byref(h)) == hfa.HFA_EINVAL
     assert b"signs[5]" in libhfa.hfa_last_error(None)

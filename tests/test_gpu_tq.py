@@ -5,7 +5,7 @@
   of the same f32 rows (both take the decisions in double precision; a code may differ only
   for a value within 1e-9 of a cell boundary, where the two independently converged
   codebooks may place it apart -- counted, expected 0), and every other slot unchanged;
-* the attention over codes (4- and 8-bit, head dims 64 to 512, ring, sliding window,
+* the attention over codes (4-, 5-, 6- and 8-bit, head dims 64 to 512, ring, sliding window,
   softcap, the hybrid raw-K layout) against the oracle on the same seeded codes, within
   relative L2 2e-3 per sequence and head group;
 * encode followed by attention against the oracle's encode followed by its attention.
@@ -32,12 +32,12 @@ def _built():
 
 
 def unpack(codes, hd, bits):
-    if bits == 8:
+    if bits != 4:  # 5-, 6- and 8-bit codes: one byte per element
         return codes.astype(np.int64)
     return np.stack([codes & 15, codes >> 4], axis=-1).reshape(codes.shape[:-1] + (hd,)).astype(np.int64)
 
 
-@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
 def test_codebook_matches_the_oracle(bits):
     fmt = hfa.TqFormat(128, bits, wl.make_tq_signs(128, 1))
     c, _, _ = oracle.lloyd_max_normal(bits)
@@ -47,7 +47,8 @@ def test_codebook_matches_the_oracle(bits):
 
 
 @pytest.mark.parametrize("hd,bits,ring", [(64, 4, False), (128, 8, False), (256, 4, True),
-                                          (512, 8, False), (128, 4, True)])
+                                          (512, 8, False), (128, 4, True), (128, 5, False),
+                                          (256, 6, True)])
 def test_append_codes_equal_the_oracle(hd, bits, ring):
     B, nkv, C = 3, 2, 40
     signs = wl.make_tq_signs(hd, hd + bits)
@@ -87,9 +88,10 @@ def test_append_codes_equal_the_oracle(hd, bits, ring):
 def _synthetic_tq_cache(B, nkv, C, hd, bits, seed):
     """Seeded synthetic coded cache: codes uniform over the levels, norms ~U[0.5, 1.5]."""
     g = torch.Generator().manual_seed(seed)
-    cb = hd * bits // 8
+    cb = hd // 2 if bits == 4 else hd
     nb = hd // min(hd, 256)
-    codes = torch.randint(0, 256, (B, nkv, C, cb), generator=g, dtype=torch.uint8)
+    top = 256 if bits in (4, 8) else 1 << bits  # nibble pairs / bytes over every code
+    codes = torch.randint(0, top, (B, nkv, C, cb), generator=g, dtype=torch.uint8)
     norms = torch.rand((B, nkv, C, nb), generator=g) + 0.5
     return codes, norms
 
@@ -142,7 +144,7 @@ def test_attention_over_codes_32k_context_8bit():
     _run_tq_attention(w, 8, [32767], seed=21)
 
 
-@pytest.mark.parametrize("hd,bits", [(64, 4), (128, 4), (256, 8), (512, 4)])
+@pytest.mark.parametrize("hd,bits", [(64, 4), (128, 4), (256, 8), (512, 4), (128, 5), (64, 6)])
 def test_attention_over_codes_head_dims(hd, bits):
     nh = 16 if hd == 512 else 8
     w = wl.Workload(name=f"tq{hd}", hidden=256, num_heads=nh, num_kv_heads=2, head_dim=hd,
@@ -173,7 +175,7 @@ def test_hybrid_raw_keys_coded_values():
     _run_tq_attention(w, 8, [1500, 600], hybrid=True, seed=33)
 
 
-@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("bits", [4, 6, 8])
 def test_encode_then_attend_matches_the_oracle_pipeline(bits):
     # f32 K/V rows appended one position at a time by the library's encoder, then attended;
     # the oracle encodes the same rows itself and attends over its own codes
