@@ -24,6 +24,13 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s: far beyond any legal w
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+// The dynamic shared array rounded up to a 1024-byte boundary by pointer arithmetic on the
+// shared array itself: the compiler then knows every pointer derived from it is in the
+// shared window and emits shared loads and stores (a round trip through an integer would
+// leave it generic pointers).
+__device__ __forceinline__ uint8_t* smem_align1024(uint8_t* smem_raw) {
+  return smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+}
 
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

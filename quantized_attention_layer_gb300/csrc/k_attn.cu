@@ -60,8 +60,7 @@ __global__ void __launch_bounds__(288)
   constexpr int kNC = Cfg::NC;
   constexpr int RS = Cfg::RS;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~(uintptr_t)1023);
+  uint8_t* smem = smem_align1024(smem_raw);
   uint8_t* stages = smem;
   uint4* qf = reinterpret_cast<uint4*>(smem + kStages * Cfg::STAGE_BYTES);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * Cfg::STAGE_BYTES + Cfg::QF_BYTES);

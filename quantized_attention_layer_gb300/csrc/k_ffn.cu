@@ -331,8 +331,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1) ffn_kernel(const __grid_
   using K = Cfg<NT>;
   constexpr int kCW = K::kCW, kConsumers = K::kConsumers, kStages = K::kStages;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~(uintptr_t)1023);
+  uint8_t* smem = smem_align1024(smem_raw);
   uint8_t* ring = smem;
   uint32_t* op = reinterpret_cast<uint32_t*>(smem + kStages * kStageBytes);
   float* red = reinterpret_cast<float*>(smem + kStages * kStageBytes + K::kOpBytes);

@@ -971,8 +971,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ StepArgs a) {
   using AC = Attn<HD>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~(uintptr_t)1023);
+  uint8_t* smem = smem_align1024(smem_raw);
   uint8_t* ring = smem;
   uint8_t* uni = smem + kStages * kStageBytes;
   uint8_t* small = uni + kUnionBytes;

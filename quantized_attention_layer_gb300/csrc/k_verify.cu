@@ -142,8 +142,7 @@ __global__ void __launch_bounds__(256) verify_prep_kernel(const __nv_bfloat16* _
 template <int MODE>
 __global__ void __launch_bounds__(128, 1) verify_gemm_kernel(const VGemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~(uintptr_t)1023);
+  uint8_t* smem = smem_align1024(smem_raw);
   uint8_t* ring = smem;  // stage i: weight tile (16 KB), then activation chunk (4 KB)
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + kVStages * kVStageBytes);
   uint64_t* empty = full + kVStages;
@@ -373,8 +372,7 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
   constexpr int NS = Cfg::NS;
   constexpr int KB = Cfg::KB;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~(uintptr_t)1023);
+  uint8_t* smem = smem_align1024(smem_raw);
   uint8_t* stages = smem;
   uint4* qf = reinterpret_cast<uint4*>(smem + NS * Cfg::STAGE);  // [warp][KS][32]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * Cfg::STAGE + 8 * Cfg::KS * 512);
@@ -664,8 +662,7 @@ __global__ void __launch_bounds__(vtc::THREADS, 1)
   constexpr int HD = 128;
   constexpr int RS = HD + 4;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~(uintptr_t)1023);
+  uint8_t* smem = smem_align1024(smem_raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + BAR_OFF);  // [NS]
   uint64_t* s_bar = full + NS;    // [2] S of stage i in TMEM buffer i % 2
   uint64_t* p_bar = s_bar + 2;    // Px, Vt written and O rescaled (one arrival per warp)
