@@ -51,8 +51,9 @@ METRIC = "decode steps/sec per layer at 1 GB300; achieved HBM GB/s as % of peak"
 UNIT = "steps/s"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0
-EXTRA = ("tiny_sliding", "sliding_b16_ring1024", "full_b4_128k_softcap", "verify_l16_8k", "ffn_b1",
-         "ffn_b16", "tq8_full_b1_32k", "tq4_full_b1_32k")
+EXTRA = ("tiny_sliding", "sliding_b16_ring1024", "full_b4_128k_softcap", "verify_l16_8k",
+         "global_hd512_32k", "drafter_l16_8k", "ffn_b1", "ffn_b16", "tq8_full_b1_32k",
+         "tq4_full_b1_32k")
 # attention over a quantised (TurboQuant) KV cache: bits, and the attention shape of the
 # headline layer (batch 1, 32/8 heads, head dim 128, 32768 visible keys)
 TQ = {"tq8_full_b1_32k": 8, "tq4_full_b1_32k": 4}
@@ -129,7 +130,8 @@ def workload_bytes(w, pos):
     """Algorithmic bytes of one step: Q8_0 weights at 34/32 B per weight, the visible
     bf16 K and V rows, activations in and out, the appended K/V row."""
     H, nkv, hd = w.hidden, w.num_kv_heads, w.head_dim
-    wbytes = (w.q_rows + 2 * w.kv_rows) * H * 34 // 32 + H * w.q_rows * 34 // 32
+    kv_proj = 1 if w.k_eq_v else 2  # k_eq_v layers have no V projection
+    wbytes = (w.q_rows + kv_proj * w.kv_rows) * H * 34 // 32 + H * w.q_rows * 34 // 32
     kv = 0
     for P in pos:
         if w.ring:
@@ -422,12 +424,15 @@ def decode_workload(w, K, W, R, world, want_cpu=False):
 
 def verify_workload(w, K, W, R, world):
     """The multi-token verify block (L tokens through one layer, bf16 weights): blocks/s,
-    and the roofline of its QKV projection (tcgen05 GEMM)."""
+    and the roofline of its QKV projection (tcgen05 GEMM).  A drafter workload (bidirectional
+    block) first appends its context rows each step (K/V projections only)."""
     from quantized_attention_layer_gb300 import hfa, workloads as wl
     weights = wl.make_weights(w)
     x = wl.make_x(w)
     kv = wl.make_kv_cache(w)
     L, base = w.verify_len, w.base_pos
+    S = wl.DRAFTER_CTX_ROWS if w.block_bidir else 0
+    x_ctx = wl.bf16_normal((S, w.hidden), torch.Generator().manual_seed(w.seed + 5)).cuda() if S else None
     dev_w = hfa.weights_to_device(w, weights)
     stream = torch.cuda.Stream()
     layers, caches = [], []
@@ -442,6 +447,8 @@ def verify_workload(w, K, W, R, world):
 
     def step(i):
         kc, vc = caches[i % R]
+        if S:
+            layers[i % R].hfa_ctx_append(x_ctx, base - S, kc, vc, stream=stream)
         layers[i % R].hfa_verify_block(xd, base, kc, vc, out, stream=stream)
 
     for i in range(max(3, W)):
@@ -474,6 +481,8 @@ def verify_workload(w, K, W, R, world):
     wo_bytes = H * qr * 2
     kv_bytes = (base + L) * w.num_kv_heads * w.head_dim * 2 * 2
     step_bytes = wqkv_bytes + wo_bytes + kv_bytes + 2 * L * H * 2
+    if S:  # the context rows: the K and V weight rows read again, their K/V rows written
+        step_bytes += 2 * kr * H * 2 + S * H * 2 + S * 2 * kr * 2
     peak, src = measured_peaks()
     g = kt.get("verify_qkv_gemm", [float("nan"), 1])
     g_us = g[0] / max(g[1], 1) * 1e3
@@ -489,7 +498,8 @@ def verify_workload(w, K, W, R, world):
            "kernels": {k: {"avg_us": v[0] / max(v[1], 1) * 1e3, "launches": v[1],
                            "timing": "events around each host-launched kernel (no overlap)"}
                        for k, v in kt.items()},
-           "clocks": clocks, "launches": 5 * K, "peak": peak, "peak_source": src}
+           "clocks": clocks, "launches": (5 + (2 if S else 0)) * K, "peak": peak,
+           "peak_source": src, "context_rows": S}
     for Lr in layers:
         Lr.hfa_destroy()
     del caches

@@ -382,7 +382,7 @@ static __device__ void finish_outputs(const StepArgs& a, int c, int nctas, float
 // in `ybuf`, shared memory), publishes sum(y^2) of its part of each row (tagged, slot 0 for
 // its first row, 1 for the second), then adds up, in CTA order, the parts of the CTAs that
 // share each of its rows, and writes its outputs.
-static __device__ __noinline__ void finish_outputs_post(const StepArgs& a, int c, int nctas,
+static __device__ __forceinline__ void finish_outputs_post(const StepArgs& a, int c, int nctas,
                                                         float* red, float* ybuf, uint32_t tag,
                                                         volatile int* abort) {
   const int S = a.o.S;
@@ -901,8 +901,8 @@ __device__ __forceinline__ void build_unit_table(const StepArgs& a, const int* g
 // Builds the o_proj operand of k-split s in xw (the union) from the records.  Batch slots
 // past B are left as they are: their MMA columns never reach a stored output.
 template <int HD, int NT>
-__device__ __noinline__ void merge_operand(const StepArgs& a, int G, int s, bool write_attn,
-                                           uint32_t* xw) {
+__device__ __forceinline__ void merge_operand(const StepArgs& a, int G, int s, bool write_attn,
+                                              uint32_t* xw) {
   const int W = a.o.nbs * 32;
   const int kvh0 = s * W / HD / G, nk = (s * W + W - 1) / HD / G - kvh0 + 1;
   const unsigned* units =

@@ -128,7 +128,22 @@ FULL_128K_B4 = Workload(
     batch=4, rope_theta=1e6, seed=4, seq_pos=131071, softcap=50.0)
 
 WORKLOADS: List[Workload] = [TINY_SLIDING, FULL_32K, SLIDING_B16, VERIFY_L16, FULL_128K_B4]
-BY_NAME: Dict[str, Workload] = {w.name: w for w in WORKLOADS}
+
+# The pages' global layer: 16 query heads of 512 dims over 2 KV heads (GQA group 8), full
+# attention, no V projection (V = unit-normed raw K), RoPE frequency factors and the
+# post-attention norm; hidden 2816 (the dense model's width) at a 32K context.
+GLOBAL_32K = Workload(name="global_hd512_32k", hidden=2816, num_heads=16, num_kv_heads=2,
+                      head_dim=512, layer_type=FULL, window=0, kv_capacity=32768, ring=False,
+                      batch=1, rope_theta=1e6, seed=70, seq_pos=32767, k_eq_v=True,
+                      rope_freq_factors=True, post_norm=True)
+# A drafter step on the verify shape: 16 context rows appended at 8176..8191 (K/V
+# projections only), then a 16-token block at 8192..8207, bidirectional within the block,
+# scale 1/sqrt(hd).
+DRAFTER_L16 = dataclasses.replace(VERIFY_L16, name="drafter_l16_8k", block_bidir=True,
+                                  attn_scale=128 ** -0.5)
+DRAFTER_CTX_ROWS = 16
+
+BY_NAME: Dict[str, Workload] = {w.name: w for w in WORKLOADS + [GLOBAL_32K, DRAFTER_L16]}
 
 
 def _gen(seed: int, stream: int) -> torch.Generator:

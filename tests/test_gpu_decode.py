@@ -70,13 +70,9 @@ def test_other_head_dims_sliding_linear(hd):
     _case(w, pos=[150, 613])
 
 
-# The pages' global layer: 16 query heads of 512 dims over 2 KV heads (GQA group 8), full
-# attention, no V projection (V = unit-normed raw K), RoPE frequency factors and the
-# post-attention norm; hidden 2816 splits the QKV rows into k-splits of 11 blocks.
-GLOBAL_32K = wl.Workload(name="global_hd512_32k", hidden=2816, num_heads=16, num_kv_heads=2,
-                         head_dim=512, layer_type=wl.FULL, window=0, kv_capacity=32768,
-                         ring=False, batch=1, rope_theta=1e6, seed=70, seq_pos=32767,
-                         k_eq_v=True, rope_freq_factors=True, post_norm=True)
+# The pages' global layer (hd 512, 16/2 heads, k_eq_v, frequency factors, post norm) at 32K;
+# hidden 2816 splits the QKV rows into k-splits of 11 blocks.
+GLOBAL_32K = wl.GLOBAL_32K
 
 
 def test_global_layer_hd512_32k_context():
