@@ -986,6 +986,8 @@ extern "C" hfa_status hfa_check_device_status(hfa_layer* L, void* stream) {
        "reset");
   if (L->post_part)
     CK(L, cudaMemsetAsync(L->post_part, 0, (size_t)L->num_sms * 2 * 8, s), "reset");
+  if (L->verify && hfa::verify_reset(L->verify, s) != HFA_OK)
+    return fail(L, HFA_ECUDA, "reset of the verify partial sums failed");
   CK(L, cudaStreamSynchronize(s), "sync");
   return fail(L, HFA_EDEVICE, "device status 0x%x:%s%s%s", v,
               (v & kErrWaitTimeout) ? " a bounded wait gave up;" : "",

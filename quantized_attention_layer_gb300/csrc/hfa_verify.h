@@ -39,6 +39,8 @@ struct VerifyCall {
 
 hfa_status verify_create(const hfa_layer_desc& d, int num_sms, VerifyState** out);
 void verify_free(VerifyState* v);
+// after a device error: the QKV GEMMs' launch counters and tagged partial sums restart
+hfa_status verify_reset(VerifyState* v, cudaStream_t s);
 const char* verify_error();
 hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int msg_len);
 // the drafter's context rows: c.x holds c.L rows, projected by Wk and Wv only (no input

@@ -13,8 +13,9 @@
 //    shared-memory image, so each is one 16 KB bulk copy -- with the matching 4 KB
 //    activation chunk into a 10-stage ring; one thread issues tcgen05.mma into a 128x32
 //    fp32 TMEM accumulator and releases stages with tcgen05.commit.  The k-splits of a
-//    row tile form a cluster and add their partial sums through distributed shared
-//    memory; then the head epilogue (norms, RoPE, KV append; the query also as the
+//    row tile add their partial sums through global memory as tagged entries (QKV: one
+//    cooperative launch, a CTA on every SM) or, in a cluster, through distributed shared
+//    memory (o_proj); then the head epilogue (norms, RoPE, KV append; the query also as the
 //    attention's operand image) or the residual epilogue runs on the complete rows.
 //  * attn_verify_tc_kernel (head_dim 128, tcgen05): one CTA per (KV head, key chunk);
 //    S = Qx K^T and O += Px Vt on the tensor cores with TMEM accumulators, the online
@@ -31,6 +32,7 @@
 
 #include "hfa_common.cuh"
 #include "hfa_finish.cuh"
+#include "hfa_gemv.cuh"
 #include "hfa_internal.h"
 #include "hfa_verify.h"
 
@@ -79,6 +81,12 @@ struct VGemmArgs {
   int splits;        // k-splits per row tile
   int tpc;           // row tiles per cluster: hd / 128 for QKV heads wider than a tile, else 1
   int tile_base;     // first row tile (the context rows start at the key rows' tile)
+  // With gpart set, the k-splits add their partial sums through global memory instead of a
+  // cluster: CTA i stores [16 tokens][128 rows] f32 as 8-byte entries (value | launch tag)
+  // at gpart + i * 2048, and the CTAs of a group (the tpc x splits consecutive CTAs that a
+  // cluster would hold) poll one another's entries.  gctr counts launches x grid (the tags).
+  unsigned long long* gpart;
+  unsigned long long* gctr;
 };
 
 // Activation operand of the verify GEMMs, built once per call: row t of the block
@@ -148,6 +156,8 @@ __global__ void __launch_bounds__(128, 1) verify_gemm_kernel(const VGemmArgs a) 
   uint64_t* empty = full + kVStages;
   uint64_t* done = empty + kVStages;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(done + 1);
+  uint32_t* s_tag = s_tmem + 1;                                  // global reduction: this launch's tag
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 2);
   float* s_tab = reinterpret_cast<float*>(ring + kVStages * kVStageBytes + 256);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = a.tile_base + blockIdx.x / a.splits, sp = blockIdx.x % a.splits;
@@ -208,6 +218,14 @@ __global__ void __launch_bounds__(128, 1) verify_gemm_kernel(const VGemmArgs a) 
   }
   pdl_wait();
   pdl_launch_dependents();
+  if (a.gpart && threadIdx.x == 0) {
+    // the launch's number: every CTA reads the counter before its own increment and after
+    // every increment of the launches before it
+    const unsigned long long n = ld_acquire_u64(a.gctr);
+    *s_tag = (uint32_t)(n / (unsigned long long)gridDim.x) + 1u;  // 0 marks "never written"
+    *s_abort = 0;
+    red_release_add_u64(a.gctr, 1ull);
+  }
 
   if (warp == 0 && lane == 0) {
     // ---- producer
@@ -263,25 +281,70 @@ __global__ void __launch_bounds__(128, 1) verify_gemm_kernel(const VGemmArgs a) 
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, kVN);
 
-  // ---- k-split reduction through distributed shared memory: the cluster is the
-  // a.splits CTAs of a.tpc consecutive row tiles (rank = tile-in-cluster * splits + split).
-  // Each output is summed over the splits in rank order, so the result does not depend
-  // on timing.
+  // ---- k-split reduction.  The group is the a.splits CTAs of a.tpc consecutive row tiles
+  // (rank = tile-in-group * splits + split): a cluster reading distributed shared memory, or
+  // (gpart set) CTAs polling one another's tagged entries in global memory.  Each output is
+  // summed over the splits in rank order, so the result does not depend on timing.
   namespace cg = cooperative_groups;
-  cg::cluster_group cluster = cg::this_cluster();
   GemvArgs g = a.g;
   if (MODE == kModeQKV) {
     g.w_q = s_tab;
     g.w_k = s_tab + a.g.hd;
     g.rope_g = reinterpret_cast<const float2*>(s_tab + 2 * a.g.hd);
   }
-  cluster.sync();  // every CTA's partial sums are visible
   const int S = a.splits;
-  const int rank = (int)cluster.block_rank(), cs = S * a.tpc;
+  const int cs = S * a.tpc;
+  int rank;
+  uint32_t tag = 0;
+  if (a.gpart) {
+    rank = (int)(blockIdx.x % (unsigned)cs);
+    tag = *s_tag;
+    unsigned long long* mine = a.gpart + (size_t)blockIdx.x * (16 * kVM);
+    for (int i = threadIdx.x; i < 16 * kVM; i += blockDim.x) st_tagged(mine + i, psum[i], tag);
+  } else {
+    rank = (int)cg::this_cluster().block_rank();
+    cg::this_cluster().sync();  // every CTA's partial sums are visible
+  }
+  const unsigned long long* gbase =
+      a.gpart ? a.gpart + (size_t)(blockIdx.x - rank) * (16 * kVM) : nullptr;
+  // output (row r of the group's rows, token t) summed over the splits
+  auto split_sum = [&](int r, int t) -> float {
+    float acc = 0.f;
+    if (a.gpart) {
+      const unsigned long long* p = gbase + (size_t)((r >> 7) * S) * (16 * kVM) + t * kVM + (r & 127);
+      for (int c0 = 0; c0 < S; c0 += 4) {
+        unsigned long long w[4];
+        const uint64_t t0 = globaltimer_ns();
+        for (;;) {
+          bool ready = true;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            w[i] = ld_tagged(p + (size_t)(c0 + i < S ? c0 + i : S - 1) * (16 * kVM));
+            ready = ready && (uint32_t)(w[i] >> 32) == tag;
+          }
+          if (ready || *s_abort) break;
+          if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(a.g.err, kErrWaitTimeout);
+            *s_abort = 1;
+            break;
+          }
+          __nanosleep(32);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (c0 + i < S) acc += tagged_value(w[i]);
+      }
+    } else {
+      cg::cluster_group cluster = cg::this_cluster();
+      for (int c = 0; c < S; ++c)
+        acc += cluster.map_shared_rank(psum, (r >> 7) * S + c)[t * kVM + (r & 127)];
+    }
+    return acc;
+  };
   if (MODE == kModeQKV) {
-    // items (head, token) of the cluster's rows, one warp each
+    // items (head, token) of the group's rows, one warp each
     const int hd = a.g.hd;
-    const int tile0 = m0 / kVM - (rank / S);  // first row tile of the cluster
+    const int tile0 = m0 / kVM - (rank / S);  // first row tile of the group
     const int rows0 = tile0 * kVM;
     const int nheads = a.tpc * kVM / hd;
     const int nitems = nheads * L;
@@ -291,35 +354,17 @@ __global__ void __launch_bounds__(128, 1) verify_gemm_kernel(const VGemmArgs a) 
       if (hd == 64) {
         float v[2];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int r = hl * 64 + lane + 32 * j;  // row within the cluster's rows
-          float acc = 0.f;
-          for (int c = 0; c < S; ++c)
-            acc += cluster.map_shared_rank(psum, (r >> 7) * S + c)[t * kVM + (r & 127)];
-          v[j] = acc;
-        }
+        for (int j = 0; j < 2; ++j) v[j] = split_sum(hl * 64 + lane + 32 * j, t);
         finish_head_row<64>(g, hh, t, v, lane);
       } else if (hd == 128) {
         float v[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int r = hl * 128 + lane + 32 * j;
-          float acc = 0.f;
-          for (int c = 0; c < S; ++c)
-            acc += cluster.map_shared_rank(psum, (r >> 7) * S + c)[t * kVM + (r & 127)];
-          v[j] = acc;
-        }
+        for (int j = 0; j < 4; ++j) v[j] = split_sum(hl * 128 + lane + 32 * j, t);
         finish_head_row<128>(g, hh, t, v, lane);
       } else {
         float v[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int r = hl * 256 + lane + 32 * j;
-          float acc = 0.f;
-          for (int c = 0; c < S; ++c)
-            acc += cluster.map_shared_rank(psum, (r >> 7) * S + c)[t * kVM + (r & 127)];
-          v[j] = acc;
-        }
+        for (int j = 0; j < 8; ++j) v[j] = split_sum(hl * 256 + lane + 32 * j, t);
         finish_head_row<256>(g, hh, t, v, lane);
       }
     }
@@ -328,12 +373,11 @@ __global__ void __launch_bounds__(128, 1) verify_gemm_kernel(const VGemmArgs a) 
     const int n = L * kVM;
     const int i0 = n * rank / S, i1 = n * (rank + 1) / S;
     for (int i = i0 + (int)threadIdx.x; i < i1; i += blockDim.x) {
-      float y = 0.f;
-      for (int c = 0; c < S; ++c) y += cluster.map_shared_rank(psum, c)[i];
+      const float y = split_sum(i & 127, i >> 7);
       finish_row_item(g, i >> 7, m0 + (i & 127), y);
     }
   }
-  cluster.sync();  // no CTA leaves while another still reads its shared memory
+  if (!a.gpart) cg::this_cluster().sync();  // no CTA leaves while another reads its shared memory
 }
 
 // ------------------------------------------------------------------ block attention
@@ -1139,6 +1183,12 @@ struct VerifyState {
   uint8_t* qx = nullptr;        // head_dim 128: attention query operand [nkv][32 KB]
   size_t part_records = 0;
   int max_clusters[9] = {};     // co-resident GEMM clusters of n CTAs (index n)
+  // the QKV GEMMs' k-split partial sums through global memory (no cluster): tagged
+  // entries [CTA][16 tokens][128 rows], and one launch counter for the block's QKV GEMM
+  // and one for the context rows' (different grids)
+  unsigned long long* gpart = nullptr;
+  unsigned long long* gctr = nullptr;  // [2]
+  size_t gpart_entries = 0;
 };
 
 static char g_verify_error[256];
@@ -1170,6 +1220,11 @@ hfa_status verify_create(const hfa_layer_desc& d, int num_sms, VerifyState** out
     if (e == cudaSuccess) e = cudaMemset(v->qx, 0, (size_t)nkv * 32768);
   }
   if (e == cudaSuccess) e = cudaMalloc(&v->y_post, (size_t)16 * d.hidden * sizeof(float));
+  v->gpart_entries = (size_t)num_sms * 16 * kVM;  // at most one CTA per SM (cooperative)
+  if (e == cudaSuccess) e = cudaMalloc(&v->gpart, v->gpart_entries * 8);
+  if (e == cudaSuccess) e = cudaMemset(v->gpart, 0, v->gpart_entries * 8);
+  if (e == cudaSuccess) e = cudaMalloc(&v->gctr, 2 * 8);
+  if (e == cudaSuccess) e = cudaMemset(v->gctr, 0, 2 * 8);
   if (e != cudaSuccess) {
     snprintf(g_verify_error, sizeof g_verify_error, "%s", cudaGetErrorString(e));
     verify_free(v);
@@ -1211,12 +1266,21 @@ void verify_free(VerifyState* v) {
   cudaFree(v->bq);
   cudaFree(v->bo);
   cudaFree(v->qx);
+  cudaFree(v->gpart);
+  cudaFree(v->gctr);
   delete v;
 }
 
+hfa_status verify_reset(VerifyState* v, cudaStream_t s) {
+  if (!v || !v->gpart) return HFA_OK;
+  cudaError_t e = cudaMemsetAsync(v->gpart, 0, v->gpart_entries * 8, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(v->gctr, 0, 2 * 8, s);
+  return e == cudaSuccess ? HFA_OK : HFA_ECUDA;
+}
+
 template <typename Kern, typename... Args>
-static cudaError_t launch_ex2(Kern kern, dim3 grid, int threads, size_t smem, bool pdl,
-                              cudaStream_t s, int cluster, Args... args) {
+static cudaError_t launch_ex3(Kern kern, dim3 grid, int threads, size_t smem, bool pdl,
+                              cudaStream_t s, int cluster, bool coop, Args... args) {
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -1225,8 +1289,12 @@ static cudaError_t launch_ex2(Kern kern, dim3 grid, int threads, size_t smem, bo
   cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   int na = 0;
+  if (coop) {
+    attr[na].id = cudaLaunchAttributeCooperative;
+    attr[na++].val.cooperative = 1;
+  }
   if (pdl) {
     attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[na++].val.programmaticStreamSerializationAllowed = 1;
@@ -1240,6 +1308,12 @@ static cudaError_t launch_ex2(Kern kern, dim3 grid, int threads, size_t smem, bo
   cfg.attrs = attr;
   cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+template <typename Kern, typename... Args>
+static cudaError_t launch_ex2(Kern kern, dim3 grid, int threads, size_t smem, bool pdl,
+                              cudaStream_t s, int cluster, Args... args) {
+  return launch_ex3(kern, grid, threads, smem, pdl, s, cluster, false, args...);
 }
 
 template <typename Kern, typename... Args>
@@ -1258,6 +1332,15 @@ static int gemm_splits(int tiles, int chunks, int num_sms, int tpc, const int* m
   while (S > 1 && tiles / tpc > max_clusters[S * tpc]) --S;
   if (S < 1) S = 1;
   return S;
+}
+
+// k-splits per row tile when the splits add through global memory: the SMs shared out over
+// the tiles (one CTA per SM, all resident: a cooperative launch), at most 8
+static int gemm_splits_flat(int tiles, int chunks, int num_sms, int tpc) {
+  int S = num_sms / tiles;
+  if (S > 8 / tpc) S = 8 / tpc;
+  if (S > chunks) S = chunks;
+  return S < 1 ? 1 : S;
 }
 
 hfa_status verify_ctx_append(VerifyState* v, const VerifyCall& c, char* msg, int n) {
@@ -1314,10 +1397,16 @@ hfa_status verify_ctx_append(VerifyState* v, const VerifyCall& c, char* msg, int
   qa.tpc = hd > kVM ? hd / kVM : 1;
   qa.tile_base = (nh * hd / kVM) / qa.tpc * qa.tpc;  // aligned to the clusters of a head
   const int ktiles = rows_qkv / kVM - qa.tile_base;
-  qa.splits = gemm_splits(ktiles, qa.chunks, c.num_sms, qa.tpc, v->max_clusters);
+  // the k-splits add through global memory when every row tile can have a CTA resident,
+  // else through clusters
+  const bool flat = ktiles <= c.num_sms;
+  qa.splits = flat ? gemm_splits_flat(ktiles, qa.chunks, c.num_sms, qa.tpc)
+                   : gemm_splits(ktiles, qa.chunks, c.num_sms, qa.tpc, v->max_clusters);
+  qa.gpart = flat ? v->gpart : nullptr;
+  qa.gctr = v->gctr + 1;
   tb("ctx_kv_gemm");
-  e = launch_ex2(verify_gemm_kernel<kModeQKV>, dim3(ktiles * qa.splits), 128, kVGemmSmem, pdl, s,
-                 qa.splits * qa.tpc, qa);
+  e = launch_ex3(verify_gemm_kernel<kModeQKV>, dim3(ktiles * qa.splits), 128, kVGemmSmem, pdl, s,
+                 flat ? 1 : qa.splits * qa.tpc, flat, qa);
   te();
   if (e != cudaSuccess) {
     snprintf(msg, n, "context K/V launch: %s", cudaGetErrorString(e));
@@ -1396,10 +1485,14 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   qa.chunks = H / kVK;
   const int qtiles = rows_qkv / kVM;
   qa.tpc = hd > kVM ? hd / kVM : 1;
-  qa.splits = gemm_splits(qtiles, qa.chunks, c.num_sms, qa.tpc, v->max_clusters);
+  const bool flat = qtiles <= c.num_sms;  // as for the context rows
+  qa.splits = flat ? gemm_splits_flat(qtiles, qa.chunks, c.num_sms, qa.tpc)
+                   : gemm_splits(qtiles, qa.chunks, c.num_sms, qa.tpc, v->max_clusters);
+  qa.gpart = flat ? v->gpart : nullptr;
+  qa.gctr = v->gctr;
   tb("verify_qkv_gemm");
-  e = launch_ex2(verify_gemm_kernel<kModeQKV>, dim3(qtiles * qa.splits), 128, kVGemmSmem, pdl, s,
-                 qa.splits * qa.tpc, qa);
+  e = launch_ex3(verify_gemm_kernel<kModeQKV>, dim3(qtiles * qa.splits), 128, kVGemmSmem, pdl, s,
+                 flat ? 1 : qa.splits * qa.tpc, flat, qa);
   te();
   if (e != cudaSuccess) {
     snprintf(msg, n, "verify QKV launch: %s", cudaGetErrorString(e));

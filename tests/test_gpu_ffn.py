@@ -79,6 +79,18 @@ def test_small_shapes(orc, H, I, B):
     ffn.hfa_ffn_destroy()
 
 
+@pytest.mark.parametrize("H,I,B,max_batch", [(352, 480, 1, 1), (352, 480, 1, 8), (96, 160, 3, 3),
+                                             (32, 32, 1, 1), (1056, 2880, 16, 16)])
+def test_odd_block_counts_and_tiny_shapes(orc, H, I, B, max_batch):
+    # block counts with odd factors (11, 15, 3, 1 blocks of 32), fewer outputs than CTAs,
+    # and a batch below the planned batch tiles
+    f = wl.FFN_B1.replace(name="ffn_odd", hidden=H, intermediate=I, batch=B, seed=94 + H)
+    ffn, weights = _make(f, max_batch=max_batch)
+    h = wl.make_ffn_input(f)
+    _check(f, _run(ffn, f, h), orc.ffn_step(f, weights, h), f"H={H} I={I} B={B}/{max_batch}")
+    ffn.hfa_ffn_destroy()
+
+
 def test_per_channel_scalar_and_batch_below_max(orc):
     f = wl.FFN_B1.replace(name="ffn_v", hidden=512, intermediate=1536, batch=6, seed=88,
                           scalar_per_channel=True)
