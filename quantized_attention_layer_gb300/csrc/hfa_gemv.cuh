@@ -43,6 +43,11 @@ __device__ __forceinline__ unsigned long long ld_tagged(const unsigned long long
   asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
   return w;
 }
+// two adjacent entries (p 16-byte aligned), each read as one 64-bit relaxed access
+__device__ __forceinline__ void ld_tagged2(const unsigned long long* p, unsigned long long& w0,
+                                           unsigned long long& w1) {
+  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(w0), "=l"(w1) : "l"(p) : "memory");
+}
 __device__ __forceinline__ float tagged_value(unsigned long long w) {
   return __uint_as_float((uint32_t)w);
 }

@@ -163,48 +163,50 @@ __device__ __forceinline__ void warp_row_max(unsigned* s_max, int b, unsigned m,
 // pass scales each batch row by the power of two of its largest |value| and splits it
 // into fp16 hi + lo.  The words of batch columns past B are left as they are: the MMA
 // keeps columns apart, and the sums of those columns are never read.  s_inv gets the
-// scales' inverse.
+// scales' inverse.  The (row, pair) items are independent: one flat loop over all of them.
 template <int NT>
 __device__ void finish_operand(uint32_t* op, const unsigned* s_max, float* s_inv, int B,
                                int pairs) {
   constexpr int C = Cfg<NT>::kConsumers;
-  const int tid = threadIdx.x;
-  for (int b = 0; b < B; ++b) {
+  const int tid = threadIdx.x, total = B * pairs;
+#pragma unroll 4
+  for (int e = tid; e < total; e += C) {
+    const int b = e / pairs, p = e - b * pairs;
     const float sc = exp2i(scale_exp(s_max[b]));
-    for (int p = tid; p < pairs; p += C) {
-      const int wd = operand_word<NT>(2 * p, b);
-      __half h0, l0, h1, l1;
-      split_f16(__uint_as_float(op[wd]) * sc, h0, l0);
-      split_f16(__uint_as_float(op[wd + 16]) * sc, h1, l1);
-      op[wd] = pack_h2(h0, h1);
-      op[wd + 16] = pack_h2(l0, l1);
-    }
+    const int wd = operand_word<NT>(2 * p, b);
+    __half h0, l0, h1, l1;
+    split_f16(__uint_as_float(op[wd]) * sc, h0, l0);
+    split_f16(__uint_as_float(op[wd + 16]) * sc, h1, l1);
+    op[wd] = pack_h2(h0, h1);
+    op[wd + 16] = pack_h2(l0, l1);
   }
   if (tid < B) s_inv[tid] = exp2i(-scale_exp(s_max[tid]));
   consumer_sync<NT>();
 }
 
 // Phase-1 operand of k-split s: v = h (.) w_pre over the split's columns.  With `signal`,
-// the consumers release the producer (barrier 2) once their first activations are in.
+// the consumers release the producer (barrier 2) once all their activations are in: loads
+// issued behind the ring's bulk copies wait for them, so none is left for after the release.
 template <int NT>
 __device__ void build_op1(const FfnArgs& a, int s, uint32_t* op, unsigned* s_max, float* s_inv,
                           bool signal) {
   constexpr int C = Cfg<NT>::kConsumers;
+  constexpr int L = NT == 4 ? 12 : 4;  // pairs per thread and round (the 16-row operand in one)
   const int tid = threadIdx.x, lane = tid & 31;
   const int ncols = a.p1.nbs * 32, c0 = s * ncols, pairs = ncols / 2, total = a.B * pairs;
   if (tid < kMaxBatch) s_max[tid] = 0u;
   consumer_sync<NT>();
-  for (int base = 0; base < total; base += 4 * C) {
-    float2 hv[4], wv[4];
+  for (int base = 0; base < total; base += L * C) {
+    float2 hv[L], wv[L];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {  // every load of the round first
+    for (int k = 0; k < L; ++k) {  // every load of the round first
       const int e = base + k * C + tid, ee = e < total ? e : total - 1;
       const int b = ee / pairs, col = c0 + 2 * (ee - b * pairs);
       hv[k] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(a.h + (size_t)b * a.H + col));
       wv[k] = __ldg(reinterpret_cast<const float2*>(a.w_pre + col));
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < L; ++k) {
       const int e = base + k * C + tid, ee = e < total ? e : total - 1;
       const int b = ee / pairs, cc = 2 * (ee - b * pairs);
       const float v0 = hv[k].x * wv[k].x, v1 = hv[k].y * wv[k].y;
@@ -215,23 +217,25 @@ __device__ void build_op1(const FfnArgs& a, int s, uint32_t* op, unsigned* s_max
       }
       warp_row_max(s_max, b, e < total ? __float_as_uint(fmaxf(fabsf(v0), fabsf(v1))) : 0u, lane);
     }
-    if (signal && base == 0)  // the values are used: their loads have completed
-      asm volatile("bar.arrive 2, %0;" ::"n"(Cfg<NT>::kThreads) : "memory");
   }
+  if (signal)  // the values are used: their loads have completed
+    asm volatile("bar.arrive 2, %0;" ::"n"(Cfg<NT>::kThreads) : "memory");
   consumer_sync<NT>();
   finish_operand<NT>(op, s_max, s_inv, a.B, pairs);
 }
 
 // Phase-2 operand of k-split s: for each column x of the split, g and u = the phase-1
 // partial sums added in k-split order, times 1/rms(h); a = gelu(g) u (written to the tap
-// by the one CTA that loads the split's first stage).  Each thread polls two columns
-// pairs at once, every load of a round issued before the first tag is checked.
+// by the one CTA that loads the split's first stage).  Each thread polls two column pairs
+// in PS k-splits at once (16-byte loads of g and u pairs), every load of a round issued
+// before the first tag is checked: the rounds are L2 round trips one after another.
 template <int NT>
 __device__ void build_op2(const FfnArgs& a, int s, uint32_t* op, unsigned* s_max, float* s_inv,
                           const float* s_hinv, bool tap, uint32_t tag, volatile int* abort) {
   constexpr int C = Cfg<NT>::kConsumers;
   const int tid = threadIdx.x, lane = tid & 31;
   const int ncols = a.p2.nbs * 32, c0 = s * ncols, pairs = ncols / 2, total = a.B * pairs;
+  constexpr int PS = NT == 4 ? 4 : 2;
   const size_t sstride = (size_t)a.B * 2 * a.I;
   if (tid < kMaxBatch) s_max[tid] = 0u;
   consumer_sync<NT>();
@@ -246,26 +250,25 @@ __device__ void build_op2(const FfnArgs& a, int s, uint32_t* op, unsigned* s_max
       cc[k] = 2 * (ee - bb[k] * pairs);
       src[k] = a.part1 + (size_t)bb[k] * 2 * a.I + c0 + cc[k];
     }
-    for (int s0 = 0; s0 < a.p1.S; s0 += 2) {
-      unsigned long long w[2][2][4];
+    for (int s0 = 0; s0 < a.p1.S; s0 += PS) {
+      unsigned long long w[2][PS][4];
       const uint64_t t0 = globaltimer_ns();
       for (;;) {
         bool ready = true;
 #pragma unroll
         for (int k = 0; k < 2; ++k)
 #pragma unroll
-          for (int i = 0; i < 2; ++i) {
+          for (int i = 0; i < PS; ++i) {
+            // entries b * 2I + c0 + cc (+ I) of a split: even indices, 16-byte aligned
             const int sx = s0 + i < a.p1.S ? s0 + i : a.p1.S - 1;
             const unsigned long long* p = src[k] + sx * sstride;
-            w[k][i][0] = ld_tagged(p);
-            w[k][i][1] = ld_tagged(p + 1);
-            w[k][i][2] = ld_tagged(p + a.I);
-            w[k][i][3] = ld_tagged(p + a.I + 1);
+            ld_tagged2(p, w[k][i][0], w[k][i][1]);
+            ld_tagged2(p + a.I, w[k][i][2], w[k][i][3]);
           }
 #pragma unroll
         for (int k = 0; k < 2; ++k)
 #pragma unroll
-          for (int i = 0; i < 2; ++i)
+          for (int i = 0; i < PS; ++i)
 #pragma unroll
             for (int m = 0; m < 4; ++m) ready = ready && (uint32_t)(w[k][i][m] >> 32) == tag;
         if (ready || poll_expired(t0, a.err, abort)) break;
@@ -274,7 +277,7 @@ __device__ void build_op2(const FfnArgs& a, int s, uint32_t* op, unsigned* s_max
 #pragma unroll
       for (int k = 0; k < 2; ++k)
 #pragma unroll
-        for (int i = 0; i < 2; ++i)
+        for (int i = 0; i < PS; ++i)
           if (s0 + i < a.p1.S) {
             g[k][0] += tagged_value(w[k][i][0]);
             g[k][1] += tagged_value(w[k][i][1]);
@@ -505,23 +508,26 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1) ffn_kernel(const __grid_
   float ps0 = 0.f, ps1 = 0.f;
   for (int e = e0 + tid; e < e1; e += kConsumers) {
     float d = 0.f;
-    for (int s0 = 0; s0 < a.p2.S; s0 += 8) {
-      unsigned long long w[8];
+    // the k-splits' entries polled P3 at a time (more with four batch tiles, whose plans
+    // have more splits and whose threads have the registers)
+    constexpr int P3 = NT == 4 ? 24 : 8;
+    for (int s0 = 0; s0 < a.p2.S; s0 += P3) {
+      unsigned long long w[P3];
       const uint64_t t0 = globaltimer_ns();
       for (;;) {
         bool ready = true;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < P3; ++k) {
           const int sx = s0 + k < a.p2.S ? s0 + k : a.p2.S - 1;
           w[k] = ld_tagged(a.part2 + sx * s2stride + e);
         }
 #pragma unroll
-        for (int k = 0; k < 8; ++k) ready = ready && (uint32_t)(w[k] >> 32) == tag;
+        for (int k = 0; k < P3; ++k) ready = ready && (uint32_t)(w[k] >> 32) == tag;
         if (ready || poll_expired(t0, a.err, s_abort)) break;
         __nanosleep(32);
       }
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
+      for (int k = 0; k < P3; ++k)
         if (s0 + k < a.p2.S) d += tagged_value(w[k]);
     }
     red[e - e0] = d;
