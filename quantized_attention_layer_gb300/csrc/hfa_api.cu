@@ -163,6 +163,24 @@ hfa_status hfa_encode_kv_map(CUtensorMap* map, void* base, int rows, int hd, int
   return r == CUDA_SUCCESS ? HFA_OK : HFA_EINVAL;
 }
 
+hfa_status hfa_encode_u8_map(CUtensorMap* map, const void* base, long long rows, int row_bytes,
+                             int box_bytes, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return HFA_EDEVICE;
+  if (box_bytes != 32 && box_bytes != 64 && box_bytes != 128) return HFA_EINVAL;
+  cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)box_bytes, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapSwizzle sw = box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : box_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                  : CU_TENSOR_MAP_SWIZZLE_32B;
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? HFA_OK : HFA_EINVAL;
+}
+
 // ------------------------------------------------------------------ timing
 static void timer_begin(hfa_layer* L, cudaStream_t s, const char* name, KernelTimer* t) {
   t->name = name;

@@ -190,9 +190,45 @@ int ffn_max_outputs_per_cta();  // B * H / grid must not exceed it
 
 cudaError_t launch_attn(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                         int grid, bool pdl, cudaStream_t s);
+
+// flash-decode over the quantised KV cache (k_tq.cu, k_tq_mma.cu)
+struct TqAttnArgs {
+  const float* q;         // [B, nh, hd] after norm and RoPE
+  const int* seq_pos;     // [B]
+  const uint8_t* k_codes;  // [B, nkv, C, code_bytes], or NULL (hybrid: raw bf16 keys)
+  const float* k_norms;   // [B, nkv, C, blocks]
+  const __nv_bfloat16* k_raw;  // hybrid: [B, nkv, C, hd]
+  const uint8_t* v_codes;
+  const float* v_norms;
+  const float* centroids;  // [levels]
+  const float* signs;      // [hd]
+  float* part;             // [units * splits][8][hd + 4]: O (rotated), m, l
+  int* ticket;             // [units]
+  float* o;                // [B, nh, hd]
+  unsigned* err;
+  int B, nh, nkv, C, sliding, window, ring, levels;
+  int splits, chunk;       // key chunks per unit, keys per chunk
+  float qscale;            // scale * log2 e, or scale / softcap
+  float cap_log2;          // softcap * log2 e, 0 = none
+};
+// the tensor-core kernel: head dims 64, 128 and 256, codes of 4 or 8 stored bits, K coded
+// or raw bf16 (kraw); tk / tv describe the K and V arrays (tq_mma_encode_maps); one CTA of
+// tq_mma_threads(hd) per SM, chunks of any length
+bool tq_mma_supported(int hd, int sbits);
+int tq_mma_keys_per_stage(int hd);
+int tq_mma_threads(int hd);
+cudaError_t launch_tq_attn_mma(const TqAttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                               int hd, int sbits, bool kraw, int grid, cudaStream_t s);
 int attn_keys_per_stage(int hd);
 size_t attn_smem_bytes(int hd);
 int attn_threads(int hd);
 int attn_record_floats(int hd);  // floats of one chunk record (8 heads x (hd + 4))
 
 }  // namespace hfa
+
+// 2-D views of a cache for the TMA unit (hfa_api.cu): bf16 [rows, hd] in boxes of 64 x
+// box_rows with 128-byte swizzle; bytes [rows, row_bytes] in boxes of box_bytes x box_rows
+// (box_bytes 32, 64 or 128, the swizzle of the same width)
+hfa_status hfa_encode_kv_map(CUtensorMap* map, void* base, int rows, int hd, int box_rows);
+hfa_status hfa_encode_u8_map(CUtensorMap* map, const void* base, long long rows, int row_bytes,
+                             int box_bytes, int box_rows);

@@ -1,0 +1,110 @@
+// hfa_tq.cuh -- pieces shared by the two flash-decode kernels over the quantised
+// (TurboQuant) KV cache (k_tq.cu: CUDA cores, every head dim; k_tq_mma.cu: tensor cores):
+// the normalised FWHT of rows in shared memory, and the last CTA's merge of the chunk
+// records followed by the inverse rotation.
+//
+// gemma4/gpu_full_attn.rs, encode_one_layer: the query is rotated like the keys (sign
+// pre-multiply, normalised FWHT per 256-dim block), scores and the weighted sum of V are
+// taken in the rotated domain, and the output is rotated back (fwht_sign_undo).
+#pragma once
+
+#include "hfa_common.cuh"
+
+namespace hfa {
+
+// Normalised FWHT (blocks of n <= 256 values) of `count` rows of `row_len` floats, `stride`
+// apart, by threads tid = 0 .. nthr-1 that all call it with the same arguments; the
+// butterflies in the order 1, 2, 4, ... (each a + b, a - b), then the 1/sqrt(n) scale.
+// `sync` is the barrier of those threads.
+template <typename Sync>
+__device__ __forceinline__ void tq_fwht_rows(float* v, int count, int stride, int n, int row_len,
+                                             int tid, int nthr, Sync sync) {
+  for (int h = 1; h < n; h <<= 1) {
+    const int pairs = count * (row_len / 2);
+    for (int p = tid; p < pairs; p += nthr) {
+      const int r = p / (row_len / 2), k = p - r * (row_len / 2);
+      // k-th pair of the row: block base + index with bit h clear
+      const int blk = k / (n / 2), kk = k - blk * (n / 2);
+      const int i = blk * n + (kk / h) * 2 * h + (kk % h);
+      float* x = v + r * stride;
+      const float a0 = x[i], a1 = x[i + h];
+      x[i] = a0 + a1;
+      x[i + h] = a0 - a1;
+    }
+    sync();
+  }
+  const float sc = rsqrtf((float)n);
+  for (int e = tid; e < count * row_len; e += nthr) {
+    const int r = e / row_len, i = e - r * row_len;
+    v[r * stride + i] *= sc;
+  }
+  sync();
+}
+
+// The last CTA of a (sequence, KV head): the chunk records at `up` ([splits][8][HD + 4]:
+// O in the rotated domain, then m and l in base-2 units) combined with the weights
+// 2^(m_s - M) / sum_s' 2^(m_s' - M) l_s', the chunks added in order, then rotated back
+// (the normalised FWHT is its own inverse; then the signs) into o ([G][HD]).  wsm holds
+// G x splits floats and s_o G x HD floats of shared memory; every thread of the CTA calls
+// it.
+template <int HD>
+__device__ void tq_merge_records(const float* up, int splits, int G, float* wsm, float* s_o,
+                                 const float* signs, float* o) {
+  constexpr int RS = HD + 4;
+  constexpr int BLK = HD < 256 ? HD : 256;
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int warp = tid >> 5, lane = tid & 31, nw = nthr >> 5;
+  for (int h = warp; h < G; h += nw) {
+    float M = -INFINITY;
+    for (int sp = lane; sp < splits; sp += 32) M = fmaxf(M, __ldcg(up + (sp * 8 + h) * RS + HD));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float Mu = M == -INFINITY ? 0.f : M;
+    float den = 0.f;
+    for (int sp = lane; sp < splits; sp += 32) {
+      const float f = exp2f(__ldcg(up + (sp * 8 + h) * RS + HD) - Mu);
+      wsm[h * splits + sp] = f;
+      den += f * __ldcg(up + (sp * 8 + h) * RS + HD + 1);
+    }
+    den = warp_sum(den);
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    __syncwarp();
+    for (int sp = lane; sp < splits; sp += 32) wsm[h * splits + sp] *= inv;
+  }
+  __syncthreads();
+  // o[h][i] = sum_s w[h][s] O_s[h][i]: one float4 column per thread, the chunks added in
+  // order, eight loads in flight at a time
+  constexpr int Q4 = HD / 4;
+  const int ncol = G * Q4;
+  for (int c = tid; c < ncol; c += nthr) {
+    const int h = c / Q4, d4 = c - h * Q4;
+    float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sp0 = 0; sp0 < splits; sp0 += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int sp = sp0 + u < splits ? sp0 + u : splits - 1;  // in range
+        v[u] = __ldcg(reinterpret_cast<const float4*>(up + (sp * 8 + h) * RS) + d4);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (sp0 + u < splits) {
+          const float w = wsm[h * splits + sp0 + u];
+          acc4.x = fmaf(w, v[u].x, acc4.x);
+          acc4.y = fmaf(w, v[u].y, acc4.y);
+          acc4.z = fmaf(w, v[u].z, acc4.z);
+          acc4.w = fmaf(w, v[u].w, acc4.w);
+        }
+      }
+    }
+    reinterpret_cast<float4*>(s_o)[c] = acc4;
+  }
+  __syncthreads();
+  tq_fwht_rows(s_o, G, HD, BLK, HD, tid, nthr, []() { __syncthreads(); });
+  for (int e = tid; e < G * HD; e += nthr) {
+    const int h = e / HD, i = e - h * HD;
+    o[h * HD + i] = s_o[h * HD + i] * signs[i];
+  }
+}
+
+}  // namespace hfa

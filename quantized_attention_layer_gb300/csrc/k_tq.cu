@@ -34,6 +34,7 @@
 
 #include "hfa_common.cuh"
 #include "hfa_internal.h"
+#include "hfa_tq.cuh"
 
 struct hfa_tq {
   int hd, bits, sbits, levels, blocks, code_bytes, device;  // sbits: bits stored per code
@@ -197,25 +198,7 @@ __global__ void __launch_bounds__(128) tq_append_kernel(const TqAppendArgs a) {
 }
 
 // ------------------------------------------------------------------ attention (device)
-struct TqAttnArgs {
-  const float* q;         // [B, nh, hd] after norm and RoPE
-  const int* seq_pos;     // [B]
-  const uint8_t* k_codes;  // [B, nkv, C, code_bytes], or NULL (hybrid: raw bf16 keys)
-  const float* k_norms;   // [B, nkv, C, blocks]
-  const __nv_bfloat16* k_raw;  // hybrid: [B, nkv, C, hd]
-  const uint8_t* v_codes;
-  const float* v_norms;
-  const float* centroids;  // [levels]
-  const float* signs;      // [hd]
-  float* part;             // [units * splits][8][hd + 4]: O (rotated), m, l
-  int* ticket;             // [units]
-  float* o;                // [B, nh, hd]
-  unsigned* err;
-  int B, nh, nkv, C, sliding, window, ring, levels;
-  int splits, chunk;       // key chunks per unit, keys per chunk (a multiple of 256)
-  float qscale;            // scale * log2 e, or scale / softcap
-  float cap_log2;          // softcap * log2 e, 0 = none
-};
+
 
 template <int HD>
 struct TqCfg {
@@ -226,32 +209,6 @@ struct TqCfg {
   static constexpr int TPR = HD / 4;
   static constexpr int NKS = kTqThreads / TPR;
 };
-
-// shared-memory normalised FWHT of n values (n <= 256) at v, all threads of the CTA
-// working on `count` independent rows of `stride` floats; butterflies in the order 1, 2,
-// 4, ... (each a + b, a - b), then the 1/sqrt(n) scale
-__device__ void smem_fwht_rows(float* v, int count, int stride, int n, int row_len) {
-  for (int h = 1; h < n; h <<= 1) {
-    const int pairs = count * (row_len / 2);
-    for (int p = threadIdx.x; p < pairs; p += blockDim.x) {
-      const int r = p / (row_len / 2), k = p - r * (row_len / 2);
-      // k-th pair of the row: block base + index with bit h clear
-      const int blk = k / (n / 2), kk = k - blk * (n / 2);
-      const int i = blk * n + (kk / h) * 2 * h + (kk % h);
-      float* x = v + r * stride;
-      const float a0 = x[i], a1 = x[i + h];
-      x[i] = a0 + a1;
-      x[i + h] = a0 - a1;
-    }
-    __syncthreads();
-  }
-  const float sc = rsqrtf((float)n);
-  for (int e = threadIdx.x; e < count * row_len; e += blockDim.x) {
-    const int r = e / row_len, i = e - r * row_len;
-    v[r * stride + i] *= sc;
-  }
-  __syncthreads();
-}
 
 // GM: the most query heads per KV head this instantiation handles (G rounded up to 2, 4, 8)
 template <int HD, int BITS, bool KRAW, int GM>
@@ -305,7 +262,8 @@ __global__ void __launch_bounds__(kTqThreads) tq_attn_kernel(const TqAttnArgs a)
     s_l[tid] = 0.f;
   }
   __syncthreads();
-  if (!KRAW) smem_fwht_rows(s_q, GM, HD, BLK, HD);  // the query in the keys' rotated domain
+  if (!KRAW)  // the query in the keys' rotated domain
+    tq_fwht_rows(s_q, GM, HD, BLK, HD, tid, kTqThreads, []() { __syncthreads(); });
 
   const int P = a.seq_pos[b];
   int lo, hi;
@@ -531,61 +489,7 @@ __global__ void __launch_bounds__(kTqThreads) tq_attn_kernel(const TqAttnArgs a)
   __threadfence();
   if (tid == 0) a.ticket[unit] = 0;
   const float* up = a.part + (size_t)unit * a.splits * 8 * RS;
-  // weight of chunk sp for head h: 2^(m_sp - M) / sum_sp' 2^(m_sp' - M) l_sp'
-  float* wsm = s_p;  // [G][splits]: kTqMaxG * kTqMaxSplits floats = the score area
-  for (int h = warp; h < G; h += kTqThreads / 32) {
-    float M = -INFINITY;
-    for (int sp = lane; sp < a.splits; sp += 32) M = fmaxf(M, __ldcg(up + (sp * 8 + h) * RS + HD));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    const float Mu = M == -INFINITY ? 0.f : M;
-    float den = 0.f;
-    for (int sp = lane; sp < a.splits; sp += 32) {
-      const float f = exp2f(__ldcg(up + (sp * 8 + h) * RS + HD) - Mu);
-      wsm[h * a.splits + sp] = f;
-      den += f * __ldcg(up + (sp * 8 + h) * RS + HD + 1);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-    __syncwarp();
-    for (int sp = lane; sp < a.splits; sp += 32) wsm[h * a.splits + sp] *= inv;
-  }
-  __syncthreads();
-  // o[h][i] = sum_sp w[h][sp] O_sp[h][i]: one float4 column per thread, the chunks added
-  // in order, eight loads in flight at a time
-  float* s_o = s_q;  // [G][HD]: the merged output, rotated
-  constexpr int Q4 = HD / 4;
-  const int ncol = G * Q4;
-  for (int c = tid; c < ncol; c += kTqThreads) {
-    const int h = c / Q4, d4 = c - h * Q4;
-    float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int sp0 = 0; sp0 < a.splits; sp0 += 8) {
-      float4 v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int sp = sp0 + u < a.splits ? sp0 + u : a.splits - 1;  // in range
-        v[u] = __ldcg(reinterpret_cast<const float4*>(up + (sp * 8 + h) * RS) + d4);
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (sp0 + u < a.splits) {
-          const float w = wsm[h * a.splits + sp0 + u];
-          acc4.x = fmaf(w, v[u].x, acc4.x);
-          acc4.y = fmaf(w, v[u].y, acc4.y);
-          acc4.z = fmaf(w, v[u].z, acc4.z);
-          acc4.w = fmaf(w, v[u].w, acc4.w);
-        }
-      }
-    }
-    reinterpret_cast<float4*>(s_o)[c] = acc4;
-  }
-  __syncthreads();
-  smem_fwht_rows(s_o, G, HD, BLK, HD);  // the normalised FWHT is its own inverse
-  for (int e = tid; e < G * HD; e += kTqThreads) {
-    const int h = e / HD, i = e - h * HD;
-    a.o[((size_t)b * a.nh + kvh * G + h) * HD + i] = s_o[h * HD + i] * a.signs[i];
-  }
+  tq_merge_records<HD>(up, a.splits, G, s_p, s_q, a.signs, a.o + ((size_t)b * a.nh + kvh * G) * HD);
 }
 
 template <int HD, int BITS>
@@ -755,6 +659,27 @@ int tq_splits(int units, int max_keys, int sms) {
   if (S < 1) S = 1;
   return S;
 }
+// the tensor-core kernel: one CTA per SM, chunks a multiple of its stage
+int tq_mma_splits(int units, int max_keys, int sms, int hd) {
+  int S = sms / units;
+  if (S > kTqMaxSplits) S = kTqMaxSplits;
+  const int T = tq_mma_keys_per_stage(hd);
+  const int tiles = (max_keys + T - 1) / T;
+  if (S > tiles) S = tiles;
+  if (S < 1) S = 1;
+  return S;
+}
+int tq_mma_chunk(int max_keys, int S, int hd) {
+  const int T = tq_mma_keys_per_stage(hd);
+  const int c = (max_keys + S - 1) / S;
+  return (c + T - 1) / T * T;
+}
+// either kernel's record count fits: the workspace does not depend on the code width
+int tq_ws_splits(int units, int max_keys, int sms, int hd) {
+  const int a = tq_splits(units, max_keys, sms);
+  const int b = hd <= 256 ? tq_mma_splits(units, max_keys, sms, hd) : 0;
+  return a > b ? a : b;
+}
 int visible(const hfa_attn_desc* d, int P) {
   const bool ring = d->flags & HFA_F_RING;
   if (ring) return (P < d->kv_capacity - 1 ? P : d->kv_capacity - 1) + 1;
@@ -774,7 +699,7 @@ extern "C" size_t hfa_attention_tq_workspace_bytes(const hfa_attn_desc* d, int b
   const int sms = sm_count();
   if (sms <= 0) return 0;
   const int units = batch * d->num_kv_heads;
-  const int S = tq_splits(units, max_keys, sms);
+  const int S = tq_ws_splits(units, max_keys, sms, d->head_dim);
   return tq_ws_head(units) + (size_t)units * S * 8 * (d->head_dim + 4) * sizeof(float);
 }
 
@@ -820,11 +745,21 @@ extern "C" hfa_status hfa_attention_decode_tq(const hfa_attn_desc* d, const hfa_
   if (sms <= 0) return tq_fail(HFA_EDEVICE, "no CUDA device");
   const int units = batch * nkv;
   if ((long long)units * d->kv_capacity >= (1ll << 40)) return tq_fail(HFA_EUNSUPPORTED, "cache too large");
-  const int S = tq_splits(units, max_keys, sms);
-  const size_t need = tq_ws_head(units) + (size_t)units * S * 8 * (hd + 4) * sizeof(float);
+  const size_t need = tq_ws_head(units) +
+                      (size_t)units * tq_ws_splits(units, max_keys, sms, hd) * 8 * (hd + 4) * sizeof(float);
   if (ws_bytes < need) return tq_fail(HFA_EINVAL, "workspace of %zu bytes, %zu needed", ws_bytes, need);
-  int chunk = (max_keys + S - 1) / S;
-  chunk = (chunk + kTqThreads - 1) / kTqThreads * kTqThreads;
+  // the tensor-core kernel for head dims up to 256 (TMA rows are 32-bit coordinates)
+  const bool mma = tq_mma_supported(hd, t->sbits) && (long long)units * d->kv_capacity < (1ll << 31);
+  int S, chunk;
+  if (mma) {
+    S = tq_mma_splits(units, max_keys, sms, hd);
+    chunk = tq_mma_chunk(max_keys, S, hd);
+    S = (max_keys + chunk - 1) / chunk;  // no chunk starts past the longest sequence
+  } else {
+    S = tq_splits(units, max_keys, sms);
+    chunk = (max_keys + S - 1) / S;
+    chunk = (chunk + kTqThreads - 1) / kTqThreads * kTqThreads;
+  }
   TqAttnArgs a{};
   a.q = q;
   a.seq_pos = pos_dev;
@@ -860,6 +795,19 @@ extern "C" hfa_status hfa_attention_decode_tq(const hfa_attn_desc* d, const hfa_
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e;
   const int grid = units * S;
+  if (mma) {
+    CUtensorMap tk, tv;
+    const long long rows = (long long)units * d->kv_capacity;
+    const int T = tq_mma_keys_per_stage(hd);
+    const int box = t->code_bytes < 128 ? t->code_bytes : 128;
+    const hfa_status mk = kraw ? hfa_encode_kv_map(&tk, const_cast<void*>(k_raw), (int)rows, hd, T)
+                               : hfa_encode_u8_map(&tk, k_codes, rows, t->code_bytes, box, T);
+    if (mk != HFA_OK || hfa_encode_u8_map(&tv, v_codes, rows, t->code_bytes, box, T) != HFA_OK)
+      return tq_fail(HFA_EINVAL, "cannot describe the code arrays to the TMA unit");
+    e = launch_tq_attn_mma(a, tk, tv, hd, t->sbits, kraw, grid, s);
+    if (e != cudaSuccess) return tq_fail(HFA_ECUDA, "attention launch: %s", cudaGetErrorString(e));
+    return HFA_OK;
+  }
   if (hd == 64) e = launch_attn_hd<64>(a, t->sbits, kraw, grid, s);
   else if (hd == 128) e = launch_attn_hd<128>(a, t->sbits, kraw, grid, s);
   else if (hd == 256) e = launch_attn_hd<256>(a, t->sbits, kraw, grid, s);

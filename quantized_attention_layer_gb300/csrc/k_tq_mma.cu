@@ -1,0 +1,519 @@
+// k_tq_mma.cu -- flash-decode over the quantised (TurboQuant) KV cache on the tensor cores:
+// head dims 64, 128 and 256 (one norm block per row), codes of 4 bits (two per byte) or
+// one byte per code, K coded or stored raw in bf16 (the hybrid layout).
+//
+// gemma4/gpu_full_attn.rs, encode_one_layer: the TQ attention (flash_attn_vec_tq,
+// flash_attn_vec_tq_hb, flash_attn_vec_hybrid): each score is the rotated query against
+// the key's centroids times the key's block norm, the output the softmax-weighted sum of
+// the value centroids times the value norms, both in the rotated domain; the output is
+// rotated back at the end.  This is the arithmetic of the CUDA-core kernel in k_tq.cu,
+// mapped onto mma.sync.
+//
+// GB300 design.  One CTA = (sequence, KV head, key chunk), one per SM.  A producer warp
+// streams stages of T keys: the K and V code tiles by 2-D TMA (byte rows, swizzled at the
+// box width, so the consumers' 32-bit reads of eight rows never share a bank) and the
+// norms by 4-byte cp.async (a chunk may start at any key), all completing on the stage's
+// mbarrier.  Consumer warps take 16 keys of each stage.  Centroids are decoded through a
+// table in shared memory (one copy per bank: entry c of lane l at word 32 c + l) holding
+// each centroid as bf16 hi + lo; two table words give a pair of MMA operand registers by
+// one byte permute each.  All query heads of the group share one m16n8k16 MMA: rows
+// 0..G-1 hold hi(q), rows 8..8+G-1 lo(q), against B = hi(c) and B = lo(c), so the scores
+// keep about 16 bits of both operands; P times the V norm is split the same way for
+// O += P V.  A 32-bit code read gives four (8-bit) or eight (4-bit) adjacent dims of one
+// key, and the MMA's k index (scores) and n index (O) walk the dims in that order: the
+// query fragments and the output columns follow the same permutation, so every code is
+// read once and nothing is transposed.
+#include "hfa_common.cuh"
+#include "hfa_internal.h"
+#include "hfa_tq.cuh"
+
+namespace hfa {
+namespace {
+
+constexpr int kTqmMaxStages = 4;
+constexpr int kTqmSmemBudget = 204800;  // stages + tables + query areas, bytes
+constexpr int kTqmMaxSplits = 256;      // the merge's weight table: 8 x 256 floats
+
+template <int HD, int SBITS, bool KRAW>
+struct TqmCfg {
+  static constexpr int NC = HD >= 256 ? 4 : 8;     // consumer warps, 16 keys each
+  static constexpr int T = NC * 16;                 // keys per stage
+  static constexpr int CB = HD * SBITS / 8;         // code bytes of a row
+  static constexpr int BOXW = CB < 128 ? CB : 128;  // bytes of a TMA box row
+  static constexpr int NBOX = CB / BOXW;
+  static constexpr int SWM = BOXW == 128 ? 7 : (BOXW == 64 ? 3 : 1);  // swizzled row bits
+  static constexpr int KTILE = KRAW ? T * HD * 2 : T * CB;
+  static constexpr int VTILE = T * CB;
+  static constexpr int NORM_OFF = KTILE + VTILE;  // f32 [T] K norms (coded K), [T] V norms
+  static constexpr int NNORM = KRAW ? 1 : 2;
+  static constexpr int STAGE = (KTILE + VTILE + NNORM * T * 4 + 1023) / 1024 * 1024;
+  static constexpr int LEV = 1 << SBITS;  // table entries
+  static constexpr int TAB = LEV * 32 * 4;
+  static constexpr int KS = HD / 16;  // k16 steps of S = Q K^T
+  static constexpr int NTO = HD / 8;  // n8 tiles of O
+  static constexpr int RS = HD + 4;   // record: O[HD], m, l, pad
+  static constexpr int QF = KS * 32 * 16;
+  static constexpr int SQ = 8 * HD * 4;  // the rotated queries (f32), later the merged O
+  static constexpr int FIXED = TAB + QF + SQ + 256;
+  static constexpr int NS0 = (kTqmSmemBudget - FIXED) / STAGE;
+  static constexpr int NS = NS0 < kTqmMaxStages ? NS0 : kTqmMaxStages;
+  static constexpr size_t SMEM = 1024 + (size_t)NS * STAGE + FIXED;
+  static constexpr int THREADS = (NC + 1) * 32;
+  static_assert(NS >= 2, "two stages at least");
+  static_assert(NC * 8 * RS * 4 <= NS * STAGE, "the warps' records fit in the stages");
+  static_assert(8 * kTqmMaxSplits * 4 <= NS * STAGE, "the merge weights fit in the stages");
+  static_assert(SMEM <= 232448, "shared memory per CTA");
+};
+
+// shared address of byte `byte` (a multiple of 4) of key row `row` in a code tile: boxes of
+// BOXW bytes x T rows one after another, each written by TMA with the swizzle of its width
+// (the 16-byte chunk index XOR the row bits above the 128-byte line)
+template <class Cfg>
+__device__ __forceinline__ uint32_t code_addr(uint32_t tile, int row, int byte) {
+  const int box = byte / Cfg::BOXW, bb = byte - box * Cfg::BOXW;
+  const uint32_t lin = (uint32_t)(row * Cfg::BOXW + bb);
+  return tile + (uint32_t)(box * (Cfg::T * Cfg::BOXW)) + (lin ^ (((lin >> 7) & Cfg::SWM) << 4));
+}
+
+// raw bf16 K tile (hybrid layout): boxes of 64 dims (128 B) x T rows, 128-byte swizzle
+template <class Cfg>
+__device__ __forceinline__ uint32_t raw_addr(uint32_t tile, int row, int chunk) {
+  const int box = chunk >> 3, c = chunk & 7;
+  return tile + (uint32_t)(box * (Cfg::T * 128) + row * 128 + ((c ^ (row & 7)) << 4));
+}
+
+// The dim that k index (2t + e) (hh = 0) or (2t + 8 + e) (hh = 1) of k16 step ks stands
+// for.  Coded K: the code word a lane reads holds adjacent dims (4 per 8-bit word, 8 per
+// 4-bit word); raw K: the natural order, as ldmatrix delivers it.
+template <int SBITS, bool KRAW>
+__device__ __forceinline__ int qdim(int ks, int t, int hh, int e) {
+  if (KRAW) return 16 * ks + 2 * t + 8 * hh + e;
+  if (SBITS == 8) return 16 * ks + 4 * t + 2 * hh + e;
+  return 32 * (ks >> 1) + 8 * t + 4 * (ks & 1) + 2 * hh + e;
+}
+
+// the table word (bf16 hi | lo << 16) of code c for this lane
+__device__ __forceinline__ uint32_t tab_ld(uint32_t tab_lane, uint32_t c) {
+  return lds32(tab_lane + (c << 7));
+}
+// operand registers of two adjacent k (or two keys) from their table words
+__device__ __forceinline__ uint32_t hi_pair(uint32_t e0, uint32_t e1) {
+  return __byte_perm(e0, e1, 0x5410);
+}
+__device__ __forceinline__ uint32_t lo_pair(uint32_t e0, uint32_t e1) {
+  return __byte_perm(e0, e1, 0x7632);
+}
+
+// S += [hi(q); lo(q)] (hi(c) + lo(c)) for one k16 step: codes c0, c1 at k = 2t, 2t + 1 (b0),
+// c2, c3 at k = 2t + 8, 2t + 9 (b1)
+__device__ __forceinline__ void score_step(float (&s)[4], const uint32_t (&A)[4], uint32_t tab,
+                                           uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3) {
+  const uint32_t e0 = tab_ld(tab, c0), e1 = tab_ld(tab, c1);
+  const uint32_t e2 = tab_ld(tab, c2), e3 = tab_ld(tab, c3);
+  mma_bf16(s, A, hi_pair(e0, e1), hi_pair(e2, e3));
+  mma_bf16(s, A, lo_pair(e0, e1), lo_pair(e2, e3));
+}
+
+// O_tile += [hi(p); lo(p)] (hi(v) + lo(v)): codes of keys 2t, 2t + 1 (b0) and 2t + 8, 2t + 9
+// (b1) at the lane's column
+__device__ __forceinline__ void pv_tile(float (&o)[4], const uint32_t (&PA)[4], uint32_t tab,
+                                        uint32_t cA, uint32_t cB, uint32_t cC, uint32_t cD) {
+  const uint32_t eA = tab_ld(tab, cA), eB = tab_ld(tab, cB);
+  const uint32_t eC = tab_ld(tab, cC), eD = tab_ld(tab, cD);
+  mma_bf16(o, PA, hi_pair(eA, eB), hi_pair(eC, eD));
+  mma_bf16(o, PA, lo_pair(eA, eB), lo_pair(eC, eD));
+}
+
+__device__ __forceinline__ void cp_async_4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+// the mbarrier gets this thread's arrival once its earlier cp.async copies have landed
+// (counted in the barrier's expected arrivals)
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+template <int NT>
+__device__ __forceinline__ void consumer_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+}
+
+template <int HD, int SBITS, bool KRAW>
+__global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
+    tq_attn_mma_kernel(const __grid_constant__ CUtensorMap tmk,
+                       const __grid_constant__ CUtensorMap tmv, const TqAttnArgs a) {
+  using Cfg = TqmCfg<HD, SBITS, KRAW>;
+  constexpr int NC = Cfg::NC, T = Cfg::T, NS = Cfg::NS, RS = Cfg::RS;
+  constexpr int NCT = NC * 32;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_align1024(smem_raw);
+  uint8_t* stages = smem;
+  uint32_t* s_tab = reinterpret_cast<uint32_t*>(smem + NS * Cfg::STAGE);
+  uint4* qf = reinterpret_cast<uint4*>(smem + NS * Cfg::STAGE + Cfg::TAB);
+  float* s_q = reinterpret_cast<float*>(smem + NS * Cfg::STAGE + Cfg::TAB + Cfg::QF);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * Cfg::STAGE + Cfg::TAB + Cfg::QF + Cfg::SQ);
+  uint64_t* empty = full + NS;
+  int* s_flags = reinterpret_cast<int*>(empty + NS);  // [0] abort, [1] issued, [2] last
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int G = a.nh / a.nkv;
+  const int unit = blockIdx.x / a.splits, split = blockIdx.x - unit * a.splits;
+  const int b = unit / a.nkv, kvh = unit - b * a.nkv;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&full[i], 1 + 32);  // the TMA issue + the producer lanes' norm copies
+      mbar_init(&empty[i], NC);
+    }
+    s_flags[0] = 0;
+    s_flags[1] = 0;
+    fence_barrier_init();
+  }
+  if (warp == NC && lane == 0) {
+    prefetch_tmap(&tmk);
+    prefetch_tmap(&tmv);
+  }
+  __syncthreads();
+
+  // visible slot range [lo, hi] of this sequence
+  const int P = a.seq_pos[b];
+  int lo, hi;
+  if (a.ring) {
+    lo = 0;
+    hi = P < a.C - 1 ? P : a.C - 1;
+  } else {
+    lo = a.sliding ? (P - a.window + 1 > 0 ? P - a.window + 1 : 0) : 0;
+    hi = P;
+  }
+  const bool bad = P < 0 || (!a.ring && P >= a.C);
+  if (bad && threadIdx.x == 0 && split == 0 && a.err) atomicOr(a.err, 2u);
+  const int k_begin = lo + split * a.chunk;
+  int k_end = k_begin + a.chunk;
+  if (k_end > hi + 1) k_end = hi + 1;
+  const int nkeys = bad ? 0 : (k_end > k_begin ? k_end - k_begin : 0);
+  const int ntiles = (nkeys + T - 1) / T;
+  const int row0 = unit * a.C + k_begin;  // TMA row of the chunk's first key
+
+  float* part = a.part + ((size_t)unit * a.splits + split) * 8 * RS;
+
+  if (warp == NC) {
+    // ------------------------------------------------------------- producer
+    int issued = 0;
+    for (int i = 0; i < ntiles; ++i) {
+      const int st = i % NS;
+      if (i >= NS && !mbar_wait(&empty[st], ((i / NS) - 1) & 1, a.err, &s_flags[0])) {
+        atomicExch(&s_flags[0], 1);
+        break;
+      }
+      if (*(volatile int*)&s_flags[0]) break;
+      uint8_t* sb = stages + st * Cfg::STAGE;
+      const int y = row0 + i * T;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&full[st], Cfg::KTILE + Cfg::VTILE);
+        if (KRAW) {
+#pragma unroll
+          for (int j = 0; j < HD / 64; ++j) tma_load_2d(sb + j * T * 128, &tmk, &full[st], 64 * j, y);
+        } else {
+#pragma unroll
+          for (int j = 0; j < Cfg::NBOX; ++j)
+            tma_load_2d(sb + j * T * Cfg::BOXW, &tmk, &full[st], j * Cfg::BOXW, y);
+        }
+#pragma unroll
+        for (int j = 0; j < Cfg::NBOX; ++j)
+          tma_load_2d(sb + Cfg::KTILE + j * T * Cfg::BOXW, &tmv, &full[st], j * Cfg::BOXW, y);
+      }
+      // the norms of the stage's keys (past the chunk: its last key, never used)
+      float* nd = reinterpret_cast<float*>(sb + Cfg::NORM_OFF);
+      const int kb0 = k_begin + i * T;
+      for (int j = lane; j < T; j += 32) {
+        const int key = kb0 + j < k_end ? kb0 + j : k_end - 1;
+        const size_t r = (size_t)unit * a.C + key;
+        if (!KRAW) cp_async_4(nd + j, a.k_norms + r);
+        cp_async_4(nd + (KRAW ? 0 : T) + j, a.v_norms + r);
+      }
+      cp_async_arrive_noinc(&full[st]);
+      issued = i + 1;
+    }
+    if (lane == 0) s_flags[1] = issued;
+  } else {
+    // ------------------------------------------------------------- consumers
+    const int ctid = threadIdx.x;
+    auto csync = []() { consumer_bar<NCT>(); };
+    for (int i = ctid; i < Cfg::LEV * 32; i += NCT) {
+      const int c = i >> 5;
+      const float f = c < a.levels ? __ldg(a.centroids + c) : 0.f;
+      __nv_bfloat16 h, l;
+      split_bf16(f, h, l);
+      s_tab[i] = pack_bf2(h, l);
+    }
+    for (int e = ctid; e < 8 * HD; e += NCT) {
+      const int h = e / HD, i = e - h * HD;
+      const float qv = h < G ? a.q[((size_t)b * a.nh + kvh * G + h) * HD + i] * a.qscale : 0.f;
+      s_q[e] = KRAW ? qv : qv * __ldg(a.signs + i);
+    }
+    csync();
+    if (!KRAW) tq_fwht_rows(s_q, G, HD, HD, HD, ctid, NCT, csync);  // the keys' rotated domain
+    // query fragments: A rows 0..G-1 = hi(q), rows 8..8+G-1 = lo(q), k in the codes' order
+    for (int ks = warp; ks < Cfg::KS; ks += NC) {
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
+      if (g < G) {
+        __nv_bfloat16 h[4], l[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          split_bf16(s_q[g * HD + qdim<SBITS, KRAW>(ks, t, k >> 1, k & 1)], h[k], l[k]);
+        w[0] = pack_bf2(h[0], h[1]);
+        w[1] = pack_bf2(l[0], l[1]);
+        w[2] = pack_bf2(h[2], h[3]);
+        w[3] = pack_bf2(l[2], l[3]);
+      }
+      qf[ks * 32 + lane] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    csync();
+
+    float m = -INFINITY, l = 0.f;
+    float o[Cfg::NTO][4];
+#pragma unroll
+    for (int i = 0; i < Cfg::NTO; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    const uint32_t tab = smem_u32(s_tab) + lane * 4;
+    const uint32_t stage_base = smem_u32(stages);
+    const int krow = warp * 16;
+
+    for (int i = 0; i < ntiles; ++i) {
+      const int st = i % NS;
+      if (*(volatile int*)&s_flags[0]) break;
+      if (!mbar_wait(&full[st], (i / NS) & 1, a.err, &s_flags[0])) {
+        atomicExch(&s_flags[0], 1);
+        break;
+      }
+      const uint32_t kb = stage_base + st * Cfg::STAGE;
+      const uint32_t vb = kb + Cfg::KTILE;
+      const float* nrm = reinterpret_cast<const float*>(stages + st * Cfg::STAGE + Cfg::NORM_OFF);
+
+      // S = Q K^T for 16 keys: n8 tiles of keys krow + g (s0) and krow + 8 + g (s1)
+      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+      if constexpr (KRAW) {
+#pragma unroll
+        for (int ks = 0; ks < Cfg::KS; ++ks) {
+          const uint4 qa = qf[ks * 32 + lane];
+          const uint32_t A[4] = {qa.x, qa.y, qa.z, qa.w};
+          const int mrow = krow + ((lane >> 4) << 3) + (lane & 7);
+          const int mchunk = ks * 2 + ((lane >> 3) & 1);
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4(raw_addr<Cfg>(kb, mrow, mchunk), b0, b1, b2, b3);
+          mma_bf16(s0, A, b0, b1);
+          mma_bf16(s1, A, b2, b3);
+        }
+      } else if constexpr (SBITS == 8) {
+#pragma unroll
+        for (int ks = 0; ks < Cfg::KS; ++ks) {
+          const uint32_t w0 = lds32(code_addr<Cfg>(kb, krow + g, 16 * ks + 4 * t));
+          const uint32_t w1 = lds32(code_addr<Cfg>(kb, krow + 8 + g, 16 * ks + 4 * t));
+          const uint4 qa = qf[ks * 32 + lane];
+          const uint32_t A[4] = {qa.x, qa.y, qa.z, qa.w};
+          score_step(s0, A, tab, w0 & 255u, (w0 >> 8) & 255u, (w0 >> 16) & 255u, w0 >> 24);
+          score_step(s1, A, tab, w1 & 255u, (w1 >> 8) & 255u, (w1 >> 16) & 255u, w1 >> 24);
+        }
+      } else {
+#pragma unroll
+        for (int mw = 0; mw < HD / 32; ++mw) {
+          const uint32_t w0 = lds32(code_addr<Cfg>(kb, krow + g, 16 * mw + 4 * t));
+          const uint32_t w1 = lds32(code_addr<Cfg>(kb, krow + 8 + g, 16 * mw + 4 * t));
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const uint4 qa = qf[(2 * mw + half) * 32 + lane];
+            const uint32_t A[4] = {qa.x, qa.y, qa.z, qa.w};
+            const uint32_t x0 = w0 >> (16 * half), x1 = w1 >> (16 * half);
+            score_step(s0, A, tab, x0 & 15u, (x0 >> 4) & 15u, (x0 >> 8) & 15u, (x0 >> 12) & 15u);
+            score_step(s1, A, tab, x1 & 15u, (x1 >> 4) & 15u, (x1 >> 8) & 15u, (x1 >> 12) & 15u);
+          }
+        }
+      }
+      // logits of head g for local keys krow + {2t, 2t+1, 8+2t, 9+2t} (hi row + lo row),
+      // times the keys' norms
+      float sv[4] = {s0[0] + s0[2], s0[1] + s0[3], s1[0] + s1[2], s1[1] + s1[3]};
+      const int kl0 = krow + 2 * t;
+      const int kidx0 = k_begin + i * T + kl0;
+      bool valid[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int dk = (e & 1) + ((e >> 1) << 3);
+        float s = sv[e];
+        if (!KRAW) s *= nrm[kl0 + dk];
+        if (a.cap_log2 != 0.f) s = a.cap_log2 * tanhf(s);
+        valid[e] = kidx0 + dk < k_end;
+        sv[e] = valid[e] ? s : -INFINITY;
+      }
+      float mloc = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+      mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
+      mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
+      const float m_new = fmaxf(m, mloc);
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
+      const float corr = exp2f(m - m_use);
+      float p[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) p[e] = exp2f(sv[e] - m_use);
+      l = l * corr + (p[0] + p[1]) + (p[2] + p[3]);
+      m = m_new;
+#pragma unroll
+      for (int nt = 0; nt < Cfg::NTO; ++nt) {
+        o[nt][0] *= corr;
+        o[nt][1] *= corr;
+        o[nt][2] *= corr;
+        o[nt][3] *= corr;
+      }
+      // P times the V norms as the A operand: row g = hi, row g + 8 = lo; k = the 16 keys
+      uint32_t PA[4];
+      {
+        __nv_bfloat16 h[4], lw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int dk = (e & 1) + ((e >> 1) << 3);
+          const float pv = valid[e] ? p[e] * nrm[(KRAW ? 0 : T) + kl0 + dk] : 0.f;
+          split_bf16(pv, h[e], lw[e]);
+        }
+        PA[0] = pack_bf2(h[0], h[1]);
+        PA[1] = pack_bf2(lw[0], lw[1]);
+        PA[2] = pack_bf2(h[2], h[3]);
+        PA[3] = pack_bf2(lw[2], lw[3]);
+      }
+      // O += P V: the lane reads keys 2t, 2t+1, 2t+8, 2t+9 at the 4 (8 for 4-bit) adjacent
+      // dims of its column; n8 tile j of a group holds the dims base + (4 or 8) col + j
+      if constexpr (SBITS == 8) {
+#pragma unroll
+        for (int grp = 0; grp < HD / 32; ++grp) {
+          const int byte = grp * 32 + 4 * g;
+          const uint32_t wA = lds32(code_addr<Cfg>(vb, krow + 2 * t, byte));
+          const uint32_t wB = lds32(code_addr<Cfg>(vb, krow + 2 * t + 1, byte));
+          const uint32_t wC = lds32(code_addr<Cfg>(vb, krow + 2 * t + 8, byte));
+          const uint32_t wD = lds32(code_addr<Cfg>(vb, krow + 2 * t + 9, byte));
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            pv_tile(o[grp * 4 + j], PA, tab, (wA >> (8 * j)) & 255u, (wB >> (8 * j)) & 255u,
+                    (wC >> (8 * j)) & 255u, (wD >> (8 * j)) & 255u);
+        }
+      } else {
+#pragma unroll
+        for (int grp = 0; grp < HD / 64; ++grp) {
+          const int byte = grp * 32 + 4 * g;
+          const uint32_t wA = lds32(code_addr<Cfg>(vb, krow + 2 * t, byte));
+          const uint32_t wB = lds32(code_addr<Cfg>(vb, krow + 2 * t + 1, byte));
+          const uint32_t wC = lds32(code_addr<Cfg>(vb, krow + 2 * t + 8, byte));
+          const uint32_t wD = lds32(code_addr<Cfg>(vb, krow + 2 * t + 9, byte));
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            pv_tile(o[grp * 8 + j], PA, tab, (wA >> (4 * j)) & 15u, (wB >> (4 * j)) & 15u,
+                    (wC >> (4 * j)) & 15u, (wD >> (4 * j)) & 15u);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+    }
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+
+    // ------------------------------------------------- merge the consumer warps
+    // every stage has been consumed (or the CTA aborted): reuse the stage buffers
+    csync();
+    float* red = reinterpret_cast<float*>(stages);  // [warp][8][RS]
+    float* mine = red + warp * 8 * RS;
+    if (g < G) {
+      if (t == 0) {
+        mine[g * RS + HD] = m;
+        mine[g * RS + HD + 1] = l;
+      }
+#pragma unroll
+      for (int nt = 0; nt < Cfg::NTO; ++nt) {
+        // columns 2t, 2t + 1 of tile nt: the dims of the permuted order
+        int d0, d1;
+        if (SBITS == 8) {
+          d0 = (nt >> 2) * 32 + 8 * t + (nt & 3);
+          d1 = d0 + 4;
+        } else {
+          d0 = (nt >> 3) * 64 + 16 * t + (nt & 7);
+          d1 = d0 + 8;
+        }
+        mine[g * RS + d0] = o[nt][0] + o[nt][2];
+        mine[g * RS + d1] = o[nt][1] + o[nt][3];
+      }
+    }
+    csync();
+    for (int e = ctid; e < G * (HD + 2); e += NCT) {
+      const int h = e / (HD + 2), d = e - h * (HD + 2);
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < NC; ++w) M = fmaxf(M, red[(w * 8 + h) * RS + HD]);
+      const float Mu = M == -INFINITY ? 0.f : M;
+      float acc = 0.f;
+      if (d == HD) {
+        acc = M;
+      } else {
+#pragma unroll
+        for (int w = 0; w < NC; ++w)
+          acc += exp2f(red[(w * 8 + h) * RS + HD] - Mu) * red[(w * 8 + h) * RS + d];
+      }
+      part[h * RS + d] = acc;
+    }
+  }
+
+  // drain: every copy this CTA issued has landed before it may exit or reuse the stages
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int issued = s_flags[1];
+    for (int st = 0; st < NS && st < issued; ++st) {
+      const int last = st + ((issued - 1 - st) / NS) * NS;
+      mbar_wait(&full[st], (last / NS) & 1, a.err);
+    }
+  }
+
+  // ------------------------------------------------- the last chunk merges the unit
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_flags[2] = atomicAdd(a.ticket + unit, 1) == a.splits - 1;
+  __syncthreads();
+  if (!s_flags[2]) return;
+  __threadfence();
+  if (threadIdx.x == 0) a.ticket[unit] = 0;
+  const float* up = a.part + (size_t)unit * a.splits * 8 * RS;
+  tq_merge_records<HD>(up, a.splits, G, reinterpret_cast<float*>(stages), s_q, a.signs,
+                       a.o + ((size_t)b * a.nh + kvh * G) * HD);
+}
+
+template <int HD, int SBITS, bool KRAW>
+cudaError_t launch_t(const TqAttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
+                     cudaStream_t s) {
+  using Cfg = TqmCfg<HD, SBITS, KRAW>;
+  auto kern = tq_attn_mma_kernel<HD, SBITS, KRAW>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)Cfg::SMEM);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, Cfg::THREADS, Cfg::SMEM, s>>>(tk, tv, a);
+  return cudaGetLastError();
+}
+
+template <int HD>
+cudaError_t launch_hd(const TqAttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                      int sbits, bool kraw, int grid, cudaStream_t s) {
+  if (sbits == 8)
+    return kraw ? launch_t<HD, 8, true>(a, tk, tv, grid, s) : launch_t<HD, 8, false>(a, tk, tv, grid, s);
+  return kraw ? launch_t<HD, 4, true>(a, tk, tv, grid, s) : launch_t<HD, 4, false>(a, tk, tv, grid, s);
+}
+
+}  // namespace
+
+bool tq_mma_supported(int hd, int sbits) {
+  return (hd == 64 || hd == 128 || hd == 256) && (sbits == 4 || sbits == 8);
+}
+int tq_mma_keys_per_stage(int hd) { return hd >= 256 ? 64 : 128; }
+int tq_mma_threads(int hd) { return (tq_mma_keys_per_stage(hd) / 16 + 1) * 32; }
+
+cudaError_t launch_tq_attn_mma(const TqAttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                               int hd, int sbits, bool kraw, int grid, cudaStream_t s) {
+  if (a.splits > kTqmMaxSplits) return cudaErrorInvalidValue;
+  if (hd == 64) return launch_hd<64>(a, tk, tv, sbits, kraw, grid, s);
+  if (hd == 128) return launch_hd<128>(a, tk, tv, sbits, kraw, grid, s);
+  return launch_hd<256>(a, tk, tv, sbits, kraw, grid, s);
+}
+
+}  // namespace hfa

@@ -36,8 +36,6 @@
 #include "hfa_internal.h"
 #include "hfa_verify.h"
 
-hfa_status hfa_encode_kv_map(CUtensorMap* map, void* base, int rows, int hd, int box_rows);
-
 namespace hfa {
 
 // ------------------------------------------------------------------ GEMM (tcgen05)

@@ -175,6 +175,16 @@ def test_hybrid_raw_keys_coded_values():
     _run_tq_attention(w, 8, [1500, 600], hybrid=True, seed=33)
 
 
+@pytest.mark.parametrize("hybrid", [False, True])
+def test_group_of_eight_4bit_values(hybrid):
+    # eight query heads per KV head (the largest group), 4-bit value codes, head_dim 128,
+    # keys coded or raw
+    w = wl.Workload(name="tq_g8", hidden=256, num_heads=16, num_kv_heads=2, head_dim=128,
+                    layer_type=wl.FULL, window=0, kv_capacity=3000, ring=False, batch=2,
+                    rope_theta=1e6, seed=26)
+    _run_tq_attention(w, 4, [2999, 77], hybrid=hybrid, seed=34)
+
+
 @pytest.mark.parametrize("bits", [4, 6, 8])
 def test_encode_then_attend_matches_the_oracle_pipeline(bits):
     # f32 K/V rows appended one position at a time by the library's encoder, then attended;
