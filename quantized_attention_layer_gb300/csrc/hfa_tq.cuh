@@ -41,6 +41,39 @@ __device__ __forceinline__ void tq_fwht_rows(float* v, int count, int stride, in
   sync();
 }
 
+// Normalised FWHT of one block of N (32..256) floats at v by one warp, in registers: lane
+// l holds elements l R .. l R + R - 1 (R = N / 32); butterflies 1 .. R / 2 inside the
+// lane, then R .. N / 2 across lanes by shuffles (the lane whose bit is set takes
+// partner - own, the other own + partner), the same additions in the same order as
+// tq_fwht_rows.
+template <int N>
+__device__ __forceinline__ void tq_fwht_warp(float* v, int lane) {
+  constexpr int R = N / 32;
+  static_assert(R >= 1 && N <= 256, "32 .. 256 values per block");
+  float x[R];
+#pragma unroll
+  for (int j = 0; j < R; ++j) x[j] = v[lane * R + j];
+#pragma unroll
+  for (int h = 1; h < R; h <<= 1)
+#pragma unroll
+    for (int j = 0; j < R; ++j)
+      if (!(j & h)) {
+        const float a0 = x[j], a1 = x[j + h];
+        x[j] = a0 + a1;
+        x[j + h] = a0 - a1;
+      }
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1)
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      const float p = __shfl_xor_sync(0xffffffffu, x[j], m);
+      x[j] = (lane & m) ? p - x[j] : x[j] + p;
+    }
+  const float sc = rsqrtf((float)N);
+#pragma unroll
+  for (int j = 0; j < R; ++j) v[lane * R + j] = x[j] * sc;
+}
+
 // The last CTA of a (sequence, KV head): the chunk records at `up` ([splits][8][HD + 4]:
 // O in the rotated domain, then m and l in base-2 units) combined with the weights
 // 2^(m_s - M) / sum_s' 2^(m_s' - M) l_s', the chunks added in order, then rotated back
@@ -100,7 +133,8 @@ __device__ void tq_merge_records(const float* up, int splits, int G, float* wsm,
     reinterpret_cast<float4*>(s_o)[c] = acc4;
   }
   __syncthreads();
-  tq_fwht_rows(s_o, G, HD, BLK, HD, tid, nthr, []() { __syncthreads(); });
+  for (int r = warp; r < G * (HD / BLK); r += nw) tq_fwht_warp<BLK>(s_o + r * BLK, lane);
+  __syncthreads();
   for (int e = tid; e < G * HD; e += nthr) {
     const int h = e / HD, i = e - h * HD;
     o[h * HD + i] = s_o[h * HD + i] * signs[i];

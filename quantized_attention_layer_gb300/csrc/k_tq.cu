@@ -249,9 +249,11 @@ __global__ void __launch_bounds__(kTqThreads) tq_attn_kernel(const TqAttnArgs a)
   const int G = a.nh / a.nkv;  // <= GM
   const int unit = blockIdx.x / a.splits, split = blockIdx.x - unit * a.splits;
   const int b = unit / a.nkv, kvh = unit - b * a.nkv;
-  // the table has room for 2^BITS levels; a byte-coded format may use fewer (5, 6 bits)
-  for (int i = tid; i < LEVELS * 32; i += kTqThreads)
-    s_tab[i] = (i >> 5) < a.levels ? a.centroids[i >> 5] : 0.f;
+  // the table has room for 2^BITS levels; a byte-coded format may use fewer (5, 6 bits).
+  // Each centroid is loaded once (into the score area), then copied to its 32 bank slots.
+  for (int c = tid; c < LEVELS; c += kTqThreads) s_p[c] = c < a.levels ? a.centroids[c] : 0.f;
+  __syncthreads();
+  for (int i = tid; i < LEVELS * 32; i += kTqThreads) s_tab[i] = s_p[i >> 5];
   for (int e = tid; e < GM * HD; e += kTqThreads) {
     const int h = e / HD, i = e - h * HD;
     const float qv = h < G ? a.q[((size_t)b * a.nh + kvh * G + h) * HD + i] * a.qscale : 0.f;

@@ -36,7 +36,8 @@ constexpr int kTqmMaxSplits = 256;      // the merge's weight table: 8 x 256 flo
 
 template <int HD, int SBITS, bool KRAW>
 struct TqmCfg {
-  static constexpr int NC = HD >= 256 ? 4 : 8;     // consumer warps, 16 keys each
+  // consumer warps, 16 keys each; with the producer 3 warps per scheduler (hd <= 128)
+  static constexpr int NC = HD >= 256 ? 4 : 11;
   static constexpr int T = NC * 16;                 // keys per stage
   static constexpr int CB = HD * SBITS / 8;         // code bytes of a row
   static constexpr int BOXW = CB < 128 ? CB : 128;  // bytes of a TMA box row
@@ -47,14 +48,19 @@ struct TqmCfg {
   static constexpr int NORM_OFF = KTILE + VTILE;  // f32 [T] K norms (coded K), [T] V norms
   static constexpr int NNORM = KRAW ? 1 : 2;
   static constexpr int STAGE = (KTILE + VTILE + NNORM * T * 4 + 1023) / 1024 * 1024;
-  static constexpr int LEV = 1 << SBITS;  // table entries
-  static constexpr int TAB = LEV * 32 * 4;
+  // the table: 8-bit codes one word per code (bf16 hi | lo << 16); 4-bit codes one 64-bit
+  // entry per byte, i.e. per pair of codes (hi pair, lo pair); both one copy per bank
+  static constexpr int LEV = 1 << SBITS;  // code levels
+  static constexpr int ENT = 256;
+  static constexpr int EB = SBITS == 8 ? 4 : 8;  // entry bytes
+  static constexpr int TAB = ENT * 32 * EB;
   static constexpr int KS = HD / 16;  // k16 steps of S = Q K^T
   static constexpr int NTO = HD / 8;  // n8 tiles of O
   static constexpr int RS = HD + 4;   // record: O[HD], m, l, pad
   static constexpr int QF = KS * 32 * 16;
   static constexpr int SQ = 8 * HD * 4;  // the rotated queries (f32), later the merged O
   static constexpr int FIXED = TAB + QF + SQ + 256;
+  static_assert(LEV * 4 <= QF, "the code words fit in the fragment area");
   static constexpr int NS0 = (kTqmSmemBudget - FIXED) / STAGE;
   static constexpr int NS = NS0 < kTqmMaxStages ? NS0 : kTqmMaxStages;
   static constexpr size_t SMEM = 1024 + (size_t)NS * STAGE + FIXED;
@@ -96,6 +102,14 @@ __device__ __forceinline__ int qdim(int ks, int t, int hh, int e) {
 __device__ __forceinline__ uint32_t tab_ld(uint32_t tab_lane, uint32_t c) {
   return lds32(tab_lane + (c << 7));
 }
+// the 4-bit table entry of byte j of w (two codes: the low nibble first) for this lane:
+// .x = (hi, hi), .y = (lo, lo); entries 256 bytes apart
+__device__ __forceinline__ uint2 pair_ld(uint32_t tab_lane8, uint32_t w, int j) {
+  const uint32_t off = __byte_perm(w, 0u, 0x4404u | ((uint32_t)j << 4));  // byte j << 8
+  uint2 v;
+  asm("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(tab_lane8 + off));
+  return v;
+}
 // operand registers of two adjacent k (or two keys) from their table words
 __device__ __forceinline__ uint32_t hi_pair(uint32_t e0, uint32_t e1) {
   return __byte_perm(e0, e1, 0x5410);
@@ -106,12 +120,14 @@ __device__ __forceinline__ uint32_t lo_pair(uint32_t e0, uint32_t e1) {
 
 // S += [hi(q); lo(q)] (hi(c) + lo(c)) for one k16 step: codes c0, c1 at k = 2t, 2t + 1 (b0),
 // c2, c3 at k = 2t + 8, 2t + 9 (b1)
-__device__ __forceinline__ void score_step(float (&s)[4], const uint32_t (&A)[4], uint32_t tab,
-                                           uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3) {
+// (hi and lo terms in separate accumulators: two dependency chains of half the length)
+__device__ __forceinline__ void score_step(float (&sh)[4], float (&sl)[4], const uint32_t (&A)[4],
+                                           uint32_t tab, uint32_t c0, uint32_t c1, uint32_t c2,
+                                           uint32_t c3) {
   const uint32_t e0 = tab_ld(tab, c0), e1 = tab_ld(tab, c1);
   const uint32_t e2 = tab_ld(tab, c2), e3 = tab_ld(tab, c3);
-  mma_bf16(s, A, hi_pair(e0, e1), hi_pair(e2, e3));
-  mma_bf16(s, A, lo_pair(e0, e1), lo_pair(e2, e3));
+  mma_bf16(sh, A, hi_pair(e0, e1), hi_pair(e2, e3));
+  mma_bf16(sl, A, lo_pair(e0, e1), lo_pair(e2, e3));
 }
 
 // O_tile += [hi(p); lo(p)] (hi(v) + lo(v)): codes of keys 2t, 2t + 1 (b0) and 2t + 8, 2t + 9
@@ -175,7 +191,30 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
     prefetch_tmap(&tmk);
     prefetch_tmap(&tmv);
   }
-  __syncthreads();
+  if (warp < NC) {
+    // the decode table (the format's centroids never change: read before the dependency
+    // wait); each centroid loaded once, then copied to its bank slots
+    uint32_t* s_cw = reinterpret_cast<uint32_t*>(qf);
+    for (int c = threadIdx.x; c < Cfg::LEV; c += NCT) {
+      const float f = c < a.levels ? __ldg(a.centroids + c) : 0.f;
+      __nv_bfloat16 h, l;
+      split_bf16(f, h, l);
+      s_cw[c] = pack_bf2(h, l);
+    }
+    consumer_bar<NCT>();
+    if (SBITS == 8) {
+      for (int i = threadIdx.x; i < 256 * 32; i += NCT) s_tab[i] = s_cw[i >> 5];
+    } else {
+      for (int i = threadIdx.x; i < 256 * 32; i += NCT) {
+        const uint32_t v = (uint32_t)(i >> 5);
+        const uint32_t e0 = s_cw[v & 15u], e1 = s_cw[v >> 4];
+        reinterpret_cast<uint2*>(s_tab)[i] = make_uint2(hi_pair(e0, e1), lo_pair(e0, e1));
+      }
+    }
+  }
+  __syncthreads();  // the table is written; the code words are no longer read
+  // Programmatic dependent launch: q and the codes come from earlier kernels
+  pdl_wait();
 
   // visible slot range [lo, hi] of this sequence
   const int P = a.seq_pos[b];
@@ -241,20 +280,16 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
     // ------------------------------------------------------------- consumers
     const int ctid = threadIdx.x;
     auto csync = []() { consumer_bar<NCT>(); };
-    for (int i = ctid; i < Cfg::LEV * 32; i += NCT) {
-      const int c = i >> 5;
-      const float f = c < a.levels ? __ldg(a.centroids + c) : 0.f;
-      __nv_bfloat16 h, l;
-      split_bf16(f, h, l);
-      s_tab[i] = pack_bf2(h, l);
-    }
     for (int e = ctid; e < 8 * HD; e += NCT) {
       const int h = e / HD, i = e - h * HD;
       const float qv = h < G ? a.q[((size_t)b * a.nh + kvh * G + h) * HD + i] * a.qscale : 0.f;
       s_q[e] = KRAW ? qv : qv * __ldg(a.signs + i);
     }
     csync();
-    if (!KRAW) tq_fwht_rows(s_q, G, HD, HD, HD, ctid, NCT, csync);  // the keys' rotated domain
+    if (!KRAW) {  // the query in the keys' rotated domain: one warp per head
+      for (int h = warp; h < G; h += NC) tq_fwht_warp<HD>(s_q + h * HD, lane);
+      csync();
+    }
     // query fragments: A rows 0..G-1 = hi(q), rows 8..8+G-1 = lo(q), k in the codes' order
     for (int ks = warp; ks < Cfg::KS; ks += NC) {
       uint32_t w[4] = {0u, 0u, 0u, 0u};
@@ -276,7 +311,7 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
     float o[Cfg::NTO][4];
 #pragma unroll
     for (int i = 0; i < Cfg::NTO; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    const uint32_t tab = smem_u32(s_tab) + lane * 4;
+    const uint32_t tab = smem_u32(s_tab) + lane * Cfg::EB;
     const uint32_t stage_base = smem_u32(stages);
     const int krow = warp * 16;
 
@@ -293,6 +328,7 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
 
       // S = Q K^T for 16 keys: n8 tiles of keys krow + g (s0) and krow + 8 + g (s1)
       float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+      float u0[4] = {0.f, 0.f, 0.f, 0.f}, u1[4] = {0.f, 0.f, 0.f, 0.f};  // lo(c) terms
       if constexpr (KRAW) {
 #pragma unroll
         for (int ks = 0; ks < Cfg::KS; ++ks) {
@@ -312,10 +348,12 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
           const uint32_t w1 = lds32(code_addr<Cfg>(kb, krow + 8 + g, 16 * ks + 4 * t));
           const uint4 qa = qf[ks * 32 + lane];
           const uint32_t A[4] = {qa.x, qa.y, qa.z, qa.w};
-          score_step(s0, A, tab, w0 & 255u, (w0 >> 8) & 255u, (w0 >> 16) & 255u, w0 >> 24);
-          score_step(s1, A, tab, w1 & 255u, (w1 >> 8) & 255u, (w1 >> 16) & 255u, w1 >> 24);
+          score_step(s0, u0, A, tab, w0 & 255u, (w0 >> 8) & 255u, (w0 >> 16) & 255u, w0 >> 24);
+          score_step(s1, u1, A, tab, w1 & 255u, (w1 >> 8) & 255u, (w1 >> 16) & 255u, w1 >> 24);
         }
       } else {
+        // byte j of a code word = the codes of k = 2t, 2t + 1 (j even) or 2t + 8, 2t + 9
+        // (j odd) of k16 step 2 mw + j / 2: one table entry gives both operand words
 #pragma unroll
         for (int mw = 0; mw < HD / 32; ++mw) {
           const uint32_t w0 = lds32(code_addr<Cfg>(kb, krow + g, 16 * mw + 4 * t));
@@ -324,15 +362,19 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
           for (int half = 0; half < 2; ++half) {
             const uint4 qa = qf[(2 * mw + half) * 32 + lane];
             const uint32_t A[4] = {qa.x, qa.y, qa.z, qa.w};
-            const uint32_t x0 = w0 >> (16 * half), x1 = w1 >> (16 * half);
-            score_step(s0, A, tab, x0 & 15u, (x0 >> 4) & 15u, (x0 >> 8) & 15u, (x0 >> 12) & 15u);
-            score_step(s1, A, tab, x1 & 15u, (x1 >> 4) & 15u, (x1 >> 8) & 15u, (x1 >> 12) & 15u);
+            const uint2 a0 = pair_ld(tab, w0, 2 * half), a1 = pair_ld(tab, w0, 2 * half + 1);
+            const uint2 c0 = pair_ld(tab, w1, 2 * half), c1 = pair_ld(tab, w1, 2 * half + 1);
+            mma_bf16(s0, A, a0.x, a1.x);
+            mma_bf16(u0, A, a0.y, a1.y);
+            mma_bf16(s1, A, c0.x, c1.x);
+            mma_bf16(u1, A, c0.y, c1.y);
           }
         }
       }
       // logits of head g for local keys krow + {2t, 2t+1, 8+2t, 9+2t} (hi row + lo row),
       // times the keys' norms
-      float sv[4] = {s0[0] + s0[2], s0[1] + s0[3], s1[0] + s1[2], s1[1] + s1[3]};
+      float sv[4] = {(s0[0] + s0[2]) + (u0[0] + u0[2]), (s0[1] + s0[3]) + (u0[1] + u0[3]),
+                     (s1[0] + s1[2]) + (u1[0] + u1[2]), (s1[1] + s1[3]) + (u1[1] + u1[3])};
       const int kl0 = krow + 2 * t;
       const int kidx0 = k_begin + i * T + kl0;
       bool valid[4];
@@ -356,12 +398,14 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
       for (int e = 0; e < 4; ++e) p[e] = exp2f(sv[e] - m_use);
       l = l * corr + (p[0] + p[1]) + (p[2] + p[3]);
       m = m_new;
+      if (__any_sync(0xffffffffu, corr != 1.f)) {  // most tiles leave every head's max
 #pragma unroll
-      for (int nt = 0; nt < Cfg::NTO; ++nt) {
-        o[nt][0] *= corr;
-        o[nt][1] *= corr;
-        o[nt][2] *= corr;
-        o[nt][3] *= corr;
+        for (int nt = 0; nt < Cfg::NTO; ++nt) {
+          o[nt][0] *= corr;
+          o[nt][1] *= corr;
+          o[nt][2] *= corr;
+          o[nt][3] *= corr;
+        }
       }
       // P times the V norms as the A operand: row g = hi, row g + 8 = lo; k = the 16 keys
       uint32_t PA[4];
@@ -401,10 +445,19 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
           const uint32_t wB = lds32(code_addr<Cfg>(vb, krow + 2 * t + 1, byte));
           const uint32_t wC = lds32(code_addr<Cfg>(vb, krow + 2 * t + 8, byte));
           const uint32_t wD = lds32(code_addr<Cfg>(vb, krow + 2 * t + 9, byte));
+          // byte k of xe / xo: the codes of dim 2k / 2k + 1 (of the lane's eight) for keys
+          // 2t (low nibble) and 2t + 1; ye / yo the same for keys 2t + 8, 2t + 9
+          const uint32_t xe = (wA & 0x0f0f0f0fu) | ((wB << 4) & 0xf0f0f0f0u);
+          const uint32_t xo = ((wA >> 4) & 0x0f0f0f0fu) | (wB & 0xf0f0f0f0u);
+          const uint32_t ye = (wC & 0x0f0f0f0fu) | ((wD << 4) & 0xf0f0f0f0u);
+          const uint32_t yo = ((wC >> 4) & 0x0f0f0f0fu) | (wD & 0xf0f0f0f0u);
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            pv_tile(o[grp * 8 + j], PA, tab, (wA >> (4 * j)) & 15u, (wB >> (4 * j)) & 15u,
-                    (wC >> (4 * j)) & 15u, (wD >> (4 * j)) & 15u);
+          for (int j = 0; j < 8; ++j) {
+            const uint2 b0 = pair_ld(tab, (j & 1) ? xo : xe, j >> 1);
+            const uint2 b1 = pair_ld(tab, (j & 1) ? yo : ye, j >> 1);
+            mma_bf16(o[grp * 8 + j], PA, b0.x, b1.x);
+            mma_bf16(o[grp * 8 + j], PA, b0.y, b1.y);
+          }
         }
       }
       __syncwarp();
@@ -488,8 +541,17 @@ cudaError_t launch_t(const TqAttnArgs& a, const CUtensorMap& tk, const CUtensorM
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)Cfg::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<grid, Cfg::THREADS, Cfg::SMEM, s>>>(tk, tv, a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(Cfg::THREADS);
+  cfg.dynamicSmemBytes = Cfg::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tk, tv, a);
 }
 
 template <int HD>
@@ -505,7 +567,7 @@ cudaError_t launch_hd(const TqAttnArgs& a, const CUtensorMap& tk, const CUtensor
 bool tq_mma_supported(int hd, int sbits) {
   return (hd == 64 || hd == 128 || hd == 256) && (sbits == 4 || sbits == 8);
 }
-int tq_mma_keys_per_stage(int hd) { return hd >= 256 ? 64 : 128; }
+int tq_mma_keys_per_stage(int hd) { return hd >= 256 ? 64 : 176; }
 int tq_mma_threads(int hd) { return (tq_mma_keys_per_stage(hd) / 16 + 1) * 32; }
 
 cudaError_t launch_tq_attn_mma(const TqAttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
