@@ -554,7 +554,7 @@ def ffn_workload(f, K, W, R, world):
     return res
 
 
-def tq_workload(bits, K, W, world):
+def tq_workload(bits, K, W, world, name):
     """Flash-decode over a coded KV cache (4- or 8-bit codes + f32 block norms for K and V;
     hfa_attention_decode_tq), and the bf16 attention of the same shape for comparison."""
     from quantized_attention_layer_gb300 import hfa, workloads as wl
@@ -619,6 +619,7 @@ def tq_workload(bits, K, W, world):
             "step_bytes": step_bytes, "step_gbs": gbs, "frac": gbs / peak, "peak_source": src,
             "bits": bits, "shape": f"batch {B}, {nh}/{nkv} heads, hd {hd}, {C} keys",
             "replicas": R, "clocks": clocks,
+            "traffic": ncu_traffic("k_tq_mma.cu", f"tq_attention_{name}.md"),
             "dense_bf16": {"ms_per_step": dms / K, "step_bytes": dense_bytes, "step_gbs": dgbs,
                            "frac": dgbs / peak}}
 
@@ -677,7 +678,7 @@ def run_ours(args, rank, world, local):
         if name == w.name:
             continue
         if name in TQ:
-            wls[name] = tq_workload(TQ[name], K, W, world)
+            wls[name] = tq_workload(TQ[name], K, W, world, name)
             continue
         if name in wl.FFN_BY_NAME:
             wls[name] = ffn_workload(wl.FFN_BY_NAME[name], K, W, 8, world)

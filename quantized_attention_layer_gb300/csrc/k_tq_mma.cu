@@ -102,6 +102,10 @@ __device__ __forceinline__ int qdim(int ks, int t, int hh, int e) {
 __device__ __forceinline__ uint32_t tab_ld(uint32_t tab_lane, uint32_t c) {
   return lds32(tab_lane + (c << 7));
 }
+// the table word of byte j of w (an 8-bit code): the byte moved down by one permute
+__device__ __forceinline__ uint32_t tab_ld8(uint32_t tab_lane, uint32_t w, int j) {
+  return tab_ld(tab_lane, __byte_perm(w, 0u, 0x4440u | (uint32_t)j));
+}
 // the 4-bit table entry of byte j of w (two codes: the low nibble first) for this lane:
 // .x = (hi, hi), .y = (lo, lo); entries 256 bytes apart
 __device__ __forceinline__ uint2 pair_ld(uint32_t tab_lane8, uint32_t w, int j) {
@@ -118,24 +122,23 @@ __device__ __forceinline__ uint32_t lo_pair(uint32_t e0, uint32_t e1) {
   return __byte_perm(e0, e1, 0x7632);
 }
 
-// S += [hi(q); lo(q)] (hi(c) + lo(c)) for one k16 step: codes c0, c1 at k = 2t, 2t + 1 (b0),
-// c2, c3 at k = 2t + 8, 2t + 9 (b1)
-// (hi and lo terms in separate accumulators: two dependency chains of half the length)
-__device__ __forceinline__ void score_step(float (&sh)[4], float (&sl)[4], const uint32_t (&A)[4],
-                                           uint32_t tab, uint32_t c0, uint32_t c1, uint32_t c2,
-                                           uint32_t c3) {
-  const uint32_t e0 = tab_ld(tab, c0), e1 = tab_ld(tab, c1);
-  const uint32_t e2 = tab_ld(tab, c2), e3 = tab_ld(tab, c3);
+// S += [hi(q); lo(q)] (hi(c) + lo(c)) for one k16 step of 8-bit codes: bytes 0, 1 of w are
+// k = 2t, 2t + 1 (b0), bytes 2, 3 are k = 2t + 8, 2t + 9 (b1) (hi and lo terms in separate
+// accumulators: two dependency chains of half the length)
+__device__ __forceinline__ void score_step8(float (&sh)[4], float (&sl)[4], const uint32_t (&A)[4],
+                                            uint32_t tab, uint32_t w) {
+  const uint32_t e0 = tab_ld8(tab, w, 0), e1 = tab_ld8(tab, w, 1);
+  const uint32_t e2 = tab_ld8(tab, w, 2), e3 = tab_ld8(tab, w, 3);
   mma_bf16(sh, A, hi_pair(e0, e1), hi_pair(e2, e3));
   mma_bf16(sl, A, lo_pair(e0, e1), lo_pair(e2, e3));
 }
 
-// O_tile += [hi(p); lo(p)] (hi(v) + lo(v)): codes of keys 2t, 2t + 1 (b0) and 2t + 8, 2t + 9
-// (b1) at the lane's column
-__device__ __forceinline__ void pv_tile(float (&o)[4], const uint32_t (&PA)[4], uint32_t tab,
-                                        uint32_t cA, uint32_t cB, uint32_t cC, uint32_t cD) {
-  const uint32_t eA = tab_ld(tab, cA), eB = tab_ld(tab, cB);
-  const uint32_t eC = tab_ld(tab, cC), eD = tab_ld(tab, cD);
+// O_tile += [hi(p); lo(p)] (hi(v) + lo(v)) for 8-bit codes: byte j of the words of keys 2t,
+// 2t + 1 (b0) and 2t + 8, 2t + 9 (b1) is the lane's column of n8 tile j
+__device__ __forceinline__ void pv_tile8(float (&o)[4], const uint32_t (&PA)[4], uint32_t tab,
+                                         uint32_t wA, uint32_t wB, uint32_t wC, uint32_t wD, int j) {
+  const uint32_t eA = tab_ld8(tab, wA, j), eB = tab_ld8(tab, wB, j);
+  const uint32_t eC = tab_ld8(tab, wC, j), eD = tab_ld8(tab, wD, j);
   mma_bf16(o, PA, hi_pair(eA, eB), hi_pair(eC, eD));
   mma_bf16(o, PA, lo_pair(eA, eB), lo_pair(eC, eD));
 }
@@ -348,8 +351,8 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
           const uint32_t w1 = lds32(code_addr<Cfg>(kb, krow + 8 + g, 16 * ks + 4 * t));
           const uint4 qa = qf[ks * 32 + lane];
           const uint32_t A[4] = {qa.x, qa.y, qa.z, qa.w};
-          score_step(s0, u0, A, tab, w0 & 255u, (w0 >> 8) & 255u, (w0 >> 16) & 255u, w0 >> 24);
-          score_step(s1, u1, A, tab, w1 & 255u, (w1 >> 8) & 255u, (w1 >> 16) & 255u, w1 >> 24);
+          score_step8(s0, u0, A, tab, w0);
+          score_step8(s1, u1, A, tab, w1);
         }
       } else {
         // byte j of a code word = the codes of k = 2t, 2t + 1 (j even) or 2t + 8, 2t + 9
@@ -433,9 +436,7 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
           const uint32_t wC = lds32(code_addr<Cfg>(vb, krow + 2 * t + 8, byte));
           const uint32_t wD = lds32(code_addr<Cfg>(vb, krow + 2 * t + 9, byte));
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            pv_tile(o[grp * 4 + j], PA, tab, (wA >> (8 * j)) & 255u, (wB >> (8 * j)) & 255u,
-                    (wC >> (8 * j)) & 255u, (wD >> (8 * j)) & 255u);
+          for (int j = 0; j < 4; ++j) pv_tile8(o[grp * 4 + j], PA, tab, wA, wB, wC, wD, j);
         }
       } else {
 #pragma unroll
