@@ -83,8 +83,11 @@ struct VGemmArgs {
   // cluster: CTA i stores [16 tokens][128 rows] f32 as 8-byte entries (value | launch tag)
   // at gpart + i * 2048, and the CTAs of a group (the tpc x splits consecutive CTAs that a
   // cluster would hold) poll one another's entries.  gctr counts launches x grid (the tags).
+  // The GEMMs that share gpart keep apart tag spaces (tag_lane 0 or 1: tags 2 n + 2 +
+  // tag_lane for the n-th launch), so no launch can take an entry another GEMM left.
   unsigned long long* gpart;
   unsigned long long* gctr;
+  uint32_t tag_lane;
 };
 
 // Activation operand of the verify GEMMs, built once per call: row t of the block
@@ -220,7 +223,8 @@ __global__ void __launch_bounds__(128, 1) verify_gemm_kernel(const VGemmArgs a) 
     // the launch's number: every CTA reads the counter before its own increment and after
     // every increment of the launches before it
     const unsigned long long n = ld_acquire_u64(a.gctr);
-    *s_tag = (uint32_t)(n / (unsigned long long)gridDim.x) + 1u;  // 0 marks "never written"
+    // 0 marks "never written"
+    *s_tag = 2u * ((uint32_t)(n / (unsigned long long)gridDim.x) + 1u) + a.tag_lane;
     *s_abort = 0;
     red_release_add_u64(a.gctr, 1ull);
   }
@@ -339,6 +343,54 @@ __global__ void __launch_bounds__(128, 1) verify_gemm_kernel(const VGemmArgs a) 
     }
     return acc;
   };
+  // rows rb + 32 j (j < nj <= 8) of token t: with gpart, every row's entries polled in one
+  // round (one L2 round trip for all of them, not one per row); the splits added in rank
+  // order as split_sum does
+  auto split_sum_rows = [&](int rb, int t, int nj, float (&v)[8]) {
+    if (!a.gpart) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j < nj) v[j] = split_sum(rb + 32 * j, t);
+      return;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = 0.f;
+    for (int c0 = 0; c0 < S; c0 += 4) {
+      unsigned long long w[8][4];
+      const uint64_t t0 = globaltimer_ns();
+      for (;;) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (j < nj) {
+            const int r = rb + 32 * j;
+            const unsigned long long* p =
+                gbase + (size_t)((r >> 7) * S) * (16 * kVM) + t * kVM + (r & 127);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              w[j][i] = ld_tagged(p + (size_t)(c0 + i < S ? c0 + i : S - 1) * (16 * kVM));
+          }
+        }
+        bool ready = true;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (j < nj) ready = ready && (uint32_t)(w[j][i] >> 32) == tag;
+        if (ready || *s_abort) break;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          atomicOr(a.g.err, kErrWaitTimeout);
+          *s_abort = 1;
+          break;
+        }
+        __nanosleep(32);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (j < nj && c0 + i < S) v[j] += tagged_value(w[j][i]);
+    }
+  };
   if (MODE == kModeQKV) {
     // items (head, token) of the group's rows, one warp each
     const int hd = a.g.hd;
@@ -349,21 +401,16 @@ __global__ void __launch_bounds__(128, 1) verify_gemm_kernel(const VGemmArgs a) 
     for (int it = rank * 4 + warp; it < nitems; it += cs * 4) {
       const int hl = it / L, t = it - hl * L;
       const int hh = rows0 / hd + hl;
+      float u[8];
+      split_sum_rows(hl * hd + lane, t, hd / 32, u);
       if (hd == 64) {
-        float v[2];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) v[j] = split_sum(hl * 64 + lane + 32 * j, t);
+        float v[2] = {u[0], u[1]};
         finish_head_row<64>(g, hh, t, v, lane);
       } else if (hd == 128) {
-        float v[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) v[j] = split_sum(hl * 128 + lane + 32 * j, t);
+        float v[4] = {u[0], u[1], u[2], u[3]};
         finish_head_row<128>(g, hh, t, v, lane);
       } else {
-        float v[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = split_sum(hl * 256 + lane + 32 * j, t);
-        finish_head_row<256>(g, hh, t, v, lane);
+        finish_head_row<256>(g, hh, t, u, lane);
       }
     }
   } else {
@@ -1402,6 +1449,7 @@ hfa_status verify_ctx_append(VerifyState* v, const VerifyCall& c, char* msg, int
                    : gemm_splits(ktiles, qa.chunks, c.num_sms, qa.tpc, v->max_clusters);
   qa.gpart = flat ? v->gpart : nullptr;
   qa.gctr = v->gctr + 1;
+  qa.tag_lane = 1;  // odd tags: the block's QKV GEMM uses the same gpart with even ones
   tb("ctx_kv_gemm");
   e = launch_ex3(verify_gemm_kernel<kModeQKV>, dim3(ktiles * qa.splits), 128, kVGemmSmem, pdl, s,
                  flat ? 1 : qa.splits * qa.tpc, flat, qa);
