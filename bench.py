@@ -53,10 +53,13 @@ FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0
 EXTRA = ("tiny_sliding", "sliding_b16_ring1024", "full_b4_128k_softcap", "verify_l16_8k",
          "global_hd512_32k", "drafter_l16_8k", "ffn_b1", "ffn_b16", "tq8_full_b1_32k",
-         "tq4_full_b1_32k")
-# attention over a quantised (TurboQuant) KV cache: bits, and the attention shape of the
-# headline layer (batch 1, 32/8 heads, head dim 128, 32768 visible keys)
-TQ = {"tq8_full_b1_32k": 8, "tq4_full_b1_32k": 4}
+         "tq4_full_b1_32k", "tq8_global_hd512_32k")
+# attention over a quantised (TurboQuant) KV cache: the attention shapes of the headline
+# layer (batch 1, 32/8 heads, head dim 128) and of the global layer (16/2 heads, head dim
+# 512), 32768 visible keys
+# coded-cache attention workloads: bits, head dim, query heads, KV heads (batch 1, 32K keys)
+TQ = {"tq8_full_b1_32k": (8, 128, 32, 8), "tq4_full_b1_32k": (4, 128, 32, 8),
+      "tq8_global_hd512_32k": (8, 512, 16, 2)}
 
 
 def parse():
@@ -554,11 +557,13 @@ def ffn_workload(f, K, W, R, world):
     return res
 
 
-def tq_workload(bits, K, W, world, name):
+def tq_workload(spec, K, W, world, name):
     """Flash-decode over a coded KV cache (4- or 8-bit codes + f32 block norms for K and V;
-    hfa_attention_decode_tq), and the bf16 attention of the same shape for comparison."""
+    hfa_attention_decode_tq), and the bf16 attention of the same shape for comparison (head
+    dims up to 256: the standalone bf16 attention has no 512 form)."""
     from quantized_attention_layer_gb300 import hfa, workloads as wl
-    B, nh, nkv, hd, C = 1, 32, 8, 128, 32768
+    bits, hd, nh, nkv = spec
+    B, C = 1, 32768
     w = wl.Workload(name="tq", hidden=256, num_heads=nh, num_kv_heads=nkv, head_dim=hd,
                     layer_type=wl.FULL, window=0, kv_capacity=C, ring=False, batch=B,
                     rope_theta=1e6, seed=11)
@@ -592,6 +597,19 @@ def tq_workload(bits, K, W, world, name):
     graph, ev0, ev1 = timed_graph(stream, lambda: [step(i) for i in range(K)], K)
     ms, clocks = time_replays(graph, ev0, ev1, stream, world)
     del graph, caches
+    fmt.destroy()
+    peak, src = measured_peaks()
+    ms_per_step = ms / K
+    gbs = step_bytes / (ms_per_step * 1e-3) / 1e9
+    out = {"unit": "attention calls/s", "value": world * 1e3 / ms_per_step,
+           "ms_per_step": ms_per_step, "step_bytes": step_bytes, "step_gbs": gbs,
+           "frac": gbs / peak, "peak_source": src, "bits": bits,
+           "shape": f"batch {B}, {nh}/{nkv} heads, hd {hd}, {C} keys", "replicas": R,
+           "clocks": clocks, "traffic": ncu_traffic("k_tq_mma.cu", f"tq_attention_{name}.md"),
+           "dense_bf16": None}
+    if hd > 256:
+        torch.cuda.empty_cache()
+        return out
     # the same attention over a dense bf16 cache
     dense_bytes = B * nkv * C * hd * 2 * 2 + 2 * q.numel() * 4
     Rd = max(2, -(-300_000_000 // dense_bytes))
@@ -609,19 +627,11 @@ def tq_workload(bits, K, W, world, name):
     graph, ev0, ev1 = timed_graph(stream, lambda: [dstep(i) for i in range(K)], K)
     dms, _ = time_replays(graph, ev0, ev1, stream, world)
     del graph, kvs
-    fmt.destroy()
     torch.cuda.empty_cache()
-    peak, src = measured_peaks()
-    ms_per_step = ms / K
-    gbs = step_bytes / (ms_per_step * 1e-3) / 1e9
     dgbs = dense_bytes / (dms / K * 1e-3) / 1e9
-    return {"unit": "attention calls/s", "value": world * 1e3 / ms_per_step, "ms_per_step": ms_per_step,
-            "step_bytes": step_bytes, "step_gbs": gbs, "frac": gbs / peak, "peak_source": src,
-            "bits": bits, "shape": f"batch {B}, {nh}/{nkv} heads, hd {hd}, {C} keys",
-            "replicas": R, "clocks": clocks,
-            "traffic": ncu_traffic("k_tq_mma.cu", f"tq_attention_{name}.md"),
-            "dense_bf16": {"ms_per_step": dms / K, "step_bytes": dense_bytes, "step_gbs": dgbs,
-                           "frac": dgbs / peak}}
+    out["dense_bf16"] = {"ms_per_step": dms / K, "step_bytes": dense_bytes, "step_gbs": dgbs,
+                         "frac": dgbs / peak}
+    return out
 
 
 def run_ours(args, rank, world, local):

@@ -204,6 +204,12 @@ struct TqAttnArgs {
   const float* signs;      // [hd]
   float* part;             // [units * splits][8][hd + 4]: O (rotated), m, l
   int* ticket;             // [units]
+  // two-level merge (tensor-core kernel): the chunks of a unit form groups of `group`; the
+  // last CTA of a group folds its records into part1 [units][16][8][hd + 4] (ticket1
+  // [units][16]), the last of those folds the groups'
+  float* part1;
+  int* ticket1;
+  int group;
   float* o;                // [B, nh, hd]
   unsigned* err;
   int B, nh, nkv, C, sliding, window, ring, levels;
@@ -211,10 +217,10 @@ struct TqAttnArgs {
   float qscale;            // scale * log2 e, or scale / softcap
   float cap_log2;          // softcap * log2 e, 0 = none
 };
-// the tensor-core kernel: head dims 64, 128 and 256, codes of 4 or 8 stored bits, K coded
-// or raw bf16 (kraw); tk / tv describe the K and V arrays (tq_mma_encode_maps); one CTA of
-// tq_mma_threads(hd) per SM, chunks of any length
-bool tq_mma_supported(int hd, int sbits);
+// the tensor-core kernel: head dims 64, 128, 256 and 512, codes of 4 or 8 stored bits, K
+// coded or raw bf16 (kraw, up to hd 256); tk / tv describe the K and V arrays as 2-D TMA
+// views; one CTA of tq_mma_threads(hd) per SM, chunks of any length
+bool tq_mma_supported(int hd, int sbits, bool kraw);
 int tq_mma_keys_per_stage(int hd);
 int tq_mma_threads(int hd);
 cudaError_t launch_tq_attn_mma(const TqAttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -74,6 +74,60 @@ __device__ __forceinline__ void tq_fwht_warp(float* v, int lane) {
   for (int j = 0; j < R; ++j) v[lane * R + j] = x[j] * sc;
 }
 
+// Folds n chunk records at `up` ([n][8][HD + 4]: O, m, l) into one record at `dst` of the
+// same form: m = max m_s, l = sum 2^(m_s - m) l_s, O = sum 2^(m_s - m) O_s (not normalised,
+// so folds compose), the records added in order.  Every thread of the CTA calls it; wsm
+// holds G x n floats of shared memory.
+template <int HD>
+__device__ void tq_fold_records(const float* up, int n, int G, float* wsm, float* dst) {
+  constexpr int RS = HD + 4;
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int warp = tid >> 5, lane = tid & 31, nw = nthr >> 5;
+  for (int h = warp; h < G; h += nw) {
+    float M = -INFINITY;
+    for (int sp = lane; sp < n; sp += 32) M = fmaxf(M, __ldcg(up + (sp * 8 + h) * RS + HD));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float Mu = M == -INFINITY ? 0.f : M;
+    float l = 0.f;
+    for (int sp = lane; sp < n; sp += 32) {
+      const float f = exp2f(__ldcg(up + (sp * 8 + h) * RS + HD) - Mu);
+      wsm[h * n + sp] = f;
+      l += f * __ldcg(up + (sp * 8 + h) * RS + HD + 1);
+    }
+    l = warp_sum(l);
+    if (lane == 0) {
+      dst[h * RS + HD] = M;
+      dst[h * RS + HD + 1] = l;
+    }
+  }
+  __syncthreads();
+  constexpr int Q4 = HD / 4;
+  for (int c = tid; c < G * Q4; c += nthr) {
+    const int h = c / Q4, d4 = c - h * Q4;
+    float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sp0 = 0; sp0 < n; sp0 += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int sp = sp0 + u < n ? sp0 + u : n - 1;  // in range
+        v[u] = __ldcg(reinterpret_cast<const float4*>(up + (sp * 8 + h) * RS) + d4);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (sp0 + u < n) {
+          const float w = wsm[h * n + sp0 + u];
+          acc4.x = fmaf(w, v[u].x, acc4.x);
+          acc4.y = fmaf(w, v[u].y, acc4.y);
+          acc4.z = fmaf(w, v[u].z, acc4.z);
+          acc4.w = fmaf(w, v[u].w, acc4.w);
+        }
+      }
+    }
+    reinterpret_cast<float4*>(dst + h * RS)[d4] = acc4;
+  }
+}
+
 // The last CTA of a (sequence, KV head): the chunk records at `up` ([splits][8][HD + 4]:
 // O in the rotated domain, then m and l in base-2 units) combined with the weights
 // 2^(m_s - M) / sum_s' 2^(m_s' - M) l_s', the chunks added in order, then rotated back

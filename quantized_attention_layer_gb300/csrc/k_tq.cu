@@ -651,8 +651,19 @@ extern "C" hfa_status hfa_tq_append(const hfa_tq* t, void* stream, const float* 
 }
 
 namespace {
-// workspace: [status word + tickets, 256-byte aligned][records]
-size_t tq_ws_head(int units) { return ((size_t)(units + 1) * 4 + 255) / 256 * 256; }
+// workspace: [status word, tickets [units], group tickets [units][16], 256-byte aligned]
+// [records [units][splits][8][hd + 4]][group folds [units][16][8][hd + 4]]
+constexpr int kTqGroups = 16;
+size_t tq_ws_head(int units) { return ((size_t)(1 + units + units * kTqGroups) * 4 + 255) / 256 * 256; }
+size_t tq_ws_folds(int units, int hd) { return (size_t)units * kTqGroups * 8 * (hd + 4) * sizeof(float); }
+// splits per group of the two-level merge: one group (a single merge) up to 32 splits, where
+// the second ticket round would cost more than the merge saves; else about sqrt(splits)
+int tq_group(int S) {
+  if (S <= 32) return S;
+  int g = 1;
+  while (g * g < S) ++g;
+  return g;
+}
 int tq_splits(int units, int max_keys, int sms) {
   int S = (8 * sms + units - 1) / units;  // many CTAs: the per-key work is latency-bound
   if (S > kTqMaxSplits) S = kTqMaxSplits;
@@ -679,7 +690,7 @@ int tq_mma_chunk(int max_keys, int S, int hd) {
 // either kernel's record count fits: the workspace does not depend on the code width
 int tq_ws_splits(int units, int max_keys, int sms, int hd) {
   const int a = tq_splits(units, max_keys, sms);
-  const int b = hd <= 256 ? tq_mma_splits(units, max_keys, sms, hd) : 0;
+  const int b = tq_mma_splits(units, max_keys, sms, hd);
   return a > b ? a : b;
 }
 int visible(const hfa_attn_desc* d, int P) {
@@ -702,7 +713,8 @@ extern "C" size_t hfa_attention_tq_workspace_bytes(const hfa_attn_desc* d, int b
   if (sms <= 0) return 0;
   const int units = batch * d->num_kv_heads;
   const int S = tq_ws_splits(units, max_keys, sms, d->head_dim);
-  return tq_ws_head(units) + (size_t)units * S * 8 * (d->head_dim + 4) * sizeof(float);
+  return tq_ws_head(units) + (size_t)units * S * 8 * (d->head_dim + 4) * sizeof(float) +
+         tq_ws_folds(units, d->head_dim);
 }
 
 extern "C" hfa_status hfa_attention_decode_tq(const hfa_attn_desc* d, const hfa_tq* t, void* stream,
@@ -747,11 +759,12 @@ extern "C" hfa_status hfa_attention_decode_tq(const hfa_attn_desc* d, const hfa_
   if (sms <= 0) return tq_fail(HFA_EDEVICE, "no CUDA device");
   const int units = batch * nkv;
   if ((long long)units * d->kv_capacity >= (1ll << 40)) return tq_fail(HFA_EUNSUPPORTED, "cache too large");
-  const size_t need = tq_ws_head(units) +
-                      (size_t)units * tq_ws_splits(units, max_keys, sms, hd) * 8 * (hd + 4) * sizeof(float);
+  const int Sws = tq_ws_splits(units, max_keys, sms, hd);
+  const size_t need = tq_ws_head(units) + (size_t)units * Sws * 8 * (hd + 4) * sizeof(float) +
+                      tq_ws_folds(units, hd);
   if (ws_bytes < need) return tq_fail(HFA_EINVAL, "workspace of %zu bytes, %zu needed", ws_bytes, need);
-  // the tensor-core kernel for head dims up to 256 (TMA rows are 32-bit coordinates)
-  const bool mma = tq_mma_supported(hd, t->sbits) && (long long)units * d->kv_capacity < (1ll << 31);
+  // the tensor-core kernel (every head dim; raw keys up to 256; TMA rows are 32-bit)
+  const bool mma = tq_mma_supported(hd, t->sbits, kraw) && (long long)units * d->kv_capacity < (1ll << 31);
   int S, chunk;
   if (mma) {
     S = tq_mma_splits(units, max_keys, sms, hd);
@@ -774,7 +787,10 @@ extern "C" hfa_status hfa_attention_decode_tq(const hfa_attn_desc* d, const hfa_
   a.signs = t->signs;
   a.err = (unsigned*)ws;
   a.ticket = (int*)ws + 1;
+  a.ticket1 = (int*)ws + 1 + units;
   a.part = (float*)((char*)ws + tq_ws_head(units));
+  a.part1 = a.part + (size_t)units * Sws * 8 * (hd + 4);
+  a.group = tq_group(S);
   a.o = o;
   a.B = batch;
   a.nh = nh;

@@ -1,6 +1,7 @@
 // k_tq_mma.cu -- flash-decode over the quantised (TurboQuant) KV cache on the tensor cores:
-// head dims 64, 128 and 256 (one norm block per row), codes of 4 bits (two per byte) or
-// one byte per code, K coded or stored raw in bf16 (the hybrid layout).
+// head dims 64, 128, 256 and 512 (one norm block per 256 dims), codes of 4 bits (two per
+// byte) or one byte per code, K coded or stored raw in bf16 (the hybrid layout, up to hd
+// 256).
 //
 // gemma4/gpu_full_attn.rs, encode_one_layer: the TQ attention (flash_attn_vec_tq,
 // flash_attn_vec_tq_hb, flash_attn_vec_hybrid): each score is the rotated query against
@@ -31,42 +32,59 @@ namespace hfa {
 namespace {
 
 constexpr int kTqmMaxStages = 4;
-constexpr int kTqmSmemBudget = 204800;  // stages + tables + query areas, bytes
+constexpr int kTqmSmemBudget = 225280;  // stages + tables + query areas, bytes
 constexpr int kTqmMaxSplits = 256;      // the merge's weight table: 8 x 256 floats
+constexpr int kTqmMaxGroups = 16;       // groups of the two-level merge (16 x 16 >= 256)
 
 template <int HD, int SBITS, bool KRAW>
 struct TqmCfg {
-  // consumer warps, 16 keys each; with the producer 3 warps per scheduler (hd <= 128)
-  static constexpr int NC = HD >= 256 ? 4 : 11;
-  static constexpr int T = NC * 16;                 // keys per stage
+  // consumer warps; with the producer 3 warps per scheduler (hd <= 128).  A key group of
+  // 16 keys belongs to QW warps, each decoding DPW of its dims (at hd 512 four warps of 128
+  // dims: the output accumulators of one warp stay at 64 registers)
+  static constexpr int NC = HD >= 512 ? 8 : (HD >= 256 ? 4 : 11);
+  static constexpr int QW = HD >= 512 ? 4 : 1;  // warps per key group
+  static constexpr int KG = NC / QW;            // key groups of a stage
+  static constexpr int DPW = HD / QW;           // dims per warp
+  static constexpr int BLK = HD < 256 ? HD : 256;  // norm block
+  static constexpr int NB = HD / BLK;              // norm blocks per row
+  static constexpr int T = KG * 16;                // keys per stage
   static constexpr int CB = HD * SBITS / 8;         // code bytes of a row
   static constexpr int BOXW = CB < 128 ? CB : 128;  // bytes of a TMA box row
   static constexpr int NBOX = CB / BOXW;
   static constexpr int SWM = BOXW == 128 ? 7 : (BOXW == 64 ? 3 : 1);  // swizzled row bits
   static constexpr int KTILE = KRAW ? T * HD * 2 : T * CB;
   static constexpr int VTILE = T * CB;
-  static constexpr int NORM_OFF = KTILE + VTILE;  // f32 [T] K norms (coded K), [T] V norms
+  // f32 [T][NB] K norms (coded K), then [T][NB] V norms
+  static constexpr int NORM_OFF = KTILE + VTILE;
   static constexpr int NNORM = KRAW ? 1 : 2;
-  static constexpr int STAGE = (KTILE + VTILE + NNORM * T * 4 + 1023) / 1024 * 1024;
+  static constexpr int STAGE = (KTILE + VTILE + NNORM * T * NB * 4 + 1023) / 1024 * 1024;
   // the table: 8-bit codes one word per code (bf16 hi | lo << 16); 4-bit codes one 64-bit
   // entry per byte, i.e. per pair of codes (hi pair, lo pair); both one copy per bank
   static constexpr int LEV = 1 << SBITS;  // code levels
   static constexpr int ENT = 256;
   static constexpr int EB = SBITS == 8 ? 4 : 8;  // entry bytes
   static constexpr int TAB = ENT * 32 * EB;
-  static constexpr int KS = HD / 16;  // k16 steps of S = Q K^T
-  static constexpr int NTO = HD / 8;  // n8 tiles of O
+  static constexpr int KS = HD / 16;    // k16 steps of S = Q K^T
+  static constexpr int KSW = DPW / 16;  // the steps of one warp
+  static constexpr int NTO = DPW / 8;   // n8 tiles of one warp's O
   static constexpr int RS = HD + 4;   // record: O[HD], m, l, pad
   static constexpr int QF = KS * 32 * 16;
   static constexpr int SQ = 8 * HD * 4;  // the rotated queries (f32), later the merged O
-  static constexpr int FIXED = TAB + QF + SQ + 256;
+  // the key groups' partial scores: [2 stage parities][KG][QW][32 lanes] float4, then the
+  // warps' stage flags [2][KG][QW] int
+  static constexpr int XFL = 2 * KG * QW * 32 * 16;
+  static constexpr int XCH = QW > 1 ? XFL + (2 * KG * QW * 4 + 15) / 16 * 16 : 0;
+  static constexpr int FIXED = TAB + QF + SQ + XCH + 256;
   static_assert(LEV * 4 <= QF, "the code words fit in the fragment area");
   static constexpr int NS0 = (kTqmSmemBudget - FIXED) / STAGE;
   static constexpr int NS = NS0 < kTqmMaxStages ? NS0 : kTqmMaxStages;
   static constexpr size_t SMEM = 1024 + (size_t)NS * STAGE + FIXED;
   static constexpr int THREADS = (NC + 1) * 32;
   static_assert(NS >= 2, "two stages at least");
-  static_assert(NC * 8 * RS * 4 <= NS * STAGE, "the warps' records fit in the stages");
+  static_assert(KG * 8 * RS * 4 <= NS * STAGE, "the groups' records fit in the stages");
+  static_assert(QW == 1 || !KRAW, "raw keys: one warp per key group");
+  static_assert(DPW % (SBITS == 8 ? 32 : 64) == 0 && BLK % DPW == 0,
+                "a warp's dims: whole code groups inside one norm block");
   static_assert(8 * kTqmMaxSplits * 4 <= NS * STAGE, "the merge weights fit in the stages");
   static_assert(SMEM <= 232448, "shared memory per CTA");
 };
@@ -171,7 +189,9 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
   uint32_t* s_tab = reinterpret_cast<uint32_t*>(smem + NS * Cfg::STAGE);
   uint4* qf = reinterpret_cast<uint4*>(smem + NS * Cfg::STAGE + Cfg::TAB);
   float* s_q = reinterpret_cast<float*>(smem + NS * Cfg::STAGE + Cfg::TAB + Cfg::QF);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * Cfg::STAGE + Cfg::TAB + Cfg::QF + Cfg::SQ);
+  float4* s_x = reinterpret_cast<float4*>(smem + NS * Cfg::STAGE + Cfg::TAB + Cfg::QF + Cfg::SQ);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * Cfg::STAGE + Cfg::TAB + Cfg::QF +
+                                               Cfg::SQ + Cfg::XCH);
   uint64_t* empty = full + NS;
   int* s_flags = reinterpret_cast<int*>(empty + NS);  // [0] abort, [1] issued, [2] last
 
@@ -269,11 +289,13 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
       // the norms of the stage's keys (past the chunk: its last key, never used)
       float* nd = reinterpret_cast<float*>(sb + Cfg::NORM_OFF);
       const int kb0 = k_begin + i * T;
-      for (int j = lane; j < T; j += 32) {
+      constexpr int NB = Cfg::NB;
+      for (int e = lane; e < T * NB; e += 32) {
+        const int j = e / NB, bk = e - j * NB;
         const int key = kb0 + j < k_end ? kb0 + j : k_end - 1;
-        const size_t r = (size_t)unit * a.C + key;
-        if (!KRAW) cp_async_4(nd + j, a.k_norms + r);
-        cp_async_4(nd + (KRAW ? 0 : T) + j, a.v_norms + r);
+        const size_t r = ((size_t)unit * a.C + key) * NB + bk;
+        if (!KRAW) cp_async_4(nd + e, a.k_norms + r);
+        cp_async_4(nd + (KRAW ? 0 : T * NB) + e, a.v_norms + r);
       }
       cp_async_arrive_noinc(&full[st]);
       issued = i + 1;
@@ -290,7 +312,7 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
     }
     csync();
     if (!KRAW) {  // the query in the keys' rotated domain: one warp per head
-      for (int h = warp; h < G; h += NC) tq_fwht_warp<HD>(s_q + h * HD, lane);
+      for (int r = warp; r < G * Cfg::NB; r += NC) tq_fwht_warp<Cfg::BLK>(s_q + r * Cfg::BLK, lane);
       csync();
     }
     // query fragments: A rows 0..G-1 = hi(q), rows 8..8+G-1 = lo(q), k in the codes' order
@@ -316,15 +338,22 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
     for (int i = 0; i < Cfg::NTO; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     const uint32_t tab = smem_u32(s_tab) + lane * Cfg::EB;
     const uint32_t stage_base = smem_u32(stages);
-    const int krow = warp * 16;
+    const int kgp = warp / Cfg::QW, qd = warp - kgp * Cfg::QW;  // key group, dim quarter
+    const int krow = kgp * 16;
+    constexpr int NB = Cfg::NB, DPW = Cfg::DPW;
+    const int blkw = qd * DPW / Cfg::BLK;  // the norm block of the warp's dims
 
     for (int i = 0; i < ntiles; ++i) {
       const int st = i % NS;
-      if (*(volatile int*)&s_flags[0]) break;
-      if (!mbar_wait(&full[st], (i / NS) & 1, a.err, &s_flags[0])) {
+      // a warp of a key group with partners leaves the loop only together with them, after
+      // the group's barrier of the stage (a warp left alone at that barrier would wait for
+      // ever); a failed wait still marks the stage bad
+      bool ok = !*(volatile int*)&s_flags[0];
+      if (ok && !mbar_wait(&full[st], (i / NS) & 1, a.err, &s_flags[0])) {
         atomicExch(&s_flags[0], 1);
-        break;
+        ok = false;
       }
+      if (Cfg::QW == 1 && !ok) break;
       const uint32_t kb = stage_base + st * Cfg::STAGE;
       const uint32_t vb = kb + Cfg::KTILE;
       const float* nrm = reinterpret_cast<const float*>(stages + st * Cfg::STAGE + Cfg::NORM_OFF);
@@ -346,7 +375,8 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
         }
       } else if constexpr (SBITS == 8) {
 #pragma unroll
-        for (int ks = 0; ks < Cfg::KS; ++ks) {
+        for (int kw = 0; kw < Cfg::KSW; ++kw) {
+          const int ks = qd * Cfg::KSW + kw;
           const uint32_t w0 = lds32(code_addr<Cfg>(kb, krow + g, 16 * ks + 4 * t));
           const uint32_t w1 = lds32(code_addr<Cfg>(kb, krow + 8 + g, 16 * ks + 4 * t));
           const uint4 qa = qf[ks * 32 + lane];
@@ -358,7 +388,8 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
         // byte j of a code word = the codes of k = 2t, 2t + 1 (j even) or 2t + 8, 2t + 9
         // (j odd) of k16 step 2 mw + j / 2: one table entry gives both operand words
 #pragma unroll
-        for (int mw = 0; mw < HD / 32; ++mw) {
+        for (int mx = 0; mx < DPW / 32; ++mx) {
+          const int mw = qd * (DPW / 32) + mx;
           const uint32_t w0 = lds32(code_addr<Cfg>(kb, krow + g, 16 * mw + 4 * t));
           const uint32_t w1 = lds32(code_addr<Cfg>(kb, krow + 8 + g, 16 * mw + 4 * t));
 #pragma unroll
@@ -382,10 +413,44 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
       const int kidx0 = k_begin + i * T + kl0;
       bool valid[4];
 #pragma unroll
+      if constexpr (Cfg::QW > 1) {
+        // the key group's warps hold the partial sums of their dims: exchange them (the
+        // buffer of this stage's parity: a warp writes it again two stages later, after the
+        // group's barrier of the stage between), then add each norm block's parts
+        int* s_ok = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(s_x) + Cfg::XFL);
+        const int xs = ((i & 1) * Cfg::KG + kgp) * Cfg::QW;
+        s_x[(xs + qd) * 32 + lane] = make_float4(sv[0], sv[1], sv[2], sv[3]);
+        if (lane == 0) s_ok[xs + qd] = ok ? 1 : 0;
+        asm volatile("bar.sync %0, %1;" ::"r"(2 + kgp), "n"(Cfg::QW * 32) : "memory");
+        bool all_ok = true;
+#pragma unroll
+        for (int q = 0; q < Cfg::QW; ++q) all_ok = all_ok && s_ok[xs + q] != 0;
+        if (!all_ok) break;  // the same decision in every warp of the group
+        float blk[NB][4];
+#pragma unroll
+        for (int bk = 0; bk < NB; ++bk) blk[bk][0] = blk[bk][1] = blk[bk][2] = blk[bk][3] = 0.f;
+#pragma unroll
+        for (int q = 0; q < Cfg::QW; ++q) {
+          const float4 x = s_x[(((i & 1) * Cfg::KG + kgp) * Cfg::QW + q) * 32 + lane];
+          const int bk = q * DPW / Cfg::BLK;
+          blk[bk][0] += x.x;
+          blk[bk][1] += x.y;
+          blk[bk][2] += x.z;
+          blk[bk][3] += x.w;
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int dk = (e & 1) + ((e >> 1) << 3);
+          float sc = 0.f;
+#pragma unroll
+          for (int bk = 0; bk < NB; ++bk) sc += blk[bk][e] * nrm[(kl0 + dk) * NB + bk];
+          sv[e] = sc;
+        }
+      }
       for (int e = 0; e < 4; ++e) {
         const int dk = (e & 1) + ((e >> 1) << 3);
         float s = sv[e];
-        if (!KRAW) s *= nrm[kl0 + dk];
+        if (!KRAW && Cfg::QW == 1) s *= nrm[kl0 + dk];
         if (a.cap_log2 != 0.f) s = a.cap_log2 * tanhf(s);
         valid[e] = kidx0 + dk < k_end;
         sv[e] = valid[e] ? s : -INFINITY;
@@ -417,7 +482,7 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int dk = (e & 1) + ((e >> 1) << 3);
-          const float pv = valid[e] ? p[e] * nrm[(KRAW ? 0 : T) + kl0 + dk] : 0.f;
+          const float pv = valid[e] ? p[e] * nrm[(KRAW ? 0 : T * NB) + (kl0 + dk) * NB + blkw] : 0.f;
           split_bf16(pv, h[e], lw[e]);
         }
         PA[0] = pack_bf2(h[0], h[1]);
@@ -429,18 +494,20 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
       // dims of its column; n8 tile j of a group holds the dims base + (4 or 8) col + j
       if constexpr (SBITS == 8) {
 #pragma unroll
-        for (int grp = 0; grp < HD / 32; ++grp) {
+        for (int gx = 0; gx < DPW / 32; ++gx) {
+          const int grp = qd * (DPW / 32) + gx;
           const int byte = grp * 32 + 4 * g;
           const uint32_t wA = lds32(code_addr<Cfg>(vb, krow + 2 * t, byte));
           const uint32_t wB = lds32(code_addr<Cfg>(vb, krow + 2 * t + 1, byte));
           const uint32_t wC = lds32(code_addr<Cfg>(vb, krow + 2 * t + 8, byte));
           const uint32_t wD = lds32(code_addr<Cfg>(vb, krow + 2 * t + 9, byte));
 #pragma unroll
-          for (int j = 0; j < 4; ++j) pv_tile8(o[grp * 4 + j], PA, tab, wA, wB, wC, wD, j);
+          for (int j = 0; j < 4; ++j) pv_tile8(o[gx * 4 + j], PA, tab, wA, wB, wC, wD, j);
         }
       } else {
 #pragma unroll
-        for (int grp = 0; grp < HD / 64; ++grp) {
+        for (int gx = 0; gx < DPW / 64; ++gx) {
+          const int grp = qd * (DPW / 64) + gx;
           const int byte = grp * 32 + 4 * g;
           const uint32_t wA = lds32(code_addr<Cfg>(vb, krow + 2 * t, byte));
           const uint32_t wB = lds32(code_addr<Cfg>(vb, krow + 2 * t + 1, byte));
@@ -456,8 +523,8 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
           for (int j = 0; j < 8; ++j) {
             const uint2 b0 = pair_ld(tab, (j & 1) ? xo : xe, j >> 1);
             const uint2 b1 = pair_ld(tab, (j & 1) ? yo : ye, j >> 1);
-            mma_bf16(o[grp * 8 + j], PA, b0.x, b1.x);
-            mma_bf16(o[grp * 8 + j], PA, b0.y, b1.y);
+            mma_bf16(o[gx * 8 + j], PA, b0.x, b1.x);
+            mma_bf16(o[gx * 8 + j], PA, b0.y, b1.y);
           }
         }
       }
@@ -470,10 +537,10 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
     // ------------------------------------------------- merge the consumer warps
     // every stage has been consumed (or the CTA aborted): reuse the stage buffers
     csync();
-    float* red = reinterpret_cast<float*>(stages);  // [warp][8][RS]
-    float* mine = red + warp * 8 * RS;
+    float* red = reinterpret_cast<float*>(stages);  // [key group][8][RS]
+    float* mine = red + kgp * 8 * RS;
     if (g < G) {
-      if (t == 0) {
+      if (t == 0 && qd == 0) {
         mine[g * RS + HD] = m;
         mine[g * RS + HD + 1] = l;
       }
@@ -482,10 +549,10 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
         // columns 2t, 2t + 1 of tile nt: the dims of the permuted order
         int d0, d1;
         if (SBITS == 8) {
-          d0 = (nt >> 2) * 32 + 8 * t + (nt & 3);
+          d0 = qd * DPW + (nt >> 2) * 32 + 8 * t + (nt & 3);
           d1 = d0 + 4;
         } else {
-          d0 = (nt >> 3) * 64 + 16 * t + (nt & 7);
+          d0 = qd * DPW + (nt >> 3) * 64 + 16 * t + (nt & 7);
           d1 = d0 + 8;
         }
         mine[g * RS + d0] = o[nt][0] + o[nt][2];
@@ -497,14 +564,14 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
       const int h = e / (HD + 2), d = e - h * (HD + 2);
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < NC; ++w) M = fmaxf(M, red[(w * 8 + h) * RS + HD]);
+      for (int w = 0; w < Cfg::KG; ++w) M = fmaxf(M, red[(w * 8 + h) * RS + HD]);
       const float Mu = M == -INFINITY ? 0.f : M;
       float acc = 0.f;
       if (d == HD) {
         acc = M;
       } else {
 #pragma unroll
-        for (int w = 0; w < NC; ++w)
+        for (int w = 0; w < Cfg::KG; ++w)
           acc += exp2f(red[(w * 8 + h) * RS + HD] - Mu) * red[(w * 8 + h) * RS + d];
       }
       part[h * RS + d] = acc;
@@ -521,16 +588,35 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
     }
   }
 
-  // ------------------------------------------------- the last chunk merges the unit
+  // ------------------------------------------------- the merge, in two levels
+  // the last chunk of each group folds the group's records; the last group of the unit
+  // merges the folds and rotates back (with one group, it merges the chunks themselves)
+  const int ng = (a.splits + a.group - 1) / a.group;
+  const int grp = split / a.group, g0 = grp * a.group;
+  const int gn = a.splits - g0 < a.group ? a.splits - g0 : a.group;
+  float* wsm = reinterpret_cast<float*>(stages);
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) s_flags[2] = atomicAdd(a.ticket + unit, 1) == a.splits - 1;
+  if (ng > 1) {
+    int* t1 = a.ticket1 + unit * kTqmMaxGroups + grp;
+    if (threadIdx.x == 0) s_flags[2] = atomicAdd(t1, 1) == gn - 1;
+    __syncthreads();
+    if (!s_flags[2]) return;
+    __threadfence();
+    if (threadIdx.x == 0) *t1 = 0;
+    tq_fold_records<HD>(a.part + ((size_t)unit * a.splits + g0) * 8 * RS, gn, G, wsm,
+                        a.part1 + ((size_t)unit * kTqmMaxGroups + grp) * 8 * RS);
+    __threadfence();
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) s_flags[2] = atomicAdd(a.ticket + unit, 1) == ng - 1;
   __syncthreads();
   if (!s_flags[2]) return;
   __threadfence();
   if (threadIdx.x == 0) a.ticket[unit] = 0;
-  const float* up = a.part + (size_t)unit * a.splits * 8 * RS;
-  tq_merge_records<HD>(up, a.splits, G, reinterpret_cast<float*>(stages), s_q, a.signs,
+  const float* up = ng > 1 ? a.part1 + (size_t)unit * kTqmMaxGroups * 8 * RS
+                           : a.part + (size_t)unit * a.splits * 8 * RS;
+  tq_merge_records<HD>(up, ng > 1 ? ng : a.splits, G, wsm, s_q, a.signs,
                        a.o + ((size_t)b * a.nh + kvh * G) * HD);
 }
 
@@ -565,18 +651,23 @@ cudaError_t launch_hd(const TqAttnArgs& a, const CUtensorMap& tk, const CUtensor
 
 }  // namespace
 
-bool tq_mma_supported(int hd, int sbits) {
-  return (hd == 64 || hd == 128 || hd == 256) && (sbits == 4 || sbits == 8);
+bool tq_mma_supported(int hd, int sbits, bool kraw) {
+  return (hd == 64 || hd == 128 || hd == 256 || (hd == 512 && !kraw)) && (sbits == 4 || sbits == 8);
 }
-int tq_mma_keys_per_stage(int hd) { return hd >= 256 ? 64 : 176; }
-int tq_mma_threads(int hd) { return (tq_mma_keys_per_stage(hd) / 16 + 1) * 32; }
+int tq_mma_keys_per_stage(int hd) { return hd >= 512 ? 32 : (hd >= 256 ? 64 : 176); }
+int tq_mma_threads(int hd) { return hd >= 512 ? 288 : (tq_mma_keys_per_stage(hd) / 16 + 1) * 32; }
 
 cudaError_t launch_tq_attn_mma(const TqAttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                                int hd, int sbits, bool kraw, int grid, cudaStream_t s) {
-  if (a.splits > kTqmMaxSplits) return cudaErrorInvalidValue;
+  if (a.splits > kTqmMaxSplits || a.group < 1 ||
+      (a.splits + a.group - 1) / a.group > kTqmMaxGroups)
+    return cudaErrorInvalidValue;
   if (hd == 64) return launch_hd<64>(a, tk, tv, sbits, kraw, grid, s);
   if (hd == 128) return launch_hd<128>(a, tk, tv, sbits, kraw, grid, s);
-  return launch_hd<256>(a, tk, tv, sbits, kraw, grid, s);
+  if (hd == 256) return launch_hd<256>(a, tk, tv, sbits, kraw, grid, s);
+  if (kraw) return cudaErrorInvalidValue;  // raw keys at hd 512: the CUDA-core kernel
+  return sbits == 8 ? launch_t<512, 8, false>(a, tk, tv, grid, s)
+                    : launch_t<512, 4, false>(a, tk, tv, grid, s);
 }
 
 }  // namespace hfa

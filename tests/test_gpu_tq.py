@@ -144,7 +144,8 @@ def test_attention_over_codes_32k_context_8bit():
     _run_tq_attention(w, 8, [32767], seed=21)
 
 
-@pytest.mark.parametrize("hd,bits", [(64, 4), (128, 4), (256, 8), (512, 4), (128, 5), (64, 6)])
+@pytest.mark.parametrize("hd,bits", [(64, 4), (128, 4), (256, 8), (512, 4), (512, 8), (128, 5),
+                                     (64, 6), (512, 6)])
 def test_attention_over_codes_head_dims(hd, bits):
     nh = 16 if hd == 512 else 8
     w = wl.Workload(name=f"tq{hd}", hidden=256, num_heads=nh, num_kv_heads=2, head_dim=hd,
@@ -183,6 +184,22 @@ def test_group_of_eight_4bit_values(hybrid):
                     layer_type=wl.FULL, window=0, kv_capacity=3000, ring=False, batch=2,
                     rope_theta=1e6, seed=26)
     _run_tq_attention(w, 4, [2999, 77], hybrid=hybrid, seed=34)
+
+
+def test_hybrid_raw_keys_head_dim_512():
+    # raw keys at hd 512 (two norm blocks per value row): the CUDA-core kernel
+    w = wl.Workload(name="tq_hyb512", hidden=256, num_heads=16, num_kv_heads=2, head_dim=512,
+                    layer_type=wl.FULL, window=0, kv_capacity=700, ring=False, batch=2,
+                    rope_theta=1e6, seed=27)
+    _run_tq_attention(w, 8, [699, 40], hybrid=True, seed=35)
+
+
+def test_global_layer_shape_32k_context_4bit():
+    # the pages' global layer with a coded cache: 16 query heads over 2 KV heads, hd 512
+    w = wl.Workload(name="tq_global", hidden=256, num_heads=16, num_kv_heads=2, head_dim=512,
+                    layer_type=wl.FULL, window=0, kv_capacity=32768, ring=False, batch=1,
+                    rope_theta=1e6, seed=28)
+    _run_tq_attention(w, 4, [32767], seed=36)
 
 
 @pytest.mark.parametrize("bits", [4, 6, 8])
