@@ -74,57 +74,116 @@ __device__ __forceinline__ void tq_fwht_warp(float* v, int lane) {
   for (int j = 0; j < R; ++j) v[lane * R + j] = x[j] * sc;
 }
 
-// Folds n chunk records at `up` ([n][8][HD + 4]: O, m, l) into one record at `dst` of the
-// same form: m = max m_s, l = sum 2^(m_s - m) l_s, O = sum 2^(m_s - m) O_s (not normalised,
-// so folds compose), the records added in order.  Every thread of the CTA calls it; wsm
-// holds G x n floats of shared memory.
-template <int HD>
-__device__ void tq_fold_records(const float* up, int n, int G, float* wsm, float* dst) {
-  constexpr int RS = HD + 4;
-  const int tid = threadIdx.x, nthr = blockDim.x;
-  const int warp = tid >> 5, lane = tid & 31, nw = nthr >> 5;
-  for (int h = warp; h < G; h += nw) {
-    float M = -INFINITY;
-    for (int sp = lane; sp < n; sp += 32) M = fmaxf(M, __ldcg(up + (sp * 8 + h) * RS + HD));
+// Columns of chunk records ([n][8][HD + 4]: O, m, l; column c = head c / (HD / 4), dims
+// 4 (c mod (HD / 4)) ..): the thread's columns are c = tid + k nthr (k < CPT).  A batch is
+// four records' values of all of them, loaded together; batches are added in record order.
+template <int HD, int CPT>
+__device__ __forceinline__ void tq_load_columns(const float* up, int n, int sp0, int G,
+                                                float4 (&v)[CPT][4], int tid, int nthr) {
+  constexpr int RS = HD + 4, Q4 = HD / 4;
+  const int ncol = G * Q4;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    const float Mu = M == -INFINITY ? 0.f : M;
-    float l = 0.f;
-    for (int sp = lane; sp < n; sp += 32) {
-      const float f = exp2f(__ldcg(up + (sp * 8 + h) * RS + HD) - Mu);
-      wsm[h * n + sp] = f;
-      l += f * __ldcg(up + (sp * 8 + h) * RS + HD + 1);
-    }
-    l = warp_sum(l);
-    if (lane == 0) {
-      dst[h * RS + HD] = M;
-      dst[h * RS + HD + 1] = l;
+  for (int k = 0; k < CPT; ++k) {
+    const int c = tid + k * nthr < ncol ? tid + k * nthr : ncol - 1;  // in range
+    const int h = c / Q4, d4 = c - h * Q4;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int sp = sp0 + u < n ? sp0 + u : n - 1;  // in range
+      v[k][u] = __ldcg(reinterpret_cast<const float4*>(up + (sp * 8 + h) * RS) + d4);
     }
   }
-  __syncthreads();
+}
+template <int HD, int CPT>
+__device__ __forceinline__ void tq_add_columns(const float4 (&v)[CPT][4], int n, int sp0, int G,
+                                               const float* wsm, float4 (&acc)[CPT], int tid,
+                                               int nthr) {
   constexpr int Q4 = HD / 4;
-  for (int c = tid; c < G * Q4; c += nthr) {
-    const int h = c / Q4, d4 = c - h * Q4;
-    float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int sp0 = 0; sp0 < n; sp0 += 8) {
-      float4 v[8];
+  const int ncol = G * Q4;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int sp = sp0 + u < n ? sp0 + u : n - 1;  // in range
-        v[u] = __ldcg(reinterpret_cast<const float4*>(up + (sp * 8 + h) * RS) + d4);
-      }
+  for (int k = 0; k < CPT; ++k) {
+    const int c = tid + k * nthr;
+    if (c < ncol) {
+      const int h = c / Q4;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < 4; ++u) {
         if (sp0 + u < n) {
           const float w = wsm[h * n + sp0 + u];
-          acc4.x = fmaf(w, v[u].x, acc4.x);
-          acc4.y = fmaf(w, v[u].y, acc4.y);
-          acc4.z = fmaf(w, v[u].z, acc4.z);
-          acc4.w = fmaf(w, v[u].w, acc4.w);
+          acc[k].x = fmaf(w, v[k][u].x, acc[k].x);
+          acc[k].y = fmaf(w, v[k][u].y, acc[k].y);
+          acc[k].z = fmaf(w, v[k][u].z, acc[k].z);
+          acc[k].w = fmaf(w, v[k][u].w, acc[k].w);
         }
       }
     }
-    reinterpret_cast<float4*>(dst + h * RS)[d4] = acc4;
+  }
+}
+
+// The per-head weights of n records: wsm[h n + sp] = 2^(m_sp - M) (times `norm` ? 1 / den :
+// 1), M = max m_sp, den = sum 2^(m_sp - M) l_sp; every m and l of a head loaded in one
+// round (up to 256 records).  One warp per head; returns nothing, writes M and den through
+// the callback of the head's lane 0.
+template <int HD, typename OnHead>
+__device__ __forceinline__ void tq_record_weights(const float* up, int n, int G, float* wsm,
+                                                  bool norm, OnHead on_head) {
+  constexpr int RS = HD + 4;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
+  for (int h = warp; h < G; h += nw) {
+    float mv[8], lv[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int sp = lane + 32 * k;
+      mv[k] = sp < n ? __ldcg(up + (sp * 8 + h) * RS + HD) : -INFINITY;
+      lv[k] = sp < n ? __ldcg(up + (sp * 8 + h) * RS + HD + 1) : 0.f;
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) M = fmaxf(M, mv[k]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float Mu = M == -INFINITY ? 0.f : M;
+    float f[8], den = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      f[k] = exp2f(mv[k] - Mu);
+      den += f[k] * lv[k];
+    }
+    den = warp_sum(den);
+    const float inv = norm ? (den > 0.f ? 1.f / den : 0.f) : 1.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (lane + 32 * k < n) wsm[h * n + lane + 32 * k] = f[k] * inv;
+    if (lane == 0) on_head(h, M, den);
+  }
+}
+
+// Folds n chunk records at `up` ([n][8][HD + 4]: O, m, l) into one record at `dst` of the
+// same form: m = max m_s, l = sum 2^(m_s - m) l_s, O = sum 2^(m_s - m) O_s (not normalised,
+// so folds compose), the records added in order.  Every thread of the CTA (NTHR of them)
+// calls it; wsm holds G x n floats of shared memory.  The first records' columns are in
+// flight while the weights are formed.
+template <int HD, int NTHR>
+__device__ void tq_fold_records(const float* up, int n, int G, float* wsm, float* dst) {
+  constexpr int RS = HD + 4, Q4 = HD / 4, CPT = (8 * Q4 + NTHR - 1) / NTHR;
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  float4 v[CPT][4];
+  tq_load_columns<HD, CPT>(up, n, 0, G, v, tid, nthr);
+  tq_record_weights<HD>(up, n, G, wsm, false, [&](int h, float M, float den) {
+    dst[h * RS + HD] = M;
+    dst[h * RS + HD + 1] = den;
+  });
+  __syncthreads();
+  float4 acc[CPT];
+#pragma unroll
+  for (int k = 0; k < CPT; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  tq_add_columns<HD, CPT>(v, n, 0, G, wsm, acc, tid, nthr);
+  for (int sp0 = 4; sp0 < n; sp0 += 4) {
+    tq_load_columns<HD, CPT>(up, n, sp0, G, v, tid, nthr);
+    tq_add_columns<HD, CPT>(v, n, sp0, G, wsm, acc, tid, nthr);
+  }
+#pragma unroll
+  for (int k = 0; k < CPT; ++k) {
+    const int c = tid + k * nthr;
+    if (c < G * Q4) reinterpret_cast<float4*>(dst + (c / Q4) * RS)[c % Q4] = acc[k];
   }
 }
 
@@ -132,59 +191,32 @@ __device__ void tq_fold_records(const float* up, int n, int G, float* wsm, float
 // O in the rotated domain, then m and l in base-2 units) combined with the weights
 // 2^(m_s - M) / sum_s' 2^(m_s' - M) l_s', the chunks added in order, then rotated back
 // (the normalised FWHT is its own inverse; then the signs) into o ([G][HD]).  wsm holds
-// G x splits floats and s_o G x HD floats of shared memory; every thread of the CTA calls
-// it.
-template <int HD>
+// G x splits floats and s_o G x HD floats of shared memory; every thread of the CTA (NTHR
+// of them) calls it.
+template <int HD, int NTHR>
 __device__ void tq_merge_records(const float* up, int splits, int G, float* wsm, float* s_o,
                                  const float* signs, float* o) {
-  constexpr int RS = HD + 4;
   constexpr int BLK = HD < 256 ? HD : 256;
+  constexpr int Q4 = HD / 4, CPT = (8 * Q4 + NTHR - 1) / NTHR;
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int warp = tid >> 5, lane = tid & 31, nw = nthr >> 5;
-  for (int h = warp; h < G; h += nw) {
-    float M = -INFINITY;
-    for (int sp = lane; sp < splits; sp += 32) M = fmaxf(M, __ldcg(up + (sp * 8 + h) * RS + HD));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    const float Mu = M == -INFINITY ? 0.f : M;
-    float den = 0.f;
-    for (int sp = lane; sp < splits; sp += 32) {
-      const float f = exp2f(__ldcg(up + (sp * 8 + h) * RS + HD) - Mu);
-      wsm[h * splits + sp] = f;
-      den += f * __ldcg(up + (sp * 8 + h) * RS + HD + 1);
-    }
-    den = warp_sum(den);
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-    __syncwarp();
-    for (int sp = lane; sp < splits; sp += 32) wsm[h * splits + sp] *= inv;
-  }
+  float4 v[CPT][4];
+  tq_load_columns<HD, CPT>(up, splits, 0, G, v, tid, nthr);
+  tq_record_weights<HD>(up, splits, G, wsm, true, [](int, float, float) {});
   __syncthreads();
-  // o[h][i] = sum_s w[h][s] O_s[h][i]: one float4 column per thread, the chunks added in
-  // order, eight loads in flight at a time
-  constexpr int Q4 = HD / 4;
-  const int ncol = G * Q4;
-  for (int c = tid; c < ncol; c += nthr) {
-    const int h = c / Q4, d4 = c - h * Q4;
-    float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int sp0 = 0; sp0 < splits; sp0 += 8) {
-      float4 v[8];
+  // o[h][i] = sum_s w[h][s] O_s[h][i], the chunks added in order
+  float4 acc[CPT];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int sp = sp0 + u < splits ? sp0 + u : splits - 1;  // in range
-        v[u] = __ldcg(reinterpret_cast<const float4*>(up + (sp * 8 + h) * RS) + d4);
-      }
+  for (int k = 0; k < CPT; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  tq_add_columns<HD, CPT>(v, splits, 0, G, wsm, acc, tid, nthr);
+  for (int sp0 = 4; sp0 < splits; sp0 += 4) {
+    tq_load_columns<HD, CPT>(up, splits, sp0, G, v, tid, nthr);
+    tq_add_columns<HD, CPT>(v, splits, sp0, G, wsm, acc, tid, nthr);
+  }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (sp0 + u < splits) {
-          const float w = wsm[h * splits + sp0 + u];
-          acc4.x = fmaf(w, v[u].x, acc4.x);
-          acc4.y = fmaf(w, v[u].y, acc4.y);
-          acc4.z = fmaf(w, v[u].z, acc4.z);
-          acc4.w = fmaf(w, v[u].w, acc4.w);
-        }
-      }
-    }
-    reinterpret_cast<float4*>(s_o)[c] = acc4;
+  for (int k = 0; k < CPT; ++k) {
+    const int c = tid + k * nthr;
+    if (c < G * Q4) reinterpret_cast<float4*>(s_o)[c] = acc[k];
   }
   __syncthreads();
   for (int r = warp; r < G * (HD / BLK); r += nw) tq_fwht_warp<BLK>(s_o + r * BLK, lane);

@@ -491,7 +491,7 @@ __global__ void __launch_bounds__(kTqThreads) tq_attn_kernel(const TqAttnArgs a)
   __threadfence();
   if (tid == 0) a.ticket[unit] = 0;
   const float* up = a.part + (size_t)unit * a.splits * 8 * RS;
-  tq_merge_records<HD>(up, a.splits, G, s_p, s_q, a.signs, a.o + ((size_t)b * a.nh + kvh * G) * HD);
+  tq_merge_records<HD, kTqThreads>(up, a.splits, G, s_p, s_q, a.signs, a.o + ((size_t)b * a.nh + kvh * G) * HD);
 }
 
 template <int HD, int BITS>
@@ -656,10 +656,11 @@ namespace {
 constexpr int kTqGroups = 16;
 size_t tq_ws_head(int units) { return ((size_t)(1 + units + units * kTqGroups) * 4 + 255) / 256 * 256; }
 size_t tq_ws_folds(int units, int hd) { return (size_t)units * kTqGroups * 8 * (hd + 4) * sizeof(float); }
-// splits per group of the two-level merge: one group (a single merge) up to 32 splits, where
-// the second ticket round would cost more than the merge saves; else about sqrt(splits)
-int tq_group(int S) {
-  if (S <= 32) return S;
+// splits per group of the two-level merge: one group (a single merge) while one CTA reads
+// at most 64 KB of records (the second ticket round would cost more than it saves); else
+// about sqrt(splits), so that each level reads a few records
+int tq_group(int S, int G, int hd) {
+  if (S <= 4 || (size_t)S * G * (hd + 4) * sizeof(float) <= 65536) return S;
   int g = 1;
   while (g * g < S) ++g;
   return g;
@@ -790,7 +791,7 @@ extern "C" hfa_status hfa_attention_decode_tq(const hfa_attn_desc* d, const hfa_
   a.ticket1 = (int*)ws + 1 + units;
   a.part = (float*)((char*)ws + tq_ws_head(units));
   a.part1 = a.part + (size_t)units * Sws * 8 * (hd + 4);
-  a.group = tq_group(S);
+  a.group = tq_group(S, nh / nkv, hd);
   a.o = o;
   a.B = batch;
   a.nh = nh;

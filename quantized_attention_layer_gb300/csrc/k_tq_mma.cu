@@ -305,10 +305,37 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
     // ------------------------------------------------------------- consumers
     const int ctid = threadIdx.x;
     auto csync = []() { consumer_bar<NCT>(); };
-    for (int e = ctid; e < 8 * HD; e += NCT) {
-      const int h = e / HD, i = e - h * HD;
-      const float qv = h < G ? a.q[((size_t)b * a.nh + kvh * G + h) * HD + i] * a.qscale : 0.f;
-      s_q[e] = KRAW ? qv : qv * __ldg(a.signs + i);
+    {
+      // the queries (scaled, and sign-multiplied for coded keys): 16-byte loads, all of a
+      // thread's in flight at once
+      constexpr int Q4 = HD / 4, QN = (8 * Q4 + NCT - 1) / NCT;
+      float4 qv[QN], sg[QN];
+#pragma unroll
+      for (int k = 0; k < QN; ++k) {
+        const int e = ctid + k * NCT, ee = e < 8 * Q4 ? e : 8 * Q4 - 1;
+        const int h = ee / Q4, i4 = ee - h * Q4;
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        qv[k] = h < G ? __ldg(reinterpret_cast<const float4*>(a.q + ((size_t)b * a.nh + kvh * G + h) * HD) + i4) : z;
+        sg[k] = KRAW ? make_float4(1.f, 1.f, 1.f, 1.f) : __ldg(reinterpret_cast<const float4*>(a.signs) + i4);
+      }
+#pragma unroll
+      for (int k = 0; k < QN; ++k) {
+        const int e = ctid + k * NCT;
+        if (e < 8 * Q4) {
+          float4 r;
+          r.x = qv[k].x * a.qscale;
+          r.y = qv[k].y * a.qscale;
+          r.z = qv[k].z * a.qscale;
+          r.w = qv[k].w * a.qscale;
+          if (!KRAW) {
+            r.x *= sg[k].x;
+            r.y *= sg[k].y;
+            r.z *= sg[k].z;
+            r.w *= sg[k].w;
+          }
+          reinterpret_cast<float4*>(s_q)[e] = r;
+        }
+      }
     }
     csync();
     if (!KRAW) {  // the query in the keys' rotated domain: one warp per head
@@ -560,21 +587,39 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
       }
     }
     csync();
-    for (int e = ctid; e < G * (HD + 2); e += NCT) {
-      const int h = e / (HD + 2), d = e - h * (HD + 2);
+    // per head: the key groups' weights 2^(m_w - M) into the records' pad words, m and l
+    // of the CTA's record
+    for (int h = ctid; h < G; h += NCT) {
       float M = -INFINITY;
 #pragma unroll
       for (int w = 0; w < Cfg::KG; ++w) M = fmaxf(M, red[(w * 8 + h) * RS + HD]);
       const float Mu = M == -INFINITY ? 0.f : M;
-      float acc = 0.f;
-      if (d == HD) {
-        acc = M;
-      } else {
+      float lsum = 0.f;
 #pragma unroll
-        for (int w = 0; w < Cfg::KG; ++w)
-          acc += exp2f(red[(w * 8 + h) * RS + HD] - Mu) * red[(w * 8 + h) * RS + d];
+      for (int w = 0; w < Cfg::KG; ++w) {
+        const float f = exp2f(red[(w * 8 + h) * RS + HD] - Mu);
+        red[(w * 8 + h) * RS + HD + 2] = f;
+        lsum += f * red[(w * 8 + h) * RS + HD + 1];
       }
-      part[h * RS + d] = acc;
+      part[h * RS + HD] = M;
+      part[h * RS + HD + 1] = lsum;
+    }
+    csync();
+    // O = sum_w f_w O_w, the groups in order, four dims a thread
+    constexpr int Q4 = HD / 4;
+    for (int e = ctid; e < G * Q4; e += NCT) {
+      const int h = e / Q4, d4 = e - h * Q4;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < Cfg::KG; ++w) {
+        const float f = red[(w * 8 + h) * RS + HD + 2];
+        const float4 x = reinterpret_cast<const float4*>(red + (w * 8 + h) * RS)[d4];
+        acc.x += f * x.x;
+        acc.y += f * x.y;
+        acc.z += f * x.z;
+        acc.w += f * x.w;
+      }
+      reinterpret_cast<float4*>(part + h * RS)[d4] = acc;
     }
   }
 
@@ -604,7 +649,7 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
     if (!s_flags[2]) return;
     __threadfence();
     if (threadIdx.x == 0) *t1 = 0;
-    tq_fold_records<HD>(a.part + ((size_t)unit * a.splits + g0) * 8 * RS, gn, G, wsm,
+    tq_fold_records<HD, Cfg::THREADS>(a.part + ((size_t)unit * a.splits + g0) * 8 * RS, gn, G, wsm,
                         a.part1 + ((size_t)unit * kTqmMaxGroups + grp) * 8 * RS);
     __threadfence();
     __syncthreads();
@@ -616,7 +661,7 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
   if (threadIdx.x == 0) a.ticket[unit] = 0;
   const float* up = ng > 1 ? a.part1 + (size_t)unit * kTqmMaxGroups * 8 * RS
                            : a.part + (size_t)unit * a.splits * 8 * RS;
-  tq_merge_records<HD>(up, ng > 1 ? ng : a.splits, G, wsm, s_q, a.signs,
+  tq_merge_records<HD, Cfg::THREADS>(up, ng > 1 ? ng : a.splits, G, wsm, s_q, a.signs,
                        a.o + ((size_t)b * a.nh + kvh * G) * HD);
 }
 
