@@ -254,6 +254,8 @@ hfa_status hfa_attention_decode_noalloc(const hfa_attn_desc* desc, void* stream,
  * j, 2j+1 in the high nibble.  A coded value decodes to centroid[code] * norm (rotated).
  *   head_dim in {64, 128, 256, 512}; bits in {4, 5, 6, 8};
  *   signs_host int8 [head_dim], each +1 or -1, copied.
+ * Synchronises the device: the format's tables are in device memory when it returns (the
+ * attention reads them before waiting for the kernels that precede it).
  * Errors: HFA_EINVAL, HFA_EUNSUPPORTED, HFA_EDEVICE, HFA_ENOMEM.
  */
 typedef struct hfa_tq hfa_tq;

@@ -576,6 +576,9 @@ extern "C" hfa_status hfa_tq_create(int head_dim, int bits, const int8_t* signs,
   if (e == cudaSuccess)
     e = cudaMemcpy(t->bounds, cb.bnd.data(), (t->levels - 1) * sizeof(double), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(t->signs, sg.data(), head_dim * sizeof(float), cudaMemcpyHostToDevice);
+  // a copy from pageable memory may return before its DMA lands, and the attention reads
+  // the centroids before its programmatic-dependency wait: the tables are complete first
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     cudaFree(t->centroids);
     cudaFree(t->bounds);

@@ -654,7 +654,9 @@ __global__ void __launch_bounds__(TqmCfg<HD, SBITS, KRAW>::THREADS, 1)
     __threadfence();
     __syncthreads();
   }
-  if (threadIdx.x == 0) s_flags[2] = atomicAdd(a.ticket + unit, 1) == ng - 1;
+  // the unit's ticket counts the folds (two levels) or the chunks (one)
+  const int arrivals = ng > 1 ? ng : a.splits;
+  if (threadIdx.x == 0) s_flags[2] = atomicAdd(a.ticket + unit, 1) == arrivals - 1;
   __syncthreads();
   if (!s_flags[2]) return;
   __threadfence();

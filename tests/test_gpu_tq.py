@@ -202,6 +202,37 @@ def test_global_layer_shape_32k_context_4bit():
     _run_tq_attention(w, 4, [32767], seed=36)
 
 
+@pytest.mark.parametrize("hd,nh,nkv", [(128, 32, 8), (512, 16, 2)])
+def test_repeated_calls_are_bit_identical(hd, nh, nkv):
+    # the chunk records are merged once, in a fixed order, by the last CTA of each unit
+    # (one level at hd 128 with 19 chunks, two levels at hd 512): every call gives the
+    # same bits, however the CTAs happen to finish
+    C, B, bits = 8192, 1, 8
+    w = wl.Workload(name="tq_det", hidden=256, num_heads=nh, num_kv_heads=nkv, head_dim=hd,
+                    layer_type=wl.FULL, window=0, kv_capacity=C, ring=False, batch=B,
+                    rope_theta=1e6, seed=29)
+    desc = hfa.attn_desc_for(w)
+    fmt = hfa.TqFormat(hd, bits, wl.make_tq_signs(hd, 37))
+    kc, kn = _synthetic_tq_cache(B, nkv, C, hd, bits, 38)
+    vc, vn = _synthetic_tq_cache(B, nkv, C, hd, bits, 39)
+    kc, kn, vc, vn = kc.cuda(), kn.cuda(), vc.cuda(), vn.cuda()
+    q = torch.randn((B, nh, hd), generator=torch.Generator().manual_seed(40)).cuda()
+    pos = np.array([C - 1], dtype=np.int32)
+    posd = torch.from_numpy(pos).cuda()
+    ws = torch.zeros(hfa.hfa_attention_tq_workspace_bytes(desc, B, C), dtype=torch.uint8,
+                     device="cuda")
+    outs = []
+    for _ in range(6):
+        o = torch.full((B, nh, hd), float("nan"), device="cuda")
+        fmt.hfa_attention_decode_tq(desc, q, posd, pos, kc, kn, None, vc, vn, ws, o)
+        torch.cuda.synchronize()
+        outs.append(o.cpu())
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int32), outs[0].view(torch.int32))
+    assert torch.isfinite(outs[0]).all()
+    fmt.destroy()
+
+
 @pytest.mark.parametrize("bits", [4, 6, 8])
 def test_encode_then_attend_matches_the_oracle_pipeline(bits):
     # f32 K/V rows appended one position at a time by the library's encoder, then attended;
