@@ -52,7 +52,7 @@ UNIT = "steps/s"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0
 EXTRA = ("tiny_sliding", "sliding_b16_ring1024", "full_b4_128k_softcap", "verify_l16_8k",
-         "global_hd512_32k", "drafter_l16_8k", "ffn_b1", "ffn_b16", "tq8_full_b1_32k",
+         "global_hd512_32k", "verify_global_hd512_32k", "drafter_l16_8k", "ffn_b1", "ffn_b16", "tq8_full_b1_32k",
          "tq4_full_b1_32k", "tq8_global_hd512_32k")
 # attention over a quantised (TurboQuant) KV cache: the attention shapes of the headline
 # layer (batch 1, 32/8 heads, head dim 128) and of the global layer (16/2 heads, head dim
@@ -480,16 +480,17 @@ def verify_workload(w, K, W, R, world):
             a[1] += cnt
         Lr.hfa_set_kernel_timing(False)
     H, qr, kr = w.hidden, w.q_rows, w.kv_rows
-    wqkv_bytes = (qr + 2 * kr) * H * 2
+    kv_proj = 1 if w.k_eq_v else 2  # k_eq_v layers have no V projection
+    wqkv_bytes = (qr + kv_proj * kr) * H * 2
     wo_bytes = H * qr * 2
     kv_bytes = (base + L) * w.num_kv_heads * w.head_dim * 2 * 2
     step_bytes = wqkv_bytes + wo_bytes + kv_bytes + 2 * L * H * 2
     if S:  # the context rows: the K and V weight rows read again, their K/V rows written
-        step_bytes += 2 * kr * H * 2 + S * H * 2 + S * 2 * kr * 2
+        step_bytes += kv_proj * kr * H * 2 + S * H * 2 + S * 2 * kr * 2
     peak, src = measured_peaks()
     g = kt.get("verify_qkv_gemm", [float("nan"), 1])
     g_us = g[0] / max(g[1], 1) * 1e3
-    flops = 2.0 * L * (qr + 2 * kr) * H
+    flops = 2.0 * L * (qr + kv_proj * kr) * H
     ms_per_step = ms / K
     res = {"ms_per_step": ms_per_step, "blocks_per_s": world * 1e3 / ms_per_step,
            "step_bytes": step_bytes, "step_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,

@@ -72,8 +72,7 @@ typedef struct {
                        multiples of 64 are supported (HFA_EUNSUPPORTED otherwise) */
   int num_heads;    /* query heads nh */
   int num_kv_heads; /* key/value heads nkv; nh % nkv == 0 and nh / nkv <= 8 */
-  int head_dim;     /* hd in {64, 128, 256, 512}; 512 (the global layers' width) for
-                       decode steps only: max_verify_len must then be 0 */
+  int head_dim;     /* hd in {64, 128, 256, 512}; 512 is the global layers' width */
   int layer_type;   /* hfa_layer_type */
   int window;       /* sliding window W (keys with P-W < p <= P visible); SLIDING only */
   float eps;        /* RMSNorm epsilon of the input norm and the per-head norms */

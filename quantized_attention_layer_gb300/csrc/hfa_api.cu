@@ -225,8 +225,6 @@ static hfa_status validate_desc(const hfa_layer_desc* d) {
   if (!step_hd(d->head_dim))
     return fail(nullptr, HFA_EUNSUPPORTED, "head_dim=%d (supported: 64, 128, 256, 512)",
                 d->head_dim);
-  if (d->head_dim == 512 && d->max_verify_len > 0)
-    return fail(nullptr, HFA_EUNSUPPORTED, "head_dim=512: decode steps only (max_verify_len 0)");
   if (d->layer_type != HFA_SLIDING && d->layer_type != HFA_FULL)
     return fail(nullptr, HFA_EINVAL, "layer_type=%d", d->layer_type);
   if (d->layer_type == HFA_SLIDING && d->window <= 0)

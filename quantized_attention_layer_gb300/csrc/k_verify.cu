@@ -20,10 +20,11 @@
 //  * attn_verify_tc_kernel (head_dim 128, tcgen05): one CTA per (KV head, key chunk);
 //    S = Qx K^T and O += Px Vt on the tensor cores with TMEM accumulators, the online
 //    softmax of each query split over the four threads that hold its two TMEM rows.
-//  * attn_verify_kernel (head_dim 64, 256; mma.sync): one CTA per (KV head, key chunk); a
-//    TMA producer warp streams K and V tiles, each consumer warp owns 8 query rows (bf16
-//    hi/lo in MMA rows g and g + 8) and takes every 64-key stage in one online-softmax
-//    update, with the causal / window mask of its rows.
+//  * attn_verify_kernel (head_dim 64, 256, 512; mma.sync): one CTA per (KV head, key
+//    chunk) -- two at head_dim 512, each accumulating half of the output dims; a TMA
+//    producer warp streams K and V tiles, each consumer warp owns 8 query rows (bf16 hi/lo
+//    in MMA rows g and g + 8) and takes every stage in online-softmax updates, with the
+//    causal / window mask of its rows.
 //    Both attention kernels write one (O, m, l) record per query row and CTA.
 //  * attn_verify_merge_kernel: the records of a KV head's chunks combined, a few query
 //    rows per CTA, into the f32 output and the o_proj activation operand.
@@ -66,7 +67,7 @@ constexpr int kVStages = 10;     // ring depth: 200 KB of copies in flight per S
 constexpr int kAStageBytes = kVM * kVK * 2;  // 16 KB weight tile
 constexpr int kBChunkBytes = kVN * kVK * 2;  // 4 KB activation chunk
 constexpr int kVStageBytes = kAStageBytes + kBChunkBytes;
-constexpr int kVTableBytes = 3 * 256 * 4;  // QKV epilogue: w_q, w_k, RoPE table (hd <= 256)
+constexpr int kVTableBytes = 3 * 512 * 4;  // QKV epilogue: w_q, w_k, RoPE table (hd <= 512)
 constexpr size_t kVGemmSmem = 1024 + (size_t)kVStages * kVStageBytes + 256 + kVTableBytes;
 
 struct VGemmArgs {
@@ -402,15 +403,25 @@ __global__ void __launch_bounds__(128, 1) verify_gemm_kernel(const VGemmArgs a) 
       const int hl = it / L, t = it - hl * L;
       const int hh = rows0 / hd + hl;
       float u[8];
-      split_sum_rows(hl * hd + lane, t, hd / 32, u);
+      split_sum_rows(hl * hd + lane, t, hd < 256 ? hd / 32 : 8, u);
       if (hd == 64) {
         float v[2] = {u[0], u[1]};
         finish_head_row<64>(g, hh, t, v, lane);
       } else if (hd == 128) {
         float v[4] = {u[0], u[1], u[2], u[3]};
         finish_head_row<128>(g, hh, t, v, lane);
-      } else {
+      } else if (hd == 256) {
         finish_head_row<256>(g, hh, t, u, lane);
+      } else {  // 512: the head's second 256 rows in a second polling round
+        float u2[8];
+        split_sum_rows(hl * hd + 256 + lane, t, 8, u2);
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          v[j] = u[j];
+          v[8 + j] = u2[j];
+        }
+        finish_head_row<512>(g, hh, t, v, lane);
       }
     }
   } else {
@@ -441,15 +452,24 @@ struct VAttnArgs {
   unsigned* err;
 };
 
+// A 512-wide head is shared by DH = 2 CTAs per (KV head, key chunk): both take the whole
+// scores (the same arithmetic on the same tiles, so the same m and l), each accumulates
+// the output over its OD = 256 dims and reads only that half of V; 32-key stages keep the
+// K tile, the V half and the query fragments inside one SM's shared memory.
 template <int HD>
 struct VACfg {
-  static constexpr int NS = HD >= 256 ? 2 : 3;  // stages (shared memory budget)
-  static constexpr int TILE = kVT * HD * 2;
-  static constexpr int STAGE = 2 * TILE;
+  static constexpr int VT = HD >= 512 ? 32 : kVT;  // keys per stage
+  static constexpr int OD = HD >= 512 ? 256 : HD;  // output dims per CTA
+  static constexpr int DH = HD / OD;               // CTAs per (KV head, key chunk)
+  static constexpr int NS = HD >= 256 ? 2 : 3;     // stages (shared memory budget)
+  static constexpr int KTILE = VT * HD * 2;
+  static constexpr int VTILE = VT * OD * 2;
+  static constexpr int STAGE = KTILE + VTILE;
   static constexpr int KS = HD / 16;
-  static constexpr int NTO = HD / 8;
+  static constexpr int NTO = OD / 8;
   static constexpr int KB = HD >= 256 ? 16 : 64;  // keys per online-softmax update (registers)
   static constexpr size_t SMEM = 1024 + (size_t)NS * STAGE + 8 * KS * 32 * 16 + 256;
+  static_assert(SMEM <= 232448, "stages and query fragments exceed one CTA's shared memory");
 };
 
 
@@ -471,7 +491,9 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
   const int nc = (blockDim.x >> 5) - 1;  // consumer warps, 8 query rows each
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  const int kvh = blockIdx.x / a.splits, split = blockIdx.x - kvh * a.splits;
+  constexpr int VT = Cfg::VT;
+  const int unit = blockIdx.x / Cfg::DH, half = blockIdx.x - unit * Cfg::DH;
+  const int kvh = unit / a.splits, split = unit - kvh * a.splits;
   const int NQ = a.L * a.G;
 
   if (threadIdx.x == 0) {
@@ -489,10 +511,10 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
   int k_end = k_begin + a.chunk;
   if (k_end > a.khi + 1) k_end = a.khi + 1;
   const int nkeys = k_end > k_begin ? k_end - k_begin : 0;
-  const int ntiles = (nkeys + kVT - 1) / kVT;
+  const int ntiles = (nkeys + VT - 1) / VT;
   const int row0 = kvh * a.C + k_begin;
   constexpr int RS = HD + 4;
-  float* part = a.part + ((size_t)kvh * a.splits + split) * 64 * RS;
+  float* part = a.part + (size_t)unit * 64 * RS;
 
   if (warp == nc) {
     if (lane == 0) {
@@ -502,7 +524,7 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
       bool waited = false;
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % NS;
-        if (!waited && (i >= NS || k_begin + (i + 1) * kVT > a.base)) {
+        if (!waited && (i >= NS || k_begin + (i + 1) * VT > a.base)) {
           pdl_wait();
           waited = true;
         }
@@ -514,10 +536,12 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
         uint8_t* kt = stages + st * Cfg::STAGE;
         mbar_arrive_expect_tx(&full[st], Cfg::STAGE);
 #pragma unroll
-        for (int j = 0; j < HD / 64; ++j) {
-          tma_load_2d(kt + j * kVT * 128, &tmk, &full[st], 64 * j, row0 + i * kVT);
-          tma_load_2d(kt + Cfg::TILE + j * kVT * 128, &tmv, &full[st], 64 * j, row0 + i * kVT);
-        }
+        for (int j = 0; j < HD / 64; ++j)
+          tma_load_2d(kt + j * VT * 128, &tmk, &full[st], 64 * j, row0 + i * VT);
+#pragma unroll
+        for (int j = 0; j < Cfg::OD / 64; ++j)
+          tma_load_2d(kt + Cfg::KTILE + j * VT * 128, &tmv, &full[st], half * Cfg::OD + 64 * j,
+                      row0 + i * VT);
         issued = i + 1;
       }
       if (!waited) pdl_wait();
@@ -556,8 +580,8 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
 #pragma unroll
     for (int i = 0; i < Cfg::NTO; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     const uint32_t stage_base = smem_u32(stages);
-    // A K or V stage holds HD / 64 boxes of 64 keys x 128 bytes: 16-byte chunk c of key
-    // row r sits at (c / 8) * 8 KB + r * 128 + ((c % 8) XOR (r % 8)) * 16.  The lane parts
+    // A K (V) tile holds HD / 64 (OD / 64) boxes of VT keys x 128 bytes: 16-byte chunk c
+    // of key row r sits at (c / 8) * VT * 128 + r * 128 + ((c % 8) XOR (r % 8)) * 16.  The lane parts
     // of the ldmatrix addresses (the compile-time row and chunk terms split off): the K
     // fragments read row 16 kg + (lane / 16) 8 + lane % 8,
     // chunk 2 ks + (lane / 8) % 2; the V fragments row 16 kk + ((lane / 8) % 2) 8 + lane % 8,
@@ -583,10 +607,10 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
         break;
       }
       const uint32_t kb0 = stage_base + st * Cfg::STAGE;
-      const uint32_t vb0 = kb0 + Cfg::TILE;
+      const uint32_t vb0 = kb0 + Cfg::KTILE;
 #pragma unroll 1
-      for (int hb = 0; hb < kVT; hb += KB) {
-      const int key_lo = k_begin + i * kVT + hb, key_hi = key_lo + KB - 1;
+      for (int hb = 0; hb < VT; hb += KB) {
+      const int key_lo = k_begin + i * VT + hb, key_hi = key_lo + KB - 1;
       if (key_lo >= k_end) break;
       // scores of KB keys, KB / 8 independent accumulator chains: n-tile j holds keys
       // 8j .. 8j + 7, rows g (q hi) and g + 8 (q lo)
@@ -600,7 +624,7 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
 #pragma unroll
         for (int kg = 0; kg < KB / 16; ++kg) {
           uint32_t b0, b1, b2, b3;
-          ldmatrix_x4(kb0 + swk[ks & 3] + (uint32_t)((ks >> 2) * (kVT * 128) + (hb + kg * 16) * 128),
+          ldmatrix_x4(kb0 + swk[ks & 3] + (uint32_t)((ks >> 2) * (VT * 128) + (hb + kg * 16) * 128),
                       b0, b1, b2, b3);
           mma_bf16(s[2 * kg], A, b0, b1);
           mma_bf16(s[2 * kg + 1], A, b2, b3);
@@ -675,7 +699,7 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
         for (int np = 0; np < Cfg::NTO / 2; ++np) {
           uint32_t b0, b1, b2, b3;
           ldmatrix_x4_trans(
-              vb0 + swv[np & 3] + (uint32_t)((np >> 2) * (kVT * 128) + (hb + kk * 16) * 128),
+              vb0 + swv[np & 3] + (uint32_t)((np >> 2) * (VT * 128) + (hb + kk * 16) * 128),
               b0, b1, b2, b3);
           if (tail) {
             b0 &= mlo;
@@ -695,7 +719,8 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
     l += __shfl_xor_sync(0xffffffffu, l, 2);
     if (qvalid) {
       float* pr = part + (size_t)qrow * RS;
-      if (t == 0) *reinterpret_cast<float2*>(pr + HD) = make_float2(m, l);
+      if (t == 0 && half == 0) *reinterpret_cast<float2*>(pr + HD) = make_float2(m, l);
+      pr += half * Cfg::OD;
 #pragma unroll
       for (int nt = 0; nt < Cfg::NTO; ++nt)
         *reinterpret_cast<float2*>(pr + nt * 8 + 2 * t) =
@@ -1090,17 +1115,20 @@ __global__ void __launch_bounds__(vtc::THREADS, 1)
 }
 
 // Combination of the block attention's split records, one CTA per RPW = 256 / HD query
-// rows of one KV head (the lanes of a row own 8 output columns each):
+// rows of one KV head (one row at HD 512; the lanes of a row own CPL = 8 output columns
+// each, 16 at HD 512):
 //   M = max_s m_s,  w_s = 2^(m_s - M),  o = sum_s w_s O_s / sum_s w_s l_s.
 // The (m, l) pairs go through shared memory; the four warps each sum a quarter of the
 // splits (their records loaded in the same round as the pairs) and the partial sums are
 // added in warp order, so the result does not depend on timing.  The output is written twice: f32 o, and the o_proj GEMM's activation operand.
 template <int HD>
 __global__ void __launch_bounds__(128) attn_verify_merge_kernel(const VAttnArgs a) {
-  constexpr int LPR = HD / 8;    // lanes per query row
-  constexpr int RPW = 32 / LPR;  // query rows per CTA
+  constexpr int CPL = HD <= 256 ? 8 : HD / 32;  // output columns per lane
+  constexpr int NV = CPL / 4;                   // float4 of a record per lane
+  constexpr int LPR = HD / CPL;                 // lanes per query row
+  constexpr int RPW = 32 / LPR;                 // query rows per CTA
   constexpr int RS = HD + 4;
-  __shared__ float4 s_acc[4][32][2];
+  __shared__ float4 s_acc[4][32][NV];
   extern __shared__ float2 s_ml[];  // [RPW][splits]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kvh = blockIdx.y;
@@ -1114,21 +1142,21 @@ __global__ void __launch_bounds__(128) attn_verify_merge_kernel(const VAttnArgs 
   pdl_launch_dependents();
   // every load in one round: the (m, l) pairs into shared memory, and this warp's first
   // MB records (splits warp, warp + 4, ...) into registers
-  constexpr int MB = 12;
+  constexpr int MB = 24 / NV;
   for (int it = threadIdx.x; it < RPW * S; it += blockDim.x) {
     const int row = it / S, sp = it - row * S;
     const int qr = blockIdx.x * RPW + row < NQ ? blockIdx.x * RPW + row : NQ - 1;
     s_ml[it] = __ldcg(reinterpret_cast<const float2*>(up + ((size_t)sp * 64 + qr) * RS + HD));
   }
-  const float* base = up + (size_t)rr * RS + 8 * d8;
-  float4 v[2 * MB];
+  const float* base = up + (size_t)rr * RS + CPL * d8;
+  float4 v[NV * MB];
 #pragma unroll
   for (int j = 0; j < MB; ++j) {
     const int sp = warp + 4 * j;
     if (sp < S) {
       const float4* src = reinterpret_cast<const float4*>(base + (size_t)sp * 64 * RS);
-      v[2 * j] = __ldcg(src);
-      v[2 * j + 1] = __ldcg(src + 1);
+#pragma unroll
+      for (int u = 0; u < NV; ++u) v[NV * j + u] = __ldcg(src + u);
     }
   }
   __syncthreads();
@@ -1138,17 +1166,22 @@ __global__ void __launch_bounds__(128) attn_verify_merge_kernel(const VAttnArgs 
 #pragma unroll
   for (int off = LPR / 2; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   const float Mu = M == -INFINITY ? 0.f : M;
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float acc[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
   for (int sp0 = warp;; sp0 += 4 * MB) {
 #pragma unroll
     for (int j = 0; j < MB; ++j) {
       const int sp = sp0 + 4 * j;
       if (sp < S) {
         const float w = ex2_approx(ml[sp].x - Mu);
-        acc[0] += w * v[2 * j].x; acc[1] += w * v[2 * j].y;
-        acc[2] += w * v[2 * j].z; acc[3] += w * v[2 * j].w;
-        acc[4] += w * v[2 * j + 1].x; acc[5] += w * v[2 * j + 1].y;
-        acc[6] += w * v[2 * j + 1].z; acc[7] += w * v[2 * j + 1].w;
+#pragma unroll
+        for (int u = 0; u < NV; ++u) {
+          acc[4 * u] += w * v[NV * j + u].x;
+          acc[4 * u + 1] += w * v[NV * j + u].y;
+          acc[4 * u + 2] += w * v[NV * j + u].z;
+          acc[4 * u + 3] += w * v[NV * j + u].w;
+        }
       }
     }
     if (sp0 + 4 * MB >= S) break;
@@ -1157,13 +1190,14 @@ __global__ void __launch_bounds__(128) attn_verify_merge_kernel(const VAttnArgs 
       const int sp = sp0 + 4 * MB + 4 * j;
       if (sp < S) {
         const float4* src = reinterpret_cast<const float4*>(base + (size_t)sp * 64 * RS);
-        v[2 * j] = __ldcg(src);
-        v[2 * j + 1] = __ldcg(src + 1);
+#pragma unroll
+        for (int u = 0; u < NV; ++u) v[NV * j + u] = __ldcg(src + u);
       }
     }
   }
-  s_acc[warp][lane][0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-  s_acc[warp][lane][1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+#pragma unroll
+  for (int u = 0; u < NV; ++u)
+    s_acc[warp][lane][u] = make_float4(acc[4 * u], acc[4 * u + 1], acc[4 * u + 2], acc[4 * u + 3]);
   __syncthreads();
   if (warp != 0) return;
   float den = 0.f;
@@ -1171,9 +1205,9 @@ __global__ void __launch_bounds__(128) attn_verify_merge_kernel(const VAttnArgs 
 #pragma unroll
   for (int off = LPR / 2; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
   const float inv = den > 0.f ? 1.f / den : 0.f;
-  float out[8];
+  float out[CPL];
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
+  for (int h = 0; h < NV; ++h) {
     float4 t0 = s_acc[0][lane][h];
 #pragma unroll
     for (int w = 1; w < 4; ++w) {
@@ -1187,11 +1221,18 @@ __global__ void __launch_bounds__(128) attn_verify_merge_kernel(const VAttnArgs 
   }
   if (r >= NQ) return;
   const int tok = r / a.G, h = kvh * a.G + r % a.G;
-  float4* dst = reinterpret_cast<float4*>(a.o + ((size_t)tok * a.nh + h) * HD) + 2 * d8;
-  dst[0] = make_float4(out[0], out[1], out[2], out[3]);
-  dst[1] = make_float4(out[4], out[5], out[6], out[7]);
-  // the same values as the o_proj GEMM's activation operand (column h * HD + 8 d8)
-  store_bop_group(a.bops, tok, (h * HD) / 8 + d8, out);
+  float4* dst = reinterpret_cast<float4*>(a.o + ((size_t)tok * a.nh + h) * HD) + NV * d8;
+#pragma unroll
+  for (int u = 0; u < NV; ++u)
+    dst[u] = make_float4(out[4 * u], out[4 * u + 1], out[4 * u + 2], out[4 * u + 3]);
+  // the same values as the o_proj GEMM's activation operand (columns h * HD + CPL d8 ..)
+#pragma unroll
+  for (int gq = 0; gq < CPL / 8; ++gq) {
+    float o8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o8[i] = out[8 * gq + i];
+    store_bop_group(a.bops, tok, (h * HD + CPL * d8) / 8 + gq, o8);
+  }
 }
 
 // Post-attention RMSNorm of the verify block, one CTA per token row: sum(y^2) in a fixed
@@ -1475,9 +1516,12 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
     return HFA_EUNSUPPORTED;
   }
 
+  // keys per attention stage and CTAs per (KV head, key chunk) of the head dim
+  const int VT = hd == 512 ? VACfg<512>::VT : kVT;
+  const int DH = hd == 512 ? VACfg<512>::DH : 1;
   CUtensorMap tk, tv;
-  if (hfa_encode_kv_map(&tk, c.k_cache, nkv * d.kv_capacity, hd, kVT) != HFA_OK ||
-      hfa_encode_kv_map(&tv, c.v_cache, nkv * d.kv_capacity, hd, kVT) != HFA_OK) {
+  if (hfa_encode_kv_map(&tk, c.k_cache, nkv * d.kv_capacity, hd, VT) != HFA_OK ||
+      hfa_encode_kv_map(&tv, c.v_cache, nkv * d.kv_capacity, hd, VT) != HFA_OK) {
     snprintf(msg, n, "cannot describe the KV cache to the TMA unit");
     return HFA_EINVAL;
   }
@@ -1568,13 +1612,13 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   aa.klo = aa.sliding ? (c.base_pos - d.window + 1 > 0 ? c.base_pos - d.window + 1 : 0) : 0;
   aa.khi = c.base_pos + c.L - 1;
   const int nkeys = aa.khi - aa.klo + 1;
-  int S = c.num_sms / nkv;
-  const int max_tiles = (nkeys + kVT - 1) / kVT;
+  int S = c.num_sms / (nkv * DH);
+  const int max_tiles = (nkeys + VT - 1) / VT;
   if (S > max_tiles) S = max_tiles;
   if ((size_t)S * nkv > v->part_records) S = (int)(v->part_records / nkv);
   if (S < 1) S = 1;
   int chunk = (nkeys + S - 1) / S;
-  chunk = (chunk + kVT - 1) / kVT * kVT;
+  chunk = (chunk + VT - 1) / VT * VT;
   S = (nkeys + chunk - 1) / chunk;
   aa.splits = S;
   aa.chunk = chunk;
@@ -1590,24 +1634,30 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
     e = launch_ex(attn_verify_kernel<64>, nkv * S, athreads, VACfg<64>::SMEM, pdl, s, tk, tv, aa);
   else if (hd == 128)  // both products on the tensor cores (TMEM accumulators)
     e = launch_ex(attn_verify_tc_kernel, nkv * S, vtc::THREADS, vtc::SMEM, pdl, s, tk, tv, aa);
-  else
+  else if (hd == 256)
     e = launch_ex(attn_verify_kernel<256>, nkv * S, athreads, VACfg<256>::SMEM, pdl, s, tk, tv,
                   aa);
+  else
+    e = launch_ex(attn_verify_kernel<512>, nkv * S * DH, athreads, VACfg<512>::SMEM, pdl, s, tk,
+                  tv, aa);
   te();
   if (e != cudaSuccess) {
     snprintf(msg, n, "verify attention launch: %s", cudaGetErrorString(e));
     return HFA_ECUDA;
   }
   // (2b) combination of the split records
-  const size_t msmem = (size_t)(256 / hd) * S * sizeof(float2);
-  const int mgrid = (c.L * G + 256 / hd - 1) / (256 / hd);
+  const int rpw = hd <= 256 ? 256 / hd : 1;  // query rows per merge CTA
+  const size_t msmem = (size_t)rpw * S * sizeof(float2);
+  const int mgrid = (c.L * G + rpw - 1) / rpw;
   tb("verify_attn_merge");
   if (hd == 64)
     e = launch_ex2(attn_verify_merge_kernel<64>, dim3(mgrid, nkv), 128, msmem, pdl, s, 1, aa);
   else if (hd == 128)
     e = launch_ex2(attn_verify_merge_kernel<128>, dim3(mgrid, nkv), 128, msmem, pdl, s, 1, aa);
-  else
+  else if (hd == 256)
     e = launch_ex2(attn_verify_merge_kernel<256>, dim3(mgrid, nkv), 128, msmem, pdl, s, 1, aa);
+  else
+    e = launch_ex2(attn_verify_merge_kernel<512>, dim3(mgrid, nkv), 128, msmem, pdl, s, 1, aa);
   te();
   if (e != cudaSuccess) {
     snprintf(msg, n, "verify attention merge launch: %s", cudaGetErrorString(e));

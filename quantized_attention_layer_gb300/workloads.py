@@ -136,6 +136,10 @@ GLOBAL_32K = Workload(name="global_hd512_32k", hidden=2816, num_heads=16, num_kv
                       head_dim=512, layer_type=FULL, window=0, kv_capacity=32768, ring=False,
                       batch=1, rope_theta=1e6, seed=70, seq_pos=32767, k_eq_v=True,
                       rope_freq_factors=True, post_norm=True)
+# The verify block on the global layer at a 32K context: GQA group 8 admits blocks of up to
+# 8 tokens (64 query rows per KV head), here the last 8 positions of the cache.
+VERIFY_GLOBAL = dataclasses.replace(GLOBAL_32K, name="verify_global_hd512_32k", seq_pos=None,
+                                    weights_bf16=True, verify_len=8, base_pos=32760)
 # A drafter step on the verify shape: 16 context rows appended at 8176..8191 (K/V
 # projections only), then a 16-token block at 8192..8207, bidirectional within the block,
 # scale 1/sqrt(hd).
@@ -143,7 +147,8 @@ DRAFTER_L16 = dataclasses.replace(VERIFY_L16, name="drafter_l16_8k", block_bidir
                                   attn_scale=128 ** -0.5)
 DRAFTER_CTX_ROWS = 16
 
-BY_NAME: Dict[str, Workload] = {w.name: w for w in WORKLOADS + [GLOBAL_32K, DRAFTER_L16]}
+BY_NAME: Dict[str, Workload] = {w.name: w for w in WORKLOADS + [GLOBAL_32K, VERIFY_GLOBAL,
+                                                                 DRAFTER_L16]}
 
 
 def _gen(seed: int, stream: int) -> torch.Generator:

@@ -97,6 +97,32 @@ def test_verify_block_hd128_sliding(window, softcap):
     _case(w, 11, 517)
 
 
+def test_verify_block_global_layer_hd512_32k():
+    # the pages' global layer (16 query heads of 512 dims over 2 KV heads, no V projection,
+    # RoPE frequency factors, post-attention norm), 8 tokens at the end of a 32K context
+    w = wl.VERIFY_GLOBAL
+    _case(w, w.verify_len, w.base_pos)
+
+
+def test_verify_block_hd512_sliding_softcap_ragged():
+    # 312 visible keys (not a multiple of the 32-key stage), the window's first key inside
+    # a stage, two CTAs per key chunk each writing half of the output dims
+    w = wl.Workload(name="ver512s", hidden=1024, num_heads=8, num_kv_heads=2, head_dim=512,
+                    layer_type=wl.SLIDING, window=300, kv_capacity=1300, ring=False, batch=1,
+                    rope_theta=1e4, seed=103, weights_bf16=True, verify_len=16, base_pos=0,
+                    softcap=30.0)
+    _case(w, 13, 1111)
+
+
+def test_verify_block_hd512_short_context_variants():
+    # fewer keys than one stage per chunk; V projected and unit-normed
+    w = wl.Workload(name="ver512v", hidden=512, num_heads=4, num_kv_heads=1, head_dim=512,
+                    layer_type=wl.FULL, window=0, kv_capacity=96, ring=False, batch=1,
+                    rope_theta=1e6, seed=104, weights_bf16=True, verify_len=16, base_pos=0,
+                    v_unit_norm=True, rope_freq_factors=True, post_norm=True)
+    _case(w, 16, 20)
+
+
 def test_verify_block_repeats_bit_for_bit():
     # no atomics on the data path: two runs on the same inputs agree in every bit
     w = wl.VERIFY_L16
@@ -116,7 +142,7 @@ def test_bidirectional_block_full_size():
     _case(w, w.verify_len, w.base_pos)
 
 
-@pytest.mark.parametrize("hd", [64, 128, 256])
+@pytest.mark.parametrize("hd", [64, 128, 256, 512])
 def test_bidirectional_block_head_dims(hd):
     w = wl.Workload(name=f"bidir{hd}", hidden=1024, num_heads=8, num_kv_heads=2, head_dim=hd,
                     layer_type=wl.FULL, window=0, kv_capacity=700, ring=False, batch=1,
@@ -181,3 +207,12 @@ def test_drafter_step_sliding_layer_stays_causal():
                     rope_theta=1e4, seed=102, weights_bf16=True, verify_len=16, base_pos=0,
                     block_bidir=True, attn_scale=256 ** -0.5)
     _drafter_step(w, S=16, L=8, base=200)
+
+
+def test_drafter_step_global_layer_hd512():
+    # context rows (at most max_verify_len = 8) through the 512-wide K/V epilogue (no V
+    # projection), then the block
+    w = wl.GLOBAL_32K.replace(name="draft_global", kv_capacity=2000, weights_bf16=True,
+                              verify_len=8, seq_pos=None, block_bidir=True,
+                              attn_scale=512 ** -0.5)
+    _drafter_step(w, S=8, L=8, base=1500)
