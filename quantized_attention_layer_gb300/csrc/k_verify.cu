@@ -412,7 +412,7 @@ __global__ void __launch_bounds__(128, 1) verify_gemm_kernel(const VGemmArgs a) 
         finish_head_row<128>(g, hh, t, v, lane);
       } else if (hd == 256) {
         finish_head_row<256>(g, hh, t, u, lane);
-      } else {  // 512: the head's second 256 rows in a second polling round
+      } else if (hd == 512) {  // the head's second 256 rows in a second polling round
         float u2[8];
         split_sum_rows(hl * hd + 256 + lane, t, 8, u2);
         float v[16];
@@ -1637,9 +1637,11 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   else if (hd == 256)
     e = launch_ex(attn_verify_kernel<256>, nkv * S, athreads, VACfg<256>::SMEM, pdl, s, tk, tv,
                   aa);
-  else
+  else if (hd == 512)
     e = launch_ex(attn_verify_kernel<512>, nkv * S * DH, athreads, VACfg<512>::SMEM, pdl, s, tk,
                   tv, aa);
+  else
+    e = cudaErrorInvalidValue;  // every kernel is sized for its head dim: none other is launched
   te();
   if (e != cudaSuccess) {
     snprintf(msg, n, "verify attention launch: %s", cudaGetErrorString(e));
@@ -1656,8 +1658,10 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
     e = launch_ex2(attn_verify_merge_kernel<128>, dim3(mgrid, nkv), 128, msmem, pdl, s, 1, aa);
   else if (hd == 256)
     e = launch_ex2(attn_verify_merge_kernel<256>, dim3(mgrid, nkv), 128, msmem, pdl, s, 1, aa);
-  else
+  else if (hd == 512)
     e = launch_ex2(attn_verify_merge_kernel<512>, dim3(mgrid, nkv), 128, msmem, pdl, s, 1, aa);
+  else
+    e = cudaErrorInvalidValue;
   te();
   if (e != cudaSuccess) {
     snprintf(msg, n, "verify attention merge launch: %s", cudaGetErrorString(e));
