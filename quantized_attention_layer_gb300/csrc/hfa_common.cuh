@@ -303,10 +303,27 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   d |= (uint64_t)2 << 61;                     // 128-byte swizzle
   return d;
 }
+// Shared-memory matrix descriptor of an MN-major bf16 operand written with the 128-byte
+// swizzle (rows along K, 64 MN elements = 128 bytes of each row in one block, 16-byte chunk
+// c of row r at (c XOR (r % 8)) within 1024-byte groups of 8 rows): 8-row K groups 1024
+// bytes apart, MN blocks `mn_stride` bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t saddr, uint32_t mn_stride) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);               // start address
+  d |= (uint64_t)((mn_stride >> 4) & 0x3FFFu) << 16;      // leading byte offset: next MN block
+  d |= (uint64_t)(1024 >> 4) << 32;                       // stride byte offset: next 8 K rows
+  d |= (uint64_t)1 << 46;                                 // descriptor version
+  d |= (uint64_t)2 << 61;                                 // 128-byte swizzle
+  return d;
+}
 // Instruction descriptor: kind::f16, A and B bf16, D f32, both K-major, M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
          ((uint32_t)(M >> 4) << 24);
+}
+// The same with B MN-major (its N index contiguous in each row)
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(int M, int N) {
+  return idesc_bf16_f32(M, N) | (1u << 16);
 }
 
 // 2^x by the SFU's base-2 exponential (PTX ex2.approx, relative error about 2^-22;

@@ -20,12 +20,13 @@
 //  * attn_verify_tc_kernel (head_dim 128, tcgen05): one CTA per (KV head, key chunk);
 //    S = Qx K^T and O += Px Vt on the tensor cores with TMEM accumulators, the online
 //    softmax of each query split over the four threads that hold its two TMEM rows.
-//  * attn_verify_kernel (head_dim 64, 256, 512; mma.sync): one CTA per (KV head, key
-//    chunk) -- two at head_dim 512, each accumulating half of the output dims; a TMA
-//    producer warp streams K and V tiles, each consumer warp owns 8 query rows (bf16 hi/lo
-//    in MMA rows g and g + 8) and takes every stage in online-softmax updates, with the
-//    causal / window mask of its rows.
-//    Both attention kernels write one (O, m, l) record per query row and CTA.
+//  * attn_verify_kernel (head_dim 64, 256; mma.sync): one CTA per (KV head, key chunk); a
+//    TMA producer warp streams K and V tiles, each consumer warp owns 8 query rows (bf16
+//    hi/lo in MMA rows g and g + 8) and takes every 64-key stage in one online-softmax
+//    update, with the causal / window mask of its rows.
+//  * attn_verify_hy_kernel (head_dim 512): the scores on mma.sync with each warp's query
+//    fragments in registers, O += P V on tcgen05 into a 512-column TMEM accumulator.
+//    The attention kernels write one (O, m, l) record per query row and CTA.
 //  * attn_verify_merge_kernel: the records of a KV head's chunks combined, a few query
 //    rows per CTA, into the f32 output and the o_proj activation operand.
 #include <cooperative_groups.h>
@@ -452,24 +453,15 @@ struct VAttnArgs {
   unsigned* err;
 };
 
-// A 512-wide head is shared by DH = 2 CTAs per (KV head, key chunk): both take the whole
-// scores (the same arithmetic on the same tiles, so the same m and l), each accumulates
-// the output over its OD = 256 dims and reads only that half of V; 32-key stages keep the
-// K tile, the V half and the query fragments inside one SM's shared memory.
 template <int HD>
 struct VACfg {
-  static constexpr int VT = HD >= 512 ? 32 : kVT;  // keys per stage
-  static constexpr int OD = HD >= 512 ? 256 : HD;  // output dims per CTA
-  static constexpr int DH = HD / OD;               // CTAs per (KV head, key chunk)
-  static constexpr int NS = HD >= 256 ? 2 : 3;     // stages (shared memory budget)
-  static constexpr int KTILE = VT * HD * 2;
-  static constexpr int VTILE = VT * OD * 2;
-  static constexpr int STAGE = KTILE + VTILE;
+  static constexpr int NS = HD >= 256 ? 2 : 3;  // stages (shared memory budget)
+  static constexpr int TILE = kVT * HD * 2;
+  static constexpr int STAGE = 2 * TILE;
   static constexpr int KS = HD / 16;
-  static constexpr int NTO = OD / 8;
+  static constexpr int NTO = HD / 8;
   static constexpr int KB = HD >= 256 ? 16 : 64;  // keys per online-softmax update (registers)
   static constexpr size_t SMEM = 1024 + (size_t)NS * STAGE + 8 * KS * 32 * 16 + 256;
-  static_assert(SMEM <= 232448, "stages and query fragments exceed one CTA's shared memory");
 };
 
 
@@ -491,9 +483,7 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
   const int nc = (blockDim.x >> 5) - 1;  // consumer warps, 8 query rows each
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  constexpr int VT = Cfg::VT;
-  const int unit = blockIdx.x / Cfg::DH, half = blockIdx.x - unit * Cfg::DH;
-  const int kvh = unit / a.splits, split = unit - kvh * a.splits;
+  const int kvh = blockIdx.x / a.splits, split = blockIdx.x - kvh * a.splits;
   const int NQ = a.L * a.G;
 
   if (threadIdx.x == 0) {
@@ -511,10 +501,10 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
   int k_end = k_begin + a.chunk;
   if (k_end > a.khi + 1) k_end = a.khi + 1;
   const int nkeys = k_end > k_begin ? k_end - k_begin : 0;
-  const int ntiles = (nkeys + VT - 1) / VT;
+  const int ntiles = (nkeys + kVT - 1) / kVT;
   const int row0 = kvh * a.C + k_begin;
   constexpr int RS = HD + 4;
-  float* part = a.part + (size_t)unit * 64 * RS;
+  float* part = a.part + ((size_t)kvh * a.splits + split) * 64 * RS;
 
   if (warp == nc) {
     if (lane == 0) {
@@ -524,7 +514,7 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
       bool waited = false;
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % NS;
-        if (!waited && (i >= NS || k_begin + (i + 1) * VT > a.base)) {
+        if (!waited && (i >= NS || k_begin + (i + 1) * kVT > a.base)) {
           pdl_wait();
           waited = true;
         }
@@ -536,12 +526,10 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
         uint8_t* kt = stages + st * Cfg::STAGE;
         mbar_arrive_expect_tx(&full[st], Cfg::STAGE);
 #pragma unroll
-        for (int j = 0; j < HD / 64; ++j)
-          tma_load_2d(kt + j * VT * 128, &tmk, &full[st], 64 * j, row0 + i * VT);
-#pragma unroll
-        for (int j = 0; j < Cfg::OD / 64; ++j)
-          tma_load_2d(kt + Cfg::KTILE + j * VT * 128, &tmv, &full[st], half * Cfg::OD + 64 * j,
-                      row0 + i * VT);
+        for (int j = 0; j < HD / 64; ++j) {
+          tma_load_2d(kt + j * kVT * 128, &tmk, &full[st], 64 * j, row0 + i * kVT);
+          tma_load_2d(kt + Cfg::TILE + j * kVT * 128, &tmv, &full[st], 64 * j, row0 + i * kVT);
+        }
         issued = i + 1;
       }
       if (!waited) pdl_wait();
@@ -580,8 +568,8 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
 #pragma unroll
     for (int i = 0; i < Cfg::NTO; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     const uint32_t stage_base = smem_u32(stages);
-    // A K (V) tile holds HD / 64 (OD / 64) boxes of VT keys x 128 bytes: 16-byte chunk c
-    // of key row r sits at (c / 8) * VT * 128 + r * 128 + ((c % 8) XOR (r % 8)) * 16.  The lane parts
+    // A K or V stage holds HD / 64 boxes of 64 keys x 128 bytes: 16-byte chunk c of key
+    // row r sits at (c / 8) * 8 KB + r * 128 + ((c % 8) XOR (r % 8)) * 16.  The lane parts
     // of the ldmatrix addresses (the compile-time row and chunk terms split off): the K
     // fragments read row 16 kg + (lane / 16) 8 + lane % 8,
     // chunk 2 ks + (lane / 8) % 2; the V fragments row 16 kk + ((lane / 8) % 2) 8 + lane % 8,
@@ -607,10 +595,10 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
         break;
       }
       const uint32_t kb0 = stage_base + st * Cfg::STAGE;
-      const uint32_t vb0 = kb0 + Cfg::KTILE;
+      const uint32_t vb0 = kb0 + Cfg::TILE;
 #pragma unroll 1
-      for (int hb = 0; hb < VT; hb += KB) {
-      const int key_lo = k_begin + i * VT + hb, key_hi = key_lo + KB - 1;
+      for (int hb = 0; hb < kVT; hb += KB) {
+      const int key_lo = k_begin + i * kVT + hb, key_hi = key_lo + KB - 1;
       if (key_lo >= k_end) break;
       // scores of KB keys, KB / 8 independent accumulator chains: n-tile j holds keys
       // 8j .. 8j + 7, rows g (q hi) and g + 8 (q lo)
@@ -624,7 +612,7 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
 #pragma unroll
         for (int kg = 0; kg < KB / 16; ++kg) {
           uint32_t b0, b1, b2, b3;
-          ldmatrix_x4(kb0 + swk[ks & 3] + (uint32_t)((ks >> 2) * (VT * 128) + (hb + kg * 16) * 128),
+          ldmatrix_x4(kb0 + swk[ks & 3] + (uint32_t)((ks >> 2) * (kVT * 128) + (hb + kg * 16) * 128),
                       b0, b1, b2, b3);
           mma_bf16(s[2 * kg], A, b0, b1);
           mma_bf16(s[2 * kg + 1], A, b2, b3);
@@ -699,7 +687,7 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
         for (int np = 0; np < Cfg::NTO / 2; ++np) {
           uint32_t b0, b1, b2, b3;
           ldmatrix_x4_trans(
-              vb0 + swv[np & 3] + (uint32_t)((np >> 2) * (VT * 128) + (hb + kk * 16) * 128),
+              vb0 + swv[np & 3] + (uint32_t)((np >> 2) * (kVT * 128) + (hb + kk * 16) * 128),
               b0, b1, b2, b3);
           if (tail) {
             b0 &= mlo;
@@ -719,8 +707,7 @@ __global__ void __launch_bounds__(288) attn_verify_kernel(const __grid_constant_
     l += __shfl_xor_sync(0xffffffffu, l, 2);
     if (qvalid) {
       float* pr = part + (size_t)qrow * RS;
-      if (t == 0 && half == 0) *reinterpret_cast<float2*>(pr + HD) = make_float2(m, l);
-      pr += half * Cfg::OD;
+      if (t == 0) *reinterpret_cast<float2*>(pr + HD) = make_float2(m, l);
 #pragma unroll
       for (int nt = 0; nt < Cfg::NTO; ++nt)
         *reinterpret_cast<float2*>(pr + nt * 8 + 2 * t) =
@@ -1112,6 +1099,417 @@ __global__ void __launch_bounds__(vtc::THREADS, 1)
   }
   tc_fence_after();
   if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// ------------------------------------------------------------------ block attention at hd 512
+// The records of attn_verify_kernel for 512-wide heads, one CTA per (KV head, key chunk),
+// over 32-key stages:
+//   scores on mma.sync: each consumer warp keeps its 8 query rows (bf16 hi in MMA rows g,
+//     lo in g + 8) as A fragments in registers for all 512 dims, so shared memory carries
+//     only the K tile to the scores;
+//   O += Px V on tcgen05 into a 128 x 512 f32 TMEM accumulator (rows 0..63 take P hi,
+//     64..127 P lo; query q's output is O[q] + O[q + 64]): per 16 keys two N = 256 MMAs,
+//     V read in place from its stage as an MN-major operand (keys along K, dims along N).
+// A row's reference maximum moves only when a stage's maximum passes it by more than
+// kRefSlack (log2 units), so P <= 2^kRefSlack and the O rows in TMEM are rescaled only
+// then; the record holds the reference as m and l = sum 2^(s - m).  One thread of warp 8
+// streams K and V with TMA and issues the MMAs; K and V stages have barriers of their own:
+// K of tile i + 2 loads once the scores have read tile i, V once its MMAs are done.
+namespace vhy {
+constexpr int HD = 512;
+constexpr int VT = 32;                       // keys per stage
+constexpr int TILE = VT * HD * 2;            // one K or V stage: 8 boxes of 32 keys x 128 B
+constexpr int K_OFF = 0;                     // K stages [2]
+constexpr int V_OFF = 2 * TILE;              // V stages [2]
+constexpr int PX_OFF = 4 * TILE;             // Px [2]: 128 rows x 128 B, keys 0..31
+constexpr int AUX_OFF = PX_OFF + 2 * 16384;  // corrections [2][64], flags [2][8], m [64], l [64]
+constexpr int BAR_OFF = AUX_OFF + 2048;
+constexpr size_t SMEM = 1024 + BAR_OFF + 256;
+constexpr int THREADS = 288;                 // 8 consumer warps + the producer warp
+constexpr int NCW = 8;
+constexpr float kRefSlack = 8.f;
+}  // namespace vhy
+
+__global__ void __launch_bounds__(vhy::THREADS, 1)
+    attn_verify_hy_kernel(const __grid_constant__ CUtensorMap tmk,
+                          const __grid_constant__ CUtensorMap tmv, const VAttnArgs a) {
+  using namespace vhy;
+  constexpr int RS = HD + 4;
+  constexpr int KS = HD / 16;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_align1024(smem_raw);
+  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + BAR_OFF);  // [2] K stage landed
+  uint64_t* vfull = kfull + 2;   // [2] V stage landed
+  uint64_t* p_bar = vfull + 2;   // Px written, rows rescaled, K read (one arrival per warp)
+  uint64_t* pv_bar = p_bar + 1;  // [2] O += P V of stage i done (Px buffer, V stage i % 2 free)
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(pv_bar + 2);
+  int* s_abort = reinterpret_cast<int*>(s_tmem + 1);
+  int* s_kiss = s_abort + 1;  // K tiles requested
+  int* s_viss = s_abort + 2;  // V tiles requested
+  float* s_corr = reinterpret_cast<float*>(smem + AUX_OFF);      // [2][64] by stage parity
+  int* s_need = reinterpret_cast<int*>(smem + AUX_OFF + 512);    // [2][8] by stage parity
+  float* s_m = reinterpret_cast<float*>(smem + AUX_OFF + 1024);  // [64]
+  float* s_l = s_m + 64;                                         // [64]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kvh = blockIdx.x / a.splits, split = blockIdx.x - kvh * a.splits;
+  const int NQ = a.L * a.G;
+  const int k_begin = a.klo + split * a.chunk;
+  int k_end = k_begin + a.chunk;
+  if (k_end > a.khi + 1) k_end = a.khi + 1;
+  const int nkeys = k_end > k_begin ? k_end - k_begin : 0;
+  const int ntiles = (nkeys + VT - 1) / VT;
+  const int row0 = kvh * a.C + k_begin;
+  const uint32_t sbase = smem_u32(smem);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kfull[i], 1);
+      mbar_init(&vfull[i], 1);
+      mbar_init(&pv_bar[i], 1);
+    }
+    mbar_init(p_bar, NCW);
+    *s_abort = 0;
+    *s_kiss = 0;
+    *s_viss = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(s_tmem, 512);  // O: 128 lanes x 512 f32 columns
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+
+  if (warp == NCW) {
+    if (lane == 0) {
+      // ---- producer and MMA issuer
+      auto load_k = [&](int i) {
+        uint8_t* st = smem + K_OFF + (i & 1) * TILE;
+        mbar_arrive_expect_tx(&kfull[i & 1], TILE);
+#pragma unroll
+        for (int j = 0; j < HD / 64; ++j)
+          tma_load_2d(st + j * VT * 128, &tmk, &kfull[i & 1], 64 * j, row0 + i * VT);
+      };
+      auto load_v = [&](int i) {
+        uint8_t* st = smem + V_OFF + (i & 1) * TILE;
+        mbar_arrive_expect_tx(&vfull[i & 1], TILE);
+#pragma unroll
+        for (int j = 0; j < HD / 64; ++j)
+          tma_load_2d(st + j * VT * 128, &tmv, &vfull[i & 1], 64 * j, row0 + i * VT);
+      };
+      // keys before the block's first position are not written by the QKV kernel
+      int n0 = 0;
+      for (; n0 < 2 && n0 < ntiles && k_begin + (n0 + 1) * VT <= a.base; ++n0) {
+        load_k(n0);
+        load_v(n0);
+      }
+      pdl_wait();
+      for (; n0 < 2 && n0 < ntiles; ++n0) {
+        load_k(n0);
+        load_v(n0);
+      }
+      int kiss = n0, viss = n0, pv_issued = 0;
+      constexpr uint32_t idPV = idesc_bf16_f32_bmn(128, 256);
+      bool ok = true;
+      for (int i = 0; ok && i < ntiles; ++i) {
+        if (!mbar_wait(p_bar, i & 1, a.err, s_abort) ||
+            !mbar_wait(&vfull[i & 1], (i >> 1) & 1, a.err, s_abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t px = sbase + PX_OFF + (uint32_t)(i & 1) * 16384;
+        const uint32_t vb = sbase + V_OFF + (uint32_t)(i & 1) * TILE;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)      // output dims 256 h .. 256 h + 255: V boxes 4 h ..
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk)  // keys 16 kk .. 16 kk + 15
+            tc_mma_f16(tmem + 256 * h, smem_desc_sw128(px + kk * 32),
+                       smem_desc_sw128_mn(vb + h * 4 * (VT * 128) + kk * 2048, VT * 128), idPV,
+                       (i | kk) != 0);
+        tc_commit(&pv_bar[i & 1]);
+        pv_issued = i + 1;
+        if (i + 2 < ntiles) {
+          load_k(i + 2);  // the scores have read K of stage i (p_bar)
+          ++kiss;
+          if (!mbar_wait(&pv_bar[i & 1], (i >> 1) & 1, a.err, s_abort)) {
+            ok = false;
+            break;
+          }
+          load_v(i + 2);  // the MMAs have read V of stage i
+          ++viss;
+        }
+      }
+      if (!ok) *(volatile int*)s_abort = 1;
+      // the MMAs complete in order: the last one's commit covers all of them
+      if (pv_issued > 0) mbar_wait(&pv_bar[(pv_issued - 1) & 1], ((pv_issued - 1) >> 1) & 1, a.err);
+      *s_kiss = kiss;
+      *s_viss = viss;
+    } else {
+      pdl_wait();
+    }
+    pdl_launch_dependents();
+  } else {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int g = lane >> 2, t = lane & 3;
+    const int qrow = 8 * warp + g;  // query of this lane's score rows
+    const bool qvalid = qrow < NQ;
+    const int tok = qvalid ? qrow / a.G : 0;
+    const int limit = a.bidir ? a.base + a.L - 1 : a.base + tok;  // last visible position
+    // the query as A fragments of every 16-dim k-step (scaled; hi in row g, lo in row g + 8)
+    uint32_t qa[KS][4];
+    {
+      const float* q = a.q + ((size_t)tok * a.nh + kvh * a.G + qrow % a.G) * HD + 2 * t;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        qa[ks][0] = qa[ks][1] = qa[ks][2] = qa[ks][3] = 0u;
+        if (qvalid) {
+          const float2 v0 = *reinterpret_cast<const float2*>(q + ks * 16);
+          const float2 v1 = *reinterpret_cast<const float2*>(q + ks * 16 + 8);
+          __nv_bfloat16 h[4], lw[4];
+          split_bf16(v0.x * a.qscale, h[0], lw[0]);
+          split_bf16(v0.y * a.qscale, h[1], lw[1]);
+          split_bf16(v1.x * a.qscale, h[2], lw[2]);
+          split_bf16(v1.y * a.qscale, h[3], lw[3]);
+          qa[ks][0] = pack_bf2(h[0], h[1]);
+          qa[ks][1] = pack_bf2(lw[0], lw[1]);
+          qa[ks][2] = pack_bf2(h[2], h[3]);
+          qa[ks][3] = pack_bf2(lw[2], lw[3]);
+        }
+      }
+    }
+    // ldmatrix lane offsets of the K fragments (row 16 hb + (lane / 16) 8 + lane % 8,
+    // 16-byte chunk 2 ks + (lane / 8) % 2 of its box, swizzled by row % 8 = lane % 8)
+    uint32_t swk[4];
+    {
+      const int l7 = lane & 7;
+      const int xk = ((lane >> 3) & 1) ^ l7;
+      const uint32_t rk = (uint32_t)((((lane >> 4) << 3) + l7) * 128);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) swk[j] = rk + (uint32_t)(((2 * j) ^ xk) << 4);
+    }
+    float m_ref = -INFINITY, l = 0.f;
+    // every consumer runs every stage's named barriers, also after a give-up (a bounded
+    // wait that runs out sets the abort flag; later waits return at once); the result is
+    // agreed across the warp, as the tcgen05 loads and stores are .sync.aligned
+    bool dead = false;
+    auto wait_ok = [&](uint64_t* bar, uint32_t parity) {
+      if (!dead && !mbar_wait(bar, parity, a.err, s_abort)) {
+        dead = true;
+        *(volatile int*)s_abort = 1;
+      }
+      dead = !__all_sync(0xffffffffu, !dead);
+      return !dead;
+    };
+    // this warp's TMEM rows (lane quadrant warp % 4) and column half (warp / 4)
+    const int r_t = 32 * (warp & 3) + lane;
+    const int q_t = r_t & 63;
+    const uint32_t t_row = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 256 * (warp >> 2);
+    for (int i = 0; i < ntiles; ++i) {
+      const int key0 = k_begin + i * VT;
+      float p[2][4];  // 16-key half hb: keys 16 hb + 8 (e / 2) + 2 t + e % 2
+      float mloc = -INFINITY;
+      if (wait_ok(&kfull[i & 1], (i >> 1) & 1)) {
+        const uint32_t kb = sbase + K_OFF + (uint32_t)(i & 1) * TILE;
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+          float s[2][4];
+#pragma unroll
+          for (int j = 0; j < 2; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) {
+            uint32_t b0, b1, b2, b3;
+            ldmatrix_x4(kb + swk[ks & 3] + (uint32_t)((ks >> 2) * (VT * 128) + hb * 16 * 128), b0,
+                        b1, b2, b3);
+            mma_bf16(s[0], qa[ks], b0, b1);
+            mma_bf16(s[1], qa[ks], b2, b3);
+          }
+          float sc[4] = {s[0][0] + s[0][2], s[0][1] + s[0][3], s[1][0] + s[1][2],
+                         s[1][1] + s[1][3]};
+          if (a.cap_log2 != 0.f) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[e] = a.cap_log2 * tanhf(sc[e]);
+          }
+          // keys past the chunk, after this row's position or before its window: masked
+          const int klo = key0 + 16 * hb;
+          if (!(klo + 15 < k_end && klo + 15 <= limit && (!a.sliding || klo > limit - a.window))) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int key = klo + 8 * (e >> 1) + 2 * t + (e & 1);
+              const bool vis = key < k_end && key <= limit && (!a.sliding || key > limit - a.window);
+              if (!vis) sc[e] = -INFINITY;
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            p[hb][e] = sc[e];
+            mloc = fmaxf(mloc, sc[e]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) p[0][e] = p[1][e] = -INFINITY;
+      }
+      mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
+      mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
+      // the reference moves only past the slack (from -inf: the O rows are exactly zero)
+      float corr = 1.f;
+      if (mloc > m_ref + kRefSlack) {
+        if (m_ref != -INFINITY) corr = ex2_approx(m_ref - mloc);
+        m_ref = mloc;
+      }
+      const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+      float psum = 0.f;
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          p[hb][e] = ex2_approx(p[hb][e] - m_use);
+          psum += p[hb][e];
+        }
+      l = l * corr + psum;
+      // P hi in row qrow, lo in row qrow + 64 of Px buffer i % 2 (its previous MMA, stage
+      // i - 2, was waited for at the end of stage i - 1): key pair (8 c + 2 t, + 1) is the
+      // t-th word of 16-byte chunk c, stored at chunk c XOR (row % 8)
+      uint8_t* px = smem + PX_OFF + (i & 1) * 16384;
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          __nv_bfloat16 h0, l0, h1, l1;
+          split_bf16(p[hb][2 * j], h0, l0);
+          split_bf16(p[hb][2 * j + 1], h1, l1);
+          const int c = 2 * hb + j;
+          const int off = (qrow & 7) * 128 + ((c ^ (qrow & 7)) << 4) + 4 * t;
+          *reinterpret_cast<uint32_t*>(px + (qrow >> 3) * 1024 + off) = pack_bf2(h0, h1);
+          *reinterpret_cast<uint32_t*>(px + ((qrow + 64) >> 3) * 1024 + off) = pack_bf2(l0, l1);
+        }
+      // the last tile's V rows past the chunk may hold any bits (a NaN times a zero weight
+      // is NaN): zeroed before the MMA reads them
+      if (i == ntiles - 1 && key0 + VT > k_end && wait_ok(&vfull[i & 1], (i >> 1) & 1)) {
+        const int nv = k_end - key0, nr = VT - nv;
+        uint8_t* vt = smem + V_OFF + (i & 1) * TILE;
+        for (int z = threadIdx.x; z < nr * 8 * 8; z += NCW * 32) {
+          const int box = z / (nr * 8), rem = z - box * (nr * 8);
+          *reinterpret_cast<uint4*>(vt + box * (VT * 128) + (nv + (rem >> 3)) * 128 + (rem & 7) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      const int b = i & 1;
+      if (t == 0) s_corr[b * 64 + qrow] = corr;
+      const bool need = __any_sync(0xffffffffu, corr != 1.f);
+      if (lane == 0) s_need[b * 8 + warp] = need ? 1 : 0;
+      fence_proxy_async_smem();
+      // O += P V of stage i - 1 is done before this stage's p_bar phase can complete (so the
+      // MMA thread has taken the previous phase), and before rows are rescaled
+      const bool prev = i == 0 || wait_ok(&pv_bar[(i - 1) & 1], ((i - 1) >> 1) & 1);
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      bool any = false;
+#pragma unroll
+      for (int w = 0; w < NCW; ++w) any = any || s_need[b * 8 + w] != 0;
+      if (i > 0 && any && prev) {
+        const float cr = s_corr[b * 64 + q_t];
+        if (__any_sync(0xffffffffu, cr != 1.f)) {
+          tc_fence_after();
+          // 16 columns a round: the query fragments stay live in registers meanwhile
+#pragma unroll 1
+          for (int c0 = 0; c0 < 256; c0 += 16) {
+            uint32_t tv[16];
+            tmem_ld16_nowait(t_row + c0, tv);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) tv[e] = __float_as_uint(__uint_as_float(tv[e]) * cr);
+            tmem_st16(t_row + c0, tv);
+          }
+          tmem_wait_st();
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_bar);
+    }
+    // m and l of each query row (its four lanes hold the same reference; l summed)
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    if (t == 0) {
+      s_m[qrow] = m_ref;
+      s_l[qrow] = l;
+    }
+    // O: the last O += P V done; the rows q + 64 (P lo) are added to rows q through shared
+    // memory (the K and V stages are idle: every copy has been consumed)
+    const bool have = ntiles > 0 && wait_ok(&pv_bar[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1);
+    tc_fence_after();
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    // every condition around a tcgen05 load or store is agreed across the warp (they are
+    // .sync.aligned); the abort flag can change while the lanes read it
+    const bool live = __all_sync(0xffffffffu, have && !*(volatile int*)s_abort);
+    const bool lo = r_t >= 64;
+    const int hf = warp >> 2;
+    float4* ox = reinterpret_cast<float4*>(smem);  // [64 queries][128 float4], swizzled
+    if (lo && live) {
+#pragma unroll 1
+      for (int c0 = 0; c0 < 256; c0 += 64) {
+        uint32_t tv[4][16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld16_nowait(t_row + c0 + 16 * c, tv[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int k4 = (256 * hf + c0) / 4 + c;
+          ox[q_t * 128 + (k4 ^ (q_t & 7))] =
+              make_float4(__uint_as_float(tv[c >> 2][4 * (c & 3)]),
+                          __uint_as_float(tv[c >> 2][4 * (c & 3) + 1]),
+                          __uint_as_float(tv[c >> 2][4 * (c & 3) + 2]),
+                          __uint_as_float(tv[c >> 2][4 * (c & 3) + 3]));
+        }
+      }
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    if (!lo) {  // a whole warp: its TMEM loads run on every lane, valid query row or not
+      const bool ok_all = __all_sync(0xffffffffu, !*(volatile int*)s_abort);  // every lane
+      const bool store = q_t < NQ && ok_all;
+      float* pr = a.part + ((size_t)kvh * a.splits + split) * 64 * RS + (size_t)q_t * RS;
+#pragma unroll 1
+      for (int c0 = 0; c0 < 256; c0 += 64) {
+        uint32_t tv[4][16];
+        if (live) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_ld16_nowait(t_row + c0 + 16 * c, tv[c]);
+          tmem_wait_ld();
+        }
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int k4 = (256 * hf + c0) / 4 + c;
+          float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (live) {
+            const float4 v = ox[q_t * 128 + (k4 ^ (q_t & 7))];
+            o = make_float4(__uint_as_float(tv[c >> 2][4 * (c & 3)]) + v.x,
+                            __uint_as_float(tv[c >> 2][4 * (c & 3) + 1]) + v.y,
+                            __uint_as_float(tv[c >> 2][4 * (c & 3) + 2]) + v.z,
+                            __uint_as_float(tv[c >> 2][4 * (c & 3) + 3]) + v.w);
+          }
+          if (store) *reinterpret_cast<float4*>(pr + 4 * k4) = o;
+        }
+      }
+      if (store && hf == 0) *reinterpret_cast<float2*>(pr + HD) = make_float2(s_m[q_t], s_l[q_t]);
+    }
+  }
+  // drain: copies may still be landing after a give-up; then TMEM back
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int kiss = *s_kiss, viss = *s_viss;
+    for (int st = 0; st < 2; ++st) {
+      if (st < kiss) mbar_wait(&kfull[st], (((st + ((kiss - 1 - st) / 2) * 2)) >> 1) & 1, a.err);
+      if (st < viss) mbar_wait(&vfull[st], (((st + ((viss - 1 - st) / 2) * 2)) >> 1) & 1, a.err);
+    }
+  }
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 // Combination of the block attention's split records, one CTA per RPW = 256 / HD query
@@ -1516,9 +1914,7 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
     return HFA_EUNSUPPORTED;
   }
 
-  // keys per attention stage and CTAs per (KV head, key chunk) of the head dim
-  const int VT = hd == 512 ? VACfg<512>::VT : kVT;
-  const int DH = hd == 512 ? VACfg<512>::DH : 1;
+  const int VT = hd == 512 ? vhy::VT : kVT;  // keys per attention stage
   CUtensorMap tk, tv;
   if (hfa_encode_kv_map(&tk, c.k_cache, nkv * d.kv_capacity, hd, VT) != HFA_OK ||
       hfa_encode_kv_map(&tv, c.v_cache, nkv * d.kv_capacity, hd, VT) != HFA_OK) {
@@ -1612,7 +2008,7 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   aa.klo = aa.sliding ? (c.base_pos - d.window + 1 > 0 ? c.base_pos - d.window + 1 : 0) : 0;
   aa.khi = c.base_pos + c.L - 1;
   const int nkeys = aa.khi - aa.klo + 1;
-  int S = c.num_sms / (nkv * DH);
+  int S = c.num_sms / nkv;
   const int max_tiles = (nkeys + VT - 1) / VT;
   if (S > max_tiles) S = max_tiles;
   if ((size_t)S * nkv > v->part_records) S = (int)(v->part_records / nkv);
@@ -1637,9 +2033,8 @@ hfa_status verify_run(VerifyState* v, const VerifyCall& c, char* msg, int n) {
   else if (hd == 256)
     e = launch_ex(attn_verify_kernel<256>, nkv * S, athreads, VACfg<256>::SMEM, pdl, s, tk, tv,
                   aa);
-  else if (hd == 512)
-    e = launch_ex(attn_verify_kernel<512>, nkv * S * DH, athreads, VACfg<512>::SMEM, pdl, s, tk,
-                  tv, aa);
+  else if (hd == 512)  // scores on mma.sync, O in TMEM (tcgen05)
+    e = launch_ex(attn_verify_hy_kernel, nkv * S, vhy::THREADS, vhy::SMEM, pdl, s, tk, tv, aa);
   else
     e = cudaErrorInvalidValue;  // every kernel is sized for its head dim: none other is launched
   te();
