@@ -80,6 +80,19 @@ def test_verify_refuses_caches_past_32_bit_rows(libhfa):
     assert b"32-bit" in libhfa.hfa_last_error(None)
 
 
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="a valid descriptor with placeholder weights must not reach a GPU")
+def test_global_layer_passes_validation_for_decode_and_verify(libhfa):
+    # head dim 512 with a verify length is a covered shape: without a GPU the create stops
+    # at the device query, after the descriptor checks
+    from quantized_attention_layer_gb300 import workloads as wl
+    for w in (wl.GLOBAL_32K, wl.VERIFY_GLOBAL):
+        d = hfa.desc_for(w)
+        assert d.head_dim == 512 and (d.max_verify_len > 0) == (w is wl.VERIFY_GLOBAL)
+        assert _create_status(libhfa, d) == hfa.HFA_EDEVICE, libhfa.hfa_last_error(None)
+        assert b"no CUDA device" in libhfa.hfa_last_error(None)
+
+
 def test_ring_needs_capacity_equal_to_window(libhfa):
     from quantized_attention_layer_gb300 import workloads as wl
     d = hfa.desc_for(wl.SLIDING_B16)
