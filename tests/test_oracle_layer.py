@@ -122,6 +122,29 @@ def test_verify_block_equals_sequential_decode_steps(orc):
     assert np.array_equal(oracle.bf16_bits(vc), ver["v_cache"])
 
 
+def test_global_layer_verify_block_equals_sequential_decode_steps(orc):
+    # the global layer's width and variants (hd 512, no V projection, RoPE frequency
+    # factors, post-attention norm, GQA group 4) through both paths of the oracle
+    w = wl.Workload(name="verglob", hidden=128, num_heads=4, num_kv_heads=1, head_dim=512,
+                    layer_type=wl.FULL, window=0, kv_capacity=20, ring=False, batch=1,
+                    rope_theta=1e6, seed=24, base_pos=9, verify_len=4, k_eq_v=True,
+                    rope_freq_factors=True, post_norm=True)
+    weights = wl.make_weights(w)
+    assert weights["wv"] is None and weights["rope_ff"] is not None
+    x = wl.make_x(w)
+    kv = wl.make_kv_cache(w)
+    ver = orc.verify_block(w, weights, x, 9, kv["k_cache"], kv["v_cache"])
+    kc, vc = kv["k_cache"], kv["v_cache"]
+    for i in range(4):
+        step = orc.decode_step(w, weights, x[i:i + 1], [9 + i], kc, vc)
+        kc = torch.from_numpy(step["k_cache"].view(np.int16)).view(torch.bfloat16)
+        vc = torch.from_numpy(step["v_cache"].view(np.int16)).view(torch.bfloat16)
+        for key in ("q", "k", "v", "attn", "out"):
+            assert np.max(np.abs(step[key][0] - ver[key][i])) <= 1e-12, (key, i)
+    assert np.array_equal(oracle.bf16_bits(kc), ver["k_cache"])
+    assert np.array_equal(oracle.bf16_bits(vc), ver["v_cache"])
+
+
 def test_sliding_verify_block_matches_decode_steps(orc):
     w = wl.Workload(name="versl", hidden=64, num_heads=2, num_kv_heads=1, head_dim=32,
                     layer_type=wl.SLIDING, window=6, kv_capacity=32, ring=False, batch=1,
