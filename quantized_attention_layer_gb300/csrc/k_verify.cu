@@ -268,7 +268,9 @@ __global__ void __launch_bounds__(128, 1) verify_gemm_kernel(const VGemmArgs a) 
   // ---- epilogue: accumulator rows 32w..32w+31, columns 0..15 hi, 16..31 lo.  The CTA's
   // partial sums go to its own shared memory (the ring is drained: every copy has been
   // consumed by the MMAs that `done` waited for) as [16 tokens][128 rows] f32.
-  const bool ok = mbar_wait(done, 0, a.g.err);
+  // agreed across the warp: the tcgen05 loads below are .sync.aligned, and a wait that runs
+  // out near its limit could end differently on different lanes
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(done, 0, a.g.err));
   tc_fence_after();
   float* psum = reinterpret_cast<float*>(ring);
   {
