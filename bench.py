@@ -502,7 +502,8 @@ def verify_workload(w, K, W, R, world):
            "kernels": {k: {"avg_us": v[0] / max(v[1], 1) * 1e3, "launches": v[1],
                            "timing": "events around each host-launched kernel (no overlap)"}
                        for k, v in kt.items()},
-           "clocks": clocks, "launches": (5 + (2 if S else 0)) * K, "peak": peak,
+           "clocks": clocks, "launches": (5 + (1 if w.post_norm else 0) + (2 if S else 0)) * K,
+           "peak": peak,
            "peak_source": src, "context_rows": S}
     for Lr in layers:
         Lr.hfa_destroy()
