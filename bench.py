@@ -49,6 +49,7 @@ import torch  # noqa: E402
 
 METRIC = "decode steps/sec per layer at 1 GB300; achieved HBM GB/s as % of peak"
 UNIT = "steps/s"
+VERIFY_METRIC = "verify blocks/sec per layer (L tokens, bf16 weights)"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0
 EXTRA = ("tiny_sliding", "sliding_b16_ring1024", "full_b4_128k_softcap", "verify_l16_8k",
@@ -258,27 +259,45 @@ def run_reference(args, rank, world):
     w = wl.BY_NAME[args.workload]
     weights = wl.make_weights(w)
     x = wl.make_x(w)
-    pos = wl.make_positions(w)
     kv = wl.make_kv_cache(w)
+    if w.verify_len:  # the same operation as our arm: a verify block (after its context rows)
+        S = wl.DRAFTER_CTX_ROWS if w.block_bidir else 0
+        x_ctx = wl.bf16_normal((S, w.hidden), torch.Generator().manual_seed(w.seed + 5)) if S else None
+
+        def step():
+            kc, vc = kv["k_cache"], kv["v_cache"]
+            if S:
+                r = oracle.ctx_append(w, weights, x_ctx, w.base_pos - S, kc, vc)
+                kc = torch.from_numpy(r["k_cache"].view(np.int16)).view(torch.bfloat16)
+                vc = torch.from_numpy(r["v_cache"].view(np.int16)).view(torch.bfloat16)
+            oracle.verify_block(w, weights, x, w.base_pos, kc, vc)
+        metric, unit, what = VERIFY_METRIC, "blocks/s", "verify blocks"
+        config = {"workload": w.name, "tokens": w.verify_len, "prior": w.base_pos}
+    else:
+        pos = wl.make_positions(w)
+
+        def step():
+            oracle.decode_step(w, weights, x, pos, kv["k_cache"], kv["v_cache"])
+        metric, unit, what = METRIC, UNIT, "decode steps"
+        config = {"workload": w.name, "batch": w.batch, "hidden": w.hidden,
+                  "heads": f"{w.num_heads}/{w.num_kv_heads}", "head_dim": w.head_dim,
+                  "context": int(pos.max()) + 1, "weights": "q8_0"}
     for _ in range(args.warmup):
-        oracle.decode_step(w, weights, x, pos, kv["k_cache"], kv["v_cache"])
+        step()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.decode_step(w, weights, x, pos, kv["k_cache"], kv["v_cache"])
+        step()
     dt = time.perf_counter() - t0
     value = args.steps / dt
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+    line = {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic",
-            "config": {"workload": w.name, "batch": w.batch, "hidden": w.hidden,
-                       "heads": f"{w.num_heads}/{w.num_kv_heads}", "head_dim": w.head_dim,
-                       "context": int(pos.max()) + 1, "weights": "q8_0"},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+            "data": "synthetic", "config": config,
+            "cpu_baseline": {"value": value, "unit": unit, "cores": oracle.num_threads(),
                              "kind": "oracle",
-                             "sample": f"{args.steps} full oracle decode steps of {w.name}",
+                             "sample": f"{args.steps} full oracle {what} of {w.name}",
                              **cpu_info()},
-            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
@@ -645,7 +664,7 @@ def run_ours(args, rank, world, local):
     K, W = args.steps, max(3, args.warmup)
     if w.verify_len:
         r = verify_workload(w, K, W, max(1, args.replicas), world)
-        line = {"metric": "verify blocks/sec per layer (L tokens, bf16 weights)", "value": r["blocks_per_s"],
+        line = {"metric": VERIFY_METRIC, "value": r["blocks_per_s"],
                 "unit": "blocks/s", "n_gpus": world, "steps": K, "warmup": W,
                 "ms_per_step": r["ms_per_step"], "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f32", "data": "synthetic",
