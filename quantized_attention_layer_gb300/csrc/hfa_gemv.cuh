@@ -16,19 +16,9 @@ __device__ __forceinline__ void red_release_add_u64(unsigned long long* p, unsig
   asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 // L2 loads the compiler keeps in place: never issued ahead of the branch that guards them
-__device__ __forceinline__ float ldcg_pinned(const float* p) {
-  float v;
-  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
-  return v;
-}
 __device__ __forceinline__ unsigned long long ldcg_pinned64(const unsigned long long* p) {
   unsigned long long v;
   asm volatile("ld.global.cg.u64 %0, [%1];" : "=l"(v) : "l"(p));
-  return v;
-}
-__device__ __forceinline__ float2 ldcg_pinned2(const float* p) {
-  float2 v;
-  asm volatile("ld.global.cg.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
   return v;
 }
 // Tagged partial sums: 8 bytes (f32 bits | step tag << 32) stored and loaded as one
