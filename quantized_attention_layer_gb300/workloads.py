@@ -237,11 +237,6 @@ def make_kv_cache(w: Workload) -> Dict[str, torch.Tensor]:
             "v_cache": bf16_normal(shape, _gen(w.seed, 51))}
 
 
-def shrink(w: Workload, **kw) -> Workload:
-    """A smaller copy of a workload for fast tests (same structure, new sizes)."""
-    return w.replace(**kw)
-
-
 def make_tq_signs(head_dim: int, seed: int) -> np.ndarray:
     """The +-1 sign pre-multiply of a quantised-KV format (int8 [head_dim]), seeded."""
     g = _gen(seed, 60)
